@@ -1,0 +1,157 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests, the bench and the oracle's tests.
+
+This module holds none of the method's arithmetic: it only draws random numbers and names the
+workloads.  Every tensor is drawn on the CPU from ``torch.Generator().manual_seed(seed)`` in
+fp32 and rounded once, round-to-nearest-even, to bf16; the same bf16 tensor is given to both
+the GPU library and the fp64 oracle.  Q, then K, then V are drawn from one generator.
+
+Workloads (shapes are [B, H, N, d], row-major, d innermost):
+
+====================  ==========================================================================
+name                  recipe
+====================  ==========================================================================
+small_b1h1n256d64     B1 H1 N256 d64, Q/K/V iid N(0,1), non-causal
+mha_b4h16n2048d64     B4 H16 N2048 d64, Q/K/V iid N(0,1), non-causal
+causal_b2h32n8192     B2 H32 N8192 d128, Q/K/V iid N(0,1), causal
+causal_b1h8n32768     B1 H8 N32768 d128, Q/K/V iid N(0,1), causal (checked on sampled rows)
+ragged_b1h16n4000     B1 H16 N4000 d128, Q,K iid N(0, sd 3) (logit sd 9), V iid U(-1,1)
+dense_b2h32n8192      B2 H32 N8192 d128, Q/K/V iid N(0,1), non-causal (the d=128 long-N case)
+softmax_65536x4000    fp32 rows [65536, 4000], x = 9*N(0,1) and per row one entry +100 and one
+                      entry -100 at seeded positions
+====================  ==========================================================================
+
+Seeds: 1000 + the workload's index in the table above (1001 ... 1005 for the five attention
+workloads in the order listed, 1006 for the non-causal d=128 case, 1005 again for the softmax
+rows, which belong to the ragged/overflow stress workload).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    qk_std: float = 1.0
+    v_dist: str = "normal"  # "normal" N(0,1) or "uniform" U(-1,1)
+    sample_rows_per_head: int = 0  # >0: parity on this many seeded rows per head
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOP: 4*B*H*N^2*d (two N x N x d contractions), halved when causal."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2.0 if self.causal else f
+
+    @property
+    def hbm_bytes(self) -> int:
+        """Compulsory HBM traffic: read Q, K, V (bf16), write O (bf16) and LSE (fp32)."""
+        n = self.B * self.H * self.N
+        return 4 * n * self.d * 2 + n * 4
+
+
+@dataclass(frozen=True)
+class SoftmaxWorkload:
+    name: str
+    rows: int
+    cols: int
+    seed: int
+    std: float = 9.0
+    spike: float = 100.0
+
+    @property
+    def hbm_bytes(self) -> int:
+        """Compulsory HBM traffic: read x once, write y once (fp32), write lse (fp32)."""
+        return self.rows * self.cols * 8 + self.rows * 4
+
+
+ATTN_WORKLOADS = {
+    w.name: w
+    for w in [
+        AttnWorkload("small_b1h1n256d64", 1, 1, 256, 64, False, 1001),
+        AttnWorkload("mha_b4h16n2048d64", 4, 16, 2048, 64, False, 1002),
+        AttnWorkload("causal_b2h32n8192", 2, 32, 8192, 128, True, 1003),
+        AttnWorkload("causal_b1h8n32768", 1, 8, 32768, 128, True, 1004, sample_rows_per_head=512),
+        AttnWorkload("ragged_b1h16n4000", 1, 16, 4000, 128, False, 1005, qk_std=3.0,
+                     v_dist="uniform"),
+        AttnWorkload("dense_b2h32n8192", 2, 32, 8192, 128, False, 1006),
+    ]
+}
+
+SOFTMAX_WORKLOADS = {
+    w.name: w for w in [SoftmaxWorkload("softmax_65536x4000", 65536, 4000, 1005)]
+}
+
+
+def attn_inputs(B, H, N, d, seed, qk_std=1.0, v_dist="normal"):
+    """Q, K, V as CPU bf16 tensors [B, H, N, d] drawn from one seeded generator."""
+    g = torch.Generator().manual_seed(int(seed))
+    shape = (B, H, N, d)
+    q = (torch.randn(shape, generator=g, dtype=torch.float32) * qk_std).to(torch.bfloat16)
+    k = (torch.randn(shape, generator=g, dtype=torch.float32) * qk_std).to(torch.bfloat16)
+    if v_dist == "normal":
+        v = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    elif v_dist == "uniform":
+        v = (torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0).to(torch.bfloat16)
+    else:
+        raise ValueError(v_dist)
+    return q, k, v
+
+
+def workload_inputs(w: AttnWorkload):
+    return attn_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_dist)
+
+
+def sample_rows(w: AttnWorkload, per_head: int, seed_offset: int = 0):
+    """Seeded flat row indices (b*H + h)*N + i, `per_head` distinct rows in every head.
+
+    Row 0 and row N-1 of every head are always included (the causal first row and the ragged
+    last row are the rows most likely to go wrong).
+    """
+    g = torch.Generator().manual_seed(int(w.seed) * 7919 + 17 + seed_offset)
+    out = []
+    k = min(per_head, w.N)
+    for bh in range(w.B * w.H):
+        idx = torch.randperm(w.N, generator=g)[:k]
+        idx[0] = 0
+        if k > 1:
+            idx[1] = w.N - 1
+        idx = torch.unique(idx)
+        out.append(idx.to(torch.int64) + bh * w.N)
+    return torch.cat(out).numpy()
+
+
+def softmax_inputs(rows, cols, seed, std=9.0, spike=100.0):
+    """fp32 [rows, cols]: std * N(0,1), and per row one +spike and one -spike entry."""
+    g = torch.Generator().manual_seed(int(seed))
+    x = torch.randn((rows, cols), generator=g, dtype=torch.float32) * std
+    if cols >= 2 and spike:
+        pos = torch.randint(0, cols, (rows, 2), generator=g)
+        pos[:, 1] = (pos[:, 0] + 1 + torch.randint(0, cols - 1, (rows,), generator=g)) % cols
+        r = torch.arange(rows)
+        x[r, pos[:, 0]] = spike
+        x[r, pos[:, 1]] = -spike
+    return x
+
+
+def softmax_workload_inputs(w: SoftmaxWorkload):
+    return softmax_inputs(w.rows, w.cols, w.seed, w.std, w.spike)
+
+
+def bf16_bits(t: torch.Tensor):
+    """uint16 numpy view of a CPU bf16 tensor (what the oracle reads)."""
+    import numpy as np
+
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)

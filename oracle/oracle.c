@@ -1,0 +1,381 @@
+/*
+ * oracle.c -- slow, plain fp64 CPU oracle for exact softmax attention and row softmax.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call this file:
+ * only the tests, the smoke check and the bench's CPU-baseline leg use it.  It shares no code,
+ * header, table or constant with the CUDA library.
+ *
+ * What it computes (the plain definitions, written out without blocking or fusion):
+ *
+ *   softmax of a row x:  m = max_j x_j,  l = sum_j exp(x_j - m),  y_j = exp(x_j - m) / l,
+ *                        lse = m + ln l.
+ *     "How FlashAttention avoids storing the giant score table" (spicyshark.co, Online softmax
+ *     lesson), sections "The fix: subtract the maximum" and "The cost: three passes": the safe
+ *     softmax needs one pass for the max, one for the sum and one to write the shares.
+ *
+ *   attention of query row i of head (b,h):
+ *        s_j  = scale * sum_k Q[b,h,i,k] * K[b,h,j,k]      for every allowed key j
+ *        m    = max_j s_j
+ *        l    = sum_j exp(s_j - m)
+ *        O_i  = sum_j exp(s_j - m) * V[b,h,j,:] / l
+ *        LSE_i = m + ln l
+ *     Allowed keys: all j < N, or j <= i when causal.  Same lesson, section "From softmax to
+ *     attention" (score = q.k scaled, output = softmax-weighted sum of the values, written in the
+ *     max-subtracted form); the masked keys carry score -inf ("The implementation": masked
+ *     positions such as the tokens after a token get score -inf).  FlashAttention computes this
+ *     exact quantity, only in another order ("kbwen.com FlashAttention" page, section "More than
+ *     two blocks": it is the same attention, not an approximation).
+ *
+ *   the streaming state (m, l, acc) of one score row read in blocks, and the merge of two such
+ *   states: same lesson, sections "The idea", "From softmax to attention" (the block recipe)
+ *   and the two-worker merge at the end of "From softmax to attention"; "kbwen.com
+ *   FlashAttention" page, sections "Two blocks" and "More than two blocks".  These are the
+ *   pages' algorithm restated step by step in the pages' order and notation; the oracle uses
+ *   them only to reproduce the pages' worked tables and laws, never to produce the reference
+ *   outputs of the attention or softmax (those come from the three-pass definitions above).
+ *
+ * Readings where the pages are silent (each listed in the design notes of the repository):
+ *   - LSE is the natural-log log-sum-exp of the SCALED scores, m + ln l.
+ *   - a row with no allowed key (all -inf) has y = 0 / O = 0 and lse = -inf: the -inf guard of
+ *     the lesson's "The implementation" section says such a block "adds nothing", and the merge
+ *     of an empty state keeps the other state.
+ *   - bf16 inputs are widened exactly (bits << 16) to fp32, then to fp64.
+ *
+ * Mutants: building with -DORACLE_MUTANT=k plants one deliberate mistake (k = 1..11) so the
+ * tests can show that the pins catch it.  The default build (no define) has none.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+#define ORACLE_ABI_VERSION 1
+
+int oracle_abi_version(void) { return ORACLE_ABI_VERSION; }
+int oracle_mutant(void) { return ORACLE_MUTANT; }
+
+/* bf16 bit pattern -> exact double. */
+static double bf16_to_double(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static int resolve_threads(int nthreads) {
+    if (nthreads > 0) return nthreads;
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    if (n < 1) n = 1;
+    if (n > 256) n = 256;
+    return (int)n;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Row softmax, three passes per row.                                                          */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    const float* x;
+    double* y;
+    double* lse;
+    int64_t cols;
+    int64_t r0, r1;
+} softmax_job;
+
+static void softmax_one_row(const float* x, double* y, double* lse, int64_t cols) {
+    /* pass 1: the maximum */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < cols; ++j) {
+        double v = (double)x[j];
+        if (v > m || isnan(v)) m = v;
+    }
+    if (cols == 0 || m == -INFINITY) {
+        /* no finite entry: nothing is allowed, every share is 0 and the log-sum-exp is -inf */
+        for (int64_t j = 0; j < cols; ++j) y[j] = 0.0;
+        if (lse) *lse = -INFINITY;
+        return;
+    }
+    /* pass 2: the sum of exp(x - m) */
+    double l = 0.0;
+    for (int64_t j = 0; j < cols; ++j) {
+#if ORACLE_MUTANT == 1
+        l += exp((double)x[j]); /* mutant: forgets the max in the sum */
+#else
+        l += exp((double)x[j] - m);
+#endif
+    }
+    /* pass 3: the shares */
+    for (int64_t j = 0; j < cols; ++j) y[j] = exp((double)x[j] - m) / l;
+    if (lse) *lse = m + log(l);
+}
+
+static void* softmax_worker(void* arg) {
+    softmax_job* jb = (softmax_job*)arg;
+    for (int64_t r = jb->r0; r < jb->r1; ++r)
+        softmax_one_row(jb->x + r * jb->cols, jb->y + r * jb->cols, jb->lse ? jb->lse + r : NULL,
+                        jb->cols);
+    return NULL;
+}
+
+/* y[rows*cols], lse[rows] (lse may be NULL). Returns 0, or -1 on bad arguments. */
+int oracle_softmax_rows(const float* x, int64_t rows, int64_t cols, double* y, double* lse,
+                        int nthreads) {
+    if (rows < 0 || cols < 0) return -1;
+    if (rows == 0) return 0;
+    if (!x || !y) return -1;
+    int nt = resolve_threads(nthreads);
+    if (nt > rows) nt = (int)rows;
+    pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+    softmax_job* jobs = (softmax_job*)calloc((size_t)nt, sizeof(softmax_job));
+    if (!th || !jobs) { free(th); free(jobs); return -1; }
+    for (int t = 0; t < nt; ++t) {
+        jobs[t].x = x; jobs[t].y = y; jobs[t].lse = lse; jobs[t].cols = cols;
+        jobs[t].r0 = rows * t / nt;
+        jobs[t].r1 = rows * (t + 1) / nt;
+    }
+    for (int t = 1; t < nt; ++t) pthread_create(&th[t], NULL, softmax_worker, &jobs[t]);
+    softmax_worker(&jobs[0]);
+    for (int t = 1; t < nt; ++t) pthread_join(th[t], NULL);
+    free(th); free(jobs);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Attention, three passes per query row.                                                      */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *Q, *K, *V;
+    int64_t H, N, d;
+    double scale;
+    int causal;
+    const int64_t* rows; /* NULL: rows [r0, r1) of the flat (b*H+h)*N+i index */
+    double *O, *LSE;
+    int64_t r0, r1;
+    int err;
+} attn_job;
+
+/* One query row.  `flat` = (b*H + h)*N + i.  s and q are scratch of N and d doubles. */
+static void attn_one_row(const attn_job* jb, int64_t flat, double* o, double* lse_out,
+                         double* s, double* q) {
+    const int64_t N = jb->N, d = jb->d;
+    const int64_t bh = flat / N;
+    const int64_t i = flat % N;
+    const uint16_t* Qh = jb->Q + bh * N * d;
+    const uint16_t* Kh = jb->K + bh * N * d;
+    const uint16_t* Vh = jb->V + bh * N * d;
+
+    for (int64_t k = 0; k < d; ++k) q[k] = bf16_to_double(Qh[i * d + k]);
+
+    /* number of allowed keys */
+    int64_t nk = N;
+    if (jb->causal) {
+#if ORACLE_MUTANT == 2
+        nk = i;     /* mutant: strict causal mask (j < i) */
+#else
+        nk = i + 1; /* key j <= query i */
+#endif
+    }
+#if ORACLE_MUTANT == 3
+    if (nk > 1) nk -= 1; /* mutant: drops the last allowed key */
+#endif
+
+    /* pass 1: scores and their maximum */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nk; ++j) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < d; ++k) {
+#if ORACLE_MUTANT == 4
+            /* mutant: reads K transposed (column j of a d x N view) */
+            double kv = bf16_to_double(Kh[(k * N + j) % (N * d)]);
+#else
+            double kv = bf16_to_double(Kh[j * d + k]);
+#endif
+            acc += q[k] * kv;
+        }
+#if ORACLE_MUTANT == 5
+        s[j] = acc; /* mutant: forgets the scale */
+#else
+        s[j] = jb->scale * acc;
+#endif
+        if (s[j] > m || isnan(s[j])) m = s[j];
+    }
+    if (nk == 0 || m == -INFINITY) {
+        for (int64_t k = 0; k < d; ++k) o[k] = 0.0;
+        *lse_out = -INFINITY;
+        return;
+    }
+    /* pass 2: the normaliser l = sum_j exp(s_j - m) */
+    double l = 0.0;
+    for (int64_t j = 0; j < nk; ++j) l += exp(s[j] - m);
+    /* pass 3: the weighted sum of the values, divided by l */
+    for (int64_t k = 0; k < d; ++k) o[k] = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+#if ORACLE_MUTANT == 6
+        double p = exp(m - s[j]); /* mutant: sign error in the exponent */
+#else
+        double p = exp(s[j] - m);
+#endif
+        const uint16_t* vj = Vh + j * d;
+        for (int64_t k = 0; k < d; ++k) o[k] += p * bf16_to_double(vj[k]);
+    }
+    for (int64_t k = 0; k < d; ++k) o[k] /= l;
+#if ORACLE_MUTANT == 7
+    *lse_out = m + log2(l); /* mutant: log base 2 in the log-sum-exp */
+#else
+    *lse_out = m + log(l);
+#endif
+}
+
+static void* attn_worker(void* arg) {
+    attn_job* jb = (attn_job*)arg;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(jb->N > 0 ? jb->N : 1));
+    double* q = (double*)malloc(sizeof(double) * (size_t)(jb->d > 0 ? jb->d : 1));
+    if (!s || !q) { jb->err = 1; free(s); free(q); return NULL; }
+    for (int64_t r = jb->r0; r < jb->r1; ++r) {
+        int64_t flat = jb->rows ? jb->rows[r] : r;
+        attn_one_row(jb, flat, jb->O + r * jb->d, jb->LSE + r, s, q);
+    }
+    free(s); free(q);
+    return NULL;
+}
+
+/*
+ * Q, K, V: bf16 bit patterns, [B, H, N, d] contiguous.
+ * rows == NULL: compute all B*H*N rows; O is [B*H*N, d] and LSE [B*H*N].
+ * rows != NULL: compute the nrows listed flat row indices (b*H + h)*N + i; O is [nrows, d].
+ * Returns 0, or -1 on bad arguments (including a listed row out of range).
+ */
+int oracle_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
+                int64_t N, int64_t d, double scale, int causal, const int64_t* rows,
+                int64_t nrows, double* O, double* LSE, int nthreads) {
+    if (B < 0 || H < 0 || N < 0 || d < 1) return -1;
+    const int64_t total = B * H * N;
+    const int64_t n = rows ? nrows : total;
+    if (n < 0) return -1;
+    if (n == 0) return 0;
+    if (!Q || !K || !V || !O || !LSE) return -1;
+    if (rows)
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= total) return -1;
+    int nt = resolve_threads(nthreads);
+    if (nt > n) nt = (int)n;
+    pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+    attn_job* jobs = (attn_job*)calloc((size_t)nt, sizeof(attn_job));
+    if (!th || !jobs) { free(th); free(jobs); return -1; }
+    for (int t = 0; t < nt; ++t) {
+        attn_job* jb = &jobs[t];
+        jb->Q = Q; jb->K = K; jb->V = V; jb->H = H; jb->N = N; jb->d = d;
+        jb->scale = scale; jb->causal = causal; jb->rows = rows; jb->O = O; jb->LSE = LSE;
+        jb->r0 = n * t / nt;
+        jb->r1 = n * (t + 1) / nt;
+    }
+    for (int t = 1; t < nt; ++t) pthread_create(&th[t], NULL, attn_worker, &jobs[t]);
+    attn_worker(&jobs[0]);
+    int err = 0;
+    for (int t = 1; t < nt; ++t) pthread_join(th[t], NULL);
+    for (int t = 0; t < nt; ++t) err |= jobs[t].err;
+    free(th); free(jobs);
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* The streaming state of one score row, block by block, and the merge of two states.          */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * Reads the n scores s[] with their value rows v[n*dv] in blocks of `block` and keeps the
+ * state (m, l, acc): m the largest score so far, l = sum exp(s_j - m), acc = sum exp(s_j - m)
+ * v_j over the scores read so far.  Per block: m_new = max(m, max of the block); a block that
+ * leaves m_new = -inf adds nothing; alpha = exp(m - m_new) rescales l and acc alike; the block's
+ * own terms p = exp(s - m_new) are added.
+ *
+ * If trace arrays are given they receive the state after every block (ceil(n/block) entries;
+ * trace_acc has dv per entry): m, alpha used, the block's own sum of p, l, acc.  A block that
+ * was skipped by the -inf guard records alpha = NAN (no rescale happened) and psum = 0.
+ * Returns the number of blocks, or -1 on bad arguments.
+ */
+int64_t oracle_online_state(const double* s, const double* v, int64_t n, int64_t dv,
+                            int64_t block, double* m_out, double* l_out, double* acc_out,
+                            double* trace_m, double* trace_alpha, double* trace_psum,
+                            double* trace_l, double* trace_acc) {
+    if (n < 0 || dv < 0 || block < 1 || !m_out || !l_out) return -1;
+    if (dv > 0 && (!acc_out || (n > 0 && !v))) return -1;
+    double m = -INFINITY, l = 0.0;
+    for (int64_t k = 0; k < dv; ++k) acc_out[k] = 0.0;
+    int64_t nb = 0;
+    for (int64_t i0 = 0; i0 < n; i0 += block, ++nb) {
+        int64_t i1 = i0 + block < n ? i0 + block : n;
+        double bmax = -INFINITY;
+        for (int64_t j = i0; j < i1; ++j)
+            if (s[j] > bmax) bmax = s[j];
+        double m_new = m > bmax ? m : bmax;
+        double alpha = NAN, psum = 0.0;
+#if ORACLE_MUTANT == 10
+        int skip = 0; /* mutant: no -inf guard */
+#else
+        int skip = (m_new == -INFINITY); /* nothing finite yet: the block adds nothing */
+#endif
+        if (!skip) {
+#if ORACLE_MUTANT == 9
+            double m_p = (m == -INFINITY) ? m_new : m; /* mutant: p against the old max */
+#else
+            double m_p = m_new;
+#endif
+            alpha = exp(m - m_new);
+            for (int64_t j = i0; j < i1; ++j) psum += exp(s[j] - m_p);
+#if ORACLE_MUTANT == 8
+            l = l + psum; /* mutant: drops the rescale of l */
+#else
+            l = l * alpha + psum;
+#endif
+            for (int64_t k = 0; k < dv; ++k) {
+                double add = 0.0;
+                for (int64_t j = i0; j < i1; ++j) add += exp(s[j] - m_p) * v[j * dv + k];
+                acc_out[k] = acc_out[k] * alpha + add;
+            }
+            m = m_new;
+        }
+        if (trace_m) trace_m[nb] = m;
+        if (trace_alpha) trace_alpha[nb] = alpha;
+        if (trace_psum) trace_psum[nb] = psum;
+        if (trace_l) trace_l[nb] = l;
+        if (trace_acc)
+            for (int64_t k = 0; k < dv; ++k) trace_acc[nb * dv + k] = acc_out[k];
+    }
+    *m_out = m;
+    *l_out = l;
+    return nb;
+}
+
+/*
+ * Merge of two states built from disjoint parts of one row: m = max(m_a, m_b); each side's l
+ * and acc are rescaled by exp(its m - m) and added.  If both are empty (m = -inf) the result is
+ * state a.  Output may alias either input.
+ */
+int oracle_merge(double m_a, double l_a, const double* acc_a, double m_b, double l_b,
+                 const double* acc_b, int64_t dv, double* m_out, double* l_out,
+                 double* acc_out) {
+    if (dv < 0 || !m_out || !l_out || (dv > 0 && (!acc_a || !acc_b || !acc_out))) return -1;
+    double m = m_a > m_b ? m_a : m_b;
+    if (m == -INFINITY) {
+        *m_out = m_a;
+        *l_out = l_a;
+        for (int64_t k = 0; k < dv; ++k) acc_out[k] = acc_a[k];
+        return 0;
+    }
+    double wa = exp(m_a - m), wb = exp(m_b - m);
+    *m_out = m;
+#if ORACLE_MUTANT == 11
+    wb = wa; /* mutant: weighs both sides by the first side's factor */
+#endif
+    *l_out = l_a * wa + l_b * wb;
+    for (int64_t k = 0; k < dv; ++k) acc_out[k] = acc_a[k] * wa + acc_b[k] * wb;
+    return 0;
+}

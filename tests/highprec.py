@@ -1,0 +1,45 @@
+"""Attention in 40-digit decimal arithmetic, by the textbook definition, for tiny inputs.
+
+Pins the fp64 oracle to something other than itself: no max subtraction, no fp64 rounding,
+softmax written as exp(s_j) / sum_k exp(s_k) exactly as the textbook formula of the
+"FlashAttention Algorithm > Online Softmax Computation" page (mbrenndoerfer.com, the softmax
+formula at the top) states it.  In decimal arithmetic the naive formula cannot overflow, so it
+is exact to ~40 digits.  Pure-Python loops: keep the inputs tiny.
+"""
+from decimal import Decimal, getcontext
+
+getcontext().prec = 40
+
+
+def attention_decimal(q, K, V, scale, causal):
+    """q, K, V: nested lists of Python floats (exact bf16 values), [B][H][N][d].
+
+    Returns (O, LSE) as nested lists of floats.
+    """
+    sc = Decimal(scale)
+    O, L = [], []
+    for b in range(len(q)):
+        Ob, Lb = [], []
+        for h in range(len(q[b])):
+            Qh, Kh, Vh = q[b][h], K[b][h], V[b][h]
+            N = len(Qh)
+            d = len(Qh[0])
+            Oh, Lh = [], []
+            for i in range(N):
+                keys = range(i + 1) if causal else range(N)
+                e = []
+                for j in keys:
+                    s = sum(Decimal(Qh[i][k]) * Decimal(Kh[j][k]) for k in range(d)) * sc
+                    e.append(s.exp())
+                tot = sum(e)
+                row = []
+                for k in range(d):
+                    num = sum(e[t] * Decimal(Vh[j][k]) for t, j in enumerate(keys))
+                    row.append(float(num / tot))
+                Oh.append(row)
+                Lh.append(float(tot.ln()))
+            Ob.append(Oh)
+            Lb.append(Lh)
+        O.append(Ob)
+        L.append(Lb)
+    return O, L

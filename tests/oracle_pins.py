@@ -1,0 +1,345 @@
+"""Pins of the fp64 oracle to things other than itself.
+
+Each ``pin_*`` function takes a loaded oracle handle and raises AssertionError when the oracle
+disagrees with what the pages or the mathematics fix.  ``test_oracle_pins.py`` runs them on the
+real oracle; ``test_oracle_mutants.py`` runs them on builds with one planted mistake each and
+requires that every planted mistake fails at least one pin.
+
+What pins what:
+  printed worked examples  -> the pages' tables and figures (tests/golden/*.txt, cited there)
+  closed forms             -> uniform scores, the causal first row, two keys (logistic form),
+                              constant values, scale 0
+  library special case     -> scipy.special.softmax / logsumexp for the row softmax
+  exact brute force        -> 40-digit decimal arithmetic by the textbook formula (highprec.py)
+  invariants               -> rows sum to 1, shift invariance, key permutation invariance,
+                              block-size independence, the two-worker merge law
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import golden_io
+import highprec
+from online_softmax_tiled_attn_gb300 import inputs
+
+
+def _bits(values, shape):
+    t = torch.tensor(values, dtype=torch.float32).reshape(shape).to(torch.bfloat16)
+    return inputs.bf16_bits(t)
+
+
+def _bf16_float(t):
+    return t.to(torch.float32).numpy().astype(np.float64)
+
+
+def _row_attention(orc, s, v):
+    """Attention of one query whose scores are s (given exactly) with values v, via the
+    three-pass oracle: d=1 keys k_j = s_j, q = 1, scale = 1 needs bf16-exact scores, so use
+    the softmax oracle for the weights instead when s is arbitrary."""
+    y, lse = orc.softmax_rows(np.asarray(s, dtype=np.float32)[None, :])
+    return y[0] @ np.asarray(v, dtype=np.float64), y[0], lse[0]
+
+
+# ----------------------------------------------------------------------------------------------
+# printed worked examples
+# ----------------------------------------------------------------------------------------------
+
+def pin_four_scores_all_at_once(orc):
+    g = golden_io.load("four_scores_kbwen.txt")
+    s, v = g["scores"], g["values"]
+    Q = _bits([1.0], (1, 1, 1, 1))
+    K = _bits(s, (1, 1, 4, 1))
+    V = _bits(v, (1, 1, 4, 1))
+    # the query is repeated as 4 rows so every row sees all four keys (non-causal)
+    Q4 = np.repeat(Q, 4, axis=2)
+    O, L = orc.attention(Q4, K, V, 1.0, False)
+    for i in range(4):
+        assert abs(O[0, 0, i, 0] - g["output_8dp"][0]) < 5e-9, O[0, 0, i, 0]
+    assert round(O[0, 0, 0, 0], 4) == g["output_4dp"][0]
+    m = max(s)
+    lsum = math.exp(L[0, 0, 0] - m)
+    assert round(lsum, 4) == g["sum_4dp"][0], lsum
+    assert round(O[0, 0, 0, 0] * lsum, 4) == g["weighted_sum_4dp"][0]
+    y, _ = orc.softmax_rows(np.array([s], dtype=np.float32))
+    assert [round(w, 4) for w in (y[0] * lsum)] == g["weights_4dp"]
+
+
+def pin_four_scores_two_blocks(orc):
+    g = golden_io.load("four_scores_kbwen.txt")
+    st = orc.online_state(g["scores"], g["values"], block=2, trace=True)
+    assert list(st["trace_m"]) == [g["block1_max"][0], max(g["scores"])]
+    l1, a1 = st["trace_l"][0], st["trace_acc"][0, 0]
+    assert round(l1, 4) == g["block1_sum_4dp"][0]
+    assert round(a1, 4) == g["block1_weighted_sum_4dp"][0]
+    assert round(a1 / l1, 2) == g["block1_output_2dp"][0]
+    alpha = st["trace_alpha"][1]
+    assert round(alpha, 4) == g["rescale_factor_4dp"][0]
+    assert round(l1 * alpha, 4) == g["carried_sum_after_rescale_4dp"][0]
+    assert round(a1 * alpha, 4) == g["carried_weighted_sum_after_rescale_4dp"][0]
+    assert round(st["trace_psum"][1], 4) == g["block2_sum_4dp"][0]
+    assert round(st["trace_acc"][1, 0] - a1 * alpha, 4) == g["block2_weighted_sum_4dp"][0]
+    assert round(st["l"], 4) == g["sum_4dp"][0]
+    assert round(st["acc"][0], 4) == g["weighted_sum_4dp"][0]
+    assert abs(st["acc"][0] / st["l"] - g["output_8dp"][0]) < 5e-9
+
+
+def pin_four_scores_random_blocks(orc):
+    """The page's random check: 1000 scores N(0, sd 4), 8-wide values, blocks of 64."""
+    g = golden_io.load("four_scores_kbwen.txt")
+    rng = np.random.default_rng(0)
+    s = rng.normal(0, 4, size=1000)
+    v = rng.normal(size=(1000, 8))
+    st = orc.online_state(s, v, block=64)
+    streamed = st["acc"] / st["l"]
+    y, _ = orc.softmax_rows(s.astype(np.float32)[None, :])
+    # compare against the three-pass weights on the same (fp32-rounded) scores
+    st32 = orc.online_state(s.astype(np.float32).astype(np.float64), v, block=64)
+    diff = np.abs(st32["acc"] / st32["l"] - y[0] @ v).max()
+    assert diff < 100 * g["random_max_abs_diff"][0], diff
+    assert np.all(np.isfinite(streamed))
+
+
+def pin_counter_example(orc):
+    g = golden_io.load("counter_example_dubiel.txt")
+    # scores 0, 0, ln3, ln3 enter as keys 0, 0, 1, 1 with q = 1 and scale = ln 3 (fp64)
+    Q = _bits([1.0], (1, 1, 1, 1))
+    K = _bits([0.0, 0.0, 1.0, 1.0], (1, 1, 4, 1))
+    V = _bits(g["values"], (1, 1, 4, 1))
+    O, L = orc.attention(np.repeat(Q, 4, axis=2), K, V, math.log(3.0), False)
+    assert abs(O[0, 0, 0, 0] - g["result"][0]) < 1e-15, O[0, 0, 0, 0]
+    assert abs(L[0, 0, 0] - math.log(8.0)) < 1e-15  # 1 + 1 + 3 + 3 = 8
+    # block results on their own are 0 and 1; their plain mean is the wrong 0.5
+    b1 = orc.online_state(g["scores"][:2], g["values"][:2], block=2)
+    b2 = orc.online_state(g["scores"][2:], g["values"][2:], block=2)
+    assert [b1["acc"][0] / b1["l"], b2["acc"][0] / b2["l"]] == g["block_results"]
+    st = orc.online_state(g["scores"], g["values"], block=2)
+    assert abs(st["acc"][0] / st["l"] - g["result"][0]) < 1e-15
+    assert abs(st["acc"][0] / st["l"] - g["wrong_block_mean"][0]) > 0.2
+    w = np.exp(np.array(g["scores"]) - min(g["scores"]))
+    assert np.allclose(w, g["weight_proportions"], rtol=1e-15)
+
+
+def pin_five_scores_table(orc):
+    g = golden_io.load("five_scores_spicyshark.txt")
+    x, v = g["scores"], g["values"]
+    st = orc.online_state(x, v, block=1, trace=True)
+    assert list(st["trace_m"]) == g["m"]
+    assert [round(a, 5) for a in st["trace_alpha"]] == g["alpha_5dp"]
+    assert [round(p, 5) for p in st["trace_psum"]] == g["new_term_5dp"]
+    assert [round(l, 4) for l in st["trace_l"]] == g["l_4dp"]
+    acc = st["trace_acc"][:, 0]
+    assert [round(a, 4) for a in acc] == g["acc_full_precision_4dp"]
+    assert np.abs(acc - np.array(g["acc_by_hand_4dp"])).max() < g["by_hand_vs_full_max_diff"][0]
+    assert [round(a / l, 2) for a, l in zip(acc, st["trace_l"])] == g["output_2dp"]
+    y, lse = orc.softmax_rows(np.array([x], dtype=np.float32))
+    assert [round(p, 4) for p in y[0]] == g["probabilities_4dp"]
+    l_final = math.exp(lse[0] - 5.0)
+    assert [round(p * l_final, 5) for p in y[0]] == g["exp_x_minus_5_5dp"]
+    hand = np.array(g["probabilities_4dp"]) @ np.array(v)
+    assert round(hand, 3) == g["textbook_weighted_sum_3dp"][0]
+    st2 = orc.online_state(x, v, block=2, trace=True)
+    assert [round(l, 4) for l in st2["trace_l"]] == g["blocks_of_two_l_4dp"]
+    # the three-pass attention of the same query equals the streamed answer
+    Q = _bits([1.0] * 5, (1, 1, 5, 1))
+    O, _ = orc.attention(Q, _bits(x, (1, 1, 5, 1)), _bits(v, (1, 1, 5, 1)), 1.0, False)
+    assert abs(O[0, 0, 4, 0] - st["acc"][0] / st["l"]) < 1e-12
+    assert round(O[0, 0, 4, 0], 2) == g["output_2dp"][-1]
+
+
+def pin_overflow_row(orc):
+    g = golden_io.load("overflow_and_masking_spicyshark.txt")
+    row = np.array([g["fp32_row"]], dtype=np.float32)
+    with np.errstate(over="ignore"):
+        assert np.isfinite(np.exp(np.float32(g["fp32_exp_finite_at"][0])))
+        assert np.isinf(np.exp(np.float32(g["fp32_exp_overflows_at"][0])))
+    y, lse = orc.softmax_rows(row)
+    t = np.exp(np.array(g["fp32_row_softmax_equals_softmax_of"]))
+    want = t / t.sum()
+    assert np.abs(y[0] - want).max() < g["fp32_row_atol"][0]
+    assert np.abs(y[0] - want).max() < 1e-15
+    assert abs(lse[0] - (1002.0 + math.log(t.sum()))) < 1e-12
+
+
+def pin_masked_prefix(orc):
+    g = golden_io.load("overflow_and_masking_spicyshark.txt")
+    blocks = g["masked_stats_blocks"]
+    s = blocks[0] + blocks[1]
+    st = orc.online_state(s, np.zeros(len(s)), block=len(blocks[0]))
+    assert st["m"] == g["masked_stats_m"][0]
+    assert abs(st["l"] - (math.exp(-1.0) + 1.0)) < 1e-15
+    # both sides get the same fp32-exact scores (the softmax oracle reads fp32 rows)
+    sc = np.array(g["masked_attention_scores"], dtype=np.float32).astype(np.float64)
+    V = np.random.default_rng(5).standard_normal((len(sc), 3))
+    st = orc.online_state(sc, V, block=int(g["masked_attention_block"][0]))
+    assert st["m"] == 2.0 and math.isfinite(st["l"]) and np.all(np.isfinite(st["acc"]))
+    out, y, _ = _row_attention(orc, sc, V)
+    assert y[0] == 0.0 and y[1] == 0.0
+    assert np.abs(st["acc"] / st["l"] - out).max() < 1e-14
+    # a row with no finite score: the softmax is all zeros and the log-sum-exp is -inf
+    yz, lz = orc.softmax_rows(np.full((1, 4), -np.inf, dtype=np.float32))
+    assert np.all(yz == 0.0) and lz[0] == -np.inf
+
+
+# ----------------------------------------------------------------------------------------------
+# library special case and exact brute force
+# ----------------------------------------------------------------------------------------------
+
+def pin_softmax_matches_scipy(orc):
+    from scipy.special import logsumexp, softmax
+
+    x = inputs.softmax_inputs(7, 53, seed=11, std=9.0, spike=100.0).numpy()
+    y, lse = orc.softmax_rows(x)
+    xd = x.astype(np.float64)
+    assert np.abs(y - softmax(xd, axis=1)).max() < 1e-15
+    assert np.abs(lse - logsumexp(xd, axis=1)).max() < 1e-12
+    assert np.abs(y.sum(axis=1) - 1.0).max() < 1e-14
+
+
+def pin_attention_decimal_bruteforce(orc):
+    cases = [
+        (1, 1, 5, 3, 0.37, False),
+        (1, 2, 7, 4, 0.61, True),
+        (2, 1, 9, 2, 1.3, False),
+        (1, 1, 6, 5, 0.5, True),
+    ]
+    for seed, (B, H, N, d, scale, causal) in enumerate(cases):
+        q, k, v = inputs.attn_inputs(B, H, N, d, seed=77 + seed, qk_std=1.5)
+        O, L = orc.attention(q, k, v, scale, causal)
+        Od, Ld = highprec.attention_decimal(_bf16_float(q).tolist(), _bf16_float(k).tolist(),
+                                            _bf16_float(v).tolist(), scale, causal)
+        assert np.abs(O - np.array(Od)).max() < 1e-13, (B, H, N, d, causal)
+        assert np.abs(L - np.array(Ld)).max() < 1e-13, (B, H, N, d, causal)
+
+
+# ----------------------------------------------------------------------------------------------
+# closed forms
+# ----------------------------------------------------------------------------------------------
+
+def pin_closed_form_uniform_scores(orc):
+    """All keys equal: every allowed key gets the same weight, so O is the mean of the
+    allowed value rows and LSE = s + ln(#allowed)."""
+    B, H, N, d = 1, 2, 11, 4
+    q, _, v = inputs.attn_inputs(B, H, N, d, seed=5)
+    krow = torch.tensor([0.5, -1.0, 0.25, 2.0]).to(torch.bfloat16)
+    k = krow.expand(B, H, N, d).contiguous()
+    qf, kf, vf = _bf16_float(q), _bf16_float(k), _bf16_float(v)
+    for causal in (False, True):
+        O, L = orc.attention(q, k, v, 0.3, causal)
+        for h in range(H):
+            for i in range(N):
+                n_allowed = i + 1 if causal else N
+                want = vf[0, h, :n_allowed].mean(axis=0)
+                s = 0.3 * float(qf[0, h, i] @ kf[0, h, 0])
+                assert np.abs(O[0, h, i] - want).max() < 1e-14
+                assert abs(L[0, h, i] - (s + math.log(n_allowed))) < 1e-13
+
+
+def pin_closed_form_first_causal_row(orc):
+    """Causal row 0 sees key 0 only: O_0 = V_0 and LSE_0 = s_00."""
+    q, k, v = inputs.attn_inputs(2, 3, 9, 8, seed=6)
+    O, L = orc.attention(q, k, v, 0.25, True)
+    qf, kf, vf = _bf16_float(q), _bf16_float(k), _bf16_float(v)
+    assert np.array_equal(O[:, :, 0], vf[:, :, 0])
+    s00 = 0.25 * np.einsum("bhk,bhk->bh", qf[:, :, 0], kf[:, :, 0])
+    assert np.abs(L[:, :, 0] - s00).max() < 1e-13
+
+
+def pin_closed_form_two_keys(orc):
+    """Two keys: weight of key 0 is the logistic 1 / (1 + exp(s1 - s0))."""
+    q, k, v = inputs.attn_inputs(1, 1, 2, 6, seed=8, qk_std=2.0)
+    O, L = orc.attention(q, k, v, 0.7, False)
+    qf, kf, vf = _bf16_float(q)[0, 0], _bf16_float(k)[0, 0], _bf16_float(v)[0, 0]
+    for i in range(2):
+        s0 = 0.7 * float(qf[i] @ kf[0])
+        s1 = 0.7 * float(qf[i] @ kf[1])
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        assert np.abs(O[0, 0, i] - (w0 * vf[0] + (1 - w0) * vf[1])).max() < 1e-14
+        hi = max(s0, s1)
+        assert abs(L[0, 0, i] - (hi + math.log1p(math.exp(-abs(s1 - s0))))) < 1e-13
+
+
+def pin_closed_form_constant_values_and_zero_scale(orc):
+    q, k, _ = inputs.attn_inputs(1, 2, 13, 4, seed=9, qk_std=3.0)
+    v = torch.full((1, 2, 13, 4), 0.75).to(torch.bfloat16)
+    O, _ = orc.attention(q, k, v, 0.5, True)
+    assert np.abs(O - 0.75).max() < 1e-14
+    q, k, v = inputs.attn_inputs(1, 1, 10, 4, seed=10)
+    O, L = orc.attention(q, k, v, 0.0, False)
+    assert np.abs(O[0, 0] - _bf16_float(v)[0, 0].mean(axis=0)).max() < 1e-14
+    assert np.abs(L - math.log(10.0)).max() < 1e-14
+
+
+# ----------------------------------------------------------------------------------------------
+# invariants and laws
+# ----------------------------------------------------------------------------------------------
+
+def pin_shift_invariance(orc):
+    """Adding one constant to every score of a row leaves O unchanged and moves LSE by it.
+    Done by appending a feature: q' = [q, a], k'_j = [k_j, b] adds scale*a*b to every s_j."""
+    q, k, v = inputs.attn_inputs(1, 2, 9, 3, seed=12)
+    O, L = orc.attention(q, k, v, 0.5, False)
+    a, b = 4.0, 8.0  # bf16-exact, shift = 0.5 * 32 = 16
+    q4 = torch.cat([q, torch.full((1, 2, 9, 1), a).to(torch.bfloat16)], dim=-1)
+    k4 = torch.cat([k, torch.full((1, 2, 9, 1), b).to(torch.bfloat16)], dim=-1)
+    v4 = torch.cat([v, torch.zeros((1, 2, 9, 1)).to(torch.bfloat16)], dim=-1)
+    O4, L4 = orc.attention(q4, k4, v4, 0.5, False)
+    assert np.abs(O4[..., :3] - O).max() < 1e-14
+    assert np.abs(L4 - (L + 16.0)).max() < 1e-12
+
+
+def pin_key_permutation_invariance(orc):
+    q, k, v = inputs.attn_inputs(1, 1, 12, 4, seed=13)
+    perm = torch.randperm(12, generator=torch.Generator().manual_seed(3))
+    O, L = orc.attention(q, k, v, 0.5, False)
+    Op, Lp = orc.attention(q, k[:, :, perm], v[:, :, perm], 0.5, False)
+    assert np.abs(O - Op).max() < 1e-14 and np.abs(L - Lp).max() < 1e-13
+    Oq, _ = orc.attention(q[:, :, perm], k, v, 0.5, False)
+    assert np.abs(Oq - O[:, :, perm.numpy()]).max() < 1e-14
+
+
+def pin_block_size_independence(orc):
+    """The streamed state at any block size gives the three-pass attention of that row."""
+    N, d = 300, 16
+    q, k, v = inputs.attn_inputs(1, 1, N, d, seed=14)
+    O, L = orc.attention(q, k, v, 0.25, False, rows=np.array([0, 117, N - 1]))
+    qf, kf, vf = _bf16_float(q)[0, 0], _bf16_float(k)[0, 0], _bf16_float(v)[0, 0]
+    for r, i in enumerate([0, 117, N - 1]):
+        s = 0.25 * (kf @ qf[i])
+        for block in (1, 7, 64, 128, N):
+            st = orc.online_state(s, vf, block=block)
+            assert np.abs(st["acc"] / st["l"] - O[r]).max() < 1e-12, block
+            assert abs(st["m"] + math.log(st["l"]) - L[r]) < 1e-12
+
+
+def pin_merge_law(orc):
+    """Two workers stream disjoint halves; merging their states equals one pass."""
+    rng = np.random.default_rng(3)
+    s, v = rng.normal(0, 3, size=100), rng.standard_normal((100, 8))
+    whole = orc.online_state(s, v, block=10)
+    left = orc.online_state(s[:37], v[:37], block=10)
+    right = orc.online_state(s[37:], v[37:], block=10)
+    for a, b in ((left, right), (right, left)):
+        mg = orc.merge(a, b)
+        assert abs(mg["m"] - whole["m"]) < 1e-15
+        assert abs(mg["l"] - whole["l"]) < 1e-12 * whole["l"]
+        assert np.abs(mg["acc"] - whole["acc"]).max() < 1e-12 * np.abs(whole["acc"]).max()
+    empty = dict(m=-math.inf, l=0.0, acc=np.zeros(8))
+    e = orc.merge(empty, left)
+    assert e["l"] == left["l"] and np.array_equal(e["acc"], left["acc"])
+
+
+def pin_softmax_rows_sum_to_one(orc):
+    x = inputs.softmax_inputs(16, 1000, seed=15).numpy()
+    y, lse = orc.softmax_rows(x)
+    assert np.abs(y.sum(axis=1) - 1.0).max() < 1e-13
+    assert np.all(y >= 0.0)
+    # shift invariance of the softmax itself
+    y2, lse2 = orc.softmax_rows(x + np.float32(3.0))
+    assert np.abs(y2 - y).max() < 1e-6  # x + 3 is rounded to fp32 again
+    assert np.abs(lse2 - lse - 3.0).max() < 1e-4
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
