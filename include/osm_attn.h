@@ -1,0 +1,98 @@
+/*
+ * osm_attn.h -- C ABI of libosmattn.so: exact attention forward with the online softmax, and
+ * the standalone single-pass row softmax, on NVIDIA GB300 (sm_103a).
+ *
+ * All pointers are DEVICE pointers (CUDA global memory) unless a comment says otherwise.
+ * The caller owns every buffer; the library allocates no device memory in any call listed
+ * here.  It caches host-side kernel attributes and the CUDA driver entry point it needs for
+ * TMA descriptors.  Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ * NULL is the legacy default stream) and returns an fa_status code.  Argument errors are
+ * found on the host before anything is launched.
+ */
+#ifndef OSM_ATTN_H
+#define OSM_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null, negative or inconsistent sizes, misaligned pointer,
+                               non-finite or non-positive scale, O aliasing an input */
+    FA_ERR_UNSUPPORTED = 2, /* a valid request this build does not serve (d not 64/128) */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch error, no device) */
+    FA_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait (reported by
+                               osm_attn_device_status) */
+} fa_status;
+
+/*
+ * fa_fwd -- O = softmax(scale * Q K^T [+ causal mask]) V and LSE, for every (b, h, i).
+ *
+ * Defines the operation of "How FlashAttention avoids storing the giant score table"
+ * (spicyshark.co, Online softmax lesson), section "From softmax to attention": the score of
+ * key j for query i is s_ij = scale * (q_i . k_j); the output is the softmax-weighted sum of
+ * the value rows, O_i = sum_j exp(s_ij - m_i) v_j / l_i with m_i = max_j s_ij and
+ * l_i = sum_j exp(s_ij - m_i).  It is computed tile by tile with the running max / running
+ * sum / rescaled accumulator of that section's block recipe (and of "kbwen.com
+ * FlashAttention", sections "Two blocks" and "More than two blocks"), with the divide by l
+ * deferred to the end, so the N x N score matrix never reaches device memory.
+ *
+ *   Q, K, V  bf16, [B, H, N, d] contiguous (d innermost), 16-byte aligned, read only.
+ *   O        bf16, [B, H, N, d] contiguous, 16-byte aligned, written; must not be Q, K or V.
+ *   LSE      fp32, [B, H, N], 4-byte aligned, written; may be NULL (not written).
+ *            LSE_i = m_i + ln l_i, the natural-log log-sum-exp of the SCALED scores.
+ *   B, H, N  batch, heads, sequence length (queries = keys = N); any N >= 0.
+ *            B*H*N == 0 is a no-op returning FA_OK.
+ *   d        head dimension: 64 or 128 (other values: FA_ERR_UNSUPPORTED).
+ *   scale    finite and > 0 (typically 1/sqrt(d)).
+ *   causal   0: every key; non-zero: key j is allowed for query i only when j <= i.
+ *   stream   cudaStream_t, or NULL.
+ * Precision: bf16 inputs, fp32 accumulation of both products, probabilities rounded to bf16
+ * for the second product, fp32 running max/sum, bf16 output, fp32 LSE.
+ */
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+           int64_t H, int64_t N, int64_t d, float scale, int causal, void* stream);
+
+/*
+ * osm_softmax -- y = softmax(x) of every row, single pass over HBM, and its log-sum-exp.
+ *
+ * Defines the operation of the same lesson, sections "The idea" and "The implementation":
+ * the running maximum m and running sum l = sum exp(x - m), rescaled by exp(m_old - m_new)
+ * whenever the maximum grows, give both statistics in one read; partial states of disjoint
+ * parts of a row combine by the lesson's two-worker merge; y_j = exp(x_j - m) / l.  Rows up
+ * to 16384 columns are read from HBM once and kept on chip for the write (one read, one
+ * write per element); longer rows are read twice (statistics, then output), the lesson's
+ * "online softmax with the output written".
+ *
+ *   x     fp32 [rows, cols] contiguous, 4-byte aligned, read only.
+ *   y     fp32 [rows, cols] contiguous, written; may equal x (in place).
+ *   lse   fp32 [rows] (m + ln l), written; may be NULL.
+ *   rows, cols >= 0; rows*cols == 0 is a no-op (lse is not written).
+ *   A row with no finite entry (all -inf) gives y = 0 and lse = -inf.
+ */
+int osm_softmax(const float* x, float* y, int64_t rows, int64_t cols, float* lse,
+                void* stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char* fa_status_string(int status);
+
+/*
+ * osm_attn_device_status -- synchronises `stream`, then reads and clears the device status
+ * word the kernels set when a bounded wait gives up (FA_OK when none did).  *status
+ * (HOST pointer) receives the code; the return value is FA_OK or FA_ERR_CUDA.
+ */
+int osm_attn_device_status(void* stream, int* status);
+
+/* ABI version of this header (incremented on any incompatible change). */
+int osm_attn_abi_version(void);
+
+#define OSM_ATTN_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSM_ATTN_H */

@@ -1,0 +1,150 @@
+"""ctypes binding of libosmattn.so: the same entry points as include/osm_attn.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA library.  PyTorch is
+used for device memory and streams.  There is no fallback: if the library cannot be built or
+loaded, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import build_lib
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libosmattn.so (building it in-tree with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build_lib.LIB
+            if not build_lib.up_to_date():
+                path = build_lib.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library {path} is missing")
+            L = ctypes.CDLL(path)
+            vp, i64 = ctypes.c_void_p, ctypes.c_int64
+            L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
+                                 ctypes.c_int, vp]
+            L.fa_fwd.restype = ctypes.c_int
+            L.osm_softmax.argtypes = [vp, vp, i64, i64, vp, vp]
+            L.osm_softmax.restype = ctypes.c_int
+            L.fa_status_string.argtypes = [ctypes.c_int]
+            L.fa_status_string.restype = ctypes.c_char_p
+            L.osm_attn_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+            L.osm_attn_device_status.restype = ctypes.c_int
+            L.osm_attn_abi_version.argtypes = []
+            L.osm_attn_abi_version.restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+# ------------------------------------------------------------------------------------------
+# raw entry points (integers for pointers): the C ABI as is
+# ------------------------------------------------------------------------------------------
+def fa_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, stream_ptr):
+    return lib().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
+                        float(scale), int(bool(causal)), stream_ptr)
+
+
+def osm_softmax_raw(x_ptr, y_ptr, rows, cols, lse_ptr, stream_ptr):
+    return lib().osm_softmax(x_ptr, y_ptr, int(rows), int(cols), lse_ptr, stream_ptr)
+
+
+def device_status(stream=None) -> int:
+    """Synchronise `stream` and read/clear the kernels' bounded-wait status word."""
+    st = ctypes.c_int(0)
+    rc = lib().osm_attn_device_status(_stream_handle(stream), ctypes.byref(st))
+    if rc != FA_OK:
+        raise FaError(rc, "osm_attn_device_status")
+    return st.value
+
+
+# ------------------------------------------------------------------------------------------
+# torch-tensor wrappers
+# ------------------------------------------------------------------------------------------
+def fa_fwd(q, k, v, scale=None, causal=False, out=None, lse=None, return_lse=True,
+           stream=None):
+    """O, LSE = attention(q, k, v) for CUDA bf16 tensors [B, H, N, d] (d = 64 or 128).
+
+    scale defaults to 1/sqrt(d).  `out` ([B,H,N,d] bf16) and `lse` ([B,H,N] fp32) may be
+    given to write into; with return_lse=False and no `lse`, LSE is not computed.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 [B, H, N, d] tensor")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise TypeError("out must be a contiguous bf16 tensor shaped like q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != B * H * N
+                            or not lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous fp32 tensor of B*H*N elements")
+    rc = fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                    lse.data_ptr() if lse is not None else None, B, H, N, d, scale, causal,
+                    _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return out, lse
+
+
+def osm_softmax(x, out=None, lse=None, return_lse=True, stream=None):
+    """y, lse = softmax of every row of a CUDA fp32 tensor [rows, cols] (out may be x)."""
+    import torch
+
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32:
+        raise TypeError("x must be a CUDA fp32 tensor")
+    if x.dim() != 2 or not x.is_contiguous():
+        raise TypeError("x must be a contiguous [rows, cols] tensor")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != torch.float32 or not out.is_contiguous():
+        raise TypeError("out must be a contiguous fp32 tensor shaped like x")
+    if lse is None and return_lse:
+        lse = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    rc = osm_softmax_raw(x.data_ptr(), out.data_ptr(), rows, cols,
+                         lse.data_ptr() if lse is not None else None, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "osm_softmax")
+    return out, lse

@@ -1,0 +1,101 @@
+// capi.cu -- the extern "C" boundary of libosmattn.so (declared in include/osm_attn.h).
+//
+// Every argument is checked here, on the host, before anything is launched; a rejected call
+// launches nothing and touches no buffer.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "osm_internal.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// [a, a + a_bytes) and [b, b + b_bytes) share at least one byte.
+bool overlaps(const void* a, uint64_t a_bytes, const void* b, uint64_t b_bytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + b_bytes && y < x + a_bytes;
+}
+
+// a * b without signed overflow, for non-negative operands; false when it would overflow.
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+           int64_t H, int64_t N, int64_t d, float scale, int causal, void* stream) {
+    if (B < 0 || H < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
+    int64_t bh, rows, elems;
+    if (!mul_ok(B, H, &bh) || !mul_ok(bh, N, &rows) || !mul_ok(rows, d, &elems) ||
+        elems > INT64_MAX / 2)
+        return FA_ERR_INVALID_ARG;
+    if (rows == 0) return FA_OK;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!Q || !K || !V || !O) return FA_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16))
+        return FA_ERR_INVALID_ARG;
+    if (LSE && !aligned(LSE, 4)) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    const uint64_t bytes = static_cast<uint64_t>(elems) * 2;      // each of Q, K, V, O
+    const uint64_t lse_bytes = static_cast<uint64_t>(rows) * 4;   // LSE
+    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) ||
+        overlaps(O, bytes, V, bytes))
+        return FA_ERR_INVALID_ARG;
+    if (LSE && (overlaps(LSE, lse_bytes, O, bytes) || overlaps(LSE, lse_bytes, Q, bytes) ||
+                overlaps(LSE, lse_bytes, K, bytes) || overlaps(LSE, lse_bytes, V, bytes)))
+        return FA_ERR_INVALID_ARG;
+    return osm::fa_fwd_launch(Q, K, V, O, LSE, bh, N, d, scale, causal != 0,
+                              static_cast<cudaStream_t>(stream));
+}
+
+int osm_softmax(const float* x, float* y, int64_t rows, int64_t cols, float* lse,
+                void* stream) {
+    if (rows < 0 || cols < 0) return FA_ERR_INVALID_ARG;
+    int64_t elems;
+    if (!mul_ok(rows, cols, &elems) || elems > INT64_MAX / 4) return FA_ERR_INVALID_ARG;
+    if (elems == 0) return FA_OK;  // nothing to read or write (lse is not written)
+    if (!x || !y) return FA_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(y, 4) || (lse && !aligned(lse, 4))) return FA_ERR_INVALID_ARG;
+    const uint64_t xy_bytes = static_cast<uint64_t>(elems) * 4;
+    if (x != y && overlaps(x, xy_bytes, y, xy_bytes)) return FA_ERR_INVALID_ARG;
+    if (lse && (overlaps(lse, static_cast<uint64_t>(rows) * 4, x, xy_bytes) ||
+                overlaps(lse, static_cast<uint64_t>(rows) * 4, y, xy_bytes)))
+        return FA_ERR_INVALID_ARG;
+    return osm::osm_softmax_launch(x, y, rows, cols, lse, static_cast<cudaStream_t>(stream));
+}
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: valid but not supported by this build";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up a bounded wait";
+        default: return "unknown fa_status";
+    }
+}
+
+int osm_attn_device_status(void* stream, int* status) {
+    if (!status) return FA_ERR_INVALID_ARG;
+    int raw = 0;
+    const int rc = osm::fa_read_device_status(static_cast<cudaStream_t>(stream), &raw);
+    if (rc != FA_OK) return rc;
+    *status = raw & 0xff;
+    return FA_OK;
+}
+
+int osm_attn_abi_version(void) { return OSM_ATTN_ABI_VERSION; }
+
+}  // extern "C"
+
+namespace osm {
+unsigned long long fa_wait_timeout_ns() { return 2000000000ull; }  // 2 s
+}  // namespace osm

@@ -1,0 +1,27 @@
+// osm_internal.h -- declarations shared by the translation units of libosmattn.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "osm_attn.h"
+
+namespace osm {
+
+// Tiled TMA descriptor over a [BH, N, d] bf16 tensor (d innermost): a box of 64 columns x 128
+// rows of one (b, h), 128-byte swizzle, zero fill outside [0, N) x [0, d).
+int make_bhnd_tensor_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t d);
+
+// Deadline of every bounded mbarrier wait in the attention kernel.
+unsigned long long fa_wait_timeout_ns();
+
+int fa_fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t BH,
+                  int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream);
+int fa_read_device_status(cudaStream_t stream, int* status);
+
+int osm_softmax_launch(const float* x, float* y, int64_t rows, int64_t cols, float* lse,
+                       cudaStream_t stream);
+
+}  // namespace osm

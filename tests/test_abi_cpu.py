@@ -1,0 +1,107 @@
+"""The C-ABI library builds, loads on a machine without a GPU, exports every function that
+include/osm_attn.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from online_softmax_tiled_attn_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for f in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_fwd", "osm_softmax", "fa_status_string", "osm_attn_device_status",
+              "osm_attn_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = binding.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), n
+        assert isinstance(getattr(L, n), ctypes._CFuncPtr)
+
+
+def test_status_strings_and_version():
+    assert binding.status_string(0) == "FA_OK"
+    for s in range(1, 5):
+        assert binding.status_string(s).startswith("FA_ERR_")
+    assert binding.status_string(99) == "unknown fa_status"
+    assert binding.lib().osm_attn_abi_version() == 1
+
+
+# A fake device address: every case below must be rejected on the host, before any launch,
+# so it is never dereferenced.
+P = 1 << 20
+
+
+@pytest.mark.parametrize(
+    "args, want",
+    [
+        ((P, P + 4096, P + 8192, P + 12288, 0, -1, 1, 128, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),
+        ((P, P + 4096, P + 8192, P + 12288, 0, 1, 1, -5, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),
+        ((0, 0, 0, 0, 0, 1, 1, 0, 64, 0.125, 0), binding.FA_OK),  # empty: no-op
+        ((0, 0, 0, 0, 0, 0, 8, 128, 64, 0.125, 1), binding.FA_OK),  # B = 0: no-op
+        ((P, P + 4096, P + 8192, P + 12288, 0, 1, 1, 128, 96, 0.125, 0), binding.FA_ERR_UNSUPPORTED),
+        ((P, P + 4096, P + 8192, P + 12288, 0, 1, 1, 128, 32, 0.125, 0), binding.FA_ERR_UNSUPPORTED),
+        ((0, P + 4096, P + 8192, P + 12288, 0, 1, 1, 128, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),
+        ((P + 2, P + 65536, P + 131072, P + 196608, 0, 1, 1, 128, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),
+        ((P, P + 65536, P + 131072, P + 196608, 0, 1, 1, 128, 64, float("nan"), 0), binding.FA_ERR_INVALID_ARG),
+        ((P, P + 65536, P + 131072, P + 196608, 0, 1, 1, 128, 64, float("inf"), 0), binding.FA_ERR_INVALID_ARG),
+        ((P, P + 65536, P + 131072, P + 196608, 0, 1, 1, 128, 64, 0.0, 0), binding.FA_ERR_INVALID_ARG),
+        ((P, P + 65536, P + 131072, P + 196608, 0, 1, 1, 128, 64, -0.125, 0), binding.FA_ERR_INVALID_ARG),
+        ((P, P + 65536, P + 131072, P, 0, 1, 1, 128, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),  # O == Q
+        ((P, P + 65536, P + 131072, P + 131072 + 64, 0, 1, 1, 128, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),  # O overlaps V
+        ((P, P + 65536, P + 131072, P + 196608, P + 196608 + 2, 1, 1, 128, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),  # LSE misaligned
+        ((P, P + 65536, P + 131072, P + 196608, 0, 1 << 40, 1 << 40, 128, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),  # overflow
+        ((P, P + 65536, P + 131072, P + 196608, P + 196608 + 4096, 1, 1, 128, 64, 0.125, 0), binding.FA_ERR_INVALID_ARG),  # LSE inside O
+    ],
+)
+def test_fa_fwd_rejects_on_host(args, want):
+    assert binding.fa_fwd_raw(*args, None) == want
+
+
+@pytest.mark.parametrize(
+    "args, want",
+    [
+        ((P, P, -1, 10, 0), binding.FA_ERR_INVALID_ARG),
+        ((P, P, 10, -1, 0), binding.FA_ERR_INVALID_ARG),
+        ((0, 0, 0, 10, 0), binding.FA_OK),
+        ((0, 0, 10, 0, P), binding.FA_OK),
+        ((0, P, 10, 10, 0), binding.FA_ERR_INVALID_ARG),
+        ((P + 1, P + 8192, 10, 10, 0), binding.FA_ERR_INVALID_ARG),
+        ((P, P + 8, 10, 10, 0), binding.FA_ERR_INVALID_ARG),  # partial overlap
+        ((P, P + 8192, 1 << 40, 1 << 40, 0), binding.FA_ERR_INVALID_ARG),
+    ],
+)
+def test_osm_softmax_rejects_on_host(args, want):
+    assert binding.osm_softmax_raw(*args, None) == want
+
+
+def test_fa_fwd_accepts_lse_just_below_an_input():
+    """A small LSE buffer that ends right where Q starts does not overlap it.  The call passes
+    validation and reaches the CUDA launch, which fails without a GPU (FA_ERR_CUDA), or
+    succeeds with one; it is never FA_ERR_INVALID_ARG."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("covered by the GPU tests on a machine with a GPU")
+    B, H, N, d = 1, 1, 128, 64
+    lse = P
+    q = P + B * H * N * 4  # LSE [P, P + 512) ends where Q starts
+    n = B * H * N * d * 2
+    rc = binding.fa_fwd_raw(q, q + n, q + 2 * n, q + 3 * n, lse, B, H, N, d, 0.125, 0, None)
+    assert rc == binding.FA_ERR_CUDA

@@ -1,0 +1,74 @@
+"""Host-side logic of bench.py, on the CPU: clock-sample parsing, the max-over-ranks timing
+with two gloo ranks, and the bounded oracle sample of the CPU baseline."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_clock_summary_flags_throttle_reasons():
+    rows = [
+        ["0", "1965", "2070", "900.1", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"],
+        ["0", "1890", "2070", "1350.0", "0x4", "Not Active", "Not Active", "Not Active", "Active"],
+        ["0", "1500", "2070", "1390.0", "0x8", "Active", "Not Active", "Not Active", "Active"],
+        ["garbage"],
+    ]
+    s = bench.ClockSampler.summarise(rows)
+    assert s["samples"] == 3 and s["sm_mhz"] == 1890 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert bench.ClockSampler.summarise([])["sm_mhz"] is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist = bench.dist_init("gloo")
+    got = bench.max_over_ranks(1.5 + rank, dist)
+    bench.barrier(dist)
+    q.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 2.5, 1: 2.5}
+
+
+def test_single_process_has_no_collective():
+    assert bench.max_over_ranks(3.0, None) == 3.0
+
+
+def test_oracle_rate_is_bounded_and_positive():
+    from online_softmax_tiled_attn_gb300 import inputs
+
+    w = inputs.ATTN_WORKLOADS["small_b1h1n256d64"]
+    rate, n, total, dt = bench.oracle_rate(w, budget_s=0.2)
+    assert rate > 0 and 1 <= n <= total == 256 and dt < 10
+
+
+def test_workload_flops_match_the_metric_definition():
+    from online_softmax_tiled_attn_gb300 import inputs
+
+    w = inputs.ATTN_WORKLOADS["mha_b4h16n2048d64"]
+    assert w.flops == 4 * 4 * 16 * 2048 ** 2 * 64
+    c = inputs.ATTN_WORKLOADS["causal_b2h32n8192"]
+    assert c.flops == 4 * 2 * 32 * 8192 ** 2 * 128 / 2

@@ -1,0 +1,160 @@
+"""fa_fwd on the GPU, through the C ABI, against the fp64 oracle on the same seeded inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from online_softmax_tiled_attn_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    binding.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+def run_gpu(q, k, v, scale, causal, stream=None):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    O, L = binding.fa_fwd(qd, kd, vd, scale=scale, causal=causal, stream=stream)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    return O.float().cpu().numpy(), L.cpu().numpy()
+
+
+SMALL = [(1, 1, 256, 64, False, 1.0)]  # the small B1 H1 N256 d64 workload, checked in full
+for _N in (1, 4, 5, 127, 128, 129, 255, 300, 1000):
+    for _d in (64, 128):
+        for _c in (False, True):
+            SMALL.append((1, 1, _N, _d, _c, 1.0))
+SMALL += [(2, 3, 700, 128, True, 1.0), (2, 3, 700, 64, False, 1.0), (1, 2, 517, 128, False, 3.0),
+          (1, 2, 517, 64, True, 3.0), (3, 1, 384, 128, True, 1.0)]
+# Cases with Q, K sd 3 (logits sd 9, as the ragged overflow stress workload) take that
+# workload's U(-1, 1) values: |O| <= 1, where bf16 output rounding stays below 2e-3.  With
+# N(0, 1) values |O| can reach 2-4, where the bf16 half-ulp alone is 7.8e-3.
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,qk_std", SMALL,
+                         ids=lambda x: str(x))
+def test_parity_full(B, H, N, d, causal, qk_std):
+    q, k, v = inputs.attn_inputs(B, H, N, d, seed=4000 + N + d + 7 * causal, qk_std=qk_std,
+                                 v_dist="uniform" if qk_std > 1.0 else "normal")
+    scale = 1.0 / math.sqrt(d)
+    O, L = run_gpu(q, k, v, scale, causal)
+    Oref, Lref = oracle.attention(q, k, v, scale, causal)
+    parity.check_attention(O, L, Oref, Lref, f"B{B}H{H}N{N}d{d}c{int(causal)}")
+
+
+@pytest.mark.parametrize("name", [n for n in inputs.ATTN_WORKLOADS if n != "small_b1h1n256d64"])
+def test_parity_full_size_sampled(name):
+    w = inputs.ATTN_WORKLOADS[name]
+    q, k, v = inputs.workload_inputs(w)
+    O, L = run_gpu(q, k, v, w.scale, w.causal)
+    per_head = w.sample_rows_per_head or 64
+    rows = inputs.sample_rows(w, per_head)
+    Oref, Lref = oracle.attention(q, k, v, w.scale, w.causal, rows=rows)
+    parity.check_attention(O.reshape(-1, w.d)[rows], L.reshape(-1)[rows], Oref, Lref, name)
+    # properties over every row: finite output, causal first row = first value row
+    assert np.isfinite(O).all() and np.isfinite(L).all()
+    if w.causal:
+        v0 = v[:, :, 0].float().numpy()
+        assert np.array_equal(O[:, :, 0], v0)
+        s00 = w.scale * np.einsum("bhk,bhk->bh", q[:, :, 0].double().numpy(),
+                                  k[:, :, 0].double().numpy())
+        assert np.abs(L[:, :, 0] - s00).max() <= 1e-3 * max(1.0, np.abs(s00).max())
+
+
+def _padded(values, N, d):
+    t = torch.zeros(1, 1, N, d)
+    t[0, 0, : len(values), 0] = torch.tensor(values)
+    return t.to(torch.bfloat16)
+
+
+def test_scalar_case_four_scores():
+    """Scores 1, 3, 5, 2 with values 10, 20, 30, 40 (one query, d = 1) at d = 64 zero-padded;
+    the exact output 28.98474626 rounds to 29.0 in bf16."""
+    q = _padded([1.0] * 4, 4, 64)
+    k = _padded([1.0, 3.0, 5.0, 2.0], 4, 64)
+    v = _padded([10.0, 20.0, 30.0, 40.0], 4, 64)
+    O, L = run_gpu(q, k, v, 1.0, False)
+    Oref, Lref = oracle.attention(q, k, v, 1.0, False)
+    assert abs(Oref[0, 0, 0, 0] - 28.98474626) < 5e-9
+    want = torch.tensor(Oref[0, 0, :, 0]).to(torch.bfloat16).float().numpy()
+    ulp = 0.125  # bf16 spacing in [16, 32)
+    assert np.abs(O[0, 0, :, 0] - want).max() <= ulp
+    assert np.all(O[0, 0, :, 1:] == 0.0)
+    assert np.abs(L[0, 0] - (5.0 + math.log(math.exp(-4) + math.exp(-2) + 1 + math.exp(-3)))).max() < 1e-5
+
+
+def test_scalar_case_counter_example():
+    """Scores 0, 0, ln3, ln3 (keys 0, 0, 1, 1 with scale = fp32(ln 3)), values 0, 0, 1, 1:
+    the answer is 0.75, not the 0.5 of averaging the two block results."""
+    q = _padded([1.0] * 4, 4, 64)
+    k = _padded([0.0, 0.0, 1.0, 1.0], 4, 64)
+    v = _padded([0.0, 0.0, 1.0, 1.0], 4, 64)
+    scale = float(np.float32(math.log(3.0)))
+    O, L = run_gpu(q, k, v, scale, False)
+    Oref, Lref = oracle.attention(q, k, v, scale, False)
+    assert np.all(O[0, 0, :, 0] == 0.75)
+    assert np.abs(L[0, 0] - Lref[0, 0]).max() < 1e-5
+    assert abs(Lref[0, 0, 0] - math.log(8.0)) < 1e-6
+
+
+def test_deterministic_and_stream():
+    q, k, v = inputs.attn_inputs(2, 2, 640, 128, seed=9)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    O1, L1 = binding.fa_fwd(qd, kd, vd, causal=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        O2, L2 = binding.fa_fwd(qd, kd, vd, causal=True, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+def test_guard_zones_untouched_and_lse_optional():
+    B, H, N, d = 1, 2, 300, 128
+    q, k, v = inputs.attn_inputs(B, H, N, d, seed=10)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    G = 4096
+    n = B * H * N * d
+    obuf = torch.full((G + n + G,), 7.0, dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((G + B * H * N + G,), -3.0, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = binding.fa_fwd_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(),
+                            obuf[G:].data_ptr(), lbuf[G:].data_ptr(), B, H, N, d,
+                            1 / math.sqrt(d), 0, stream)
+    assert rc == binding.FA_OK
+    torch.cuda.synchronize()
+    assert torch.all(obuf[:G] == 7.0) and torch.all(obuf[G + n:] == 7.0)
+    assert torch.all(lbuf[:G] == -3.0) and torch.all(lbuf[G + B * H * N:] == -3.0)
+    Oref, Lref = oracle.attention(q, k, v, 1 / math.sqrt(d), False)
+    O = obuf[G:G + n].float().cpu().numpy().reshape(B, H, N, d)
+    L = lbuf[G:G + B * H * N].cpu().numpy().reshape(B, H, N)
+    parity.check_attention(O, L, Oref, Lref)
+    # LSE may be NULL
+    O2, L2 = binding.fa_fwd(qd, kd, vd, return_lse=False)
+    torch.cuda.synchronize()
+    assert L2 is None
+    assert torch.equal(O2, obuf[G:G + n].view(B, H, N, d))
+
+
+def test_empty_and_invalid_on_device():
+    q = torch.zeros(1, 1, 0, 64, dtype=torch.bfloat16, device="cuda")
+    O, L = binding.fa_fwd(q, q, q)
+    assert O.numel() == 0
+    bad = torch.zeros(1, 1, 16, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.FaError) as e:
+        binding.fa_fwd(bad, bad, bad)
+    assert e.value.status == binding.FA_ERR_UNSUPPORTED
+    x = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.FaError):
+        binding.fa_fwd(x, x, x, out=x)
+    with pytest.raises(binding.FaError):
+        binding.fa_fwd(x, x, x, scale=0.0)
