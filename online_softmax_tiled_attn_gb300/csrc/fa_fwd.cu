@@ -10,26 +10,29 @@
 // exponentials may be any common constant per row ("The fix: subtract the maximum": the
 // factor cancels), which is what allows the lazy rescale below.
 //
-// GB300 mapping.  One CTA owns two 128-row query tiles (t = 0, 1) of one (b, h); both walk the
-// same 128-key K/V tiles, so each K/V tile is staged once for 256 query rows.
-//   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: one query row per thread, the
-//               row's TMEM lane.  tcgen05.ld of the S row (128 fp32), mask, row max, ex2 of
-//               the scaled and shifted scores (scale*log2(e) folded into one FFMA), row sum,
-//               P rounded to bf16 and written back into TMEM over the upper half of S.
-//               At the end: O / l to bf16 and LSE = (m + log2 l) * ln 2.
-//   warps 8-11  correction: when a row's reference max moved, scale that row of the O
-//               accumulator in TMEM by alpha before the next P V is issued.
-//   warp 12     tcgen05.mma (one thread): S_t = Q_t K^T (A and B from shared memory), then
-//               O_t += P_t V (A = P_t from TMEM, B = V from shared memory); fp32 accumulators.
-//               The two tiles alternate, so the tensor core works on one tile while the
-//               other tile's softmax runs.
-//   warp 13     TMA: Q_0, Q_1 once, K and V tiles into 2-stage rings (128-byte swizzle,
-//               zero fill past N).
-// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256, 256+d), O_1 [256+d, 256+2d);
-// P_t occupies columns [64,128) of S_t (two bf16 per column).
-// Lazy rescale: a row keeps its reference max m until a tile's max exceeds it by more than
-// 8 (log2 units); the exponentials then stay <= 2^8, far inside fp32/bf16 range, and O only
-// needs rescaling when the reference moves.
+// GB300 mapping.  One CTA owns one 128-row query tile of one (b, h) and walks its key tiles
+// (128 keys each).  Both products run on the tensor cores with A taken from tensor memory:
+//   S = Q K^T   A = Q (copied once into TMEM), B = K tile (shared memory, K-major)
+//   O += P V    A = P (TMEM),                  B = V tile (shared memory, MN-major)
+// TMEM (512 columns): S_a [0,128), S_b [128,256), O [256, 256+d), P [256+d, 256+d+64),
+// Q [256+d+64, 256+d+64+d/2); bf16 operands hold two values per 32-bit column.
+// S is double-buffered: S(j+2) is computed while the softmax of S(j+1) runs, and P has its
+// own columns, so the tensor core never waits for P V before the next S.
+//   warps 0-3 / 4-7  softmax of score columns [0,64) / [64,128): one query row per thread (its
+//                    TMEM lane).  tcgen05.ld of 64 S values, mask, half-row max, the two halves
+//                    exchange their maxima through shared memory (one mbarrier), lazy
+//                    reference max, ex2 of the scaled and shifted scores (scale*log2(e) folded
+//                    into one FFMA), half-row sum, P rounded to bf16 and stored to TMEM.  When a
+//                    row's reference max moves (rare: only beyond 2^8), the thread scales its
+//                    half of the O row in TMEM by alpha before storing P.  At the end: O / l to
+//                    bf16 and LSE = (m + log2 l) * ln 2.
+//   warps 8, 9       tcgen05.mma, one thread each: warp 8 issues S(j+2) as soon as the softmax
+//                    has read S(j); warp 9 issues O += P(j) V(j) as soon as P(j) is stored.  One
+//                    thread cannot issue M128 N128 K16 MMAs much faster than the tensor core runs
+//                    them, so with a single issuer every wait and commit between groups left the
+//                    tensor core idle; two independent streams keep it fed.  fp32 accumulators.
+//   warps 10, 11     TMA: Q once and the K ring (warp 10), the V ring (warp 11); 128-byte
+//                    swizzle, zero fill past N.  K runs ahead of V on its own.
 // Causal: key tiles above the diagonal are never visited; only diagonal and ragged tiles are
 // masked element by element.
 //
@@ -52,37 +55,51 @@ namespace {
 
 constexpr int kBM = 128;       // query rows per tile: one TMEM lane per row
 constexpr int kBN = 128;       // keys per key/value tile
-constexpr int kThreads = 512;  // 16 warps, see the role table above
+constexpr int kThreads = 384;  // 12 warps, see the role table above
+constexpr int kMmaWarp = 8;    // issues S = Q K^T (and owns the TMEM allocation)
+constexpr int kMmaPvWarp = 9;  // issues O += P V
+constexpr int kTmaWarp = 10;   // Q and K loads
+constexpr int kTmaVWarp = 11;  // V loads
 constexpr uint32_t kTmemCols = 512;
 constexpr int kHalfBytes = 128 * 128;         // one 64-column half of a 128-row bf16 tile
 constexpr uint64_t kDrainNs = 1000000000ull;  // drain waits: at least 1 s
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 struct Bars {
-    uint64_t q_full[2];
-    uint64_t k_full[2], k_empty[2];
-    uint64_t v_full[2], v_empty[2];
-    uint64_t s_full[2];       // S_t computed (tcgen05.commit)
-    uint64_t p_full[2];       // P_t written to TMEM (128 softmax threads)
-    uint64_t pv_done[2];      // O_t += P_t V finished (tcgen05.commit)
-    uint64_t alpha_ready[2];  // per-row rescale factors published (128 softmax threads)
-    uint64_t o_ready[2];      // O_t rescaled, ready for the next P V (128 correction threads)
+    uint64_t q_full;        // Q tile landed in shared memory (TMA)
+    uint64_t q_tmem;        // Q copied into TMEM (4 warps)
+    uint64_t k_full[4], k_empty[4];
+    uint64_t v_full[4], v_empty[4];
+    uint64_t s_full[2];     // S buffer computed (tcgen05.commit)
+    uint64_t s_free[2];     // S buffer read into registers (8 warps)
+    uint64_t p_full;        // P stored to TMEM and O rescaled if needed (8 warps)
+    uint64_t pv_done;       // O += P V finished (tcgen05.commit)
     uint64_t mma_done;
+    uint64_t mma_pv_done;
+    uint64_t red_full[2];   // both halves' maxima published for an iteration parity (8 warps)
+    uint64_t sum_full;      // both halves' sums published (8 warps)
     uint32_t tmem_base;
-    float alpha[2][kBM];
+    float red[2][2][kBM];   // [iteration parity][half][row]: half-row maxima, then sums
 };
 
 template <int D>
-struct Layout {
+struct Cfg {
     static constexpr int kHalves = D / 64;
     static constexpr int kTileBytes = kHalves * kHalfBytes;  // 128 rows x D bf16
-    static constexpr int kQ = 0;                             // 2 tiles
-    static constexpr int kK = kQ + 2 * kTileBytes;           // 2 stages
-    static constexpr int kV = kK + 2 * kTileBytes;           // 2 stages
-    static constexpr int kBars = kV + 2 * kTileBytes;
+    static constexpr int kStages = D == 128 ? 3 : 4;         // K ring and V ring depth
+    static constexpr int kK = 0;
+    static constexpr int kV = kK + kStages * kTileBytes;
+    // Q is staged in the last V slot: it is copied into TMEM before V of that slot is loaded.
+    static constexpr int kQ = kV + (kStages - 1) * kTileBytes;
+    static constexpr int kBars = kV + kStages * kTileBytes;
     static constexpr int kBytes = kBars + static_cast<int>(sizeof(Bars));
     static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
-    static constexpr uint32_t kTmemO = 256;         // O_0 at 256, O_1 at 256 + D
+    static constexpr uint32_t kTmemS = 0;           // S_a, S_b
+    static constexpr uint32_t kTmemO = 256;
+    static constexpr uint32_t kTmemP = 256 + D;
+    static constexpr uint32_t kTmemQ = 256 + D + 64;
+    static_assert(kTmemQ + D / 2 <= kTmemCols, "TMEM budget");
+    static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
 };
 
 // All 32 lanes wait on the same phase; the outcome is made warp-uniform so that the
@@ -90,6 +107,13 @@ struct Layout {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
     const bool ok = mbar_wait(bar, parity, timeout_ns);
     return __all_sync(0xffffffffu, ok);
+}
+
+// One arrival per warp, after every lane's prior tcgen05 accesses are ordered before it.
+__device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 __device__ __forceinline__ void record_timeout(int where) {
@@ -100,58 +124,55 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                  float* __restrict__ LSE, int N, int BH, int n_pairs, float scale_log2,
+                  float* __restrict__ LSE, int N, int BH, int n_qtiles, float scale_log2,
                   unsigned long long timeout_ns) {
-    using L = Layout<D>;
+    using C = Cfg<D>;
+    constexpr int S_ = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
-    const uint32_t sQ = smem_u32(smem + L::kQ);
-    const uint32_t sK = smem_u32(smem + L::kK);
-    const uint32_t sV = smem_u32(smem + L::kV);
+    Bars* bars = reinterpret_cast<Bars*>(smem + C::kBars);
+    const uint32_t sK = smem_u32(smem + C::kK);
+    const uint32_t sV = smem_u32(smem + C::kV);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work item: a pair of query tiles.  Causal runs the longest rows first.
-    int pair, bh;
+    // Work item: causal runs the longest rows (highest query tiles) first.
+    int q_tile, bh;
     if (CAUSAL) {
-        pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
+        q_tile = n_qtiles - 1 - static_cast<int>(blockIdx.x) / BH;
         bh = static_cast<int>(blockIdx.x) % BH;
     } else {
-        pair = static_cast<int>(blockIdx.x) % n_pairs;
-        bh = static_cast<int>(blockIdx.x) / n_pairs;
+        q_tile = static_cast<int>(blockIdx.x) % n_qtiles;
+        bh = static_cast<int>(blockIdx.x) / n_qtiles;
     }
     const int n_kv_all = (N + kBN - 1) / kBN;
-    int n_kv[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int qt = 2 * pair + t;
-        if (qt * kBM >= N)
-            n_kv[t] = 0;  // a tile entirely past N: nothing to compute or store
-        else
-            n_kv[t] = CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all;
-    }
-    const int J = max(n_kv[0], n_kv[1]);
+    const int n_kv = CAUSAL ? min(n_kv_all, q_tile + 1) : n_kv_all;
 
     if (threadIdx.x == 0) {
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(&bars->q_full[t], 1);
-            mbar_init(&bars->k_full[t], 1);
-            mbar_init(&bars->k_empty[t], 1);
-            mbar_init(&bars->v_full[t], 1);
-            mbar_init(&bars->v_empty[t], 1);
-            mbar_init(&bars->s_full[t], 1);
-            mbar_init(&bars->p_full[t], 128);
-            mbar_init(&bars->pv_done[t], 1);
-            mbar_init(&bars->alpha_ready[t], 128);
-            mbar_init(&bars->o_ready[t], 128);
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_tmem, 4);
+        for (int s = 0; s < S_; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->s_full[b], 1);
+            mbar_init(&bars->s_free[b], 8);
+        }
+        mbar_init(&bars->p_full, 8);
+        mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->mma_done, 1);
+        mbar_init(&bars->mma_pv_done, 1);
+        mbar_init(&bars->red_full[0], 8);
+        mbar_init(&bars->red_full[1], 8);
+        mbar_init(&bars->sum_full, 8);
         fence_mbar_init();
     }
-    if (warp == 12) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -160,253 +181,273 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp >= 12) {
-        setmaxnreg_dec<56>();
-        if (warp == 13 && lane == 0) {
-            // ---------------------------------------------------------------- TMA producer
+    if (warp == kTmaWarp) {
+        // -------------------------------------------------------------------- TMA producer
+        if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            constexpr uint32_t kTx = L::kTileBytes;
-            for (int t = 0; t < 2; ++t) {
-                mbar_arrive_expect_tx(&bars->q_full[t], kTx);
-                for (int h = 0; h < L::kHalves; ++h)
-                    tma_load_3d(smem + L::kQ + t * L::kTileBytes + h * kHalfBytes, &tmQ,
-                                &bars->q_full[t], h * 64, (2 * pair + t) * kBM, bh);
-            }
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < J; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = ((j >> 1) - 1) & 1;
-                if (j >= 2 && !mbar_wait(&bars->k_empty[s], ph, timeout_ns)) {
+            constexpr uint32_t kTx = C::kTileBytes;
+            mbar_arrive_expect_tx(&bars->q_full, kTx);
+            for (int h = 0; h < C::kHalves; ++h)
+                tma_load_3d(smem + C::kQ + h * kHalfBytes, &tmQ, &bars->q_full, h * 64,
+                            q_tile * kBM, bh);
+            int k_issued = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % S_;
+                if (j >= S_ && !mbar_wait(&bars->k_empty[s], ((j / S_) - 1) & 1, timeout_ns)) {
                     record_timeout(1);
                     break;
                 }
                 mbar_arrive_expect_tx(&bars->k_full[s], kTx);
-                for (int h = 0; h < L::kHalves; ++h)
-                    tma_load_3d(smem + L::kK + s * L::kTileBytes + h * kHalfBytes, &tmK,
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, &tmK,
                                 &bars->k_full[s], h * 64, j * kBN, bh);
                 k_issued = j + 1;
-                if (j >= 2 && !mbar_wait(&bars->v_empty[s], ph, timeout_ns)) {
-                    record_timeout(2);
-                    break;
-                }
-                mbar_arrive_expect_tx(&bars->v_full[s], kTx);
-                for (int h = 0; h < L::kHalves; ++h)
-                    tma_load_3d(smem + L::kV + s * L::kTileBytes + h * kHalfBytes, &tmV,
-                                &bars->v_full[s], h * 64, j * kBN, bh);
-                v_issued = j + 1;
             }
             // Drain: every load this thread issued has landed before the CTA may exit.  The
             // last load into a stage is the last phase of that stage's barrier, so it ends.
             const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
-            mbar_wait(&bars->q_full[0], 0, drain_ns);
-            mbar_wait(&bars->q_full[1], 0, drain_ns);
-            for (int s = 0; s < 2; ++s) {
-                if (s < k_issued) {
-                    const int jl = s + ((k_issued - 1 - s) >> 1) * 2;
-                    mbar_wait(&bars->k_full[s], (jl >> 1) & 1, drain_ns);
-                }
-                if (s < v_issued) {
-                    const int jl = s + ((v_issued - 1 - s) >> 1) * 2;
-                    mbar_wait(&bars->v_full[s], (jl >> 1) & 1, drain_ns);
-                }
+            mbar_wait(&bars->q_full, 0, drain_ns);
+            for (int s = 0; s < S_ && s < k_issued; ++s) {
+                const int jl = s + ((k_issued - 1 - s) / S_) * S_;
+                mbar_wait(&bars->k_full[s], (jl / S_) & 1, drain_ns);
             }
-        } else if (warp == 12 && lane == 0) {
-            // ---------------------------------------------------------------- MMA issuer
+        }
+    } else if (warp == kTmaVWarp) {
+        // -------------------------------------------------------------------- TMA, V ring
+        if (lane == 0) {
+            constexpr uint32_t kTx = C::kTileBytes;
+            int v_issued = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % S_;
+                // The last slot holds the staged Q until it has been copied into TMEM.
+                if (j == S_ - 1 && !mbar_wait(&bars->q_tmem, 0, timeout_ns)) {
+                    record_timeout(13);
+                    break;
+                }
+                if (j >= S_ && !mbar_wait(&bars->v_empty[s], ((j / S_) - 1) & 1, timeout_ns)) {
+                    record_timeout(2);
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars->v_full[s], kTx);
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
+                                &bars->v_full[s], h * 64, j * kBN, bh);
+                v_issued = j + 1;
+            }
+            const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
+            for (int s = 0; s < S_ && s < v_issued; ++s) {
+                const int jl = s + ((v_issued - 1 - s) / S_) * S_;
+                mbar_wait(&bars->v_full[s], (jl / S_) & 1, drain_ns);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------------------- MMA: S = Q K^T
+        if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0);
-            constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 1);
-            auto issue_s = [&](int t, int j) {
-                const uint32_t qb = sQ + t * L::kTileBytes;
-                const uint32_t kb = sK + (j & 1) * L::kTileBytes;
+            bool ok = mbar_wait(&bars->q_tmem, 0, timeout_ns);
+            if (!ok) record_timeout(3);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                // S(j) goes into buffer j & 1 once the softmax has read S(j - 2) from it.
+                const int s = j % S_;
+                if ((j >= 2 && !mbar_wait(&bars->s_free[j & 1], ((j - 2) >> 1) & 1, timeout_ns)) ||
+                    !mbar_wait(&bars->k_full[s], (j / S_) & 1, timeout_ns)) {
+                    record_timeout(5);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t kb = sK + s * C::kTileBytes;
+                const uint32_t d_tmem = tmem + C::kTmemS + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    umma_ss(tmem + t * 128, smem_desc_sw128(qb + off, 16, 1024),
-                            smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    umma_ts(d_tmem, tmem + C::kTmemQ + kk * 8, smem_desc_sw128(kb + off, 16, 1024),
+                            idS, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&bars->s_full[t]);
-            };
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t vb = sV + (j & 1) * L::kTileBytes;
-                const uint32_t p_tmem = tmem + t * 128 + 64;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    umma_ts(tmem + L::kTmemO + t * D, p_tmem + kk * 8,
-                            smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idO,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars->pv_done[t]);
-            };
-            bool ok = J > 0;
-            if (ok) {
-                ok = mbar_wait(&bars->q_full[0], 0, timeout_ns) &&
-                     mbar_wait(&bars->q_full[1], 0, timeout_ns) &&
-                     mbar_wait(&bars->k_full[0], 0, timeout_ns);
-                if (!ok) record_timeout(3);
+                umma_commit(&bars->s_full[j & 1]);
+                umma_commit(&bars->k_empty[s]);
             }
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < 2; ++t)
-                    if (n_kv[t] > 0) issue_s(t, 0);
-                umma_commit(&bars->k_empty[0]);
-            }
-            for (int j = 0; ok && j < J; ++j) {
-                const int s = j & 1;
-                if (!mbar_wait(&bars->v_full[s], (j >> 1) & 1, timeout_ns)) {
-                    record_timeout(4);
-                    break;
-                }
-                bool k_next = false;  // K_{j+1} seen landed
-                for (int t = 0; ok && t < 2; ++t) {
-                    if (j >= n_kv[t]) continue;
-                    if (!mbar_wait(&bars->p_full[t], j & 1, timeout_ns) ||
-                        !mbar_wait(&bars->o_ready[t], j & 1, timeout_ns)) {
-                        record_timeout(5);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_pv(t, j);
-                    if (j + 1 < n_kv[t]) {
-                        // S_t(j+1) overwrites the columns P_t(j) is read from: wait for P V.
-                        if ((!k_next && !mbar_wait(&bars->k_full[(j + 1) & 1], ((j + 1) >> 1) & 1,
-                                                   timeout_ns)) ||
-                            !mbar_wait(&bars->pv_done[t], j & 1, timeout_ns)) {
-                            record_timeout(6);
-                            ok = false;
-                            break;
-                        }
-                        k_next = true;
-                        tc_fence_after();
-                        issue_s(t, j + 1);
-                    }
-                }
-                if (!ok) break;
-                umma_commit(&bars->v_empty[s]);
-                if (j + 1 < J) umma_commit(&bars->k_empty[(j + 1) & 1]);
-            }
-            // Drain: no MMA may still write TMEM when it is freed.
+            // Drain: no MMA of this thread may still write TMEM when it is freed.
             umma_commit(&bars->mma_done);
             mbar_wait(&bars->mma_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
         }
         __syncwarp();
-    } else if (warp >= 8) {
-        // -------------------------------------------------------------------- correction
-        setmaxnreg_dec<72>();
-        const int r = threadIdx.x - 256;  // row == TMEM lane (warp % 4 selects the lane quarter)
-        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        bool ok = true;
-        for (int j = 0; ok && j < J; ++j) {
-            for (int t = 0; t < 2; ++t) {
-                if (j >= n_kv[t]) continue;
-                if (!warp_wait(&bars->alpha_ready[t], j & 1, timeout_ns)) {
-                    record_timeout(7);
-                    ok = false;
+    } else if (warp == kMmaPvWarp) {
+        // -------------------------------------------------------------------- MMA: O += P V
+        if (lane == 0) {
+            constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 1);
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % S_;
+                if (!mbar_wait(&bars->v_full[s], (j / S_) & 1, timeout_ns) ||
+                    !mbar_wait(&bars->p_full, j & 1, timeout_ns)) {
+                    record_timeout(6);
                     break;
                 }
-                if (j > 0) {
-                    if (!warp_wait(&bars->pv_done[t], (j - 1) & 1, timeout_ns)) {
-                        record_timeout(8);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const float a = bars->alpha[t][r];
-                    if (__any_sync(0xffffffffu, a != 1.f)) {
-                        const uint32_t tO = tmem + lane_addr + L::kTmemO + t * D;
+                tc_fence_after();
+                const uint32_t vb = sV + s * C::kTileBytes;
 #pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t o[32];
-                            tmem_ld32_sync(tO + c * 32, o);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-                            tmem_st32_sync(tO + c * 32, o);
-                        }
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->o_ready[t]);
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    umma_ts(tmem + C::kTmemO, tmem + C::kTmemP + kk * 8,
+                            smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idO,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars->pv_done);
+                umma_commit(&bars->v_empty[s]);
             }
+            umma_commit(&bars->mma_pv_done);
+            mbar_wait(&bars->mma_pv_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
         }
+        __syncwarp();
     } else {
         // -------------------------------------------------------------------- softmax
-        setmaxnreg_inc<192>();
-        const int t = warp >> 2;               // query tile of this warpgroup
-        const int r = threadIdx.x & 127;        // row in the tile == TMEM lane
+        const int h = warp >> 2;          // score columns [64h, 64h + 64)
+        const int r = threadIdx.x & 127;  // row in the tile == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_addr + t * 128;
-        const uint32_t tP = tS + 64;
-        const uint32_t tO = tmem + lane_addr + L::kTmemO + t * D;
-        const int q_row = (2 * pair + t) * kBM + r;
+        const int q_row = q_tile * kBM + r;
         const int key_limit = CAUSAL ? min(N - 1, q_row) : N - 1;  // last allowed key
-        const int nkv = n_kv[t];
-        float m = -INFINITY;  // reference max of scale*log2(e)*s for this row
-        float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            if (!warp_wait(&bars->s_full[t], j & 1, timeout_ns)) {
-                record_timeout(9);
+
+        if (h == 0) {
+            // Q row r: shared memory (128-byte swizzled, as TMA wrote it) -> TMEM lane r.
+            if (!warp_wait(&bars->q_full, 0, timeout_ns)) {
+                record_timeout(7);
+                ok = false;
+            } else {
+                const uint8_t* qs = smem + C::kQ;
+#pragma unroll
+                for (int hh = 0; hh < C::kHalves; ++hh) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(
+                            qs + hh * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4));
+                        w[4 * c] = v.x;
+                        w[4 * c + 1] = v.y;
+                        w[4 * c + 2] = v.z;
+                        w[4 * c + 3] = v.w;
+                    }
+                    tmem_st32_sync(tmem + lane_addr + C::kTmemQ + hh * 32, w);
+                }
+                // The staged Q slot is refilled by TMA (async proxy) after this arrival.
+                fence_proxy_async_smem();
+            }
+            warp_arrive_tc(&bars->q_tmem);
+        }
+
+        float m = -INFINITY;  // reference max of scale*log2(e)*s for this row
+        float l = 0.f;        // this half's running sum of 2^(scale*log2(e)*s - m)
+        const uint32_t tS = tmem + lane_addr + C::kTmemS + h * 64;
+        const uint32_t tP = tmem + lane_addr + C::kTmemP + h * 32;
+        const uint32_t tO = tmem + lane_addr + C::kTmemO + h * (D / 2);
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const int b = j & 1;
+            if (!warp_wait(&bars->s_full[b], (j >> 1) & 1, timeout_ns)) {
+                record_timeout(8);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sr[128];
-            tmem_ld128_sync(tS, sr);
+            uint32_t sr[64];
+            tmem_ld64_sync(tS + b * 128, sr);
+            warp_arrive_tc(&bars->s_free[b]);  // S(j) is in registers: S(j+2) may overwrite it
 
-            const int kv0 = j * kBN;
-            if (kv0 + kBN - 1 > key_limit) {
+            const int kv0 = j * kBN + h * 64;
+            if (kv0 + 63 > key_limit) {
 #pragma unroll
-                for (int e = 0; e < 128; ++e)
+                for (int e = 0; e < 64; ++e)
                     if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
             }
             float mx8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(sr[u]);
 #pragma unroll
-            for (int e = 8; e < 128; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sr[e]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                             scale_log2;
+            for (int e = 8; e < 64; e += 2)
+                mx8[(e >> 1) & 7] =
+                    fmax3(mx8[(e >> 1) & 7], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+            float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
+            // The two halves of the row agree on one maximum.
+            bars->red[b][h][r] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->red_full[b]);
+            if (!warp_wait(&bars->red_full[b], (j >> 1) & 1, timeout_ns)) {
+                record_timeout(11);
+                ok = false;
+                break;
+            }
+            mx = fmaxf(mx, bars->red[b][h ^ 1][r]) * scale_log2;
             // Move the reference only when this tile's max exceeds it by more than the
             // threshold (always on the first finite tile: m = -inf gives +inf > threshold).
             const float m_new = (mx - m > kRescaleThreshold) ? mx : m;
             const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_new);
-            bars->alpha[t][r] = alpha;
-            mbar_arrive(&bars->alpha_ready[t]);
             // Nothing allowed yet (m_new = -inf): shift by 0 so every term is exp(-inf) = 0.
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            uint32_t p[64];
+            uint32_t p[32];
+            float2 rs = make_float2(0.f, 0.f);
+            float2 rs2 = make_float2(0.f, 0.f);
+            const float2 c2 = make_float2(scale_log2, scale_log2);
+            const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
-            for (int e = 0; e < 128; e += 2) {
-                const float a = ex2_approx(fmaf(__uint_as_float(sr[e]), scale_log2, -m_use));
-                const float b = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), scale_log2, -m_use));
-                rs8[(e >> 1) & 7] += a + b;
-                p[e >> 1] = pack_bf16x2(a, b);
+            for (int e = 0; e < 64; e += 4) {
+                float2 t0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                  c2, nm2);
+                float2 t1 = ffma2(
+                    make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
+                t0.x = ex2_approx(t0.x);
+                t0.y = ex2_approx(t0.y);
+                t1.x = ex2_approx(t1.x);
+                t1.y = ex2_approx(t1.y);
+                rs = fadd2(rs, t0);
+                rs2 = fadd2(rs2, t1);
+                p[e >> 1] = pack_bf16x2(t0.x, t0.y);
+                p[(e >> 1) + 1] = pack_bf16x2(t1.x, t1.y);
             }
-            tmem_st64_sync(tP, p);
-            tc_fence_before();
-            mbar_arrive(&bars->p_full[t]);
-            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
-                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-            l = l * alpha + rs;
+            l = l * alpha + ((rs.x + rs.y) + (rs2.x + rs2.y));
             m = m_new;
-        }
-        if (ok && nkv > 0) {
-            if (!warp_wait(&bars->pv_done[t], (nkv - 1) & 1, timeout_ns)) {
-                record_timeout(10);
-                ok = false;
+            if (j > 0) {
+                // P(j-1) V must be done: P is overwritten below, and O is rescaled here.
+                if (!warp_wait(&bars->pv_done, (j - 1) & 1, timeout_ns)) {
+                    record_timeout(9);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32_sync(tO + c * 32, o);
+                    }
+                }
             }
+            tmem_st32_sync(tP, p);
+            warp_arrive_tc(&bars->p_full);
+        }
+        if (ok && !warp_wait(&bars->pv_done, (n_kv - 1) & 1, timeout_ns)) {
+            record_timeout(10);
+            ok = false;
         }
         tc_fence_after();
-        if (ok && nkv > 0) {
-            // Epilogue: O = acc / l in bf16, LSE = (m + log2 l) * ln 2.
+        // The two halves of the row add their sums.
+        bars->red[n_kv & 1][h][r] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->sum_full);
+        if (!warp_wait(&bars->sum_full, 0, timeout_ns)) {
+            record_timeout(12);
+            ok = false;
+        }
+        l += bars->red[n_kv & 1][h ^ 1][r];
+        if (ok) {
+            // Epilogue: this thread writes columns [h*D/2, (h+1)*D/2) of O row r.
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const bool store = q_row < N;
-            __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q_row) * D;
+            __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q_row) * D + h * (D / 2);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
                 tmem_ld32_sync(tO + c * 32, o);
                 uint32_t pk[16];
@@ -421,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
-            if (store && LSE != nullptr)
+            if (store && h == 0 && LSE != nullptr)
                 LSE[static_cast<size_t>(bh) * N + q_row] = (m + __log2f(l)) * 0.69314718055994531f;
         }
     }
@@ -429,27 +470,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 12) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int D, bool CAUSAL>
 int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* O,
                float* LSE, int N, int BH, float scale, cudaStream_t stream) {
-    using L = Layout<D>;
+    using C = Cfg<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
     });
     if (attr_err != cudaSuccess) return FA_ERR_CUDA;
     const int n_qtiles = (N + kBM - 1) / kBM;
-    const int n_pairs = (n_qtiles + 1) / 2;
-    const long long ctas = static_cast<long long>(n_pairs) * BH;
+    const long long ctas = static_cast<long long>(n_qtiles) * BH;
     if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     const float scale_log2 = scale * 1.4426950408889634f;
-    fa_fwd_kernel<D, CAUSAL><<<static_cast<unsigned>(ctas), kThreads, L::kDynSmem, stream>>>(
-        tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, N, BH, n_pairs, scale_log2,
+    fa_fwd_kernel<D, CAUSAL><<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(
+        tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, N, BH, n_qtiles, scale_log2,
         fa_wait_timeout_ns());
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
