@@ -20,7 +20,7 @@
 // own columns, so the tensor core never waits for P V before the next S.
 //   warps 0-3 / 4-7  softmax of score columns [0,64) / [64,128): one query row per thread (its
 //                    TMEM lane).  tcgen05.ld of 64 S values, mask, half-row max, the two halves
-//                    exchange their maxima through shared memory (one mbarrier), lazy
+//                    exchange their maxima through shared memory (one named barrier), lazy
 //                    reference max, ex2 of the scaled and shifted scores (scale*log2(e) folded
 //                    into one FFMA), half-row sum, P rounded to bf16 and stored to TMEM.  When a
 //                    row's reference max moves (rare: only beyond 2^8), the thread scales its
@@ -64,6 +64,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kHalfBytes = 128 * 128;         // one 64-column half of a 128-row bf16 tile
 constexpr uint64_t kDrainNs = 1000000000ull;  // drain waits: at least 1 s
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr uint32_t kBarSoftmax = 1;           // named barrier of the 8 softmax warps
 
 struct Bars {
     uint64_t q_full;        // Q tile landed in shared memory (TMA)
@@ -76,8 +77,6 @@ struct Bars {
     uint64_t pv_done;       // O += P V finished (tcgen05.commit)
     uint64_t mma_done;
     uint64_t mma_pv_done;
-    uint64_t red_full[2];   // both halves' maxima published for an iteration parity (8 warps)
-    uint64_t sum_full;      // both halves' sums published (8 warps)
     uint32_t tmem_base;
     float red[2][2][kBM];   // [iteration parity][half][row]: half-row maxima, then sums
 };
@@ -118,6 +117,65 @@ __device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
 
 __device__ __forceinline__ void record_timeout(int where) {
     atomicCAS(&g_fa_device_status, 0, FA_ERR_TIMEOUT | (where << 8));
+}
+
+// The rest of one softmax step of a half row, after the row maximum is known: lazy reference
+// max, exponentials and half-row sum, rescale of this half of the O row when the reference
+// moved, P stored to TMEM.  Returns false if a wait gave up.
+template <int D>
+__device__ __forceinline__ bool softmax_tail(Bars* bars, const uint32_t (&sr)[64], float mx,
+                                             float scale_log2, float& m, float& l, int j,
+                                             uint32_t tP, uint32_t tO,
+                                             unsigned long long timeout_ns) {
+    // Move the reference only when this tile's max exceeds it by more than the threshold
+    // (always on the first finite tile: m = -inf gives +inf > threshold).
+    const float m_new = (mx - m > kRescaleThreshold) ? mx : m;
+    const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_new);
+    // Nothing allowed yet (m_new = -inf): shift by 0 so every term is exp(-inf) = 0.
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    uint32_t p[32];
+    float2 rs = make_float2(0.f, 0.f);
+    float2 rs2 = make_float2(0.f, 0.f);
+    const float2 c2 = make_float2(scale_log2, scale_log2);
+    const float2 nm2 = make_float2(-m_use, -m_use);
+#pragma unroll
+    for (int e = 0; e < 64; e += 4) {
+        float2 t0 =
+            ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
+        float2 t1 =
+            ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
+        t0.x = ex2_approx(t0.x);
+        t0.y = ex2_approx(t0.y);
+        t1.x = ex2_approx(t1.x);
+        t1.y = ex2_approx(t1.y);
+        rs = fadd2(rs, t0);
+        rs2 = fadd2(rs2, t1);
+        p[e >> 1] = pack_bf16x2(t0.x, t0.y);
+        p[(e >> 1) + 1] = pack_bf16x2(t1.x, t1.y);
+    }
+    l = l * alpha + ((rs.x + rs.y) + (rs2.x + rs2.y));
+    m = m_new;
+    if (j > 0) {
+        // P(j-1) V must be done: P is overwritten below, and O is rescaled here.
+        if (!warp_wait(&bars->pv_done, (j - 1) & 1, timeout_ns)) {
+            record_timeout(9);
+            return false;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t o[32];
+                tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tmem_st32_sync(tO + c * 32, o);
+            }
+        }
+    }
+    tmem_st32_sync(tP, p);
+    warp_arrive_tc(&bars->p_full);
+    return true;
 }
 
 template <int D, bool CAUSAL>
@@ -167,9 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->mma_done, 1);
         mbar_init(&bars->mma_pv_done, 1);
-        mbar_init(&bars->red_full[0], 8);
-        mbar_init(&bars->red_full[1], 8);
-        mbar_init(&bars->sum_full, 8);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -339,6 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_addr + C::kTmemS + h * 64;
         const uint32_t tP = tmem + lane_addr + C::kTmemP + h * 32;
         const uint32_t tO = tmem + lane_addr + C::kTmemO + h * (D / 2);
+        // Every softmax thread passes the named barrier exactly n_kv times in the loop (plus once
+        // after it): a thread that left the loop early because a wait gave up makes up the
+        // missing passes below, so the barrier can never hang.
+        int bar_passes = 0;
         for (int j = 0; ok && j < n_kv; ++j) {
             const int b = j & 1;
             if (!warp_wait(&bars->s_full[b], (j >> 1) & 1, timeout_ns)) {
@@ -350,7 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sr[64];
             tmem_ld64_sync(tS + b * 128, sr);
             warp_arrive_tc(&bars->s_free[b]);  // S(j) is in registers: S(j+2) may overwrite it
-
             const int kv0 = j * kBN + h * 64;
             if (kv0 + 63 > key_limit) {
 #pragma unroll
@@ -366,80 +424,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fmax3(mx8[(e >> 1) & 7], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
             float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                              fmaxf(mx8[6], mx8[7]));
-            // The two halves of the row agree on one maximum.
+            // The two halves of the row agree on one maximum (shared memory + named barrier).
             bars->red[b][h][r] = mx;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->red_full[b]);
-            if (!warp_wait(&bars->red_full[b], (j >> 1) & 1, timeout_ns)) {
-                record_timeout(11);
-                ok = false;
-                break;
-            }
+            named_bar_sync(kBarSoftmax, 256);
+            ++bar_passes;
             mx = fmaxf(mx, bars->red[b][h ^ 1][r]) * scale_log2;
-            // Move the reference only when this tile's max exceeds it by more than the
-            // threshold (always on the first finite tile: m = -inf gives +inf > threshold).
-            const float m_new = (mx - m > kRescaleThreshold) ? mx : m;
-            const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_new);
-            // Nothing allowed yet (m_new = -inf): shift by 0 so every term is exp(-inf) = 0.
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            uint32_t p[32];
-            float2 rs = make_float2(0.f, 0.f);
-            float2 rs2 = make_float2(0.f, 0.f);
-            const float2 c2 = make_float2(scale_log2, scale_log2);
-            const float2 nm2 = make_float2(-m_use, -m_use);
-#pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                float2 t0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                  c2, nm2);
-                float2 t1 = ffma2(
-                    make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
-                t0.x = ex2_approx(t0.x);
-                t0.y = ex2_approx(t0.y);
-                t1.x = ex2_approx(t1.x);
-                t1.y = ex2_approx(t1.y);
-                rs = fadd2(rs, t0);
-                rs2 = fadd2(rs2, t1);
-                p[e >> 1] = pack_bf16x2(t0.x, t0.y);
-                p[(e >> 1) + 1] = pack_bf16x2(t1.x, t1.y);
-            }
-            l = l * alpha + ((rs.x + rs.y) + (rs2.x + rs2.y));
-            m = m_new;
-            if (j > 0) {
-                // P(j-1) V must be done: P is overwritten below, and O is rescaled here.
-                if (!warp_wait(&bars->pv_done, (j - 1) & 1, timeout_ns)) {
-                    record_timeout(9);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32_sync(tO + c * 32, o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32_sync(tO + c * 32, o);
-                    }
-                }
-            }
-            tmem_st32_sync(tP, p);
-            warp_arrive_tc(&bars->p_full);
+            ok = softmax_tail<D>(bars, sr, mx, scale_log2, m, l, j, tP, tO, timeout_ns);
         }
+        for (; bar_passes < n_kv; ++bar_passes) named_bar_sync(kBarSoftmax, 256);
         if (ok && !warp_wait(&bars->pv_done, (n_kv - 1) & 1, timeout_ns)) {
             record_timeout(10);
             ok = false;
         }
         tc_fence_after();
-        // The two halves of the row add their sums.
+        // The two halves of the row add their sums (every softmax thread reaches this barrier).
         bars->red[n_kv & 1][h][r] = l;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->sum_full);
-        if (!warp_wait(&bars->sum_full, 0, timeout_ns)) {
-            record_timeout(12);
-            ok = false;
-        }
+        named_bar_sync(kBarSoftmax, 256);
         l += bars->red[n_kv & 1][h ^ 1][r];
         if (ok) {
             // Epilogue: this thread writes columns [h*D/2, (h+1)*D/2) of O row r.
