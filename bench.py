@@ -273,9 +273,13 @@ def roofline_hbm(nbytes, ms, peaks, kind, traffic=None):
             "peak_kind": f"copy bandwidth, {kind}"}
 
 
-# Traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
-# summaries; None until a capture of the current kernel exists.
-NCU_TRAFFIC_BYTES = {}
+# Traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
+# summarised under profiles/ (same kernel version).  Workloads without a capture report None.
+NCU_TRAFFIC_BYTES = {
+    "dense_b2h32n8192": 402.693888e6 + 118.795776e6,
+    "mha_b4h16n2048d64": 50.372352e6 + 0.767232e6,
+    "softmax_65536x4000": 1.0487e9 + 0.998584576e9,
+}
 
 
 # ---------------------------------------------------------------------------------------------
