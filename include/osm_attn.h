@@ -86,6 +86,17 @@ const char* fa_status_string(int status);
  */
 int osm_attn_device_status(void* stream, int* status);
 
+/*
+ * osm_attn_selftest_wait -- diagnostic for the bounded-wait error path (the pages have no
+ * counterpart).  Launches one warp that waits, with the same bounded mbarrier wait the
+ * attention kernel uses, on a barrier that nothing ever completes; after `timeout_us`
+ * microseconds (1 .. 10 000 000) the wait gives up and records FA_ERR_TIMEOUT in the device
+ * status word, which osm_attn_device_status then returns (and clears).  No GPU fault is
+ * involved: the kernel exits normally and the context stays usable.  Returns FA_OK when the
+ * launch succeeded, FA_ERR_INVALID_ARG for a timeout out of range, FA_ERR_CUDA otherwise.
+ */
+int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
+
 /* ABI version of this header (incremented on any incompatible change). */
 int osm_attn_abi_version(void);
 

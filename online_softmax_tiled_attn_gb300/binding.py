@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
             L.fa_status_string.restype = ctypes.c_char_p
             L.osm_attn_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
             L.osm_attn_device_status.restype = ctypes.c_int
+            L.osm_attn_selftest_wait.argtypes = [i64, vp]
+            L.osm_attn_selftest_wait.restype = ctypes.c_int
             L.osm_attn_abi_version.argtypes = []
             L.osm_attn_abi_version.restype = ctypes.c_int
             _lib = L
@@ -78,6 +80,14 @@ def fa_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, s
 
 def osm_softmax_raw(x_ptr, y_ptr, rows, cols, lse_ptr, stream_ptr):
     return lib().osm_softmax(x_ptr, y_ptr, int(rows), int(cols), lse_ptr, stream_ptr)
+
+
+def selftest_wait(timeout_us: int, stream=None) -> None:
+    """Launch the bounded-wait diagnostic (a wait that nothing completes gives up after
+    timeout_us and records FA_ERR_TIMEOUT for device_status to report)."""
+    rc = lib().osm_attn_selftest_wait(int(timeout_us), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "osm_attn_selftest_wait")
 
 
 def device_status(stream=None) -> int:

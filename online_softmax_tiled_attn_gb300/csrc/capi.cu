@@ -92,6 +92,10 @@ int osm_attn_device_status(void* stream, int* status) {
     return FA_OK;
 }
 
+int osm_attn_selftest_wait(int64_t timeout_us, void* stream) {
+    return osm::selftest_wait_launch(timeout_us, static_cast<cudaStream_t>(stream));
+}
+
 int osm_attn_abi_version(void) { return OSM_ATTN_ABI_VERSION; }
 
 }  // extern "C"

@@ -514,6 +514,27 @@ int fa_fwd_launch(const void* Q, const void* K, const void* V, void* O, float* L
     return FA_ERR_UNSUPPORTED;
 }
 
+namespace {
+// Waits on an mbarrier that nothing ever completes, with the same bounded wait the attention
+// kernel uses, and records the timeout in the device status word.  Exercises the error path
+// without touching TMA, TMEM or the tensor cores.
+__global__ void __launch_bounds__(32, 1) selftest_wait_kernel(unsigned long long timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (!warp_wait(&bar, 0, timeout_ns) && threadIdx.x == 0) record_timeout(15);
+}
+}  // namespace
+
+int selftest_wait_launch(long long timeout_us, cudaStream_t stream) {
+    if (timeout_us < 1 || timeout_us > 10000000) return FA_ERR_INVALID_ARG;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_us) * 1000ull);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_read_device_status(cudaStream_t stream, int* status) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
     int v = 0;

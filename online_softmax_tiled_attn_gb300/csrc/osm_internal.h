@@ -20,6 +20,7 @@ unsigned long long fa_wait_timeout_ns();
 int fa_fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t BH,
                   int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream);
 int fa_read_device_status(cudaStream_t stream, int* status);
+int selftest_wait_launch(long long timeout_us, cudaStream_t stream);
 
 int osm_softmax_launch(const float* x, float* y, int64_t rows, int64_t cols, float* lse,
                        cudaStream_t stream);

@@ -11,6 +11,8 @@ Functions (each a thin ctypes wrapper around ``oracle.c``; the arithmetic lives 
   "The fix: subtract the maximum" and "The cost: three passes".
 * :func:`attention` -- exact attention O = softmax(scale*Q K^T [causal]) V and LSE = m + ln l,
   three passes per query row.  Same lesson, section "From softmax to attention".
+* :func:`attention_qk` -- the same with Nq queries against Nk keys (the queries are the last Nq
+  positions when causal), for the split-key path.
 * :func:`online_state` -- the pages' block-by-block streaming state (m, l, acc) of one score row
   with an optional trace.  Same lesson, sections "The idea", "From softmax to attention" and
   "A worked example by hand" (Tables 1 and 2); "kbwen.com FlashAttention" page, sections "Two
@@ -56,6 +58,11 @@ class Oracle:
                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
                                     _i64p, ctypes.c_int64, _dp, _dp, ctypes.c_int]
         lib.oracle_attn.restype = ctypes.c_int
+        lib.oracle_attn2.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_double, ctypes.c_int, _i64p, ctypes.c_int64, _dp,
+                                     _dp, ctypes.c_int]
+        lib.oracle_attn2.restype = ctypes.c_int
         lib.oracle_online_state.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                             _dp]
@@ -106,6 +113,34 @@ class Oracle:
                                    _ptr(O, _dp), _ptr(L, _dp), nthreads)
         if rc != 0:
             raise ValueError("oracle_attn rejected its arguments")
+        return O, L
+
+    def attention_qk(self, Q, K, V, scale: float, causal: bool, rows=None, nthreads: int = 0):
+        """Nq queries against Nk keys: Q [B, H, Nq, d], K and V [B, H, Nk, d] (bf16 bits).
+
+        Causal: query i attends to keys j <= i + (Nk - Nq) (the queries are the last Nq of the
+        Nk positions).  rows: optional flat indices (b*H + h)*Nq + i.
+        """
+        Q, K, V = (_as_bf16_bits(t) for t in (Q, K, V))
+        if Q.ndim != 4 or K.shape != V.shape or K.ndim != 4 or Q.shape[:2] != K.shape[:2] \
+                or Q.shape[3] != K.shape[3]:
+            raise ValueError("Q [B,H,Nq,d] and K, V [B,H,Nk,d] disagree")
+        B, H, Nq, d = Q.shape
+        Nk = K.shape[2]
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            O = np.empty((rows.size, d), dtype=np.float64)
+            L = np.empty(rows.size, dtype=np.float64)
+            nrows = rows.size
+        else:
+            O = np.empty((B, H, Nq, d), dtype=np.float64)
+            L = np.empty((B, H, Nq), dtype=np.float64)
+            nrows = 0
+        rc = self._lib.oracle_attn2(_ptr(Q, _u16p), _ptr(K, _u16p), _ptr(V, _u16p), B, H, Nq,
+                                    Nk, d, float(scale), int(bool(causal)), _ptr(rows, _i64p),
+                                    nrows, _ptr(O, _dp), _ptr(L, _dp), nthreads)
+        if rc != 0:
+            raise ValueError("oracle_attn2 rejected its arguments")
         return O, L
 
     # -- streaming state ---------------------------------------------------------------------
@@ -190,6 +225,10 @@ def softmax_rows(x, nthreads: int = 0):
 
 def attention(Q, K, V, scale, causal, rows=None, nthreads: int = 0):
     return load().attention(Q, K, V, scale, causal, rows, nthreads)
+
+
+def attention_qk(Q, K, V, scale, causal, rows=None, nthreads: int = 0):
+    return load().attention_qk(Q, K, V, scale, causal, rows, nthreads)
 
 
 def online_state(s, v, block, trace=False):

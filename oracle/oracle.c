@@ -152,7 +152,7 @@ int oracle_softmax_rows(const float* x, int64_t rows, int64_t cols, double* y, d
 
 typedef struct {
     const uint16_t *Q, *K, *V;
-    int64_t H, N, d;
+    int64_t H, N, Nk, d; /* N = queries per head, Nk = keys per head */
     double scale;
     int causal;
     const int64_t* rows; /* NULL: rows [r0, r1) of the flat (b*H+h)*N+i index */
@@ -161,26 +161,29 @@ typedef struct {
     int err;
 } attn_job;
 
-/* One query row.  `flat` = (b*H + h)*N + i.  s and q are scratch of N and d doubles. */
+/* One query row.  `flat` = (b*H + h)*N + i.  s and q are scratch of Nk and d doubles. */
 static void attn_one_row(const attn_job* jb, int64_t flat, double* o, double* lse_out,
                          double* s, double* q) {
-    const int64_t N = jb->N, d = jb->d;
+    const int64_t N = jb->N, Nk = jb->Nk, d = jb->d;
     const int64_t bh = flat / N;
     const int64_t i = flat % N;
     const uint16_t* Qh = jb->Q + bh * N * d;
-    const uint16_t* Kh = jb->K + bh * N * d;
-    const uint16_t* Vh = jb->V + bh * N * d;
+    const uint16_t* Kh = jb->K + bh * Nk * d;
+    const uint16_t* Vh = jb->V + bh * Nk * d;
 
     for (int64_t k = 0; k < d; ++k) q[k] = bf16_to_double(Qh[i * d + k]);
 
-    /* number of allowed keys */
-    int64_t nk = N;
+    /* number of allowed keys: all Nk, or, causal, the keys up to the query's own position when
+       the N queries are the last N of the Nk positions (query i sits at position i + Nk - N) */
+    int64_t nk = Nk;
     if (jb->causal) {
 #if ORACLE_MUTANT == 2
-        nk = i;     /* mutant: strict causal mask (j < i) */
+        nk = i + (Nk - N);     /* mutant: strict causal mask (j < position) */
 #else
-        nk = i + 1; /* key j <= query i */
+        nk = i + (Nk - N) + 1; /* key j <= position of query i */
 #endif
+        if (nk < 0) nk = 0;
+        if (nk > Nk) nk = Nk;
     }
 #if ORACLE_MUTANT == 3
     if (nk > 1) nk -= 1; /* mutant: drops the last allowed key */
@@ -192,8 +195,8 @@ static void attn_one_row(const attn_job* jb, int64_t flat, double* o, double* ls
         double acc = 0.0;
         for (int64_t k = 0; k < d; ++k) {
 #if ORACLE_MUTANT == 4
-            /* mutant: reads K transposed (column j of a d x N view) */
-            double kv = bf16_to_double(Kh[(k * N + j) % (N * d)]);
+            /* mutant: reads K transposed (column j of a d x Nk view) */
+            double kv = bf16_to_double(Kh[(k * Nk + j) % (Nk * d)]);
 #else
             double kv = bf16_to_double(Kh[j * d + k]);
 #endif
@@ -235,7 +238,7 @@ static void attn_one_row(const attn_job* jb, int64_t flat, double* o, double* ls
 
 static void* attn_worker(void* arg) {
     attn_job* jb = (attn_job*)arg;
-    double* s = (double*)malloc(sizeof(double) * (size_t)(jb->N > 0 ? jb->N : 1));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(jb->Nk > 0 ? jb->Nk : 1));
     double* q = (double*)malloc(sizeof(double) * (size_t)(jb->d > 0 ? jb->d : 1));
     if (!s || !q) { jb->err = 1; free(s); free(q); return NULL; }
     for (int64_t r = jb->r0; r < jb->r1; ++r) {
@@ -247,20 +250,22 @@ static void* attn_worker(void* arg) {
 }
 
 /*
- * Q, K, V: bf16 bit patterns, [B, H, N, d] contiguous.
- * rows == NULL: compute all B*H*N rows; O is [B*H*N, d] and LSE [B*H*N].
- * rows != NULL: compute the nrows listed flat row indices (b*H + h)*N + i; O is [nrows, d].
+ * Q: bf16 bit patterns [B, H, Nq, d]; K, V: [B, H, Nk, d]; all contiguous.
+ * Query i of a head attends to keys j < Nk, or, when causal, to keys j <= i + (Nk - Nq) (the
+ * Nq queries are the last Nq of the Nk positions; Nq == Nk is the usual square mask).
+ * rows == NULL: compute all B*H*Nq rows; O is [B*H*Nq, d] and LSE [B*H*Nq].
+ * rows != NULL: compute the nrows listed flat row indices (b*H + h)*Nq + i; O is [nrows, d].
  * Returns 0, or -1 on bad arguments (including a listed row out of range).
  */
-int oracle_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
-                int64_t N, int64_t d, double scale, int causal, const int64_t* rows,
-                int64_t nrows, double* O, double* LSE, int nthreads) {
-    if (B < 0 || H < 0 || N < 0 || d < 1) return -1;
-    const int64_t total = B * H * N;
+int oracle_attn2(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
+                 int64_t Nq, int64_t Nk, int64_t d, double scale, int causal, const int64_t* rows,
+                 int64_t nrows, double* O, double* LSE, int nthreads) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 1) return -1;
+    const int64_t total = B * H * Nq;
     const int64_t n = rows ? nrows : total;
     if (n < 0) return -1;
     if (n == 0) return 0;
-    if (!Q || !K || !V || !O || !LSE) return -1;
+    if (!Q || !O || !LSE || (Nk > 0 && (!K || !V))) return -1;
     if (rows)
         for (int64_t r = 0; r < nrows; ++r)
             if (rows[r] < 0 || rows[r] >= total) return -1;
@@ -271,7 +276,7 @@ int oracle_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t
     if (!th || !jobs) { free(th); free(jobs); return -1; }
     for (int t = 0; t < nt; ++t) {
         attn_job* jb = &jobs[t];
-        jb->Q = Q; jb->K = K; jb->V = V; jb->H = H; jb->N = N; jb->d = d;
+        jb->Q = Q; jb->K = K; jb->V = V; jb->H = H; jb->N = Nq; jb->Nk = Nk; jb->d = d;
         jb->scale = scale; jb->causal = causal; jb->rows = rows; jb->O = O; jb->LSE = LSE;
         jb->r0 = n * t / nt;
         jb->r1 = n * (t + 1) / nt;
@@ -283,6 +288,13 @@ int oracle_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t
     for (int t = 0; t < nt; ++t) err |= jobs[t].err;
     free(th); free(jobs);
     return err ? -1 : 0;
+}
+
+/* Square attention: queries and keys are the same N positions. */
+int oracle_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
+                int64_t N, int64_t d, double scale, int causal, const int64_t* rows,
+                int64_t nrows, double* O, double* LSE, int nthreads) {
+    return oracle_attn2(Q, K, V, B, H, N, N, d, scale, causal, rows, nrows, O, LSE, nthreads);
 }
 
 /* ------------------------------------------------------------------------------------------ */

@@ -12,7 +12,8 @@ getcontext().prec = 40
 
 
 def attention_decimal(q, K, V, scale, causal):
-    """q, K, V: nested lists of Python floats (exact bf16 values), [B][H][N][d].
+    """q, K, V: nested lists of Python floats (exact bf16 values), q [B][H][Nq][d] and
+    K, V [B][H][Nk][d].  Causal: query i sees keys j <= i + Nk - Nq.
 
     Returns (O, LSE) as nested lists of floats.
     """
@@ -23,10 +24,11 @@ def attention_decimal(q, K, V, scale, causal):
         for h in range(len(q[b])):
             Qh, Kh, Vh = q[b][h], K[b][h], V[b][h]
             N = len(Qh)
+            Nk = len(Kh)
             d = len(Qh[0])
             Oh, Lh = [], []
             for i in range(N):
-                keys = range(i + 1) if causal else range(N)
+                keys = range(min(Nk, i + Nk - N + 1)) if causal else range(Nk)
                 e = []
                 for j in keys:
                     s = sum(Decimal(Qh[i][k]) * Decimal(Kh[j][k]) for k in range(d)) * sc

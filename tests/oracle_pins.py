@@ -214,6 +214,51 @@ def pin_attention_decimal_bruteforce(orc):
         assert np.abs(L - np.array(Ld)).max() < 1e-13, (B, H, N, d, causal)
 
 
+def pin_attention_qk_decimal_bruteforce(orc):
+    """Nq queries against Nk keys (the split-key path's definition), causal and not."""
+    cases = [(1, 2, 1, 9, 4, 0.45, True), (1, 1, 3, 8, 3, 0.8, True), (2, 1, 4, 7, 2, 1.1, False),
+             (1, 1, 5, 5, 3, 0.6, True)]
+    for seed, (B, H, Nq, Nk, d, scale, causal) in enumerate(cases):
+        q, _, _ = inputs.attn_inputs(B, H, Nq, d, seed=91 + seed, qk_std=1.5)
+        _, k, v = inputs.attn_inputs(B, H, Nk, d, seed=191 + seed, qk_std=1.5)
+        O, L = orc.attention_qk(q, k, v, scale, causal)
+        Od, Ld = highprec.attention_decimal(_bf16_float(q).tolist(), _bf16_float(k).tolist(),
+                                            _bf16_float(v).tolist(), scale, causal)
+        assert np.abs(O - np.array(Od)).max() < 1e-13, (B, H, Nq, Nk, causal)
+        assert np.abs(L - np.array(Ld)).max() < 1e-13, (B, H, Nq, Nk, causal)
+
+
+def pin_attention_qk_square_is_attention(orc):
+    q, k, v = inputs.attn_inputs(1, 2, 17, 8, seed=23)
+    for causal in (False, True):
+        O, L = orc.attention(q, k, v, 0.3, causal)
+        O2, L2 = orc.attention_qk(q, k, v, 0.3, causal)
+        assert np.array_equal(O, O2) and np.array_equal(L, L2)
+
+
+def pin_split_keys_merge_to_full(orc):
+    """Attention over disjoint key ranges, merged by the two-worker merge, equals attention over
+    all keys (the Flash-Decoding combination).  A range state (O_s, LSE_s) is the state
+    (m = LSE_s, l = 1, acc = O_s): same acc / l and same m + ln l."""
+    B, H, Nq, Nk, d = 1, 1, 3, 50, 4
+    q, _, _ = inputs.attn_inputs(B, H, Nq, d, seed=31)
+    _, k, v = inputs.attn_inputs(B, H, Nk, d, seed=32)
+    O, L = orc.attention_qk(q, k, v, 0.5, False)
+    for cuts in ((0, 17, 50), (0, 1, 2, 49, 50), (0, 25, 25, 50)):
+        for i in range(Nq):
+            st = dict(m=-math.inf, l=0.0, acc=np.zeros(d))
+            for a, b in zip(cuts[:-1], cuts[1:]):
+                if a == b:
+                    part = dict(m=-math.inf, l=0.0, acc=np.zeros(d))  # an empty range
+                else:
+                    Os, Ls = orc.attention_qk(q[:, :, i:i + 1], k[:, :, a:b], v[:, :, a:b], 0.5,
+                                              False)
+                    part = dict(m=float(Ls[0, 0, 0]), l=1.0, acc=Os[0, 0, 0])
+                st = orc.merge(st, part)
+            assert np.abs(st["acc"] / st["l"] - O[0, 0, i]).max() < 1e-13
+            assert abs(st["m"] + math.log(st["l"]) - L[0, 0, i]) < 1e-12
+
+
 # ----------------------------------------------------------------------------------------------
 # closed forms
 # ----------------------------------------------------------------------------------------------
@@ -235,6 +280,19 @@ def pin_closed_form_uniform_scores(orc):
                 s = 0.3 * float(qf[0, h, i] @ kf[0, h, 0])
                 assert np.abs(O[0, h, i] - want).max() < 1e-14
                 assert abs(L[0, h, i] - (s + math.log(n_allowed))) < 1e-13
+
+
+def pin_closed_form_last_query_sees_all_keys(orc):
+    """With the queries at the end of the key positions, the last query is not masked at all:
+    causal and non-causal agree for it, and a single causal query equals full attention."""
+    q, _, _ = inputs.attn_inputs(1, 2, 3, 8, seed=41)
+    _, k, v = inputs.attn_inputs(1, 2, 12, 8, seed=42)
+    Oc, Lc = orc.attention_qk(q, k, v, 0.4, True)
+    On, Ln = orc.attention_qk(q, k, v, 0.4, False)
+    assert np.array_equal(Oc[:, :, -1], On[:, :, -1]) and np.array_equal(Lc[:, :, -1], Ln[:, :, -1])
+    # query 0 of 3 sits at position 9: it sees keys 0..9, i.e. not the last two
+    O9, L9 = orc.attention_qk(q[:, :, :1], k[:, :, :10], v[:, :, :10], 0.4, False)
+    assert np.abs(Oc[:, :, 0] - O9[:, :, 0]).max() < 1e-15
 
 
 def pin_closed_form_first_causal_row(orc):

@@ -105,3 +105,9 @@ def test_fa_fwd_accepts_lse_just_below_an_input():
     n = B * H * N * d * 2
     rc = binding.fa_fwd_raw(q, q + n, q + 2 * n, q + 3 * n, lse, B, H, N, d, 0.125, 0, None)
     assert rc == binding.FA_ERR_CUDA
+
+
+def test_selftest_rejects_out_of_range_timeout_on_host():
+    L = binding.lib()
+    assert L.osm_attn_selftest_wait(0, None) == binding.FA_ERR_INVALID_ARG
+    assert L.osm_attn_selftest_wait(10_000_001, None) == binding.FA_ERR_INVALID_ARG

@@ -158,3 +158,16 @@ def test_empty_and_invalid_on_device():
         binding.fa_fwd(x, x, x, out=x)
     with pytest.raises(binding.FaError):
         binding.fa_fwd(x, x, x, scale=0.0)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait on a barrier that nothing completes gives up after its limit, the device status
+    word reports FA_ERR_TIMEOUT (read and cleared), and the next attention call is correct."""
+    assert binding.device_status() == 0
+    binding.selftest_wait(2000)
+    assert binding.device_status() == binding.FA_ERR_TIMEOUT
+    assert binding.device_status() == 0  # cleared by the read
+    q, k, v = inputs.attn_inputs(1, 1, 200, 64, seed=11)
+    O, L = run_gpu(q, k, v, 0.125, False)
+    Oref, Lref = oracle.attention(q, k, v, 0.125, False)
+    parity.check_attention(O, L, Oref, Lref, "after timeout")
