@@ -256,6 +256,43 @@ def time_softmax(sw, steps, warmup, device, flush):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def time_splitkv(w, steps, warmup, device, flush):
+    """Per-launch device time (ms) of fa_fwd_splitkv (attention kernel + combine) on a decode
+    workload, workspace allocated once outside the timed region."""
+    import torch
+
+    from online_softmax_tiled_attn_gb300 import binding, inputs
+
+    q, k, v = inputs.decode_inputs(w)
+    qd, kd, vd = q.to(device), k.to(device), v.to(device)
+    del q, k, v
+    splits, wo, wl = binding.splitkv_plan(w.B, w.H, w.Nq, w.Nk, w.d, 0)
+    ws = (torch.empty(max(wo, 1), dtype=torch.float32, device=device),
+          torch.empty(max(wl, 1), dtype=torch.float32, device=device))
+    O = torch.empty_like(qd)
+    L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        binding.fa_fwd_splitkv(qd, kd, vd, n_splits=splits, scale=w.scale, causal=w.causal,
+                               out=O, lse=L, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    if binding.device_status() != 0:
+        raise RuntimeError("fa_fwd_splitkv reported a device status")
+    return [a.elapsed_time(b) for a, b in ev], splits
+
+
 def roofline_tensor(flops, ms, peaks, kind, traffic=None):
     achieved = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -376,6 +413,8 @@ def main(argv=None):
                     help="launch only (no timing, no flush, no oracle): for ncu captures")
     ap.add_argument("--softmax", action="store_true",
                     help="with --profile: launch osm_softmax instead of fa_fwd")
+    ap.add_argument("--decode", action="store_true",
+                    help="with --profile: launch fa_fwd_splitkv on the decode workload")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be at least 3")
@@ -397,7 +436,10 @@ def main(argv=None):
     w = inputs.ATTN_WORKLOADS[args.workload]
 
     if args.profile:
-        if args.softmax:
+        if args.decode:
+            dw = next(iter(inputs.DECODE_WORKLOADS.values()))
+            time_splitkv(dw, args.steps, args.warmup, device, None)
+        elif args.softmax:
             sw = inputs.SOFTMAX_WORKLOADS["softmax_65536x4000"]
             x = inputs.softmax_workload_inputs(sw).to(device)
             for _ in range(args.warmup + args.steps):
@@ -455,6 +497,15 @@ def main(argv=None):
                            "ms_per_step": round(oms, 4),
                            "roofline": roofline_tensor(ow.flops, oms, peaks, peaks_kind,
                                                        NCU_TRAFFIC_BYTES.get(name))}
+            torch.cuda.empty_cache()
+        for name, dw in inputs.DECODE_WORKLOADS.items():
+            t, splits = time_splitkv(dw, 20, 3, device, flush)
+            dms = max_over_ranks(sum(t) / len(t), dist, device)
+            other[name] = {"GB/s": round(world * dw.hbm_bytes / (dms * 1e-3) / 1e9, 1),
+                           "TFLOP/s": round(world * dw.flops / (dms * 1e-3) / 1e12, 2),
+                           "ms_per_step": round(dms, 4), "n_splits": splits,
+                           "roofline": roofline_hbm(dw.hbm_bytes, dms, peaks, peaks_kind,
+                                                    NCU_TRAFFIC_BYTES.get(name))}
             torch.cuda.empty_cache()
         sw = inputs.SOFTMAX_WORKLOADS["softmax_65536x4000"]
         t = time_softmax(sw, 20, 3, device, flush)

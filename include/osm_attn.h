@@ -14,6 +14,13 @@
 
 #include <stdint.h>
 
+/* Only the functions declared here are exported from the shared library. */
+#if defined(__GNUC__)
+#define OSM_ATTN_API __attribute__((visibility("default")))
+#else
+#define OSM_ATTN_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -53,8 +60,48 @@ typedef enum {
  * Precision: bf16 inputs, fp32 accumulation of both products, probabilities rounded to bf16
  * for the second product, fp32 running max/sum, bf16 output, fp32 LSE.
  */
-int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
-           int64_t H, int64_t N, int64_t d, float scale, int causal, void* stream);
+OSM_ATTN_API int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                        void* stream);
+
+/*
+ * fa_fwd_splitkv -- attention of Nq queries against Nk keys with the keys cut into n_splits
+ * contiguous ranges that are processed in parallel (Flash-Decoding), then combined.
+ *
+ * The same lesson, section "Where this is used in practice" (Flash-Decoding splits the keys
+ * across several workers when there are few queries and combines the partial results) and
+ * the two-worker merge at the end of "From softmax to attention": each range yields its
+ * normalised partial output O_s and log-sum-exp LSE_s; the combine takes M = max_s LSE_s,
+ * w_s = exp(LSE_s - M), O = sum_s w_s O_s / sum_s w_s and LSE = M + ln sum_s w_s.
+ *
+ *   Q        bf16 [B, H, Nq, d]; K, V bf16 [B, H, Nk, d]; all contiguous, 16-byte aligned.
+ *   O, LSE   as fa_fwd, shaped [B, H, Nq, d] and [B, H, Nq]; LSE may be NULL.
+ *   causal   non-zero: the Nq queries are the last Nq of the Nk positions, so query i sees keys
+ *            j <= i + (Nk - Nq) (Nq == Nk: the usual mask; a query with no allowed key gets
+ *            O = 0 and LSE = -inf).
+ *   n_splits 1 .. 256, normally the value fa_fwd_splitkv_plan returns.  1 runs the one-pass
+ *            kernel directly (no workspace needed).
+ *   ws_O     fp32 workspace of n_splits * B*H*Nq * d floats, 16-byte aligned (n_splits > 1);
+ *   ws_LSE   fp32 workspace of n_splits * B*H*Nq floats (n_splits > 1).  Both owned by the
+ *            caller, overwritten, and must not overlap any input or output.
+ * Nk == 0 writes O = 0 and LSE = -inf; B*H*Nq == 0 is a no-op.  Errors as fa_fwd.
+ */
+OSM_ATTN_API int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O,
+                                float* LSE, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                                int64_t d, float scale, int causal, int64_t n_splits,
+                                float* ws_O, float* ws_LSE, void* stream);
+
+/*
+ * fa_fwd_splitkv_plan -- the number of key ranges fa_fwd_splitkv should use for this shape and
+ * the workspace it then needs.  n_splits = 0 asks the library to choose (enough CTAs for about
+ * eight waves on this GPU, at most 64 ranges and one key tile per range); 1 .. 256 is clamped to
+ * the number of 128-key tiles.  Writes *splits_out (0 when Nk == 0), *ws_o_floats and
+ * *ws_lse_floats (both 0 when one range suffices).  All three are HOST pointers.  Queries the
+ * current CUDA device for its SM count when choosing.
+ */
+OSM_ATTN_API int fa_fwd_splitkv_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                                     int64_t d, int64_t n_splits, int64_t* splits_out,
+                                     int64_t* ws_o_floats, int64_t* ws_lse_floats);
 
 /*
  * osm_softmax -- y = softmax(x) of every row, single pass over HBM, and its log-sum-exp.
@@ -73,18 +120,18 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
  *   rows, cols >= 0; rows*cols == 0 is a no-op (lse is not written).
  *   A row with no finite entry (all -inf) gives y = 0 and lse = -inf.
  */
-int osm_softmax(const float* x, float* y, int64_t rows, int64_t cols, float* lse,
-                void* stream);
+OSM_ATTN_API int osm_softmax(const float* x, float* y, int64_t rows, int64_t cols,
+                             float* lse, void* stream);
 
 /* A static, human-readable name for a status code (never NULL). */
-const char* fa_status_string(int status);
+OSM_ATTN_API const char* fa_status_string(int status);
 
 /*
  * osm_attn_device_status -- synchronises `stream`, then reads and clears the device status
  * word the kernels set when a bounded wait gives up (FA_OK when none did).  *status
  * (HOST pointer) receives the code; the return value is FA_OK or FA_ERR_CUDA.
  */
-int osm_attn_device_status(void* stream, int* status);
+OSM_ATTN_API int osm_attn_device_status(void* stream, int* status);
 
 /*
  * osm_attn_selftest_wait -- diagnostic for the bounded-wait error path (the pages have no
@@ -95,10 +142,10 @@ int osm_attn_device_status(void* stream, int* status);
  * involved: the kernel exits normally and the context stays usable.  Returns FA_OK when the
  * launch succeeded, FA_ERR_INVALID_ARG for a timeout out of range, FA_ERR_CUDA otherwise.
  */
-int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
+OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 
 /* ABI version of this header (incremented on any incompatible change). */
-int osm_attn_abi_version(void);
+OSM_ATTN_API int osm_attn_abi_version(void);
 
 #define OSM_ATTN_ABI_VERSION 1
 

@@ -7,11 +7,11 @@ CPU fallback.
 """
 from __future__ import annotations
 
-__all__ = ["fa_fwd", "osm_softmax", "lib"]
+__all__ = ["fa_fwd", "fa_fwd_splitkv", "osm_softmax", "lib"]
 
 
 def __getattr__(name):
-    if name in ("fa_fwd", "osm_softmax", "lib", "FaError", "device_status"):
+    if name in ("fa_fwd", "fa_fwd_splitkv", "osm_softmax", "lib", "FaError", "device_status"):
         from . import binding
 
         return getattr(binding, name)

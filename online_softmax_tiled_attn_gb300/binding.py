@@ -44,6 +44,12 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_int, vp]
             L.fa_fwd.restype = ctypes.c_int
+            L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                         ctypes.c_float, ctypes.c_int, i64, vp, vp, vp]
+            L.fa_fwd_splitkv.restype = ctypes.c_int
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            L.fa_fwd_splitkv_plan.argtypes = [i64, i64, i64, i64, i64, i64, i64p, i64p, i64p]
+            L.fa_fwd_splitkv_plan.restype = ctypes.c_int
             L.osm_softmax.argtypes = [vp, vp, i64, i64, vp, vp]
             L.osm_softmax.restype = ctypes.c_int
             L.fa_status_string.argtypes = [ctypes.c_int]
@@ -76,6 +82,23 @@ def _stream_handle(stream):
 def fa_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, stream_ptr):
     return lib().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
                         float(scale), int(bool(causal)), stream_ptr)
+
+
+def fa_fwd_splitkv_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, causal,
+                       n_splits, ws_o_ptr, ws_lse_ptr, stream_ptr):
+    return lib().fa_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(Nq),
+                                int(Nk), int(d), float(scale), int(bool(causal)), int(n_splits),
+                                ws_o_ptr, ws_lse_ptr, stream_ptr)
+
+
+def splitkv_plan(B, H, Nq, Nk, d, n_splits=0):
+    """(splits, workspace O floats, workspace LSE floats) for fa_fwd_splitkv."""
+    s, wo, wl = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = lib().fa_fwd_splitkv_plan(int(B), int(H), int(Nq), int(Nk), int(d), int(n_splits),
+                                   ctypes.byref(s), ctypes.byref(wo), ctypes.byref(wl))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv_plan")
+    return s.value, wo.value, wl.value
 
 
 def osm_softmax_raw(x_ptr, y_ptr, rows, cols, lse_ptr, stream_ptr):
@@ -135,6 +158,49 @@ def fa_fwd(q, k, v, scale=None, causal=False, out=None, lse=None, return_lse=Tru
                     _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+    return out, lse
+
+
+def fa_fwd_splitkv(q, k, v, n_splits=0, scale=None, causal=False, out=None, lse=None,
+                   return_lse=True, workspace=None, stream=None):
+    """Attention of q [B,H,Nq,d] against k, v [B,H,Nk,d] (CUDA bf16) with the keys split into
+    key ranges computed in parallel and combined (Flash-Decoding).  n_splits = 0 lets the
+    library choose.  `workspace` may be a (ws_O, ws_LSE) pair of fp32 CUDA tensors; otherwise
+    it is allocated here (the library itself never allocates).  Returns (O, LSE)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 [B, H, N, d] tensor")
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] disagree")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    splits, wo, wl = splitkv_plan(B, H, Nq, Nk, d, n_splits)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ws_o = ws_l = None
+    if splits > 1:
+        if workspace is None:
+            ws_o = torch.empty(wo, dtype=torch.float32, device=q.device)
+            ws_l = torch.empty(wl, dtype=torch.float32, device=q.device)
+        else:
+            ws_o, ws_l = workspace
+            if ws_o.numel() < wo or ws_l.numel() < wl:
+                raise ValueError("workspace too small for this split count")
+    rc = fa_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, scale,
+                            causal, max(splits, 1) if Nk > 0 else 0,
+                            ws_o.data_ptr() if ws_o is not None else None,
+                            ws_l.data_ptr() if ws_l is not None else None, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv")
     return out, lse
 
 

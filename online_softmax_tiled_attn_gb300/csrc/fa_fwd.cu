@@ -178,12 +178,27 @@ __device__ __forceinline__ bool softmax_tail(Bars* bars, const uint32_t (&sr)[64
     return true;
 }
 
-template <int D, bool CAUSAL>
+// Launch parameters.  The key range of one head is cut into n_splits contiguous ranges of
+// tiles_per_split key tiles; with n_splits == 1 (SPLIT == false) a CTA covers every key and
+// writes the final O (bf16) and LSE, otherwise it writes its range's normalised partial output
+// (fp32) and log-sum-exp to the workspace for the combine kernel.
+struct FaParams {
+    __nv_bfloat16* O;  // [BH, Nq, D] bf16 (SPLIT == false)
+    float* LSE;        // [BH, Nq] or nullptr (SPLIT == false)
+    float* ws_O;       // [n_splits, BH, Nq, D] fp32 (SPLIT == true)
+    float* ws_LSE;     // [n_splits, BH, Nq] (SPLIT == true)
+    int Nq, Nk, BH, n_qtiles, n_splits, tiles_per_split;
+    float scale_log2;
+    unsigned long long timeout_ns;
+};
+
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                  float* __restrict__ LSE, int N, int BH, int n_qtiles, float scale_log2,
-                  unsigned long long timeout_ns) {
+                  const __grid_constant__ CUtensorMap tmV, const FaParams prm) {
+    const int Nq = prm.Nq, Nk = prm.Nk;
+    const float scale_log2 = prm.scale_log2;
+    const unsigned long long timeout_ns = prm.timeout_ns;
     using C = Cfg<D>;
     constexpr int S_ = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -196,17 +211,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work item: causal runs the longest rows (highest query tiles) first.
-    int q_tile, bh;
-    if (CAUSAL) {
-        q_tile = n_qtiles - 1 - static_cast<int>(blockIdx.x) / BH;
-        bh = static_cast<int>(blockIdx.x) % BH;
-    } else {
-        q_tile = static_cast<int>(blockIdx.x) % n_qtiles;
-        bh = static_cast<int>(blockIdx.x) / n_qtiles;
+    // Work item (query tile, head, key range).  Causal runs the longest rows (highest query
+    // tiles) first.
+    int q_tile, bh, split;
+    {
+        const int idx = static_cast<int>(blockIdx.x);
+        const int per_tile = prm.BH * prm.n_splits;
+        if (CAUSAL) {
+            q_tile = prm.n_qtiles - 1 - idx / per_tile;
+            bh = (idx % per_tile) / prm.n_splits;
+            split = idx % prm.n_splits;
+        } else {
+            split = idx % prm.n_splits;
+            q_tile = (idx / prm.n_splits) % prm.n_qtiles;
+            bh = idx / (prm.n_splits * prm.n_qtiles);
+        }
     }
-    const int n_kv_all = (N + kBN - 1) / kBN;
-    const int n_kv = CAUSAL ? min(n_kv_all, q_tile + 1) : n_kv_all;
+    // Key tiles [kt0, kt0 + n_kv).  Causal: the queries are the last Nq of the Nk positions, so
+    // query row q sees keys j <= q + Nk - Nq; tiles wholly past the tile's last row are skipped.
+    const int n_kv_all = (Nk + kBN - 1) / kBN;
+    const int kt0 = split * prm.tiles_per_split;
+    int kt1 = min(n_kv_all, kt0 + prm.tiles_per_split);
+    if (CAUSAL) {
+        const long long last_key = static_cast<long long>(q_tile) * kBM + kBM - 1 + (Nk - Nq);
+        kt1 = min(static_cast<long long>(kt1), last_key < 0 ? 0 : last_key / kBN + 1);
+    }
+    const int n_kv = max(0, kt1 - kt0);
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
@@ -257,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&bars->k_full[s], kTx);
                 for (int h = 0; h < C::kHalves; ++h)
                     tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, &tmK,
-                                &bars->k_full[s], h * 64, j * kBN, bh);
+                                &bars->k_full[s], h * 64, (kt0 + j) * kBN, bh);
                 k_issued = j + 1;
             }
             // Drain: every load this thread issued has landed before the CTA may exit.  The
@@ -288,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&bars->v_full[s], kTx);
                 for (int h = 0; h < C::kHalves; ++h)
                     tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
-                                &bars->v_full[s], h * 64, j * kBN, bh);
+                                &bars->v_full[s], h * 64, (kt0 + j) * kBN, bh);
                 v_issued = j + 1;
             }
             const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
@@ -359,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x & 127;  // row in the tile == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int q_row = q_tile * kBM + r;
-        const int key_limit = CAUSAL ? min(N - 1, q_row) : N - 1;  // last allowed key
+        const int key_limit = CAUSAL ? min(Nk - 1, q_row + (Nk - Nq)) : Nk - 1;  // last allowed key
         bool ok = true;
 
         if (h == 0) {
@@ -409,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sr[64];
             tmem_ld64_sync(tS + b * 128, sr);
             warp_arrive_tc(&bars->s_free[b]);  // S(j) is in registers: S(j+2) may overwrite it
-            const int kv0 = j * kBN + h * 64;
+            const int kv0 = (kt0 + j) * kBN + h * 64;
             if (kv0 + 63 > key_limit) {
 #pragma unroll
                 for (int e = 0; e < 64; ++e)
@@ -432,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = softmax_tail<D>(bars, sr, mx, scale_log2, m, l, j, tP, tO, timeout_ns);
         }
         for (; bar_passes < n_kv; ++bar_passes) named_bar_sync(kBarSoftmax, 256);
-        if (ok && !warp_wait(&bars->pv_done, (n_kv - 1) & 1, timeout_ns)) {
+        if (ok && n_kv > 0 && !warp_wait(&bars->pv_done, (n_kv - 1) & 1, timeout_ns)) {
             record_timeout(10);
             ok = false;
         }
@@ -442,28 +472,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(kBarSoftmax, 256);
         l += bars->red[n_kv & 1][h ^ 1][r];
         if (ok) {
-            // Epilogue: this thread writes columns [h*D/2, (h+1)*D/2) of O row r.
+            // Epilogue: this thread writes columns [h*D/2, (h+1)*D/2) of row q_row.  A CTA whose
+            // key range is empty (n_kv == 0: split-key CTAs past the diagonal or past Nk) never
+            // ran P V, so it writes the empty state O = 0, LSE = -inf without reading TMEM.
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const bool store = q_row < N;
-            __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q_row) * D + h * (D / 2);
+            const bool store = q_row < Nq;
+            const bool have = n_kv > 0;
+            const float lse = have ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            const size_t row = static_cast<size_t>(bh) * Nq + q_row;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
-                tmem_ld32_sync(tO + c * 32, o);
-                uint32_t pk[16];
+                if (have) {
+                    tmem_ld32_sync(tO + c * 32, o);
+                } else {
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
-                                        __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                if (SPLIT) {
+                    float* orow = prm.ws_O +
+                                  (static_cast<size_t>(split) * prm.BH * Nq + row) * D + h * (D / 2);
+                    if (store) {
+                        float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l,
+                                                 __uint_as_float(o[4 * v + 1]) * inv_l,
+                                                 __uint_as_float(o[4 * v + 2]) * inv_l,
+                                                 __uint_as_float(o[4 * v + 3]) * inv_l);
+                    }
+                } else {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
+                                            __uint_as_float(o[2 * e + 1]) * inv_l);
+                    if (store) {
+                        uint4* dst =
+                            reinterpret_cast<uint4*>(prm.O + row * D + h * (D / 2) + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] =
+                                make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
                 }
             }
-            if (store && h == 0 && LSE != nullptr)
-                LSE[static_cast<size_t>(bh) * N + q_row] = (m + __log2f(l)) * 0.69314718055994531f;
+            if (store && h == 0) {
+                if (SPLIT)
+                    prm.ws_LSE[static_cast<size_t>(split) * prm.BH * Nq + row] = lse;
+                else if (prm.LSE != nullptr)
+                    prm.LSE[row] = lse;
+            }
         }
     }
 
@@ -473,45 +532,198 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool CAUSAL>
-int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* O,
-               float* LSE, int N, int BH, float scale, cudaStream_t stream) {
+// Combine of the split-key partial states: for each row, the partial outputs O_s (normalised
+// by their own sums) and log-sum-exps LSE_s are merged with the lesson's two-worker merge in
+// log form: M = max_s LSE_s, w_s = exp(LSE_s - M), O = sum_s w_s O_s / sum_s w_s,
+// LSE = M + ln sum_s w_s.  Empty ranges have LSE_s = -inf and weigh nothing; a row with no
+// allowed key at all gets O = 0 and LSE = -inf.  One warp per row, D/32 values per lane.
+template <int D>
+__global__ void __launch_bounds__(256)
+    splitkv_combine_kernel(const float* __restrict__ ws_O, const float* __restrict__ ws_LSE,
+                           __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, long long rows,
+                           int n_splits) {
+    constexpr int E = D / 32;  // values per lane
+    const int lane = threadIdx.x & 31;
+    for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         r < rows; r += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+        float M = -INFINITY;
+        for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, ws_LSE[s * rows + r]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        float wsum = 0.f;
+        if (M != -INFINITY) {
+            for (int s = 0; s < n_splits; ++s) {
+                const float ls = ws_LSE[s * rows + r];
+                const float w = ex2_approx((ls - M) * 1.4426950408889634f);  // ls = -inf -> 0
+                wsum += w;
+                const float* src = ws_O + (static_cast<size_t>(s) * rows + r) * D + lane * E;
+                if (E == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    acc[0] += w * v.x;
+                    acc[1] += w * v.y;
+                    acc[2] += w * v.z;
+                    acc[E > 3 ? 3 : 0] += w * v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(src);
+                    acc[0] += w * v.x;
+                    acc[E > 1 ? 1 : 0] += w * v.y;
+                }
+            }
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        __nv_bfloat16* dst = O + static_cast<size_t>(r) * D + lane * E;
+        if (E == 4) {
+            uint2 pk;
+            pk.x = pack_bf16x2(acc[0] * inv, acc[1 % E] * inv);
+            pk.y = pack_bf16x2(acc[2 % E] * inv, acc[3 % E] * inv);
+            *reinterpret_cast<uint2*>(dst) = pk;
+        } else {
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % E] * inv);
+        }
+        if (lane == 0 && LSE != nullptr)
+            LSE[r] = (M == -INFINITY) ? -INFINITY : M + logf(wsum);
+    }
+}
+
+int device_sm_count() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 0;
+    });
+    return n;
+}
+
+template <int D, bool CAUSAL, bool SPLIT>
+int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const FaParams& prm, cudaStream_t stream) {
     using C = Cfg<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL>,
+        attr_err = cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, SPLIT>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
     });
     if (attr_err != cudaSuccess) return FA_ERR_CUDA;
-    const int n_qtiles = (N + kBM - 1) / kBM;
-    const long long ctas = static_cast<long long>(n_qtiles) * BH;
+    const long long ctas = static_cast<long long>(prm.n_qtiles) * prm.BH * prm.n_splits;
     if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    const float scale_log2 = scale * 1.4426950408889634f;
-    fa_fwd_kernel<D, CAUSAL><<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(
-        tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, N, BH, n_qtiles, scale_log2,
-        fa_wait_timeout_ns());
+    fa_fwd_kernel<D, CAUSAL, SPLIT>
+        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <bool SPLIT>
+int launch_dispatch(int64_t d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                    const CUtensorMap& tv, const FaParams& prm, cudaStream_t stream) {
+    if (d == 64)
+        return causal ? launch_kernel<64, true, SPLIT>(tq, tk, tv, prm, stream)
+                      : launch_kernel<64, false, SPLIT>(tq, tk, tv, prm, stream);
+    if (d == 128)
+        return causal ? launch_kernel<128, true, SPLIT>(tq, tk, tv, prm, stream)
+                      : launch_kernel<128, false, SPLIT>(tq, tk, tv, prm, stream);
+    return FA_ERR_UNSUPPORTED;
+}
+
+int make_maps(const void* Q, const void* K, const void* V, int64_t BH, int64_t Nq, int64_t Nk,
+              int64_t d, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
+    int st = make_bhnd_tensor_map(tq, Q, BH, Nq, d);
+    if (st == FA_OK) st = make_bhnd_tensor_map(tk, K, BH, Nk, d);
+    if (st == FA_OK) st = make_bhnd_tensor_map(tv, V, BH, Nk, d);
+    return st;
 }
 
 }  // namespace
 
 int fa_fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t BH,
                   int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream) {
-    if (N > (1LL << 30) || BH > (1LL << 30)) return FA_ERR_UNSUPPORTED;
+    return fa_fwd_qk_launch(Q, K, V, O, LSE, BH, N, N, d, scale, causal, stream);
+}
+
+int fa_fwd_qk_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     int64_t BH, int64_t Nq, int64_t Nk, int64_t d, float scale, bool causal,
+                     cudaStream_t stream) {
+    if (Nq > (1LL << 30) || Nk > (1LL << 30) || BH > (1LL << 30)) return FA_ERR_UNSUPPORTED;
     CUtensorMap tq, tk, tv;
-    int st = make_bhnd_tensor_map(&tq, Q, BH, N, d);
-    if (st == FA_OK) st = make_bhnd_tensor_map(&tk, K, BH, N, d);
-    if (st == FA_OK) st = make_bhnd_tensor_map(&tv, V, BH, N, d);
+    const int st = make_maps(Q, K, V, BH, Nq, Nk, d, &tq, &tk, &tv);
     if (st != FA_OK) return st;
-    const int n = static_cast<int>(N), bh = static_cast<int>(BH);
+    FaParams prm{};
+    prm.O = static_cast<__nv_bfloat16*>(O);
+    prm.LSE = LSE;
+    prm.Nq = static_cast<int>(Nq);
+    prm.Nk = static_cast<int>(Nk);
+    prm.BH = static_cast<int>(BH);
+    prm.n_qtiles = static_cast<int>((Nq + kBM - 1) / kBM);
+    prm.n_splits = 1;
+    prm.tiles_per_split = static_cast<int>((Nk + kBN - 1) / kBN);
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.timeout_ns = fa_wait_timeout_ns();
+    return launch_dispatch<false>(d, causal, tq, tk, tv, prm, stream);
+}
+
+int64_t splitkv_choose_splits(int64_t BH, int64_t Nq, int64_t Nk, int64_t requested) {
+    const int64_t n_kv_all = (Nk + kBN - 1) / kBN;
+    if (n_kv_all <= 0) return 0;
+    int64_t splits = requested;
+    if (splits <= 0) {
+        // Enough CTAs for about eight waves, so the key ranges of a few heads spread over
+        // every SM; the combine that follows is cheap next to the attention.
+        const int64_t base = ((Nq + kBM - 1) / kBM) * BH;
+        const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 148;
+        splits = base > 0 ? (8 * sms + base - 1) / base : 1;
+        if (splits > 64) splits = 64;
+    }
+    if (splits > n_kv_all) splits = n_kv_all;
+    if (splits < 1) splits = 1;
+    // Every split gets the same number of key tiles; drop the ranges left empty by rounding.
+    const int64_t tps = (n_kv_all + splits - 1) / splits;
+    return (n_kv_all + tps - 1) / tps;
+}
+
+int fa_fwd_splitkv_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                          int64_t BH, int64_t Nq, int64_t Nk, int64_t d, float scale, bool causal,
+                          int64_t n_splits, float* ws_O, float* ws_LSE, cudaStream_t stream) {
+    if (Nq > (1LL << 30) || Nk > (1LL << 30) || BH > (1LL << 30)) return FA_ERR_UNSUPPORTED;
+    const long long rows = static_cast<long long>(BH) * Nq;
+    if (n_splits > 1) {
+        CUtensorMap tq, tk, tv;
+        const int st = make_maps(Q, K, V, BH, Nq, Nk, d, &tq, &tk, &tv);
+        if (st != FA_OK) return st;
+        const int64_t n_kv_all = (Nk + kBN - 1) / kBN;
+        FaParams prm{};
+        prm.ws_O = ws_O;
+        prm.ws_LSE = ws_LSE;
+        prm.Nq = static_cast<int>(Nq);
+        prm.Nk = static_cast<int>(Nk);
+        prm.BH = static_cast<int>(BH);
+        prm.n_qtiles = static_cast<int>((Nq + kBM - 1) / kBM);
+        prm.n_splits = static_cast<int>(n_splits);
+        prm.tiles_per_split = static_cast<int>((n_kv_all + n_splits - 1) / n_splits);
+        prm.scale_log2 = scale * 1.4426950408889634f;
+        prm.timeout_ns = fa_wait_timeout_ns();
+        const int rc = launch_dispatch<true>(d, causal, tq, tk, tv, prm, stream);
+        if (rc != FA_OK) return rc;
+    } else if (n_splits == 1) {
+        return fa_fwd_qk_launch(Q, K, V, O, LSE, BH, Nq, Nk, d, scale, causal, stream);
+    }
+    // n_splits > 1: merge the partial states; n_splits == 0 (no key at all): O = 0, LSE = -inf.
+    const long long warps = rows;
+    long long grid = (warps + 7) / 8;
+    if (grid > 65535LL * 64) grid = 65535LL * 64;
+    if (grid < 1) return FA_OK;
+    const int ns = static_cast<int>(n_splits > 1 ? n_splits : 0);
     if (d == 64)
-        return causal ? launch_one<64, true>(tq, tk, tv, O, LSE, n, bh, scale, stream)
-                      : launch_one<64, false>(tq, tk, tv, O, LSE, n, bh, scale, stream);
-    if (d == 128)
-        return causal ? launch_one<128, true>(tq, tk, tv, O, LSE, n, bh, scale, stream)
-                      : launch_one<128, false>(tq, tk, tv, O, LSE, n, bh, scale, stream);
-    return FA_ERR_UNSUPPORTED;
+        splitkv_combine_kernel<64><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+            ws_O, ws_LSE, static_cast<__nv_bfloat16*>(O), LSE, rows, ns);
+    else
+        splitkv_combine_kernel<128><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+            ws_O, ws_LSE, static_cast<__nv_bfloat16*>(O), LSE, rows, ns);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 namespace {

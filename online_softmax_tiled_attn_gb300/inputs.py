@@ -18,6 +18,8 @@ ragged_b1h16n4000     B1 H16 N4000 d128, Q,K iid N(0, sd 3) (logit sd 9), V iid 
 dense_b2h32n8192      B2 H32 N8192 d128, Q/K/V iid N(0,1), non-causal (the d=128 long-N case)
 softmax_65536x4000    fp32 rows [65536, 4000], x = 9*N(0,1) and per row one entry +100 and one
                       entry -100 at seeded positions
+decode_b8h32q1k32768  B8 H32, one query against 32768 cached keys, d128, N(0,1), non-causal
+                      (the split-key path); seed 1007
 ====================  ==========================================================================
 
 Seeds: 1000 + the workload's index in the table above (1001 ... 1005 for the five attention
@@ -89,6 +91,49 @@ ATTN_WORKLOADS = {
         AttnWorkload("dense_b2h32n8192", 2, 32, 8192, 128, False, 1006),
     ]
 }
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq queries against a cache of Nk keys (the split-key / Flash-Decoding case)."""
+
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        return 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
+
+    @property
+    def hbm_bytes(self) -> int:
+        """Compulsory HBM traffic: read Q, K, V (bf16), write O (bf16) and LSE (fp32)."""
+        bh = self.B * self.H
+        return bh * (2 * self.Nq * self.d * 2 + 2 * self.Nk * self.d * 2 + self.Nq * 4)
+
+
+DECODE_WORKLOADS = {
+    w.name: w
+    for w in [DecodeWorkload("decode_b8h32q1k32768d128", 8, 32, 1, 32768, 128, False, 1007)]
+}
+
+
+def decode_inputs(w: DecodeWorkload):
+    """Q [B,H,Nq,d] and K, V [B,H,Nk,d], bf16 N(0,1), from one seeded generator."""
+    g = torch.Generator().manual_seed(int(w.seed))
+    q = torch.randn((w.B, w.H, w.Nq, w.d), generator=g).to(torch.bfloat16)
+    k = torch.randn((w.B, w.H, w.Nk, w.d), generator=g).to(torch.bfloat16)
+    v = torch.randn((w.B, w.H, w.Nk, w.d), generator=g).to(torch.bfloat16)
+    return q, k, v
+
 
 SOFTMAX_WORKLOADS = {
     w.name: w for w in [SoftmaxWorkload("softmax_65536x4000", 65536, 4000, 1005)]

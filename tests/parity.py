@@ -45,3 +45,15 @@ def check_softmax(y, lse, yref, lseref, what=""):
         ds = np.abs(sums[rows_ok] - 1.0).max()
         assert ds <= SOFTMAX_SUM_ATOL, f"{what}: max|sum-1| = {ds:.3e}"
     return dy
+
+
+def check_attention_allow_empty(O, L, Oref, Lref, what=""):
+    """As check_attention, but rows with no allowed key (Lref = -inf) must be exactly O = 0 and
+    LSE = -inf."""
+    O = np.asarray(O, dtype=np.float64)
+    L = np.asarray(L, dtype=np.float64)
+    empty = np.isneginf(Lref)
+    assert np.array_equal(np.isneginf(L), empty), f"{what}: empty rows differ"
+    assert np.all(O[empty] == 0.0), f"{what}: empty rows are not zero"
+    if (~empty).any():
+        check_attention(O[~empty], L[~empty], Oref[~empty], Lref[~empty], what)

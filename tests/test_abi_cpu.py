@@ -17,22 +17,31 @@ def declared_functions():
         if f.endswith(".h"):
             text = open(os.path.join(ROOT, "include", f)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+            names += re.findall(r"^\s*(?:OSM_ATTN_API\s+)?(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(",
+                                text, flags=re.M)
     return names
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("fa_fwd", "osm_softmax", "fa_status_string", "osm_attn_device_status",
+    for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "osm_softmax",
+              "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
 
 
-def test_library_exports_every_declared_symbol():
+def test_library_exports_every_declared_symbol_and_nothing_else():
+    import subprocess
+
     L = binding.lib()
     for n in declared_functions():
         assert hasattr(L, n), n
         assert isinstance(getattr(L, n), ctypes._CFuncPtr)
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.build_lib.LIB],
+                         capture_output=True, text=True)
+    if out.returncode == 0:
+        exported = {ln.split()[-1] for ln in out.stdout.splitlines() if " T " in ln}
+        assert exported == set(declared_functions()), exported ^ set(declared_functions())
 
 
 def test_status_strings_and_version():
