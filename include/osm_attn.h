@@ -31,8 +31,10 @@ typedef enum {
                                non-finite or non-positive scale, O aliasing an input */
     FA_ERR_UNSUPPORTED = 2, /* a valid request this build does not serve (d not 64/128) */
     FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch error, no device) */
-    FA_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait (reported by
+    FA_ERR_TIMEOUT = 4,     /* a kernel gave up a bounded wait (reported by
                                osm_attn_device_status) */
+    FA_ERR_SCRATCH_LIMIT = 5 /* fa_fwd_splitkv_noalloc: the partial states of this shape do not
+                                fit in the library's fixed scratch array */
 } fa_status;
 
 /*
@@ -102,6 +104,28 @@ OSM_ATTN_API int fa_fwd_splitkv(const void* Q, const void* K, const void* V, voi
 OSM_ATTN_API int fa_fwd_splitkv_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk,
                                      int64_t d, int64_t n_splits, int64_t* splits_out,
                                      int64_t* ws_o_floats, int64_t* ws_lse_floats);
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv without any workspace argument and without any
+ * device allocation (the pages have no counterpart: it serves callers that cannot allocate
+ * device memory during a call, such as a plugin or custom-operator hook whose host framework
+ * forbids allocation there, or a latency-critical decode loop).
+ *
+ * Same arguments and results as fa_fwd_splitkv, minus ws_O / ws_LSE; n_splits = 0 lets the
+ * library choose as fa_fwd_splitkv_plan does.  The per-range partial states live in a fixed
+ * array of 4 Mi floats (16 MiB) that every GPU loading the library holds until the process
+ * exits: a shape needs n_splits * B*H*Nq * (d + 1) floats of it, and one that needs more returns
+ * FA_ERR_SCRATCH_LIMIT without launching anything.  The first call made with a device current
+ * resolves that device's array address (cudaGetSymbolAddress) and caches it; make that first
+ * call before any stream capture.  All calls on a device share the one array: calls that can
+ * overlap on the GPU (different streams, or streams not ordered with each other) race on it
+ * and must be serialised by the caller.  The array keeps the last call's contents; every entry a
+ * call reads is written earlier in the same call, so nothing needs clearing between calls.
+ */
+OSM_ATTN_API int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
+                                        float* LSE, int64_t B, int64_t H, int64_t Nq,
+                                        int64_t Nk, int64_t d, float scale, int causal,
+                                        int64_t n_splits, void* stream);
 
 /*
  * osm_softmax -- y = softmax(x) of every row, single pass over HBM, and its log-sum-exp.

@@ -18,6 +18,7 @@ FA_ERR_INVALID_ARG = 1
 FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
+FA_ERR_SCRATCH_LIMIT = 5
 
 _lock = threading.Lock()
 _lib = None
@@ -47,6 +48,9 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                          ctypes.c_float, ctypes.c_int, i64, vp, vp, vp]
             L.fa_fwd_splitkv.restype = ctypes.c_int
+            L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                 ctypes.c_float, ctypes.c_int, i64, vp]
+            L.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
             i64p = ctypes.POINTER(ctypes.c_int64)
             L.fa_fwd_splitkv_plan.argtypes = [i64, i64, i64, i64, i64, i64, i64p, i64p, i64p]
             L.fa_fwd_splitkv_plan.restype = ctypes.c_int
@@ -89,6 +93,15 @@ def fa_fwd_splitkv_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, sca
     return lib().fa_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(Nq),
                                 int(Nk), int(d), float(scale), int(bool(causal)), int(n_splits),
                                 ws_o_ptr, ws_lse_ptr, stream_ptr)
+
+
+def fa_fwd_splitkv_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale,
+                               causal, n_splits, stream_ptr):
+    """The split-key attention with its partial states in the library's fixed scratch array
+    (no workspace argument, no allocation)."""
+    return lib().fa_fwd_splitkv_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
+                                        int(Nq), int(Nk), int(d), float(scale),
+                                        int(bool(causal)), int(n_splits), stream_ptr)
 
 
 def splitkv_plan(B, H, Nq, Nk, d, n_splits=0):

@@ -151,6 +151,8 @@ const char* fa_status_string(int status) {
         case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: valid but not supported by this build";
         case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up a bounded wait";
+        case FA_ERR_SCRATCH_LIMIT:
+            return "FA_ERR_SCRATCH_LIMIT: the partial states do not fit in the fixed scratch array";
         default: return "unknown fa_status";
     }
 }
