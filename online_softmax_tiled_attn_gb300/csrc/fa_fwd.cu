@@ -3,42 +3,46 @@
 // The method: "How FlashAttention avoids storing the giant score table" (spicyshark.co,
 // Online softmax lesson), section "From softmax to attention" (per key block: scores, new
 // running max, alpha = exp(m - m_new), p = exp(s - m_new), l = l*alpha + sum p,
-// acc = acc*alpha + p V, divide by l after the last block) and "The implementation" (a block
-// that leaves the max at -inf adds nothing); "kbwen.com FlashAttention", sections "Two
-// blocks" and "More than two blocks" (query blocks in the outer loop, key blocks inside,
-// each query row with its own max, sum and partial output).  The shift used inside the
-// exponentials may be any common constant per row ("The fix: subtract the maximum": the
-// factor cancels), which is what allows the lazy rescale below.
+// acc = acc*alpha + p V, divide by l after the last block), "The implementation" (a block that
+// leaves the max at -inf adds nothing) and the two-worker merge at the end of "From softmax to
+// attention"; "kbwen.com FlashAttention", sections "Two blocks" and "More than two blocks"
+// (query blocks in the outer loop, key blocks inside, each query row with its own max, sum
+// and partial output).  The shift used inside the exponentials may be any common constant per
+// row ("The fix: subtract the maximum": the factor cancels), which allows the lazy rescale.
 //
-// GB300 mapping.  One CTA owns one 128-row query tile of one (b, h) and walks its key tiles
-// (128 keys each).  Both products run on the tensor cores with A taken from tensor memory:
+// GB300 mapping.  One CTA owns one 128-row query tile of one (b, h) and walks a range of its
+// key tiles (128 keys each).  Both products run on the tensor cores with A in tensor memory:
 //   S = Q K^T   A = Q (copied once into TMEM), B = K tile (shared memory, K-major)
 //   O += P V    A = P (TMEM),                  B = V tile (shared memory, MN-major)
-// TMEM (512 columns): S_a [0,128), S_b [128,256), O [256, 256+d), P [256+d, 256+d+64),
-// Q [256+d+64, 256+d+64+d/2); bf16 operands hold two values per 32-bit column.
-// S is double-buffered: S(j+2) is computed while the softmax of S(j+1) runs, and P has its
-// own columns, so the tensor core never waits for P V before the next S.
-//   warps 0-3 / 4-7  softmax of score columns [0,64) / [64,128): one query row per thread (its
-//                    TMEM lane).  tcgen05.ld of 64 S values, mask, half-row max, the two halves
-//                    exchange their maxima through shared memory (one named barrier), lazy
-//                    reference max, ex2 of the scaled and shifted scores (scale*log2(e) folded
-//                    into one FFMA), half-row sum, P rounded to bf16 and stored to TMEM.  When a
-//                    row's reference max moves (rare: only beyond 2^8), the thread scales its
-//                    half of the O row in TMEM by alpha before storing P.  At the end: O / l to
-//                    bf16 and LSE = (m + log2 l) * ln 2.
-//   warps 8, 9       tcgen05.mma, one thread each: warp 8 issues S(j+2) as soon as the softmax
-//                    has read S(j); warp 9 issues O += P(j) V(j) as soon as P(j) is stored.  One
-//                    thread cannot issue M128 N128 K16 MMAs much faster than the tensor core runs
-//                    them, so with a single issuer every wait and commit between groups left the
-//                    tensor core idle; two independent streams keep it fed.  fp32 accumulators.
-//   warps 10, 11     TMA: Q once and the K ring (warp 10), the V ring (warp 11); 128-byte
-//                    swizzle, zero fill past N.  K runs ahead of V on its own.
+// TMEM (512 columns): S0 [0,128), S1 [128,256), then kP P buffers of 64 columns (two for d=64,
+// one for d=128), O (d columns) and Q (d/2 columns); bf16 operands hold two values per 32-bit
+// column.  S of key tile j goes to S(j & 1), P of tile j to P(j % kP).
+//   warps 0-3, 4-7  two softmax warpgroups that take the key tiles in turn (group g the tiles
+//                   j = g, g+2, ...), one query row per thread (its TMEM lane), whole rows:
+//                   tcgen05.ld of the 128 scores, mask, row max, the row's reference max
+//                   handed on from the previous tile through shared memory (a producer /
+//                   consumer named barrier, the only link between the groups), lazy reference
+//                   max, ex2 of the scaled and shifted scores (scale*log2(e) folded into one
+//                   FFMA), the group's own running sum, P rounded to bf16 into the group's P
+//                   buffer.  While one group computes the exponentials of tile j the other
+//                   already works on tile j+1.  When the reference moves (rare: only beyond
+//                   2^8) the group scales the O accumulator in TMEM by alpha before its P V.
+//                   At the end the two groups' (m, l) are combined with the two-worker merge,
+//                   then O / l to bf16 and LSE = (m + log2 l) * ln 2.
+//   warps 8, 9      tcgen05.mma, one thread each: warp 8 issues S(j+2) as soon as S(j) has been
+//                   read (two tiles ahead of the softmax), warp 9 issues O += P(j) V(j) as soon
+//                   as P(j) is stored.  One thread
+//                   cannot issue M128 N128 K16 MMAs much faster than the tensor core runs them,
+//                   so two independent issuers keep it fed.  fp32 accumulators.
+//   warps 10, 11    TMA: Q once and the K ring (warp 10), the V ring (warp 11); 128-byte
+//                   swizzle, zero fill past the end of the sequence.
 // Causal: key tiles above the diagonal are never visited; only diagonal and ragged tiles are
 // masked element by element.
 //
 // Every mbarrier wait is bounded (%globaltimer deadline).  A wait that gives up records
 // FA_ERR_TIMEOUT in a device status word; the CTA then drains its own TMA loads and MMAs,
-// frees its TMEM and exits.
+// frees its TMEM and exits.  The named barriers between the softmax groups are passed the same
+// number of times by every thread also after a timeout, so they cannot hang.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -64,21 +68,30 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kHalfBytes = 128 * 128;         // one 64-column half of a 128-row bf16 tile
 constexpr uint64_t kDrainNs = 1000000000ull;  // drain waits: at least 1 s
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
-constexpr uint32_t kBarSoftmax = 1;           // named barrier of the 8 softmax warps
+constexpr uint32_t kBarHandOff = 1;  // named barriers 1, 2: reference max of tile j -> j+1
+constexpr uint32_t kBarFinal = 3;    // named barrier 3: the two groups' final (m, l)
+constexpr uint32_t kBarTeardown = 4; // named barrier 4: TMEM no longer used (warps 0-9)
+constexpr uint32_t kTeardownThreads = 320;
 
 struct Bars {
-    uint64_t q_full;        // Q tile landed in shared memory (TMA)
-    uint64_t q_tmem;        // Q copied into TMEM (4 warps)
+    uint64_t q_full;      // Q tile landed in shared memory (TMA)
+    uint64_t q_tmem;      // Q copied into TMEM (4 warps)
     uint64_t k_full[4], k_empty[4];
     uint64_t v_full[4], v_empty[4];
-    uint64_t s_full[2];     // S buffer computed (tcgen05.commit)
-    uint64_t s_free[2];     // S buffer read into registers (8 warps)
-    uint64_t p_full;        // P stored to TMEM and O rescaled if needed (8 warps)
-    uint64_t pv_done;       // O += P V finished (tcgen05.commit)
+    uint64_t s_full[2];   // S buffer b holds S of a tile j with j & 1 == b (tcgen05.commit)
+    uint64_t s_free[2];   // S buffer b read into registers by its group (4 warps)
+    uint64_t p_full[2];   // P buffer b stored, O rescaled if needed (4 warps)
+    // O += P(j) V finished (tcgen05.commit) -> pv_done[j & 3].  A parity wait tells a phase
+    // from the one two completions later only if the waiter is never that far behind: every
+    // wait below is for a P V at most one tile older than one it has already seen complete and
+    // at least one tile older than any that can complete, so four barriers make each wait
+    // exact (see pv_wait).
+    uint64_t pv_done[4];
     uint64_t mma_done;
     uint64_t mma_pv_done;
     uint32_t tmem_base;
-    float red[2][2][kBM];   // [iteration parity][half][row]: half-row maxima, then sums
+    float mref[2][kBM];   // reference max of tile j for tile j+1: [j & 1][row]
+    float fin[2][2][kBM]; // each group's final [m, l] per row
 };
 
 template <int D>
@@ -93,10 +106,11 @@ struct Cfg {
     static constexpr int kBars = kV + kStages * kTileBytes;
     static constexpr int kBytes = kBars + static_cast<int>(sizeof(Bars));
     static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
-    static constexpr uint32_t kTmemS = 0;           // S_a, S_b
-    static constexpr uint32_t kTmemO = 256;
-    static constexpr uint32_t kTmemP = 256 + D;
-    static constexpr uint32_t kTmemQ = 256 + D + 64;
+    static constexpr int kP = D == 64 ? 2 : 1;      // P buffers
+    static constexpr uint32_t kTmemS = 0;           // S0, S1: 128 columns each
+    static constexpr uint32_t kTmemP = 256;         // P buffers: 64 columns each
+    static constexpr uint32_t kTmemO = kTmemP + 64 * kP;
+    static constexpr uint32_t kTmemQ = kTmemO + D;
     static_assert(kTmemQ + D / 2 <= kTmemCols, "TMEM budget");
     static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
 };
@@ -115,67 +129,18 @@ __device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// Wait until O += P(k) V has finished.  Callers guarantee that P(k-4) V has finished and that
+// P(k+4) V cannot have, so the parity of completion k >> 2 of barrier k & 3 is unambiguous.
+__device__ __forceinline__ bool pv_wait(Bars* bars, int k, uint64_t timeout_ns) {
+    return warp_wait(&bars->pv_done[k & 3], (k >> 2) & 1, timeout_ns);
+}
+
 __device__ __forceinline__ void record_timeout(int where) {
     atomicCAS(&g_fa_device_status, 0, FA_ERR_TIMEOUT | (where << 8));
 }
 
-// The rest of one softmax step of a half row, after the row maximum is known: lazy reference
-// max, exponentials and half-row sum, rescale of this half of the O row when the reference
-// moved, P stored to TMEM.  Returns false if a wait gave up.
-template <int D>
-__device__ __forceinline__ bool softmax_tail(Bars* bars, const uint32_t (&sr)[64], float mx,
-                                             float scale_log2, float& m, float& l, int j,
-                                             uint32_t tP, uint32_t tO,
-                                             unsigned long long timeout_ns) {
-    // Move the reference only when this tile's max exceeds it by more than the threshold
-    // (always on the first finite tile: m = -inf gives +inf > threshold).
-    const float m_new = (mx - m > kRescaleThreshold) ? mx : m;
-    const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_new);
-    // Nothing allowed yet (m_new = -inf): shift by 0 so every term is exp(-inf) = 0.
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    uint32_t p[32];
-    float2 rs = make_float2(0.f, 0.f);
-    float2 rs2 = make_float2(0.f, 0.f);
-    const float2 c2 = make_float2(scale_log2, scale_log2);
-    const float2 nm2 = make_float2(-m_use, -m_use);
-#pragma unroll
-    for (int e = 0; e < 64; e += 4) {
-        float2 t0 =
-            ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
-        float2 t1 =
-            ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
-        t0.x = ex2_approx(t0.x);
-        t0.y = ex2_approx(t0.y);
-        t1.x = ex2_approx(t1.x);
-        t1.y = ex2_approx(t1.y);
-        rs = fadd2(rs, t0);
-        rs2 = fadd2(rs2, t1);
-        p[e >> 1] = pack_bf16x2(t0.x, t0.y);
-        p[(e >> 1) + 1] = pack_bf16x2(t1.x, t1.y);
-    }
-    l = l * alpha + ((rs.x + rs.y) + (rs2.x + rs2.y));
-    m = m_new;
-    if (j > 0) {
-        // P(j-1) V must be done: P is overwritten below, and O is rescaled here.
-        if (!warp_wait(&bars->pv_done, (j - 1) & 1, timeout_ns)) {
-            record_timeout(9);
-            return false;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t o[32];
-                tmem_ld32_sync(tO + c * 32, o);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                tmem_st32_sync(tO + c * 32, o);
-            }
-        }
-    }
-    tmem_st32_sync(tP, p);
-    warp_arrive_tc(&bars->p_full);
-    return true;
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Launch parameters.  The key range of one head is cut into n_splits contiguous ranges of
@@ -196,11 +161,11 @@ template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FaParams prm) {
+    using C = Cfg<D>;
+    constexpr int S_ = C::kStages;
     const int Nq = prm.Nq, Nk = prm.Nk;
     const float scale_log2 = prm.scale_log2;
     const unsigned long long timeout_ns = prm.timeout_ns;
-    using C = Cfg<D>;
-    constexpr int S_ = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -249,10 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->s_full[b], 1);
-            mbar_init(&bars->s_free[b], 8);
+            mbar_init(&bars->s_free[b], 4);
+            mbar_init(&bars->p_full[b], 4);
         }
-        mbar_init(&bars->p_full, 8);
-        mbar_init(&bars->pv_done, 1);
+        for (int b = 0; b < 4; ++b) mbar_init(&bars->pv_done[b], 1);
         mbar_init(&bars->mma_done, 1);
         mbar_init(&bars->mma_pv_done, 1);
         fence_mbar_init();
@@ -266,133 +231,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == kTmaWarp) {
-        // -------------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            constexpr uint32_t kTx = C::kTileBytes;
-            mbar_arrive_expect_tx(&bars->q_full, kTx);
-            for (int h = 0; h < C::kHalves; ++h)
-                tma_load_3d(smem + C::kQ + h * kHalfBytes, &tmQ, &bars->q_full, h * 64,
-                            q_tile * kBM, bh);
-            int k_issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % S_;
-                if (j >= S_ && !mbar_wait(&bars->k_empty[s], ((j / S_) - 1) & 1, timeout_ns)) {
-                    record_timeout(1);
-                    break;
-                }
-                mbar_arrive_expect_tx(&bars->k_full[s], kTx);
+    // Registers: a softmax thread holds a whole row of 128 scores, the issue and TMA warps
+    // almost nothing: 2 x 128 x 208 + 128 x 80 stays within the 384 x 168 launched.  Each role
+    // branch sets its own limit and never rejoins the others; the TMEM is freed by warp 8 after
+    // a named barrier that the softmax groups and warp 9 arrive at when they are done with it.
+    if (warp >= kMmaWarp) {
+        setmaxnreg_dec<80>();
+        if (warp == kTmaWarp) {
+            // -------------------------------------------------------------------- TMA: Q and K
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+                constexpr uint32_t kTx = C::kTileBytes;
+                mbar_arrive_expect_tx(&bars->q_full, kTx);
                 for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, &tmK,
-                                &bars->k_full[s], h * 64, (kt0 + j) * kBN, bh);
-                k_issued = j + 1;
+                    tma_load_3d(smem + C::kQ + h * kHalfBytes, &tmQ, &bars->q_full, h * 64,
+                                q_tile * kBM, bh);
+                int k_issued = 0;
+                for (int j = 0; j < n_kv; ++j) {
+                    const int s = j % S_;
+                    if (j >= S_ && !mbar_wait(&bars->k_empty[s], ((j / S_) - 1) & 1, timeout_ns)) {
+                        record_timeout(1);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->k_full[s], kTx);
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, &tmK,
+                                    &bars->k_full[s], h * 64, (kt0 + j) * kBN, bh);
+                    k_issued = j + 1;
+                }
+                // Drain: every load this thread issued has landed before the CTA may exit.  The
+                // last load into a stage is the last phase of that stage's barrier, so it ends.
+                const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
+                mbar_wait(&bars->q_full, 0, drain_ns);
+                for (int s = 0; s < S_ && s < k_issued; ++s) {
+                    const int jl = s + ((k_issued - 1 - s) / S_) * S_;
+                    mbar_wait(&bars->k_full[s], (jl / S_) & 1, drain_ns);
+                }
             }
-            // Drain: every load this thread issued has landed before the CTA may exit.  The
-            // last load into a stage is the last phase of that stage's barrier, so it ends.
-            const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
-            mbar_wait(&bars->q_full, 0, drain_ns);
-            for (int s = 0; s < S_ && s < k_issued; ++s) {
-                const int jl = s + ((k_issued - 1 - s) / S_) * S_;
-                mbar_wait(&bars->k_full[s], (jl / S_) & 1, drain_ns);
+        } else if (warp == kTmaVWarp) {
+            // -------------------------------------------------------------------- TMA: V ring
+            if (lane == 0) {
+                constexpr uint32_t kTx = C::kTileBytes;
+                int v_issued = 0;
+                for (int j = 0; j < n_kv; ++j) {
+                    const int s = j % S_;
+                    // The last slot holds the staged Q until it has been copied into TMEM.
+                    if (j == S_ - 1 && !mbar_wait(&bars->q_tmem, 0, timeout_ns)) {
+                        record_timeout(13);
+                        break;
+                    }
+                    if (j >= S_ && !mbar_wait(&bars->v_empty[s], ((j / S_) - 1) & 1, timeout_ns)) {
+                        record_timeout(2);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->v_full[s], kTx);
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
+                                    &bars->v_full[s], h * 64, (kt0 + j) * kBN, bh);
+                    v_issued = j + 1;
+                }
+                const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
+                for (int s = 0; s < S_ && s < v_issued; ++s) {
+                    const int jl = s + ((v_issued - 1 - s) / S_) * S_;
+                    mbar_wait(&bars->v_full[s], (jl / S_) & 1, drain_ns);
+                }
             }
+        } else if (warp == kMmaWarp) {
+            // -------------------------------------------------------------------- MMA: S = Q K^T
+            if (lane == 0) {
+                constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0);
+                bool ok = mbar_wait(&bars->q_tmem, 0, timeout_ns);
+                if (!ok) record_timeout(3);
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    // S(j) overwrites S(j-2): its group must have read it.
+                    const int s = j % S_;
+                    const int b = j & 1;
+                    if ((j >= 2 && !mbar_wait(&bars->s_free[b], ((j >> 1) - 1) & 1, timeout_ns)) ||
+                        !mbar_wait(&bars->k_full[s], (j / S_) & 1, timeout_ns)) {
+                        record_timeout(5);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kb = sK + s * C::kTileBytes;
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        umma_ts(tmem + C::kTmemS + b * 128, tmem + C::kTmemQ + kk * 8,
+                                smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&bars->s_full[b]);
+                    umma_commit(&bars->k_empty[s]);
+                }
+                // Drain: no MMA of this thread may still write TMEM when it is freed.
+                umma_commit(&bars->mma_done);
+                mbar_wait(&bars->mma_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
+            }
+            __syncwarp();
+            named_bar_sync(kBarTeardown, kTeardownThreads);
+            tc_fence_after();
+            tmem_dealloc(tmem, kTmemCols);
+        } else if (warp == kMmaPvWarp) {
+            // -------------------------------------------------------------------- MMA: O += P V
+            if (lane == 0) {
+                constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 1);
+                for (int j = 0; j < n_kv; ++j) {
+                    const int s = j % S_;
+                    const int b = j % C::kP;
+                    if (!mbar_wait(&bars->v_full[s], (j / S_) & 1, timeout_ns) ||
+                        !mbar_wait(&bars->p_full[b], (j / C::kP) & 1, timeout_ns)) {
+                        record_timeout(6);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vb = sV + s * C::kTileBytes;
+                    const uint32_t pb = tmem + C::kTmemP + b * 64;
+    #pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        umma_ts(tmem + C::kTmemO, pb + kk * 8,
+                                smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idO,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&bars->pv_done[j & 3]);
+                    umma_commit(&bars->v_empty[s]);
+                }
+                umma_commit(&bars->mma_pv_done);
+                mbar_wait(&bars->mma_pv_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
+            }
+            __syncwarp();
+            tc_fence_before();
+            named_bar_arrive(kBarTeardown, kTeardownThreads);
         }
-    } else if (warp == kTmaVWarp) {
-        // -------------------------------------------------------------------- TMA, V ring
-        if (lane == 0) {
-            constexpr uint32_t kTx = C::kTileBytes;
-            int v_issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % S_;
-                // The last slot holds the staged Q until it has been copied into TMEM.
-                if (j == S_ - 1 && !mbar_wait(&bars->q_tmem, 0, timeout_ns)) {
-                    record_timeout(13);
-                    break;
-                }
-                if (j >= S_ && !mbar_wait(&bars->v_empty[s], ((j / S_) - 1) & 1, timeout_ns)) {
-                    record_timeout(2);
-                    break;
-                }
-                mbar_arrive_expect_tx(&bars->v_full[s], kTx);
-                for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
-                                &bars->v_full[s], h * 64, (kt0 + j) * kBN, bh);
-                v_issued = j + 1;
-            }
-            const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
-            for (int s = 0; s < S_ && s < v_issued; ++s) {
-                const int jl = s + ((v_issued - 1 - s) / S_) * S_;
-                mbar_wait(&bars->v_full[s], (jl / S_) & 1, drain_ns);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // -------------------------------------------------------------------- MMA: S = Q K^T
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0);
-            bool ok = mbar_wait(&bars->q_tmem, 0, timeout_ns);
-            if (!ok) record_timeout(3);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                // S(j) goes into buffer j & 1 once the softmax has read S(j - 2) from it.
-                const int s = j % S_;
-                if ((j >= 2 && !mbar_wait(&bars->s_free[j & 1], ((j - 2) >> 1) & 1, timeout_ns)) ||
-                    !mbar_wait(&bars->k_full[s], (j / S_) & 1, timeout_ns)) {
-                    record_timeout(5);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t kb = sK + s * C::kTileBytes;
-                const uint32_t d_tmem = tmem + C::kTmemS + (j & 1) * 128;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    umma_ts(d_tmem, tmem + C::kTmemQ + kk * 8, smem_desc_sw128(kb + off, 16, 1024),
-                            idS, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(&bars->s_full[j & 1]);
-                umma_commit(&bars->k_empty[s]);
-            }
-            // Drain: no MMA of this thread may still write TMEM when it is freed.
-            umma_commit(&bars->mma_done);
-            mbar_wait(&bars->mma_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
-        }
-        __syncwarp();
-    } else if (warp == kMmaPvWarp) {
-        // -------------------------------------------------------------------- MMA: O += P V
-        if (lane == 0) {
-            constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 1);
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % S_;
-                if (!mbar_wait(&bars->v_full[s], (j / S_) & 1, timeout_ns) ||
-                    !mbar_wait(&bars->p_full, j & 1, timeout_ns)) {
-                    record_timeout(6);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t vb = sV + s * C::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    umma_ts(tmem + C::kTmemO, tmem + C::kTmemP + kk * 8,
-                            smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idO,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars->pv_done);
-                umma_commit(&bars->v_empty[s]);
-            }
-            umma_commit(&bars->mma_pv_done);
-            mbar_wait(&bars->mma_pv_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
-        }
-        __syncwarp();
     } else {
+        setmaxnreg_inc<208>();
         // -------------------------------------------------------------------- softmax
-        const int h = warp >> 2;          // score columns [64h, 64h + 64)
+        const int g = warp >> 2;          // this group takes the key tiles j = g, g+2, ...
         const int r = threadIdx.x & 127;  // row in the tile == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int q_row = q_tile * kBM + r;
-        const int key_limit = CAUSAL ? min(Nk - 1, q_row + (Nk - Nq)) : Nk - 1;  // last allowed key
+        const int key_limit = CAUSAL ? min(Nk - 1, q_row + (Nk - Nq)) : Nk - 1;  // last allowed
+        const uint32_t tS = tmem + lane_addr + C::kTmemS + g * 128;
+        const uint32_t tO = tmem + lane_addr + C::kTmemO;
         bool ok = true;
 
-        if (h == 0) {
+        if (g == 0) {
             // Q row r: shared memory (128-byte swizzled, as TMA wrote it) -> TMEM lane r.
             if (!warp_wait(&bars->q_full, 0, timeout_ns)) {
                 record_timeout(7);
@@ -419,79 +401,154 @@ __global__ void __launch_bounds__(kThreads, 1)
             warp_arrive_tc(&bars->q_tmem);
         }
 
-        float m = -INFINITY;  // reference max of scale*log2(e)*s for this row
-        float l = 0.f;        // this half's running sum of 2^(scale*log2(e)*s - m)
-        const uint32_t tS = tmem + lane_addr + C::kTmemS + h * 64;
-        const uint32_t tP = tmem + lane_addr + C::kTmemP + h * 32;
-        const uint32_t tO = tmem + lane_addr + C::kTmemO + h * (D / 2);
-        // Every softmax thread passes the named barrier exactly n_kv times in the loop (plus once
-        // after it): a thread that left the loop early because a wait gave up makes up the
-        // missing passes below, so the barrier can never hang.
-        int bar_passes = 0;
-        for (int j = 0; ok && j < n_kv; ++j) {
-            const int b = j & 1;
-            if (!warp_wait(&bars->s_full[b], (j >> 1) & 1, timeout_ns)) {
+        float m_last = -INFINITY;  // reference max this group used last (log2 units, scaled)
+        float l = 0.f;             // this group's running sum of 2^(t - m_last) over its tiles
+        // Hand-off barrier passes of this group, in order: for each of its tiles j, a consumer
+        // pass (bar.sync) when j >= 1 and a producer pass (bar.arrive) when j + 1 < n_kv.  A
+        // group that stops early because a wait gave up makes up the missing passes below.
+        int j = g;
+        int stage = 0;  // 0: before tile j's consumer pass, 1: before its producer pass
+        for (; ok && j < n_kv; j += 2, stage = 0) {
+            if (!warp_wait(&bars->s_full[g], (j >> 1) & 1, timeout_ns)) {
                 record_timeout(8);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld64_sync(tS + b * 128, sr);
-            warp_arrive_tc(&bars->s_free[b]);  // S(j) is in registers: S(j+2) may overwrite it
-            const int kv0 = (kt0 + j) * kBN + h * 64;
-            if (kv0 + 63 > key_limit) {
+            uint32_t sr[128];
+            tmem_ld128_sync(tS, sr);
+            warp_arrive_tc(&bars->s_free[g]);  // S(j) is in registers: S(j+2) may overwrite it
+            const int kv0 = (kt0 + j) * kBN;
+            if (kv0 + kBN - 1 > key_limit) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e)
+                for (int e = 0; e < 128; ++e)
                     if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
             }
             float mx8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(sr[u]);
 #pragma unroll
-            for (int e = 8; e < 64; e += 2)
+            for (int e = 8; e < 128; e += 2)
                 mx8[(e >> 1) & 7] =
                     fmax3(mx8[(e >> 1) & 7], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-            float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                             fmaxf(mx8[6], mx8[7]));
-            // The two halves of the row agree on one maximum (shared memory + named barrier).
-            bars->red[b][h][r] = mx;
-            named_bar_sync(kBarSoftmax, 256);
-            ++bar_passes;
-            mx = fmaxf(mx, bars->red[b][h ^ 1][r]) * scale_log2;
-            ok = softmax_tail<D>(bars, sr, mx, scale_log2, m, l, j, tP, tO, timeout_ns);
+            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                   fmaxf(mx8[6], mx8[7])) *
+                             scale_log2;
+            // Reference max after tile j-1 (the other group's), handed over per row.
+            float m_prev = -INFINITY;
+            if (j >= 1) {
+                named_bar_sync(kBarHandOff + ((j - 1) & 1), 256);
+                m_prev = bars->mref[(j - 1) & 1][r];
+            }
+            stage = 1;
+            // Move the reference only when this tile's max exceeds it by more than the
+            // threshold (always on the first finite tile: -inf gives +inf > threshold).
+            const float m_new = (mx - m_prev > kRescaleThreshold) ? mx : m_prev;
+            if (j + 1 < n_kv) {
+                bars->mref[j & 1][r] = m_new;
+                named_bar_arrive(kBarHandOff + (j & 1), 256);
+            }
+            stage = 2;
+            // O (after P(j-1) V) is relative to m_prev; this group's l to m_last.
+            const float alpha_o = (m_new == m_prev) ? 1.f : ex2_approx(m_prev - m_new);
+            const float alpha_l = (m_new == m_last) ? 1.f : ex2_approx(m_last - m_new);
+            // Nothing allowed yet (m_new = -inf): shift by 0 so every term is exp(-inf) = 0.
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            uint32_t p[64];
+            float2 rs = make_float2(0.f, 0.f), rs2 = make_float2(0.f, 0.f);
+            const float2 c2 = make_float2(scale_log2, scale_log2);
+            const float2 nm2 = make_float2(-m_use, -m_use);
+#pragma unroll
+            for (int e = 0; e < 128; e += 4) {
+                float2 t0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                  c2, nm2);
+                float2 t1 = ffma2(
+                    make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
+                t0.x = ex2_approx(t0.x);
+                t0.y = ex2_approx(t0.y);
+                t1.x = ex2_approx(t1.x);
+                t1.y = ex2_approx(t1.y);
+                rs = fadd2(rs, t0);
+                rs2 = fadd2(rs2, t1);
+                p[e >> 1] = pack_bf16x2(t0.x, t0.y);
+                p[(e >> 1) + 1] = pack_bf16x2(t1.x, t1.y);
+            }
+            l = l * alpha_l + ((rs.x + rs.y) + (rs2.x + rs2.y));
+            m_last = m_new;
+            // P buffer pb was last read by P(j - kP) V.
+            const int pb = j % C::kP;
+            if (j >= C::kP && !pv_wait(bars, j - C::kP, timeout_ns)) {
+                record_timeout(9);
+                ok = false;
+                break;
+            }
+            // The reference moved: O must be rescaled after P(j-1) V and before P(j) V.
+            if (j >= 1 && __any_sync(0xffffffffu, alpha_o != 1.f)) {
+                if (!pv_wait(bars, j - 1, timeout_ns)) {
+                    record_timeout(14);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_o);
+                    tmem_st32_sync(tO + c * 32, o);
+                }
+            }
+            tc_fence_after();
+            tmem_st64_sync(tmem + lane_addr + C::kTmemP + pb * 64, p);
+            warp_arrive_tc(&bars->p_full[pb]);
         }
-        for (; bar_passes < n_kv; ++bar_passes) named_bar_sync(kBarSoftmax, 256);
-        if (ok && n_kv > 0 && !warp_wait(&bars->pv_done, (n_kv - 1) & 1, timeout_ns)) {
+        // Make up the hand-off passes a stop left out, in the same order.
+        for (; j < n_kv; j += 2, stage = 0) {
+            if (stage == 0 && j >= 1) named_bar_sync(kBarHandOff + ((j - 1) & 1), 256);
+            if (stage <= 1 && j + 1 < n_kv) named_bar_arrive(kBarHandOff + (j & 1), 256);
+        }
+        // Wait for the last P V, then combine the two groups' (m, l) with the two-worker merge.
+        if (ok && n_kv > 0 &&
+            !pv_wait(bars, n_kv - 1, timeout_ns)) {
             record_timeout(10);
             ok = false;
         }
         tc_fence_after();
-        // The two halves of the row add their sums (every softmax thread reaches this barrier).
-        bars->red[n_kv & 1][h][r] = l;
-        named_bar_sync(kBarSoftmax, 256);
-        l += bars->red[n_kv & 1][h ^ 1][r];
+        bars->fin[g][0][r] = m_last;
+        bars->fin[g][1][r] = l;
+        named_bar_sync(kBarFinal, 256);
+        const float mo = bars->fin[g ^ 1][0][r];
+        const float lo = bars->fin[g ^ 1][1][r];
+        const float M = fmaxf(m_last, mo);
+        float lt = 0.f;
+        if (M != -INFINITY) {
+            lt = (m_last == -INFINITY ? 0.f : l * ex2_approx(m_last - M)) +
+                 (mo == -INFINITY ? 0.f : lo * ex2_approx(mo - M));
+        }
         if (ok) {
-            // Epilogue: this thread writes columns [h*D/2, (h+1)*D/2) of row q_row.  A CTA whose
+            // Epilogue: this thread writes columns [g*D/2, (g+1)*D/2) of row q_row.  A CTA whose
             // key range is empty (n_kv == 0: split-key CTAs past the diagonal or past Nk) never
             // ran P V, so it writes the empty state O = 0, LSE = -inf without reading TMEM.
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
             const bool store = q_row < Nq;
             const bool have = n_kv > 0;
-            const float lse = have ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            const float lse = have ? (M + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
             const size_t row = static_cast<size_t>(bh) * Nq + q_row;
+            const uint32_t tOh = tO + g * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
                 if (have) {
-                    tmem_ld32_sync(tO + c * 32, o);
+                    tmem_ld32_sync(tOh + c * 32, o);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
                 if (SPLIT) {
-                    float* orow = prm.ws_O +
-                                  (static_cast<size_t>(split) * prm.BH * Nq + row) * D + h * (D / 2);
+                    const size_t ws_row = static_cast<size_t>(split) * prm.BH * Nq + row;
+                    float* orow = prm.ws_O + ws_row * D + g * (D / 2);
                     if (store) {
                         float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
@@ -509,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             __uint_as_float(o[2 * e + 1]) * inv_l);
                     if (store) {
                         uint4* dst =
-                            reinterpret_cast<uint4*>(prm.O + row * D + h * (D / 2) + c * 32);
+                            reinterpret_cast<uint4*>(prm.O + row * D + g * (D / 2) + c * 32);
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
                             dst[v] =
@@ -517,19 +574,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (store && h == 0) {
+            if (store && g == 0) {
                 if (SPLIT)
                     prm.ws_LSE[static_cast<size_t>(split) * prm.BH * Nq + row] = lse;
                 else if (prm.LSE != nullptr)
                     prm.LSE[row] = lse;
             }
         }
+        tc_fence_before();
+        named_bar_arrive(kBarTeardown, kTeardownThreads);
     }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Combine of the split-key partial states: for each row, the partial outputs O_s (normalised
@@ -743,7 +797,8 @@ __global__ void __launch_bounds__(32, 1) selftest_wait_kernel(unsigned long long
 
 int selftest_wait_launch(long long timeout_us, cudaStream_t stream) {
     if (timeout_us < 1 || timeout_us > 10000000) return FA_ERR_INVALID_ARG;
-    selftest_wait_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_us) * 1000ull);
+    const unsigned long long timeout_ns = static_cast<unsigned long long>(timeout_us) * 1000ull;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(timeout_ns);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
