@@ -10,32 +10,35 @@
 // and partial output).  The shift used inside the exponentials may be any common constant per
 // row ("The fix: subtract the maximum": the factor cancels), which allows the lazy rescale.
 //
-// GB300 mapping.  One CTA owns one 128-row query tile of one (b, h) and walks a range of its
-// key tiles (128 keys each).  Both products run on the tensor cores with A in tensor memory:
-//   S = Q K^T   A = Q (copied once into TMEM), B = K tile (shared memory, K-major)
-//   O += P V    A = P (TMEM),                  B = V tile (shared memory, MN-major)
-// TMEM (512 columns): S0 [0,128), S1 [128,256), then kP P buffers of 64 columns (two for d=64,
-// one for d=128), O (d columns) and Q (d/2 columns); bf16 operands hold two values per 32-bit
-// column.  S of key tile j goes to S(j & 1), P of tile j to P(j % kP).
+// GB300 mapping.  A persistent CTA per SM works through a list of work items, each a 128-row
+// query tile of one (b, h) against a range of its key tiles (128 keys each); the pipelines run
+// on from one item into the next.  Both products run on the tensor cores with A in TMEM:
+//   S = Q K^T   A = Q (tcgen05.cp from shared memory), B = K tile (shared memory, K-major)
+//   O += P V    A = P (TMEM),                          B = V tile (shared memory, MN-major)
+// TMEM (512 columns): S0 [0,128), S1 [128,256), then kP P buffers of 64 columns, O (d columns)
+// and kQ Q buffers of d/2 columns (kP = kQ = 2 for d=64, 1 for d=128); bf16 operands hold two
+// values per 32-bit column.  S of key tile J goes to S(J & 1), P of tile J to P(J % kP).
 //   warps 0-3, 4-7  two softmax warpgroups that take the key tiles in turn (group g the tiles
-//                   j = g, g+2, ...), one query row per thread (its TMEM lane), whole rows:
+//                   J with J & 1 == g), one query row per thread (its TMEM lane), whole rows:
 //                   tcgen05.ld of the 128 scores, mask, row max, the row's reference max
 //                   handed on from the previous tile through shared memory (a producer /
 //                   consumer named barrier, the only link between the groups), lazy reference
 //                   max, ex2 of the scaled and shifted scores (scale*log2(e) folded into one
-//                   FFMA), the group's own running sum, P rounded to bf16 into the group's P
-//                   buffer.  While one group computes the exponentials of tile j the other
-//                   already works on tile j+1.  When the reference moves (rare: only beyond
-//                   2^8) the group scales the O accumulator in TMEM by alpha before its P V.
-//                   At the end the two groups' (m, l) are combined with the two-worker merge,
-//                   then O / l to bf16 and LSE = (m + log2 l) * ln 2.
-//   warps 8, 9      tcgen05.mma, one thread each: warp 8 issues S(j+2) as soon as S(j) has been
-//                   read (two tiles ahead of the softmax), warp 9 issues O += P(j) V(j) as soon
-//                   as P(j) is stored.  One thread
-//                   cannot issue M128 N128 K16 MMAs much faster than the tensor core runs them,
-//                   so two independent issuers keep it fed.  fp32 accumulators.
-//   warps 10, 11    TMA: Q once and the K ring (warp 10), the V ring (warp 11); 128-byte
-//                   swizzle, zero fill past the end of the sequence.
+//                   FFMA), the group's own running sum, P rounded to bf16 into a P buffer.
+//                   While one group computes the exponentials of tile J the other already
+//                   works on tile J+1.  When the reference moves (rare: only beyond 2^8) the
+//                   group scales the O accumulator in TMEM by alpha before its P V.  At the
+//                   end of an item each group leaves its (m, l) for the epilogue.
+//   warps 8, 9      tcgen05.mma, one thread each: warp 8 copies each item's Q into TMEM and
+//                   issues S(J+2) as soon as S(J) has been read (two tiles ahead of the
+//                   softmax), warp 9 issues O += P(J) V(J) as soon as P(J) is stored.  One
+//                   thread cannot issue M128 N128 K16 MMAs much faster than the tensor core
+//                   runs them, so two independent issuers keep it fed.  fp32 accumulators.
+//   warps 10, 11    TMA: the K ring (each item's Q tile, then its K tiles; warp 10) and the V
+//                   ring (warp 11); 128-byte swizzle, zero fill past the end of the sequence.
+//   warps 12-15     epilogue: the two groups' (m, l) combined with the two-worker merge, O read
+//                   from TMEM once the item's last P V is done (the next item's first P V
+//                   waits for that read), O / l to bf16 and LSE = (m + log2 l) * ln 2.
 // Causal: key tiles above the diagonal are never visited; only diagonal and ragged tiles are
 // masked element by element.
 //
@@ -57,62 +60,74 @@ __device__ int g_fa_device_status = 0;
 
 namespace {
 
-constexpr int kBM = 128;       // query rows per tile: one TMEM lane per row
-constexpr int kBN = 128;       // keys per key/value tile
-constexpr int kThreads = 384;  // 12 warps, see the role table above
-constexpr int kMmaWarp = 8;    // issues S = Q K^T (and owns the TMEM allocation)
-constexpr int kMmaPvWarp = 9;  // issues O += P V
-constexpr int kTmaWarp = 10;   // Q and K loads
-constexpr int kTmaVWarp = 11;  // V loads
+constexpr int kBM = 128;        // query rows per tile: one TMEM lane per row
+constexpr int kBN = 128;        // keys per key/value tile
+constexpr int kThreads = 512;   // 16 warps, see the role table above
+constexpr int kMmaWarp = 8;     // issues S = Q K^T (and owns the TMEM allocation)
+constexpr int kMmaPvWarp = 9;   // issues O += P V
+constexpr int kTmaWarp = 10;    // Q and K loads
+constexpr int kTmaVWarp = 11;   // V loads
+constexpr int kEpiWarp0 = 12;   // warps 12-15: epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr int kHalfBytes = 128 * 128;         // one 64-column half of a 128-row bf16 tile
 constexpr uint64_t kDrainNs = 1000000000ull;  // drain waits: at least 1 s
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
-constexpr uint32_t kBarHandOff = 1;  // named barriers 1, 2: reference max of tile j -> j+1
-constexpr uint32_t kBarFinal = 3;    // named barrier 3: the two groups' final (m, l)
-constexpr uint32_t kBarTeardown = 4; // named barrier 4: TMEM no longer used (warps 0-9)
-constexpr uint32_t kTeardownThreads = 320;
+constexpr uint32_t kBarHandOff = 1;  // named barriers 1, 2: reference max of tile J -> J+1
+constexpr uint32_t kBarTeardown = 3; // named barrier 3: TMEM no longer used (warps 0-9, 12-15)
+constexpr uint32_t kTeardownThreads = 448;
+constexpr int kMaxStages = 8;
+constexpr int kFinSlots = 4;         // final (m, l) of the last items, see fin_full
 
+// Counters.  A CTA works through its work items (query tile, head, key range) in order and
+// numbers everything it streams across items: the key tiles J (S buffer J & 1, P buffer
+// J % kP, V ring slot J % stages), the K-ring entries (each non-empty item's Q tile followed by
+// its K tiles), the items it and the non-empty items qi (Q buffer qi % kQ).  Barrier phases
+// follow from these counters, so the pipelines run on from one item into the next.
 struct Bars {
-    uint64_t q_full;      // Q tile landed in shared memory (TMA)
-    uint64_t q_tmem;      // Q copied into TMEM (4 warps)
-    uint64_t k_full[4], k_empty[4];
-    uint64_t v_full[4], v_empty[4];
-    uint64_t s_full[2];   // S buffer b holds S of a tile j with j & 1 == b (tcgen05.commit)
+    uint64_t k_full[kMaxStages], k_empty[kMaxStages];  // K ring (Q tiles and K tiles)
+    uint64_t v_full[kMaxStages], v_empty[kMaxStages];  // V ring
+    uint64_t s_full[2];   // S buffer b holds S of a tile J with J & 1 == b (tcgen05.commit)
     uint64_t s_free[2];   // S buffer b read into registers by its group (4 warps)
     uint64_t p_full[2];   // P buffer b stored, O rescaled if needed (4 warps)
-    // O += P(j) V finished (tcgen05.commit) -> pv_done[j & 3].  A parity wait tells a phase
+    // O += P(J) V finished (tcgen05.commit) -> pv_done[J & 3].  A parity wait tells a phase
     // from the one two completions later only if the waiter is never that far behind: every
-    // wait below is for a P V at most one tile older than one it has already seen complete and
-    // at least one tile older than any that can complete, so four barriers make each wait
-    // exact (see pv_wait).
+    // wait on these is for a P V at most one tile older than one the waiter has already seen
+    // complete and at least one tile older than any that can complete, so four barriers make
+    // each wait exact (see pv_wait).
     uint64_t pv_done[4];
+    uint64_t q_free[2];   // the last S of item qi has read Q buffer qi % kQ (tcgen05.commit)
+    uint64_t o_full;      // every P V of a non-empty item finished (tcgen05.commit)
+    uint64_t o_free;      // O of a non-empty item read by the epilogue (4 warps)
+    // Both softmax groups have written their final (m, l) of item k into fin[k % kFinSlots]
+    // (8 warps); the epilogue has read them (4 warps) and the slot may take item k + kFinSlots.
+    uint64_t fin_full[kFinSlots];
+    uint64_t fin_free[kFinSlots];
     uint64_t mma_done;
     uint64_t mma_pv_done;
     uint32_t tmem_base;
-    float mref[2][kBM];   // reference max of tile j for tile j+1: [j & 1][row]
-    float fin[2][2][kBM]; // each group's final [m, l] per row
+    float mref[2][kBM];                // reference max of tile J for tile J+1: [J & 1][row]
+    float fin[kFinSlots][2][2][kBM];   // [item slot][group][m, l][row]
 };
 
 template <int D>
 struct Cfg {
     static constexpr int kHalves = D / 64;
     static constexpr int kTileBytes = kHalves * kHalfBytes;  // 128 rows x D bf16
-    static constexpr int kStages = D == 128 ? 3 : 4;         // K ring and V ring depth
+    static constexpr int kStages = D == 128 ? 3 : 6;         // K ring and V ring depth
     static constexpr int kK = 0;
     static constexpr int kV = kK + kStages * kTileBytes;
-    // Q is staged in the last V slot: it is copied into TMEM before V of that slot is loaded.
-    static constexpr int kQ = kV + (kStages - 1) * kTileBytes;
     static constexpr int kBars = kV + kStages * kTileBytes;
     static constexpr int kBytes = kBars + static_cast<int>(sizeof(Bars));
     static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
     static constexpr int kP = D == 64 ? 2 : 1;      // P buffers
+    static constexpr int kQ = D == 64 ? 2 : 1;      // Q buffers
     static constexpr uint32_t kTmemS = 0;           // S0, S1: 128 columns each
     static constexpr uint32_t kTmemP = 256;         // P buffers: 64 columns each
     static constexpr uint32_t kTmemO = kTmemP + 64 * kP;
-    static constexpr uint32_t kTmemQ = kTmemO + D;
-    static_assert(kTmemQ + D / 2 <= kTmemCols, "TMEM budget");
+    static constexpr uint32_t kTmemQ = kTmemO + D;  // Q buffers: D/2 columns each
+    static_assert(kTmemQ + kQ * (D / 2) <= kTmemCols, "TMEM budget");
     static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
+    static_assert(kStages <= kMaxStages, "ring depth");
 };
 
 // All 32 lanes wait on the same phase; the outcome is made warp-uniform so that the
@@ -144,18 +159,72 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
 }
 
 // Launch parameters.  The key range of one head is cut into n_splits contiguous ranges of
-// tiles_per_split key tiles; with n_splits == 1 (SPLIT == false) a CTA covers every key and
-// writes the final O (bf16) and LSE, otherwise it writes its range's normalised partial output
-// (fp32) and log-sum-exp to the workspace for the combine kernel.
+// tiles_per_split key tiles; with n_splits == 1 (SPLIT == false) a work item covers every key
+// and writes the final O (bf16) and LSE, otherwise it writes its range's normalised partial
+// output (fp32) and log-sum-exp to the workspace for the combine kernel.
 struct FaParams {
     __nv_bfloat16* O;  // [BH, Nq, D] bf16 (SPLIT == false)
     float* LSE;        // [BH, Nq] or nullptr (SPLIT == false)
     float* ws_O;       // [n_splits, BH, Nq, D] fp32 (SPLIT == true)
     float* ws_LSE;     // [n_splits, BH, Nq] (SPLIT == true)
-    int Nq, Nk, BH, n_qtiles, n_splits, tiles_per_split;
+    int Nq, Nk, BH, n_qtiles, n_splits, tiles_per_split, n_items;
     float scale_log2;
     unsigned long long timeout_ns;
 };
+
+// One work item: a 128-row query tile of one (b, h) against key tiles [kt0, kt0 + n_kv).
+struct Item {
+    int q_tile, bh, split, kt0, n_kv;
+};
+
+// Work item idx of the launch.  Causal runs the longest rows (highest query tiles) first.
+template <bool CAUSAL>
+__device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
+    Item w;
+    const int per_tile = prm.BH * prm.n_splits;
+    if (CAUSAL) {
+        w.q_tile = prm.n_qtiles - 1 - idx / per_tile;
+        w.bh = (idx % per_tile) / prm.n_splits;
+        w.split = idx % prm.n_splits;
+    } else {
+        w.split = idx % prm.n_splits;
+        w.q_tile = (idx / prm.n_splits) % prm.n_qtiles;
+        w.bh = idx / (prm.n_splits * prm.n_qtiles);
+    }
+    // Causal: the queries are the last Nq of the Nk positions, so query row q sees keys
+    // j <= q + Nk - Nq; key tiles wholly past the query tile's last row are skipped.
+    const int n_kv_all = (prm.Nk + kBN - 1) / kBN;
+    w.kt0 = w.split * prm.tiles_per_split;
+    int kt1 = min(n_kv_all, w.kt0 + prm.tiles_per_split);
+    if (CAUSAL) {
+        const long long last_key =
+            static_cast<long long>(w.q_tile) * kBM + kBM - 1 + (prm.Nk - prm.Nq);
+        kt1 = min(static_cast<long long>(kt1), last_key < 0 ? 0 : last_key / kBN + 1);
+    }
+    w.n_kv = max(0, kt1 - w.kt0);
+    return w;
+}
+
+// The k-th work item of this CTA, or -1 past the end.  Items are dealt out in rounds of
+// gridDim.x, alternately forwards and backwards (CTA c takes item c of round 0, item G-1-c of
+// round 1, ...), so that with the longest items first every CTA gets a similar total.
+__device__ __forceinline__ int cta_item(int k, int n_items) {
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    const int idx = k * G + ((k & 1) ? G - 1 - c : c);
+    return idx < n_items ? idx : -1;
+}
+
+// Waits until every phase a producer thread started on a ring has completed: the last entry
+// put into each slot is the last phase of that slot's barrier, so each of these waits ends.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int stages, int issued,
+                                           uint64_t timeout_ns) {
+    const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
+    for (int s = 0; s < stages && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / stages) * stages;
+        mbar_wait(&full[s], (last / stages) & 1, drain_ns);
+    }
+}
 
 template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -164,7 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<D>;
     constexpr int S_ = C::kStages;
     const int Nq = prm.Nq, Nk = prm.Nk;
-    const float scale_log2 = prm.scale_log2;
     const unsigned long long timeout_ns = prm.timeout_ns;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -172,40 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars* bars = reinterpret_cast<Bars*>(smem + C::kBars);
     const uint32_t sK = smem_u32(smem + C::kK);
     const uint32_t sV = smem_u32(smem + C::kV);
-
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work item (query tile, head, key range).  Causal runs the longest rows (highest query
-    // tiles) first.
-    int q_tile, bh, split;
-    {
-        const int idx = static_cast<int>(blockIdx.x);
-        const int per_tile = prm.BH * prm.n_splits;
-        if (CAUSAL) {
-            q_tile = prm.n_qtiles - 1 - idx / per_tile;
-            bh = (idx % per_tile) / prm.n_splits;
-            split = idx % prm.n_splits;
-        } else {
-            split = idx % prm.n_splits;
-            q_tile = (idx / prm.n_splits) % prm.n_qtiles;
-            bh = idx / (prm.n_splits * prm.n_qtiles);
-        }
-    }
-    // Key tiles [kt0, kt0 + n_kv).  Causal: the queries are the last Nq of the Nk positions, so
-    // query row q sees keys j <= q + Nk - Nq; tiles wholly past the tile's last row are skipped.
-    const int n_kv_all = (Nk + kBN - 1) / kBN;
-    const int kt0 = split * prm.tiles_per_split;
-    int kt1 = min(n_kv_all, kt0 + prm.tiles_per_split);
-    if (CAUSAL) {
-        const long long last_key = static_cast<long long>(q_tile) * kBM + kBM - 1 + (Nk - Nq);
-        kt1 = min(static_cast<long long>(kt1), last_key < 0 ? 0 : last_key / kBN + 1);
-    }
-    const int n_kv = max(0, kt1 - kt0);
-
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, 1);
-        mbar_init(&bars->q_tmem, 4);
         for (int s = 0; s < S_; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->k_empty[s], 1);
@@ -216,8 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->s_full[b], 1);
             mbar_init(&bars->s_free[b], 4);
             mbar_init(&bars->p_full[b], 4);
+            mbar_init(&bars->q_free[b], 1);
         }
         for (int b = 0; b < 4; ++b) mbar_init(&bars->pv_done[b], 1);
+        for (int b = 0; b < kFinSlots; ++b) {
+            mbar_init(&bars->fin_full[b], 8);
+            mbar_init(&bars->fin_free[b], 4);
+        }
+        mbar_init(&bars->o_full, 1);
+        mbar_init(&bars->o_free, 4);
         mbar_init(&bars->mma_done, 1);
         mbar_init(&bars->mma_pv_done, 1);
         fence_mbar_init();
@@ -231,98 +276,222 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    // Registers: a softmax thread holds a whole row of 128 scores, the issue and TMA warps
-    // almost nothing: 2 x 128 x 208 + 128 x 80 stays within the 384 x 168 launched.  Each role
-    // branch sets its own limit and never rejoins the others; the TMEM is freed by warp 8 after
-    // a named barrier that the softmax groups and warp 9 arrive at when they are done with it.
-    if (warp >= kMmaWarp) {
-        setmaxnreg_dec<80>();
+    // Registers: a softmax thread holds a whole row of 128 scores, the other warps little:
+    // 2 x 128 x 208 + 128 x 40 + 128 x 56 is the 512 x 128 launched.  Each role branch sets its
+    // own limit and never rejoins the others; the TMEM is freed by warp 8 after a named
+    // barrier that the softmax groups, warp 9 and the epilogue arrive at when done with it.
+    if (warp >= kEpiWarp0) {
+        setmaxnreg_dec<56>();
+        // ------------------------------------------------------------------ epilogue
+        // Per item: the two groups' (m, l) merged with the two-worker merge, O / l read from
+        // TMEM once every P V of the item is done, then O (bf16, or the fp32 partial for the
+        // split-key path) and LSE = (m + log2 l) * ln 2 written out; row r of the tile is TMEM
+        // lane r, one per thread.  An item whose key range is empty (split-key ranges past the
+        // diagonal or past Nk) never ran P V: it writes O = 0 and LSE = -inf.
+        const int r = threadIdx.x & 127;
+        const uint32_t tO = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kTmemO;
+        bool ok = true;
+        int qi = 0;
+        for (int k = 0;; ++k) {
+            const int idx = cta_item(k, prm.n_items);
+            if (idx < 0) break;
+            const Item w = decode_item<CAUSAL>(idx, prm);
+            const int slot = k % kFinSlots;
+            if (!warp_wait(&bars->fin_full[slot], (k / kFinSlots) & 1, timeout_ns)) {
+                record_timeout(12);
+                ok = false;
+                break;
+            }
+            const float m0 = bars->fin[slot][0][0][r], l0 = bars->fin[slot][0][1][r];
+            const float m1 = bars->fin[slot][1][0][r], l1 = bars->fin[slot][1][1][r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->fin_free[slot]);
+            const float M = fmaxf(m0, m1);
+            float lt = 0.f;
+            if (M != -INFINITY)
+                lt = (m0 == -INFINITY ? 0.f : l0 * ex2_approx(m0 - M)) +
+                     (m1 == -INFINITY ? 0.f : l1 * ex2_approx(m1 - M));
+            const bool have = w.n_kv > 0;
+            if (have) {
+                if (!warp_wait(&bars->o_full, qi & 1, timeout_ns)) {
+                    record_timeout(13);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            const int q_row = w.q_tile * kBM + r;
+            const bool store = q_row < Nq;
+            const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+            const size_t row = static_cast<size_t>(w.bh) * Nq + q_row;
+            const size_t ws_row = static_cast<size_t>(w.split) * prm.BH * Nq + row;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (have) {
+                    tmem_ld32_sync(tO + c * 32, o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                // After the last read of O the next item's first P V may overwrite it.
+                if (have && c == D / 32 - 1) warp_arrive_tc(&bars->o_free);
+                if (!store) continue;
+                if (SPLIT) {
+                    float4* dst = reinterpret_cast<float4*>(prm.ws_O + ws_row * D + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l,
+                                             __uint_as_float(o[4 * v + 1]) * inv_l,
+                                             __uint_as_float(o[4 * v + 2]) * inv_l,
+                                             __uint_as_float(o[4 * v + 3]) * inv_l);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(prm.O + row * D + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[8 * v]) * inv_l,
+                                        __uint_as_float(o[8 * v + 1]) * inv_l),
+                            pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l,
+                                        __uint_as_float(o[8 * v + 3]) * inv_l),
+                            pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l,
+                                        __uint_as_float(o[8 * v + 5]) * inv_l),
+                            pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l,
+                                        __uint_as_float(o[8 * v + 7]) * inv_l));
+                }
+            }
+            if (store) {
+                const float lse = have ? (M + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+                if (SPLIT)
+                    prm.ws_LSE[ws_row] = lse;
+                else if (prm.LSE != nullptr)
+                    prm.LSE[row] = lse;
+            }
+            qi += have ? 1 : 0;
+        }
+        (void)ok;
+        tc_fence_before();
+        named_bar_arrive(kBarTeardown, kTeardownThreads);
+    } else if (warp >= kMmaWarp) {
+        setmaxnreg_dec<40>();
         if (warp == kTmaWarp) {
-            // -------------------------------------------------------------------- TMA: Q and K
+            // ------------------------------------------------------ TMA: Q and K tiles, K ring
             if (lane == 0) {
                 tma_prefetch_desc(&tmQ);
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
                 constexpr uint32_t kTx = C::kTileBytes;
-                mbar_arrive_expect_tx(&bars->q_full, kTx);
-                for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(smem + C::kQ + h * kHalfBytes, &tmQ, &bars->q_full, h * 64,
-                                q_tile * kBM, bh);
-                int k_issued = 0;
-                for (int j = 0; j < n_kv; ++j) {
-                    const int s = j % S_;
-                    if (j >= S_ && !mbar_wait(&bars->k_empty[s], ((j / S_) - 1) & 1, timeout_ns)) {
-                        record_timeout(1);
-                        break;
+                int e = 0;  // K-ring entries issued
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int idx = cta_item(k, prm.n_items);
+                    if (idx < 0) break;
+                    const Item w = decode_item<CAUSAL>(idx, prm);
+                    // t = -1: the item's Q tile, then its key tiles.
+                    for (int t = w.n_kv > 0 ? -1 : 0; t < w.n_kv; ++t, ++e) {
+                        const int s = e % S_;
+                        if (e >= S_ &&
+                            !mbar_wait(&bars->k_empty[s], ((e / S_) - 1) & 1, timeout_ns)) {
+                            record_timeout(1);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars->k_full[s], kTx);
+                        const CUtensorMap* map = t < 0 ? &tmQ : &tmK;
+                        const int row = t < 0 ? w.q_tile * kBM : (w.kt0 + t) * kBN;
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, map,
+                                        &bars->k_full[s], h * 64, row, w.bh);
                     }
-                    mbar_arrive_expect_tx(&bars->k_full[s], kTx);
-                    for (int h = 0; h < C::kHalves; ++h)
-                        tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, &tmK,
-                                    &bars->k_full[s], h * 64, (kt0 + j) * kBN, bh);
-                    k_issued = j + 1;
                 }
-                // Drain: every load this thread issued has landed before the CTA may exit.  The
-                // last load into a stage is the last phase of that stage's barrier, so it ends.
-                const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
-                mbar_wait(&bars->q_full, 0, drain_ns);
-                for (int s = 0; s < S_ && s < k_issued; ++s) {
-                    const int jl = s + ((k_issued - 1 - s) / S_) * S_;
-                    mbar_wait(&bars->k_full[s], (jl / S_) & 1, drain_ns);
-                }
+                drain_ring(bars->k_full, S_, e, timeout_ns);
             }
         } else if (warp == kTmaVWarp) {
-            // -------------------------------------------------------------------- TMA: V ring
+            // ------------------------------------------------------ TMA: V tiles, V ring
             if (lane == 0) {
                 constexpr uint32_t kTx = C::kTileBytes;
-                int v_issued = 0;
-                for (int j = 0; j < n_kv; ++j) {
-                    const int s = j % S_;
-                    // The last slot holds the staged Q until it has been copied into TMEM.
-                    if (j == S_ - 1 && !mbar_wait(&bars->q_tmem, 0, timeout_ns)) {
-                        record_timeout(13);
-                        break;
+                int J = 0;  // V tiles issued
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int idx = cta_item(k, prm.n_items);
+                    if (idx < 0) break;
+                    const Item w = decode_item<CAUSAL>(idx, prm);
+                    for (int t = 0; t < w.n_kv; ++t, ++J) {
+                        const int s = J % S_;
+                        if (J >= S_ &&
+                            !mbar_wait(&bars->v_empty[s], ((J / S_) - 1) & 1, timeout_ns)) {
+                            record_timeout(2);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars->v_full[s], kTx);
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
+                                        &bars->v_full[s], h * 64, (w.kt0 + t) * kBN, w.bh);
                     }
-                    if (j >= S_ && !mbar_wait(&bars->v_empty[s], ((j / S_) - 1) & 1, timeout_ns)) {
-                        record_timeout(2);
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&bars->v_full[s], kTx);
-                    for (int h = 0; h < C::kHalves; ++h)
-                        tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
-                                    &bars->v_full[s], h * 64, (kt0 + j) * kBN, bh);
-                    v_issued = j + 1;
                 }
-                const uint64_t drain_ns = timeout_ns > kDrainNs ? timeout_ns : kDrainNs;
-                for (int s = 0; s < S_ && s < v_issued; ++s) {
-                    const int jl = s + ((v_issued - 1 - s) / S_) * S_;
-                    mbar_wait(&bars->v_full[s], (jl / S_) & 1, drain_ns);
-                }
+                drain_ring(bars->v_full, S_, J, timeout_ns);
             }
         } else if (warp == kMmaWarp) {
-            // -------------------------------------------------------------------- MMA: S = Q K^T
+            // ------------------------------------------------------ MMA: S = Q K^T
             if (lane == 0) {
                 constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0);
-                bool ok = mbar_wait(&bars->q_tmem, 0, timeout_ns);
-                if (!ok) record_timeout(3);
-                for (int j = 0; ok && j < n_kv; ++j) {
-                    // S(j) overwrites S(j-2): its group must have read it.
-                    const int s = j % S_;
-                    const int b = j & 1;
-                    if ((j >= 2 && !mbar_wait(&bars->s_free[b], ((j >> 1) - 1) & 1, timeout_ns)) ||
-                        !mbar_wait(&bars->k_full[s], (j / S_) & 1, timeout_ns)) {
-                        record_timeout(5);
+                int e = 0, J = 0, qi = 0;
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int idx = cta_item(k, prm.n_items);
+                    if (idx < 0) break;
+                    const Item w = decode_item<CAUSAL>(idx, prm);
+                    if (w.n_kv == 0) continue;
+                    // The item's Q tile: K ring -> Q buffer qb in TMEM (tcgen05.cp, ordered
+                    // before the MMAs below), once the S of item qi - kQ, the buffer's
+                    // previous reader, has finished.
+                    const int qb = qi % C::kQ;
+                    const uint32_t tQ = tmem + C::kTmemQ + qb * (D / 2);
+                    int s = e % S_;
+                    if ((qi >= C::kQ &&
+                         !mbar_wait(&bars->q_free[qb], ((qi - C::kQ) / C::kQ) & 1, timeout_ns)) ||
+                        !mbar_wait(&bars->k_full[s], (e / S_) & 1, timeout_ns)) {
+                        record_timeout(3);
+                        ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kb = sK + s * C::kTileBytes;
-    #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        umma_ts(tmem + C::kTmemS + b * 128, tmem + C::kTmemQ + kk * 8,
-                                smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    {
+                        const uint32_t qs = sK + s * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            tmem_cp_128x256b(tQ + kk * 8,
+                                             smem_desc_sw128(qs + (kk >> 2) * kHalfBytes +
+                                                                 (kk & 3) * 32,
+                                                             16, 1024));
                     }
-                    umma_commit(&bars->s_full[b]);
                     umma_commit(&bars->k_empty[s]);
+                    ++e;
+                    for (int t = 0; t < w.n_kv; ++t, ++J, ++e) {
+                        // S(J) overwrites S(J-2): its group must have read it.
+                        s = e % S_;
+                        const int b = J & 1;
+                        if ((J >= 2 &&
+                             !mbar_wait(&bars->s_free[b], ((J >> 1) - 1) & 1, timeout_ns)) ||
+                            !mbar_wait(&bars->k_full[s], (e / S_) & 1, timeout_ns)) {
+                            record_timeout(5);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t kb = sK + s * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                            umma_ts(tmem + C::kTmemS + b * 128, tQ + kk * 8,
+                                    smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&bars->s_full[b]);
+                        umma_commit(&bars->k_empty[s]);
+                    }
+                    if (ok) umma_commit(&bars->q_free[qb]);
+                    ++qi;
                 }
                 // Drain: no MMA of this thread may still write TMEM when it is freed.
                 umma_commit(&bars->mma_done);
@@ -333,27 +502,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             tmem_dealloc(tmem, kTmemCols);
         } else if (warp == kMmaPvWarp) {
-            // -------------------------------------------------------------------- MMA: O += P V
+            // ------------------------------------------------------ MMA: O += P V
             if (lane == 0) {
                 constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 1);
-                for (int j = 0; j < n_kv; ++j) {
-                    const int s = j % S_;
-                    const int b = j % C::kP;
-                    if (!mbar_wait(&bars->v_full[s], (j / S_) & 1, timeout_ns) ||
-                        !mbar_wait(&bars->p_full[b], (j / C::kP) & 1, timeout_ns)) {
-                        record_timeout(6);
+                int J = 0, qi = 0;
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int idx = cta_item(k, prm.n_items);
+                    if (idx < 0) break;
+                    const Item w = decode_item<CAUSAL>(idx, prm);
+                    if (w.n_kv == 0) continue;
+                    // The first P V of an item overwrites O: the epilogue must have read the
+                    // previous item's.
+                    if (qi >= 1 && !mbar_wait(&bars->o_free, (qi - 1) & 1, timeout_ns)) {
+                        record_timeout(11);
+                        ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t vb = sV + s * C::kTileBytes;
-                    const uint32_t pb = tmem + C::kTmemP + b * 64;
-    #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        umma_ts(tmem + C::kTmemO, pb + kk * 8,
-                                smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idO,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&bars->pv_done[j & 3]);
-                    umma_commit(&bars->v_empty[s]);
+                    for (int t = 0; t < w.n_kv; ++t, ++J) {
+                        const int s = J % S_;
+                        const int b = J % C::kP;
+                        if (!mbar_wait(&bars->v_full[s], (J / S_) & 1, timeout_ns) ||
+                            !mbar_wait(&bars->p_full[b], (J / C::kP) & 1, timeout_ns)) {
+                            record_timeout(6);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t vb = sV + s * C::kTileBytes;
+                        const uint32_t pb = tmem + C::kTmemP + b * 64;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            umma_ts(tmem + C::kTmemO, pb + kk * 8,
+                                    smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idO,
+                                    (t > 0 || kk > 0) ? 1u : 0u);
+                        umma_commit(&bars->pv_done[J & 3]);
+                        umma_commit(&bars->v_empty[s]);
+                    }
+                    if (ok) umma_commit(&bars->o_full);  // every P V of the item, for the epilogue
+                    ++qi;
                 }
                 umma_commit(&bars->mma_pv_done);
                 mbar_wait(&bars->mma_pv_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
@@ -365,221 +552,160 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         setmaxnreg_inc<208>();
         // -------------------------------------------------------------------- softmax
-        const int g = warp >> 2;          // this group takes the key tiles j = g, g+2, ...
+        const int g = warp >> 2;          // this group takes the key tiles J with J & 1 == g
         const int r = threadIdx.x & 127;  // row in the tile == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const int q_row = q_tile * kBM + r;
-        const int key_limit = CAUSAL ? min(Nk - 1, q_row + (Nk - Nq)) : Nk - 1;  // last allowed
         const uint32_t tS = tmem + lane_addr + C::kTmemS + g * 128;
         const uint32_t tO = tmem + lane_addr + C::kTmemO;
-        bool ok = true;
-
-        if (g == 0) {
-            // Q row r: shared memory (128-byte swizzled, as TMA wrote it) -> TMEM lane r.
-            if (!warp_wait(&bars->q_full, 0, timeout_ns)) {
-                record_timeout(7);
-                ok = false;
-            } else {
-                const uint8_t* qs = smem + C::kQ;
-#pragma unroll
-                for (int hh = 0; hh < C::kHalves; ++hh) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(
-                            qs + hh * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4));
-                        w[4 * c] = v.x;
-                        w[4 * c + 1] = v.y;
-                        w[4 * c + 2] = v.z;
-                        w[4 * c + 3] = v.w;
-                    }
-                    tmem_st32_sync(tmem + lane_addr + C::kTmemQ + hh * 32, w);
-                }
-                // The staged Q slot is refilled by TMA (async proxy) after this arrival.
-                fence_proxy_async_smem();
-            }
-            warp_arrive_tc(&bars->q_tmem);
+        const float scale_log2 = prm.scale_log2;
+        // Key tiles of this CTA over all its items: the hand-off of the reference max runs
+        // through all of them (a tile that starts an item ignores what it receives), so that
+        // every tile J >= 1 passes its consumer barrier and the groups stay in step.
+        int J_total = 0;
+        for (int k = 0;; ++k) {
+            const int idx = cta_item(k, prm.n_items);
+            if (idx < 0) break;
+            J_total += decode_item<CAUSAL>(idx, prm).n_kv;
         }
-
-        float m_last = -INFINITY;  // reference max this group used last (log2 units, scaled)
-        float l = 0.f;             // this group's running sum of 2^(t - m_last) over its tiles
-        // Hand-off barrier passes of this group, in order: for each of its tiles j, a consumer
-        // pass (bar.sync) when j >= 1 and a producer pass (bar.arrive) when j + 1 < n_kv.  A
-        // group that stops early because a wait gave up makes up the missing passes below.
-        int j = g;
-        int stage = 0;  // 0: before tile j's consumer pass, 1: before its producer pass
-        for (; ok && j < n_kv; j += 2, stage = 0) {
-            if (!warp_wait(&bars->s_full[g], (j >> 1) & 1, timeout_ns)) {
-                record_timeout(8);
-                ok = false;
-                break;
+        bool ok = true;
+        int J0 = 0;  // first key tile of the item
+        for (int k = 0;; ++k) {
+            const int idx = cta_item(k, prm.n_items);
+            if (idx < 0) break;
+            int n, kt0, key_limit;
+            {
+                const Item w = decode_item<CAUSAL>(idx, prm);
+                n = w.n_kv;
+                kt0 = w.kt0;
+                const int q_row = w.q_tile * kBM + r;
+                key_limit = CAUSAL ? min(Nk - 1, q_row + (Nk - Nq)) : Nk - 1;
             }
-            tc_fence_after();
-            uint32_t sr[128];
-            tmem_ld128_sync(tS, sr);
-            warp_arrive_tc(&bars->s_free[g]);  // S(j) is in registers: S(j+2) may overwrite it
-            const int kv0 = (kt0 + j) * kBN;
-            if (kv0 + kBN - 1 > key_limit) {
-#pragma unroll
-                for (int e = 0; e < 128; ++e)
-                    if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
-            }
-            float mx8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(sr[u]);
-#pragma unroll
-            for (int e = 8; e < 128; e += 2)
-                mx8[(e >> 1) & 7] =
-                    fmax3(mx8[(e >> 1) & 7], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                   fmaxf(mx8[6], mx8[7])) *
-                             scale_log2;
-            // Reference max after tile j-1 (the other group's), handed over per row.
-            float m_prev = -INFINITY;
-            if (j >= 1) {
-                named_bar_sync(kBarHandOff + ((j - 1) & 1), 256);
-                m_prev = bars->mref[(j - 1) & 1][r];
-            }
-            stage = 1;
-            // Move the reference only when this tile's max exceeds it by more than the
-            // threshold (always on the first finite tile: -inf gives +inf > threshold).
-            const float m_new = (mx - m_prev > kRescaleThreshold) ? mx : m_prev;
-            if (j + 1 < n_kv) {
-                bars->mref[j & 1][r] = m_new;
-                named_bar_arrive(kBarHandOff + (j & 1), 256);
-            }
-            stage = 2;
-            // O (after P(j-1) V) is relative to m_prev; this group's l to m_last.
-            const float alpha_o = (m_new == m_prev) ? 1.f : ex2_approx(m_prev - m_new);
-            const float alpha_l = (m_new == m_last) ? 1.f : ex2_approx(m_last - m_new);
-            // Nothing allowed yet (m_new = -inf): shift by 0 so every term is exp(-inf) = 0.
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            uint32_t p[64];
-            float2 rs = make_float2(0.f, 0.f), rs2 = make_float2(0.f, 0.f);
-            const float2 c2 = make_float2(scale_log2, scale_log2);
-            const float2 nm2 = make_float2(-m_use, -m_use);
-#pragma unroll
-            for (int e = 0; e < 128; e += 4) {
-                float2 t0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                  c2, nm2);
-                float2 t1 = ffma2(
-                    make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
-                t0.x = ex2_approx(t0.x);
-                t0.y = ex2_approx(t0.y);
-                t1.x = ex2_approx(t1.x);
-                t1.y = ex2_approx(t1.y);
-                rs = fadd2(rs, t0);
-                rs2 = fadd2(rs2, t1);
-                p[e >> 1] = pack_bf16x2(t0.x, t0.y);
-                p[(e >> 1) + 1] = pack_bf16x2(t1.x, t1.y);
-            }
-            l = l * alpha_l + ((rs.x + rs.y) + (rs2.x + rs2.y));
-            m_last = m_new;
-            // P buffer pb was last read by P(j - kP) V.
-            const int pb = j % C::kP;
-            if (j >= C::kP && !pv_wait(bars, j - C::kP, timeout_ns)) {
-                record_timeout(9);
-                ok = false;
-                break;
-            }
-            // The reference moved: O must be rescaled after P(j-1) V and before P(j) V.
-            if (j >= 1 && __any_sync(0xffffffffu, alpha_o != 1.f)) {
-                if (!pv_wait(bars, j - 1, timeout_ns)) {
-                    record_timeout(14);
+            float m_last = -INFINITY;  // reference max this group used last (scaled, log2)
+            float l = 0.f;             // this group's sum of 2^(t - m_last) over its tiles
+            // Hand-off barrier passes of this group, in order: for each of its tiles J, a
+            // consumer pass (bar.sync) when J >= 1 and a producer pass (bar.arrive) when
+            // J + 1 < J_total.  A group that stops early because a wait gave up makes up the
+            // missing passes after the loop.
+            int J = J0 + ((J0 & 1) != g ? 1 : 0);
+            int stage = 0;  // 0: before tile J's consumer pass, 1: before its producer pass
+            for (; ok && J < J0 + n; J += 2, stage = 0) {
+                const int t = J - J0;  // tile within the item
+                if (!warp_wait(&bars->s_full[g], (J >> 1) & 1, timeout_ns)) {
+                    record_timeout(8);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                uint32_t sr[128];
+                tmem_ld128_sync(tS, sr);
+                warp_arrive_tc(&bars->s_free[g]);  // S(J) is in registers: S(J+2) may go there
+                const int kv0 = (kt0 + t) * kBN;
+                if (kv0 + kBN - 1 > key_limit) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32_sync(tO + c * 32, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_o);
-                    tmem_st32_sync(tO + c * 32, o);
+                    for (int e = 0; e < 128; ++e)
+                        if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
                 }
-            }
-            tc_fence_after();
-            tmem_st64_sync(tmem + lane_addr + C::kTmemP + pb * 64, p);
-            warp_arrive_tc(&bars->p_full[pb]);
-        }
-        // Make up the hand-off passes a stop left out, in the same order.
-        for (; j < n_kv; j += 2, stage = 0) {
-            if (stage == 0 && j >= 1) named_bar_sync(kBarHandOff + ((j - 1) & 1), 256);
-            if (stage <= 1 && j + 1 < n_kv) named_bar_arrive(kBarHandOff + (j & 1), 256);
-        }
-        // Wait for the last P V, then combine the two groups' (m, l) with the two-worker merge.
-        if (ok && n_kv > 0 &&
-            !pv_wait(bars, n_kv - 1, timeout_ns)) {
-            record_timeout(10);
-            ok = false;
-        }
-        tc_fence_after();
-        bars->fin[g][0][r] = m_last;
-        bars->fin[g][1][r] = l;
-        named_bar_sync(kBarFinal, 256);
-        const float mo = bars->fin[g ^ 1][0][r];
-        const float lo = bars->fin[g ^ 1][1][r];
-        const float M = fmaxf(m_last, mo);
-        float lt = 0.f;
-        if (M != -INFINITY) {
-            lt = (m_last == -INFINITY ? 0.f : l * ex2_approx(m_last - M)) +
-                 (mo == -INFINITY ? 0.f : lo * ex2_approx(mo - M));
-        }
-        if (ok) {
-            // Epilogue: this thread writes columns [g*D/2, (g+1)*D/2) of row q_row.  A CTA whose
-            // key range is empty (n_kv == 0: split-key CTAs past the diagonal or past Nk) never
-            // ran P V, so it writes the empty state O = 0, LSE = -inf without reading TMEM.
-            const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-            const bool store = q_row < Nq;
-            const bool have = n_kv > 0;
-            const float lse = have ? (M + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
-            const size_t row = static_cast<size_t>(bh) * Nq + q_row;
-            const uint32_t tOh = tO + g * (D / 2);
+                float mx8[8];
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t o[32];
-                if (have) {
-                    tmem_ld32_sync(tOh + c * 32, o);
-                } else {
+                for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(sr[u]);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                for (int e = 8; e < 128; e += 2)
+                    mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(sr[e]),
+                                              __uint_as_float(sr[e + 1]));
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]),
+                                       fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) *
+                                 scale_log2;
+                // Reference max after tile J-1 (the other group's), handed over per row; the
+                // first tile of an item starts from -inf.
+                float m_prev = -INFINITY;
+                if (J >= 1) {
+                    named_bar_sync(kBarHandOff + ((J - 1) & 1), 256);
+                    if (t >= 1) m_prev = bars->mref[(J - 1) & 1][r];
                 }
-                if (SPLIT) {
-                    const size_t ws_row = static_cast<size_t>(split) * prm.BH * Nq + row;
-                    float* orow = prm.ws_O + ws_row * D + g * (D / 2);
-                    if (store) {
-                        float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+                stage = 1;
+                // Move the reference only when this tile's max exceeds it by more than the
+                // threshold (always on the first finite tile: -inf gives +inf > threshold).
+                const float m_new = (mx - m_prev > kRescaleThreshold) ? mx : m_prev;
+                if (J + 1 < J_total) {
+                    bars->mref[J & 1][r] = m_new;
+                    named_bar_arrive(kBarHandOff + (J & 1), 256);
+                }
+                stage = 2;
+                // O (after P(J-1) V) is relative to m_prev; this group's l to m_last.
+                const float alpha_o = (m_new == m_prev) ? 1.f : ex2_approx(m_prev - m_new);
+                const float alpha_l = (m_new == m_last) ? 1.f : ex2_approx(m_last - m_new);
+                // Nothing allowed yet (m_new = -inf): shift by 0 so every term is exp(-inf) = 0.
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                uint32_t p[64];
+                float2 rs = make_float2(0.f, 0.f), rs2 = make_float2(0.f, 0.f);
+                const float2 c2 = make_float2(scale_log2, scale_log2);
+                const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l,
-                                                 __uint_as_float(o[4 * v + 1]) * inv_l,
-                                                 __uint_as_float(o[4 * v + 2]) * inv_l,
-                                                 __uint_as_float(o[4 * v + 3]) * inv_l);
+                for (int e = 0; e < 128; e += 4) {
+                    float2 t0 = ffma2(
+                        make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
+                    float2 t1 = ffma2(
+                        make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2,
+                        nm2);
+                    t0.x = ex2_approx(t0.x);
+                    t0.y = ex2_approx(t0.y);
+                    t1.x = ex2_approx(t1.x);
+                    t1.y = ex2_approx(t1.y);
+                    rs = fadd2(rs, t0);
+                    rs2 = fadd2(rs2, t1);
+                    p[e >> 1] = pack_bf16x2(t0.x, t0.y);
+                    p[(e >> 1) + 1] = pack_bf16x2(t1.x, t1.y);
+                }
+                l = l * alpha_l + ((rs.x + rs.y) + (rs2.x + rs2.y));
+                m_last = m_new;
+                // P buffer pb was last read by P(J - kP) V.
+                const int pb = J % C::kP;
+                if (J >= C::kP && !pv_wait(bars, J - C::kP, timeout_ns)) {
+                    record_timeout(9);
+                    ok = false;
+                    break;
+                }
+                // The reference moved: O must be rescaled after P(J-1) V and before P(J) V.
+                if (t >= 1 && __any_sync(0xffffffffu, alpha_o != 1.f)) {
+                    if (!pv_wait(bars, J - 1, timeout_ns)) {
+                        record_timeout(14);
+                        ok = false;
+                        break;
                     }
-                } else {
-                    uint32_t pk[16];
+                    tc_fence_after();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
-                                            __uint_as_float(o[2 * e + 1]) * inv_l);
-                    if (store) {
-                        uint4* dst =
-                            reinterpret_cast<uint4*>(prm.O + row * D + g * (D / 2) + c * 32);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32_sync(tO + c * 32, o);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] =
-                                make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_o);
+                        tmem_st32_sync(tO + c * 32, o);
                     }
                 }
+                tc_fence_after();
+                tmem_st64_sync(tmem + lane_addr + C::kTmemP + pb * 64, p);
+                warp_arrive_tc(&bars->p_full[pb]);
             }
-            if (store && g == 0) {
-                if (SPLIT)
-                    prm.ws_LSE[static_cast<size_t>(split) * prm.BH * Nq + row] = lse;
-                else if (prm.LSE != nullptr)
-                    prm.LSE[row] = lse;
+            // Make up the hand-off passes a stop left out, in the same order.
+            for (; J < J0 + n; J += 2, stage = 0) {
+                if (stage == 0 && J >= 1) named_bar_sync(kBarHandOff + ((J - 1) & 1), 256);
+                if (stage <= 1 && J + 1 < J_total)
+                    named_bar_arrive(kBarHandOff + (J & 1), 256);
             }
+            // This group's (m, l) of the item for the epilogue, once it has read the slot's
+            // previous item.
+            const int slot = k % kFinSlots;
+            if (ok && k >= kFinSlots &&
+                !warp_wait(&bars->fin_free[slot], ((k / kFinSlots) - 1) & 1, timeout_ns)) {
+                record_timeout(16);
+                ok = false;
+            }
+            bars->fin[slot][g][0][r] = m_last;
+            bars->fin[slot][g][1][r] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->fin_full[slot]);
+            J0 += n;
         }
         tc_fence_before();
         named_bar_arrive(kBarTeardown, kTeardownThreads);
@@ -665,10 +791,17 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
     });
     if (attr_err != cudaSuccess) return FA_ERR_CUDA;
-    const long long ctas = static_cast<long long>(prm.n_qtiles) * prm.BH * prm.n_splits;
-    if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const long long items = static_cast<long long>(prm.n_qtiles) * prm.BH * prm.n_splits;
+    if (items > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    if (items == 0) return FA_OK;
+    // Persistent: one CTA per SM (the shared memory and TMEM allow no more), each taking every
+    // gridDim.x-th work item.
+    FaParams p = prm;
+    p.n_items = static_cast<int>(items);
+    const int sms = device_sm_count();
+    const long long ctas = (sms > 0 && items > sms) ? sms : items;
     fa_fwd_kernel<D, CAUSAL, SPLIT>
-        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, prm);
+        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -156,6 +156,14 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         : "memory");
 }
 
+// Asynchronous copy of a 128-row x 256-bit matrix from shared memory (described by a matrix
+// descriptor, like an MMA operand) into TMEM lanes 0-127, 8 columns from `taddr`.  Ordered
+// before the tcgen05.mma instructions that the same thread issues after it.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc)
+                 : "memory");
+}
+
 // Arrives once on `bar` when all tcgen05 async operations issued so far by this thread end.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile(
