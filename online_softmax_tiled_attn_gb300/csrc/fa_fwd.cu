@@ -480,13 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
+                        // B_k: the K tile's 16-element slice k (32 bytes apart within each
+                        // 64-column half of the K-major, 128-byte swizzled tile).
                         const uint32_t kb = sK + s * C::kTileBytes;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                            umma_ts(tmem + C::kTmemS + b * 128, tQ + kk * 8,
-                                    smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
-                        }
+                        for (int h = 0; h < C::kHalves; ++h)
+                            umma_ts_x4(tmem + C::kTmemS + b * 128, tQ + h * 32,
+                                       smem_desc_sw128(kb + h * kHalfBytes, 16, 1024), 32 / 16,
+                                       idS, h > 0 ? 1u : 0u);
                         umma_commit(&bars->s_full[b]);
                         umma_commit(&bars->k_empty[s]);
                     }
@@ -506,6 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 1);
                 int J = 0, qi = 0;
+                int vs = 0, vph = 0;  // V ring slot of tile J and its phase
+                int pb = 0, pph = 0;  // P buffer of tile J and its phase
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
@@ -520,24 +523,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     for (int t = 0; t < w.n_kv; ++t, ++J) {
-                        const int s = J % S_;
-                        const int b = J % C::kP;
-                        if (!mbar_wait(&bars->v_full[s], (J / S_) & 1, timeout_ns) ||
-                            !mbar_wait(&bars->p_full[b], (J / C::kP) & 1, timeout_ns)) {
+                        // P is what the tile usually waits for; V has landed long before.
+                        if (!mbar_wait(&bars->p_full[pb], pph, timeout_ns) ||
+                            !mbar_wait(&bars->v_full[vs], vph, timeout_ns)) {
                             record_timeout(6);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t vb = sV + s * C::kTileBytes;
-                        const uint32_t pb = tmem + C::kTmemP + b * 64;
-#pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk)
-                            umma_ts(tmem + C::kTmemO, pb + kk * 8,
-                                    smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idO,
-                                    (t > 0 || kk > 0) ? 1u : 0u);
+                        // B_k: rows 16k..16k+15 of the V tile (MN-major), 2048 bytes apart.
+                        umma_ts_x8(tmem + C::kTmemO, tmem + C::kTmemP + pb * 64,
+                                   smem_desc_sw128(sV + vs * C::kTileBytes, kHalfBytes, 1024),
+                                   2048 / 16, idO, t > 0 ? 1u : 0u);
                         umma_commit(&bars->pv_done[J & 3]);
-                        umma_commit(&bars->v_empty[s]);
+                        umma_commit(&bars->v_empty[vs]);
+                        if (++vs == S_) { vs = 0; vph ^= 1; }
+                        if (++pb == C::kP) { pb = 0; pph ^= 1; }
                     }
                     if (ok) umma_commit(&bars->o_full);  // every P V of the item, for the epilogue
                     ++qi;
@@ -605,16 +606,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 128; ++e)
                         if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
                 }
-                float mx8[8];
+                // Row max with two-input max.f32: on this GPU the three-input form issues far
+                // more slowly and holds back the exponentials that follow.
+                float m16[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(sr[u]);
+                for (int u = 0; u < 16; ++u) m16[u] = __uint_as_float(sr[u]);
 #pragma unroll
-                for (int e = 8; e < 128; e += 2)
-                    mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(sr[e]),
-                                              __uint_as_float(sr[e + 1]));
-                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]),
-                                       fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) *
-                                 scale_log2;
+                for (int e = 16; e < 128; ++e) m16[e & 15] = fmaxf(m16[e & 15], __uint_as_float(sr[e]));
+#pragma unroll
+                for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int u = 0; u < w; ++u) m16[u] = fmaxf(m16[u], m16[u + w]);
+                const float mx = m16[0] * scale_log2;
                 // Reference max after tile J-1 (the other group's), handed over per row; the
                 // first tile of an item starts from -inf.
                 float m_prev = -INFINITY;

@@ -156,6 +156,57 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         : "memory");
 }
 
+// Eight back-to-back TS MMAs D += A_k B_k (k = 0..7) in one statement, so that the issuing
+// thread spends as few instructions as possible between them: A_k at TMEM column a_tmem + 8k
+// (16 bf16 values per row), B_k described by b_desc with its start address advanced by
+// b_step16 x 16 bytes per k.  The first MMA overwrites D when `accumulate` is 0.
+__device__ __forceinline__ void umma_ts_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t b_step16, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t.reg .b64 st;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 q, %5, %5;\n\t"
+        "cvt.u64.u32 st, %3;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(b_step16), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Four back-to-back TS MMAs, as umma_ts_x8.
+__device__ __forceinline__ void umma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t b_step16, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t.reg .b64 st;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 q, %5, %5;\n\t"
+        "cvt.u64.u32 st, %3;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(b_step16), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Asynchronous copy of a 128-row x 256-bit matrix from shared memory (described by a matrix
 // descriptor, like an MMA operand) into TMEM lanes 0-127, 8 columns from `taddr`.  Ordered
 // before the tcgen05.mma instructions that the same thread issues after it.
