@@ -132,8 +132,9 @@ struct Cfg {
 
 // All 32 lanes wait on the same phase; the outcome is made warp-uniform so that the
 // .sync.aligned tcgen05 instructions that follow are never reached by a partial warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-    const bool ok = mbar_wait(bar, parity, timeout_ns);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                          bool suspend = false) {
+    const bool ok = mbar_wait(bar, parity, timeout_ns, suspend);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (idx < 0) break;
             const Item w = decode_item<CAUSAL>(idx, prm);
             const int slot = k % kFinSlots;
-            if (!warp_wait(&bars->fin_full[slot], (k / kFinSlots) & 1, timeout_ns)) {
+            if (!warp_wait(&bars->fin_full[slot], (k / kFinSlots) & 1, timeout_ns, true)) {
                 record_timeout(12);
                 ok = false;
                 break;
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (m1 == -INFINITY ? 0.f : l1 * ex2_approx(m1 - M));
             const bool have = w.n_kv > 0;
             if (have) {
-                if (!warp_wait(&bars->o_full, qi & 1, timeout_ns)) {
+                if (!warp_wait(&bars->o_full, qi & 1, timeout_ns, true)) {
                     record_timeout(13);
                     ok = false;
                     break;
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = w.n_kv > 0 ? -1 : 0; t < w.n_kv; ++t, ++e) {
                         const int s = e % S_;
                         if (e >= S_ &&
-                            !mbar_wait(&bars->k_empty[s], ((e / S_) - 1) & 1, timeout_ns)) {
+                            !mbar_wait(&bars->k_empty[s], ((e / S_) - 1) & 1, timeout_ns, true)) {
                             record_timeout(1);
                             ok = false;
                             break;
@@ -419,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < w.n_kv; ++t, ++J) {
                         const int s = J % S_;
                         if (J >= S_ &&
-                            !mbar_wait(&bars->v_empty[s], ((J / S_) - 1) & 1, timeout_ns)) {
+                            !mbar_wait(&bars->v_empty[s], ((J / S_) - 1) & 1, timeout_ns, true)) {
                             record_timeout(2);
                             ok = false;
                             break;
@@ -612,7 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 16; ++u) m16[u] = __uint_as_float(sr[u]);
 #pragma unroll
-                for (int e = 16; e < 128; ++e) m16[e & 15] = fmaxf(m16[e & 15], __uint_as_float(sr[e]));
+                for (int e = 16; e < 128; ++e)
+                    m16[e & 15] = fmaxf(m16[e & 15], __uint_as_float(sr[e]));
 #pragma unroll
                 for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll

@@ -56,14 +56,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended until the phase completes or about
+// `suspend_ns` nanoseconds have passed, instead of returning at once: waiting threads then
+// take no issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if `timeout_ns`
-// elapsed first (the caller then records an error and stops).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+// elapsed first (the caller then records an error and stops).  Waits on the critical path
+// poll; the others (`suspend`) let the thread sleep between polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                          bool suspend = false) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u && globaltimer_ns() - t0 > timeout_ns) return false;
+        if (suspend ? mbar_try_wait_suspend(bar, parity, 100000u) : mbar_try_wait(bar, parity))
+            return true;
+        if ((suspend || (it & 63u) == 63u) && globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }
 
