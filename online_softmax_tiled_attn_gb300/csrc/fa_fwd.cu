@@ -169,6 +169,7 @@ struct FaParams {
     float* ws_O;       // [n_splits, BH, Nq, D] fp32 (SPLIT == true)
     float* ws_LSE;     // [n_splits, BH, Nq] (SPLIT == true)
     int Nq, Nk, BH, n_qtiles, n_splits, tiles_per_split, n_items;
+    int head_group;  // causal: heads whose items are interleaved (their K, V share the L2)
     float scale_log2;
     unsigned long long timeout_ns;
 };
@@ -178,15 +179,22 @@ struct Item {
     int q_tile, bh, split, kt0, n_kv;
 };
 
-// Work item idx of the launch.  Causal runs the longest rows (highest query tiles) first.
+// Work item idx of the launch.  Non-causal items go head by head, so the CTAs running at one
+// time share the K and V of a few heads.  Causal items go in groups of head_group heads (as
+// many as keep their K and V in L2 together), and within a group the longest rows (highest
+// query tiles) first, so that the CTAs' shares even out.
 template <bool CAUSAL>
 __device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
     Item w;
-    const int per_tile = prm.BH * prm.n_splits;
     if (CAUSAL) {
-        w.q_tile = prm.n_qtiles - 1 - idx / per_tile;
-        w.bh = (idx % per_tile) / prm.n_splits;
-        w.split = idx % prm.n_splits;
+        const int per_head = prm.n_qtiles * prm.n_splits;
+        const int group = idx / (prm.head_group * per_head);
+        const int h0 = group * prm.head_group;
+        const int hg = min(prm.head_group, prm.BH - h0);  // heads in this group
+        const int r = idx - h0 * per_head;
+        w.q_tile = prm.n_qtiles - 1 - r / (hg * prm.n_splits);
+        w.bh = h0 + (r % (hg * prm.n_splits)) / prm.n_splits;
+        w.split = r % prm.n_splits;
     } else {
         w.split = idx % prm.n_splits;
         w.q_tile = (idx / prm.n_splits) % prm.n_qtiles;
@@ -803,6 +811,14 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     // gridDim.x-th work item.
     FaParams p = prm;
     p.n_items = static_cast<int>(items);
+    {
+        // Causal: when the K and V of all heads (2 x Nk x D bf16 each per head) would not stay
+        // in the L2 together, interleave only as many heads as fit in 64 MB, about half of it.
+        const long long kv_bytes = 4LL * prm.Nk * D;
+        long long g = prm.BH;
+        if (kv_bytes > 0 && kv_bytes * prm.BH > (128LL << 20)) g = (64LL << 20) / kv_bytes;
+        p.head_group = static_cast<int>(g < 1 ? 1 : (g > prm.BH ? prm.BH : g));
+    }
     const int sms = device_sm_count();
     const long long ctas = (sms > 0 && items > sms) ? sms : items;
     fa_fwd_kernel<D, CAUSAL, SPLIT>
