@@ -13,6 +13,9 @@ Functions (each a thin ctypes wrapper around ``oracle.c``; the arithmetic lives 
   three passes per query row.  Same lesson, section "From softmax to attention".
 * :func:`attention_qk` -- the same with Nq queries against Nk keys (the queries are the last Nq
   positions when causal), for the split-key path.
+* :func:`attention_gqa` -- the same with H_kv key/value heads shared by the H query heads (query
+  head h reads key/value head h // (H // H_kv)) and optional per-sequence key lengths (keys at
+  or past kv_lens[b] are masked like any other key: score -inf).
 * :func:`online_state` -- the pages' block-by-block streaming state (m, l, acc) of one score row
   with an optional trace.  Same lesson, sections "The idea", "From softmax to attention" and
   "A worked example by hand" (Tables 1 and 2); "kbwen.com FlashAttention" page, sections "Two
@@ -37,6 +40,7 @@ _dp = ctypes.POINTER(ctypes.c_double)
 _fp = ctypes.POINTER(ctypes.c_float)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i64p = ctypes.POINTER(ctypes.c_int64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
 
 
 def _ptr(a, t):
@@ -63,6 +67,11 @@ class Oracle:
                                      ctypes.c_double, ctypes.c_int, _i64p, ctypes.c_int64, _dp,
                                      _dp, ctypes.c_int]
         lib.oracle_attn2.restype = ctypes.c_int
+        lib.oracle_attn3.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_double, ctypes.c_int, _i32p,
+                                     _i64p, ctypes.c_int64, _dp, _dp, ctypes.c_int]
+        lib.oracle_attn3.restype = ctypes.c_int
         lib.oracle_online_state.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                             _dp]
@@ -141,6 +150,42 @@ class Oracle:
                                     nrows, _ptr(O, _dp), _ptr(L, _dp), nthreads)
         if rc != 0:
             raise ValueError("oracle_attn2 rejected its arguments")
+        return O, L
+
+    def attention_gqa(self, Q, K, V, scale: float, causal: bool, kv_lens=None, rows=None,
+                      nthreads: int = 0):
+        """Q [B, H, Nq, d]; K, V [B, H_kv, Nk, d] (bf16 bits), H_kv dividing H.
+
+        kv_lens: optional int32 [B], the valid keys of each sequence (keys j >= kv_lens[b] are
+        masked).  Causal: query i sees keys j <= i + (Nk - Nq).  rows: optional flat indices
+        (b*H + h)*Nq + i.  A row with no allowed key gets O = 0 and LSE = -inf.
+        """
+        Q, K, V = (_as_bf16_bits(t) for t in (Q, K, V))
+        if Q.ndim != 4 or K.shape != V.shape or K.ndim != 4 or Q.shape[0] != K.shape[0] \
+                or Q.shape[3] != K.shape[3]:
+            raise ValueError("Q [B,H,Nq,d] and K, V [B,H_kv,Nk,d] disagree")
+        B, H, Nq, d = Q.shape
+        H_kv, Nk = K.shape[1], K.shape[2]
+        lens = None
+        if kv_lens is not None:
+            lens = np.ascontiguousarray(np.asarray(kv_lens), dtype=np.int32)
+            if lens.shape != (B,):
+                raise ValueError("kv_lens must have one entry per sequence")
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            O = np.empty((rows.size, d), dtype=np.float64)
+            L = np.empty(rows.size, dtype=np.float64)
+            nrows = rows.size
+        else:
+            O = np.empty((B, H, Nq, d), dtype=np.float64)
+            L = np.empty((B, H, Nq), dtype=np.float64)
+            nrows = 0
+        rc = self._lib.oracle_attn3(_ptr(Q, _u16p), _ptr(K, _u16p), _ptr(V, _u16p), B, H, H_kv,
+                                    Nq, Nk, d, float(scale), int(bool(causal)), _ptr(lens, _i32p),
+                                    _ptr(rows, _i64p), nrows, _ptr(O, _dp), _ptr(L, _dp),
+                                    nthreads)
+        if rc != 0:
+            raise ValueError("oracle_attn3 rejected its arguments")
         return O, L
 
     # -- streaming state ---------------------------------------------------------------------
@@ -229,6 +274,10 @@ def attention(Q, K, V, scale, causal, rows=None, nthreads: int = 0):
 
 def attention_qk(Q, K, V, scale, causal, rows=None, nthreads: int = 0):
     return load().attention_qk(Q, K, V, scale, causal, rows, nthreads)
+
+
+def attention_gqa(Q, K, V, scale, causal, kv_lens=None, rows=None, nthreads: int = 0):
+    return load().attention_gqa(Q, K, V, scale, causal, kv_lens, rows, nthreads)
 
 
 def online_state(s, v, block, trace=False):

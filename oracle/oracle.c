@@ -19,7 +19,10 @@
  *        l    = sum_j exp(s_j - m)
  *        O_i  = sum_j exp(s_j - m) * V[b,h,j,:] / l
  *        LSE_i = m + ln l
- *     Allowed keys: all j < N, or j <= i when causal.  Same lesson, section "From softmax to
+ *     Allowed keys: all j < N, or j <= i when causal, and, with per-sequence key lengths,
+ *     only j < kv_len[b] (padding keys carry score -inf like any masked key).  With grouped
+ *     heads (H_kv key/value heads shared by H query heads) query head h reads key/value head
+ *     h / (H / H_kv).  Same lesson, section "From softmax to
  *     attention" (score = q.k scaled, output = softmax-weighted sum of the values, written in the
  *     max-subtracted form); the masked keys carry score -inf ("The implementation": masked
  *     positions such as the tokens after a token get score -inf).  FlashAttention computes this
@@ -41,7 +44,7 @@
  *     of an empty state keeps the other state.
  *   - bf16 inputs are widened exactly (bits << 16) to fp32, then to fp64.
  *
- * Mutants: building with -DORACLE_MUTANT=k plants one deliberate mistake (k = 1..11) so the
+ * Mutants: building with -DORACLE_MUTANT=k plants one deliberate mistake (k = 1..13) so the
  * tests can show that the pins catch it.  The default build (no define) has none.
  */
 #include <math.h>
@@ -152,9 +155,10 @@ int oracle_softmax_rows(const float* x, int64_t rows, int64_t cols, double* y, d
 
 typedef struct {
     const uint16_t *Q, *K, *V;
-    int64_t H, N, Nk, d; /* N = queries per head, Nk = keys per head */
+    int64_t H, H_kv, N, Nk, d; /* N = queries per head, Nk = keys per head */
     double scale;
     int causal;
+    const int32_t* kv_lens; /* NULL, or [B] valid keys per sequence */
     const int64_t* rows; /* NULL: rows [r0, r1) of the flat (b*H+h)*N+i index */
     double *O, *LSE;
     int64_t r0, r1;
@@ -167,9 +171,16 @@ static void attn_one_row(const attn_job* jb, int64_t flat, double* o, double* ls
     const int64_t N = jb->N, Nk = jb->Nk, d = jb->d;
     const int64_t bh = flat / N;
     const int64_t i = flat % N;
+    const int64_t b = bh / jb->H, h = bh % jb->H;
+#if ORACLE_MUTANT == 12
+    const int64_t hk = h % jb->H_kv; /* mutant: query heads dealt round-robin to K/V heads */
+#else
+    const int64_t hk = h / (jb->H / jb->H_kv); /* the K/V head this query head shares */
+#endif
+    const int64_t bhk = b * jb->H_kv + hk;
     const uint16_t* Qh = jb->Q + bh * N * d;
-    const uint16_t* Kh = jb->K + bh * Nk * d;
-    const uint16_t* Vh = jb->V + bh * Nk * d;
+    const uint16_t* Kh = jb->K + bhk * Nk * d;
+    const uint16_t* Vh = jb->V + bhk * Nk * d;
 
     for (int64_t k = 0; k < d; ++k) q[k] = bf16_to_double(Qh[i * d + k]);
 
@@ -187,6 +198,10 @@ static void attn_one_row(const attn_job* jb, int64_t flat, double* o, double* ls
     }
 #if ORACLE_MUTANT == 3
     if (nk > 1) nk -= 1; /* mutant: drops the last allowed key */
+#endif
+    /* keys past the sequence's own length are padding */
+#if ORACLE_MUTANT != 13 /* mutant 13: ignores the key lengths */
+    if (jb->kv_lens && nk > jb->kv_lens[b]) nk = jb->kv_lens[b] > 0 ? jb->kv_lens[b] : 0;
 #endif
 
     /* pass 1: scores and their maximum */
@@ -250,17 +265,22 @@ static void* attn_worker(void* arg) {
 }
 
 /*
- * Q: bf16 bit patterns [B, H, Nq, d]; K, V: [B, H, Nk, d]; all contiguous.
+ * Q: bf16 bit patterns [B, H, Nq, d]; K, V: [B, H_kv, Nk, d]; all contiguous; H_kv divides H
+ * and query head h reads key/value head h / (H / H_kv).
  * Query i of a head attends to keys j < Nk, or, when causal, to keys j <= i + (Nk - Nq) (the
- * Nq queries are the last Nq of the Nk positions; Nq == Nk is the usual square mask).
+ * Nq queries are the last Nq of the Nk positions; Nq == Nk is the usual square mask), and, when
+ * kv_lens is given, only to keys j < kv_lens[b].  A row with no allowed key gets O = 0 and
+ * LSE = -inf.
  * rows == NULL: compute all B*H*Nq rows; O is [B*H*Nq, d] and LSE [B*H*Nq].
  * rows != NULL: compute the nrows listed flat row indices (b*H + h)*Nq + i; O is [nrows, d].
  * Returns 0, or -1 on bad arguments (including a listed row out of range).
  */
-int oracle_attn2(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
-                 int64_t Nq, int64_t Nk, int64_t d, double scale, int causal, const int64_t* rows,
-                 int64_t nrows, double* O, double* LSE, int nthreads) {
+int oracle_attn3(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
+                 int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d, double scale, int causal,
+                 const int32_t* kv_lens, const int64_t* rows, int64_t nrows, double* O,
+                 double* LSE, int nthreads) {
     if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 1) return -1;
+    if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return -1;
     const int64_t total = B * H * Nq;
     const int64_t n = rows ? nrows : total;
     if (n < 0) return -1;
@@ -276,8 +296,9 @@ int oracle_attn2(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_
     if (!th || !jobs) { free(th); free(jobs); return -1; }
     for (int t = 0; t < nt; ++t) {
         attn_job* jb = &jobs[t];
-        jb->Q = Q; jb->K = K; jb->V = V; jb->H = H; jb->N = Nq; jb->Nk = Nk; jb->d = d;
-        jb->scale = scale; jb->causal = causal; jb->rows = rows; jb->O = O; jb->LSE = LSE;
+        jb->Q = Q; jb->K = K; jb->V = V; jb->H = H; jb->H_kv = H_kv; jb->N = Nq; jb->Nk = Nk;
+        jb->d = d; jb->scale = scale; jb->causal = causal; jb->kv_lens = kv_lens;
+        jb->rows = rows; jb->O = O; jb->LSE = LSE;
         jb->r0 = n * t / nt;
         jb->r1 = n * (t + 1) / nt;
     }
@@ -288,6 +309,14 @@ int oracle_attn2(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_
     for (int t = 0; t < nt; ++t) err |= jobs[t].err;
     free(th); free(jobs);
     return err ? -1 : 0;
+}
+
+/* Every query head with its own key/value head, every key valid. */
+int oracle_attn2(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
+                 int64_t Nq, int64_t Nk, int64_t d, double scale, int causal, const int64_t* rows,
+                 int64_t nrows, double* O, double* LSE, int nthreads) {
+    return oracle_attn3(Q, K, V, B, H, H, Nq, Nk, d, scale, causal, NULL, rows, nrows, O, LSE,
+                        nthreads);
 }
 
 /* Square attention: queries and keys are the same N positions. */

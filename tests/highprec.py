@@ -45,3 +45,37 @@ def attention_decimal(q, K, V, scale, causal):
         O.append(Ob)
         L.append(Lb)
     return O, L
+
+
+def attention_decimal_gqa(q, K, V, scale, causal, kv_lens=None):
+    """As attention_decimal, with K, V [B][H_kv][Nk][d] shared by the H query heads (query head
+    h reads key/value head h // (H // H_kv)) and optional key lengths per sequence (keys
+    j >= kv_lens[b] take no part).  A row with no key left gets O = 0 and LSE = -inf.
+    """
+    sc = Decimal(scale)
+    O, L = [], []
+    for b in range(len(q)):
+        H, H_kv = len(q[b]), len(K[b])
+        Ob, Lb = [], []
+        for h in range(H):
+            Qh, Kh, Vh = q[b][h], K[b][h // (H // H_kv)], V[b][h // (H // H_kv)]
+            N, Nk, d = len(Qh), len(Kh), len(Qh[0])
+            Oh, Lh = [], []
+            for i in range(N):
+                keys = [j for j in range(Nk)
+                        if (not causal or j <= i + Nk - N) and (kv_lens is None or j < kv_lens[b])]
+                if not keys:
+                    Oh.append([0.0] * d)
+                    Lh.append(float("-inf"))
+                    continue
+                e = [(sum(Decimal(Qh[i][k]) * Decimal(Kh[j][k]) for k in range(d)) * sc).exp()
+                     for j in keys]
+                tot = sum(e)
+                Oh.append([float(sum(e[t] * Decimal(Vh[j][k]) for t, j in enumerate(keys)) / tot)
+                           for k in range(d)])
+                Lh.append(float(tot.ln()))
+            Ob.append(Oh)
+            Lb.append(Lh)
+        O.append(Ob)
+        L.append(Lb)
+    return O, L

@@ -259,6 +259,71 @@ def pin_split_keys_merge_to_full(orc):
             assert abs(st["m"] + math.log(st["l"]) - L[0, 0, i]) < 1e-12
 
 
+def pin_gqa_key_lengths_decimal_bruteforce(orc):
+    """Grouped heads and per-sequence key lengths, against the 40-digit textbook formula.  A
+    sequence with no key (length 0) must give O = 0 and LSE = -inf (the empty state)."""
+    cases = [(2, 4, 2, 3, 6, 3, 0.7, False, [6, 2]), (2, 4, 1, 4, 5, 2, 0.9, True, [5, 3]),
+             (1, 6, 3, 2, 7, 3, 0.5, True, [4]), (2, 2, 2, 2, 4, 2, 1.2, False, [0, 3])]
+    for seed, (B, H, H_kv, Nq, Nk, d, scale, causal, lens) in enumerate(cases):
+        q, _, _ = inputs.attn_inputs(B, H, Nq, d, seed=301 + seed, qk_std=1.5)
+        _, k, v = inputs.attn_inputs(B, H_kv, Nk, d, seed=401 + seed, qk_std=1.5)
+        O, L = orc.attention_gqa(q, k, v, scale, causal, kv_lens=np.array(lens, np.int32))
+        Od, Ld = highprec.attention_decimal_gqa(_bf16_float(q).tolist(), _bf16_float(k).tolist(),
+                                                _bf16_float(v).tolist(), scale, causal, lens)
+        assert np.abs(O - np.array(Od)).max() < 1e-13, (B, H, H_kv, causal, lens)
+        Ld = np.array(Ld)
+        assert np.array_equal(np.isinf(L), np.isinf(Ld)), (B, H, H_kv, causal, lens)
+        fin = np.isfinite(Ld)
+        assert np.abs(L[fin] - Ld[fin]).max() < 1e-13, (B, H, H_kv, causal, lens)
+
+
+def pin_key_padding_ignores_what_lies_beyond(orc):
+    """Keys at or past a sequence's length take no part: whatever sits there (here, huge keys
+    that would dominate every softmax and huge values) cannot change O or LSE."""
+    B, H, Nq, Nk, d = 2, 2, 4, 9, 3
+    q, k, v = inputs.attn_inputs(B, H, Nq, d, seed=61)
+    _, k, v = inputs.attn_inputs(B, H, Nk, d, seed=62)
+    lens = np.array([5, 7], np.int32)
+    O, L = orc.attention_gqa(q, k, v, 0.8, False, kv_lens=lens)
+    k2, v2 = k.clone(), v.clone()
+    for b in range(B):
+        k2[b, :, lens[b]:] = 30.0
+        v2[b, :, lens[b]:] = -1000.0
+    O2, L2 = orc.attention_gqa(q, k2, v2, 0.8, False, kv_lens=lens)
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
+    # ... and a length of Nk is the same as no lengths at all
+    O3, L3 = orc.attention_gqa(q, k, v, 0.8, True, kv_lens=np.array([Nk, Nk], np.int32))
+    O4, L4 = orc.attention_qk(q, k, v, 0.8, True)
+    assert np.array_equal(O3, O4) and np.array_equal(L3, L4)
+
+
+def pin_gqa_is_attention_with_shared_heads(orc):
+    """Grouped heads are the plain attention of each query head with its group's key/value
+    head: query heads 2g and 2g+1 of H = 4 read key/value head g of H_kv = 2."""
+    B, H, H_kv, N, d = 1, 4, 2, 6, 3
+    q, _, _ = inputs.attn_inputs(B, H, N, d, seed=71)
+    _, k, v = inputs.attn_inputs(B, H_kv, N, d, seed=72)
+    O, L = orc.attention_gqa(q, k, v, 0.6, True)
+    for h in range(H):
+        g = h // 2
+        Oh, Lh = orc.attention(q[:, h:h + 1], k[:, g:g + 1], v[:, g:g + 1], 0.6, True)
+        assert np.array_equal(O[:, h:h + 1], Oh) and np.array_equal(L[:, h:h + 1], Lh)
+
+
+def pin_closed_form_single_valid_key(orc):
+    """A sequence of length 1: every query sees key 0 alone, so O = V_0 and LSE = s_0."""
+    B, H, Nq, Nk, d = 1, 2, 3, 5, 4
+    q, _, _ = inputs.attn_inputs(B, H, Nq, d, seed=81)
+    _, k, v = inputs.attn_inputs(B, H, Nk, d, seed=82)
+    O, L = orc.attention_gqa(q, k, v, 0.4, False, kv_lens=np.array([1], np.int32))
+    qf, kf, vf = _bf16_float(q), _bf16_float(k), _bf16_float(v)
+    for h in range(H):
+        for i in range(Nq):
+            assert np.abs(O[0, h, i] - vf[0, h, 0]).max() < 1e-15
+            s0 = 0.4 * float(np.dot(qf[0, h, i].astype(np.float64), kf[0, h, 0]))
+            assert abs(L[0, h, i] - s0) < 1e-12
+
+
 # ----------------------------------------------------------------------------------------------
 # closed forms
 # ----------------------------------------------------------------------------------------------

@@ -1,5 +1,6 @@
 """Every planted mistake in the oracle (a dropped term, a wrong sign, index or operand, a
-missing rescale, a missing -inf guard) must fail at least one pin.  The mistakes are planted
+missing rescale, a missing -inf guard, a wrong head map, ignored key lengths) must fail at least
+one pin.  The mistakes are planted
 in copies of the oracle built on the CPU with -DORACLE_MUTANT=k; the real oracle has none."""
 import pytest
 
@@ -18,6 +19,8 @@ MUTANTS = {
     9: "streaming state computes p against the old max",
     10: "streaming state has no -inf guard",
     11: "merge weighs both sides by one factor",
+    12: "grouped heads dealt round-robin to the key/value heads",
+    13: "per-sequence key lengths ignored",
 }
 
 
