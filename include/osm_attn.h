@@ -94,6 +94,33 @@ OSM_ATTN_API int fa_fwd_splitkv(const void* Q, const void* K, const void* V, voi
                                 float* ws_O, float* ws_LSE, void* stream);
 
 /*
+ * fa_fwd_gqa -- fa_fwd_splitkv with grouped key/value heads and per-sequence key lengths.
+ *
+ * Grouped heads: "FlashAttention" (paweldubiel.com notes), section "Averaging block results is
+ * not enough" (grouped-query attention keeps fewer key/value heads and combines with the tiled
+ * computation): H_kv key/value heads serve the H query heads, query head h of a sequence
+ * reading key/value head h / (H / H_kv) of it.  Key lengths: the masking of "How FlashAttention
+ * avoids storing the giant score table" (spicyshark.co, Online softmax lesson), section "The
+ * implementation" (a position a query may not look at gets score -inf, and a block whose scores
+ * are all -inf adds nothing): keys j >= kv_lens[b] of sequence b are masked, on top of the
+ * causal mask when causal is set.  A query left with no key gets O = 0 and LSE = -inf.
+ *
+ *   Q, O     bf16 [B, H, Nq, d]; K, V bf16 [B, H_kv, Nk, d]; LSE fp32 [B, H, Nq] or NULL.
+ *   H_kv     >= 1 and divides H (H_kv == H: every query head has its own key/value head).
+ *   kv_lens  DEVICE pointer to B int32 key counts, 4-byte aligned, read only; NULL means Nk for
+ *            every sequence.  Values are read by the kernel: below 0 counts as 0, above Nk as Nk.
+ *   causal   as fa_fwd_splitkv: query i sees keys j <= i + (Nk - Nq), and j < kv_lens[b].
+ *   n_splits, ws_O, ws_LSE  as fa_fwd_splitkv (fa_fwd_splitkv_plan(B, H, Nq, Nk, d, ...) gives
+ *            them; 1 runs one pass and needs no workspace).
+ * Errors as fa_fwd_splitkv, plus FA_ERR_INVALID_ARG when H_kv does not divide H or kv_lens is
+ * misaligned or overlaps an output.
+ */
+OSM_ATTN_API int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk,
+                            int64_t d, float scale, int causal, const int32_t* kv_lens,
+                            int64_t n_splits, float* ws_O, float* ws_LSE, void* stream);
+
+/*
  * fa_fwd_splitkv_plan -- the number of key ranges fa_fwd_splitkv should use for this shape and
  * the workspace it then needs.  n_splits = 0 asks the library to choose (enough CTAs for about
  * eight waves on this GPU, at most 64 ranges and one key tile per range); 1 .. 256 is clamped to
@@ -171,7 +198,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 1
+#define OSM_ATTN_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

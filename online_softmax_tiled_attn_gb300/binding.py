@@ -51,6 +51,9 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                                  ctypes.c_float, ctypes.c_int, i64, vp]
             L.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
+            L.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                     ctypes.c_float, ctypes.c_int, vp, i64, vp, vp, vp]
+            L.fa_fwd_gqa.restype = ctypes.c_int
             i64p = ctypes.POINTER(ctypes.c_int64)
             L.fa_fwd_splitkv_plan.argtypes = [i64, i64, i64, i64, i64, i64, i64p, i64p, i64p]
             L.fa_fwd_splitkv_plan.restype = ctypes.c_int
@@ -93,6 +96,13 @@ def fa_fwd_splitkv_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, sca
     return lib().fa_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(Nq),
                                 int(Nk), int(d), float(scale), int(bool(causal)), int(n_splits),
                                 ws_o_ptr, ws_lse_ptr, stream_ptr)
+
+
+def fa_fwd_gqa_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, H_kv, Nq, Nk, d, scale, causal,
+                   kv_lens_ptr, n_splits, ws_o_ptr, ws_lse_ptr, stream_ptr):
+    return lib().fa_fwd_gqa(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(H_kv),
+                            int(Nq), int(Nk), int(d), float(scale), int(bool(causal)),
+                            kv_lens_ptr, int(n_splits), ws_o_ptr, ws_lse_ptr, stream_ptr)
 
 
 def fa_fwd_splitkv_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale,
@@ -214,6 +224,56 @@ def fa_fwd_splitkv(q, k, v, n_splits=0, scale=None, causal=False, out=None, lse=
                             ws_l.data_ptr() if ws_l is not None else None, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv")
+    return out, lse
+
+
+def fa_fwd_gqa(q, k, v, kv_lens=None, n_splits=1, scale=None, causal=False, out=None, lse=None,
+               return_lse=True, workspace=None, stream=None):
+    """Attention of q [B,H,Nq,d] against k, v [B,H_kv,Nk,d] (CUDA bf16; H_kv divides H, query
+    head h reads key/value head h // (H // H_kv)), with optional per-sequence key lengths
+    kv_lens (CUDA int32 [B]: keys at or past kv_lens[b] are masked).  n_splits = 1 runs one
+    pass; 0 lets the library choose a key split (Flash-Decoding), with a workspace allocated
+    here unless `workspace` = (ws_O, ws_LSE) is given.  Returns (O, LSE)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 [B, H, N, d] tensor")
+    if k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H_kv,Nk,d] disagree")
+    B, H, Nq, d = q.shape
+    H_kv, Nk = k.shape[1], k.shape[2]
+    if kv_lens is not None:
+        if not isinstance(kv_lens, torch.Tensor) or not kv_lens.is_cuda or \
+                kv_lens.dtype != torch.int32 or kv_lens.shape != (B,) or \
+                not kv_lens.is_contiguous():
+            raise TypeError("kv_lens must be a contiguous CUDA int32 tensor of shape [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    splits, wo, wl = splitkv_plan(B, H, Nq, Nk, d, n_splits)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ws_o = ws_l = None
+    if splits > 1:
+        if workspace is None:
+            ws_o = torch.empty(wo, dtype=torch.float32, device=q.device)
+            ws_l = torch.empty(wl, dtype=torch.float32, device=q.device)
+        else:
+            ws_o, ws_l = workspace
+            if ws_o.numel() < wo or ws_l.numel() < wl:
+                raise ValueError("workspace too small for this split count")
+    rc = fa_fwd_gqa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                        lse.data_ptr() if lse is not None else None, B, H, H_kv, Nq, Nk, d, scale,
+                        causal, kv_lens.data_ptr() if kv_lens is not None else None,
+                        max(splits, 1) if Nk > 0 else 0,
+                        ws_o.data_ptr() if ws_o is not None else None,
+                        ws_l.data_ptr() if ws_l is not None else None, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_gqa")
     return out, lse
 
 

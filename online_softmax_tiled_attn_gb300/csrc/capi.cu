@@ -26,6 +26,71 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
     return true;
 }
 
+// The checks and dispatch shared by the split-key and grouped-head entry points: Q, O
+// [B, H, Nq, d], K, V [B, H_kv, Nk, d], LSE [B, H, Nq], optional kv_lens [B] (device),
+// n_splits key ranges (1: one pass, no workspace; > 1: partial states in ws_O, ws_LSE).
+int attention_call(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+                   int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d, float scale,
+                   int causal, const int32_t* kv_lens, int64_t n_splits, float* ws_O,
+                   float* ws_LSE, void* stream) {
+    if (B < 0 || H < 0 || H_kv < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
+    if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
+    int64_t bh, rows, q_elems, bh_kv, kv_rows, kv_elems;
+    if (!mul_ok(B, H, &bh) || !mul_ok(bh, Nq, &rows) || !mul_ok(rows, d, &q_elems) ||
+        !mul_ok(B, H_kv, &bh_kv) || !mul_ok(bh_kv, Nk, &kv_rows) ||
+        !mul_ok(kv_rows, d, &kv_elems) || q_elems > INT64_MAX / 4 || kv_elems > INT64_MAX / 4)
+        return FA_ERR_INVALID_ARG;
+    if (rows == 0) return FA_OK;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!O || !aligned(O, 16) || (LSE && !aligned(LSE, 4))) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    const uint64_t q_bytes = static_cast<uint64_t>(q_elems) * 2;
+    const uint64_t lse_bytes = static_cast<uint64_t>(rows) * 4;
+    if (LSE && overlaps(LSE, lse_bytes, O, q_bytes)) return FA_ERR_INVALID_ARG;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Nk == 0)  // no key at all: every row is empty (O = 0, LSE = -inf)
+        return osm::fa_fwd_splitkv_launch(nullptr, nullptr, nullptr, O, LSE,
+                                          osm::AttnShape{bh, 1, 1, Nq, 0, d, nullptr}, scale,
+                                          causal != 0, 0, nullptr, nullptr, st);
+    if (!Q || !K || !V) return FA_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return FA_ERR_INVALID_ARG;
+    if (n_splits < 1 || n_splits > 256) return FA_ERR_INVALID_ARG;
+    const uint64_t kv_bytes = static_cast<uint64_t>(kv_elems) * 2;
+    if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
+        overlaps(O, q_bytes, V, kv_bytes))
+        return FA_ERR_INVALID_ARG;
+    if (LSE && (overlaps(LSE, lse_bytes, Q, q_bytes) || overlaps(LSE, lse_bytes, K, kv_bytes) ||
+                overlaps(LSE, lse_bytes, V, kv_bytes)))
+        return FA_ERR_INVALID_ARG;
+    const uint64_t len_bytes = static_cast<uint64_t>(B) * 4;
+    if (kv_lens && (!aligned(kv_lens, 4) || overlaps(kv_lens, len_bytes, O, q_bytes) ||
+                    (LSE && overlaps(kv_lens, len_bytes, LSE, lse_bytes))))
+        return FA_ERR_INVALID_ARG;
+    if (n_splits > 1) {
+        int64_t wo, wl;
+        if (!mul_ok(q_elems, n_splits, &wo) || !mul_ok(rows, n_splits, &wl) || wo > INT64_MAX / 4)
+            return FA_ERR_INVALID_ARG;
+        if (!ws_O || !ws_LSE || !aligned(ws_O, 16) || !aligned(ws_LSE, 4))
+            return FA_ERR_INVALID_ARG;
+        const uint64_t wo_bytes = static_cast<uint64_t>(wo) * 4;
+        const uint64_t wl_bytes = static_cast<uint64_t>(wl) * 4;
+        const void* ins[4] = {Q, K, V, kv_lens};
+        const uint64_t in_bytes[4] = {q_bytes, kv_bytes, kv_bytes, kv_lens ? len_bytes : 0};
+        for (int i = 0; i < 4; ++i)
+            if (overlaps(ws_O, wo_bytes, ins[i], in_bytes[i]) ||
+                overlaps(ws_LSE, wl_bytes, ins[i], in_bytes[i]))
+                return FA_ERR_INVALID_ARG;
+        if (overlaps(ws_O, wo_bytes, O, q_bytes) || overlaps(ws_LSE, wl_bytes, O, q_bytes) ||
+            overlaps(ws_O, wo_bytes, ws_LSE, wl_bytes) ||
+            (LSE && (overlaps(ws_O, wo_bytes, LSE, lse_bytes) ||
+                     overlaps(ws_LSE, wl_bytes, LSE, lse_bytes))))
+            return FA_ERR_INVALID_ARG;
+    }
+    return osm::fa_fwd_splitkv_launch(Q, K, V, O, LSE,
+                                      osm::AttnShape{B, H, H_kv, Nq, Nk, d, kv_lens}, scale,
+                                      causal != 0, n_splits, ws_O, ws_LSE, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -79,53 +144,16 @@ int fa_fwd_splitkv_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
 int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                    int64_t H, int64_t Nq, int64_t Nk, int64_t d, float scale, int causal,
                    int64_t n_splits, float* ws_O, float* ws_LSE, void* stream) {
-    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
-    int64_t bh, rows, q_elems, kv_rows, kv_elems;
-    if (!mul_ok(B, H, &bh) || !mul_ok(bh, Nq, &rows) || !mul_ok(rows, d, &q_elems) ||
-        !mul_ok(bh, Nk, &kv_rows) || !mul_ok(kv_rows, d, &kv_elems) || q_elems > INT64_MAX / 4 ||
-        kv_elems > INT64_MAX / 4)
-        return FA_ERR_INVALID_ARG;
-    if (rows == 0) return FA_OK;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    if (!O || !aligned(O, 16) || (LSE && !aligned(LSE, 4))) return FA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-    const uint64_t q_bytes = static_cast<uint64_t>(q_elems) * 2;
-    const uint64_t lse_bytes = static_cast<uint64_t>(rows) * 4;
-    if (LSE && overlaps(LSE, lse_bytes, O, q_bytes)) return FA_ERR_INVALID_ARG;
-    if (Nk == 0)  // no key at all: every row is empty (O = 0, LSE = -inf)
-        return osm::fa_fwd_splitkv_launch(nullptr, nullptr, nullptr, O, LSE, bh, Nq, 0, d, scale,
-                                          causal != 0, 0, nullptr, nullptr,
-                                          static_cast<cudaStream_t>(stream));
-    if (!Q || !K || !V) return FA_ERR_INVALID_ARG;
-    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return FA_ERR_INVALID_ARG;
-    if (n_splits < 1 || n_splits > 256) return FA_ERR_INVALID_ARG;
-    const uint64_t kv_bytes = static_cast<uint64_t>(kv_elems) * 2;
-    if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
-        overlaps(O, q_bytes, V, kv_bytes))
-        return FA_ERR_INVALID_ARG;
-    if (LSE && (overlaps(LSE, lse_bytes, Q, q_bytes) || overlaps(LSE, lse_bytes, K, kv_bytes) ||
-                overlaps(LSE, lse_bytes, V, kv_bytes)))
-        return FA_ERR_INVALID_ARG;
-    if (n_splits > 1) {
-        int64_t wo, wl;
-        if (!mul_ok(q_elems, n_splits, &wo) || !mul_ok(rows, n_splits, &wl) || wo > INT64_MAX / 4)
-            return FA_ERR_INVALID_ARG;
-        if (!ws_O || !ws_LSE || !aligned(ws_O, 16) || !aligned(ws_LSE, 4)) return FA_ERR_INVALID_ARG;
-        const uint64_t wo_bytes = static_cast<uint64_t>(wo) * 4, wl_bytes = static_cast<uint64_t>(wl) * 4;
-        const void* ins[3] = {Q, K, V};
-        const uint64_t in_bytes[3] = {q_bytes, kv_bytes, kv_bytes};
-        for (int i = 0; i < 3; ++i)
-            if (overlaps(ws_O, wo_bytes, ins[i], in_bytes[i]) ||
-                overlaps(ws_LSE, wl_bytes, ins[i], in_bytes[i]))
-                return FA_ERR_INVALID_ARG;
-        if (overlaps(ws_O, wo_bytes, O, q_bytes) || overlaps(ws_LSE, wl_bytes, O, q_bytes) ||
-            overlaps(ws_O, wo_bytes, ws_LSE, wl_bytes) ||
-            (LSE && (overlaps(ws_O, wo_bytes, LSE, lse_bytes) ||
-                     overlaps(ws_LSE, wl_bytes, LSE, lse_bytes))))
-            return FA_ERR_INVALID_ARG;
-    }
-    return osm::fa_fwd_splitkv_launch(Q, K, V, O, LSE, bh, Nq, Nk, d, scale, causal != 0, n_splits,
-                                      ws_O, ws_LSE, static_cast<cudaStream_t>(stream));
+    return attention_call(Q, K, V, O, LSE, B, H, H, Nq, Nk, d, scale, causal, nullptr, n_splits,
+                          ws_O, ws_LSE, stream);
+}
+
+int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+               int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d, float scale,
+               int causal, const int32_t* kv_lens, int64_t n_splits, float* ws_O, float* ws_LSE,
+               void* stream) {
+    return attention_call(Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, causal, kv_lens,
+                          n_splits, ws_O, ws_LSE, stream);
 }
 
 int osm_softmax(const float* x, float* y, int64_t rows, int64_t cols, float* lse,

@@ -170,13 +170,16 @@ struct FaParams {
     float* ws_LSE;     // [n_splits, BH, Nq] (SPLIT == true)
     int Nq, Nk, BH, n_qtiles, n_splits, tiles_per_split, n_items;
     int head_group;  // causal: heads whose items are interleaved (their K, V share the L2)
+    int H, H_kv;     // query heads and key/value heads per sequence (BH = sequences x H)
+    const int32_t* kv_lens;  // [BH / H] valid keys per sequence, or nullptr (all Nk valid)
     float scale_log2;
     unsigned long long timeout_ns;
 };
 
-// One work item: a 128-row query tile of one (b, h) against key tiles [kt0, kt0 + n_kv).
+// One work item: a 128-row query tile of query head bh (over all sequences) against key tiles
+// [kt0, kt0 + n_kv) of key/value head kvh, which holds kv_len valid keys.
 struct Item {
-    int q_tile, bh, split, kt0, n_kv;
+    int q_tile, bh, split, kt0, n_kv, kvh, kv_len;
 };
 
 // Work item idx of the launch.  Non-causal items go head by head, so the CTAs running at one
@@ -200,9 +203,15 @@ __device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
         w.q_tile = (idx / prm.n_splits) % prm.n_qtiles;
         w.bh = idx / (prm.n_splits * prm.n_qtiles);
     }
+    // Grouped heads: query head h of sequence b reads key/value head h / (H / H_kv) of it.
+    const int b = w.bh / prm.H;
+    w.kvh = b * prm.H_kv + (w.bh - b * prm.H) / (prm.H / prm.H_kv);
+    w.kv_len = prm.Nk;
+    if (prm.kv_lens != nullptr) w.kv_len = min(max(prm.kv_lens[b], 0), prm.Nk);
     // Causal: the queries are the last Nq of the Nk positions, so query row q sees keys
-    // j <= q + Nk - Nq; key tiles wholly past the query tile's last row are skipped.
-    const int n_kv_all = (prm.Nk + kBN - 1) / kBN;
+    // j <= q + Nk - Nq; key tiles wholly past the query tile's last row, or past the
+    // sequence's own keys, are skipped.
+    const int n_kv_all = (w.kv_len + kBN - 1) / kBN;
     w.kt0 = w.split * prm.tiles_per_split;
     int kt1 = min(n_kv_all, w.kt0 + prm.tiles_per_split);
     if (CAUSAL) {
@@ -408,9 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(&bars->k_full[s], kTx);
                         const CUtensorMap* map = t < 0 ? &tmQ : &tmK;
                         const int row = t < 0 ? w.q_tile * kBM : (w.kt0 + t) * kBN;
+                        const int head = t < 0 ? w.bh : w.kvh;
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, map,
-                                        &bars->k_full[s], h * 64, row, w.bh);
+                                        &bars->k_full[s], h * 64, row, head);
                     }
                 }
                 drain_ring(bars->k_full, S_, e, timeout_ns);
@@ -436,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(&bars->v_full[s], kTx);
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
-                                        &bars->v_full[s], h * 64, (w.kt0 + t) * kBN, w.bh);
+                                        &bars->v_full[s], h * 64, (w.kt0 + t) * kBN, w.kvh);
                     }
                 }
                 drain_ring(bars->v_full, S_, J, timeout_ns);
@@ -588,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 n = w.n_kv;
                 kt0 = w.kt0;
                 const int q_row = w.q_tile * kBM + r;
-                key_limit = CAUSAL ? min(Nk - 1, q_row + (Nk - Nq)) : Nk - 1;
+                key_limit = CAUSAL ? min(w.kv_len - 1, q_row + (Nk - Nq)) : w.kv_len - 1;
             }
             float m_last = -INFINITY;  // reference max this group used last (scaled, log2)
             float l = 0.f;             // this group's sum of 2^(t - m_last) over its tiles
@@ -815,8 +825,10 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
         // Causal: when the K and V of all heads (2 x Nk x D bf16 each per head) would not stay
         // in the L2 together, interleave only as many heads as fit in 64 MB, about half of it.
         const long long kv_bytes = 4LL * prm.Nk * D;
+        const long long share = prm.H / prm.H_kv;  // query heads reading one K/V head
         long long g = prm.BH;
-        if (kv_bytes > 0 && kv_bytes * prm.BH > (128LL << 20)) g = (64LL << 20) / kv_bytes;
+        if (kv_bytes > 0 && kv_bytes * (prm.BH / share) > (128LL << 20))
+            g = ((64LL << 20) / kv_bytes) * share;
         p.head_group = static_cast<int>(g < 1 ? 1 : (g > prm.BH ? prm.BH : g));
     }
     const int sms = device_sm_count();
@@ -838,40 +850,53 @@ int launch_dispatch(int64_t d, bool causal, const CUtensorMap& tq, const CUtenso
     return FA_ERR_UNSUPPORTED;
 }
 
-int make_maps(const void* Q, const void* K, const void* V, int64_t BH, int64_t Nq, int64_t Nk,
-              int64_t d, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
-    int st = make_bhnd_tensor_map(tq, Q, BH, Nq, d);
-    if (st == FA_OK) st = make_bhnd_tensor_map(tk, K, BH, Nk, d);
-    if (st == FA_OK) st = make_bhnd_tensor_map(tv, V, BH, Nk, d);
+int make_maps(const void* Q, const void* K, const void* V, const AttnShape& sh, CUtensorMap* tq,
+              CUtensorMap* tk, CUtensorMap* tv) {
+    int st = make_bhnd_tensor_map(tq, Q, sh.B * sh.H, sh.Nq, sh.d);
+    if (st == FA_OK) st = make_bhnd_tensor_map(tk, K, sh.B * sh.H_kv, sh.Nk, sh.d);
+    if (st == FA_OK) st = make_bhnd_tensor_map(tv, V, sh.B * sh.H_kv, sh.Nk, sh.d);
     return st;
+}
+
+bool shape_fits(const AttnShape& sh) {
+    return sh.Nq <= (1LL << 30) && sh.Nk <= (1LL << 30) && sh.B * sh.H <= (1LL << 30) &&
+           sh.H_kv >= 1 && sh.H % sh.H_kv == 0;
+}
+
+FaParams base_params(const AttnShape& sh, float scale) {
+    FaParams prm{};
+    prm.Nq = static_cast<int>(sh.Nq);
+    prm.Nk = static_cast<int>(sh.Nk);
+    prm.BH = static_cast<int>(sh.B * sh.H);
+    prm.H = static_cast<int>(sh.H);
+    prm.H_kv = static_cast<int>(sh.H_kv);
+    prm.kv_lens = sh.kv_lens;
+    prm.n_qtiles = static_cast<int>((sh.Nq + kBM - 1) / kBM);
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.timeout_ns = fa_wait_timeout_ns();
+    return prm;
 }
 
 }  // namespace
 
 int fa_fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t BH,
                   int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream) {
-    return fa_fwd_qk_launch(Q, K, V, O, LSE, BH, N, N, d, scale, causal, stream);
+    return fa_fwd_shape_launch(Q, K, V, O, LSE, AttnShape{BH, 1, 1, N, N, d, nullptr}, scale,
+                               causal, stream);
 }
 
-int fa_fwd_qk_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                     int64_t BH, int64_t Nq, int64_t Nk, int64_t d, float scale, bool causal,
-                     cudaStream_t stream) {
-    if (Nq > (1LL << 30) || Nk > (1LL << 30) || BH > (1LL << 30)) return FA_ERR_UNSUPPORTED;
+int fa_fwd_shape_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        const AttnShape& sh, float scale, bool causal, cudaStream_t stream) {
+    if (!shape_fits(sh)) return FA_ERR_UNSUPPORTED;
     CUtensorMap tq, tk, tv;
-    const int st = make_maps(Q, K, V, BH, Nq, Nk, d, &tq, &tk, &tv);
+    const int st = make_maps(Q, K, V, sh, &tq, &tk, &tv);
     if (st != FA_OK) return st;
-    FaParams prm{};
+    FaParams prm = base_params(sh, scale);
     prm.O = static_cast<__nv_bfloat16*>(O);
     prm.LSE = LSE;
-    prm.Nq = static_cast<int>(Nq);
-    prm.Nk = static_cast<int>(Nk);
-    prm.BH = static_cast<int>(BH);
-    prm.n_qtiles = static_cast<int>((Nq + kBM - 1) / kBM);
     prm.n_splits = 1;
-    prm.tiles_per_split = static_cast<int>((Nk + kBN - 1) / kBN);
-    prm.scale_log2 = scale * 1.4426950408889634f;
-    prm.timeout_ns = fa_wait_timeout_ns();
-    return launch_dispatch<false>(d, causal, tq, tk, tv, prm, stream);
+    prm.tiles_per_split = static_cast<int>((sh.Nk + kBN - 1) / kBN);
+    return launch_dispatch<false>(sh.d, causal, tq, tk, tv, prm, stream);
 }
 
 int64_t splitkv_choose_splits(int64_t BH, int64_t Nq, int64_t Nk, int64_t requested) {
@@ -894,30 +919,24 @@ int64_t splitkv_choose_splits(int64_t BH, int64_t Nq, int64_t Nk, int64_t reques
 }
 
 int fa_fwd_splitkv_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                          int64_t BH, int64_t Nq, int64_t Nk, int64_t d, float scale, bool causal,
-                          int64_t n_splits, float* ws_O, float* ws_LSE, cudaStream_t stream) {
-    if (Nq > (1LL << 30) || Nk > (1LL << 30) || BH > (1LL << 30)) return FA_ERR_UNSUPPORTED;
-    const long long rows = static_cast<long long>(BH) * Nq;
+                          const AttnShape& sh, float scale, bool causal, int64_t n_splits,
+                          float* ws_O, float* ws_LSE, cudaStream_t stream) {
+    if (!shape_fits(sh)) return FA_ERR_UNSUPPORTED;
+    const long long rows = static_cast<long long>(sh.B * sh.H) * sh.Nq;
     if (n_splits > 1) {
         CUtensorMap tq, tk, tv;
-        const int st = make_maps(Q, K, V, BH, Nq, Nk, d, &tq, &tk, &tv);
+        const int st = make_maps(Q, K, V, sh, &tq, &tk, &tv);
         if (st != FA_OK) return st;
-        const int64_t n_kv_all = (Nk + kBN - 1) / kBN;
-        FaParams prm{};
+        const int64_t n_kv_all = (sh.Nk + kBN - 1) / kBN;
+        FaParams prm = base_params(sh, scale);
         prm.ws_O = ws_O;
         prm.ws_LSE = ws_LSE;
-        prm.Nq = static_cast<int>(Nq);
-        prm.Nk = static_cast<int>(Nk);
-        prm.BH = static_cast<int>(BH);
-        prm.n_qtiles = static_cast<int>((Nq + kBM - 1) / kBM);
         prm.n_splits = static_cast<int>(n_splits);
         prm.tiles_per_split = static_cast<int>((n_kv_all + n_splits - 1) / n_splits);
-        prm.scale_log2 = scale * 1.4426950408889634f;
-        prm.timeout_ns = fa_wait_timeout_ns();
-        const int rc = launch_dispatch<true>(d, causal, tq, tk, tv, prm, stream);
+        const int rc = launch_dispatch<true>(sh.d, causal, tq, tk, tv, prm, stream);
         if (rc != FA_OK) return rc;
     } else if (n_splits == 1) {
-        return fa_fwd_qk_launch(Q, K, V, O, LSE, BH, Nq, Nk, d, scale, causal, stream);
+        return fa_fwd_shape_launch(Q, K, V, O, LSE, sh, scale, causal, stream);
     }
     // n_splits > 1: merge the partial states; n_splits == 0 (no key at all): O = 0, LSE = -inf.
     const long long warps = rows;
@@ -925,7 +944,7 @@ int fa_fwd_splitkv_launch(const void* Q, const void* K, const void* V, void* O, 
     if (grid > 65535LL * 64) grid = 65535LL * 64;
     if (grid < 1) return FA_OK;
     const int ns = static_cast<int>(n_splits > 1 ? n_splits : 0);
-    if (d == 64)
+    if (sh.d == 64)
         splitkv_combine_kernel<64><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
             ws_O, ws_LSE, static_cast<__nv_bfloat16*>(O), LSE, rows, ns);
     else

@@ -17,17 +17,24 @@ int make_bhnd_tensor_map(CUtensorMap* map, const void* base, int64_t BH, int64_t
 // Deadline of every bounded mbarrier wait in the attention kernel.
 unsigned long long fa_wait_timeout_ns();
 
+// Shape of one attention call: Q, O [B, H, Nq, d]; K, V [B, H_kv, Nk, d] (H_kv divides H;
+// query head h reads key/value head h / (H / H_kv)); kv_lens, if not null, a device array of
+// the B valid key counts (clamped to [0, Nk] in the kernel).
+struct AttnShape {
+    int64_t B, H, H_kv, Nq, Nk, d;
+    const int32_t* kv_lens;
+};
+
 int fa_fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t BH,
                   int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream);
-int fa_fwd_qk_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                     int64_t BH, int64_t Nq, int64_t Nk, int64_t d, float scale, bool causal,
-                     cudaStream_t stream);
+int fa_fwd_shape_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        const AttnShape& sh, float scale, bool causal, cudaStream_t stream);
 // Number of key ranges the split-key path uses for `requested` (<= 0: chosen from the shape and
 // the SM count); 0 when there is no key.
 int64_t splitkv_choose_splits(int64_t BH, int64_t Nq, int64_t Nk, int64_t requested);
 int fa_fwd_splitkv_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                          int64_t BH, int64_t Nq, int64_t Nk, int64_t d, float scale, bool causal,
-                          int64_t n_splits, float* ws_O, float* ws_LSE, cudaStream_t stream);
+                          const AttnShape& sh, float scale, bool causal, int64_t n_splits,
+                          float* ws_O, float* ws_LSE, cudaStream_t stream);
 int fa_read_device_status(cudaStream_t stream, int* status);
 int selftest_wait_launch(long long timeout_us, cudaStream_t stream);
 

@@ -24,7 +24,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "osm_softmax",
+    for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "osm_softmax",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
@@ -49,7 +49,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 1
+    assert binding.lib().osm_attn_abi_version() == 2
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -114,6 +114,40 @@ def test_fa_fwd_accepts_lse_just_below_an_input():
     n = B * H * N * d * 2
     rc = binding.fa_fwd_raw(q, q + n, q + 2 * n, q + 3 * n, lse, B, H, N, d, 0.125, 0, None)
     assert rc == binding.FA_ERR_CUDA
+
+
+# fa_fwd_gqa(Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, causal, kv_lens, n_splits, ...):
+# B1 H4 Nq=Nk=128 d64; Q/O 64 KiB each, K/V sized by H_kv.
+Q4 = 4 * 128 * 64 * 2
+
+
+@pytest.mark.parametrize(
+    "args, want",
+    [
+        ((P, P + Q4, P + 2 * Q4, P + 3 * Q4, 0, 1, 4, 3, 128, 128, 64, 0.125, 0, 0, 1),
+         binding.FA_ERR_INVALID_ARG),  # H_kv does not divide H
+        ((P, P + Q4, P + 2 * Q4, P + 3 * Q4, 0, 1, 4, 0, 128, 128, 64, 0.125, 0, 0, 1),
+         binding.FA_ERR_INVALID_ARG),  # H_kv = 0
+        ((P, P + Q4, P + 2 * Q4, P + 3 * Q4, 0, 1, 4, 2, 128, 128, 64, 0.125, 0, 0, 1),
+         binding.FA_ERR_CUDA),  # valid: reaches the launch, which fails without a GPU
+        ((P, P + Q4, P + 2 * Q4, P + 3 * Q4, 0, 1, 4, 2, 128, 128, 64, 0.125, 0, P + 5 * Q4 + 2,
+          1), binding.FA_ERR_INVALID_ARG),  # kv_lens misaligned
+        ((P, P + Q4, P + 2 * Q4, P + 3 * Q4, 0, 1, 4, 2, 128, 128, 64, 0.125, 0, P + 3 * Q4 + 64,
+          1), binding.FA_ERR_INVALID_ARG),  # kv_lens inside O
+        ((P, P + Q4, P + 2 * Q4, P + 3 * Q4, 0, 1, 4, 2, 128, 128, 64, 0.125, 0, 0, 0),
+         binding.FA_ERR_INVALID_ARG),  # n_splits 0 is for the plan call, not this one
+        ((P, P + Q4, P + 2 * Q4, P + 3 * Q4, 0, 1, 4, 2, 128, 128, 64, 0.125, 0, 0, 2),
+         binding.FA_ERR_INVALID_ARG),  # two ranges without a workspace
+        ((0, 0, 0, P, 0, 1, 4, 2, 128, 0, 64, 0.125, 0, 0, 1),
+         binding.FA_ERR_CUDA),  # no key: the empty-row path, launched (fails without a GPU)
+    ],
+)
+def test_fa_fwd_gqa_rejects_on_host(args, want):
+    import torch
+
+    if want == binding.FA_ERR_CUDA and torch.cuda.is_available():
+        pytest.skip("reaches a launch; covered by the GPU tests on a machine with a GPU")
+    assert binding.fa_fwd_gqa_raw(*args, None, None, None) == want
 
 
 def test_selftest_rejects_out_of_range_timeout_on_host():
