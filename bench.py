@@ -293,6 +293,45 @@ def time_splitkv(w, steps, warmup, device, flush):
     return [a.elapsed_time(b) for a, b in ev], splits
 
 
+def time_gqa(w, steps, warmup, device, flush):
+    """Per-launch device time (ms) of fa_fwd_gqa on a grouped-head workload (the key split and
+    its workspace, if any, are set up outside the timed region)."""
+    import torch
+
+    from online_softmax_tiled_attn_gb300 import binding, inputs
+
+    q, k, v = inputs.gqa_inputs(w)
+    qd, kd, vd = q.to(device), k.to(device), v.to(device)
+    del q, k, v
+    lens = (torch.tensor(w.kv_lens, dtype=torch.int32, device=device)
+            if w.kv_lens is not None else None)
+    splits, wo, wl = binding.gqa_plan(w.B, w.H, w.H_kv, w.Nq, w.Nk, w.d, w.n_splits)
+    ws = (torch.empty(max(wo, 1), dtype=torch.float32, device=device),
+          torch.empty(max(wl, 1), dtype=torch.float32, device=device))
+    O = torch.empty_like(qd)
+    L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        binding.fa_fwd_gqa(qd, kd, vd, kv_lens=lens, n_splits=splits, scale=w.scale,
+                           causal=w.causal, out=O, lse=L, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    if binding.device_status() != 0:
+        raise RuntimeError("fa_fwd_gqa reported a device status")
+    return [a.elapsed_time(b) for a, b in ev], splits
+
+
 def roofline_tensor(flops, ms, peaks, kind, traffic=None):
     achieved = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -506,6 +545,19 @@ def main(argv=None):
                            "ms_per_step": round(dms, 4), "n_splits": splits,
                            "roofline": roofline_hbm(dw.hbm_bytes, dms, peaks, peaks_kind,
                                                     NCU_TRAFFIC_BYTES.get(name))}
+            torch.cuda.empty_cache()
+        for name, gw in inputs.GQA_WORKLOADS.items():
+            t, splits = time_gqa(gw, 20, 3, device, flush)
+            gms = max_over_ranks(sum(t) / len(t), dist, device)
+            entry = {"TFLOP/s": round(world * gw.flops / (gms * 1e-3) / 1e12, 2),
+                     "GB/s": round(world * gw.hbm_bytes / (gms * 1e-3) / 1e9, 1),
+                     "ms_per_step": round(gms, 4), "n_splits": splits}
+            # One query per head is HBM-bound; longer query blocks are tensor-bound.
+            entry["roofline"] = (roofline_hbm(gw.hbm_bytes, gms, peaks, peaks_kind,
+                                              NCU_TRAFFIC_BYTES.get(name)) if gw.Nq == 1 else
+                                 roofline_tensor(gw.flops, gms, peaks, peaks_kind,
+                                                 NCU_TRAFFIC_BYTES.get(name)))
+            other[name] = entry
             torch.cuda.empty_cache()
         sw = inputs.SOFTMAX_WORKLOADS["softmax_65536x4000"]
         t = time_softmax(sw, 20, 3, device, flush)

@@ -110,8 +110,8 @@ OSM_ATTN_API int fa_fwd_splitkv(const void* Q, const void* K, const void* V, voi
  *   kv_lens  DEVICE pointer to B int32 key counts, 4-byte aligned, read only; NULL means Nk for
  *            every sequence.  Values are read by the kernel: below 0 counts as 0, above Nk as Nk.
  *   causal   as fa_fwd_splitkv: query i sees keys j <= i + (Nk - Nq), and j < kv_lens[b].
- *   n_splits, ws_O, ws_LSE  as fa_fwd_splitkv (fa_fwd_splitkv_plan(B, H, Nq, Nk, d, ...) gives
- *            them; 1 runs one pass and needs no workspace).
+ *   n_splits, ws_O, ws_LSE  as fa_fwd_splitkv (fa_fwd_gqa_plan gives them; 1 runs one pass
+ *            and needs no workspace).
  * Errors as fa_fwd_splitkv, plus FA_ERR_INVALID_ARG when H_kv does not divide H or kv_lens is
  * misaligned or overlaps an output.
  */
@@ -119,6 +119,17 @@ OSM_ATTN_API int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O
                             int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk,
                             int64_t d, float scale, int causal, const int32_t* kv_lens,
                             int64_t n_splits, float* ws_O, float* ws_LSE, void* stream);
+
+/*
+ * fa_fwd_gqa_plan -- fa_fwd_splitkv_plan for fa_fwd_gqa: the number of key ranges and the
+ * workspace for Q [B, H, Nq, d] against K, V [B, H_kv, Nk, d].  The kernel runs the H / H_kv
+ * query heads that share a key/value head as one block of (H / H_kv) * Nq rows, so the choice
+ * counts blocks, not heads.  n_splits = 0 lets the library choose.  Host pointers; errors as
+ * fa_fwd_splitkv_plan, plus FA_ERR_INVALID_ARG when H_kv does not divide H.
+ */
+OSM_ATTN_API int fa_fwd_gqa_plan(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk,
+                                 int64_t d, int64_t n_splits, int64_t* splits_out,
+                                 int64_t* ws_o_floats, int64_t* ws_lse_floats);
 
 /*
  * fa_fwd_splitkv_plan -- the number of key ranges fa_fwd_splitkv should use for this shape and

@@ -54,6 +54,11 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                      ctypes.c_float, ctypes.c_int, vp, i64, vp, vp, vp]
             L.fa_fwd_gqa.restype = ctypes.c_int
+            L.fa_fwd_gqa_plan.argtypes = [i64, i64, i64, i64, i64, i64, i64,
+                                          ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_int64)]
+            L.fa_fwd_gqa_plan.restype = ctypes.c_int
             i64p = ctypes.POINTER(ctypes.c_int64)
             L.fa_fwd_splitkv_plan.argtypes = [i64, i64, i64, i64, i64, i64, i64p, i64p, i64p]
             L.fa_fwd_splitkv_plan.restype = ctypes.c_int
@@ -121,6 +126,16 @@ def splitkv_plan(B, H, Nq, Nk, d, n_splits=0):
                                    ctypes.byref(s), ctypes.byref(wo), ctypes.byref(wl))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv_plan")
+    return s.value, wo.value, wl.value
+
+
+def gqa_plan(B, H, H_kv, Nq, Nk, d, n_splits=0):
+    """(splits, workspace O floats, workspace LSE floats) for fa_fwd_gqa."""
+    s, wo, wl = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = lib().fa_fwd_gqa_plan(int(B), int(H), int(H_kv), int(Nq), int(Nk), int(d),
+                               int(n_splits), ctypes.byref(s), ctypes.byref(wo), ctypes.byref(wl))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_gqa_plan")
     return s.value, wo.value, wl.value
 
 
@@ -252,7 +267,7 @@ def fa_fwd_gqa(q, k, v, kv_lens=None, n_splits=1, scale=None, causal=False, out=
             raise TypeError("kv_lens must be a contiguous CUDA int32 tensor of shape [B]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    splits, wo, wl = splitkv_plan(B, H, Nq, Nk, d, n_splits)
+    splits, wo, wl = gqa_plan(B, H, H_kv, Nq, Nk, d, n_splits)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_lse:

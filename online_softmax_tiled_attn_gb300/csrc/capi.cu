@@ -50,7 +50,7 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (Nk == 0)  // no key at all: every row is empty (O = 0, LSE = -inf)
         return osm::fa_fwd_splitkv_launch(nullptr, nullptr, nullptr, O, LSE,
-                                          osm::AttnShape{bh, 1, 1, Nq, 0, d, nullptr}, scale,
+                                          osm::AttnShape{bh, 1, 1, Nq, 0, d, nullptr, 0}, scale,
                                           causal != 0, 0, nullptr, nullptr, st);
     if (!Q || !K || !V) return FA_ERR_INVALID_ARG;
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return FA_ERR_INVALID_ARG;
@@ -87,13 +87,38 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
             return FA_ERR_INVALID_ARG;
     }
     return osm::fa_fwd_splitkv_launch(Q, K, V, O, LSE,
-                                      osm::AttnShape{B, H, H_kv, Nq, Nk, d, kv_lens}, scale,
+                                      osm::AttnShape{B, H, H_kv, Nq, Nk, d, kv_lens, 0}, scale,
                                       causal != 0, n_splits, ws_O, ws_LSE, st);
 }
 
 }  // namespace
 
 extern "C" {
+
+int fa_fwd_gqa_plan(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d,
+                    int64_t n_splits, int64_t* splits_out, int64_t* ws_o_floats,
+                    int64_t* ws_lse_floats) {
+    if (!splits_out || !ws_o_floats || !ws_lse_floats) return FA_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || H_kv < 0 || Nq < 0 || Nk < 0 || d < 0 || n_splits < 0 ||
+        n_splits > 256)
+        return FA_ERR_INVALID_ARG;
+    if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
+    int64_t bh, rows, elems, bh_kv;
+    if (!mul_ok(B, H, &bh) || !mul_ok(bh, Nq, &rows) || !mul_ok(rows, d, &elems) ||
+        !mul_ok(B, H_kv, &bh_kv))
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    // The kernel runs the query heads of a key/value head as one packed row block.
+    const int64_t packed_rows = H_kv > 0 && H > 0 ? (H / H_kv) * Nq : Nq;
+    const int64_t splits = osm::splitkv_choose_splits(bh_kv, packed_rows, Nk, n_splits);
+    int64_t o = 0, l = 0;
+    if (splits > 1 && (!mul_ok(elems, splits, &o) || !mul_ok(rows, splits, &l)))
+        return FA_ERR_INVALID_ARG;
+    *splits_out = splits;
+    *ws_o_floats = splits > 1 ? o : 0;
+    *ws_lse_floats = splits > 1 ? l : 0;
+    return FA_OK;
+}
 
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
            int64_t H, int64_t N, int64_t d, float scale, int causal, void* stream) {

@@ -171,6 +171,10 @@ struct FaParams {
     int Nq, Nk, BH, n_qtiles, n_splits, tiles_per_split, n_items;
     int head_group;  // causal: heads whose items are interleaved (their K, V share the L2)
     int H, H_kv;     // query heads and key/value heads per sequence (BH = sequences x H)
+    // Query positions per original head.  Nq == q_pos, except when the query heads that share
+    // a key/value head are packed into one row block (Nq = group x q_pos): row r of a block is
+    // then position r % q_pos of query head r / q_pos.
+    int q_pos;
     const int32_t* kv_lens;  // [BH / H] valid keys per sequence, or nullptr (all Nk valid)
     float scale_log2;
     unsigned long long timeout_ns;
@@ -215,8 +219,10 @@ __device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
     w.kt0 = w.split * prm.tiles_per_split;
     int kt1 = min(n_kv_all, w.kt0 + prm.tiles_per_split);
     if (CAUSAL) {
-        const long long last_key =
-            static_cast<long long>(w.q_tile) * kBM + kBM - 1 + (prm.Nk - prm.Nq);
+        // the largest query position among the tile's rows
+        const int r0 = w.q_tile * kBM, r1 = min(r0 + kBM, prm.Nq) - 1;
+        const int pos_max = (r0 / prm.q_pos != r1 / prm.q_pos) ? prm.q_pos - 1 : r1 % prm.q_pos;
+        const long long last_key = static_cast<long long>(pos_max) + (prm.Nk - prm.q_pos);
         kt1 = min(static_cast<long long>(kt1), last_key < 0 ? 0 : last_key / kBN + 1);
     }
     w.n_kv = max(0, kt1 - w.kt0);
@@ -598,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 n = w.n_kv;
                 kt0 = w.kt0;
                 const int q_row = w.q_tile * kBM + r;
-                key_limit = CAUSAL ? min(w.kv_len - 1, q_row + (Nk - Nq)) : w.kv_len - 1;
+                const int pos = q_row % prm.q_pos;  // position of the row's query
+                key_limit = CAUSAL ? min(w.kv_len - 1, pos + (Nk - prm.q_pos)) : w.kv_len - 1;
             }
             float m_last = -INFINITY;  // reference max this group used last (scaled, log2)
             float l = 0.f;             // this group's sum of 2^(t - m_last) over its tiles
@@ -871,6 +878,7 @@ FaParams base_params(const AttnShape& sh, float scale) {
     prm.H = static_cast<int>(sh.H);
     prm.H_kv = static_cast<int>(sh.H_kv);
     prm.kv_lens = sh.kv_lens;
+    prm.q_pos = static_cast<int>(sh.q_pos > 0 ? sh.q_pos : sh.Nq);
     prm.n_qtiles = static_cast<int>((sh.Nq + kBM - 1) / kBM);
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.timeout_ns = fa_wait_timeout_ns();
@@ -879,14 +887,21 @@ FaParams base_params(const AttnShape& sh, float scale) {
 
 }  // namespace
 
+AttnShape pack_query_heads(const AttnShape& sh) {
+    if (sh.H_kv <= 0 || sh.H_kv >= sh.H || sh.q_pos > 0) return sh;
+    return AttnShape{sh.B, sh.H_kv, sh.H_kv, (sh.H / sh.H_kv) * sh.Nq, sh.Nk, sh.d, sh.kv_lens,
+                     sh.Nq};
+}
+
 int fa_fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t BH,
                   int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream) {
-    return fa_fwd_shape_launch(Q, K, V, O, LSE, AttnShape{BH, 1, 1, N, N, d, nullptr}, scale,
+    return fa_fwd_shape_launch(Q, K, V, O, LSE, AttnShape{BH, 1, 1, N, N, d, nullptr, 0}, scale,
                                causal, stream);
 }
 
 int fa_fwd_shape_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                        const AttnShape& sh, float scale, bool causal, cudaStream_t stream) {
+                        const AttnShape& shape, float scale, bool causal, cudaStream_t stream) {
+    const AttnShape sh = pack_query_heads(shape);
     if (!shape_fits(sh)) return FA_ERR_UNSUPPORTED;
     CUtensorMap tq, tk, tv;
     const int st = make_maps(Q, K, V, sh, &tq, &tk, &tv);
@@ -919,8 +934,9 @@ int64_t splitkv_choose_splits(int64_t BH, int64_t Nq, int64_t Nk, int64_t reques
 }
 
 int fa_fwd_splitkv_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                          const AttnShape& sh, float scale, bool causal, int64_t n_splits,
+                          const AttnShape& shape, float scale, bool causal, int64_t n_splits,
                           float* ws_O, float* ws_LSE, cudaStream_t stream) {
+    const AttnShape sh = pack_query_heads(shape);
     if (!shape_fits(sh)) return FA_ERR_UNSUPPORTED;
     const long long rows = static_cast<long long>(sh.B * sh.H) * sh.Nq;
     if (n_splits > 1) {

@@ -19,11 +19,19 @@ unsigned long long fa_wait_timeout_ns();
 
 // Shape of one attention call: Q, O [B, H, Nq, d]; K, V [B, H_kv, Nk, d] (H_kv divides H;
 // query head h reads key/value head h / (H / H_kv)); kv_lens, if not null, a device array of
-// the B valid key counts (clamped to [0, Nk] in the kernel).
+// the B valid key counts (clamped to [0, Nk] in the kernel).  q_pos = 0 means Nq; otherwise
+// the rows are packed query heads (see pack_query_heads) with q_pos positions each.
 struct AttnShape {
     int64_t B, H, H_kv, Nq, Nk, d;
     const int32_t* kv_lens;
+    int64_t q_pos;
 };
+
+// The same call with the H / H_kv query heads that share a key/value head packed into one row
+// block of (H / H_kv) * Nq rows: the [B, H, Nq, d] memory of Q, O and LSE read as
+// [B, H_kv, (H / H_kv) * Nq, d].  Each key/value tile is then loaded once per block instead of
+// once per query head, and short query blocks (decoding) fill the 128-row tiles.
+AttnShape pack_query_heads(const AttnShape& sh);
 
 int fa_fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t BH,
                   int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream);

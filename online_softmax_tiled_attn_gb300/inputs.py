@@ -20,6 +20,9 @@ softmax_65536x4000    fp32 rows [65536, 4000], x = 9*N(0,1) and per row one entr
                       entry -100 at seeded positions
 decode_b8h32q1k32768  B8 H32, one query against 32768 cached keys, d128, N(0,1), non-causal
                       (the split-key path); seed 1007
+gqa_*                 grouped key/value heads (H_kv < H) and per-sequence key lengths, N(0,1):
+                      a causal prefill, a ragged-length batch and a grouped decode; seeds
+                      1008-1010 (see GQA_WORKLOADS)
 ====================  ==========================================================================
 
 Seeds: 1000 + the workload's index in the table above (1001 ... 1005 for the five attention
@@ -124,6 +127,77 @@ DECODE_WORKLOADS = {
     w.name: w
     for w in [DecodeWorkload("decode_b8h32q1k32768d128", 8, 32, 1, 32768, 128, False, 1007)]
 }
+
+
+@dataclass(frozen=True)
+class GqaWorkload:
+    """Q [B, H, Nq, d] against K, V [B, H_kv, Nk, d], optional key lengths per sequence."""
+
+    name: str
+    B: int
+    H: int
+    H_kv: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+    kv_lens: tuple = None  # valid keys per sequence, or None (all Nk)
+    n_splits: int = 1      # 0: the library chooses a key split
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def lens(self):
+        return list(self.kv_lens) if self.kv_lens is not None else [self.Nk] * self.B
+
+    def allowed_pairs(self) -> int:
+        """Allowed (query, key) pairs of one head summed over the sequences: query i of
+        sequence b sees min(kv_len_b, i + 1 + Nk - Nq) keys when causal, kv_len_b otherwise."""
+        tot = 0
+        for L in self.lens():
+            if not self.causal:
+                tot += self.Nq * L
+                continue
+            off = self.Nk - self.Nq
+            for i in range(self.Nq):
+                tot += max(0, min(L, i + 1 + off))
+        return tot
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOP: 4*d per allowed (query, key) pair, for every query head."""
+        return 4.0 * self.d * self.H * self.allowed_pairs()
+
+    @property
+    def hbm_bytes(self) -> int:
+        """Compulsory HBM traffic: Q and O (bf16), LSE (fp32), and the valid keys' K and V."""
+        q = self.B * self.H * self.Nq
+        kv = self.H_kv * sum(self.lens())
+        return q * self.d * 2 * 2 + q * 4 + kv * self.d * 2 * 2
+
+
+GQA_WORKLOADS = {
+    w.name: w
+    for w in [
+        GqaWorkload("gqa_causal_b2h32kv8n8192d128", 2, 32, 8, 8192, 8192, 128, True, 1008),
+        GqaWorkload("gqa_ragged_b4h32kv8n4096d128", 4, 32, 8, 4096, 4096, 128, False, 1009,
+                    kv_lens=(4096, 3000, 1500, 577)),
+        GqaWorkload("gqa_decode_b8h32kv8q1k32768d128", 8, 32, 8, 1, 32768, 128, False, 1010,
+                    n_splits=0),
+    ]
+}
+
+
+def gqa_inputs(w: GqaWorkload):
+    """Q [B,H,Nq,d], K and V [B,H_kv,Nk,d], bf16 N(0,1), drawn in that order from one seeded
+    generator."""
+    g = torch.Generator().manual_seed(int(w.seed))
+    q = torch.randn((w.B, w.H, w.Nq, w.d), generator=g).to(torch.bfloat16)
+    k = torch.randn((w.B, w.H_kv, w.Nk, w.d), generator=g).to(torch.bfloat16)
+    v = torch.randn((w.B, w.H_kv, w.Nk, w.d), generator=g).to(torch.bfloat16)
+    return q, k, v
 
 
 def decode_inputs(w: DecodeWorkload):

@@ -24,7 +24,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "osm_softmax",
+    for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "fa_fwd_gqa_plan",
+              "osm_softmax",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names

@@ -98,3 +98,34 @@ def test_key_lengths_ignore_what_lies_beyond():
         v2[b, :, n:] = -500.0
     O2, L2 = run(q, k2, v2, lens, False, 1)
     assert np.array_equal(O, O2) and np.array_equal(L, L2)
+
+
+def _sample(w, per_head, seed_offset=0):
+    g = torch.Generator().manual_seed(int(w.seed) * 7919 + 29 + seed_offset)
+    out = []
+    for bh in range(w.B * w.H):
+        k = min(per_head, w.Nq)
+        idx = torch.randperm(w.Nq, generator=g)[:k]
+        idx[0] = w.Nq - 1  # the last row sees the most keys
+        out.append(torch.unique(idx).to(torch.int64) + bh * w.Nq)
+    return torch.cat(out).numpy()
+
+
+@pytest.mark.parametrize("name", list(inputs.GQA_WORKLOADS))
+def test_gqa_workloads_full_size_sampled(name):
+    """The grouped-head bench workloads at full size, in the bench's launch configuration
+    (the library's split choice), on seeded sampled rows."""
+    w = inputs.GQA_WORKLOADS[name]
+    q, k, v = inputs.gqa_inputs(w)
+    lens = None if w.kv_lens is None else torch.tensor(w.kv_lens, dtype=torch.int32).cuda()
+    O, L = binding.fa_fwd_gqa(q.cuda(), k.cuda(), v.cuda(), kv_lens=lens, n_splits=w.n_splits,
+                              scale=w.scale, causal=w.causal)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    rows = _sample(w, 24)
+    Oref, Lref = oracle.attention_gqa(q, k, v, w.scale, w.causal,
+                                      kv_lens=None if w.kv_lens is None
+                                      else np.array(w.kv_lens, np.int32), rows=rows)
+    Og = O.float().cpu().numpy().reshape(-1, w.d)[rows]
+    Lg = L.cpu().numpy().reshape(-1)[rows]
+    parity.check_attention_allow_empty(Og, Lg, Oref, Lref, name)
