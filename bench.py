@@ -350,11 +350,14 @@ def roofline_hbm(nbytes, ms, peaks, kind, traffic=None):
 
 
 # Traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
-# summarised under profiles/ (same kernel version).  Workloads without a capture report None.
+# summarised under profiles/, one per workload.  Workloads without a capture report None.
 NCU_TRAFFIC_BYTES = {
-    "dense_b2h32n8192": 402.693888e6 + 118.795776e6,
-    "mha_b4h16n2048d64": 50.372352e6 + 0.767232e6,
-    "softmax_65536x4000": 1.0487e9 + 0.998584576e9,
+    "mha_b4h16n2048d64": 50.39488e6 + 0.222976e6,
+    "dense_b2h32n8192": 402.803968e6 + 115.572992e6,
+    "causal_b2h32n8192": 680.285696e6 + 120.198656e6,
+    "decode_b8h32q1k32768d128": 4.295259e9 + 3.723264e6,
+    "gqa_decode_b8h32kv8q1k32768d128": 1.073947e9 + 5.79328e6,
+    "softmax_65536x4000": 1.048683e9 + 0.997987072e9,
 }
 
 
@@ -454,6 +457,8 @@ def main(argv=None):
                     help="with --profile: launch osm_softmax instead of fa_fwd")
     ap.add_argument("--decode", action="store_true",
                     help="with --profile: launch fa_fwd_splitkv on the decode workload")
+    ap.add_argument("--gqa", default=None,
+                    help="with --profile: launch fa_fwd_gqa on this grouped-head workload")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be at least 3")
@@ -475,7 +480,9 @@ def main(argv=None):
     w = inputs.ATTN_WORKLOADS[args.workload]
 
     if args.profile:
-        if args.decode:
+        if args.gqa:
+            time_gqa(inputs.GQA_WORKLOADS[args.gqa], args.steps, args.warmup, device, None)
+        elif args.decode:
             dw = next(iter(inputs.DECODE_WORKLOADS.values()))
             time_splitkv(dw, args.steps, args.warmup, device, None)
         elif args.softmax:

@@ -199,7 +199,16 @@ __device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
         const int h0 = group * prm.head_group;
         const int hg = min(prm.head_group, prm.BH - h0);  // heads in this group
         const int r = idx - h0 * per_head;
-        w.q_tile = prm.n_qtiles - 1 - r / (hg * prm.n_splits);
+        const int k = r / (hg * prm.n_splits);  // rank of the query tile, longest rows first
+        const int packed = (prm.q_pos % kBM == 0 && prm.Nq % prm.q_pos == 0)
+                               ? prm.Nq / prm.q_pos : 1;  // query heads per row block
+        if (packed > 1) {
+            // packed query heads: the tiles at the same position of the block's heads in turn
+            const int per = prm.q_pos / kBM;  // tiles per query head
+            w.q_tile = (k % packed) * per + (per - 1 - k / packed);
+        } else {
+            w.q_tile = prm.n_qtiles - 1 - k;
+        }
         w.bh = h0 + (r % (hg * prm.n_splits)) / prm.n_splits;
         w.split = r % prm.n_splits;
     } else {
