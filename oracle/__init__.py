@@ -9,6 +9,9 @@ Functions (each a thin ctypes wrapper around ``oracle.c``; the arithmetic lives 
 * :func:`softmax_rows` -- three-pass safe softmax of every row, and its log-sum-exp.
   "How FlashAttention avoids storing the giant score table" (spicyshark.co), sections
   "The fix: subtract the maximum" and "The cost: three passes".
+* :func:`softmax_topk` -- softmax of every row with its k largest entries (ties: the smaller
+  column first): their columns, their shares and the row's log-sum-exp.  Same lesson, section
+  "Where this is used in practice" (softmax fused with top-k selection).
 * :func:`attention` -- exact attention O = softmax(scale*Q K^T [causal]) V and LSE = m + ln l,
   three passes per query row.  Same lesson, section "From softmax to attention".
 * :func:`attention_qk` -- the same with Nq queries against Nk keys (the queries are the last Nq
@@ -58,6 +61,9 @@ class Oracle:
         lib.oracle_softmax_rows.argtypes = [_fp, ctypes.c_int64, ctypes.c_int64, _dp, _dp,
                                             ctypes.c_int]
         lib.oracle_softmax_rows.restype = ctypes.c_int
+        lib.oracle_softmax_topk.argtypes = [_fp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                            _dp, _i64p, _dp, ctypes.c_int]
+        lib.oracle_softmax_topk.restype = ctypes.c_int
         lib.oracle_attn.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64, ctypes.c_int64,
                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
                                     _i64p, ctypes.c_int64, _dp, _dp, ctypes.c_int]
@@ -96,6 +102,23 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_softmax_rows rejected its arguments")
         return y, lse
+
+    def softmax_topk(self, x, k: int, nthreads: int = 0):
+        """x: float32 [rows, cols] (no NaN).  Returns (values fp64 [rows, k], indices int64
+        [rows, k], lse fp64 [rows]): the k entries with the largest x in descending order
+        (ties: the smaller column first) and their softmax shares."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim == 1:
+            x = x[None, :]
+        rows, cols = x.shape
+        vals = np.empty((rows, k), dtype=np.float64)
+        idx = np.empty((rows, k), dtype=np.int64)
+        lse = np.empty(rows, dtype=np.float64)
+        rc = self._lib.oracle_softmax_topk(_ptr(x, _fp), rows, cols, int(k), _ptr(vals, _dp),
+                                           _ptr(idx, _i64p), _ptr(lse, _dp), nthreads)
+        if rc != 0:
+            raise ValueError("oracle_softmax_topk rejected its arguments")
+        return vals, idx, lse
 
     # -- attention ---------------------------------------------------------------------------
     def attention(self, Q, K, V, scale: float, causal: bool, rows=None, nthreads: int = 0):
@@ -266,6 +289,10 @@ def load(mutant: int = 0) -> Oracle:
 
 def softmax_rows(x, nthreads: int = 0):
     return load().softmax_rows(x, nthreads)
+
+
+def softmax_topk(x, k, nthreads: int = 0):
+    return load().softmax_topk(x, k, nthreads)
 
 
 def attention(Q, K, V, scale, causal, rows=None, nthreads: int = 0):

@@ -29,6 +29,12 @@
  *     exact quantity, only in another order ("kbwen.com FlashAttention" page, section "More than
  *     two blocks": it is the same attention, not an approximation).
  *
+ *   softmax with top-k selection: the k entries of a row with the largest x (ties: the smaller
+ *     column first), their columns and their shares y_j, and lse.  Same lesson, section "Where
+ *     this is used in practice" (the online normaliser serves softmax fused with top-k
+ *     selection, keeping only the k largest scores); the shares are the three-pass softmax above
+ *     and the selection is a plain sort of the row.
+ *
  *   the streaming state (m, l, acc) of one score row read in blocks, and the merge of two such
  *   states: same lesson, sections "The idea", "From softmax to attention" (the block recipe)
  *   and the two-worker merge at the end of "From softmax to attention"; "kbwen.com
@@ -44,7 +50,7 @@
  *     of an empty state keeps the other state.
  *   - bf16 inputs are widened exactly (bits << 16) to fp32, then to fp64.
  *
- * Mutants: building with -DORACLE_MUTANT=k plants one deliberate mistake (k = 1..13) so the
+ * Mutants: building with -DORACLE_MUTANT=k plants one deliberate mistake (k = 1..15) so the
  * tests can show that the pins catch it.  The default build (no define) has none.
  */
 #include <math.h>
@@ -147,6 +153,91 @@ int oracle_softmax_rows(const float* x, int64_t rows, int64_t cols, double* y, d
     for (int t = 1; t < nt; ++t) pthread_join(th[t], NULL);
     free(th); free(jobs);
     return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Softmax with top-k selection.                                                               */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    float x;
+    int64_t j;
+} ranked;
+
+/* x descending, then column ascending */
+static int rank_cmp(const void* a, const void* b) {
+    const ranked* p = (const ranked*)a;
+    const ranked* q = (const ranked*)b;
+    if (p->x > q->x) return -1;
+    if (p->x < q->x) return 1;
+#if ORACLE_MUTANT == 14
+    return (p->j > q->j) ? -1 : (p->j < q->j); /* mutant: ties go to the larger column */
+#else
+    return (p->j < q->j) ? -1 : (p->j > q->j);
+#endif
+}
+
+typedef struct {
+    const float* x;
+    int64_t cols, k;
+    double* values;
+    int64_t* indices;
+    double* lse;
+    int64_t r0, r1;
+    int err;
+} topk_job;
+
+static void* topk_worker(void* arg) {
+    topk_job* jb = (topk_job*)arg;
+    double* y = (double*)malloc(sizeof(double) * (size_t)jb->cols);
+    ranked* order = (ranked*)malloc(sizeof(ranked) * (size_t)jb->cols);
+    if (!y || !order) { jb->err = 1; free(y); free(order); return NULL; }
+    for (int64_t r = jb->r0; r < jb->r1; ++r) {
+        const float* xr = jb->x + r * jb->cols;
+        double lse;
+        softmax_one_row(xr, y, &lse, jb->cols);
+        if (jb->lse) jb->lse[r] = lse;
+        for (int64_t j = 0; j < jb->cols; ++j) { order[j].x = xr[j]; order[j].j = j; }
+        qsort(order, (size_t)jb->cols, sizeof(ranked), rank_cmp);
+        for (int64_t t = 0; t < jb->k; ++t) {
+#if ORACLE_MUTANT == 15
+            const int64_t pick = (t + 1 < jb->cols) ? t + 1 : t; /* mutant: skips the largest */
+#else
+            const int64_t pick = t;
+#endif
+            jb->indices[r * jb->k + t] = order[pick].j;
+            jb->values[r * jb->k + t] = y[order[pick].j];
+        }
+    }
+    free(y); free(order);
+    return NULL;
+}
+
+/* x [rows, cols] fp32 (no NaN); values [rows, k] fp64, indices [rows, k] int64, lse [rows] or
+   NULL.  1 <= k <= cols.  Returns 0, or -1 on bad arguments. */
+int oracle_softmax_topk(const float* x, int64_t rows, int64_t cols, int64_t k, double* values,
+                        int64_t* indices, double* lse, int nthreads) {
+    if (rows < 0 || cols < 1 || k < 1 || k > cols) return -1;
+    if (rows == 0) return 0;
+    if (!x || !values || !indices) return -1;
+    int nt = resolve_threads(nthreads);
+    if (nt > rows) nt = (int)rows;
+    pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+    topk_job* jobs = (topk_job*)calloc((size_t)nt, sizeof(topk_job));
+    if (!th || !jobs) { free(th); free(jobs); return -1; }
+    for (int t = 0; t < nt; ++t) {
+        jobs[t].x = x; jobs[t].cols = cols; jobs[t].k = k; jobs[t].values = values;
+        jobs[t].indices = indices; jobs[t].lse = lse;
+        jobs[t].r0 = rows * t / nt;
+        jobs[t].r1 = rows * (t + 1) / nt;
+    }
+    for (int t = 1; t < nt; ++t) pthread_create(&th[t], NULL, topk_worker, &jobs[t]);
+    topk_worker(&jobs[0]);
+    int err = 0;
+    for (int t = 1; t < nt; ++t) pthread_join(th[t], NULL);
+    for (int t = 0; t < nt; ++t) err |= jobs[t].err;
+    free(th); free(jobs);
+    return err ? -1 : 0;
 }
 
 /* ------------------------------------------------------------------------------------------ */

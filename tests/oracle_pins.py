@@ -324,6 +324,38 @@ def pin_closed_form_single_valid_key(orc):
             assert abs(L[0, h, i] - s0) < 1e-12
 
 
+def pin_softmax_topk_brute_force(orc):
+    """Top-k against Python's own sort of (value descending, column ascending) and the shares
+    against scipy's softmax; rows with repeated values, -inf entries and the overflow row."""
+    from scipy.special import softmax
+
+    g = np.random.default_rng(5)
+    x = g.integers(-3, 4, size=(40, 23)).astype(np.float32)  # many ties
+    x[3, :20] = -np.inf
+    x[7] = np.float32([1000, 1001, 1002] * 7 + [1000, 1000])
+    x[9] = g.standard_normal(23).astype(np.float32) * 30
+    for k in (1, 2, 5, 23):
+        vals, idx, lse = orc.softmax_topk(x, k)
+        for r in range(x.shape[0]):
+            want = sorted(range(23), key=lambda j: (-float(x[r, j]), j))[:k]
+            assert list(idx[r]) == want, (r, k)
+            y = softmax(x[r].astype(np.float64))
+            assert np.abs(vals[r] - y[want]).max() < 1e-15, (r, k)
+
+
+def pin_softmax_topk_full_is_sorted_softmax(orc):
+    """k = cols: every share once, in order, summing to 1; k = 1 is the arg-max."""
+    x = inputs.softmax_inputs(6, 50, seed=17)
+    vals, idx, lse = orc.softmax_topk(x.numpy(), 50)
+    assert np.all(np.diff(vals, axis=1) <= 0)
+    assert np.abs(vals.sum(axis=1) - 1.0).max() < 1e-14
+    assert all(sorted(r) == list(range(50)) for r in idx.tolist())
+    v1, i1, _ = orc.softmax_topk(x.numpy(), 1)
+    assert np.array_equal(i1[:, 0], np.argmax(x.numpy(), axis=1))
+    y, l2 = orc.softmax_rows(x.numpy())
+    assert np.array_equal(lse, l2) and np.array_equal(v1[:, 0], y.max(axis=1))
+
+
 # ----------------------------------------------------------------------------------------------
 # closed forms
 # ----------------------------------------------------------------------------------------------

@@ -21,6 +21,8 @@ MUTANTS = {
     11: "merge weighs both sides by one factor",
     12: "grouped heads dealt round-robin to the key/value heads",
     13: "per-sequence key lengths ignored",
+    14: "top-k ties go to the larger column",
+    15: "top-k skips the largest entry",
 }
 
 
