@@ -256,6 +256,31 @@ def time_softmax(sw, steps, warmup, device, flush):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def time_topk(tw, steps, warmup, device, flush):
+    """Per-launch device time (ms) of osm_softmax_topk on a top-k workload."""
+    import torch
+
+    from online_softmax_tiled_attn_gb300 import binding, inputs
+
+    x = inputs.softmax_inputs(tw.rows, tw.cols, tw.seed, tw.std, tw.spike).to(device)
+    vals = torch.empty((tw.rows, tw.k), dtype=torch.float32, device=device)
+    idx = torch.empty((tw.rows, tw.k), dtype=torch.int32, device=device)
+    lse = torch.empty((tw.rows,), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        binding.osm_softmax_topk(x, tw.k, values=vals, indices=idx, lse=lse)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        binding.osm_softmax_topk(x, tw.k, values=vals, indices=idx, lse=lse)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def time_splitkv(w, steps, warmup, device, flush):
     """Per-launch device time (ms) of fa_fwd_splitkv (attention kernel + combine) on a decode
     workload, workspace allocated once outside the timed region."""
@@ -459,6 +484,8 @@ def main(argv=None):
                     help="with --profile: launch fa_fwd_splitkv on the decode workload")
     ap.add_argument("--gqa", default=None,
                     help="with --profile: launch fa_fwd_gqa on this grouped-head workload")
+    ap.add_argument("--topk", default=None,
+                    help="with --profile: launch osm_softmax_topk on this top-k workload")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be at least 3")
@@ -480,7 +507,9 @@ def main(argv=None):
     w = inputs.ATTN_WORKLOADS[args.workload]
 
     if args.profile:
-        if args.gqa:
+        if args.topk:
+            time_topk(inputs.TOPK_WORKLOADS[args.topk], args.steps, args.warmup, device, None)
+        elif args.gqa:
             time_gqa(inputs.GQA_WORKLOADS[args.gqa], args.steps, args.warmup, device, None)
         elif args.decode:
             dw = next(iter(inputs.DECODE_WORKLOADS.values()))
@@ -573,6 +602,14 @@ def main(argv=None):
                           "ms_per_step": round(sms, 4),
                           "roofline": roofline_hbm(sw.hbm_bytes, sms, peaks, peaks_kind,
                                                    NCU_TRAFFIC_BYTES.get(sw.name))}
+        for name, tw in inputs.TOPK_WORKLOADS.items():
+            t = time_topk(tw, 20, 3, device, flush)
+            tms = max_over_ranks(sum(t) / len(t), dist, device)
+            other[name] = {"GB/s": round(world * tw.hbm_bytes / (tms * 1e-3) / 1e9, 1),
+                           "ms_per_step": round(tms, 4),
+                           "roofline": roofline_hbm(tw.hbm_bytes, tms, peaks, peaks_kind,
+                                                    NCU_TRAFFIC_BYTES.get(name))}
+            torch.cuda.empty_cache()
         result["other_workloads"] = other
 
     if rank == 0:

@@ -166,6 +166,27 @@ OSM_ATTN_API int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void
                                         int64_t n_splits, void* stream);
 
 /*
+ * osm_softmax_topk -- the k largest entries of every row with their softmax shares, in one
+ * read of the row.
+ *
+ * "How FlashAttention avoids storing the giant score table" (spicyshark.co, Online softmax
+ * lesson), section "Where this is used in practice": the online normaliser also serves softmax
+ * fused with top-k selection, keeping only the k largest scores.  For row r:
+ * indices[r, 0..k) are the columns of the k largest x[r, :] in descending order (ties: the
+ * smaller column first), values[r, t] = exp(x[r, c] - m_r) / l_r for c = indices[r, t] (m_r
+ * the row max, l_r = sum_j exp(x[r, j] - m_r)), and lse[r] = m_r + ln l_r.
+ *
+ *   x        fp32 [rows, cols] contiguous, 4-byte aligned, read only; no NaN (NaN rows give
+ *            unspecified results).  A row of -inf gives values 0 and lse -inf.
+ *   k        1 .. min(cols, 32) (k > 32: FA_ERR_UNSUPPORTED; k > cols: FA_ERR_INVALID_ARG).
+ *   values   fp32 [rows, k], indices int32 [rows, k], lse fp32 [rows] or NULL; written; none
+ *            may overlap x or each other.
+ * rows == 0 is a no-op.  All pointers are device pointers; asynchronous on `stream`.
+ */
+OSM_ATTN_API int osm_softmax_topk(const float* x, int64_t rows, int64_t cols, int64_t k,
+                                  float* values, int32_t* indices, float* lse, void* stream);
+
+/*
  * osm_softmax -- y = softmax(x) of every row, single pass over HBM, and its log-sum-exp.
  *
  * Defines the operation of the same lesson, sections "The idea" and "The implementation":
@@ -209,7 +230,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 2
+#define OSM_ATTN_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_splitkv_plan.restype = ctypes.c_int
             L.osm_softmax.argtypes = [vp, vp, i64, i64, vp, vp]
             L.osm_softmax.restype = ctypes.c_int
+            L.osm_softmax_topk.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
+            L.osm_softmax_topk.restype = ctypes.c_int
             L.fa_status_string.argtypes = [ctypes.c_int]
             L.fa_status_string.restype = ctypes.c_char_p
             L.osm_attn_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -141,6 +143,11 @@ def gqa_plan(B, H, H_kv, Nq, Nk, d, n_splits=0):
 
 def osm_softmax_raw(x_ptr, y_ptr, rows, cols, lse_ptr, stream_ptr):
     return lib().osm_softmax(x_ptr, y_ptr, int(rows), int(cols), lse_ptr, stream_ptr)
+
+
+def osm_softmax_topk_raw(x_ptr, rows, cols, k, values_ptr, indices_ptr, lse_ptr, stream_ptr):
+    return lib().osm_softmax_topk(x_ptr, int(rows), int(cols), int(k), values_ptr, indices_ptr,
+                                  lse_ptr, stream_ptr)
 
 
 def selftest_wait(timeout_us: int, stream=None) -> None:
@@ -312,3 +319,27 @@ def osm_softmax(x, out=None, lse=None, return_lse=True, stream=None):
     if rc != FA_OK:
         raise FaError(rc, "osm_softmax")
     return out, lse
+
+
+def osm_softmax_topk(x, k, values=None, indices=None, lse=None, return_lse=True, stream=None):
+    """(values, indices, lse): the k largest entries of every row of a CUDA fp32 [rows, cols]
+    tensor in descending order (ties: the smaller column first), their softmax shares (fp32)
+    and columns (int32), and the rows' log-sum-exp."""
+    import torch
+
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32:
+        raise TypeError("x must be a CUDA fp32 tensor")
+    if x.dim() != 2 or not x.is_contiguous():
+        raise TypeError("x must be a contiguous [rows, cols] tensor")
+    rows, cols = x.shape
+    if values is None:
+        values = torch.empty((rows, k), dtype=torch.float32, device=x.device)
+    if indices is None:
+        indices = torch.empty((rows, k), dtype=torch.int32, device=x.device)
+    if lse is None and return_lse:
+        lse = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    rc = osm_softmax_topk_raw(x.data_ptr(), rows, cols, k, values.data_ptr(), indices.data_ptr(),
+                              lse.data_ptr() if lse is not None else None, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "osm_softmax_topk")
+    return values, indices, lse

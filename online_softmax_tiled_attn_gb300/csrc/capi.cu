@@ -181,6 +181,31 @@ int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
                           n_splits, ws_O, ws_LSE, stream);
 }
 
+int osm_softmax_topk(const float* x, int64_t rows, int64_t cols, int64_t k, float* values,
+                     int32_t* indices, float* lse, void* stream) {
+    if (rows < 0 || cols < 0 || k < 1) return FA_ERR_INVALID_ARG;
+    if (rows == 0) return FA_OK;
+    if (k > cols) return FA_ERR_INVALID_ARG;
+    if (k > 32) return FA_ERR_UNSUPPORTED;
+    int64_t elems, outs;
+    if (!mul_ok(rows, cols, &elems) || !mul_ok(rows, k, &outs) || elems > INT64_MAX / 4)
+        return FA_ERR_INVALID_ARG;
+    if (!x || !values || !indices) return FA_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(values, 4) || !aligned(indices, 4) || (lse && !aligned(lse, 4)))
+        return FA_ERR_INVALID_ARG;
+    const uint64_t x_bytes = static_cast<uint64_t>(elems) * 4;
+    const uint64_t o_bytes = static_cast<uint64_t>(outs) * 4;
+    const uint64_t l_bytes = static_cast<uint64_t>(rows) * 4;
+    if (overlaps(values, o_bytes, x, x_bytes) || overlaps(indices, o_bytes, x, x_bytes) ||
+        overlaps(values, o_bytes, indices, o_bytes))
+        return FA_ERR_INVALID_ARG;
+    if (lse && (overlaps(lse, l_bytes, x, x_bytes) || overlaps(lse, l_bytes, values, o_bytes) ||
+                overlaps(lse, l_bytes, indices, o_bytes)))
+        return FA_ERR_INVALID_ARG;
+    return osm::osm_softmax_topk_launch(x, rows, cols, k, values, indices, lse,
+                                        static_cast<cudaStream_t>(stream));
+}
+
 int osm_softmax(const float* x, float* y, int64_t rows, int64_t cols, float* lse,
                 void* stream) {
     if (rows < 0 || cols < 0) return FA_ERR_INVALID_ARG;

@@ -48,5 +48,7 @@ int selftest_wait_launch(long long timeout_us, cudaStream_t stream);
 
 int osm_softmax_launch(const float* x, float* y, int64_t rows, int64_t cols, float* lse,
                        cudaStream_t stream);
+int osm_softmax_topk_launch(const float* x, int64_t rows, int64_t cols, int64_t k, float* vals,
+                            int32_t* idx, float* lse, cudaStream_t stream);
 
 }  // namespace osm

@@ -1,0 +1,335 @@
+// osm_softmax_topk.cu -- softmax with top-k selection in one read of each row, for sm_103a.
+//
+// The method: "How FlashAttention avoids storing the giant score table" (spicyshark.co,
+// Online softmax lesson), section "Where this is used in practice": the online normaliser also
+// serves softmax fused with top-k selection (only the k largest scores are kept).  While a
+// thread streams its part of a row it keeps the running (m, l) of "The idea" and the k best
+// (value, column) pairs it has seen; the threads' partial states are then combined, (m, l) by
+// the two-worker merge of "From softmax to attention" and the top-k lists by repeatedly taking
+// the best head among the lists.  The outputs are the k columns with the largest x (ties: the
+// smaller column first), their shares y = exp(x - m) / l, and lse = m + ln l.
+//
+// GB300 mapping (HBM-bound: 4 bytes read per element, nothing written per element):
+//   * rows up to 4096 columns: one warp per row; longer rows: the 8 warps of a CTA share a row
+//     and their lists meet in shared memory;
+//   * 16-byte streaming loads when the row allows them;
+//   * the k best so far live across the lanes of a warp, one per lane; a new value is compared
+//     with the k-th best (the bar, the same in every lane), and the few that beat it are
+//     inserted with a ballot and a shuffle.  (Per-thread sorted lists, which most values of a
+//     short per-thread stream enter, measured 0.2-1 TB/s for k = 8..32.)
+//   * persistent grid, rows handed out round-robin.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "osm_internal.h"
+
+namespace osm {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ float ex2a(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// (x, j) ranks before (y, i): larger value first, then the smaller column.
+__device__ __forceinline__ bool before(float x, int j, float y, int i) {
+    return x > y || (x == y && j < i);
+}
+
+struct Stat {
+    float m, l;
+};
+
+__device__ __forceinline__ Stat merge(Stat a, Stat b) {
+    const float m = fmaxf(a.m, b.m);
+    if (m == -INFINITY) return Stat{-INFINITY, 0.f};
+    return Stat{m, a.l * ex2a((a.m - m) * kLog2e) + b.l * ex2a((b.m - m) * kLog2e)};
+}
+
+__device__ __forceinline__ Stat warp_merge(Stat s) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Stat o;
+        o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
+        o.l = __shfl_xor_sync(0xffffffffu, s.l, off);
+        s = merge(s, o);
+    }
+    return s;
+}
+
+// One block of the online recurrence: the values v[0..n) enter the state.
+template <int N>
+__device__ __forceinline__ void update(Stat& s, const float (&v)[N]) {
+    float mx = v[0];
+#pragma unroll
+    for (int e = 1; e < N; ++e) mx = fmaxf(mx, v[e]);
+    const float m = fmaxf(s.m, mx);
+    if (m == -INFINITY) return;  // nothing finite yet: adds nothing
+    float l = s.m == -INFINITY ? 0.f : s.l * ex2a((s.m - m) * kLog2e);
+#pragma unroll
+    for (int e = 0; e < N; ++e) l += ex2a((v[e] - m) * kLog2e);
+    s = Stat{m, l};
+}
+
+// The warp's k best (value, column) pairs so far, one per lane, best in lane 0; lanes >= k hold
+// nothing (-inf, INT_MAX).  The k-th best (lane k - 1) is the bar a new value must beat, so
+// once the bar has risen almost every value costs one comparison.
+struct WarpTop {
+    float v = -INFINITY;
+    int c = INT_MAX;
+    float bar_v = -INFINITY;  // the k-th best so far, the same in every lane
+    int bar_c = INT_MAX;
+
+    // Inserts (x, j), which ranks before the bar, at its place; the entries after it move down
+    // one lane and the k-th drops out.
+    __device__ __forceinline__ void insert(float x, int j, int k) {
+        const int lane = threadIdx.x & 31;
+        const unsigned ahead = __ballot_sync(0xffffffffu, lane < k && before(v, c, x, j));
+        const int pos = __popc(ahead);  // entries that stay ahead of (x, j)
+        const float uv = __shfl_up_sync(0xffffffffu, v, 1);
+        const int uc = __shfl_up_sync(0xffffffffu, c, 1);
+        if (lane < k) {
+            if (lane > pos) {
+                v = uv;
+                c = uc;
+            } else if (lane == pos) {
+                v = x;
+                c = j;
+            }
+        }
+        bar_v = __shfl_sync(0xffffffffu, v, k - 1);
+        bar_c = __shfl_sync(0xffffffffu, c, k - 1);
+    }
+    __device__ __forceinline__ void finish() {}
+
+    // Every lane offers n values (x[e], col[e]); one vote tells whether any lane holds a value
+    // that beats the bar, and those lanes' values are then inserted one at a time, each
+    // re-checked against the bar as it rises.
+    template <int N>
+    __device__ __forceinline__ void offer(const float (&x)[N], const int (&col)[N], int k) {
+        bool mine = false;
+#pragma unroll
+        for (int e = 0; e < N; ++e) mine |= before(x[e], col[e], bar_v, bar_c);
+        unsigned lanes = __ballot_sync(0xffffffffu, mine);
+        while (lanes) {
+            const int src = __ffs(lanes) - 1;
+            lanes &= lanes - 1;
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                const float xv = __shfl_sync(0xffffffffu, x[e], src);
+                const int xc = __shfl_sync(0xffffffffu, col[e], src);
+                if (before(xv, xc, bar_v, bar_c)) insert(xv, xc, k);
+            }
+        }
+    }
+};
+
+// k = 1: each lane keeps its own best (no vote per step); finish() leaves the warp's best in
+// lane 0 and nothing in the other lanes, as WarpTop holds it.
+struct LaneBest {
+    float v = -INFINITY;
+    int c = INT_MAX;
+
+    template <int N>
+    __device__ __forceinline__ void offer(const float (&x)[N], const int (&col)[N], int) {
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            if (before(x[e], col[e], v, c)) {
+                v = x[e];
+                c = col[e];
+            }
+    }
+    __device__ __forceinline__ void finish() {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+            const int oc = __shfl_xor_sync(0xffffffffu, c, off);
+            if (before(ov, oc, v, c)) {
+                v = ov;
+                c = oc;
+            }
+        }
+        if ((threadIdx.x & 31) != 0) {
+            v = -INFINITY;
+            c = INT_MAX;
+        }
+    }
+};
+
+// Streams the row part of thread t (of nthr threads sharing the row) into its state and the
+// warp's list.  All 32 lanes of a warp run the same iterations (the list lives across lanes).
+template <bool VEC, class Top>
+__device__ __forceinline__ void scan(const float* row, int cols, int t, int nthr, int k,
+                                     Stat& st, Top& top) {
+    const int lane = threadIdx.x & 31;
+    const int lane0 = t - lane;  // the warp's first thread
+    if constexpr (VEC) {
+        // Four 16-byte loads in flight per thread before any of them is used.
+        constexpr int kAhead = 4;
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+        const int n4 = cols >> 2;
+        for (int u0 = lane0; u0 < n4; u0 += kAhead * nthr) {
+            float4 q[kAhead];
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const int u = u0 + a * nthr + lane;
+                q[a] = u < n4 ? __ldcs(r4 + u)
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const int u = u0 + a * nthr + lane;
+                const float v[4] = {q[a].x, q[a].y, q[a].z, q[a].w};
+                const bool in = u < n4;
+                if (in) update(st, v);
+                // past the row: (-inf, INT_MAX) never beats the bar
+                const int col[4] = {in ? 4 * u : INT_MAX, in ? 4 * u + 1 : INT_MAX,
+                                    in ? 4 * u + 2 : INT_MAX, in ? 4 * u + 3 : INT_MAX};
+                top.offer(v, col, k);
+            }
+        }
+    } else {
+        // Four 4-byte loads per thread per step, columns nthr apart.
+        for (int j0 = lane0; j0 < cols; j0 += 4 * nthr) {
+            float v[4];
+            int col[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int j = j0 + a * nthr + lane;
+                const bool in = j < cols;
+                v[a] = in ? __ldcs(row + j) : -INFINITY;
+                col[a] = in ? j : INT_MAX;
+            }
+            update(st, v);  // -inf past the row adds nothing
+            top.offer(v, col, k);
+        }
+    }
+}
+
+// Lane t < k writes the t-th best with its share.
+template <class Top>
+__device__ __forceinline__ void write_top(const Top& top, int k, Stat s, float* vals, int* idx) {
+    const int lane = threadIdx.x & 31;
+    const float mu = s.m == -INFINITY ? 0.f : s.m;
+    const float inv_l = s.l > 0.f ? 1.f / s.l : 0.f;
+    if (lane < k) {
+        vals[lane] = ex2a((top.v - mu) * kLog2e) * inv_l;
+        idx[lane] = top.c;
+    }
+}
+
+template <bool VEC, class Top>
+__global__ void __launch_bounds__(kThreads) topk_warp_rows(const float* __restrict__ x,
+                                                           long long rows, int cols, int k,
+                                                           float* __restrict__ vals,
+                                                           int* __restrict__ idx,
+                                                           float* __restrict__ lse) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (long long r = static_cast<long long>(blockIdx.x) * kWarps + warp; r < rows;
+         r += static_cast<long long>(gridDim.x) * kWarps) {
+        Stat st{-INFINITY, 0.f};
+        Top top;
+        scan<VEC>(x + r * cols, cols, lane, 32, k, st, top);
+        top.finish();
+        st = warp_merge(st);
+        if (lse && lane == 0) lse[r] = st.m + logf(st.l);
+        write_top(top, k, st, vals + r * k, idx + r * k);
+    }
+}
+
+template <bool VEC, class Top>
+__global__ void __launch_bounds__(kThreads) topk_cta_rows(const float* __restrict__ x,
+                                                          long long rows, int cols, int k,
+                                                          float* __restrict__ vals,
+                                                          int* __restrict__ idx,
+                                                          float* __restrict__ lse) {
+    __shared__ float cv[kWarps][32];
+    __shared__ int cc[kWarps][32];
+    __shared__ Stat cs[kWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+        Stat st{-INFINITY, 0.f};
+        Top top;
+        scan<VEC>(x + r * cols, cols, threadIdx.x, kThreads, k, st, top);
+        top.finish();
+        st = warp_merge(st);
+        cv[warp][lane] = top.v;
+        cc[warp][lane] = top.c;
+        if (lane == 0) cs[warp] = st;
+        __syncthreads();
+        if (warp == 0) {
+            Stat s = lane < kWarps ? cs[lane] : Stat{-INFINITY, 0.f};
+            s = warp_merge(s);
+            if (lse && lane == 0) lse[r] = s.m + logf(s.l);
+            // The other warps' lists enter warp 0's list, one warp's list per step.
+            for (int w = 1; w < kWarps; ++w) {
+                const float v[1] = {cv[w][lane]};
+                const int col[1] = {cc[w][lane]};
+                top.offer(v, col, k);
+            }
+            top.finish();
+            write_top(top, k, s, vals + r * k, idx + r * k);
+        }
+        __syncthreads();  // the shared lists are refilled for the next row
+    }
+}
+
+int sm_count() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 0;
+    });
+    return n;
+}
+
+template <class Top>
+int launch(const float* x, long long rows, int cols, int k, float* vals, int* idx, float* lse,
+           cudaStream_t stream) {
+    const bool vec = (cols % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
+    const long long sms = sm_count() > 0 ? sm_count() : 148;
+    if (cols <= 4096) {
+        long long grid = (rows + kWarps - 1) / kWarps;
+        if (grid > sms * 8) grid = sms * 8;
+        if (vec)
+            topk_warp_rows<true, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+                x, rows, cols, k, vals, idx, lse);
+        else
+            topk_warp_rows<false, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+                x, rows, cols, k, vals, idx, lse);
+    } else {
+        long long grid = rows;
+        if (grid > sms * 8) grid = sms * 8;
+        if (vec)
+            topk_cta_rows<true, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+                x, rows, cols, k, vals, idx, lse);
+        else
+            topk_cta_rows<false, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+                x, rows, cols, k, vals, idx, lse);
+    }
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+int osm_softmax_topk_launch(const float* x, int64_t rows, int64_t cols, int64_t k, float* vals,
+                            int32_t* idx, float* lse, cudaStream_t stream) {
+    if (cols > INT_MAX / 2 || rows > (1LL << 40)) return FA_ERR_UNSUPPORTED;
+    if (k < 1 || k > 32) return FA_ERR_UNSUPPORTED;
+    const int c = static_cast<int>(cols), kk = static_cast<int>(k);
+    if (k == 1) return launch<LaneBest>(x, rows, c, kk, vals, idx, lse, stream);
+    return launch<WarpTop>(x, rows, c, kk, vals, idx, lse, stream);
+}
+
+}  // namespace osm

@@ -20,6 +20,8 @@ softmax_65536x4000    fp32 rows [65536, 4000], x = 9*N(0,1) and per row one entr
                       entry -100 at seeded positions
 decode_b8h32q1k32768  B8 H32, one query against 32768 cached keys, d128, N(0,1), non-causal
                       (the split-key path); seed 1007
+softmax_topk_*        the softmax workload's rows with top-k selection: [65536, 4000] k = 8 (seed
+                      1005, the same rows) and a vocabulary-sized [512, 131072] k = 32 (1011)
 gqa_*                 grouped key/value heads (H_kv < H) and per-sequence key lengths, N(0,1):
                       a causal prefill, a ragged-length batch and a grouped decode; seeds
                       1008-1010 (see GQA_WORKLOADS)
@@ -250,6 +252,34 @@ def sample_rows(w: AttnWorkload, per_head: int, seed_offset: int = 0):
         idx = torch.unique(idx)
         out.append(idx.to(torch.int64) + bh * w.N)
     return torch.cat(out).numpy()
+
+
+@dataclass(frozen=True)
+class TopkWorkload:
+    """Softmax with top-k selection over fp32 rows drawn as the softmax workload's."""
+
+    name: str
+    rows: int
+    cols: int
+    k: int
+    seed: int
+    std: float = 9.0
+    spike: float = 100.0
+
+    @property
+    def hbm_bytes(self) -> int:
+        """Compulsory HBM traffic: read x once; write k shares (fp32) and columns (int32) and
+        the lse (fp32) of every row."""
+        return self.rows * self.cols * 4 + self.rows * (self.k * 8 + 4)
+
+
+TOPK_WORKLOADS = {
+    w.name: w
+    for w in [
+        TopkWorkload("softmax_topk_65536x4000_k8", 65536, 4000, 8, 1005),
+        TopkWorkload("softmax_topk_512x131072_k32", 512, 131072, 32, 1011),
+    ]
+}
 
 
 def softmax_inputs(rows, cols, seed, std=9.0, spike=100.0):

@@ -25,7 +25,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "fa_fwd_gqa_plan",
-              "osm_softmax",
+              "osm_softmax", "osm_softmax_topk",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
@@ -50,7 +50,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 2
+    assert binding.lib().osm_attn_abi_version() == 3
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -149,6 +149,25 @@ def test_fa_fwd_gqa_rejects_on_host(args, want):
     if want == binding.FA_ERR_CUDA and torch.cuda.is_available():
         pytest.skip("reaches a launch; covered by the GPU tests on a machine with a GPU")
     assert binding.fa_fwd_gqa_raw(*args, None, None, None) == want
+
+
+@pytest.mark.parametrize(
+    "args, want",
+    [
+        ((P, -1, 10, 1, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),
+        ((P, 10, 10, 0, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),   # k = 0
+        ((P, 10, 10, 11, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),  # k > cols
+        ((P, 10, 100, 33, P + 40960, P + 81920, 0), binding.FA_ERR_UNSUPPORTED),  # k > 32
+        ((0, 0, 10, 4, 0, 0, 0), binding.FA_OK),                               # no rows
+        ((0, 10, 10, 4, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),   # x null
+        ((P + 2, 10, 10, 4, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),  # misaligned
+        ((P, 10, 10, 4, P + 200, P + 8192, 0), binding.FA_ERR_INVALID_ARG),    # values in x
+        ((P, 10, 10, 4, P + 4096, P + 4096 + 80, 0), binding.FA_ERR_INVALID_ARG),  # overlap
+        ((P, 10, 10, 4, P + 4096, P + 8192, P + 8192 + 8), binding.FA_ERR_INVALID_ARG),
+    ],
+)
+def test_osm_softmax_topk_rejects_on_host(args, want):
+    assert binding.osm_softmax_topk_raw(*args, None) == want
 
 
 def test_selftest_rejects_out_of_range_timeout_on_host():
