@@ -19,6 +19,9 @@ Functions (each a thin ctypes wrapper around ``oracle.c``; the arithmetic lives 
 * :func:`attention_gqa` -- the same with H_kv key/value heads shared by the H query heads (query
   head h reads key/value head h // (H // H_kv)) and optional per-sequence key lengths (keys at
   or past kv_lens[b] are masked like any other key: score -inf).
+* :func:`attention_bwd` -- the gradients dQ, dK, dV of the attention for an output gradient dO,
+  the derivative of the definition (the backward pass that recomputes the scores: "FlashAttention"
+  (paweldubiel.com notes), "Mechanism and details").
 * :func:`online_state` -- the pages' block-by-block streaming state (m, l, acc) of one score row
   with an optional trace.  Same lesson, sections "The idea", "From softmax to attention" and
   "A worked example by hand" (Tables 1 and 2); "kbwen.com FlashAttention" page, sections "Two
@@ -78,6 +81,11 @@ class Oracle:
                                      ctypes.c_int64, ctypes.c_double, ctypes.c_int, _i32p,
                                      _i64p, ctypes.c_int64, _dp, _dp, ctypes.c_int]
         lib.oracle_attn3.restype = ctypes.c_int
+        lib.oracle_attn_bwd.argtypes = [_u16p, _u16p, _u16p, _u16p, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_double, ctypes.c_int, _dp, _dp, _dp,
+                                         ctypes.c_int]
+        lib.oracle_attn_bwd.restype = ctypes.c_int
         lib.oracle_online_state.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                             _dp]
@@ -211,6 +219,23 @@ class Oracle:
             raise ValueError("oracle_attn3 rejected its arguments")
         return O, L
 
+    def attention_bwd(self, Q, K, V, dO, scale: float, causal: bool, nthreads: int = 0):
+        """Q, K, V, dO: bf16 [B, H, N, d] (bits or CPU torch bf16).  Returns fp64 (dQ, dK, dV)."""
+        Q, K, V, dO = (_as_bf16_bits(t) for t in (Q, K, V, dO))
+        if not (Q.shape == K.shape == V.shape == dO.shape) or Q.ndim != 4:
+            raise ValueError("Q, K, V, dO must share one [B, H, N, d] shape")
+        B, H, N, d = Q.shape
+        dQ = np.empty((B, H, N, d), dtype=np.float64)
+        dK = np.empty_like(dQ)
+        dV = np.empty_like(dQ)
+        rc = self._lib.oracle_attn_bwd(_ptr(Q, _u16p), _ptr(K, _u16p), _ptr(V, _u16p),
+                                       _ptr(dO, _u16p), B, H, N, d, float(scale),
+                                       int(bool(causal)), _ptr(dQ, _dp), _ptr(dK, _dp),
+                                       _ptr(dV, _dp), nthreads)
+        if rc != 0:
+            raise ValueError("oracle_attn_bwd rejected its arguments")
+        return dQ, dK, dV
+
     # -- streaming state ---------------------------------------------------------------------
     def online_state(self, s, v, block: int, trace: bool = False):
         """Stream scores s [n] with values v [n, dv] (or [n]) in blocks of `block`.
@@ -305,6 +330,10 @@ def attention_qk(Q, K, V, scale, causal, rows=None, nthreads: int = 0):
 
 def attention_gqa(Q, K, V, scale, causal, kv_lens=None, rows=None, nthreads: int = 0):
     return load().attention_gqa(Q, K, V, scale, causal, kv_lens, rows, nthreads)
+
+
+def attention_bwd(Q, K, V, dO, scale, causal, nthreads: int = 0):
+    return load().attention_bwd(Q, K, V, dO, scale, causal, nthreads)
 
 
 def online_state(s, v, block, trace=False):

@@ -35,6 +35,17 @@
  *     selection, keeping only the k largest scores); the shares are the three-pass softmax above
  *     and the selection is a plain sort of the row.
  *
+ *   the gradients of the attention (the backward pass): with P the softmax shares above, O the
+ *     output and dO the gradient of a loss with respect to O,
+ *        dV_j = sum_i P_ij dO_i,   dP_ij = dO_i . V_j,   D_i = dO_i . O_i,
+ *        dS_ij = P_ij (dP_ij - D_i),   dQ_i = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i
+ *     -- the chain rule through O = P V and the softmax (the derivative of a softmax share is
+ *     P_ij (delta - P_ik), which summed against dP gives P_ij (dP_ij - sum_k P_ik dP_ik) and
+ *     sum_k P_ik dP_ik = dO_i . O_i).  The pages say only that training recomputes the scores in
+ *     the backward pass instead of storing them ("FlashAttention" (paweldubiel.com notes),
+ *     "Mechanism and details"; the lesson's "Where this is used in practice"); the formulas are
+ *     the derivative of the definition, and the tests pin them by finite differences.
+ *
  *   the streaming state (m, l, acc) of one score row read in blocks, and the merge of two such
  *   states: same lesson, sections "The idea", "From softmax to attention" (the block recipe)
  *   and the two-worker merge at the end of "From softmax to attention"; "kbwen.com
@@ -50,7 +61,7 @@
  *     of an empty state keeps the other state.
  *   - bf16 inputs are widened exactly (bits << 16) to fp32, then to fp64.
  *
- * Mutants: building with -DORACLE_MUTANT=k plants one deliberate mistake (k = 1..15) so the
+ * Mutants: building with -DORACLE_MUTANT=k plants one deliberate mistake (k = 1..18) so the
  * tests can show that the pins catch it.  The default build (no define) has none.
  */
 #include <math.h>
@@ -395,6 +406,124 @@ int oracle_attn3(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_
     }
     for (int t = 1; t < nt; ++t) pthread_create(&th[t], NULL, attn_worker, &jobs[t]);
     attn_worker(&jobs[0]);
+    int err = 0;
+    for (int t = 1; t < nt; ++t) pthread_join(th[t], NULL);
+    for (int t = 0; t < nt; ++t) err |= jobs[t].err;
+    free(th); free(jobs);
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Attention gradients.                                                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *Q, *K, *V, *dO;
+    int64_t N, d;
+    double scale;
+    int causal;
+    double *dQ, *dK, *dV;
+    int64_t h0, h1; /* heads [h0, h1) of the flat (b*H + h) index */
+    int err;
+} bwd_job;
+
+static void* bwd_worker(void* arg) {
+    bwd_job* jb = (bwd_job*)arg;
+    const int64_t N = jb->N, d = jb->d;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double* q = (double*)malloc(sizeof(double) * (size_t)d);
+    double* o = (double*)malloc(sizeof(double) * (size_t)d);
+    double* g = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!s || !q || !o || !g) { jb->err = 1; free(s); free(q); free(o); free(g); return NULL; }
+    for (int64_t bh = jb->h0; bh < jb->h1; ++bh) {
+        const uint16_t* Qh = jb->Q + bh * N * d;
+        const uint16_t* Kh = jb->K + bh * N * d;
+        const uint16_t* Vh = jb->V + bh * N * d;
+        const uint16_t* Gh = jb->dO + bh * N * d;
+        double* dQh = jb->dQ + bh * N * d;
+        double* dKh = jb->dK + bh * N * d;
+        double* dVh = jb->dV + bh * N * d;
+        for (int64_t t = 0; t < N * d; ++t) { dQh[t] = 0.0; dKh[t] = 0.0; dVh[t] = 0.0; }
+        for (int64_t i = 0; i < N; ++i) {
+            const int64_t nk = jb->causal ? i + 1 : N;
+            for (int64_t k = 0; k < d; ++k) {
+                q[k] = bf16_to_double(Qh[i * d + k]);
+                g[k] = bf16_to_double(Gh[i * d + k]);
+            }
+            /* the shares P_ij of row i (three passes, as the forward definition) */
+            double m = -INFINITY;
+            for (int64_t j = 0; j < nk; ++j) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < d; ++k) acc += q[k] * bf16_to_double(Kh[j * d + k]);
+                s[j] = jb->scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < nk; ++j) l += exp(s[j] - m);
+            for (int64_t j = 0; j < nk; ++j) s[j] = exp(s[j] - m) / l; /* s now holds P_ij */
+            /* O_i and D_i = dO_i . O_i */
+            for (int64_t k = 0; k < d; ++k) o[k] = 0.0;
+            for (int64_t j = 0; j < nk; ++j)
+                for (int64_t k = 0; k < d; ++k) o[k] += s[j] * bf16_to_double(Vh[j * d + k]);
+            double D = 0.0;
+            for (int64_t k = 0; k < d; ++k) D += g[k] * o[k];
+#if ORACLE_MUTANT == 16
+            D = 0.0; /* mutant: drops the D_i term */
+#endif
+            for (int64_t j = 0; j < nk; ++j) {
+                const double p = s[j];
+                double dp = 0.0;
+                for (int64_t k = 0; k < d; ++k) {
+                    dp += g[k] * bf16_to_double(Vh[j * d + k]);
+                    dVh[j * d + k] += p * g[k];
+                }
+#if ORACLE_MUTANT == 17
+                const double ds = p * (D - dp); /* mutant: sign of dS flipped */
+#else
+                const double ds = p * (dp - D);
+#endif
+#if ORACLE_MUTANT == 18
+                const double sc = 1.0; /* mutant: forgets the scale in dQ and dK */
+#else
+                const double sc = jb->scale;
+#endif
+                for (int64_t k = 0; k < d; ++k) {
+                    dQh[i * d + k] += sc * ds * bf16_to_double(Kh[j * d + k]);
+                    dKh[j * d + k] += sc * ds * q[k];
+                }
+            }
+        }
+    }
+    free(s); free(q); free(o); free(g);
+    return NULL;
+}
+
+/*
+ * Gradients of O = softmax(scale Q K^T [causal]) V with respect to Q, K and V for the output
+ * gradient dO.  Q, K, V, dO: bf16 bit patterns [B, H, N, d]; dQ, dK, dV: fp64 [B, H, N, d].
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_bwd(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const uint16_t* dO,
+                    int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                    double* dQ, double* dK, double* dV, int nthreads) {
+    if (B < 0 || H < 0 || N < 0 || d < 1) return -1;
+    const int64_t heads = B * H;
+    if (heads == 0 || N == 0) return 0;
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return -1;
+    int nt = resolve_threads(nthreads);
+    if (nt > heads) nt = (int)heads;
+    pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+    bwd_job* jobs = (bwd_job*)calloc((size_t)nt, sizeof(bwd_job));
+    if (!th || !jobs) { free(th); free(jobs); return -1; }
+    for (int t = 0; t < nt; ++t) {
+        bwd_job* jb = &jobs[t];
+        jb->Q = Q; jb->K = K; jb->V = V; jb->dO = dO; jb->N = N; jb->d = d; jb->scale = scale;
+        jb->causal = causal; jb->dQ = dQ; jb->dK = dK; jb->dV = dV;
+        jb->h0 = heads * t / nt;
+        jb->h1 = heads * (t + 1) / nt;
+    }
+    for (int t = 1; t < nt; ++t) pthread_create(&th[t], NULL, bwd_worker, &jobs[t]);
+    bwd_worker(&jobs[0]);
     int err = 0;
     for (int t = 1; t < nt; ++t) pthread_join(th[t], NULL);
     for (int t = 0; t < nt; ++t) err |= jobs[t].err;

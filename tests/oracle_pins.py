@@ -356,6 +356,69 @@ def pin_softmax_topk_full_is_sorted_softmax(orc):
     assert np.array_equal(lse, l2) and np.array_equal(v1[:, 0], y.max(axis=1))
 
 
+def _forward_fp64(q, k, v, scale, causal):
+    """O of the definition in plain numpy fp64 (an implementation independent of the oracle),
+    [H, N, d] inputs."""
+    s = scale * np.einsum("hid,hjd->hij", q, k)
+    if causal:
+        n = s.shape[-1]
+        s = np.where(np.tril(np.ones((n, n), bool)), s, -np.inf)
+    p = np.exp(s - s.max(axis=-1, keepdims=True))
+    p /= p.sum(axis=-1, keepdims=True)
+    return np.einsum("hij,hjd->hid", p, v)
+
+
+def pin_attention_bwd_finite_differences(orc):
+    """The gradients against central differences of L = sum(dO * O) through the definition."""
+    for causal in (False, True):
+        q, k, v = inputs.attn_inputs(1, 2, 5, 3, seed=501 + causal)
+        g, _, _ = inputs.attn_inputs(1, 2, 5, 3, seed=601 + causal)
+        dQ, dK, dV = orc.attention_bwd(q, k, v, g, 0.7, causal)
+        qf, kf, vf, gf = (_bf16_float(t)[0].astype(np.float64) for t in (q, k, v, g))
+
+        def loss(qq, kk, vv):
+            return float((gf * _forward_fp64(qq, kk, vv, 0.7, causal)).sum())
+
+        eps = 1e-5
+        for which, grad in ((0, dQ), (1, dK), (2, dV)):
+            args = [qf, kf, vf]
+            num = np.zeros_like(qf)
+            for idx in np.ndindex(qf.shape):
+                plus = [a.copy() for a in args]
+                minus = [a.copy() for a in args]
+                plus[which][idx] += eps
+                minus[which][idx] -= eps
+                num[idx] = (loss(*plus) - loss(*minus)) / (2 * eps)
+            assert np.abs(grad[0] - num).max() < 1e-7 * max(1.0, np.abs(num).max()), (which, causal)
+
+
+def pin_attention_bwd_key_gradients_sum_to_zero(orc):
+    """Each row of dS sums to zero (the softmax's shares sum to one), so the key gradients of a
+    head sum to the zero vector: sum_j dK_j = scale sum_i Q_i sum_j dS_ij = 0."""
+    q, k, v = inputs.attn_inputs(2, 2, 33, 8, seed=701)
+    g, _, _ = inputs.attn_inputs(2, 2, 33, 8, seed=702)
+    for causal in (False, True):
+        _, dK, _ = orc.attention_bwd(q, k, v, g, 0.4, causal)
+        assert np.abs(dK.sum(axis=2)).max() < 1e-12, causal
+
+
+def pin_attention_bwd_uniform_scores(orc):
+    """Q = 0: every allowed key gets the same share, so dV_j = sum over the queries that see
+    key j of dO_i / (their number of keys): the mean of dO (non-causal), sum_{i>=j} dO_i/(i+1)
+    (causal)."""
+    N, d = 6, 4
+    _, k, v = inputs.attn_inputs(1, 1, N, d, seed=801)
+    g, _, _ = inputs.attn_inputs(1, 1, N, d, seed=802)
+    q = k.clone()
+    q.zero_()
+    gf = _bf16_float(g)[0, 0].astype(np.float64)
+    _, _, dV = orc.attention_bwd(q, k, v, g, 0.5, False)
+    assert np.abs(dV[0, 0] - gf.mean(axis=0)).max() < 1e-14
+    _, _, dV = orc.attention_bwd(q, k, v, g, 0.5, True)
+    want = np.array([sum(gf[i] / (i + 1) for i in range(j, N)) for j in range(N)])
+    assert np.abs(dV[0, 0] - want).max() < 1e-14
+
+
 # ----------------------------------------------------------------------------------------------
 # closed forms
 # ----------------------------------------------------------------------------------------------

@@ -23,6 +23,9 @@ MUTANTS = {
     13: "per-sequence key lengths ignored",
     14: "top-k ties go to the larger column",
     15: "top-k skips the largest entry",
+    16: "backward drops the D term of dS",
+    17: "backward flips the sign of dS",
+    18: "backward forgets the scale in dQ and dK",
 }
 
 
