@@ -357,6 +357,38 @@ def time_gqa(w, steps, warmup, device, flush):
     return [a.elapsed_time(b) for a, b in ev], splits
 
 
+def time_bwd(w, steps, warmup, device, flush):
+    """Per-call device time (ms) of fa_bwd (its three launches) on a backward workload; the
+    forward's O and LSE and the workspace are made outside the timed region."""
+    import torch
+
+    from online_softmax_tiled_attn_gb300 import binding, inputs
+
+    qd, kd, vd, gd = (t.to(device) for t in inputs.bwd_inputs(w.B, w.H, w.N, w.d, w.seed))
+    O, L = binding.fa_fwd(qd, kd, vd, scale=w.scale, causal=w.causal)
+    ws = (torch.empty(qd.numel(), dtype=torch.float32, device=device),
+          torch.empty(qd.numel() // w.d, dtype=torch.float32, device=device))
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        binding.fa_bwd(qd, kd, vd, O, gd, L, scale=w.scale, causal=w.causal, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    if binding.device_status() != 0:
+        raise RuntimeError("fa_bwd reported a device status")
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def roofline_tensor(flops, ms, peaks, kind, traffic=None):
     achieved = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -484,6 +516,8 @@ def main(argv=None):
                     help="with --profile: launch fa_fwd_splitkv on the decode workload")
     ap.add_argument("--gqa", default=None,
                     help="with --profile: launch fa_fwd_gqa on this grouped-head workload")
+    ap.add_argument("--bwd", default=None,
+                    help="with --profile: launch fa_bwd on this backward workload")
     ap.add_argument("--topk", default=None,
                     help="with --profile: launch osm_softmax_topk on this top-k workload")
     args = ap.parse_args(argv)
@@ -507,7 +541,9 @@ def main(argv=None):
     w = inputs.ATTN_WORKLOADS[args.workload]
 
     if args.profile:
-        if args.topk:
+        if args.bwd:
+            time_bwd(inputs.BWD_WORKLOADS[args.bwd], args.steps, args.warmup, device, None)
+        elif args.topk:
             time_topk(inputs.TOPK_WORKLOADS[args.topk], args.steps, args.warmup, device, None)
         elif args.gqa:
             time_gqa(inputs.GQA_WORKLOADS[args.gqa], args.steps, args.warmup, device, None)
@@ -609,6 +645,14 @@ def main(argv=None):
                            "ms_per_step": round(tms, 4),
                            "roofline": roofline_hbm(tw.hbm_bytes, tms, peaks, peaks_kind,
                                                     NCU_TRAFFIC_BYTES.get(name))}
+            torch.cuda.empty_cache()
+        for name, bw in inputs.BWD_WORKLOADS.items():
+            t = time_bwd(bw, 20, 3, device, flush)
+            bms = max_over_ranks(sum(t) / len(t), dist, device)
+            other[name] = {"TFLOP/s": round(world * bw.flops / (bms * 1e-3) / 1e12, 2),
+                           "ms_per_step": round(bms, 4),
+                           "roofline": roofline_tensor(bw.flops, bms, peaks, peaks_kind,
+                                                       NCU_TRAFFIC_BYTES.get(name))}
             torch.cuda.empty_cache()
         result["other_workloads"] = other
 

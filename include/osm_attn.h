@@ -166,6 +166,33 @@ OSM_ATTN_API int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void
                                         int64_t n_splits, void* stream);
 
 /*
+ * fa_bwd -- the gradients dQ, dK, dV of fa_fwd's attention for an output gradient dO.
+ *
+ * "FlashAttention" (paweldubiel.com notes), "Mechanism and details", and "How FlashAttention
+ * avoids storing the giant score table" (spicyshark.co, Online softmax lesson), "Where this is
+ * used in practice": training recomputes the scores in the backward pass instead of storing
+ * them.  With the forward's LSE the shares are P_ij = exp(scale q_i . k_j - LSE_i); the
+ * gradients are the derivative of the definition: D_i = dO_i . O_i, dP_ij = dO_i . v_j,
+ * dS_ij = P_ij (dP_ij - D_i), dQ_i = scale sum_j dS_ij k_j, dK_j = scale sum_i dS_ij q_i,
+ * dV_j = sum_i P_ij dO_i (causal: only the pairs j <= i).
+ *
+ *   Q, K, V, O, dO  bf16 [B, H, N, d] contiguous, 16-byte aligned, read only (O and LSE as
+ *            fa_fwd wrote them for the same Q, K, V, scale and causal).
+ *   LSE      fp32 [B, H, N], read only.
+ *   dQ, dK, dV  bf16 [B, H, N, d], 16-byte aligned, written.
+ *   ws_dQ    fp32 workspace of B*H*N*d floats, 16-byte aligned; ws_D fp32 workspace of B*H*N
+ *            floats.  Owned by the caller, overwritten.  No output or workspace may overlap an
+ *            input or another output.
+ *   d        64 or 128; scale finite and > 0.  B*H*N == 0 is a no-op.
+ * Precision: P and dS are rounded to bf16 for the tensor-core products, which accumulate in
+ * fp32; dQ is summed in fp32 over the key tiles.  Errors as fa_fwd.
+ */
+OSM_ATTN_API int fa_bwd(const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                        float* ws_dQ, float* ws_D, int64_t B, int64_t H, int64_t N, int64_t d,
+                        float scale, int causal, void* stream);
+
+/*
  * osm_softmax_topk -- the k largest entries of every row with their softmax shares, in one
  * read of the row.
  *
@@ -230,7 +257,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 3
+#define OSM_ATTN_ABI_VERSION 4
 
 #ifdef __cplusplus
 }

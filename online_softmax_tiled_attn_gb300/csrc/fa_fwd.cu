@@ -1000,6 +1000,17 @@ int selftest_wait_launch(long long timeout_us, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int* device_status_word() {
+    static int* addr = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fa_device_status) == cudaSuccess)
+            addr = static_cast<int*>(p);
+    });
+    return addr;
+}
+
 int fa_read_device_status(cudaStream_t stream, int* status) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
     int v = 0;

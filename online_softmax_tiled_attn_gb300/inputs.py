@@ -216,6 +216,55 @@ SOFTMAX_WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class BwdWorkload:
+    """Gradients of attention over Q, K, V, dO [B, H, N, d] (O and LSE from the forward)."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOP: 10*B*H*N^2*d (five N x N x d contractions: S, dP, dV, dK, dQ),
+        halved when causal."""
+        f = 10.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2.0 if self.causal else f
+
+    @property
+    def hbm_bytes(self) -> int:
+        """Compulsory HBM traffic: read Q, K, V, O, dO (bf16) and LSE (fp32), write dQ, dK, dV
+        (bf16)."""
+        n = self.B * self.H * self.N
+        return 8 * n * self.d * 2 + n * 4
+
+
+BWD_WORKLOADS = {
+    w.name: w
+    for w in [
+        BwdWorkload("bwd_b4h16n2048d64", 4, 16, 2048, 64, False, 1012),
+        BwdWorkload("bwd_b2h16n8192d128", 2, 16, 8192, 128, False, 1013),
+        BwdWorkload("bwd_causal_b2h16n8192d128", 2, 16, 8192, 128, True, 1014),
+    ]
+}
+
+
+def bwd_inputs(B, H, N, d, seed):
+    """Q, K, V, dO as CPU bf16 tensors [B, H, N, d], N(0,1), drawn in that order from one seeded
+    generator."""
+    g = torch.Generator().manual_seed(int(seed))
+    shape = (B, H, N, d)
+    return tuple(torch.randn(shape, generator=g).to(torch.bfloat16) for _ in range(4))
+
+
 def attn_inputs(B, H, N, d, seed, qk_std=1.0, v_dist="normal"):
     """Q, K, V as CPU bf16 tensors [B, H, N, d] drawn from one seeded generator."""
     g = torch.Generator().manual_seed(int(seed))

@@ -25,7 +25,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "fa_fwd_gqa_plan",
-              "osm_softmax", "osm_softmax_topk",
+              "osm_softmax", "osm_softmax_topk", "fa_bwd",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
@@ -50,7 +50,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 3
+    assert binding.lib().osm_attn_abi_version() == 4
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -168,6 +168,38 @@ def test_fa_fwd_gqa_rejects_on_host(args, want):
 )
 def test_osm_softmax_topk_rejects_on_host(args, want):
     assert binding.osm_softmax_topk_raw(*args, None) == want
+
+
+def _bwd_args(**over):
+    """fa_bwd arguments for B1 H1 N128 d64 at distinct fake addresses (16 KiB per tensor)."""
+    T = 128 * 64 * 2
+    a = dict(q=P, k=P + T, v=P + 2 * T, o=P + 3 * T, do=P + 4 * T, lse=P + 5 * T,
+             dq=P + 6 * T, dk=P + 7 * T, dv=P + 8 * T, ws_dq=P + 9 * T, ws_d=P + 11 * T,
+             B=1, H=1, N=128, d=64, scale=0.125, causal=0)
+    a.update(over)
+    return a
+
+
+@pytest.mark.parametrize(
+    "over, want",
+    [
+        (dict(N=-1), binding.FA_ERR_INVALID_ARG),
+        (dict(N=0), binding.FA_OK),
+        (dict(d=96), binding.FA_ERR_UNSUPPORTED),
+        (dict(scale=0.0), binding.FA_ERR_INVALID_ARG),
+        (dict(dq=0), binding.FA_ERR_INVALID_ARG),
+        (dict(dk=P + 2), binding.FA_ERR_INVALID_ARG),          # misaligned
+        (dict(dv=P + 64), binding.FA_ERR_INVALID_ARG),         # dV inside Q
+        (dict(ws_dq=P + 6 * 16384), binding.FA_ERR_INVALID_ARG),  # workspace on dQ
+        (dict(ws_d=P + 5 * 16384), binding.FA_ERR_INVALID_ARG),   # workspace on LSE
+    ],
+)
+def test_fa_bwd_rejects_on_host(over, want):
+    a = _bwd_args(**over)
+    rc = binding.fa_bwd_raw(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
+                            a["dv"], a["ws_dq"], a["ws_d"], a["B"], a["H"], a["N"], a["d"],
+                            a["scale"], a["causal"], None)
+    assert rc == want
 
 
 def test_selftest_rejects_out_of_range_timeout_on_host():
