@@ -366,8 +366,7 @@ def time_bwd(w, steps, warmup, device, flush):
 
     qd, kd, vd, gd = (t.to(device) for t in inputs.bwd_inputs(w.B, w.H, w.N, w.d, w.seed))
     O, L = binding.fa_fwd(qd, kd, vd, scale=w.scale, causal=w.causal)
-    ws = (torch.empty(qd.numel(), dtype=torch.float32, device=device),
-          torch.empty(qd.numel() // w.d, dtype=torch.float32, device=device))
+    ws = torch.empty(qd.numel() // w.d, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
     def call():

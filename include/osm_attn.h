@@ -180,17 +180,16 @@ OSM_ATTN_API int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void
  *            fa_fwd wrote them for the same Q, K, V, scale and causal).
  *   LSE      fp32 [B, H, N], read only.
  *   dQ, dK, dV  bf16 [B, H, N, d], 16-byte aligned, written.
- *   ws_dQ    fp32 workspace of B*H*N*d floats, 16-byte aligned; ws_D fp32 workspace of B*H*N
- *            floats.  Owned by the caller, overwritten.  No output or workspace may overlap an
- *            input or another output.
+ *   ws_D     fp32 workspace of B*H*N floats (D_i), 4-byte aligned, owned by the caller and
+ *            overwritten.  No output or the workspace may overlap an input or another output.
  *   d        64 or 128; scale finite and > 0.  B*H*N == 0 is a no-op.
  * Precision: P and dS are rounded to bf16 for the tensor-core products, which accumulate in
- * fp32; dQ is summed in fp32 over the key tiles.  Errors as fa_fwd.
+ * fp32 in a fixed order (the results repeat bit for bit).  Errors as fa_fwd.
  */
 OSM_ATTN_API int fa_bwd(const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-                        float* ws_dQ, float* ws_D, int64_t B, int64_t H, int64_t N, int64_t d,
-                        float scale, int causal, void* stream);
+                        float* ws_D, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                        int causal, void* stream);
 
 /*
  * osm_softmax_topk -- the k largest entries of every row with their softmax shares, in one
@@ -257,7 +256,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 4
+#define OSM_ATTN_ABI_VERSION 5
 
 #ifdef __cplusplus
 }

@@ -64,7 +64,7 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_splitkv_plan.restype = ctypes.c_int
             L.osm_softmax.argtypes = [vp, vp, i64, i64, vp, vp]
             L.osm_softmax.restype = ctypes.c_int
-            L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
+            L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                  ctypes.c_float, ctypes.c_int, vp]
             L.fa_bwd.restype = ctypes.c_int
             L.osm_softmax_topk.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
@@ -148,10 +148,9 @@ def osm_softmax_raw(x_ptr, y_ptr, rows, cols, lse_ptr, stream_ptr):
     return lib().osm_softmax(x_ptr, y_ptr, int(rows), int(cols), lse_ptr, stream_ptr)
 
 
-def fa_bwd_raw(q, k, v, o, do, lse, dq, dk, dv, ws_dq, ws_d, B, H, N, d, scale, causal,
-               stream_ptr):
-    return lib().fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws_dq, ws_d, int(B), int(H), int(N),
-                        int(d), float(scale), int(bool(causal)), stream_ptr)
+def fa_bwd_raw(q, k, v, o, do, lse, dq, dk, dv, ws_d, B, H, N, d, scale, causal, stream_ptr):
+    return lib().fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws_d, int(B), int(H), int(N), int(d),
+                        float(scale), int(bool(causal)), stream_ptr)
 
 
 def osm_softmax_topk_raw(x_ptr, rows, cols, k, values_ptr, indices_ptr, lse_ptr, stream_ptr):
@@ -356,8 +355,8 @@ def osm_softmax_topk(x, k, values=None, indices=None, lse=None, return_lse=True,
 
 def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, workspace=None, stream=None):
     """(dQ, dK, dV) of fa_fwd's attention for the output gradient do (CUDA bf16 [B,H,N,d]),
-    given the forward's o and lse.  `workspace` may be a (ws_dQ [B*H*N*d], ws_D [B*H*N]) pair
-    of fp32 CUDA tensors; otherwise it is allocated here (the library never allocates)."""
+    given the forward's o and lse.  `workspace` may be an fp32 CUDA tensor of B*H*N floats;
+    otherwise it is allocated here (the library never allocates)."""
     import torch
 
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
@@ -373,14 +372,11 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, workspace=None, stream
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    if workspace is None:
-        ws_dq = torch.empty(B * H * N * d, dtype=torch.float32, device=q.device)
-        ws_d = torch.empty(B * H * N, dtype=torch.float32, device=q.device)
-    else:
-        ws_dq, ws_d = workspace
+    ws_d = (torch.empty(B * H * N, dtype=torch.float32, device=q.device) if workspace is None
+            else workspace)
     rc = fa_bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws_dq.data_ptr(),
-                    ws_d.data_ptr(), B, H, N, d, scale, causal, _stream_handle(stream))
+                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws_d.data_ptr(),
+                    B, H, N, d, scale, causal, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv

@@ -182,8 +182,8 @@ int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-           const float* LSE, void* dQ, void* dK, void* dV, float* ws_dQ, float* ws_D, int64_t B,
-           int64_t H, int64_t N, int64_t d, float scale, int causal, void* stream) {
+           const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t B, int64_t H,
+           int64_t N, int64_t d, float scale, int causal, void* stream) {
     if (B < 0 || H < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
     int64_t bh, rows, elems;
     if (!mul_ok(B, H, &bh) || !mul_ok(bh, N, &rows) || !mul_ok(rows, d, &elems) ||
@@ -193,22 +193,22 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
     const void* ins[6] = {Q, K, V, O, dO, LSE};
-    const void* outs[5] = {dQ, dK, dV, ws_dQ, ws_D};
+    const void* outs[4] = {dQ, dK, dV, ws_D};
     const uint64_t t_bytes = static_cast<uint64_t>(elems) * 2;  // one bf16 tensor
     const uint64_t r_bytes = static_cast<uint64_t>(rows) * 4;   // one fp32 value per row
     const uint64_t in_bytes[6] = {t_bytes, t_bytes, t_bytes, t_bytes, t_bytes, r_bytes};
-    const uint64_t out_bytes[5] = {t_bytes, t_bytes, t_bytes, 2 * t_bytes, r_bytes};
+    const uint64_t out_bytes[4] = {t_bytes, t_bytes, t_bytes, r_bytes};
     for (int i = 0; i < 6; ++i)
         if (!ins[i] || !aligned(ins[i], i < 5 ? 16 : 4)) return FA_ERR_INVALID_ARG;
-    for (int i = 0; i < 5; ++i)
-        if (!outs[i] || !aligned(outs[i], i < 4 ? 16 : 4)) return FA_ERR_INVALID_ARG;
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 4; ++i)
+        if (!outs[i] || !aligned(outs[i], i < 3 ? 16 : 4)) return FA_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i) {
         for (int j = 0; j < 6; ++j)
             if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return FA_ERR_INVALID_ARG;
-        for (int j = i + 1; j < 5; ++j)
+        for (int j = i + 1; j < 4; ++j)
             if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return FA_ERR_INVALID_ARG;
     }
-    return osm::fa_bwd_launch(Q, K, V, O, dO, LSE, dQ, dK, dV, ws_dQ, ws_D, bh, N, d, scale,
+    return osm::fa_bwd_launch(Q, K, V, O, dO, LSE, dQ, dK, dV, ws_D, bh, N, d, scale,
                               causal != 0, static_cast<cudaStream_t>(stream));
 }
 

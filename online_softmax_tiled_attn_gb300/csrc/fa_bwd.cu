@@ -9,25 +9,28 @@
 //     dV_j = sum_i P_ij dO_i,  dP_ij = dO_i . V_j,  D_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - D_i),
 //     dQ_i = scale sum_j dS_ij K_j,  dK_j = scale sum_i dS_ij Q_i.
 //
-// GB300 mapping.  One CTA (4 warps) per (head, 128-key tile) walks the query tiles that see
-// its keys.  Every product runs on the tensor cores (tcgen05.mma, fp32 accumulators in TMEM),
-// issued by one thread:
-//   S^T  = K Q^T    (keys x queries)      A = K, B = Q      shared memory
-//   dP^T = V dO^T   (keys x queries)      A = V, B = dO     shared memory
-//   dV  += P^T dO   (keys x d)            A = P^T (TMEM, bf16), B = dO
-//   dK  += dS^T Q   (keys x d)            A = dS^T (TMEM, bf16), B = Q
-//   dQ_i = dS K     (queries x d)         A = dS (shared memory, written by the threads), B = K
-// Thread r owns key row r (its TMEM lane) for P and dS and query row r for dQ_i, whose fp32
-// partial sums are added to a workspace with vector reductions (each query tile receives one
-// from every key tile); a last kernel scales it by `scale` into bf16 dQ.  D is computed first
-// by its own kernel.  The steps of a query tile run one after the other (load, two products,
-// shares, three products, dQ out): this kernel is written for clarity, not yet overlapped.
-// TMEM (512 columns): S^T [0,128), whose 32-column groups, once read, take P^T and dS^T of the
-// same queries (P^T in the first 16 columns of a group, dS^T in the last 16); dP^T [128,256)
-// then dQ_i [128, 128 + d); dV [256, 256 + d); dK [256 + d, 256 + 2d).
+// GB300 mapping: three launches on the caller's stream.
+//   1. bwd_prep_kernel: D_i = dO_i . O_i (fp32, one warp per row).
+//   2. bwd_kv_kernel: one CTA per (head, 128-key tile) walks the query tiles that see its
+//      keys and accumulates dK and dV of its keys in TMEM (keys = TMEM lanes).
+//   3. bwd_q_kernel: one CTA per (head, 128-query tile) walks the key tiles its queries see,
+//      recomputes S and dP and accumulates dQ in TMEM (queries = TMEM lanes).
+// Computing dQ by its own pass costs two more products per tile pair than adding per-key-tile
+// partial sums of dQ into memory, but on this part the L2 reductions that the partial sums
+// need (64 KB per tile pair) run slower than the products they would save, and the pass
+// leaves every gradient deterministic: each is summed in a fixed order.
 //
-// Every wait is bounded; a wait that gives up records FA_ERR_TIMEOUT and the CTA stops after
-// draining its own loads and products.
+// Both tile kernels put their roles on separate warps so that loads, tensor-core products and
+// element-wise work overlap:
+//   warp 16      TMA loads (the CTA's own tile once, the walked tiles into a two-stage ring).
+//   warp 17      one thread issues every tcgen05.mma (bf16 operands, fp32 accumulators).
+//   warps 0-15   the element-wise work, thread = TMEM lane (row), four warps per 32 lanes
+//                with 16 of each 64 columns each (enough warps to hide the TMEM load and
+//                store latencies); a tile's first half of the walked rows is handed to the
+//                tensor cores before the second half is computed.  They also write the CTA's
+//                gradients at the end.
+// Every wait is bounded; a wait that gives up records FA_ERR_TIMEOUT and its role stops; the
+// CTA drains its own loads and products before it frees TMEM and exits.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -40,57 +43,72 @@ namespace osm {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 128;
 constexpr int kHalf = 128 * 128;  // bytes of one 64-column half of a 128-row bf16 tile
+constexpr int kSoftWarps = 16;    // warps 0-15
+constexpr int kTmaWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 18 * 32;
 constexpr uint64_t kDrainNs = 1000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
-struct BwdCfg {
-    static constexpr int kTileBytes = (D / 64) * kHalf;
-    static constexpr int kK = 0;
-    static constexpr int kV = kK + kTileBytes;
-    static constexpr int kQ = kV + kTileBytes;
-    static constexpr int kG = kQ + kTileBytes;   // dO
-    static constexpr int kS = kG + kTileBytes;   // dS^T, 128 keys x 128 queries bf16
-    static constexpr int kLse = kS + 2 * kHalf;  // 128 floats
-    static constexpr int kDd = kLse + 512;       // 128 floats
-    static constexpr int kBar = kDd + 512;       // mbarriers
-    static constexpr int kBytes = kBar + 64;
-    // Every CTA holds all 512 TMEM columns: the request is kept above half of the SM's shared
-    // memory so that two CTAs never share an SM (the second would wait in its allocation).
-    static constexpr int kDynSmem = kBytes + 1024 > 116 * 1024 ? kBytes + 1024 : 116 * 1024;
-    static constexpr uint32_t kTmemS = 0, kTmemDP = 128;
-    static constexpr uint32_t kTmemDQ = 128, kTmemDV = 256, kTmemDK = 256 + D;
-    static_assert(kTmemDK + D <= 512, "TMEM budget");
-    static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
-};
+// Every CTA holds all 512 TMEM columns: the shared-memory request is kept above half of the
+// SM's so that two CTAs never share an SM (the second would wait in its allocation).
+constexpr int dyn_smem(int bytes) { return bytes + 1024 > 116 * 1024 ? bytes + 1024 : 116 * 1024; }
 
 struct BwdParams {
-    float* ws_dQ;       // [BH, N, D] fp32, zeroed by the first kernel
     const float* LSE;   // [BH, N]
-    const float* Dv;    // [BH, N]
-    __nv_bfloat16* dK;  // [BH, N, D]
+    const float* Dv;    // [BH, N], written by bwd_prep_kernel
+    __nv_bfloat16* dQ;  // [BH, N, D]
+    __nv_bfloat16* dK;
     __nv_bfloat16* dV;
-    int N, n_tiles;
+    int N, n_tiles, BH;
     float scale, scale_log2;
     unsigned long long timeout_ns;
     int* status;  // the library's device status word
 };
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
+__device__ __forceinline__ void record_timeout(int* status, int where) {
+    atomicCAS(status, 0, FA_ERR_TIMEOUT | (where << 8));
 }
 
-// D_i = dO_i . O_i for every row (fp32 from the bf16 rows), and the dQ workspace set to zero.
-// One warp per row.
+// Eight (d = 128) or four (d = 64) K16 steps of an SS product over K-major 128-byte swizzled
+// tiles stored as 64-column halves.
+template <int D>
+__device__ __forceinline__ void mma_ss_kmajor(uint32_t d_tmem, uint32_t sA, uint32_t sB,
+                                              uint32_t idesc) {
+    umma_ss_x4(d_tmem, smem_desc_sw128(sA, 16, 1024), smem_desc_sw128(sB, 16, 1024), idesc, 0u);
+    if constexpr (D == 128)
+        umma_ss_x4(d_tmem, smem_desc_sw128(sA + kHalf, 16, 1024),
+                   smem_desc_sw128(sB + kHalf, 16, 1024), idesc, 1u);
+}
+
+// Rows [64 half, 64 half + 64) of the walked dimension of a TS product whose A operand (bf16
+// pairs, in TMEM) starts every 16-column group (the layout the element-wise warps write: the
+// 16 walked rows of K16 step k at columns 16 k .. 16 k + 7); B is the MN-major tile at sB.
+__device__ __forceinline__ void mma_ts_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB,
+                                            int half, uint32_t idesc, uint32_t accumulate) {
+    umma_ts_x4_stride16(d_tmem, a_tmem + half * 64,
+                        smem_desc_sw128(sB + half * 4 * 2048, kHalf, 1024), idesc, accumulate);
+}
+
+// Writes N fp32 values (times sc) of one row as bf16.
+template <int N>
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t (&v)[N], float sc) {
+    uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int w = 0; w < N / 8; ++w)
+        o[w] = make_uint4(
+            pack_bf16x2(__uint_as_float(v[8 * w]) * sc, __uint_as_float(v[8 * w + 1]) * sc),
+            pack_bf16x2(__uint_as_float(v[8 * w + 2]) * sc, __uint_as_float(v[8 * w + 3]) * sc),
+            pack_bf16x2(__uint_as_float(v[8 * w + 4]) * sc, __uint_as_float(v[8 * w + 5]) * sc),
+            pack_bf16x2(__uint_as_float(v[8 * w + 6]) * sc, __uint_as_float(v[8 * w + 7]) * sc));
+}
+
+// D_i = dO_i . O_i for every row (fp32 from the bf16 rows).  One warp per row.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ O,
                                                        const __nv_bfloat16* __restrict__ dO,
-                                                       float* __restrict__ Dv,
-                                                       float* __restrict__ ws_dQ,
-                                                       long long rows) {
+                                                       float* __restrict__ Dv, long long rows) {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
     for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -100,7 +118,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
         for (int e = 0; e < E; ++e) {
             const size_t k = static_cast<size_t>(r) * D + lane * E + e;
             acc += __bfloat162float(O[k]) * __bfloat162float(dO[k]);
-            ws_dQ[k] = 0.f;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -108,42 +125,115 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
     }
 }
 
-// dQ = scale * workspace, to bf16.
-__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ ws,
-                                                     __nv_bfloat16* __restrict__ dQ, float scale,
-                                                     long long n) {
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += static_cast<long long>(gridDim.x) * blockDim.x)
-        dQ[i] = __float2bfloat16_rn(ws[i] * scale);
+// ============================================================================================
+// dK, dV: one CTA per (head, key tile)
+// ============================================================================================
+// TMEM (512 columns): S^T [0,128) (keys x queries), whose 16-column groups, once read by the
+// warp that owns them, take P^T and dS^T of the same 16 queries (P^T in the first 8 columns of
+// a group, dS^T in the last 8, bf16 pairs); dP^T [128,256); dV [256, 256 + d);
+// dK [256 + d, 256 + 2d).
+//   S^T  = K Q_i^T     A = K, B = Q_i      shared memory, K-major
+//   dP^T = V dO_i^T    A = V, B = dO_i     shared memory, K-major
+//   dV  += P^T dO_i    A = P^T in TMEM, B = dO_i MN-major
+//   dK  += dS^T Q_i    A = dS^T in TMEM, B = Q_i MN-major
+template <int D>
+struct KvCfg {
+    static constexpr int kTileBytes = (D / 64) * kHalf;
+    static constexpr int kK = 0;
+    static constexpr int kV = kK + kTileBytes;
+    static constexpr int kQ = kV + kTileBytes;      // two stages
+    static constexpr int kG = kQ + 2 * kTileBytes;  // dO, two stages
+    static constexpr int kLD = kG + 2 * kTileBytes; // per query pair: -LSE log2e (x2), -D (x2)
+    static constexpr int kBar = kLD + 1024;
+    static constexpr int kBytes = kBar + 128;
+    static constexpr int kDynSmem = dyn_smem(kBytes);
+    static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDV = 256, kTmemDK = 256 + D;
+    static_assert(kTmemDK + D <= 512, "TMEM budget");
+    static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
+};
+
+enum KvBar {
+    kKvBarKV = 0,      // K, V landed
+    kKvBarFull = 1,    // [2] Q_i, dO_i landed in a stage
+    kKvBarEmpty = 3,   // [2] a stage's products are done
+    kKvBarSFull = 5,   // S^T in TMEM
+    kKvBarDpFull = 6,  // dP^T in TMEM
+    kKvBarP0 = 7,      // P^T, dS^T of queries 0-63 written (one arrival per element-wise warp)
+    kKvBarP1 = 8,      // ... of queries 64-127 (and all of S^T, dP^T read)
+    kKvBarSFree = 9,   // dV, dK products of a tile done: S^T columns may be rewritten
+    kKvBarAcc = 10,    // the last dV, dK products done
+    kKvBarDrain = 11,  // the issuing thread's products done, on the way out after a timeout
+    kKvNumBars = 12
+};
+
+// P^T and dS^T of 16 queries (part `part` of the 32-query chunk c) of the current tile, from
+// the S^T and dP^T columns of this thread's key row, written back over the same 16 S^T columns
+// (which no other warp reads): P^T in the first 8, dS^T in the last 8 (bf16 pairs).  `lo`:
+// first allowed query column of this row (0 unless the tile needs masking; 128 masks the row).
+template <bool MASK>
+__device__ __forceinline__ void kv_part(uint32_t t_row, const float4* ld, int c, int part, int lo,
+                                        float scale_log2) {
+    const int c0 = c * 32 + part * 16;  // first query column
+    uint32_t sv[16], gv[16];
+    tmem_ld16x2_sync(t_row + c0, t_row + 128 + c0, sv, gv);
+    uint32_t pw[8], dw[8];
+    const float2 sl2 = make_float2(scale_log2, scale_log2);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float4 L = ld[c0 / 2 + e];  // columns c0 + 2e, +1: -LSE log2e, -D
+        const float2 a = ffma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
+                               sl2, make_float2(L.x, L.y));
+        float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+        if (MASK) {
+            const int col = c0 + 2 * e;
+            p0 = col >= lo ? p0 : 0.f;
+            p1 = col + 1 >= lo ? p1 : 0.f;
+        }
+        const float2 g = fadd2(make_float2(__uint_as_float(gv[2 * e]), __uint_as_float(gv[2 * e + 1])),
+                               make_float2(L.z, L.w));
+        const float2 ds = fmul2(make_float2(p0, p1), g);
+        pw[e] = pack_bf16x2(p0, p1);
+        dw[e] = pack_bf16x2(ds.x, ds.y);
+    }
+    tmem_st8x2_sync(t_row + c0, pw, t_row + c0 + 8, dw);
 }
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-               const BwdParams prm) {
-    using C = BwdCfg<D>;
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                  const BwdParams prm) {
+    using C = KvCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* bar_kv = reinterpret_cast<uint64_t*>(smem + C::kBar);
-    uint64_t* bar_qg = bar_kv + 1;
-    uint64_t* bar_mma = bar_kv + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kv + 3);
-    float* lse_s = reinterpret_cast<float*>(smem + C::kLse);
-    float* d_s = reinterpret_cast<float*>(smem + C::kDd);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int bh = blockIdx.x / prm.n_tiles, jt = blockIdx.x % prm.n_tiles;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKvNumBars);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Key tiles in the outer position of the grid: with a causal mask the tiles that see the
+    // most query tiles start first.
+    const int bh = blockIdx.x % prm.BH, jt = blockIdx.x / prm.BH;
     const int N = prm.N;
+    const int i0 = CAUSAL ? jt : 0;
+    const int n_it = prm.n_tiles - i0;
     const unsigned long long tmo = prm.timeout_ns;
 
-    if (tid == 0) {
-        mbar_init(bar_kv, 1);
-        mbar_init(bar_qg, 1);
-        mbar_init(bar_mma, 1);
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[kKvBarKV], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[kKvBarFull + s], 1);
+            mbar_init(&bars[kKvBarEmpty + s], 1);
+        }
+        mbar_init(&bars[kKvBarSFull], 1);
+        mbar_init(&bars[kKvBarDpFull], 1);
+        mbar_init(&bars[kKvBarP0], kSoftWarps);
+        mbar_init(&bars[kKvBarP1], kSoftWarps);
+        mbar_init(&bars[kKvBarSFree], 1);
+        mbar_init(&bars[kKvBarAcc], 1);
+        mbar_init(&bars[kKvBarDrain], 1);
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -151,223 +241,446 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
 
-    if (tid == 0) {
-        mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
-        for (int h = 0; h < D / 64; ++h) {
-            tma_load_3d(smem + C::kK + h * kHalf, &tmK, bar_kv, h * 64, jt * kTile, bh);
-            tma_load_3d(smem + C::kV + h * kHalf, &tmV, bar_kv, h * 64, jt * kTile, bh);
-        }
-    }
-    bool ok = mbar_wait(bar_kv, 0, tmo);
-    ok = __syncthreads_and(ok);
-    if (!ok && tid == 0) atomicCAS(prm.status, 0, FA_ERR_TIMEOUT | (20 << 8));
-
-    const uint32_t sK = smem_u32(smem + C::kK), sV = smem_u32(smem + C::kV);
-    const uint32_t sQ = smem_u32(smem + C::kQ), sG = smem_u32(smem + C::kG);
-    const uint32_t sS = smem_u32(smem + C::kS);
-    const int key = jt * kTile + tid;  // this thread's key row
-    const int i_begin = CAUSAL ? jt : 0;
-    const int n_q = (N + kTile - 1) / kTile;
-    int phase = 0, mphase = 0;
-    int issued_loads = 0;
-    bool mma_pending = false;  // products issued whose completion has not been waited for
-    bool first = true;
-
-    for (int it = i_begin; ok && it < n_q; ++it) {
-        // ---- load Q_i, dO_i (TMA) and LSE_i, D_i (plain loads) ----------------------------
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_qg, 2 * C::kTileBytes);
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            // ---- loads ----------------------------------------------------------------------
+            mbar_arrive_expect_tx(&bars[kKvBarKV], 2 * C::kTileBytes);
             for (int h = 0; h < D / 64; ++h) {
-                tma_load_3d(smem + C::kQ + h * kHalf, &tmQ, bar_qg, h * 64, it * kTile, bh);
-                tma_load_3d(smem + C::kG + h * kHalf, &tmG, bar_qg, h * 64, it * kTile, bh);
+                tma_load_3d(smem + C::kK + h * kHalf, &tmK, &bars[kKvBarKV], h * 64, jt * kTile, bh);
+                tma_load_3d(smem + C::kV + h * kHalf, &tmV, &bars[kKvBarKV], h * 64, jt * kTile, bh);
             }
-        }
-        ++issued_loads;
-        {
-            const int q = it * kTile + tid;
-            const size_t row = static_cast<size_t>(bh) * N + q;
-            lse_s[tid] = q < N ? prm.LSE[row] : INFINITY;  // past the end: share 0
-            d_s[tid] = q < N ? prm.Dv[row] : 0.f;
-        }
-        ok = mbar_wait(bar_qg, phase, tmo);
-        ok = __syncthreads_and(ok);
-        if (!ok) {
-            if (tid == 0) atomicCAS(prm.status, 0, FA_ERR_TIMEOUT | (21 << 8));
-            break;
-        }
-        phase ^= 1;
-
-        // ---- S^T = K Q^T and dP^T = V dO^T ---------------------------------------------------
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16_f32_ab(kTile, kTile, 0, 0);
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                umma_ss(tmem + C::kTmemS, smem_desc_sw128(sK + off, 16, 1024),
-                        smem_desc_sw128(sQ + off, 16, 1024), id, kk > 0 ? 1u : 0u);
-            }
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                umma_ss(tmem + C::kTmemDP, smem_desc_sw128(sV + off, 16, 1024),
-                        smem_desc_sw128(sG + off, 16, 1024), id, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(bar_mma);
-        }
-        mma_pending = true;
-        ok = mbar_wait(bar_mma, mphase, tmo);
-        ok = __syncthreads_and(ok);
-        if (!ok) {
-            if (tid == 0) atomicCAS(prm.status, 0, FA_ERR_TIMEOUT | (22 << 8));
-            break;
-        }
-        mphase ^= 1;
-        mma_pending = false;
-        tc_fence_after();
-
-        // ---- P^T = exp(scale S^T - LSE), dS^T = P^T (dP^T - D) ------------------------------
-        {
-            const bool key_ok = key < N;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {  // 32 query columns at a time
-                uint32_t sv[32], gv[32], pw[16], dsw[16];
-                tmem_ld32_sync(tmem + lane_addr + C::kTmemS + c * 32, sv);
-                tmem_ld32_sync(tmem + lane_addr + C::kTmemDP + c * 32, gv);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p2[2], d2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = c * 32 + e + u;
-                        const int q = it * kTile + col;
-                        const bool allowed = key_ok && (!CAUSAL || key <= q);
-                        const float p =
-                            allowed ? ex2_approx(__uint_as_float(sv[e + u]) * prm.scale_log2 -
-                                                 lse_s[col] * 1.4426950408889634f)
-                                    : 0.f;
-                        p2[u] = p;
-                        d2[u] = p * (__uint_as_float(gv[e + u]) - d_s[col]);
-                    }
-                    pw[e / 2] = pack_bf16x2(p2[0], p2[1]);
-                    dsw[e / 2] = pack_bf16x2(d2[0], d2[1]);
+            int issued = 0;
+            for (int t = 0; t < n_it; ++t) {
+                const int s = t & 1;
+                if (t >= 2 && !mbar_wait(&bars[kKvBarEmpty + s], ((t >> 1) - 1) & 1, tmo, true)) {
+                    record_timeout(prm.status, 20);
+                    break;
                 }
-                // P^T and dS^T of these 32 query columns (16 bf16 pairs each) go into the 32
-                // columns of S^T just read: P^T at [32c, 32c + 16), dS^T at [32c + 16, 32c + 32).
-                tmem_st16_sync(tmem + lane_addr + C::kTmemS + c * 32, pw);
-                tmem_st16_sync(tmem + lane_addr + C::kTmemS + c * 32 + 16, dsw);
-                // dS^T row `tid` into shared memory, 128-byte swizzled as a TMA tile would be:
-                // half c / 2, 16-byte chunks (c % 2) * 4 .. + 4 of the row.
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int ch = (c & 1) * 4 + u;
-                    st_shared_v4(sS + (c >> 1) * kHalf + tid * 128 + ((ch ^ (tid & 7)) << 4),
-                                 dsw[4 * u], dsw[4 * u + 1], dsw[4 * u + 2], dsw[4 * u + 3]);
+                uint8_t* q = smem + C::kQ + s * C::kTileBytes;
+                uint8_t* g = smem + C::kG + s * C::kTileBytes;
+                mbar_arrive_expect_tx(&bars[kKvBarFull + s], 2 * C::kTileBytes);
+                for (int h = 0; h < D / 64; ++h) {
+                    tma_load_3d(q + h * kHalf, &tmQ, &bars[kKvBarFull + s], h * 64, (i0 + t) * kTile, bh);
+                    tma_load_3d(g + h * kHalf, &tmG, &bars[kKvBarFull + s], h * 64, (i0 + t) * kTile, bh);
                 }
+                ++issued;
             }
+            // Whatever happened elsewhere, the copies this thread started land before exit.
+            const uint64_t drain = tmo > kDrainNs ? tmo : kDrainNs;
+            mbar_wait(&bars[kKvBarKV], 0, drain, true);
+            if (issued > 0)
+                mbar_wait(&bars[kKvBarFull + ((issued - 1) & 1)], ((issued - 1) >> 1) & 1, drain, true);
         }
-        fence_proxy_async_smem();  // the tensor core reads dS^T through the async proxy
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- dV += P^T dO, dK += dS^T Q, dQ_i = dS K ---------------------------------------
-        if (tid == 0) {
-            tc_fence_after();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            // ---- tensor-core products -------------------------------------------------------
+            // Order per query tile t: dV, dK of the first half of its queries (once the
+            // element-wise warps hand them over), those of the second half, then dP^T of tile
+            // t + 1 (its columns were read with the hand-over) and S^T of tile t + 1 (once the
+            // dV, dK products have read the P^T, dS^T columns).
+            const uint32_t sK = smem_u32(smem + C::kK), sV = smem_u32(smem + C::kV);
+            constexpr uint32_t idS = idesc_bf16_f32_ab(kTile, kTile, 0, 0);
             constexpr uint32_t idT = idesc_bf16_f32_ab(kTile, D, 0, 1);
-            constexpr uint32_t idQ = idesc_bf16_f32_ab(kTile, D, 1, 1);
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-                // A_k: queries 16k..16k+15 of P^T / dS^T (8 columns; see the layout above);
-                // B_k: query rows 16k..16k+15 of dO / Q, MN-major (d contiguous)
-                const uint32_t a = C::kTmemS + (kk >> 1) * 32 + (kk & 1) * 8;
-                umma_ts(tmem + C::kTmemDV, tmem + a, smem_desc_sw128(sG + kk * 2048, kHalf, 1024),
-                        idT, (!first || kk > 0) ? 1u : 0u);
-                umma_ts(tmem + C::kTmemDK, tmem + a + 16,
-                        smem_desc_sw128(sQ + kk * 2048, kHalf, 1024), idT,
-                        (!first || kk > 0) ? 1u : 0u);
+            int where = 21;
+            bool ok = mbar_wait(&bars[kKvBarKV], 0, tmo) && mbar_wait(&bars[kKvBarFull], 0, tmo);
+            if (ok) {
+                tc_fence_after();
+                mma_ss_kmajor<D>(tmem + C::kTmemS, sK, smem_u32(smem + C::kQ), idS);
+                umma_commit(&bars[kKvBarSFull]);
+                mma_ss_kmajor<D>(tmem + C::kTmemDP, sV, smem_u32(smem + C::kG), idS);
+                umma_commit(&bars[kKvBarDpFull]);
             }
-            for (int kk = 0; kk < kTile / 16; ++kk)
-                // A_k: key rows 16k..16k+15 of dS^T (queries contiguous), B_k: of K
-                umma_ss(tmem + C::kTmemDQ, smem_desc_sw128(sS + kk * 2048, kHalf, 1024),
-                        smem_desc_sw128(sK + kk * 2048, kHalf, 1024), idQ, kk > 0 ? 1u : 0u);
-            umma_commit(bar_mma);
-        }
-        first = false;
-        mma_pending = true;
-        ok = mbar_wait(bar_mma, mphase, tmo);
-        ok = __syncthreads_and(ok);
-        if (!ok) {
-            if (tid == 0) atomicCAS(prm.status, 0, FA_ERR_TIMEOUT | (23 << 8));
-            break;
-        }
-        mphase ^= 1;
-        mma_pending = false;
-        tc_fence_after();
-
-        // ---- dQ_i partial sums into the workspace -----------------------------------------
-        {
-            const int q = it * kTile + tid;  // TMEM lane = query row for this product
-            float* dst = prm.ws_dQ + (static_cast<size_t>(bh) * N + q) * D;
+            for (int t = 0; ok && t < n_it; ++t) {
+                const int s = t & 1;
+                const uint32_t sQ = smem_u32(smem + C::kQ + s * C::kTileBytes);
+                const uint32_t sG = smem_u32(smem + C::kG + s * C::kTileBytes);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32_sync(tmem + lane_addr + C::kTmemDQ + c * 32, v);
-                if (q < N) {
+                for (int half = 0; half < 2; ++half) {
+                    where = 22 + half;
+                    if (!(ok = mbar_wait(&bars[kKvBarP0 + half], t & 1, tmo))) break;
+                    tc_fence_after();
+                    const uint32_t acc = (t > 0 || half > 0) ? 1u : 0u;
+                    mma_ts_half(tmem + C::kTmemDV, tmem + C::kTmemS, sG, half, idT, acc);
+                    mma_ts_half(tmem + C::kTmemDK, tmem + C::kTmemS + 8, sQ, half, idT, acc);
+                }
+                if (!ok) break;
+                umma_commit(&bars[kKvBarSFree]);
+                umma_commit(&bars[kKvBarEmpty + s]);
+                if (t + 1 < n_it) {
+                    const int s1 = (t + 1) & 1;
+                    where = 24;
+                    if (!(ok = mbar_wait(&bars[kKvBarFull + s1], ((t + 1) >> 1) & 1, tmo))) break;
+                    tc_fence_after();
+                    mma_ss_kmajor<D>(tmem + C::kTmemDP, sV,
+                                     smem_u32(smem + C::kG + s1 * C::kTileBytes), idS);
+                    umma_commit(&bars[kKvBarDpFull]);
+                    where = 25;
+                    if (!(ok = mbar_wait(&bars[kKvBarSFree], t & 1, tmo))) break;
+                    tc_fence_after();
+                    mma_ss_kmajor<D>(tmem + C::kTmemS, sK,
+                                     smem_u32(smem + C::kQ + s1 * C::kTileBytes), idS);
+                    umma_commit(&bars[kKvBarSFull]);
+                }
+            }
+            if (ok) {
+                umma_commit(&bars[kKvBarAcc]);
+            } else {
+                record_timeout(prm.status, where);
+                // The products already issued finish before TMEM is freed.
+                umma_commit(&bars[kKvBarDrain]);
+                mbar_wait(&bars[kKvBarDrain], 0, tmo > kDrainNs ? tmo : kDrainNs, true);
+            }
+        }
+    } else {
+        // ---- P^T and dS^T (warps 0-15) ------------------------------------------------------
+        const int q4 = warp & 3, sub = warp >> 2;
+        const int r = q4 * 32 + lane;  // key row within the tile = TMEM lane
+        const int key = jt * kTile + r;
+        const uint32_t t_row = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+        float* ld_s = reinterpret_cast<float*>(smem + C::kLD);
+        const float4* ld4 = reinterpret_cast<const float4*>(smem + C::kLD);
+        // Thread st (0..255) stages one value per query tile: -LSE log2e of column st (st < 128)
+        // or -D of column st - 128; a column past N gets -inf and 0 (its shares are 0).
+        const int st = warp * 32 + lane;
+        const bool stager = st < 256;
+        const int col = st & 127;
+        const int slot = (col >> 1) * 4 + (col & 1) + (st >= 128 ? 2 : 0);
+        auto stage_value = [&](int it) -> float {
+            const int q = it * kTile + col;
+            if (q >= N) return st < 128 ? -INFINITY : 0.f;
+            const size_t row = static_cast<size_t>(bh) * N + q;
+            return st < 128 ? -prm.LSE[row] * kLog2e : -prm.Dv[row];
+        };
+        // Rows past N (a ragged last key tile) and, on the diagonal tile of a causal mask, the
+        // queries before the key are masked: first allowed column of this row.
+        const bool ragged_keys = (jt + 1) * kTile > N;
+        const int lo_row = key < N ? 0 : kTile;
+        if (stager) ld_s[slot] = stage_value(i0);
+        named_bar_sync(1, kSoftWarps * 32);
+        bool ok = true;
+        for (int t = 0; t < n_it; ++t) {
+            const int it = i0 + t;
+            const float next = stager && t + 1 < n_it ? stage_value(it + 1) : 0.f;
+            bool good = mbar_wait(&bars[kKvBarSFull], t & 1, tmo) &&
+                        mbar_wait(&bars[kKvBarDpFull], t & 1, tmo);
+            if (good) {
+                tc_fence_after();
+                const bool diag = CAUSAL && it == jt;
+                const int lo = diag ? (key < N ? r : kTile) : lo_row;
+#pragma unroll 1
+                for (int k = 0; k < 2; ++k) {
+                    const int c = 2 * k + (sub >> 1);  // queries 0-63 first, then 64-127
+                    if (diag || ragged_keys)
+                        kv_part<true>(t_row, ld4, c, sub & 1, lo, prm.scale_log2);
+                    else
+                        kv_part<false>(t_row, ld4, c, sub & 1, 0, prm.scale_log2);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[kKvBarP0 + k]);
+                }
+            } else if (lane == 0) {
+                record_timeout(prm.status, 26);
+            }
+            // All element-wise warps agree before the staged values are replaced.
+            if (!named_bar_and(1, kSoftWarps * 32, good)) {
+                ok = false;
+                break;
+            }
+            if (stager) ld_s[slot] = next;
+            named_bar_sync(1, kSoftWarps * 32);
+        }
+        if (ok) {
+            // ---- dV (warps 0-7) and scale * dK (warps 8-15), half of the columns per warp ----
+            if (!mbar_wait(&bars[kKvBarAcc], 0, tmo)) {
+                if (lane == 0) record_timeout(prm.status, 27);
+            } else {
+                tc_fence_after();
+                // The TMEM loads are warp-wide (.sync.aligned): every lane issues them, and
+                // only the stores are limited to the keys that exist.
+                const bool is_v = sub < 2;
+                const int c0 = (sub & 1) * (D / 2);
+                const uint32_t src = t_row + (is_v ? C::kTmemDV : C::kTmemDK) + c0;
+                __nv_bfloat16* out = (is_v ? prm.dV : prm.dK) +
+                                     (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * D + c0;
+                const float sc = is_v ? 1.f : prm.scale;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        red_add_v4(dst + c * 32 + e, __uint_as_float(v[e]),
-                                   __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                                   __uint_as_float(v[e + 3]));
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32_sync(src + c * 32, v);
+                    if (key < N) store_row<32>(out + c * 32, v, sc);
                 }
             }
         }
-        tc_fence_before();
-        __syncthreads();
-    }
-
-    if (ok) {
-        // ---- dV and scale * dK of this key tile ----------------------------------------------
-        // The TMEM loads are warp-wide (.sync.aligned): every lane issues them, and only the
-        // stores are limited to the keys that exist.
-        tc_fence_after();
-        const size_t row = static_cast<size_t>(bh) * N + (key < N ? key : 0);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32], k[32];
-            tmem_ld32_sync(tmem + lane_addr + C::kTmemDV + c * 32, v);
-            tmem_ld32_sync(tmem + lane_addr + C::kTmemDK + c * 32, k);
-            if (key < N) {
-                uint4* dv = reinterpret_cast<uint4*>(prm.dV + row * D + c * 32);
-                uint4* dk = reinterpret_cast<uint4*>(prm.dK + row * D + c * 32);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    dv[w] = make_uint4(
-                        pack_bf16x2(__uint_as_float(v[8 * w]), __uint_as_float(v[8 * w + 1])),
-                        pack_bf16x2(__uint_as_float(v[8 * w + 2]), __uint_as_float(v[8 * w + 3])),
-                        pack_bf16x2(__uint_as_float(v[8 * w + 4]), __uint_as_float(v[8 * w + 5])),
-                        pack_bf16x2(__uint_as_float(v[8 * w + 6]), __uint_as_float(v[8 * w + 7])));
-                    const float s = prm.scale;
-                    dk[w] = make_uint4(pack_bf16x2(__uint_as_float(k[8 * w]) * s,
-                                                   __uint_as_float(k[8 * w + 1]) * s),
-                                       pack_bf16x2(__uint_as_float(k[8 * w + 2]) * s,
-                                                   __uint_as_float(k[8 * w + 3]) * s),
-                                       pack_bf16x2(__uint_as_float(k[8 * w + 4]) * s,
-                                                   __uint_as_float(k[8 * w + 5]) * s),
-                                       pack_bf16x2(__uint_as_float(k[8 * w + 6]) * s,
-                                                   __uint_as_float(k[8 * w + 7]) * s));
-                }
-            }
-        }
-    } else if (tid == 0) {
-        // Drain: the loads and products this CTA started finish before it exits.
-        const uint64_t drain = tmo > kDrainNs ? tmo : kDrainNs;
-        mbar_wait(bar_kv, 0, drain);
-        if (issued_loads > 0) mbar_wait(bar_qg, (issued_loads - 1) & 1, drain);
-        if (mma_pending) mbar_wait(bar_mma, mphase, drain);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================================================
+// dQ: one CTA per (head, query tile)
+// ============================================================================================
+// TMEM (512 columns): S [0,128) and [128,256) (two buffers, queries x keys), whose 16-column
+// groups, once read by the warp that owns them, take dS of the same 16 keys in their first 8
+// columns (bf16 pairs); dP [256,384); dQ [384, 384 + d).
+//   S   = Q K_j^T      A = Q, B = K_j       shared memory, K-major
+//   dP  = dO V_j^T     A = dO, B = V_j      shared memory, K-major
+//   dQ += dS K_j       A = dS in TMEM, B = K_j MN-major
+template <int D>
+struct QCfg {
+    static constexpr int kTileBytes = (D / 64) * kHalf;
+    static constexpr int kQ = 0;
+    static constexpr int kG = kQ + kTileBytes;      // dO
+    static constexpr int kK = kG + kTileBytes;      // two stages
+    static constexpr int kV = kK + 2 * kTileBytes;  // two stages
+    static constexpr int kBar = kV + 2 * kTileBytes;
+    static constexpr int kBytes = kBar + 128;
+    static constexpr int kDynSmem = dyn_smem(kBytes);
+    static constexpr uint32_t kTmemS = 0, kTmemDP = 256, kTmemDQ = 384;
+    static_assert(kTmemDQ + D <= 512, "TMEM budget");
+    static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
+};
+
+enum QBar {
+    kQBarQG = 0,      // Q, dO landed
+    kQBarFull = 1,    // [2] K_j, V_j landed in a stage
+    kQBarEmpty = 3,   // [2] a stage's products are done
+    kQBarSFull = 5,   // [2] S in TMEM buffer b
+    kQBarSFree = 7,   // [2] dQ products done with the dS in buffer b
+    kQBarDpFull = 9,  // dP in TMEM
+    kQBarP0 = 10,     // dS of keys 0-63 written (one arrival per element-wise warp)
+    kQBarP1 = 11,     // ... of keys 64-127 (and all of S, dP read)
+    kQBarAcc = 12,    // the last dQ products done
+    kQBarDrain = 13,
+    kQNumBars = 14
+};
+
+// dS of 16 keys (part `part` of the 32-key chunk c) of the current key tile for this thread's
+// query row, written over the first 8 of the same 16 S columns (bf16 pairs).
+// nlse2 = -LSE log2e and nD = -D of the row; `hi`: last allowed key column of this row (127
+// unless the tile needs masking).
+template <bool MASK>
+__device__ __forceinline__ void q_part(uint32_t t_s, uint32_t t_dp, int c, int part, float nlse2,
+                                       float nD, int hi, float scale_log2) {
+    const int c0 = c * 32 + part * 16;  // first key column
+    uint32_t sv[16], gv[16];
+    tmem_ld16x2_sync(t_s + c0, t_dp + c0, sv, gv);
+    uint32_t dw[8];
+    const float2 sl2 = make_float2(scale_log2, scale_log2);
+    const float2 nl = make_float2(nlse2, nlse2), nd = make_float2(nD, nD);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float2 a = ffma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
+                               sl2, nl);
+        float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+        if (MASK) {
+            const int col = c0 + 2 * e;
+            p0 = col <= hi ? p0 : 0.f;
+            p1 = col + 1 <= hi ? p1 : 0.f;
+        }
+        const float2 g = fadd2(make_float2(__uint_as_float(gv[2 * e]), __uint_as_float(gv[2 * e + 1])), nd);
+        const float2 ds = fmul2(make_float2(p0, p1), g);
+        dw[e] = pack_bf16x2(ds.x, ds.y);
+    }
+    tmem_st8_sync(t_s + c0, dw);
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                 const BwdParams prm) {
+    using C = QCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kQNumBars);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Query tiles in the outer position of the grid, last first: with a causal mask the tiles
+    // that see the most key tiles start first.
+    const int bh = blockIdx.x % prm.BH;
+    const int qt = prm.n_tiles - 1 - static_cast<int>(blockIdx.x / prm.BH);
+    const int N = prm.N;
+    const int n_j = CAUSAL ? qt + 1 : prm.n_tiles;
+    const unsigned long long tmo = prm.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[kQBarQG], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[kQBarFull + s], 1);
+            mbar_init(&bars[kQBarEmpty + s], 1);
+            mbar_init(&bars[kQBarSFull + s], 1);
+            mbar_init(&bars[kQBarSFree + s], 1);
+        }
+        mbar_init(&bars[kQBarDpFull], 1);
+        mbar_init(&bars[kQBarP0], kSoftWarps);
+        mbar_init(&bars[kQBarP1], kSoftWarps);
+        mbar_init(&bars[kQBarAcc], 1);
+        mbar_init(&bars[kQBarDrain], 1);
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            // ---- loads ----------------------------------------------------------------------
+            mbar_arrive_expect_tx(&bars[kQBarQG], 2 * C::kTileBytes);
+            for (int h = 0; h < D / 64; ++h) {
+                tma_load_3d(smem + C::kQ + h * kHalf, &tmQ, &bars[kQBarQG], h * 64, qt * kTile, bh);
+                tma_load_3d(smem + C::kG + h * kHalf, &tmG, &bars[kQBarQG], h * 64, qt * kTile, bh);
+            }
+            int issued = 0;
+            for (int j = 0; j < n_j; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !mbar_wait(&bars[kQBarEmpty + s], ((j >> 1) - 1) & 1, tmo, true)) {
+                    record_timeout(prm.status, 30);
+                    break;
+                }
+                uint8_t* k = smem + C::kK + s * C::kTileBytes;
+                uint8_t* v = smem + C::kV + s * C::kTileBytes;
+                mbar_arrive_expect_tx(&bars[kQBarFull + s], 2 * C::kTileBytes);
+                for (int h = 0; h < D / 64; ++h) {
+                    tma_load_3d(k + h * kHalf, &tmK, &bars[kQBarFull + s], h * 64, j * kTile, bh);
+                    tma_load_3d(v + h * kHalf, &tmV, &bars[kQBarFull + s], h * 64, j * kTile, bh);
+                }
+                ++issued;
+            }
+            const uint64_t drain = tmo > kDrainNs ? tmo : kDrainNs;
+            mbar_wait(&bars[kQBarQG], 0, drain, true);
+            if (issued > 0)
+                mbar_wait(&bars[kQBarFull + ((issued - 1) & 1)], ((issued - 1) >> 1) & 1, drain, true);
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            // ---- tensor-core products -------------------------------------------------------
+            // Order per key tile j: S of tile j + 1 into the other buffer (while the
+            // element-wise warps work on tile j), dQ of the first half of tile j's keys, of the
+            // second half, then dP of tile j + 1 (its columns were read with the hand-over).
+            const uint32_t sQ = smem_u32(smem + C::kQ), sG = smem_u32(smem + C::kG);
+            constexpr uint32_t idS = idesc_bf16_f32_ab(kTile, kTile, 0, 0);
+            constexpr uint32_t idT = idesc_bf16_f32_ab(kTile, D, 0, 1);
+            int where = 31;
+            bool ok = mbar_wait(&bars[kQBarQG], 0, tmo) && mbar_wait(&bars[kQBarFull], 0, tmo);
+            if (ok) {
+                tc_fence_after();
+                mma_ss_kmajor<D>(tmem + C::kTmemS, sQ, smem_u32(smem + C::kK), idS);
+                umma_commit(&bars[kQBarSFull]);
+                mma_ss_kmajor<D>(tmem + C::kTmemDP, sG, smem_u32(smem + C::kV), idS);
+                umma_commit(&bars[kQBarDpFull]);
+            }
+            for (int j = 0; ok && j < n_j; ++j) {
+                const int s = j & 1, s1 = (j + 1) & 1;
+                if (j + 1 < n_j) {
+                    where = 32;
+                    if (!(ok = mbar_wait(&bars[kQBarFull + s1], ((j + 1) >> 1) & 1, tmo))) break;
+                    where = 33;
+                    if (j >= 1 && !(ok = mbar_wait(&bars[kQBarSFree + s1], ((j - 1) >> 1) & 1, tmo)))
+                        break;
+                    tc_fence_after();
+                    mma_ss_kmajor<D>(tmem + C::kTmemS + s1 * 128, sQ,
+                                     smem_u32(smem + C::kK + s1 * C::kTileBytes), idS);
+                    umma_commit(&bars[kQBarSFull + s1]);
+                }
+                const uint32_t sKj = smem_u32(smem + C::kK + s * C::kTileBytes);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    where = 34 + half;
+                    if (!(ok = mbar_wait(&bars[kQBarP0 + half], j & 1, tmo))) break;
+                    tc_fence_after();
+                    mma_ts_half(tmem + C::kTmemDQ, tmem + C::kTmemS + s * 128, sKj, half, idT,
+                                (j > 0 || half > 0) ? 1u : 0u);
+                }
+                if (!ok) break;
+                umma_commit(&bars[kQBarSFree + s]);
+                umma_commit(&bars[kQBarEmpty + s]);
+                if (j + 1 < n_j) {
+                    mma_ss_kmajor<D>(tmem + C::kTmemDP, sG,
+                                     smem_u32(smem + C::kV + s1 * C::kTileBytes), idS);
+                    umma_commit(&bars[kQBarDpFull]);
+                }
+            }
+            if (ok) {
+                umma_commit(&bars[kQBarAcc]);
+            } else {
+                record_timeout(prm.status, where);
+                umma_commit(&bars[kQBarDrain]);
+                mbar_wait(&bars[kQBarDrain], 0, tmo > kDrainNs ? tmo : kDrainNs, true);
+            }
+        }
+    } else {
+        // ---- dS (warps 0-15) -----------------------------------------------------------------
+        const int q4 = warp & 3, sub = warp >> 2;
+        const int r = q4 * 32 + lane;  // query row within the tile = TMEM lane
+        const int q = qt * kTile + r;
+        const uint32_t t_row = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+        // A row past N has shares 0 (-LSE log2e = -inf) and is never written.
+        const size_t row = static_cast<size_t>(bh) * N + (q < N ? q : 0);
+        const float nlse2 = q < N ? -prm.LSE[row] * kLog2e : -INFINITY;
+        const float nD = q < N ? -prm.Dv[row] : 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_j; ++j) {
+            const int s = j & 1;
+            bool good = mbar_wait(&bars[kQBarSFull + s], (j >> 1) & 1, tmo) &&
+                        mbar_wait(&bars[kQBarDpFull], j & 1, tmo);
+            if (!good) {
+                if (lane == 0) record_timeout(prm.status, 36);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // Masks: keys after the query on the diagonal tile of a causal mask, and keys past
+            // N (the ragged last key tile): last allowed key column of this row.
+            const bool diag = CAUSAL && j == qt;
+            const bool ragged_keys = (j + 1) * kTile > N;
+            int hi = kTile - 1;
+            if (diag) hi = r;
+            if (ragged_keys && N - 1 - j * kTile < hi) hi = N - 1 - j * kTile;
+            const uint32_t t_s = t_row + C::kTmemS + s * 128, t_dp = t_row + C::kTmemDP;
+#pragma unroll 1
+            for (int k = 0; k < 2; ++k) {
+                const int c = 2 * k + (sub >> 1);  // keys 0-63 first, then 64-127
+                if (diag || ragged_keys)
+                    q_part<true>(t_s, t_dp, c, sub & 1, nlse2, nD, hi, prm.scale_log2);
+                else
+                    q_part<false>(t_s, t_dp, c, sub & 1, nlse2, nD, kTile - 1, prm.scale_log2);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kQBarP0 + k]);
+            }
+        }
+        if (ok) {
+            // ---- scale * dQ of this query tile (a quarter of the columns per warp) ------------
+            if (!mbar_wait(&bars[kQBarAcc], 0, tmo)) {
+                if (lane == 0) record_timeout(prm.status, 37);
+            } else {
+                tc_fence_after();
+                constexpr int kCols = D / 4;
+                const uint32_t src = t_row + C::kTmemDQ + sub * kCols;
+                __nv_bfloat16* out = prm.dQ + row * D + sub * kCols;
+                uint32_t v[kCols];
+                if constexpr (kCols == 32) {
+                    tmem_ld32_sync(src, v);
+                } else {
+                    tmem_ld16_sync(src, v);
+                }
+                if (q < N) store_row<kCols>(out, v, prm.scale);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 int bwd_sm_count() {
@@ -383,29 +696,35 @@ int bwd_sm_count() {
 }
 
 template <int D, bool CAUSAL>
-int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tg, const BwdParams& prm, long long BH, cudaStream_t stream) {
-    using C = BwdCfg<D>;
+int launch_tiles(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 const CUtensorMap& tg, const BwdParams& prm, long long BH, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(bwd_kernel<D, CAUSAL>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+        attr = cudaFuncSetAttribute(bwd_kv_kernel<D, CAUSAL>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    KvCfg<D>::kDynSmem);
+        if (attr == cudaSuccess)
+            attr = cudaFuncSetAttribute(bwd_q_kernel<D, CAUSAL>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        QCfg<D>::kDynSmem);
     });
     if (attr != cudaSuccess) return FA_ERR_CUDA;
-    const long long ctas = BH * prm.n_tiles;
+    const long long ctas = BH * prm.n_tiles;  // tiles outer, heads inner
     if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    bwd_kernel<D, CAUSAL>
-        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, tg, prm);
+    bwd_kv_kernel<D, CAUSAL><<<static_cast<unsigned>(ctas), kThreads, KvCfg<D>::kDynSmem, stream>>>(
+        tq, tk, tv, tg, prm);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    bwd_q_kernel<D, CAUSAL><<<static_cast<unsigned>(ctas), kThreads, QCfg<D>::kDynSmem, stream>>>(
+        tq, tk, tv, tg, prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
 
 int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                  const float* LSE, void* dQ, void* dK, void* dV, float* ws_dQ, float* ws_D,
-                  int64_t BH, int64_t N, int64_t d, float scale, bool causal,
-                  cudaStream_t stream) {
+                  const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t BH,
+                  int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream) {
     if (N > (1LL << 30) || BH > (1LL << 30)) return FA_ERR_UNSUPPORTED;
     const long long rows = BH * N;
     const long long sms = bwd_sm_count() > 0 ? bwd_sm_count() : 148;
@@ -414,11 +733,11 @@ int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, co
     if (d == 64)
         bwd_prep_kernel<64><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), ws_D,
-            ws_dQ, rows);
+            rows);
     else
         bwd_prep_kernel<128><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), ws_D,
-            ws_dQ, rows);
+            rows);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
     CUtensorMap tq, tk, tv, tg;
@@ -428,32 +747,24 @@ int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, co
     if (st == FA_OK) st = make_bhnd_tensor_map(&tg, dO, BH, N, d);
     if (st != FA_OK) return st;
     BwdParams prm{};
-    prm.ws_dQ = ws_dQ;
     prm.LSE = LSE;
     prm.Dv = ws_D;
+    prm.dQ = static_cast<__nv_bfloat16*>(dQ);
     prm.dK = static_cast<__nv_bfloat16*>(dK);
     prm.dV = static_cast<__nv_bfloat16*>(dV);
     prm.N = static_cast<int>(N);
     prm.n_tiles = static_cast<int>((N + kTile - 1) / kTile);
+    prm.BH = static_cast<int>(BH);
     prm.scale = scale;
-    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.scale_log2 = scale * kLog2e;
     prm.timeout_ns = fa_wait_timeout_ns();
     prm.status = device_status_word();
     if (!prm.status) return FA_ERR_CUDA;
     if (d == 64)
-        st = causal ? launch_bwd<64, true>(tq, tk, tv, tg, prm, BH, stream)
-                    : launch_bwd<64, false>(tq, tk, tv, tg, prm, BH, stream);
-    else
-        st = causal ? launch_bwd<128, true>(tq, tk, tv, tg, prm, BH, stream)
-                    : launch_bwd<128, false>(tq, tk, tv, tg, prm, BH, stream);
-    if (st != FA_OK) return st;
-
-    const long long n = rows * d;
-    long long g2 = (n + 255) / 256;
-    if (g2 > sms * 32) g2 = sms * 32;
-    bwd_dq_kernel<<<static_cast<unsigned>(g2), 256, 0, stream>>>(
-        ws_dQ, static_cast<__nv_bfloat16*>(dQ), scale, n);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+        return causal ? launch_tiles<64, true>(tq, tk, tv, tg, prm, BH, stream)
+                      : launch_tiles<64, false>(tq, tk, tv, tg, prm, BH, stream);
+    return causal ? launch_tiles<128, true>(tq, tk, tv, tg, prm, BH, stream)
+                  : launch_tiles<128, false>(tq, tk, tv, tg, prm, BH, stream);
 }
 
 }  // namespace osm

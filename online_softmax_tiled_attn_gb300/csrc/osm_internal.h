@@ -47,9 +47,8 @@ int fa_read_device_status(cudaStream_t stream, int* status);
 // Device address of the status word the kernels' bounded waits report to (null on failure).
 int* device_status_word();
 int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                  const float* LSE, void* dQ, void* dK, void* dV, float* ws_dQ, float* ws_D,
-                  int64_t BH, int64_t N, int64_t d, float scale, bool causal,
-                  cudaStream_t stream);
+                  const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t BH,
+                  int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream);
 int selftest_wait_launch(long long timeout_us, cudaStream_t stream);
 
 int osm_softmax_launch(const float* x, float* y, int64_t rows, int64_t cols, float* lse,

@@ -50,7 +50,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 4
+    assert binding.lib().osm_attn_abi_version() == 5
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -174,7 +174,7 @@ def _bwd_args(**over):
     """fa_bwd arguments for B1 H1 N128 d64 at distinct fake addresses (16 KiB per tensor)."""
     T = 128 * 64 * 2
     a = dict(q=P, k=P + T, v=P + 2 * T, o=P + 3 * T, do=P + 4 * T, lse=P + 5 * T,
-             dq=P + 6 * T, dk=P + 7 * T, dv=P + 8 * T, ws_dq=P + 9 * T, ws_d=P + 11 * T,
+             dq=P + 6 * T, dk=P + 7 * T, dv=P + 8 * T, ws_d=P + 9 * T,
              B=1, H=1, N=128, d=64, scale=0.125, causal=0)
     a.update(over)
     return a
@@ -190,15 +190,16 @@ def _bwd_args(**over):
         (dict(dq=0), binding.FA_ERR_INVALID_ARG),
         (dict(dk=P + 2), binding.FA_ERR_INVALID_ARG),          # misaligned
         (dict(dv=P + 64), binding.FA_ERR_INVALID_ARG),         # dV inside Q
-        (dict(ws_dq=P + 6 * 16384), binding.FA_ERR_INVALID_ARG),  # workspace on dQ
+        (dict(ws_d=P + 6 * 16384), binding.FA_ERR_INVALID_ARG),   # workspace on dQ
         (dict(ws_d=P + 5 * 16384), binding.FA_ERR_INVALID_ARG),   # workspace on LSE
+        (dict(ws_d=P + 9 * 16384 + 2), binding.FA_ERR_INVALID_ARG),  # misaligned workspace
     ],
 )
 def test_fa_bwd_rejects_on_host(over, want):
     a = _bwd_args(**over)
     rc = binding.fa_bwd_raw(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
-                            a["dv"], a["ws_dq"], a["ws_d"], a["B"], a["H"], a["N"], a["d"],
-                            a["scale"], a["causal"], None)
+                            a["dv"], a["ws_d"], a["B"], a["H"], a["N"], a["d"], a["scale"],
+                            a["causal"], None)
     assert rc == want
 
 
