@@ -128,74 +128,110 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 // ============================================================================================
 // dK, dV: one CTA per (head, key tile)
 // ============================================================================================
-// TMEM (512 columns): S^T [0,128) (keys x queries), whose 16-column groups, once read by the
-// warp that owns them, take P^T and dS^T of the same 16 queries (P^T in the first 8 columns of
-// a group, dS^T in the last 8, bf16 pairs); dP^T [128,256); dV [256, 256 + d);
-// dK [256 + d, 256 + 2d).
-//   S^T  = K Q_i^T     A = K, B = Q_i      shared memory, K-major
-//   dP^T = V dO_i^T    A = V, B = dO_i     shared memory, K-major
-//   dV  += P^T dO_i    A = P^T in TMEM, B = dO_i MN-major
-//   dK  += dS^T Q_i    A = dS^T in TMEM, B = Q_i MN-major
+// TMEM (512 columns): two buffers of 128 columns (keys x queries), one per query tile in
+// flight, and the accumulators dV [256, 256 + d), dK [256 + d, 256 + 2d).  The buffer of query
+// tile t holds in turn:
+//   S^T = K Q_t^T        B = Q_t (shared memory, K-major)
+//   dP^T = V dO_t^T      B = dO_t, written over S^T once the element-wise warps have read it
+//                        (they keep the shares P^T in registers meanwhile)
+//   P^T, dS^T (bf16)     written over dP^T by the element-wise warps: each 16-column group,
+//                        read by the warp that owns it, takes P^T in its first 8 columns and
+//                        dS^T in its last 8
+//   dV += P^T dO_t, dK += dS^T Q_t     A in TMEM, B = dO_t, Q_t MN-major
+// For d = 64 K and V, the A operands of S^T and dP^T, are copied once into TMEM too (the last
+// 64 columns): those products then read only B from shared memory (an N = 128 product with
+// both operands in shared memory needs the port's whole 128 bytes a clock), and their shared
+// memory serves a three-stage Q, dO ring.  For d = 128 TMEM has no room for them: they stay in
+// shared memory with a two-stage ring.
 template <int D>
 struct KvCfg {
     static constexpr int kTileBytes = (D / 64) * kHalf;
-    static constexpr int kK = 0;
+    static constexpr bool kKvInTmem = D == 64;
+    static constexpr int kStages = kKvInTmem ? 3 : 2;
+    static constexpr int kK = 0;                             // K, V (d = 128)
     static constexpr int kV = kK + kTileBytes;
-    static constexpr int kQ = kV + kTileBytes;      // two stages
-    static constexpr int kG = kQ + 2 * kTileBytes;  // dO, two stages
-    static constexpr int kLD = kG + 2 * kTileBytes; // per query pair: -LSE log2e (x2), -D (x2)
+    static constexpr int kQ = kKvInTmem ? 0 : kV + kTileBytes;  // Q, kStages stages
+    static constexpr int kG = kQ + kStages * kTileBytes;     // dO, kStages stages
+    static constexpr int kLD = kG + kStages * kTileBytes;    // per query pair: -LSE log2e, -D
     static constexpr int kBar = kLD + 1024;
-    static constexpr int kBytes = kBar + 128;
+    static constexpr int kBytes = kBar + 256;
     static constexpr int kDynSmem = dyn_smem(kBytes);
-    static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDV = 256, kTmemDK = 256 + D;
-    static_assert(kTmemDK + D <= 512, "TMEM budget");
+    // d = 64: K and V arrive in the last stage (its Q and dO halves) and are copied to TMEM
+    // before the stage's first Q, dO load.
+    static constexpr int kKLoad = kKvInTmem ? kQ + (kStages - 1) * kTileBytes : kK;
+    static constexpr int kVLoad = kKvInTmem ? kG + (kStages - 1) * kTileBytes : kV;
+    static constexpr uint32_t kTmemBuf = 0, kTmemDV = 256, kTmemDK = 256 + D;
+    static constexpr uint32_t kTmemK = kTmemDK + D, kTmemV = kTmemK + D / 2;
+    static_assert(kKvInTmem ? kTmemV + D / 2 <= 512 : kTmemDK + D <= 512, "TMEM budget");
     static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
 };
 
 enum KvBar {
-    kKvBarKV = 0,      // K, V landed
-    kKvBarFull = 1,    // [2] Q_i, dO_i landed in a stage
-    kKvBarEmpty = 3,   // [2] a stage's products are done
-    kKvBarSFull = 5,   // S^T in TMEM
-    kKvBarDpFull = 6,  // dP^T in TMEM
-    kKvBarP0 = 7,      // P^T, dS^T of queries 0-63 written (one arrival per element-wise warp)
-    kKvBarP1 = 8,      // ... of queries 64-127 (and all of S^T, dP^T read)
-    kKvBarSFree = 9,   // dV, dK products of a tile done: S^T columns may be rewritten
-    kKvBarAcc = 10,    // the last dV, dK products done
-    kKvBarDrain = 11,  // the issuing thread's products done, on the way out after a timeout
-    kKvNumBars = 12
+    kKvBarKV = 0,       // K, V landed
+    kKvBarKVCopied = 1, // K, V copied to TMEM: their shared memory may be reused (d = 64)
+    kKvBarFull = 2,     // [3] Q_t, dO_t landed in a stage
+    kKvBarEmpty = 5,    // [3] a stage's products are done
+    kKvBarSFull = 8,    // [2] S^T in TMEM buffer b
+    kKvBarSFree = 10,   // [2] the dV, dK products have read buffer b
+    kKvBarRead = 12,    // S^T read (one arrival per element-wise warp)
+    kKvBarDpFull = 13,  // dP^T in the buffer
+    kKvBarPds = 14,     // [2] P^T, dS^T of query half h written (one arrival per warp)
+    kKvBarAcc = 16,     // the last dV, dK products done
+    kKvBarDrain = 17,   // the issuing thread's products done, on the way out after a timeout
+    kKvNumBars = 18
 };
 
-// P^T and dS^T of 16 queries (part `part` of the 32-query chunk c) of the current tile, from
-// the S^T and dP^T columns of this thread's key row, written back over the same 16 S^T columns
-// (which no other warp reads): P^T in the first 8, dS^T in the last 8 (bf16 pairs).  `lo`:
-// first allowed query column of this row (0 unless the tile needs masking; 128 masks the row).
+// The shares of 16 queries (columns c0 .. c0 + 15 of the buffer at t_buf) for this thread's
+// key row: P = exp2(S scale log2e - LSE log2e).  `lo`: first allowed query column of the row
+// (0 unless the tile needs masking; 128 masks the row).
 template <bool MASK>
-__device__ __forceinline__ void kv_part(uint32_t t_row, const float4* ld, int c, int part, int lo,
-                                        float scale_log2) {
-    const int c0 = c * 32 + part * 16;  // first query column
-    uint32_t sv[16], gv[16];
-    tmem_ld16x2_sync(t_row + c0, t_row + 128 + c0, sv, gv);
-    uint32_t pw[8], dw[8];
+__device__ __forceinline__ void kv_shares(uint32_t t_buf, const float4* ld, int c0, int lo,
+                                          float scale_log2, float (&p)[16]) {
+    uint32_t sv[16];
+    tmem_ld16_sync(t_buf + c0, sv);
     const float2 sl2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const float4 L = ld[c0 / 2 + e];  // columns c0 + 2e, +1: -LSE log2e, -D
         const float2 a = ffma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
                                sl2, make_float2(L.x, L.y));
-        float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+        p[2 * e] = ex2_approx(a.x);
+        p[2 * e + 1] = ex2_approx(a.y);
         if (MASK) {
-            const int col = c0 + 2 * e;
-            p0 = col >= lo ? p0 : 0.f;
-            p1 = col + 1 >= lo ? p1 : 0.f;
+            if (c0 + 2 * e < lo) p[2 * e] = 0.f;
+            if (c0 + 2 * e + 1 < lo) p[2 * e + 1] = 0.f;
         }
+    }
+}
+
+// dS = P (dP - D) of the same 16 queries from the dP^T columns, then P^T and dS^T (bf16 pairs)
+// written over those columns: P^T in the first 8, dS^T in the last 8.
+__device__ __forceinline__ void kv_grads(uint32_t t_buf, const float4* ld, int c0,
+                                         const float (&p)[16]) {
+    uint32_t gv[16];
+    tmem_ld16_sync(t_buf + c0, gv);
+    uint32_t pw[8], dw[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float4 L = ld[c0 / 2 + e];
         const float2 g = fadd2(make_float2(__uint_as_float(gv[2 * e]), __uint_as_float(gv[2 * e + 1])),
                                make_float2(L.z, L.w));
-        const float2 ds = fmul2(make_float2(p0, p1), g);
-        pw[e] = pack_bf16x2(p0, p1);
+        const float2 ds = fmul2(make_float2(p[2 * e], p[2 * e + 1]), g);
+        pw[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
         dw[e] = pack_bf16x2(ds.x, ds.y);
     }
-    tmem_st8x2_sync(t_row + c0, pw, t_row + c0 + 8, dw);
+    tmem_st8x2_sync(t_buf + c0, pw, t_buf + c0 + 8, dw);
+}
+
+// A TS product over d: A (bf16 pairs, d / 2 TMEM columns at a_tmem) times the K-major,
+// 128-byte swizzled tile at sB (64-column halves), overwriting D.
+template <int D>
+__device__ __forceinline__ void mma_ts_kmajor(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB,
+                                              uint32_t idesc) {
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+        umma_ts_x4(d_tmem, a_tmem + h * 32, smem_desc_sw128(sB + h * kHalf, 16, 1024), 32 / 16,
+                   idesc, h > 0 ? 1u : 0u);
 }
 
 template <int D, bool CAUSAL>
@@ -204,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                   const BwdParams prm) {
     using C = KvCfg<D>;
+    constexpr int NS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -220,15 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[kKvBarKV], 1);
-        for (int s = 0; s < 2; ++s) {
+        mbar_init(&bars[kKvBarKVCopied], 1);
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&bars[kKvBarFull + s], 1);
             mbar_init(&bars[kKvBarEmpty + s], 1);
         }
-        mbar_init(&bars[kKvBarSFull], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[kKvBarSFull + s], 1);
+            mbar_init(&bars[kKvBarSFree + s], 1);
+            mbar_init(&bars[kKvBarPds + s], kSoftWarps);
+        }
+        mbar_init(&bars[kKvBarRead], kSoftWarps);
         mbar_init(&bars[kKvBarDpFull], 1);
-        mbar_init(&bars[kKvBarP0], kSoftWarps);
-        mbar_init(&bars[kKvBarP1], kSoftWarps);
-        mbar_init(&bars[kKvBarSFree], 1);
         mbar_init(&bars[kKvBarAcc], 1);
         mbar_init(&bars[kKvBarDrain], 1);
         fence_mbar_init();
@@ -247,13 +287,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- loads ----------------------------------------------------------------------
             mbar_arrive_expect_tx(&bars[kKvBarKV], 2 * C::kTileBytes);
             for (int h = 0; h < D / 64; ++h) {
-                tma_load_3d(smem + C::kK + h * kHalf, &tmK, &bars[kKvBarKV], h * 64, jt * kTile, bh);
-                tma_load_3d(smem + C::kV + h * kHalf, &tmV, &bars[kKvBarKV], h * 64, jt * kTile, bh);
+                tma_load_3d(smem + C::kKLoad + h * kHalf, &tmK, &bars[kKvBarKV], h * 64, jt * kTile, bh);
+                tma_load_3d(smem + C::kVLoad + h * kHalf, &tmV, &bars[kKvBarKV], h * 64, jt * kTile, bh);
             }
             int issued = 0;
             for (int t = 0; t < n_it; ++t) {
-                const int s = t & 1;
-                if (t >= 2 && !mbar_wait(&bars[kKvBarEmpty + s], ((t >> 1) - 1) & 1, tmo, true)) {
+                const int s = t % NS, u = t / NS;  // stage, its use count
+                bool waited = true;
+                if (u >= 1)
+                    waited = mbar_wait(&bars[kKvBarEmpty + s], (u - 1) & 1, tmo, true);
+                else if (C::kKvInTmem && s == NS - 1)  // K, V sit in the last stage until copied
+                    waited = mbar_wait(&bars[kKvBarKVCopied], 0, tmo, true);
+                if (!waited) {
                     record_timeout(prm.status, 20);
                     break;
                 }
@@ -270,58 +315,83 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t drain = tmo > kDrainNs ? tmo : kDrainNs;
             mbar_wait(&bars[kKvBarKV], 0, drain, true);
             if (issued > 0)
-                mbar_wait(&bars[kKvBarFull + ((issued - 1) & 1)], ((issued - 1) >> 1) & 1, drain, true);
+                mbar_wait(&bars[kKvBarFull + (issued - 1) % NS], ((issued - 1) / NS) & 1, drain, true);
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             // ---- tensor-core products -------------------------------------------------------
-            // Order per query tile t: dV, dK of the first half of its queries (once the
-            // element-wise warps hand them over), those of the second half, then dP^T of tile
-            // t + 1 (its columns were read with the hand-over) and S^T of tile t + 1 (once the
-            // dV, dK products have read the P^T, dS^T columns).
-            const uint32_t sK = smem_u32(smem + C::kK), sV = smem_u32(smem + C::kV);
+            // Order per query tile t (buffer b = t % 2): dP^T once S^T is read, S^T of tile
+            // t + 1 into the other buffer (once tile t - 1's dV, dK are done with it), then
+            // dV, dK of each query half once its P^T, dS^T are written.  (A scheduler that
+            // issued whichever product was ready, testing the barriers without blocking, ran
+            // slower: its polling took issue slots from the element-wise warps.)
             constexpr uint32_t idS = idesc_bf16_f32_ab(kTile, kTile, 0, 0);
             constexpr uint32_t idT = idesc_bf16_f32_ab(kTile, D, 0, 1);
+            const uint32_t tK = tmem + C::kTmemK, tV = tmem + C::kTmemV;
+            const uint32_t sK = smem_u32(smem + C::kK), sV = smem_u32(smem + C::kV);
+            bool ok = mbar_wait(&bars[kKvBarKV], 0, tmo);
             int where = 21;
-            bool ok = mbar_wait(&bars[kKvBarKV], 0, tmo) && mbar_wait(&bars[kKvBarFull], 0, tmo);
+            if (ok && C::kKvInTmem) {
+                tc_fence_after();
+                const uint32_t sKs = smem_u32(smem + C::kKLoad), sVs = smem_u32(smem + C::kVLoad);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tmem_cp_128x256b(tK + kk * 8, smem_desc_sw128(sKs + off, 16, 1024));
+                    tmem_cp_128x256b(tV + kk * 8, smem_desc_sw128(sVs + off, 16, 1024));
+                }
+                umma_commit(&bars[kKvBarKVCopied]);
+            }
+            if (ok) ok = mbar_wait(&bars[kKvBarFull], 0, tmo);
             if (ok) {
                 tc_fence_after();
-                mma_ss_kmajor<D>(tmem + C::kTmemS, sK, smem_u32(smem + C::kQ), idS);
+                const uint32_t sQ0 = smem_u32(smem + C::kQ);
+                if constexpr (C::kKvInTmem)
+                    mma_ts_kmajor<D>(tmem + C::kTmemBuf, tK, sQ0, idS);
+                else
+                    mma_ss_kmajor<D>(tmem + C::kTmemBuf, sK, sQ0, idS);
                 umma_commit(&bars[kKvBarSFull]);
-                mma_ss_kmajor<D>(tmem + C::kTmemDP, sV, smem_u32(smem + C::kG), idS);
-                umma_commit(&bars[kKvBarDpFull]);
             }
             for (int t = 0; ok && t < n_it; ++t) {
-                const int s = t & 1;
+                const int b = t & 1, s = t % NS, s1 = (t + 1) % NS;
+                const uint32_t buf = tmem + C::kTmemBuf + b * 128;
                 const uint32_t sQ = smem_u32(smem + C::kQ + s * C::kTileBytes);
                 const uint32_t sG = smem_u32(smem + C::kG + s * C::kTileBytes);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    where = 22 + half;
-                    if (!(ok = mbar_wait(&bars[kKvBarP0 + half], t & 1, tmo))) break;
+                where = 22;
+                if (!(ok = mbar_wait(&bars[kKvBarRead], t & 1, tmo))) break;
+                tc_fence_after();
+                if constexpr (C::kKvInTmem)
+                    mma_ts_kmajor<D>(buf, tV, sG, idS);
+                else
+                    mma_ss_kmajor<D>(buf, sV, sG, idS);
+                umma_commit(&bars[kKvBarDpFull]);
+                if (t + 1 < n_it) {
+                    where = 24;
+                    if (!(ok = mbar_wait(&bars[kKvBarFull + s1], ((t + 1) / NS) & 1, tmo))) break;
+                    where = 25;
+                    if (t >= 1 && !(ok = mbar_wait(&bars[kKvBarSFree + (b ^ 1)], ((t - 1) >> 1) & 1, tmo)))
+                        break;
                     tc_fence_after();
-                    const uint32_t acc = (t > 0 || half > 0) ? 1u : 0u;
-                    mma_ts_half(tmem + C::kTmemDV, tmem + C::kTmemS, sG, half, idT, acc);
-                    mma_ts_half(tmem + C::kTmemDK, tmem + C::kTmemS + 8, sQ, half, idT, acc);
+                    const uint32_t nbuf = tmem + C::kTmemBuf + (b ^ 1) * 128;
+                    const uint32_t sQ1 = smem_u32(smem + C::kQ + s1 * C::kTileBytes);
+                    if constexpr (C::kKvInTmem)
+                        mma_ts_kmajor<D>(nbuf, tK, sQ1, idS);
+                    else
+                        mma_ss_kmajor<D>(nbuf, sK, sQ1, idS);
+                    umma_commit(&bars[kKvBarSFull + (b ^ 1)]);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    where = 26 + h;
+                    if (!(ok = mbar_wait(&bars[kKvBarPds + h], t & 1, tmo))) break;
+                    tc_fence_after();
+                    const uint32_t acc = (t > 0 || h > 0) ? 1u : 0u;
+                    mma_ts_half(tmem + C::kTmemDV, buf, sG, h, idT, acc);
+                    mma_ts_half(tmem + C::kTmemDK, buf + 8, sQ, h, idT, acc);
                 }
                 if (!ok) break;
-                umma_commit(&bars[kKvBarSFree]);
+                umma_commit(&bars[kKvBarSFree + b]);
                 umma_commit(&bars[kKvBarEmpty + s]);
-                if (t + 1 < n_it) {
-                    const int s1 = (t + 1) & 1;
-                    where = 24;
-                    if (!(ok = mbar_wait(&bars[kKvBarFull + s1], ((t + 1) >> 1) & 1, tmo))) break;
-                    tc_fence_after();
-                    mma_ss_kmajor<D>(tmem + C::kTmemDP, sV,
-                                     smem_u32(smem + C::kG + s1 * C::kTileBytes), idS);
-                    umma_commit(&bars[kKvBarDpFull]);
-                    where = 25;
-                    if (!(ok = mbar_wait(&bars[kKvBarSFree], t & 1, tmo))) break;
-                    tc_fence_after();
-                    mma_ss_kmajor<D>(tmem + C::kTmemS, sK,
-                                     smem_u32(smem + C::kQ + s1 * C::kTileBytes), idS);
-                    umma_commit(&bars[kKvBarSFull]);
-                }
             }
             if (ok) {
                 umma_commit(&bars[kKvBarAcc]);
@@ -360,28 +430,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, kSoftWarps * 32);
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
-            const int it = i0 + t;
+            const int it = i0 + t, b = t & 1;
+            const uint32_t t_buf = t_row + C::kTmemBuf + b * 128;
             const float next = stager && t + 1 < n_it ? stage_value(it + 1) : 0.f;
-            bool good = mbar_wait(&bars[kKvBarSFull], t & 1, tmo) &&
-                        mbar_wait(&bars[kKvBarDpFull], t & 1, tmo);
+            bool good = mbar_wait(&bars[kKvBarSFull + b], (t >> 1) & 1, tmo);
             if (good) {
                 tc_fence_after();
                 const bool diag = CAUSAL && it == jt;
                 const int lo = diag ? (key < N ? r : kTile) : lo_row;
-#pragma unroll 1
-                for (int k = 0; k < 2; ++k) {
-                    const int c = 2 * k + (sub >> 1);  // queries 0-63 first, then 64-127
+                float p[2][16];
+                // shares of both query halves (this warp's 16 columns of each); the S^T
+                // columns are then handed over to dP^T
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c0 = h * 64 + sub * 16;
                     if (diag || ragged_keys)
-                        kv_part<true>(t_row, ld4, c, sub & 1, lo, prm.scale_log2);
+                        kv_shares<true>(t_buf, ld4, c0, lo, prm.scale_log2, p[h]);
                     else
-                        kv_part<false>(t_row, ld4, c, sub & 1, 0, prm.scale_log2);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[kKvBarP0 + k]);
+                        kv_shares<false>(t_buf, ld4, c0, 0, prm.scale_log2, p[h]);
                 }
-            } else if (lane == 0) {
-                record_timeout(prm.status, 26);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kKvBarRead]);
+                good = mbar_wait(&bars[kKvBarDpFull], t & 1, tmo);
+                if (good) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        kv_grads(t_buf, ld4, h * 64 + sub * 16, p[h]);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[kKvBarPds + h]);
+                    }
+                }
             }
+            if (!good && lane == 0) record_timeout(prm.status, 28);
             // All element-wise warps agree before the staged values are replaced.
             if (!named_bar_and(1, kSoftWarps * 32, good)) {
                 ok = false;
@@ -393,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             // ---- dV (warps 0-7) and scale * dK (warps 8-15), half of the columns per warp ----
             if (!mbar_wait(&bars[kKvBarAcc], 0, tmo)) {
-                if (lane == 0) record_timeout(prm.status, 27);
+                if (lane == 0) record_timeout(prm.status, 29);
             } else {
                 tc_fence_after();
                 // The TMEM loads are warp-wide (.sync.aligned): every lane issues them, and
@@ -428,15 +511,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   S   = Q K_j^T      A = Q, B = K_j       shared memory, K-major
 //   dP  = dO V_j^T     A = dO, B = V_j      shared memory, K-major
 //   dQ += dS K_j       A = dS in TMEM, B = K_j MN-major
+// K_j is read by the first and the last product of a key tile, V_j only by dP: K gets three
+// ring stages and V two, each released as soon as its last reader is done, so that the load of
+// a tile has about a tile's time to land.
 template <int D>
 struct QCfg {
     static constexpr int kTileBytes = (D / 64) * kHalf;
+    static constexpr int kKStages = 3, kVStages = 2;
     static constexpr int kQ = 0;
-    static constexpr int kG = kQ + kTileBytes;      // dO
-    static constexpr int kK = kG + kTileBytes;      // two stages
-    static constexpr int kV = kK + 2 * kTileBytes;  // two stages
-    static constexpr int kBar = kV + 2 * kTileBytes;
-    static constexpr int kBytes = kBar + 128;
+    static constexpr int kG = kQ + kTileBytes;                // dO
+    static constexpr int kK = kG + kTileBytes;                // kKStages stages
+    static constexpr int kV = kK + kKStages * kTileBytes;     // kVStages stages
+    static constexpr int kBar = kV + kVStages * kTileBytes;
+    static constexpr int kBytes = kBar + 256;
     static constexpr int kDynSmem = dyn_smem(kBytes);
     static constexpr uint32_t kTmemS = 0, kTmemDP = 256, kTmemDQ = 384;
     static_assert(kTmemDQ + D <= 512, "TMEM budget");
@@ -444,17 +531,19 @@ struct QCfg {
 };
 
 enum QBar {
-    kQBarQG = 0,      // Q, dO landed
-    kQBarFull = 1,    // [2] K_j, V_j landed in a stage
-    kQBarEmpty = 3,   // [2] a stage's products are done
-    kQBarSFull = 5,   // [2] S in TMEM buffer b
-    kQBarSFree = 7,   // [2] dQ products done with the dS in buffer b
-    kQBarDpFull = 9,  // dP in TMEM
-    kQBarP0 = 10,     // dS of keys 0-63 written (one arrival per element-wise warp)
-    kQBarP1 = 11,     // ... of keys 64-127 (and all of S, dP read)
-    kQBarAcc = 12,    // the last dQ products done
-    kQBarDrain = 13,
-    kQNumBars = 14
+    kQBarQG = 0,       // Q, dO landed
+    kQBarKFull = 1,    // [3] K_j landed in a stage
+    kQBarKEmpty = 4,   // [3] the products reading a K stage are done
+    kQBarVFull = 7,    // [2] V_j landed in a stage
+    kQBarVEmpty = 9,   // [2] dP has read a V stage
+    kQBarSFull = 11,   // [2] S in TMEM buffer b
+    kQBarSFree = 13,   // [2] dQ products done with the dS in buffer b
+    kQBarDpFull = 15,  // dP in TMEM
+    kQBarP0 = 16,      // dS of keys 0-63 written (one arrival per element-wise warp)
+    kQBarP1 = 17,      // ... of keys 64-127 (and all of S, dP read)
+    kQBarAcc = 18,     // the last dQ products done
+    kQBarDrain = 19,
+    kQNumBars = 20
 };
 
 // dS of 16 keys (part `part` of the 32-key chunk c) of the current key tile for this thread's
@@ -509,9 +598,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[kQBarQG], 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(&bars[kQBarKFull + s], 1);
+            mbar_init(&bars[kQBarKEmpty + s], 1);
+        }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[kQBarFull + s], 1);
-            mbar_init(&bars[kQBarEmpty + s], 1);
+            mbar_init(&bars[kQBarVFull + s], 1);
+            mbar_init(&bars[kQBarVEmpty + s], 1);
             mbar_init(&bars[kQBarSFull + s], 1);
             mbar_init(&bars[kQBarSFree + s], 1);
         }
@@ -539,26 +632,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(smem + C::kQ + h * kHalf, &tmQ, &bars[kQBarQG], h * 64, qt * kTile, bh);
                 tma_load_3d(smem + C::kG + h * kHalf, &tmG, &bars[kQBarQG], h * 64, qt * kTile, bh);
             }
-            int issued = 0;
+            int k_issued = 0, v_issued = 0;
             for (int j = 0; j < n_j; ++j) {
-                const int s = j & 1;
-                if (j >= 2 && !mbar_wait(&bars[kQBarEmpty + s], ((j >> 1) - 1) & 1, tmo, true)) {
+                const int ks = j % C::kKStages, ku = j / C::kKStages;  // stage, its use count
+                if (ku >= 1 && !mbar_wait(&bars[kQBarKEmpty + ks], (ku - 1) & 1, tmo, true)) {
                     record_timeout(prm.status, 30);
                     break;
                 }
-                uint8_t* k = smem + C::kK + s * C::kTileBytes;
-                uint8_t* v = smem + C::kV + s * C::kTileBytes;
-                mbar_arrive_expect_tx(&bars[kQBarFull + s], 2 * C::kTileBytes);
-                for (int h = 0; h < D / 64; ++h) {
-                    tma_load_3d(k + h * kHalf, &tmK, &bars[kQBarFull + s], h * 64, j * kTile, bh);
-                    tma_load_3d(v + h * kHalf, &tmV, &bars[kQBarFull + s], h * 64, j * kTile, bh);
+                uint8_t* k = smem + C::kK + ks * C::kTileBytes;
+                mbar_arrive_expect_tx(&bars[kQBarKFull + ks], C::kTileBytes);
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_3d(k + h * kHalf, &tmK, &bars[kQBarKFull + ks], h * 64, j * kTile, bh);
+                ++k_issued;
+                const int vs = j & 1;
+                if (j >= 2 && !mbar_wait(&bars[kQBarVEmpty + vs], ((j >> 1) - 1) & 1, tmo, true)) {
+                    record_timeout(prm.status, 30);
+                    break;
                 }
-                ++issued;
+                uint8_t* v = smem + C::kV + vs * C::kTileBytes;
+                mbar_arrive_expect_tx(&bars[kQBarVFull + vs], C::kTileBytes);
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_3d(v + h * kHalf, &tmV, &bars[kQBarVFull + vs], h * 64, j * kTile, bh);
+                ++v_issued;
             }
             const uint64_t drain = tmo > kDrainNs ? tmo : kDrainNs;
             mbar_wait(&bars[kQBarQG], 0, drain, true);
-            if (issued > 0)
-                mbar_wait(&bars[kQBarFull + ((issued - 1) & 1)], ((issued - 1) >> 1) & 1, drain, true);
+            if (k_issued > 0) {
+                const int j = k_issued - 1;
+                mbar_wait(&bars[kQBarKFull + j % C::kKStages], (j / C::kKStages) & 1, drain, true);
+            }
+            if (v_issued > 0) {
+                const int j = v_issued - 1;
+                mbar_wait(&bars[kQBarVFull + (j & 1)], (j >> 1) & 1, drain, true);
+            }
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
@@ -570,28 +676,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_bf16_f32_ab(kTile, kTile, 0, 0);
             constexpr uint32_t idT = idesc_bf16_f32_ab(kTile, D, 0, 1);
             int where = 31;
-            bool ok = mbar_wait(&bars[kQBarQG], 0, tmo) && mbar_wait(&bars[kQBarFull], 0, tmo);
+            bool ok = mbar_wait(&bars[kQBarQG], 0, tmo) && mbar_wait(&bars[kQBarKFull], 0, tmo) &&
+                      mbar_wait(&bars[kQBarVFull], 0, tmo);
             if (ok) {
                 tc_fence_after();
                 mma_ss_kmajor<D>(tmem + C::kTmemS, sQ, smem_u32(smem + C::kK), idS);
                 umma_commit(&bars[kQBarSFull]);
                 mma_ss_kmajor<D>(tmem + C::kTmemDP, sG, smem_u32(smem + C::kV), idS);
                 umma_commit(&bars[kQBarDpFull]);
+                umma_commit(&bars[kQBarVEmpty]);
             }
             for (int j = 0; ok && j < n_j; ++j) {
                 const int s = j & 1, s1 = (j + 1) & 1;
+                const int ks = j % C::kKStages, ks1 = (j + 1) % C::kKStages;
                 if (j + 1 < n_j) {
                     where = 32;
-                    if (!(ok = mbar_wait(&bars[kQBarFull + s1], ((j + 1) >> 1) & 1, tmo))) break;
+                    if (!(ok = mbar_wait(&bars[kQBarKFull + ks1], ((j + 1) / C::kKStages) & 1, tmo)))
+                        break;
                     where = 33;
                     if (j >= 1 && !(ok = mbar_wait(&bars[kQBarSFree + s1], ((j - 1) >> 1) & 1, tmo)))
                         break;
                     tc_fence_after();
                     mma_ss_kmajor<D>(tmem + C::kTmemS + s1 * 128, sQ,
-                                     smem_u32(smem + C::kK + s1 * C::kTileBytes), idS);
+                                     smem_u32(smem + C::kK + ks1 * C::kTileBytes), idS);
                     umma_commit(&bars[kQBarSFull + s1]);
                 }
-                const uint32_t sKj = smem_u32(smem + C::kK + s * C::kTileBytes);
+                const uint32_t sKj = smem_u32(smem + C::kK + ks * C::kTileBytes);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     where = 34 + half;
@@ -602,11 +712,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 umma_commit(&bars[kQBarSFree + s]);
-                umma_commit(&bars[kQBarEmpty + s]);
+                umma_commit(&bars[kQBarKEmpty + ks]);
                 if (j + 1 < n_j) {
+                    where = 36;
+                    if (!(ok = mbar_wait(&bars[kQBarVFull + s1], ((j + 1) >> 1) & 1, tmo))) break;
+                    tc_fence_after();
                     mma_ss_kmajor<D>(tmem + C::kTmemDP, sG,
                                      smem_u32(smem + C::kV + s1 * C::kTileBytes), idS);
                     umma_commit(&bars[kQBarDpFull]);
+                    umma_commit(&bars[kQBarVEmpty + s1]);
                 }
             }
             if (ok) {
@@ -633,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool good = mbar_wait(&bars[kQBarSFull + s], (j >> 1) & 1, tmo) &&
                         mbar_wait(&bars[kQBarDpFull], j & 1, tmo);
             if (!good) {
-                if (lane == 0) record_timeout(prm.status, 36);
+                if (lane == 0) record_timeout(prm.status, 37);
                 ok = false;
                 break;
             }
@@ -661,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             // ---- scale * dQ of this query tile (a quarter of the columns per warp) ------------
             if (!mbar_wait(&bars[kQBarAcc], 0, tmo)) {
-                if (lane == 0) record_timeout(prm.status, 37);
+                if (lane == 0) record_timeout(prm.status, 38);
             } else {
                 tc_fence_after();
                 constexpr int kCols = D / 4;
