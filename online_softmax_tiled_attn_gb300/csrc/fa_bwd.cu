@@ -62,6 +62,7 @@ struct BwdParams {
     __nv_bfloat16* dK;
     __nv_bfloat16* dV;
     int N, n_tiles, BH;
+    int head_group;  // heads per L2-sized group of the grid
     float scale, scale_log2;
     unsigned long long timeout_ns;
     int* status;  // the library's device status word
@@ -69,6 +70,18 @@ struct BwdParams {
 
 __device__ __forceinline__ void record_timeout(int* status, int where) {
     atomicCAS(status, 0, FA_ERR_TIMEOUT | (where << 8));
+}
+
+// The grid walks groups of heads whose walked tiles fit in L2 together; inside a group the
+// tile index is outer and the head inner, so that the CTAs in flight read different heads'
+// tiles and, with a causal mask, the tiles with the most work start first.  Returns the head
+// and the tile position (0 = first to start) of this CTA.
+__device__ __forceinline__ void grid_place(const BwdParams& prm, int& bh, int& pos) {
+    const int per_group = prm.head_group * prm.n_tiles;
+    const int g = blockIdx.x / per_group, idx = blockIdx.x % per_group;
+    const int heads = min(prm.head_group, prm.BH - g * prm.head_group);
+    bh = g * prm.head_group + idx % heads;
+    pos = idx / heads;
 }
 
 // Eight (d = 128) or four (d = 64) K16 steps of an SS product over K-major 128-byte swizzled
@@ -247,9 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKvNumBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Key tiles in the outer position of the grid: with a causal mask the tiles that see the
-    // most query tiles start first.
-    const int bh = blockIdx.x % prm.BH, jt = blockIdx.x / prm.BH;
+    // Key tile 0 sees the most query tiles under a causal mask: it starts first.
+    int bh, jt;
+    grid_place(prm, bh, jt);
     const int N = prm.N;
     const int i0 = CAUSAL ? jt : 0;
     const int n_it = prm.n_tiles - i0;
@@ -588,10 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kQNumBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Query tiles in the outer position of the grid, last first: with a causal mask the tiles
-    // that see the most key tiles start first.
-    const int bh = blockIdx.x % prm.BH;
-    const int qt = prm.n_tiles - 1 - static_cast<int>(blockIdx.x / prm.BH);
+    // The last query tile sees the most key tiles under a causal mask: it starts first.
+    int bh, pos;
+    grid_place(prm, bh, pos);
+    const int qt = prm.n_tiles - 1 - pos;
     const int N = prm.N;
     const int n_j = CAUSAL ? qt + 1 : prm.n_tiles;
     const unsigned long long tmo = prm.timeout_ns;
@@ -824,7 +837,7 @@ int launch_tiles(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
                                         QCfg<D>::kDynSmem);
     });
     if (attr != cudaSuccess) return FA_ERR_CUDA;
-    const long long ctas = BH * prm.n_tiles;  // tiles outer, heads inner
+    const long long ctas = BH * prm.n_tiles;
     if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     bwd_kv_kernel<D, CAUSAL><<<static_cast<unsigned>(ctas), kThreads, KvCfg<D>::kDynSmem, stream>>>(
         tq, tk, tv, tg, prm);
@@ -869,6 +882,14 @@ int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, co
     prm.N = static_cast<int>(N);
     prm.n_tiles = static_cast<int>((N + kTile - 1) / kTile);
     prm.BH = static_cast<int>(BH);
+    // Heads per group of the grid.  If the walked tiles of all heads (two bf16 [N, d] tensors
+    // each) fit in 64 MB, half of L2, one group.  Otherwise, with a causal mask, groups that
+    // fit (inside a group the longest tiles start first, which keeps the tail short); without
+    // one, a head at a time (measured fastest: the CTAs in flight share two or three heads).
+    const long long head_bytes = 4LL * N * d, budget = 64LL << 20;
+    long long group = BH;
+    if (head_bytes * BH > budget) group = causal ? budget / head_bytes : 1;
+    prm.head_group = static_cast<int>(group < 1 ? 1 : (group > BH ? BH : group));
     prm.scale = scale;
     prm.scale_log2 = scale * kLog2e;
     prm.timeout_ns = fa_wait_timeout_ns();
