@@ -12,11 +12,23 @@
 // GB300 mapping (HBM-bound: 4 bytes read per element, nothing written per element):
 //   * rows up to 4096 columns: one warp per row; longer rows: the 8 warps of a CTA share a row
 //     and their lists meet in shared memory;
-//   * 16-byte streaming loads when the row allows them;
-//   * the k best so far live across the lanes of a warp, one per lane; a new value is compared
+//   * 16-byte loads when the row allows them;
+//   * k >= 2, two passes over the row, the second from L2: the first keeps the running (m, l)
+//     of each thread's part, whose running maximum comes with it; the k-th largest of the
+//     threads' maxima (over a warp; the largest such value over the warps of a CTA) is a floor
+//     under the row's k-th largest value, since k distinct entries reach it.  The second pass
+//     offers only the values at or above max(floor, the list's bar) to the list, so that almost
+//     every value costs a load and one comparison.  (One pass that offered every value to the
+//     list ran at 2.1 and 1.5 TB/s for the two bench workloads: while the list's bar is still
+//     low, most values of the first steps enter it; one pass that compared against a floor
+//     taken after its first step ran at 3.0 and 1.7 TB/s, with fewer loads in flight than a
+//     pure first pass; fewer rows in flight, or chunks, so that the second pass surely hits
+//     L2, ran slower than the full grid.)
+//   * the k best so far live across the lanes of a warp, one per lane; a value is compared
 //     with the k-th best (the bar, the same in every lane), and the few that beat it are
 //     inserted with a ballot and a shuffle.  (Per-thread sorted lists, which most values of a
 //     short per-thread stream enter, measured 0.2-1 TB/s for k = 8..32.)
+//   * k = 1: one pass, a best per lane;
 //   * persistent grid, rows handed out round-robin.
 #include <cuda_runtime.h>
 
@@ -214,6 +226,112 @@ __device__ __forceinline__ void scan(const float* row, int cols, int t, int nthr
     }
 }
 
+// The k-th largest of the 32 lanes' values (the same in every lane): a bitonic sort across the
+// warp into descending order, then lane k - 1's value.
+__device__ __forceinline__ float warp_kth_largest(float x, int k) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, x, stride);
+            const bool desc = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            x = (lower == desc) ? fmaxf(x, o) : fminf(x, o);
+        }
+    }
+    return __shfl_sync(0xffffffffu, x, k - 1);
+}
+
+// k >= 2, pass 1 over units [lo, hi) of a row (a unit is a float4 in the vector form, a
+// float otherwise; thread t of nthr takes units lo + t, lo + t + nthr, ...): the online state,
+// whose running maximum st.m comes with it.  The loads keep the data in L2 for pass 2.
+template <bool VEC>
+__device__ __forceinline__ void stats_pass(const float* row, int lo, int hi, int t, int nthr,
+                                           Stat& st) {
+    constexpr int kAhead = 4;
+    for (int u0 = lo + t; u0 < hi; u0 += kAhead * nthr) {
+        if constexpr (VEC) {
+            const float4* r4 = reinterpret_cast<const float4*>(row);
+            float4 q[kAhead];
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const int u = u0 + a * nthr;
+                q[a] = u < hi ? __ldcg(r4 + u)
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const float v[4] = {q[a].x, q[a].y, q[a].z, q[a].w};
+                update(st, v);  // -inf past the range adds nothing
+            }
+        } else {
+            float v[kAhead];
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const int j = u0 + a * nthr;
+                v[a] = j < hi ? __ldcg(row + j) : -INFINITY;
+            }
+            update(st, v);
+        }
+    }
+}
+
+// k >= 2, pass 2 over the same units: the values at or above `floor` are offered to the warp's
+// list.  All 32 lanes of a warp run the same iterations (the list lives across lanes).
+template <bool VEC>
+__device__ __forceinline__ void select_pass(const float* row, int lo, int hi, int t, int nthr,
+                                            int k, float floor, WarpTop& top) {
+    constexpr int kAhead = 4;
+    const int lane = threadIdx.x & 31;
+    for (int u0 = lo + t - lane; u0 < hi; u0 += kAhead * nthr) {
+        if constexpr (VEC) {
+            const float4* r4 = reinterpret_cast<const float4*>(row);
+            float4 q[kAhead];
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const int u = u0 + a * nthr + lane;
+                q[a] = u < hi ? __ldcs(r4 + u)
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const int u = u0 + a * nthr + lane;
+                const float thr = fmaxf(floor, top.bar_v);
+                const bool cand = u < hi && (q[a].x >= thr || q[a].y >= thr || q[a].z >= thr ||
+                                             q[a].w >= thr);
+                if (__ballot_sync(0xffffffffu, cand)) {
+                    // a lane without a candidate offers nothing: (-inf, INT_MAX) never enters
+                    const float v[4] = {cand ? q[a].x : -INFINITY, cand ? q[a].y : -INFINITY,
+                                        cand ? q[a].z : -INFINITY, cand ? q[a].w : -INFINITY};
+                    const int col[4] = {cand ? 4 * u : INT_MAX, cand ? 4 * u + 1 : INT_MAX,
+                                        cand ? 4 * u + 2 : INT_MAX, cand ? 4 * u + 3 : INT_MAX};
+                    top.offer(v, col, k);
+                }
+            }
+        } else {
+            float v[kAhead];
+            int col[kAhead];
+            const float thr = fmaxf(floor, top.bar_v);
+            bool cand = false;
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                const int j = u0 + a * nthr + lane;
+                const bool in = j < hi;
+                v[a] = in ? __ldcs(row + j) : -INFINITY;
+                col[a] = in ? j : INT_MAX;
+                cand |= in && v[a] >= thr;
+            }
+            if (__ballot_sync(0xffffffffu, cand)) top.offer(v, col, k);
+        }
+    }
+}
+
+template <class Top>
+constexpr bool kFiltered = false;
+template <>
+constexpr bool kFiltered<WarpTop> = true;
+
 // Lane t < k writes the t-th best with its share.
 template <class Top>
 __device__ __forceinline__ void write_top(const Top& top, int k, Stat s, float* vals, int* idx) {
@@ -237,7 +355,13 @@ __global__ void __launch_bounds__(kThreads) topk_warp_rows(const float* __restri
          r += static_cast<long long>(gridDim.x) * kWarps) {
         Stat st{-INFINITY, 0.f};
         Top top;
-        scan<VEC>(x + r * cols, cols, lane, 32, k, st, top);
+        if constexpr (kFiltered<Top>) {
+            const int n = VEC ? cols >> 2 : cols;
+            stats_pass<VEC>(x + r * cols, 0, n, lane, 32, st);
+            select_pass<VEC>(x + r * cols, 0, n, lane, 32, k, warp_kth_largest(st.m, k), top);
+        } else {
+            scan<VEC>(x + r * cols, cols, lane, 32, k, st, top);
+        }
         top.finish();
         st = warp_merge(st);
         if (lse && lane == 0) lse[r] = st.m + logf(st.l);
@@ -254,11 +378,25 @@ __global__ void __launch_bounds__(kThreads) topk_cta_rows(const float* __restric
     __shared__ float cv[kWarps][32];
     __shared__ int cc[kWarps][32];
     __shared__ Stat cs[kWarps];
+    __shared__ float cf[kWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
         Stat st{-INFINITY, 0.f};
         Top top;
-        scan<VEC>(x + r * cols, cols, threadIdx.x, kThreads, k, st, top);
+        if constexpr (kFiltered<Top>) {
+            const int n = VEC ? cols >> 2 : cols;
+            stats_pass<VEC>(x + r * cols, 0, n, threadIdx.x, kThreads, st);
+            // each warp's floor holds for the whole row; the largest is the tightest
+            const float f = warp_kth_largest(st.m, k);
+            if (lane == 0) cf[warp] = f;
+            __syncthreads();
+            float floor = cf[0];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) floor = fmaxf(floor, cf[w]);
+            select_pass<VEC>(x + r * cols, 0, n, threadIdx.x, kThreads, k, floor, top);
+        } else {
+            scan<VEC>(x + r * cols, cols, threadIdx.x, kThreads, k, st, top);
+        }
         top.finish();
         st = warp_merge(st);
         cv[warp][lane] = top.v;
