@@ -36,6 +36,7 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 
@@ -263,6 +264,40 @@ def bwd_inputs(B, H, N, d, seed):
     g = torch.Generator().manual_seed(int(seed))
     shape = (B, H, N, d)
     return tuple(torch.randn(shape, generator=g).to(torch.bfloat16) for _ in range(4))
+
+
+def random_mask(B, H, Nq, Nk, density, seed, full_rows=0, full_keys=0):
+    """A seeded attention mask, uint8 [B, H, Nq, Nk] (1 = allowed), each entry allowed with
+    probability `density`; then `full_rows` seeded query rows of every (b, h) are masked
+    entirely and `full_keys` seeded keys are masked for every query."""
+    g = torch.Generator().manual_seed(int(seed))
+    m = (torch.rand((B, H, Nq, Nk), generator=g) < density).to(torch.uint8)
+    for _ in range(full_rows):
+        m[:, :, int(torch.randint(Nq, (1,), generator=g)), :] = 0
+    for _ in range(full_keys):
+        m[:, :, :, int(torch.randint(Nk, (1,), generator=g))] = 0
+    return m.numpy()
+
+
+def window_mask(Nq, Nk, window, doc_len):
+    """uint8 [1, 1, Nq, Nk]: query i sees key j when they lie in the same document of `doc_len`
+    positions and j <= i < j + window (a sliding window inside documents)."""
+    i = np.arange(Nq)[:, None]
+    j = np.arange(Nk)[None, :]
+    m = (j <= i) & (i < j + window) & (i // doc_len == j // doc_len)
+    return m.astype(np.uint8)[None, None]
+
+
+def pack_mask(mask):
+    """The bit layout fa_fwd_mask reads: uint32 [Bm, Hm, Nq, W] with W = 4 * ceil(Nk / 128);
+    bit j % 32 of word j // 32 of a row is entry j (1 = allowed); bits past Nk are 0."""
+    m = np.asarray(mask) != 0
+    Bm, Hm, Nq, Nk = m.shape
+    W = 4 * ((Nk + 127) // 128)
+    padded = np.zeros((Bm, Hm, Nq, W * 32), dtype=bool)
+    padded[..., :Nk] = m
+    bits = np.packbits(padded.reshape(Bm, Hm, Nq, W, 32), axis=-1, bitorder="little")
+    return np.ascontiguousarray(bits.view(np.uint32).reshape(Bm, Hm, Nq, W))
 
 
 def attn_inputs(B, H, N, d, seed, qk_std=1.0, v_dist="normal"):

@@ -47,6 +47,7 @@ _fp = ctypes.POINTER(ctypes.c_float)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _i32p = ctypes.POINTER(ctypes.c_int32)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
 def _ptr(a, t):
@@ -81,6 +82,12 @@ class Oracle:
                                      ctypes.c_int64, ctypes.c_double, ctypes.c_int, _i32p,
                                      _i64p, ctypes.c_int64, _dp, _dp, ctypes.c_int]
         lib.oracle_attn3.restype = ctypes.c_int
+        lib.oracle_attn4.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_double, ctypes.c_int, _i32p,
+                                     _u8p, ctypes.c_int64, ctypes.c_int64, _i64p, ctypes.c_int64,
+                                     _dp, _dp, ctypes.c_int]
+        lib.oracle_attn4.restype = ctypes.c_int
         lib.oracle_attn_bwd.argtypes = [_u16p, _u16p, _u16p, _u16p, ctypes.c_int64,
                                          ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_double, ctypes.c_int, _dp, _dp, _dp,
@@ -184,12 +191,13 @@ class Oracle:
         return O, L
 
     def attention_gqa(self, Q, K, V, scale: float, causal: bool, kv_lens=None, rows=None,
-                      nthreads: int = 0):
+                      nthreads: int = 0, mask=None):
         """Q [B, H, Nq, d]; K, V [B, H_kv, Nk, d] (bf16 bits), H_kv dividing H.
 
         kv_lens: optional int32 [B], the valid keys of each sequence (keys j >= kv_lens[b] are
-        masked).  Causal: query i sees keys j <= i + (Nk - Nq).  rows: optional flat indices
-        (b*H + h)*Nq + i.  A row with no allowed key gets O = 0 and LSE = -inf.
+        masked).  Causal: query i sees keys j <= i + (Nk - Nq).  mask: optional [B or 1, H or 1,
+        Nq, Nk] array, nonzero = allowed (size-1 leading dimensions repeat).  rows: optional
+        flat indices (b*H + h)*Nq + i.  A row with no allowed key gets O = 0 and LSE = -inf.
         """
         Q, K, V = (_as_bf16_bits(t) for t in (Q, K, V))
         if Q.ndim != 4 or K.shape != V.shape or K.ndim != 4 or Q.shape[0] != K.shape[0] \
@@ -202,6 +210,14 @@ class Oracle:
             lens = np.ascontiguousarray(np.asarray(kv_lens), dtype=np.int32)
             if lens.shape != (B,):
                 raise ValueError("kv_lens must have one entry per sequence")
+        mk, m_bs, m_hs = None, 0, 0
+        if mask is not None:
+            mk = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+            if mk.ndim != 4 or mk.shape[2:] != (Nq, Nk) or mk.shape[0] not in (1, B) \
+                    or mk.shape[1] not in (1, H):
+                raise ValueError("mask must be [B or 1, H or 1, Nq, Nk]")
+            m_hs = Nq * Nk if mk.shape[1] == H and H > 1 else 0
+            m_bs = mk.shape[1] * Nq * Nk if mk.shape[0] == B and B > 1 else 0
         if rows is not None:
             rows = np.ascontiguousarray(rows, dtype=np.int64)
             O = np.empty((rows.size, d), dtype=np.float64)
@@ -211,12 +227,12 @@ class Oracle:
             O = np.empty((B, H, Nq, d), dtype=np.float64)
             L = np.empty((B, H, Nq), dtype=np.float64)
             nrows = 0
-        rc = self._lib.oracle_attn3(_ptr(Q, _u16p), _ptr(K, _u16p), _ptr(V, _u16p), B, H, H_kv,
+        rc = self._lib.oracle_attn4(_ptr(Q, _u16p), _ptr(K, _u16p), _ptr(V, _u16p), B, H, H_kv,
                                     Nq, Nk, d, float(scale), int(bool(causal)), _ptr(lens, _i32p),
-                                    _ptr(rows, _i64p), nrows, _ptr(O, _dp), _ptr(L, _dp),
-                                    nthreads)
+                                    _ptr(mk, _u8p), m_bs, m_hs, _ptr(rows, _i64p), nrows,
+                                    _ptr(O, _dp), _ptr(L, _dp), nthreads)
         if rc != 0:
-            raise ValueError("oracle_attn3 rejected its arguments")
+            raise ValueError("oracle_attn4 rejected its arguments")
         return O, L
 
     def attention_bwd(self, Q, K, V, dO, scale: float, causal: bool, nthreads: int = 0):
@@ -326,6 +342,11 @@ def attention(Q, K, V, scale, causal, rows=None, nthreads: int = 0):
 
 def attention_qk(Q, K, V, scale, causal, rows=None, nthreads: int = 0):
     return load().attention_qk(Q, K, V, scale, causal, rows, nthreads)
+
+
+def attention_masked(Q, K, V, scale, causal, mask, rows=None, nthreads: int = 0):
+    """Attention with an explicit mask [B or 1, H or 1, Nq, Nk] (nonzero = allowed)."""
+    return load().attention_gqa(Q, K, V, scale, causal, rows=rows, nthreads=nthreads, mask=mask)
 
 
 def attention_gqa(Q, K, V, scale, causal, kv_lens=None, rows=None, nthreads: int = 0):

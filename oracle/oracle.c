@@ -261,6 +261,8 @@ typedef struct {
     double scale;
     int causal;
     const int32_t* kv_lens; /* NULL, or [B] valid keys per sequence */
+    const uint8_t* mask;    /* NULL, or 1 = key allowed, [b*mask_bs + h*mask_hs + i*Nk + j] */
+    int64_t mask_bs, mask_hs;
     const int64_t* rows; /* NULL: rows [r0, r1) of the flat (b*H+h)*N+i index */
     double *O, *LSE;
     int64_t r0, r1;
@@ -306,9 +308,26 @@ static void attn_one_row(const attn_job* jb, int64_t flat, double* o, double* ls
     if (jb->kv_lens && nk > jb->kv_lens[b]) nk = jb->kv_lens[b] > 0 ? jb->kv_lens[b] : 0;
 #endif
 
+    /* an explicit mask: keys whose entry is 0 take no part (score -inf) */
+    const uint8_t* mrow = jb->mask ? jb->mask + b * jb->mask_bs + h * jb->mask_hs + i * Nk : NULL;
+
     /* pass 1: scores and their maximum */
     double m = -INFINITY;
     for (int64_t j = 0; j < nk; ++j) {
+#if ORACLE_MUTANT == 19 /* mutant 19: ignores the explicit mask */
+        (void)mrow;
+#elif ORACLE_MUTANT == 20 /* mutant 20: reads the mask transposed (entry j, i) */
+        if (mrow && j < N && i < Nk &&
+            !jb->mask[b * jb->mask_bs + h * jb->mask_hs + j * Nk + i]) {
+            s[j] = -INFINITY;
+            continue;
+        }
+#else
+        if (mrow && !mrow[j]) {
+            s[j] = -INFINITY;
+            continue;
+        }
+#endif
         double acc = 0.0;
         for (int64_t k = 0; k < d; ++k) {
 #if ORACLE_MUTANT == 4
@@ -371,16 +390,17 @@ static void* attn_worker(void* arg) {
  * and query head h reads key/value head h / (H / H_kv).
  * Query i of a head attends to keys j < Nk, or, when causal, to keys j <= i + (Nk - Nq) (the
  * Nq queries are the last Nq of the Nk positions; Nq == Nk is the usual square mask), and, when
- * kv_lens is given, only to keys j < kv_lens[b].  A row with no allowed key gets O = 0 and
- * LSE = -inf.
+ * kv_lens is given, only to keys j < kv_lens[b], and, when mask is given (uint8, 1 = allowed),
+ * only to keys with mask[b*mask_bs + h*mask_hs + i*Nk + j] != 0 (a stride of 0 repeats the
+ * mask over batches or heads).  A row with no allowed key gets O = 0 and LSE = -inf.
  * rows == NULL: compute all B*H*Nq rows; O is [B*H*Nq, d] and LSE [B*H*Nq].
  * rows != NULL: compute the nrows listed flat row indices (b*H + h)*Nq + i; O is [nrows, d].
  * Returns 0, or -1 on bad arguments (including a listed row out of range).
  */
-int oracle_attn3(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
+int oracle_attn4(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
                  int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d, double scale, int causal,
-                 const int32_t* kv_lens, const int64_t* rows, int64_t nrows, double* O,
-                 double* LSE, int nthreads) {
+                 const int32_t* kv_lens, const uint8_t* mask, int64_t mask_bs, int64_t mask_hs,
+                 const int64_t* rows, int64_t nrows, double* O, double* LSE, int nthreads) {
     if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 1) return -1;
     if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return -1;
     const int64_t total = B * H * Nq;
@@ -400,6 +420,7 @@ int oracle_attn3(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_
         attn_job* jb = &jobs[t];
         jb->Q = Q; jb->K = K; jb->V = V; jb->H = H; jb->H_kv = H_kv; jb->N = Nq; jb->Nk = Nk;
         jb->d = d; jb->scale = scale; jb->causal = causal; jb->kv_lens = kv_lens;
+        jb->mask = mask; jb->mask_bs = mask_bs; jb->mask_hs = mask_hs;
         jb->rows = rows; jb->O = O; jb->LSE = LSE;
         jb->r0 = n * t / nt;
         jb->r1 = n * (t + 1) / nt;
@@ -411,6 +432,15 @@ int oracle_attn3(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_
     for (int t = 0; t < nt; ++t) err |= jobs[t].err;
     free(th); free(jobs);
     return err ? -1 : 0;
+}
+
+/* As oracle_attn4 without an explicit mask. */
+int oracle_attn3(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B, int64_t H,
+                 int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d, double scale, int causal,
+                 const int32_t* kv_lens, const int64_t* rows, int64_t nrows, double* O,
+                 double* LSE, int nthreads) {
+    return oracle_attn4(Q, K, V, B, H, H_kv, Nq, Nk, d, scale, causal, kv_lens, NULL, 0, 0, rows,
+                        nrows, O, LSE, nthreads);
 }
 
 /* ------------------------------------------------------------------------------------------ */

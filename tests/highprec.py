@@ -47,10 +47,11 @@ def attention_decimal(q, K, V, scale, causal):
     return O, L
 
 
-def attention_decimal_gqa(q, K, V, scale, causal, kv_lens=None):
+def attention_decimal_gqa(q, K, V, scale, causal, kv_lens=None, mask=None):
     """As attention_decimal, with K, V [B][H_kv][Nk][d] shared by the H query heads (query head
-    h reads key/value head h // (H // H_kv)) and optional key lengths per sequence (keys
-    j >= kv_lens[b] take no part).  A row with no key left gets O = 0 and LSE = -inf.
+    h reads key/value head h // (H // H_kv)), optional key lengths per sequence (keys
+    j >= kv_lens[b] take no part) and an optional mask[b][h][i][j] (false: key j takes no part
+    for query i).  A row with no key left gets O = 0 and LSE = -inf.
     """
     sc = Decimal(scale)
     O, L = [], []
@@ -63,7 +64,8 @@ def attention_decimal_gqa(q, K, V, scale, causal, kv_lens=None):
             Oh, Lh = [], []
             for i in range(N):
                 keys = [j for j in range(Nk)
-                        if (not causal or j <= i + Nk - N) and (kv_lens is None or j < kv_lens[b])]
+                        if (not causal or j <= i + Nk - N) and (kv_lens is None or j < kv_lens[b])
+                        and (mask is None or mask[b][h][i][j])]
                 if not keys:
                     Oh.append([0.0] * d)
                     Lh.append(float("-inf"))

@@ -310,6 +310,70 @@ def pin_gqa_is_attention_with_shared_heads(orc):
         assert np.array_equal(O[:, h:h + 1], Oh) and np.array_equal(L[:, h:h + 1], Lh)
 
 
+def pin_mask_decimal_bruteforce(orc):
+    """An explicit mask (random entries, a fully masked query row, a key masked for every query;
+    alone and with the causal mask, key lengths and grouped heads), against the 40-digit
+    textbook formula.  A row with no allowed key gives O = 0 and LSE = -inf."""
+    cases = [(2, 2, 2, 5, 7, 3, 0.8, False, None, 0.6), (1, 4, 2, 6, 6, 2, 1.1, True, [5], 0.7),
+             (2, 2, 1, 4, 9, 3, 0.5, False, [9, 4], 0.3), (1, 1, 1, 7, 7, 4, 0.9, True, None, 1.0)]
+    for seed, (B, H, H_kv, Nq, Nk, d, scale, causal, lens, dens) in enumerate(cases):
+        q, _, _ = inputs.attn_inputs(B, H, Nq, d, seed=901 + seed, qk_std=1.5)
+        _, k, v = inputs.attn_inputs(B, H_kv, Nk, d, seed=911 + seed, qk_std=1.5)
+        m = inputs.random_mask(B, H, Nq, Nk, dens, seed=921 + seed, full_rows=1, full_keys=1)
+        kl = None if lens is None else np.array(lens, np.int32)
+        O, L = orc.attention_gqa(q, k, v, scale, causal, kv_lens=kl, mask=m)
+        Od, Ld = highprec.attention_decimal_gqa(_bf16_float(q).tolist(), _bf16_float(k).tolist(),
+                                                _bf16_float(v).tolist(), scale, causal, lens,
+                                                mask=m.astype(bool).tolist())
+        what = (B, H, H_kv, causal, lens, dens)
+        assert np.abs(O - np.array(Od)).max() < 1e-13, what
+        Ld = np.array(Ld)
+        assert np.isinf(Ld).any(), what  # the fully masked rows
+        assert np.array_equal(np.isinf(L), np.isinf(Ld)), what
+        fin = np.isfinite(Ld)
+        assert np.abs(L[fin] - Ld[fin]).max() < 1e-13, what
+
+
+def pin_mask_patterns(orc):
+    """Masks that state another rule give that rule's result bit for bit: all ones = no mask,
+    the lower triangle = the causal flag, a prefix of each sequence = its key length; a mask
+    given once for all heads = the same mask repeated."""
+    B, H, N, d = 2, 3, 11, 4
+    q, k, v = inputs.attn_inputs(B, H, N, d, seed=931)
+    O0, L0 = orc.attention(q, k, v, 0.7, False)
+    O1, L1 = orc.attention_gqa(q, k, v, 0.7, False, mask=np.ones((1, 1, N, N), np.uint8))
+    assert np.array_equal(O0, O1) and np.array_equal(L0, L1)
+    Oc, Lc = orc.attention(q, k, v, 0.7, True)
+    Om, Lm = orc.attention_gqa(q, k, v, 0.7, False, mask=np.tril(np.ones((N, N), np.uint8))[None, None])
+    assert np.array_equal(Oc, Om) and np.array_equal(Lc, Lm)
+    lens = [7, 3]
+    pref = np.zeros((B, 1, N, N), np.uint8)
+    for b, n in enumerate(lens):
+        pref[b, :, :, :n] = 1
+    Ok, Lk = orc.attention_gqa(q, k, v, 0.7, False, kv_lens=np.array(lens, np.int32))
+    Op, Lp = orc.attention_gqa(q, k, v, 0.7, False, mask=pref)
+    assert np.array_equal(Ok, Op) and np.array_equal(Lk, Lp)
+    m = inputs.random_mask(1, 1, N, N, 0.5, seed=932)
+    Ob, Lb = orc.attention_gqa(q, k, v, 0.7, False, mask=m)
+    Or, Lr = orc.attention_gqa(q, k, v, 0.7, False, mask=np.broadcast_to(m, (B, H, N, N)))
+    assert np.array_equal(Ob, Or) and np.array_equal(Lb, Lr)
+
+
+def pin_mask_ignores_masked_keys(orc):
+    """A key masked for every query takes no part: huge keys and values planted there change
+    nothing."""
+    B, H, N, d = 1, 2, 8, 3
+    q, k, v = inputs.attn_inputs(B, H, N, d, seed=941)
+    m = inputs.random_mask(B, H, N, N, 0.8, seed=942)
+    m[:, :, :, 5] = 0
+    O, L = orc.attention_gqa(q, k, v, 0.9, False, mask=m)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :, 5] = 50.0
+    v2[:, :, 5] = -1000.0
+    O2, L2 = orc.attention_gqa(q, k2, v2, 0.9, False, mask=m)
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
+
+
 def pin_closed_form_single_valid_key(orc):
     """A sequence of length 1: every query sees key 0 alone, so O = V_0 and LSE = s_0."""
     B, H, Nq, Nk, d = 1, 2, 3, 5, 4

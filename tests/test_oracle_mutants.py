@@ -26,6 +26,8 @@ MUTANTS = {
     16: "backward drops the D term of dS",
     17: "backward flips the sign of dS",
     18: "backward forgets the scale in dQ and dK",
+    19: "explicit mask ignored",
+    20: "explicit mask read transposed",
 }
 
 
