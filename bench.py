@@ -357,6 +357,38 @@ def time_gqa(w, steps, warmup, device, flush):
     return [a.elapsed_time(b) for a, b in ev], splits
 
 
+def time_mask(w, steps, warmup, device, flush):
+    """Per-launch device time (ms) of fa_fwd_mask on a mask workload (mask bits made once)."""
+    import numpy as np
+    import torch
+
+    from online_softmax_tiled_attn_gb300 import binding, inputs
+
+    qd, kd, vd = (t.to(device) for t in inputs.attn_inputs(w.B, w.H, w.N, w.d, w.seed))
+    mb = torch.from_numpy(inputs.pack_mask(w.mask()).view(np.int32)).to(device)
+    O = torch.empty_like(qd)
+    L = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        binding.fa_fwd_mask(qd, kd, vd, mb, scale=w.scale, out=O, lse=L)
+
+    for _ in range(warmup):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    if binding.device_status() != 0:
+        raise RuntimeError("fa_fwd_mask reported a device status")
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def time_bwd(w, steps, warmup, device, flush):
     """Per-call device time (ms) of fa_bwd (its three launches) on a backward workload; the
     forward's O and LSE and the workspace are made outside the timed region."""
@@ -519,6 +551,8 @@ def main(argv=None):
                     help="with --profile: launch fa_fwd_splitkv on the decode workload")
     ap.add_argument("--gqa", default=None,
                     help="with --profile: launch fa_fwd_gqa on this grouped-head workload")
+    ap.add_argument("--mask", default=None,
+                    help="with --profile: launch fa_fwd_mask on this mask workload")
     ap.add_argument("--bwd", default=None,
                     help="with --profile: launch fa_bwd on this backward workload")
     ap.add_argument("--topk", default=None,
@@ -544,7 +578,9 @@ def main(argv=None):
     w = inputs.ATTN_WORKLOADS[args.workload]
 
     if args.profile:
-        if args.bwd:
+        if args.mask:
+            time_mask(inputs.MASK_WORKLOADS[args.mask], args.steps, args.warmup, device, None)
+        elif args.bwd:
             time_bwd(inputs.BWD_WORKLOADS[args.bwd], args.steps, args.warmup, device, None)
         elif args.topk:
             time_topk(inputs.TOPK_WORKLOADS[args.topk], args.steps, args.warmup, device, None)
@@ -648,6 +684,14 @@ def main(argv=None):
                            "ms_per_step": round(tms, 4),
                            "roofline": roofline_hbm(tw.hbm_bytes, tms, peaks, peaks_kind,
                                                     NCU_TRAFFIC_BYTES.get(name))}
+            torch.cuda.empty_cache()
+        for name, mw in inputs.MASK_WORKLOADS.items():
+            t = time_mask(mw, 20, 3, device, flush)
+            mms = max_over_ranks(sum(t) / len(t), dist, device)
+            other[name] = {"TFLOP/s": round(world * mw.flops / (mms * 1e-3) / 1e12, 2),
+                           "ms_per_step": round(mms, 4),
+                           "roofline": roofline_tensor(mw.flops, mms, peaks, peaks_kind,
+                                                       NCU_TRAFFIC_BYTES.get(name))}
             torch.cuda.empty_cache()
         for name, bw in inputs.BWD_WORKLOADS.items():
             t = time_bwd(bw, 20, 3, device, flush)

@@ -166,6 +166,31 @@ OSM_ATTN_API int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void
                                         int64_t n_splits, void* stream);
 
 /*
+ * fa_fwd_mask -- fa_fwd with an explicit mask: an arbitrary set of (query, key) pairs excluded.
+ *
+ * "How FlashAttention avoids storing the giant score table" (spicyshark.co, Online softmax
+ * lesson), section "The implementation": a position a query may not look at gets score -inf,
+ * a block whose scores are all -inf adds nothing, and a row with no allowed key keeps the
+ * empty state (here O = 0, LSE = -inf).  Key j is allowed for query i of head (b, h) when bit
+ * j % 32 of word j / 32 of the row at
+ *     mask + b * mask_b_stride + h * mask_h_stride + i * W,   W = 4 * ceil(Nk / 128)
+ * is set, and, when causal is set, j <= i + (Nk - Nq).
+ *
+ *   Q, O     bf16 [B, H, Nq, d]; K, V bf16 [B, H, Nk, d]; LSE fp32 [B, H, Nq] or NULL.
+ *   mask     DEVICE pointer to uint32 words, 16-byte aligned, read only; each row holds W words
+ *            (the bits past Nk are ignored).
+ *   mask_b_stride, mask_h_stride   words between the masks of consecutive sequences and heads,
+ *            >= 0 and multiples of 4; 0 repeats one mask over all sequences or heads (e.g.
+ *            a [Nq, W] mask shared by every head of every sequence).
+ * Errors as fa_fwd_gqa, plus FA_ERR_INVALID_ARG for a NULL or misaligned mask, bad strides, or
+ * a mask reaching O or LSE.
+ */
+OSM_ATTN_API int fa_fwd_mask(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                             int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                             float scale, int causal, const uint32_t* mask,
+                             int64_t mask_b_stride, int64_t mask_h_stride, void* stream);
+
+/*
  * fa_bwd -- the gradients dQ, dK, dV of fa_fwd's attention for an output gradient dO.
  *
  * "FlashAttention" (paweldubiel.com notes), "Mechanism and details", and "How FlashAttention
@@ -256,7 +281,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 5
+#define OSM_ATTN_ABI_VERSION 6
 
 #ifdef __cplusplus
 }

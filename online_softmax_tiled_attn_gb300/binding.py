@@ -64,6 +64,9 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_splitkv_plan.restype = ctypes.c_int
             L.osm_softmax.argtypes = [vp, vp, i64, i64, vp, vp]
             L.osm_softmax.restype = ctypes.c_int
+            L.fa_fwd_mask.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                      ctypes.c_float, ctypes.c_int, vp, i64, i64, vp]
+            L.fa_fwd_mask.restype = ctypes.c_int
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                  ctypes.c_float, ctypes.c_int, vp]
             L.fa_bwd.restype = ctypes.c_int
@@ -146,6 +149,13 @@ def gqa_plan(B, H, H_kv, Nq, Nk, d, n_splits=0):
 
 def osm_softmax_raw(x_ptr, y_ptr, rows, cols, lse_ptr, stream_ptr):
     return lib().osm_softmax(x_ptr, y_ptr, int(rows), int(cols), lse_ptr, stream_ptr)
+
+
+def fa_fwd_mask_raw(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, mask, mask_b_stride,
+                    mask_h_stride, stream_ptr):
+    return lib().fa_fwd_mask(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d),
+                             float(scale), int(bool(causal)), mask, int(mask_b_stride),
+                             int(mask_h_stride), stream_ptr)
 
 
 def fa_bwd_raw(q, k, v, o, do, lse, dq, dk, dv, ws_d, B, H, N, d, scale, causal, stream_ptr):
@@ -380,3 +390,38 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, workspace=None, stream
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+def fa_fwd_mask(q, k, v, mask_bits, scale=None, causal=False, out=None, lse=None, stream=None):
+    """Attention of q [B,H,Nq,d] over k, v [B,H,Nk,d] (CUDA bf16) with an explicit mask:
+    mask_bits is the CUDA uint32/int32 tensor [B or 1, H or 1, Nq, 4 * ceil(Nk / 128)] that
+    inputs.pack_mask builds (size-1 leading dimensions repeat).  Returns (O, LSE)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 [B, H, N, d] tensor")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k, v must be [B, H, Nk, d] with q's B, H and d")
+    W = 4 * ((Nk + 127) // 128)
+    if (not isinstance(mask_bits, torch.Tensor) or not mask_bits.is_cuda
+            or mask_bits.dtype not in (torch.int32, torch.uint32) or mask_bits.dim() != 4
+            or not mask_bits.is_contiguous() or tuple(mask_bits.shape[2:]) != (Nq, W)
+            or mask_bits.shape[0] not in (1, B) or mask_bits.shape[1] not in (1, H)):
+        raise TypeError("mask_bits must be a contiguous CUDA int32 [B or 1, H or 1, Nq, W]")
+    hs = Nq * W if mask_bits.shape[1] == H and H > 1 else 0
+    bs = mask_bits.shape[1] * Nq * W if mask_bits.shape[0] == B and B > 1 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    O = torch.empty_like(q) if out is None else out
+    L = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = fa_fwd_mask_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), L.data_ptr(),
+                         B, H, Nq, Nk, d, scale, causal, mask_bits.data_ptr(), bs, hs,
+                         _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_mask")
+    return O, L

@@ -32,7 +32,8 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
 int attention_call(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                    int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d, float scale,
                    int causal, const int32_t* kv_lens, int64_t n_splits, float* ws_O,
-                   float* ws_LSE, void* stream) {
+                   float* ws_LSE, void* stream, const uint32_t* mask = nullptr,
+                   int64_t mask_bs = 0, int64_t mask_hs = 0) {
     if (B < 0 || H < 0 || H_kv < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
     if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
     int64_t bh, rows, q_elems, bh_kv, kv_rows, kv_elems;
@@ -62,6 +63,23 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
     if (LSE && (overlaps(LSE, lse_bytes, Q, q_bytes) || overlaps(LSE, lse_bytes, K, kv_bytes) ||
                 overlaps(LSE, lse_bytes, V, kv_bytes)))
         return FA_ERR_INVALID_ARG;
+    if (mask) {
+        // Rows of 4 * ceil(Nk / 128) words, 16-byte aligned: the strides are whole 16-byte
+        // groups, and the furthest row must not reach an output.
+        const int64_t words = 4 * ((Nk + 127) / 128);
+        if (!aligned(mask, 16) || mask_bs < 0 || mask_hs < 0 || mask_bs % 4 != 0 ||
+            mask_hs % 4 != 0 || H_kv != H)
+            return FA_ERR_INVALID_ARG;
+        int64_t ext, t1, t2, t3;
+        if (!mul_ok(B - 1, mask_bs, &t1) || !mul_ok(H - 1, mask_hs, &t2) ||
+            !mul_ok(Nq, words, &t3) || t1 > INT64_MAX / 8 || t2 > INT64_MAX / 8 ||
+            t3 > INT64_MAX / 8)
+            return FA_ERR_INVALID_ARG;
+        ext = (t1 + t2 + t3) * 4;
+        if (overlaps(mask, static_cast<uint64_t>(ext), O, q_bytes) ||
+            (LSE && overlaps(mask, static_cast<uint64_t>(ext), LSE, lse_bytes)))
+            return FA_ERR_INVALID_ARG;
+    }
     const uint64_t len_bytes = static_cast<uint64_t>(B) * 4;
     if (kv_lens && (!aligned(kv_lens, 4) || overlaps(kv_lens, len_bytes, O, q_bytes) ||
                     (LSE && overlaps(kv_lens, len_bytes, LSE, lse_bytes))))
@@ -86,9 +104,9 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
                      overlaps(ws_LSE, wl_bytes, LSE, lse_bytes))))
             return FA_ERR_INVALID_ARG;
     }
-    return osm::fa_fwd_splitkv_launch(Q, K, V, O, LSE,
-                                      osm::AttnShape{B, H, H_kv, Nq, Nk, d, kv_lens, 0}, scale,
-                                      causal != 0, n_splits, ws_O, ws_LSE, st);
+    return osm::fa_fwd_splitkv_launch(
+        Q, K, V, O, LSE, osm::AttnShape{B, H, H_kv, Nq, Nk, d, kv_lens, 0, mask, mask_bs, mask_hs},
+        scale, causal != 0, n_splits, ws_O, ws_LSE, st);
 }
 
 }  // namespace
@@ -179,6 +197,15 @@ int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
                void* stream) {
     return attention_call(Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, causal, kv_lens,
                           n_splits, ws_O, ws_LSE, stream);
+}
+
+int fa_fwd_mask(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+                int64_t H, int64_t Nq, int64_t Nk, int64_t d, float scale, int causal,
+                const uint32_t* mask, int64_t mask_b_stride, int64_t mask_h_stride,
+                void* stream) {
+    if (!mask) return FA_ERR_INVALID_ARG;
+    return attention_call(Q, K, V, O, LSE, B, H, H, Nq, Nk, d, scale, causal, nullptr, 1,
+                          nullptr, nullptr, stream, mask, mask_b_stride, mask_h_stride);
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,

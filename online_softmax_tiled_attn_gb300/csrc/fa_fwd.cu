@@ -176,6 +176,12 @@ struct FaParams {
     // then position r % q_pos of query head r / q_pos.
     int q_pos;
     const int32_t* kv_lens;  // [BH / H] valid keys per sequence, or nullptr (all Nk valid)
+    // Explicit mask (uint32 words, one bit per key, 1 = allowed), or nullptr: the row of query
+    // head bh = b H + h, position i, starts at mask + b mask_bs + h mask_hs + i mask_words, and
+    // each key tile's 128 bits are one 16-byte group of it.
+    const uint32_t* mask;
+    long long mask_bs, mask_hs;
+    int mask_words;
     float scale_log2;
     unsigned long long timeout_ns;
 };
@@ -259,7 +265,9 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int stages, int issue
     }
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+// MASK: an explicit mask is read (prm.mask); a separate instantiation, so that the unmasked
+// kernels' code is unchanged.
+template <int D, bool CAUSAL, bool SPLIT, bool MASK = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FaParams prm) {
@@ -608,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = cta_item(k, prm.n_items);
             if (idx < 0) break;
             int n, kt0, key_limit;
+            const uint4* mask_row = nullptr;  // this row's mask bits, 16 bytes per key tile
             {
                 const Item w = decode_item<CAUSAL>(idx, prm);
                 n = w.n_kv;
@@ -615,6 +624,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int q_row = w.q_tile * kBM + r;
                 const int pos = q_row % prm.q_pos;  // position of the row's query
                 key_limit = CAUSAL ? min(w.kv_len - 1, pos + (Nk - prm.q_pos)) : w.kv_len - 1;
+                if (MASK) {
+                    const long long b = w.bh / prm.H, h = w.bh % prm.H;
+                    const long long i = q_row < prm.Nq ? q_row : 0;  // rows past Nq: unused
+                    mask_row = reinterpret_cast<const uint4*>(prm.mask + b * prm.mask_bs +
+                                                              h * prm.mask_hs +
+                                                              i * prm.mask_words);
+                }
             }
             float m_last = -INFINITY;  // reference max this group used last (scaled, log2)
             float l = 0.f;             // this group's sum of 2^(t - m_last) over its tiles
@@ -640,6 +656,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 128; ++e)
                         if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
+                }
+                if (MASK) {
+                    // The explicit mask: a key whose bit is 0 takes no part (score -inf).
+                    // Words of all ones or all zeros (the usual case for structured masks)
+                    // cost one test.
+                    const uint4 mw = mask_row[kt0 + t];
+                    const uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (words[c] == 0xffffffffu) continue;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (!((words[c] >> e) & 1u)) sr[c * 32 + e] = __float_as_uint(-INFINITY);
+                    }
                 }
                 // Row max with two-input max.f32: on this GPU the three-input form issues far
                 // more slowly and holds back the exponentials that follow.
@@ -819,14 +849,14 @@ int device_sm_count() {
     return n;
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool MASK = false>
 int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const FaParams& prm, cudaStream_t stream) {
     using C = Cfg<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, SPLIT>,
+        attr_err = cudaFuncSetAttribute(fa_fwd_kernel<D, CAUSAL, SPLIT, MASK>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
     });
     if (attr_err != cudaSuccess) return FA_ERR_CUDA;
@@ -849,7 +879,7 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     }
     const int sms = device_sm_count();
     const long long ctas = (sms > 0 && items > sms) ? sms : items;
-    fa_fwd_kernel<D, CAUSAL, SPLIT>
+    fa_fwd_kernel<D, CAUSAL, SPLIT, MASK>
         <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -857,6 +887,16 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
 template <bool SPLIT>
 int launch_dispatch(int64_t d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                     const CUtensorMap& tv, const FaParams& prm, cudaStream_t stream) {
+    if (prm.mask) {  // explicit masks run one pass
+        if (SPLIT) return FA_ERR_UNSUPPORTED;
+        if (d == 64)
+            return causal ? launch_kernel<64, true, false, true>(tq, tk, tv, prm, stream)
+                          : launch_kernel<64, false, false, true>(tq, tk, tv, prm, stream);
+        if (d == 128)
+            return causal ? launch_kernel<128, true, false, true>(tq, tk, tv, prm, stream)
+                          : launch_kernel<128, false, false, true>(tq, tk, tv, prm, stream);
+        return FA_ERR_UNSUPPORTED;
+    }
     if (d == 64)
         return causal ? launch_kernel<64, true, SPLIT>(tq, tk, tv, prm, stream)
                       : launch_kernel<64, false, SPLIT>(tq, tk, tv, prm, stream);
@@ -887,6 +927,10 @@ FaParams base_params(const AttnShape& sh, float scale) {
     prm.H = static_cast<int>(sh.H);
     prm.H_kv = static_cast<int>(sh.H_kv);
     prm.kv_lens = sh.kv_lens;
+    prm.mask = sh.mask;
+    prm.mask_bs = sh.mask_bs;
+    prm.mask_hs = sh.mask_hs;
+    prm.mask_words = static_cast<int>(4 * ((sh.Nk + kBN - 1) / kBN));
     prm.q_pos = static_cast<int>(sh.q_pos > 0 ? sh.q_pos : sh.Nq);
     prm.n_qtiles = static_cast<int>((sh.Nq + kBM - 1) / kBM);
     prm.scale_log2 = scale * 1.4426950408889634f;
@@ -897,7 +941,7 @@ FaParams base_params(const AttnShape& sh, float scale) {
 }  // namespace
 
 AttnShape pack_query_heads(const AttnShape& sh) {
-    if (sh.H_kv <= 0 || sh.H_kv >= sh.H || sh.q_pos > 0) return sh;
+    if (sh.H_kv <= 0 || sh.H_kv >= sh.H || sh.q_pos > 0 || sh.mask) return sh;
     return AttnShape{sh.B, sh.H_kv, sh.H_kv, (sh.H / sh.H_kv) * sh.Nq, sh.Nk, sh.d, sh.kv_lens,
                      sh.Nq};
 }

@@ -25,6 +25,11 @@ struct AttnShape {
     int64_t B, H, H_kv, Nq, Nk, d;
     const int32_t* kv_lens;
     int64_t q_pos;
+    // Optional explicit mask: uint32 words, row i of query head (b, h) at
+    // mask + b * mask_bs + h * mask_hs + i * 4 * ceil(Nk / 128); bit j % 32 of word j / 32 set =
+    // key j allowed.  Not combined with packed query heads.
+    const uint32_t* mask = nullptr;
+    int64_t mask_bs = 0, mask_hs = 0;
 };
 
 // The same call with the H / H_kv query heads that share a key/value head packed into one row

@@ -300,6 +300,61 @@ def pack_mask(mask):
     return np.ascontiguousarray(bits.view(np.uint32).reshape(Bm, Hm, Nq, W))
 
 
+@dataclass(frozen=True)
+class MaskWorkload:
+    """Attention over Q, K, V [B, H, N, d] (N(0,1), from attn_inputs with this seed) with an
+    explicit mask: "prefix_lm" (keys before `prefix` seen by every query, the rest causally;
+    one [1, 1, N, N] mask for all heads) or "random" (each entry allowed with probability
+    `density`, one mask per head, [1, H, N, N])."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    seed: int
+    kind: str
+    prefix: int = 0
+    density: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def mask(self):
+        if self.kind == "prefix_lm":
+            i = np.arange(self.N)[:, None]
+            j = np.arange(self.N)[None, :]
+            return ((j < self.prefix) | (j <= i)).astype(np.uint8)[None, None]
+        return random_mask(1, self.H, self.N, self.N, self.density, self.seed + 1)
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOP: 4*d per allowed (query, key) pair, summed over every head."""
+        m = self.mask()
+        per_mask = float(np.count_nonzero(m))
+        heads_per_mask = self.B * self.H / m.shape[1]
+        return 4.0 * self.d * per_mask * heads_per_mask
+
+    @property
+    def hbm_bytes(self) -> int:
+        """Compulsory HBM traffic: Q, K, V read and O written (bf16), LSE (fp32), the mask bits."""
+        n = self.B * self.H * self.N
+        m = self.mask()
+        return 4 * n * self.d * 2 + n * 4 + m.shape[1] * self.N * (4 * ((self.N + 127) // 128)) * 4
+
+
+MASK_WORKLOADS = {
+    w.name: w
+    for w in [
+        MaskWorkload("mask_prefixlm_b2h16n4096d128", 2, 16, 4096, 128, 1015, "prefix_lm",
+                     prefix=1024),
+        MaskWorkload("mask_random_b2h16n4096d128", 2, 16, 4096, 128, 1016, "random",
+                     density=0.9),
+    ]
+}
+
+
 def attn_inputs(B, H, N, d, seed, qk_std=1.0, v_dist="normal"):
     """Q, K, V as CPU bf16 tensors [B, H, N, d] drawn from one seeded generator."""
     g = torch.Generator().manual_seed(int(seed))

@@ -25,7 +25,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "fa_fwd_gqa_plan",
-              "osm_softmax", "osm_softmax_topk", "fa_bwd",
+              "osm_softmax", "osm_softmax_topk", "fa_bwd", "fa_fwd_mask",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
@@ -50,7 +50,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 5
+    assert binding.lib().osm_attn_abi_version() == 6
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -200,6 +200,30 @@ def test_fa_bwd_rejects_on_host(over, want):
     rc = binding.fa_bwd_raw(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
                             a["dv"], a["ws_d"], a["B"], a["H"], a["N"], a["d"], a["scale"],
                             a["causal"], None)
+    assert rc == want
+
+
+@pytest.mark.parametrize(
+    "over, want",
+    [
+        (dict(mask=0), binding.FA_ERR_INVALID_ARG),               # no mask
+        (dict(mask=P + 9 * 16384 + 4), binding.FA_ERR_INVALID_ARG),  # misaligned
+        (dict(mbs=-4), binding.FA_ERR_INVALID_ARG),
+        (dict(mhs=6), binding.FA_ERR_INVALID_ARG),                 # not whole 16-byte groups
+        (dict(mask=P + 3 * 16384), binding.FA_ERR_INVALID_ARG),    # mask on O
+        (dict(d=96), binding.FA_ERR_UNSUPPORTED),
+        (dict(Nq=0), binding.FA_OK),
+    ],
+)
+def test_fa_fwd_mask_rejects_on_host(over, want):
+    """B1 H1 N128 d64 at distinct fake addresses (16 KiB per tensor), mask at the tenth."""
+    T = 128 * 64 * 2
+    a = dict(q=P, k=P + T, v=P + 2 * T, o=P + 3 * T, lse=P + 4 * T, B=1, H=1, Nq=128, Nk=128,
+             d=64, scale=0.125, causal=0, mask=P + 9 * T, mbs=0, mhs=0)
+    a.update(over)
+    rc = binding.fa_fwd_mask_raw(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                                 a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], a["mask"],
+                                 a["mbs"], a["mhs"], None)
     assert rc == want
 
 
