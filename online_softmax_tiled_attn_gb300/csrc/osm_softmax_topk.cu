@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include "osm_internal.h"
+#include "ptx_sm103.cuh"
 
 namespace osm {
 namespace {
@@ -226,9 +227,9 @@ __device__ __forceinline__ void scan(const float* row, int cols, int t, int nthr
     }
 }
 
-// The k-th largest of the 32 lanes' values (the same in every lane): a bitonic sort across the
-// warp into descending order, then lane k - 1's value.
-__device__ __forceinline__ float warp_kth_largest(float x, int k) {
+// The 32 lanes' values sorted across the warp in descending order (bitonic network): lane i
+// gets the (i+1)-th largest.
+__device__ __forceinline__ float warp_sorted_desc(float x) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int size = 2; size <= 32; size <<= 1) {
@@ -240,7 +241,12 @@ __device__ __forceinline__ float warp_kth_largest(float x, int k) {
             x = (lower == desc) ? fmaxf(x, o) : fminf(x, o);
         }
     }
-    return __shfl_sync(0xffffffffu, x, k - 1);
+    return x;
+}
+
+// The k-th largest of the 32 lanes' values (the same in every lane).
+__device__ __forceinline__ float warp_kth_largest(float x, int k) {
+    return __shfl_sync(0xffffffffu, warp_sorted_desc(x), k - 1);
 }
 
 // k >= 2, pass 1 over units [lo, hi) of a row (a unit is a float4 in the vector form, a
@@ -344,6 +350,224 @@ __device__ __forceinline__ void write_top(const Top& top, int k, Stat s, float* 
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Rows of up to 4096 columns with 16-byte access, k >= 2: rows staged in shared memory.
+// Each warp owns one or more row buffers; its lane 0 brings rows into them with bulk copies
+// (cp.async.bulk), and a buffer takes its next row as soon as the warp has swept it, so the
+// copy runs while the warp finishes the row (the row is read from HBM once, and no register
+// holds it across a wait).  From shared memory the warp sweeps the row twice:
+//   1. the lane maxima, sorted across the warp: the largest is the row max m, the k-th largest
+//      the floor (k distinct entries reach it, so every entry of the top k does too);
+//   2. each lane's sum of exp(x - m), and the compaction of the entries that can still enter
+//      the top k (at or above the floor and ranking before the list's k-th entry, the bar)
+//      into a small candidate buffer.  Whenever it holds 32 or more, 32 of them are sorted
+//      across the warp (a bitonic network) and merged into the warp's list of the best 32 so
+//      far (the better of entry i and entry 31 - i of the two sorted lists, then a bitonic
+//      merge), and the bar rises.
+// The lane sums add up to l by a warp sum; lse = m + ln l.
+constexpr int kStagedMaxCols = 4096;
+constexpr int kStagedWarps = 4;       // warps per CTA
+constexpr int kStagedMaxRing = 4;     // row buffers per warp
+constexpr int kCandCap = 288;         // a batch of 32 plus one step's 256 candidates
+constexpr unsigned long long kStagedDrainNs = 1000000000ull;
+
+__device__ __forceinline__ float max4(const float4& q) {
+    return fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
+}
+
+// Compare-exchange with the lane `stride` away: this lane keeps the better of the two entries
+// if keep_better, else the worse (the order of `before`; all entries are distinct except the
+// padding (-inf, INT_MAX)).
+__device__ __forceinline__ void cmpx(float& v, int& c, int stride, bool keep_better) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+    const int oc = __shfl_xor_sync(0xffffffffu, c, stride);
+    if (before(ov, oc, v, c) == keep_better) {
+        v = ov;
+        c = oc;
+    }
+}
+
+// Sorts one entry per lane across the warp, best in lane 0 (bitonic network).
+__device__ __forceinline__ void warp_sort_desc(float& v, int& c) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const bool desc = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            cmpx(v, c, stride, lower == desc);
+        }
+    }
+}
+
+// (lv, lc): the warp's list of the best 32 so far, sorted, best in lane 0.  (xv, xc): one new
+// entry per lane.  Leaves the best 32 of both in (lv, lc), sorted.
+__device__ __forceinline__ void merge_batch(float& lv, int& lc, float xv, int xc) {
+    const int lane = threadIdx.x & 31;
+    warp_sort_desc(xv, xc);
+    // the new entries in ascending order against the list's descending: the better of each
+    // pair are the best 32 of the union, as a bitonic sequence
+    const float rv = __shfl_sync(0xffffffffu, xv, 31 - lane);
+    const int rc = __shfl_sync(0xffffffffu, xc, 31 - lane);
+    if (before(rv, rc, lv, lc)) {
+        lv = rv;
+        lc = rc;
+    }
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) cmpx(lv, lc, stride, (lane & stride) == 0);
+}
+
+// Lane 0 only: the bulk copy of row r into buffer `buf`, completing on `bar`.
+__device__ __forceinline__ void staged_issue(float4* buf, const float* x, long long r, int cols,
+                                             uint64_t* bar) {
+    const uint32_t bytes = static_cast<uint32_t>(cols) * 4u;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(buf, x + r * cols, bytes, bar);
+}
+
+// The staged kernel.  Warp w of CTA c takes rows c * kStagedWarps + w, then that plus the
+// number of warps in the grid, and so on; `ring` buffers of `pitch4` float4 per warp, then a
+// candidate buffer per warp.  Every wait is bounded: a warp that gives up records
+// FA_ERR_TIMEOUT in *status, waits (bounded) for the copies it still has in flight and leaves.
+__global__ void __launch_bounds__(kStagedWarps * 32)
+    topk_staged_rows(const float* __restrict__ x, long long rows, int cols, int k,
+                     float* __restrict__ vals, int* __restrict__ idx, float* __restrict__ lse,
+                     int ring, int pitch4, int* status, unsigned long long timeout_ns) {
+    extern __shared__ __align__(128) float4 staged_smem[];
+    __shared__ uint64_t bars[kStagedWarps][kStagedMaxRing];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row_f4 = static_cast<long long>(ring) * pitch4;  // per warp
+    float4* buf = staged_smem + warp * row_f4;
+    float* cv = reinterpret_cast<float*>(staged_smem + kStagedWarps * row_f4) + warp * 2 * kCandCap;
+    int* cc = reinterpret_cast<int*>(cv + kCandCap);
+    uint64_t* bar = bars[warp];
+    const long long tw = static_cast<long long>(gridDim.x) * kStagedWarps;
+    const long long r0 = static_cast<long long>(blockIdx.x) * kStagedWarps + warp;
+    const int n4 = cols >> 2;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    if (lane == 0) {
+        for (int b = 0; b < ring; ++b) mbar_init(&bar[b], 1);
+        fence_mbar_init();
+        for (int b = 0; b < ring; ++b)
+            if (r0 + b * tw < rows) staged_issue(buf + b * pitch4, x, r0 + b * tw, cols, &bar[b]);
+    }
+    __syncwarp();
+    int i = 0;
+    for (long long r = r0; r < rows; r += tw, ++i) {
+        const int b = i % ring;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar[b], (i / ring) & 1, timeout_ns))) {
+            if (lane == 0) {
+                atomicCAS(status, 0, FA_ERR_TIMEOUT | (40 << 8));
+                const unsigned long long drain =
+                    timeout_ns > kStagedDrainNs ? timeout_ns : kStagedDrainNs;
+                for (int j = i; j < i + ring && r0 + j * tw < rows; ++j)
+                    mbar_wait(&bar[j % ring], (j / ring) & 1, drain);
+            }
+            return;
+        }
+        const float4* s4 = buf + b * pitch4;
+        // Sweep 1: the lane's maximum, four independent chains; sorted across the warp.
+        float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+        int u = lane;
+        for (; u + 96 < n4; u += 128) {
+            ma = fmaxf(ma, max4(s4[u]));
+            mb = fmaxf(mb, max4(s4[u + 32]));
+            mc = fmaxf(mc, max4(s4[u + 64]));
+            md = fmaxf(md, max4(s4[u + 96]));
+        }
+        for (; u < n4; u += 32) ma = fmaxf(ma, max4(s4[u]));
+        const float sorted = warp_sorted_desc(fmaxf(fmaxf(ma, mb), fmaxf(mc, md)));
+        const float m = __shfl_sync(0xffffffffu, sorted, 0);
+        const float floor = __shfl_sync(0xffffffffu, sorted, k - 1);
+        // Sweep 2: every lane runs the same iterations, two float4 per lane per step.
+        const float mu = m == -INFINITY ? 0.f : m;  // a row of -inf: every term exp(-inf) = 0
+        const float2 nmu = make_float2(-mu, -mu);
+        const float2 c2 = make_float2(kLog2e, kLog2e);
+        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
+        const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        float lv = -INFINITY, bar_v = -INFINITY;  // list entry of this lane; the k-th entry
+        int lc = INT_MAX, bar_c = INT_MAX;
+        int n = 0;  // entries in the candidate buffer (the same in every lane)
+        for (int u0 = 0; u0 < n4; u0 += 64) {
+            const int ua = u0 + lane, ub = u0 + 32 + lane;
+            const float4 qa = ua < n4 ? s4[ua] : ninf;
+            const float4 qb = ub < n4 ? s4[ub] : ninf;
+            // x - m first, then the scale: the largest terms keep full relative accuracy
+            float2 ta = fmul2(fadd2(make_float2(qa.x, qa.y), nmu), c2);
+            float2 tb = fmul2(fadd2(make_float2(qa.z, qa.w), nmu), c2);
+            la = fadd2(la, make_float2(ex2a(ta.x), ex2a(ta.y)));
+            lb = fadd2(lb, make_float2(ex2a(tb.x), ex2a(tb.y)));
+            ta = fmul2(fadd2(make_float2(qb.x, qb.y), nmu), c2);
+            tb = fmul2(fadd2(make_float2(qb.z, qb.w), nmu), c2);
+            la = fadd2(la, make_float2(ex2a(ta.x), ex2a(ta.y)));
+            lb = fadd2(lb, make_float2(ex2a(tb.x), ex2a(tb.y)));
+            // quick test per float4, the exact one per entry only where it passes
+            const float thr = fmaxf(floor, bar_v);
+            const bool pa = ua < n4 && max4(qa) >= thr;
+            const bool pb = ub < n4 && max4(qb) >= thr;
+            if (__any_sync(0xffffffffu, pa || pb)) {
+                const float v[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int col = (e < 4 ? 4 * ua : 4 * ub) + (e & 3);
+                    const bool cand = (e < 4 ? pa : pb) && v[e] >= floor &&
+                                      before(v[e], col, bar_v, bar_c);
+                    const unsigned bal = __ballot_sync(0xffffffffu, cand);
+                    if (cand) {
+                        const int pos = n + __popc(bal & lt_mask);
+                        cv[pos] = v[e];
+                        cc[pos] = col;
+                    }
+                    n += __popc(bal);
+                }
+                if (n >= 32) {
+                    __syncwarp();
+                    int base = 0;
+                    for (; n - base >= 32; base += 32)
+                        merge_batch(lv, lc, cv[base + lane], cc[base + lane]);
+                    // the rest (fewer than 32) moves to the front
+                    const int rem = n - base;
+                    float tv = 0.f;
+                    int tc = 0;
+                    if (lane < rem) {
+                        tv = cv[base + lane];
+                        tc = cc[base + lane];
+                    }
+                    __syncwarp();
+                    if (lane < rem) {
+                        cv[lane] = tv;
+                        cc[lane] = tc;
+                    }
+                    __syncwarp();
+                    n = rem;
+                    bar_v = __shfl_sync(0xffffffffu, lv, k - 1);
+                    bar_c = __shfl_sync(0xffffffffu, lc, k - 1);
+                }
+            }
+        }
+        // Every lane has read buffer b: it may take row r + ring * tw.  The generic-proxy
+        // reads are ordered before the bulk copy's writes by the fence.
+        __syncwarp();
+        if (lane == 0 && r + ring * tw < rows) {
+            fence_proxy_async_smem();
+            staged_issue(buf + b * pitch4, x, r + ring * tw, cols, &bar[b]);
+        }
+        if (n > 0) {
+            const bool has = lane < n;
+            merge_batch(lv, lc, has ? cv[lane] : -INFINITY, has ? cc[lane] : INT_MAX);
+        }
+        float l = (la.x + la.y) + (lb.x + lb.y);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if (lse && lane == 0) lse[r] = m + logf(l);
+        if (lane < k) {
+            vals[r * k + lane] = ex2a((lv - mu) * kLog2e) * (l > 0.f ? 1.f / l : 0.f);
+            idx[r * k + lane] = lc;
+        }
+    }
+}
+
 template <bool VEC, class Top>
 __global__ void __launch_bounds__(kThreads) topk_warp_rows(const float* __restrict__ x,
                                                            long long rows, int cols, int k,
@@ -432,11 +656,44 @@ int sm_count() {
     return n;
 }
 
+// The staged kernel: up to four CTAs of four warps per SM, each warp with one to kStagedMaxRing
+// row buffers.
+int launch_staged(const float* x, long long rows, int cols, int k, float* vals, int* idx,
+                  float* lse, cudaStream_t stream) {
+    constexpr int kSmemCap = 100 * 1024;  // above any request below
+    static cudaError_t attr = cudaSuccess;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(topk_staged_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemCap);
+    });
+    if (attr != cudaSuccess) return FA_ERR_CUDA;
+    int* status = device_status_word();
+    if (!status) return FA_ERR_CUDA;
+    const int pitch4 = ((cols >> 2) + 7) & ~7;  // float4 per buffer: 128-byte multiples
+    const int buf_bytes = pitch4 * 16;
+    // About 18 KB of row buffers per warp (one buffer for the longest rows), so that three or
+    // four CTAs (12-16 warps) fit on an SM.
+    int ring = 18 * 1024 / buf_bytes;
+    ring = ring < 1 ? 1 : (ring > kStagedMaxRing ? kStagedMaxRing : ring);
+    const int smem = kStagedWarps * (ring * buf_bytes + 2 * kCandCap * 4);
+    long long per_sm = (227 * 1024) / (smem + 1152);
+    per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+    const long long sms = sm_count() > 0 ? sm_count() : 148;
+    long long grid = (rows + kStagedWarps - 1) / kStagedWarps;
+    if (grid > sms * per_sm) grid = sms * per_sm;
+    topk_staged_rows<<<static_cast<unsigned>(grid), kStagedWarps * 32, smem, stream>>>(
+        x, rows, cols, k, vals, idx, lse, ring, pitch4, status, fa_wait_timeout_ns());
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 template <class Top>
 int launch(const float* x, long long rows, int cols, int k, float* vals, int* idx, float* lse,
            cudaStream_t stream) {
     const bool vec = (cols % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
     const long long sms = sm_count() > 0 ? sm_count() : 148;
+    if (kFiltered<Top> && vec && cols <= kStagedMaxCols)
+        return launch_staged(x, rows, cols, k, vals, idx, lse, stream);
     if (cols <= 4096) {
         long long grid = (rows + kWarps - 1) / kWarps;
         if (grid > sms * 8) grid = sms * 8;
