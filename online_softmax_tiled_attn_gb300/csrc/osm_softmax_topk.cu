@@ -358,17 +358,21 @@ __device__ __forceinline__ void write_top(const Top& top, int k, Stat s, float* 
 // holds it across a wait).  From shared memory the warp sweeps the row twice:
 //   1. the lane maxima, sorted across the warp: the largest is the row max m, the k-th largest
 //      the floor (k distinct entries reach it, so every entry of the top k does too);
-//   2. each lane's sum of exp(x - m), and the compaction of the entries that can still enter
-//      the top k (at or above the floor and ranking before the list's k-th entry, the bar)
-//      into a small candidate buffer.  Whenever it holds 32 or more, 32 of them are sorted
-//      across the warp (a bitonic network) and merged into the warp's list of the best 32 so
-//      far (the better of entry i and entry 31 - i of the two sorted lists, then a bitonic
-//      merge), and the bar rises.
+//   2. each lane's sum of exp(x - m), and the compaction of the float4 groups that can still
+//      bring an entry into the top k (largest entry at or above the floor and not below the
+//      list's k-th entry, the bar) into a small candidate buffer, one vote per group.
+//      Whenever it holds 32 entries or more, 32 of them are sorted across the warp (a bitonic
+//      network) and merged into the warp's list of the best 32 so far (the better of entry i
+//      and entry 31 - i of the two sorted lists, then a bitonic merge), and the bar rises.
+//      (Entry-by-entry compaction, eight votes per step, cost half again as many
+//      instructions per row.)
 // The lane sums add up to l by a warp sum; lse = m + ln l.
 constexpr int kStagedMaxCols = 4096;
 constexpr int kStagedWarps = 4;       // warps per CTA
 constexpr int kStagedMaxRing = 4;     // row buffers per warp
-constexpr int kCandCap = 288;         // a batch of 32 plus one step's 256 candidates
+constexpr int kCoarseCap = 136;       // 7 groups left over + one step's 128 groups
+constexpr int kFineCap = 64;          // 31 entries left over + one batch's 32
+constexpr int kCandBytes = kCoarseCap * 4 + kFineCap * 8;  // per warp
 constexpr unsigned long long kStagedDrainNs = 1000000000ull;
 
 __device__ __forceinline__ float max4(const float4& q) {
@@ -426,6 +430,125 @@ __device__ __forceinline__ void staged_issue(float4* buf, const float* x, long l
     bulk_load(buf, x + r * cols, bytes, bar);
 }
 
+// The warp's selection state while it sweeps a row: its list of the best 32 so far (one entry
+// per lane, sorted), the bar (the list's k-th entry), the floor, and two candidate buffers.
+// The coarse one holds float4 groups of the row (by index: the row is still in shared memory)
+// whose largest entry can still reach the top k; their entries are then tested one by one, and
+// the few that pass go to the fine buffer, which is merged into the list 32 at a time.
+struct Sweep {
+    int* cu;    // [kCoarseCap] groups (float4 index in the row)
+    float* fv;  // [kFineCap] entries: value
+    int* fc;    //             and column
+    float floor;
+    float lv = -INFINITY, bar_v = -INFINITY;
+    int lc = INT_MAX, bar_c = INT_MAX;
+    int n = 0, nf = 0;  // entries of the two buffers (the same in every lane)
+    float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // lane sums, 4 chains
+};
+
+// Tests the coarse buffer's groups, 8 at a time (32 entries, one per lane), entry by entry
+// against the floor and the bar; the entries that pass go to the fine buffer, which is merged
+// into the list whenever it holds 32.  Without `all`, only whole batches of 8 groups are taken
+// and the rest moves to the front; with `all`, every group is taken.
+__device__ __forceinline__ void sweep_flush(const float* __restrict__ rowf, Sweep& S, int k,
+                                            bool all) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    __syncwarp();
+    const int lim = all ? S.n : (S.n & ~7);
+    int base = 0;
+    for (; base < lim; base += 8) {
+        const int g = base + (lane >> 2);
+        float v = -INFINITY;
+        int c = INT_MAX;
+        if (g < S.n) {
+            c = 4 * S.cu[g] + (lane & 3);
+            v = rowf[c];
+        }
+        const bool keep = g < S.n && v >= S.floor && before(v, c, S.bar_v, S.bar_c);
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+            const int pos = S.nf + __popc(bal & lt);
+            S.fv[pos] = v;
+            S.fc[pos] = c;
+        }
+        S.nf += __popc(bal);
+        if (S.nf >= 32) {
+            __syncwarp();
+            merge_batch(S.lv, S.lc, S.fv[lane], S.fc[lane]);
+            const int rem = S.nf - 32;
+            float tv = 0.f;
+            int tc = 0;
+            if (lane < rem) {
+                tv = S.fv[32 + lane];
+                tc = S.fc[32 + lane];
+            }
+            __syncwarp();
+            if (lane < rem) {
+                S.fv[lane] = tv;
+                S.fc[lane] = tc;
+            }
+            __syncwarp();
+            S.nf = rem;
+            S.bar_v = __shfl_sync(0xffffffffu, S.lv, k - 1);
+            S.bar_c = __shfl_sync(0xffffffffu, S.lc, k - 1);
+        }
+    }
+    const int rem = all ? 0 : S.n - base;  // fewer than 8 groups
+    int tu = 0;
+    if (lane < rem) tu = S.cu[base + lane];
+    __syncwarp();
+    if (lane < rem) S.cu[lane] = tu;
+    __syncwarp();
+    S.n = rem;
+}
+
+// One step of the second sweep: four float4 per lane from u0 (bounds-checked if CHECK).  The
+// lane sums take exp2((x - m) * log2e): x - m first, so that the largest terms keep full
+// relative accuracy whatever the size of m.
+template <bool CHECK>
+__device__ __forceinline__ void sweep_step(const float4* __restrict__ s4, int n4, int u0,
+                                           float2 c2, float2 nmu, Sweep& S, int k) {
+    const int lane = threadIdx.x & 31;
+    float4 q[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int u = u0 + 32 * a + lane;
+        q[a] = (!CHECK || u < n4) ? s4[u]
+                                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const float2 t0 = fmul2(fadd2(make_float2(q[a].x, q[a].y), nmu), c2);
+        const float2 t1 = fmul2(fadd2(make_float2(q[a].z, q[a].w), nmu), c2);
+        S.acc[(2 * a) & 3] = fadd2(S.acc[(2 * a) & 3], make_float2(ex2a(t0.x), ex2a(t0.y)));
+        S.acc[(2 * a + 1) & 3] =
+            fadd2(S.acc[(2 * a + 1) & 3], make_float2(ex2a(t1.x), ex2a(t1.y)));
+    }
+    const float thr = fmaxf(S.floor, S.bar_v);
+    float m4[4];
+    bool p[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        m4[a] = max4(q[a]);
+        p[a] = (!CHECK || u0 + 32 * a + lane < n4) && m4[a] >= thr;
+    }
+    if (__any_sync(0xffffffffu, p[0] || p[1] || p[2] || p[3])) {
+        const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int u = u0 + 32 * a + lane;
+            // a group whose largest entry only equals the bar can beat it only with a smaller
+            // column (ties at the floor, below any bar, all enter)
+            const bool in = p[a] && (m4[a] > thr || thr > S.bar_v || 4 * u < S.bar_c);
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            if (in) S.cu[S.n + __popc(bal & lt)] = u;
+            S.n += __popc(bal);
+        }
+        if (S.n >= 8) sweep_flush(reinterpret_cast<const float*>(s4), S, k, false);
+    }
+}
+
 // The staged kernel.  Warp w of CTA c takes rows c * kStagedWarps + w, then that plus the
 // number of warps in the grid, and so on; `ring` buffers of `pitch4` float4 per warp, then a
 // candidate buffer per warp.  Every wait is bounded: a warp that gives up records
@@ -439,13 +562,12 @@ __global__ void __launch_bounds__(kStagedWarps * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row_f4 = static_cast<long long>(ring) * pitch4;  // per warp
     float4* buf = staged_smem + warp * row_f4;
-    float* cv = reinterpret_cast<float*>(staged_smem + kStagedWarps * row_f4) + warp * 2 * kCandCap;
-    int* cc = reinterpret_cast<int*>(cv + kCandCap);
+    uint8_t* cand = reinterpret_cast<uint8_t*>(staged_smem + kStagedWarps * row_f4) +
+                    warp * kCandBytes;
     uint64_t* bar = bars[warp];
     const long long tw = static_cast<long long>(gridDim.x) * kStagedWarps;
     const long long r0 = static_cast<long long>(blockIdx.x) * kStagedWarps + warp;
     const int n4 = cols >> 2;
-    const unsigned lt_mask = (1u << lane) - 1u;
     if (lane == 0) {
         for (int b = 0; b < ring; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
@@ -480,72 +602,19 @@ __global__ void __launch_bounds__(kStagedWarps * 32)
         const float sorted = warp_sorted_desc(fmaxf(fmaxf(ma, mb), fmaxf(mc, md)));
         const float m = __shfl_sync(0xffffffffu, sorted, 0);
         const float floor = __shfl_sync(0xffffffffu, sorted, k - 1);
-        // Sweep 2: every lane runs the same iterations, two float4 per lane per step.
+        // Sweep 2: every lane runs the same steps (the list lives across lanes).
         const float mu = m == -INFINITY ? 0.f : m;  // a row of -inf: every term exp(-inf) = 0
-        const float2 nmu = make_float2(-mu, -mu);
+        Sweep S;
+        S.cu = reinterpret_cast<int*>(cand);
+        S.fv = reinterpret_cast<float*>(cand + kCoarseCap * 4);
+        S.fc = reinterpret_cast<int*>(cand + kCoarseCap * 4 + kFineCap * 4);
+        S.floor = floor;
         const float2 c2 = make_float2(kLog2e, kLog2e);
-        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
-        const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        float lv = -INFINITY, bar_v = -INFINITY;  // list entry of this lane; the k-th entry
-        int lc = INT_MAX, bar_c = INT_MAX;
-        int n = 0;  // entries in the candidate buffer (the same in every lane)
-        for (int u0 = 0; u0 < n4; u0 += 64) {
-            const int ua = u0 + lane, ub = u0 + 32 + lane;
-            const float4 qa = ua < n4 ? s4[ua] : ninf;
-            const float4 qb = ub < n4 ? s4[ub] : ninf;
-            // x - m first, then the scale: the largest terms keep full relative accuracy
-            float2 ta = fmul2(fadd2(make_float2(qa.x, qa.y), nmu), c2);
-            float2 tb = fmul2(fadd2(make_float2(qa.z, qa.w), nmu), c2);
-            la = fadd2(la, make_float2(ex2a(ta.x), ex2a(ta.y)));
-            lb = fadd2(lb, make_float2(ex2a(tb.x), ex2a(tb.y)));
-            ta = fmul2(fadd2(make_float2(qb.x, qb.y), nmu), c2);
-            tb = fmul2(fadd2(make_float2(qb.z, qb.w), nmu), c2);
-            la = fadd2(la, make_float2(ex2a(ta.x), ex2a(ta.y)));
-            lb = fadd2(lb, make_float2(ex2a(tb.x), ex2a(tb.y)));
-            // quick test per float4, the exact one per entry only where it passes
-            const float thr = fmaxf(floor, bar_v);
-            const bool pa = ua < n4 && max4(qa) >= thr;
-            const bool pb = ub < n4 && max4(qb) >= thr;
-            if (__any_sync(0xffffffffu, pa || pb)) {
-                const float v[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int col = (e < 4 ? 4 * ua : 4 * ub) + (e & 3);
-                    const bool cand = (e < 4 ? pa : pb) && v[e] >= floor &&
-                                      before(v[e], col, bar_v, bar_c);
-                    const unsigned bal = __ballot_sync(0xffffffffu, cand);
-                    if (cand) {
-                        const int pos = n + __popc(bal & lt_mask);
-                        cv[pos] = v[e];
-                        cc[pos] = col;
-                    }
-                    n += __popc(bal);
-                }
-                if (n >= 32) {
-                    __syncwarp();
-                    int base = 0;
-                    for (; n - base >= 32; base += 32)
-                        merge_batch(lv, lc, cv[base + lane], cc[base + lane]);
-                    // the rest (fewer than 32) moves to the front
-                    const int rem = n - base;
-                    float tv = 0.f;
-                    int tc = 0;
-                    if (lane < rem) {
-                        tv = cv[base + lane];
-                        tc = cc[base + lane];
-                    }
-                    __syncwarp();
-                    if (lane < rem) {
-                        cv[lane] = tv;
-                        cc[lane] = tc;
-                    }
-                    __syncwarp();
-                    n = rem;
-                    bar_v = __shfl_sync(0xffffffffu, lv, k - 1);
-                    bar_c = __shfl_sync(0xffffffffu, lc, k - 1);
-                }
-            }
-        }
+        const float2 nmu = make_float2(-mu, -mu);
+        int u0 = 0;
+        for (; u0 + 128 <= n4; u0 += 128) sweep_step<false>(s4, n4, u0, c2, nmu, S, k);
+        if (u0 < n4) sweep_step<true>(s4, n4, u0, c2, nmu, S, k);
+        if (S.n > 0) sweep_flush(reinterpret_cast<const float*>(s4), S, k, true);
         // Every lane has read buffer b: it may take row r + ring * tw.  The generic-proxy
         // reads are ordered before the bulk copy's writes by the fence.
         __syncwarp();
@@ -553,17 +622,18 @@ __global__ void __launch_bounds__(kStagedWarps * 32)
             fence_proxy_async_smem();
             staged_issue(buf + b * pitch4, x, r + ring * tw, cols, &bar[b]);
         }
-        if (n > 0) {
-            const bool has = lane < n;
-            merge_batch(lv, lc, has ? cv[lane] : -INFINITY, has ? cc[lane] : INT_MAX);
+        if (S.nf > 0) {
+            const bool has = lane < S.nf;
+            merge_batch(S.lv, S.lc, has ? S.fv[lane] : -INFINITY, has ? S.fc[lane] : INT_MAX);
         }
-        float l = (la.x + la.y) + (lb.x + lb.y);
+        float l = (S.acc[0].x + S.acc[0].y) + (S.acc[1].x + S.acc[1].y) +
+                  ((S.acc[2].x + S.acc[2].y) + (S.acc[3].x + S.acc[3].y));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
         if (lse && lane == 0) lse[r] = m + logf(l);
         if (lane < k) {
-            vals[r * k + lane] = ex2a((lv - mu) * kLog2e) * (l > 0.f ? 1.f / l : 0.f);
-            idx[r * k + lane] = lc;
+            vals[r * k + lane] = ex2a((S.lv - mu) * kLog2e) * (l > 0.f ? 1.f / l : 0.f);
+            idx[r * k + lane] = S.lc;
         }
     }
 }
@@ -656,8 +726,8 @@ int sm_count() {
     return n;
 }
 
-// The staged kernel: up to four CTAs of four warps per SM, each warp with one to kStagedMaxRing
-// row buffers.
+// The staged kernel: CTAs of four warps, each warp with one to kStagedMaxRing row buffers, as
+// many CTAs per SM as fit.
 int launch_staged(const float* x, long long rows, int cols, int k, float* vals, int* idx,
                   float* lse, cudaStream_t stream) {
     constexpr int kSmemCap = 100 * 1024;  // above any request below
@@ -672,13 +742,16 @@ int launch_staged(const float* x, long long rows, int cols, int k, float* vals, 
     if (!status) return FA_ERR_CUDA;
     const int pitch4 = ((cols >> 2) + 7) & ~7;  // float4 per buffer: 128-byte multiples
     const int buf_bytes = pitch4 * 16;
-    // About 18 KB of row buffers per warp (one buffer for the longest rows), so that three or
-    // four CTAs (12-16 warps) fit on an SM.
-    int ring = 18 * 1024 / buf_bytes;
+    // Row buffers: as many (up to kStagedMaxRing) as leave room for four CTAs (16 warps) per SM
+    // in 228 KB; at least one (the longest rows: three CTAs).
+    int ring = (228 * 1024 / 16 - kCandBytes - 512) / buf_bytes;
     ring = ring < 1 ? 1 : (ring > kStagedMaxRing ? kStagedMaxRing : ring);
-    const int smem = kStagedWarps * (ring * buf_bytes + 2 * kCandCap * 4);
-    long long per_sm = (227 * 1024) / (smem + 1152);
-    per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+    const int smem = kStagedWarps * (ring * buf_bytes + kCandBytes);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_staged_rows,
+                                                      kStagedWarps * 32, smem) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (per_sm < 1) per_sm = 1;
     const long long sms = sm_count() > 0 ? sm_count() : 148;
     long long grid = (rows + kStagedWarps - 1) / kStagedWarps;
     if (grid > sms * per_sm) grid = sms * per_sm;
