@@ -443,6 +443,7 @@ struct Sweep {
     float lv = -INFINITY, bar_v = -INFINITY;
     int lc = INT_MAX, bar_c = INT_MAX;
     int n = 0, nf = 0;  // entries of the two buffers (the same in every lane)
+    int col0 = 0;       // column of the staged segment's first entry
     float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // lane sums, 4 chains
 };
 
@@ -462,8 +463,9 @@ __device__ __forceinline__ void sweep_flush(const float* __restrict__ rowf, Swee
         float v = -INFINITY;
         int c = INT_MAX;
         if (g < S.n) {
-            c = 4 * S.cu[g] + (lane & 3);
-            v = rowf[c];
+            const int cr = 4 * S.cu[g] + (lane & 3);  // within the segment
+            v = rowf[cr];
+            c = S.col0 + cr;
         }
         const bool keep = g < S.n && v >= S.floor && before(v, c, S.bar_v, S.bar_c);
         const unsigned bal = __ballot_sync(0xffffffffu, keep);
@@ -540,13 +542,76 @@ __device__ __forceinline__ void sweep_step(const float4* __restrict__ s4, int n4
             const int u = u0 + 32 * a + lane;
             // a group whose largest entry only equals the bar can beat it only with a smaller
             // column (ties at the floor, below any bar, all enter)
-            const bool in = p[a] && (m4[a] > thr || thr > S.bar_v || 4 * u < S.bar_c);
+            const bool in = p[a] && (m4[a] > thr || thr > S.bar_v || S.col0 + 4 * u < S.bar_c);
             const unsigned bal = __ballot_sync(0xffffffffu, in);
             if (in) S.cu[S.n + __popc(bal & lt)] = u;
             S.n += __popc(bal);
         }
         if (S.n >= 8) sweep_flush(reinterpret_cast<const float*>(s4), S, k, false);
     }
+}
+
+// One staged segment of a row (n4 float4 in shared memory) enters the warp's state: sweep 1
+// (the lane maxima, sorted across the warp: the segment's max, and its floor, which raises
+// the running floor), the running max m, with the lane sums rescaled by exp(m_old - m_new)
+// when it grows (the online recurrence of "The idea"), then sweep 2.  The segment's coarse
+// candidates are all tested before it returns, so that its buffer can take the next copy.
+__device__ __forceinline__ void sweep_segment(const float4* __restrict__ s4, int n4, int k,
+                                              Sweep& S, float& m) {
+    const int lane = threadIdx.x & 31;
+    float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+    int u = lane;
+    for (; u + 96 < n4; u += 128) {
+        ma = fmaxf(ma, max4(s4[u]));
+        mb = fmaxf(mb, max4(s4[u + 32]));
+        mc = fmaxf(mc, max4(s4[u + 64]));
+        md = fmaxf(md, max4(s4[u + 96]));
+    }
+    for (; u < n4; u += 32) ma = fmaxf(ma, max4(s4[u]));
+    const float sorted = warp_sorted_desc(fmaxf(fmaxf(ma, mb), fmaxf(mc, md)));
+    S.floor = fmaxf(S.floor, __shfl_sync(0xffffffffu, sorted, k - 1));
+    const float m_new = fmaxf(m, __shfl_sync(0xffffffffu, sorted, 0));
+    if (m != -INFINITY && m_new != m) {  // the same in every lane
+        const float f = ex2a((m - m_new) * kLog2e);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) S.acc[a] = fmul2(S.acc[a], make_float2(f, f));
+    }
+    m = m_new;
+    // Sweep 2: every lane runs the same steps (the list lives across lanes).
+    const float mu = m == -INFINITY ? 0.f : m;  // nothing finite yet: every term exp(-inf) = 0
+    const float2 c2 = make_float2(kLog2e, kLog2e);
+    const float2 nmu = make_float2(-mu, -mu);
+    int u0 = 0;
+    for (; u0 + 128 <= n4; u0 += 128) sweep_step<false>(s4, n4, u0, c2, nmu, S, k);
+    if (u0 < n4) sweep_step<true>(s4, n4, u0, c2, nmu, S, k);
+    if (S.n > 0) sweep_flush(reinterpret_cast<const float*>(s4), S, k, true);
+}
+
+// The list after the last segment: the fine buffer's rest merged in.
+__device__ __forceinline__ void sweep_finish(Sweep& S) {
+    const int lane = threadIdx.x & 31;
+    if (S.nf > 0) {
+        __syncwarp();
+        const bool has = lane < S.nf;
+        merge_batch(S.lv, S.lc, has ? S.fv[lane] : -INFINITY, has ? S.fc[lane] : INT_MAX);
+        S.nf = 0;
+    }
+}
+
+// The warp's sum of exp(x - m) over everything it swept (the same in every lane).
+__device__ __forceinline__ float sweep_sum(const Sweep& S) {
+    float l = (S.acc[0].x + S.acc[0].y) + (S.acc[1].x + S.acc[1].y) +
+              ((S.acc[2].x + S.acc[2].y) + (S.acc[3].x + S.acc[3].y));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    return l;
+}
+
+// The candidate buffers of a warp in its kCandBytes of shared memory.
+__device__ __forceinline__ void sweep_bind(Sweep& S, uint8_t* cand) {
+    S.cu = reinterpret_cast<int*>(cand);
+    S.fv = reinterpret_cast<float*>(cand + kCoarseCap * 4);
+    S.fc = reinterpret_cast<int*>(cand + kCoarseCap * 4 + kFineCap * 4);
 }
 
 // The staged kernel.  Warp w of CTA c takes rows c * kStagedWarps + w, then that plus the
@@ -588,33 +653,11 @@ __global__ void __launch_bounds__(kStagedWarps * 32)
             }
             return;
         }
-        const float4* s4 = buf + b * pitch4;
-        // Sweep 1: the lane's maximum, four independent chains; sorted across the warp.
-        float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
-        int u = lane;
-        for (; u + 96 < n4; u += 128) {
-            ma = fmaxf(ma, max4(s4[u]));
-            mb = fmaxf(mb, max4(s4[u + 32]));
-            mc = fmaxf(mc, max4(s4[u + 64]));
-            md = fmaxf(md, max4(s4[u + 96]));
-        }
-        for (; u < n4; u += 32) ma = fmaxf(ma, max4(s4[u]));
-        const float sorted = warp_sorted_desc(fmaxf(fmaxf(ma, mb), fmaxf(mc, md)));
-        const float m = __shfl_sync(0xffffffffu, sorted, 0);
-        const float floor = __shfl_sync(0xffffffffu, sorted, k - 1);
-        // Sweep 2: every lane runs the same steps (the list lives across lanes).
-        const float mu = m == -INFINITY ? 0.f : m;  // a row of -inf: every term exp(-inf) = 0
         Sweep S;
-        S.cu = reinterpret_cast<int*>(cand);
-        S.fv = reinterpret_cast<float*>(cand + kCoarseCap * 4);
-        S.fc = reinterpret_cast<int*>(cand + kCoarseCap * 4 + kFineCap * 4);
-        S.floor = floor;
-        const float2 c2 = make_float2(kLog2e, kLog2e);
-        const float2 nmu = make_float2(-mu, -mu);
-        int u0 = 0;
-        for (; u0 + 128 <= n4; u0 += 128) sweep_step<false>(s4, n4, u0, c2, nmu, S, k);
-        if (u0 < n4) sweep_step<true>(s4, n4, u0, c2, nmu, S, k);
-        if (S.n > 0) sweep_flush(reinterpret_cast<const float*>(s4), S, k, true);
+        sweep_bind(S, cand);
+        S.floor = -INFINITY;
+        float m = -INFINITY;
+        sweep_segment(buf + b * pitch4, n4, k, S, m);
         // Every lane has read buffer b: it may take row r + ring * tw.  The generic-proxy
         // reads are ordered before the bulk copy's writes by the fence.
         __syncwarp();
@@ -622,19 +665,134 @@ __global__ void __launch_bounds__(kStagedWarps * 32)
             fence_proxy_async_smem();
             staged_issue(buf + b * pitch4, x, r + ring * tw, cols, &bar[b]);
         }
-        if (S.nf > 0) {
-            const bool has = lane < S.nf;
-            merge_batch(S.lv, S.lc, has ? S.fv[lane] : -INFINITY, has ? S.fc[lane] : INT_MAX);
-        }
-        float l = (S.acc[0].x + S.acc[0].y) + (S.acc[1].x + S.acc[1].y) +
-                  ((S.acc[2].x + S.acc[2].y) + (S.acc[3].x + S.acc[3].y));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        sweep_finish(S);
+        const float l = sweep_sum(S);
+        const float mu = m == -INFINITY ? 0.f : m;
         if (lse && lane == 0) lse[r] = m + logf(l);
         if (lane < k) {
             vals[r * k + lane] = ex2a((S.lv - mu) * kLog2e) * (l > 0.f ? 1.f / l : 0.f);
             idx[r * k + lane] = S.lc;
         }
+    }
+}
+
+// Rows longer than kStagedMaxCols (16-byte access, k >= 2): each row is cut into segments of
+// kSegCols columns, staged like the short rows, and the W warps of a CTA share a row: warp w
+// takes segments w, w + W, ... and carries its running floor, bar, list and (m, l) across
+// them.  At the end of the row the warps' states meet in shared memory: warp 0 merges the
+// lists (merge_batch) and the (m, l) pairs (the two-worker merge) and writes the row.  A CTA
+// takes rows blockIdx.x, blockIdx.x + gridDim.x, ...  W is chosen per launch so that the rows
+// fill the SMs in as few segment times as possible.
+constexpr int kSegCols = 4096;
+constexpr int kLongMaxWarps = 8;
+
+__global__ void __launch_bounds__(kLongMaxWarps * 32)
+    topk_staged_long(const float* __restrict__ x, long long rows, int cols, int k,
+                     float* __restrict__ vals, int* __restrict__ idx, float* __restrict__ lse,
+                     int ring, int* status, unsigned long long timeout_ns) {
+    extern __shared__ __align__(128) float4 long_smem[];
+    __shared__ uint64_t bars[kLongMaxWarps][kStagedMaxRing];
+    __shared__ float xv[2][kLongMaxWarps][32];  // [row parity][warp][list entry]
+    __shared__ int xc[2][kLongMaxWarps][32];
+    __shared__ float xm[2][kLongMaxWarps], xl[2][kLongMaxWarps];
+    constexpr int kSeg4 = kSegCols / 4;
+    const int W = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float4* buf = long_smem + static_cast<long long>(warp) * ring * kSeg4;
+    uint8_t* cand = reinterpret_cast<uint8_t*>(long_smem + static_cast<long long>(W) * ring * kSeg4) +
+                    warp * kCandBytes;
+    uint64_t* bar = bars[warp];
+    const int nseg = (cols + kSegCols - 1) / kSegCols;
+    const int spw = (nseg + W - 1) / W;  // segment slots of a warp per row (some past nseg)
+    const long long my_rows =
+        rows > blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const long long n_items = my_rows * spw;
+    // Lane 0 issues the copies: item i is segment warp + (i % spw) W of the CTA's row i / spw
+    // (no copy past the last segment); copy number c goes to buffer c % ring.
+    long long next_item = 0;
+    int issued = 0;
+    auto issue_upto = [&](int limit) {
+        while (issued < limit && next_item < n_items) {
+            const int sg = warp + static_cast<int>(next_item % spw) * W;
+            if (sg < nseg) {
+                const long long row = blockIdx.x + (next_item / spw) * gridDim.x;
+                const int c0 = sg * kSegCols;
+                const uint32_t bytes = static_cast<uint32_t>(min(kSegCols, cols - c0)) * 4u;
+                const int b = issued % ring;
+                mbar_arrive_expect_tx(&bar[b], bytes);
+                bulk_load(buf + b * kSeg4, x + row * cols + c0, bytes, &bar[b]);
+                ++issued;
+            }
+            ++next_item;
+        }
+    };
+    if (lane == 0) {
+        for (int b = 0; b < ring; ++b) mbar_init(&bar[b], 1);
+        fence_mbar_init();
+        issue_upto(ring);
+    }
+    __syncwarp();
+    int consumed = 0;   // copies this warp has waited for
+    bool dead = false;  // a wait gave up: no more waits or copies, but every barrier is kept
+    for (long long ri = 0; ri < my_rows; ++ri) {
+        const long long r = blockIdx.x + ri * gridDim.x;
+        const int par = static_cast<int>(ri & 1);
+        Sweep S;
+        sweep_bind(S, cand);
+        S.floor = -INFINITY;
+        float m = -INFINITY;
+        for (int j = 0; j < spw && !dead; ++j) {
+            const int sg = warp + j * W;
+            if (sg >= nseg) break;
+            const int b = consumed % ring;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&bar[b], (consumed / ring) & 1, timeout_ns))) {
+                if (lane == 0) atomicCAS(status, 0, FA_ERR_TIMEOUT | (41 << 8));
+                dead = true;
+                break;
+            }
+            S.col0 = sg * kSegCols;
+            sweep_segment(buf + b * kSeg4, (min(kSegCols, cols - sg * kSegCols)) >> 2, k, S, m);
+            ++consumed;
+            // every lane has read the buffer: it may take the next copy
+            __syncwarp();
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue_upto(consumed + ring);
+            }
+        }
+        sweep_finish(S);
+        const float l = sweep_sum(S);
+        xv[par][warp][lane] = S.lv;
+        xc[par][warp][lane] = S.lc;
+        if (lane == 0) {
+            xm[par][warp] = m;
+            xl[par][warp] = l;
+        }
+        // The slots of this parity were last read for row ri - 2, before warp 0 arrived here
+        // for row ri - 1, so one barrier per row keeps writers and the reader apart.
+        named_bar_sync(1, blockDim.x);
+        if (warp == 0) {
+            float M = -INFINITY;
+            for (int w = 0; w < W; ++w) M = fmaxf(M, xm[par][w]);
+            float L = 0.f;
+            for (int w = 0; w < W; ++w)
+                if (xm[par][w] != -INFINITY) L += xl[par][w] * ex2a((xm[par][w] - M) * kLog2e);
+            float lv = S.lv;
+            int lc = S.lc;
+            for (int w = 1; w < W; ++w) merge_batch(lv, lc, xv[par][w][lane], xc[par][w][lane]);
+            const float mu = M == -INFINITY ? 0.f : M;
+            if (lse && lane == 0) lse[r] = M + logf(L);
+            if (lane < k) {
+                vals[r * k + lane] = ex2a((lv - mu) * kLog2e) * (L > 0.f ? 1.f / L : 0.f);
+                idx[r * k + lane] = lc;
+            }
+        }
+    }
+    // Copies still in flight (only after a wait gave up) end before the CTA leaves.
+    if (lane == 0) {
+        const unsigned long long drain = timeout_ns > kStagedDrainNs ? timeout_ns : kStagedDrainNs;
+        for (int c = consumed; c < issued; ++c) mbar_wait(&bar[c % ring], (c / ring) & 1, drain);
     }
 }
 
@@ -760,13 +918,55 @@ int launch_staged(const float* x, long long rows, int cols, int k, float* vals, 
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// The long-row kernel: one segment buffer per warp; the CTA width W (1 to kLongMaxWarps) with
+// the fewest segment times, ceil(rows / resident CTAs) x ceil(segments / W), the narrowest on
+// ties.
+int launch_long(const float* x, long long rows, int cols, int k, float* vals, int* idx,
+                float* lse, cudaStream_t stream) {
+    constexpr int kRing = 1;
+    constexpr int kWarpBytes = kRing * kSegCols * 4 + kCandBytes;
+    static cudaError_t attr = cudaSuccess;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(topk_staged_long, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kLongMaxWarps * kWarpBytes);
+    });
+    if (attr != cudaSuccess) return FA_ERR_CUDA;
+    int* status = device_status_word();
+    if (!status) return FA_ERR_CUDA;
+    const long long sms = sm_count() > 0 ? sm_count() : 148;
+    const long long nseg = (cols + kSegCols - 1) / kSegCols;
+    int best_w = 1;
+    long long best_cost = -1, best_grid = 1;
+    for (int w = 1; w <= kLongMaxWarps; ++w) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_staged_long, w * 32,
+                                                          w * kWarpBytes) != cudaSuccess)
+            return FA_ERR_CUDA;
+        if (per_sm < 1) continue;
+        const long long slots = sms * per_sm;
+        const long long cost = ((rows + slots - 1) / slots) * ((nseg + w - 1) / w);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_w = w;
+            best_grid = rows < slots ? rows : slots;
+        }
+    }
+    if (best_cost < 0) return FA_ERR_CUDA;
+    topk_staged_long<<<static_cast<unsigned>(best_grid), best_w * 32, best_w * kWarpBytes,
+                       stream>>>(x, rows, cols, k, vals, idx, lse, kRing, status,
+                                 fa_wait_timeout_ns());
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 template <class Top>
 int launch(const float* x, long long rows, int cols, int k, float* vals, int* idx, float* lse,
            cudaStream_t stream) {
     const bool vec = (cols % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
     const long long sms = sm_count() > 0 ? sm_count() : 148;
-    if (kFiltered<Top> && vec && cols <= kStagedMaxCols)
-        return launch_staged(x, rows, cols, k, vals, idx, lse, stream);
+    if (kFiltered<Top> && vec)
+        return cols <= kStagedMaxCols ? launch_staged(x, rows, cols, k, vals, idx, lse, stream)
+                                      : launch_long(x, rows, cols, k, vals, idx, lse, stream);
     if (cols <= 4096) {
         long long grid = (rows + kWarps - 1) / kWarps;
         if (grid > sms * 8) grid = sms * 8;

@@ -40,7 +40,10 @@ CASES = [(64, 4000, 8), (33, 4001, 5), (7, 100000, 32), (100, 50, 1), (10, 4096,
          (9, 4097, 32), (5, 9000, 2), (300, 128, 4), (3, 33, 32), (2, 1, 1), (11, 262144, 12),
          # rows staged in shared memory: many rows per warp (the ring wraps), the widest row,
          # rows shorter than a warp's loads
-         (40000, 128, 3), (5000, 1024, 9), (37, 4096, 32), (129, 12, 2)]
+         (40000, 128, 3), (5000, 1024, 9), (37, 4096, 32), (129, 12, 2),
+         # long rows staged in segments shared by the warps of a CTA: a partial last segment,
+         # several rows per CTA
+         (40, 12300, 7), (2000, 4100, 16)]
 
 
 @pytest.mark.parametrize("rows,cols,k", CASES, ids=lambda x: str(x))
