@@ -447,7 +447,8 @@ NCU_TRAFFIC_BYTES = {
     "gqa_decode_b8h32kv8q1k32768d128": 1.073947e9 + 5.79328e6,
     "softmax_65536x4000": 1.048683e9 + 0.997987072e9,
     "gqa_causal_b2h32kv8n8192d128": 354.289408e6 + 99.04384e6,
-    "softmax_topk_65536x4000_k8": 1.048618e9 + 5.45408e6,
+    "softmax_topk_65536x4000_k8": 1.048666e9 + 7.303424e6,
+    "softmax_topk_512x131072_k32": 268.514816e6 + 3.573504e6,
 }
 # The backward workloads run three kernels per call; their per-kernel traffic is in the
 # bwd_kv_kernel / bwd_q_kernel summaries, and the call's roofline reports none.
