@@ -182,13 +182,33 @@ OSM_ATTN_API int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void
  *   mask_b_stride, mask_h_stride   words between the masks of consecutive sequences and heads,
  *            >= 0 and multiples of 4; 0 repeats one mask over all sequences or heads (e.g.
  *            a [Nq, W] mask shared by every head of every sequence).
- * Errors as fa_fwd_gqa, plus FA_ERR_INVALID_ARG for a NULL or misaligned mask, bad strides, or
- * a mask reaching O or LSE.
+ *   tile_map optional DEVICE workspace of tile_map_words uint32 words (at least what
+ *            fa_fwd_mask_plan returns), 4-byte aligned, owned by the caller, apart from every
+ *            input and output; NULL skips nothing.  When given, a pre-pass on the same stream
+ *            writes into it, for every 128-row query tile and mask instance, which 128-key
+ *            tiles hold an allowed key, and the attention then skips the tiles that hold none
+ *            (a block of -inf scores adds nothing, so the results are those without skipping
+ *            up to the order of the floating-point sums).  Its contents are rewritten by every
+ *            call; calls that overlap on the GPU need their own.
+ * Errors as fa_fwd_gqa, plus FA_ERR_INVALID_ARG for a NULL or misaligned mask, bad strides, a
+ * mask reaching O or LSE, or a tile map that is misaligned, too small or overlaps an input or
+ * output.
  */
 OSM_ATTN_API int fa_fwd_mask(const void* Q, const void* K, const void* V, void* O, float* LSE,
                              int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
                              float scale, int causal, const uint32_t* mask,
-                             int64_t mask_b_stride, int64_t mask_h_stride, void* stream);
+                             int64_t mask_b_stride, int64_t mask_h_stride, uint32_t* tile_map,
+                             int64_t tile_map_words, void* stream);
+
+/*
+ * fa_fwd_mask_plan -- the size of fa_fwd_mask's tile map for a shape and mask strides: one row
+ * of ceil(ceil(Nk / 128) / 32) words per 128-row query tile and mask instance (B instances
+ * when mask_b_stride != 0, times H when mask_h_stride != 0).  Host pointer; writes
+ * *tile_map_words.  FA_ERR_INVALID_ARG for negative or oversized arguments or a NULL output.
+ */
+OSM_ATTN_API int fa_fwd_mask_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                                  int64_t mask_b_stride, int64_t mask_h_stride,
+                                  int64_t* tile_map_words);
 
 /*
  * fa_bwd -- the gradients dQ, dK, dV of fa_fwd's attention for an output gradient dO.
@@ -281,7 +301,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 6
+#define OSM_ATTN_ABI_VERSION 7
 
 #ifdef __cplusplus
 }

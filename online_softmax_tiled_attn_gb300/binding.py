@@ -65,8 +65,10 @@ def lib() -> ctypes.CDLL:
             L.osm_softmax.argtypes = [vp, vp, i64, i64, vp, vp]
             L.osm_softmax.restype = ctypes.c_int
             L.fa_fwd_mask.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
-                                      ctypes.c_float, ctypes.c_int, vp, i64, i64, vp]
+                                      ctypes.c_float, ctypes.c_int, vp, i64, i64, vp, i64, vp]
             L.fa_fwd_mask.restype = ctypes.c_int
+            L.fa_fwd_mask_plan.argtypes = [i64, i64, i64, i64, i64, i64, i64p]
+            L.fa_fwd_mask_plan.restype = ctypes.c_int
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                  ctypes.c_float, ctypes.c_int, vp]
             L.fa_bwd.restype = ctypes.c_int
@@ -152,10 +154,20 @@ def osm_softmax_raw(x_ptr, y_ptr, rows, cols, lse_ptr, stream_ptr):
 
 
 def fa_fwd_mask_raw(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, mask, mask_b_stride,
-                    mask_h_stride, stream_ptr):
+                    mask_h_stride, tile_map, tile_map_words, stream_ptr):
     return lib().fa_fwd_mask(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d),
                              float(scale), int(bool(causal)), mask, int(mask_b_stride),
-                             int(mask_h_stride), stream_ptr)
+                             int(mask_h_stride), tile_map, int(tile_map_words), stream_ptr)
+
+
+def mask_plan(B, H, Nq, Nk, mask_b_stride, mask_h_stride):
+    """Words of fa_fwd_mask's tile map for this shape and these mask strides."""
+    w = ctypes.c_int64(0)
+    rc = lib().fa_fwd_mask_plan(int(B), int(H), int(Nq), int(Nk), int(mask_b_stride),
+                                int(mask_h_stride), ctypes.byref(w))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_mask_plan")
+    return w.value
 
 
 def fa_bwd_raw(q, k, v, o, do, lse, dq, dk, dv, ws_d, B, H, N, d, scale, causal, stream_ptr):
@@ -392,10 +404,13 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, workspace=None, stream
     return dq, dk, dv
 
 
-def fa_fwd_mask(q, k, v, mask_bits, scale=None, causal=False, out=None, lse=None, stream=None):
+def fa_fwd_mask(q, k, v, mask_bits, scale=None, causal=False, out=None, lse=None, stream=None,
+                skip_tiles=True, tile_map=None):
     """Attention of q [B,H,Nq,d] over k, v [B,H,Nk,d] (CUDA bf16) with an explicit mask:
     mask_bits is the CUDA uint32/int32 tensor [B or 1, H or 1, Nq, 4 * ceil(Nk / 128)] that
-    inputs.pack_mask builds (size-1 leading dimensions repeat).  Returns (O, LSE)."""
+    inputs.pack_mask builds (size-1 leading dimensions repeat).  skip_tiles: pass a tile map
+    (tile_map, a CUDA int32 tensor of at least mask_plan words, or one made here) so that key
+    tiles with no allowed key are skipped.  Returns (O, LSE)."""
     import torch
 
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -419,9 +434,19 @@ def fa_fwd_mask(q, k, v, mask_bits, scale=None, causal=False, out=None, lse=None
         scale = 1.0 / math.sqrt(d)
     O = torch.empty_like(q) if out is None else out
     L = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    tm_ptr, tm_words = 0, 0
+    if skip_tiles:
+        need = mask_plan(B, H, Nq, Nk, bs, hs)
+        if tile_map is None:
+            tile_map = torch.empty(max(need, 1), dtype=torch.int32, device=q.device)
+        if (not isinstance(tile_map, torch.Tensor) or not tile_map.is_cuda
+                or tile_map.dtype not in (torch.int32, torch.uint32)
+                or not tile_map.is_contiguous() or tile_map.numel() < need):
+            raise TypeError(f"tile_map must be a contiguous CUDA int32 tensor of >= {need} words")
+        tm_ptr, tm_words = tile_map.data_ptr(), tile_map.numel()
     rc = fa_fwd_mask_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), L.data_ptr(),
                          B, H, Nq, Nk, d, scale, causal, mask_bits.data_ptr(), bs, hs,
-                         _stream_handle(stream))
+                         tm_ptr, tm_words, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_mask")
     return O, L

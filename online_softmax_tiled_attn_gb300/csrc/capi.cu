@@ -33,7 +33,8 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
                    int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d, float scale,
                    int causal, const int32_t* kv_lens, int64_t n_splits, float* ws_O,
                    float* ws_LSE, void* stream, const uint32_t* mask = nullptr,
-                   int64_t mask_bs = 0, int64_t mask_hs = 0) {
+                   int64_t mask_bs = 0, int64_t mask_hs = 0, uint32_t* tile_map = nullptr,
+                   int64_t tile_map_words = 0) {
     if (B < 0 || H < 0 || H_kv < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
     if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
     int64_t bh, rows, q_elems, bh_kv, kv_rows, kv_elems;
@@ -79,6 +80,23 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
         if (overlaps(mask, static_cast<uint64_t>(ext), O, q_bytes) ||
             (LSE && overlaps(mask, static_cast<uint64_t>(ext), LSE, lse_bytes)))
             return FA_ERR_INVALID_ARG;
+        if (tile_map) {
+            // written by the pre-pass, then read by the attention: apart from every input
+            // and output
+            const int64_t need = osm::mask_tile_map_words(B, H, Nq, Nk, mask_bs, mask_hs);
+            if (!aligned(tile_map, 4) || need < 0 || tile_map_words < need ||
+                need > INT64_MAX / 8)
+                return FA_ERR_INVALID_ARG;
+            const uint64_t tm_bytes = static_cast<uint64_t>(need) * 4;
+            const void* other[6] = {Q, K, V, O, LSE, mask};
+            const uint64_t other_bytes[6] = {q_bytes, kv_bytes, kv_bytes, q_bytes,
+                                             LSE ? lse_bytes : 0, static_cast<uint64_t>(ext)};
+            for (int i = 0; i < 6; ++i)
+                if (overlaps(tile_map, tm_bytes, other[i], other_bytes[i]))
+                    return FA_ERR_INVALID_ARG;
+        }
+    } else if (tile_map) {
+        return FA_ERR_INVALID_ARG;
     }
     const uint64_t len_bytes = static_cast<uint64_t>(B) * 4;
     if (kv_lens && (!aligned(kv_lens, 4) || overlaps(kv_lens, len_bytes, O, q_bytes) ||
@@ -105,7 +123,8 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
             return FA_ERR_INVALID_ARG;
     }
     return osm::fa_fwd_splitkv_launch(
-        Q, K, V, O, LSE, osm::AttnShape{B, H, H_kv, Nq, Nk, d, kv_lens, 0, mask, mask_bs, mask_hs},
+        Q, K, V, O, LSE,
+        osm::AttnShape{B, H, H_kv, Nq, Nk, d, kv_lens, 0, mask, mask_bs, mask_hs, tile_map},
         scale, causal != 0, n_splits, ws_O, ws_LSE, st);
 }
 
@@ -202,10 +221,23 @@ int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
 int fa_fwd_mask(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                 int64_t H, int64_t Nq, int64_t Nk, int64_t d, float scale, int causal,
                 const uint32_t* mask, int64_t mask_b_stride, int64_t mask_h_stride,
-                void* stream) {
+                uint32_t* tile_map, int64_t tile_map_words, void* stream) {
     if (!mask) return FA_ERR_INVALID_ARG;
     return attention_call(Q, K, V, O, LSE, B, H, H, Nq, Nk, d, scale, causal, nullptr, 1,
-                          nullptr, nullptr, stream, mask, mask_b_stride, mask_h_stride);
+                          nullptr, nullptr, stream, mask, mask_b_stride, mask_h_stride,
+                          tile_map, tile_map_words);
+}
+
+int fa_fwd_mask_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t mask_b_stride,
+                     int64_t mask_h_stride, int64_t* tile_map_words) {
+    if (!tile_map_words || B < 0 || H < 0 || Nq < 0 || Nk < 0 || mask_b_stride < 0 ||
+        mask_h_stride < 0 || Nq > (1LL << 30) || Nk > (1LL << 30) || B > (1LL << 30) ||
+        H > (1LL << 30))
+        return FA_ERR_INVALID_ARG;
+    int64_t words = osm::mask_tile_map_words(B, H, Nq, Nk, mask_b_stride, mask_h_stride);
+    if (words < 0) return FA_ERR_INVALID_ARG;
+    *tile_map_words = words;
+    return FA_OK;
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,

@@ -105,6 +105,9 @@ struct Bars {
     uint64_t mma_done;
     uint64_t mma_pv_done;
     uint32_t tmem_base;
+    // MASK: the key tile in V ring slot s, written by the V producer before its arrival on
+    // v_full[s] (ordered by that barrier for the softmax, which reads it after the wait).
+    int v_kt[kMaxStages];
     float mref[2][kBM];                // reference max of tile J for tile J+1: [J & 1][row]
     float fin[kFinSlots][2][2][kBM];   // [item slot][group][m, l][row]
 };
@@ -116,7 +119,9 @@ struct Cfg {
     static constexpr int kStages = D == 128 ? 3 : 6;         // K ring and V ring depth
     static constexpr int kK = 0;
     static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kBars = kV + kStages * kTileBytes;
+    static constexpr int kMsk = kV + kStages * kTileBytes;  // MASK: a key tile's mask bits
+    static constexpr int kMskBytes = kBM * 16;              // 128 query rows x 16 bytes
+    static constexpr int kBars = kMsk + kStages * kMskBytes;
     static constexpr int kBytes = kBars + static_cast<int>(sizeof(Bars));
     static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
     static constexpr int kP = D == 64 ? 2 : 1;      // P buffers
@@ -182,6 +187,12 @@ struct FaParams {
     const uint32_t* mask;
     long long mask_bs, mask_hs;
     int mask_words;
+    // Optional tile map of the mask (MASK only), or nullptr: bit kt % 32 of word kt / 32 of
+    // the row at tile_map + (inst * n_qtiles + q_tile) * tmap_words is 0 when no key of key
+    // tile kt is allowed for any query of the query tile; such tiles are skipped.  inst is the
+    // mask's instance: b and h of the query head where the mask strides are nonzero.
+    const uint32_t* tile_map;
+    int tmap_words;
     float scale_log2;
     unsigned long long timeout_ns;
 };
@@ -190,13 +201,28 @@ struct FaParams {
 // [kt0, kt0 + n_kv) of key/value head kvh, which holds kv_len valid keys.
 struct Item {
     int q_tile, bh, split, kt0, n_kv, kvh, kv_len;
+    // MASK with a tile map that leaves some tile out: the item visits only the allowed tiles
+    // of [kt0, kt_end), n_kv of them; tm is the query tile's row of the map, and tm_bits holds
+    // the allowed tiles of its word tm_word not visited yet.  Otherwise (tm == nullptr) tiles
+    // kt0 .. kt0 + n_kv - 1.
+    const uint32_t* tm;
+    int kt_end, tm_word;
+    uint32_t tm_bits;
 };
+
+// Word wi of an item's tile-map row, without the tiles outside [kt0, kt_end).
+__device__ __forceinline__ uint32_t map_word(const Item& w, int wi) {
+    uint32_t bits = w.tm[wi];
+    if (wi == (w.kt0 >> 5)) bits &= ~0u << (w.kt0 & 31);
+    if (wi == ((w.kt_end - 1) >> 5) && (w.kt_end & 31)) bits &= ~(~0u << (w.kt_end & 31));
+    return bits;
+}
 
 // Work item idx of the launch.  Non-causal items go head by head, so the CTAs running at one
 // time share the K and V of a few heads.  Causal items go in groups of head_group heads (as
 // many as keep their K and V in L2 together), and within a group the longest rows (highest
 // query tiles) first, so that the CTAs' shares even out.
-template <bool CAUSAL>
+template <bool CAUSAL, bool TMAP = false>
 __device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
     Item w;
     if (CAUSAL) {
@@ -241,8 +267,55 @@ __device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
         kt1 = min(static_cast<long long>(kt1), last_key < 0 ? 0 : last_key / kBN + 1);
     }
     w.n_kv = max(0, kt1 - w.kt0);
+    w.tm = nullptr;
+    w.kt_end = w.kt0 + w.n_kv;
+    w.tm_word = -1;
+    w.tm_bits = 0u;
+    if (TMAP && prm.tile_map != nullptr && w.n_kv > 0) {
+        const int b = w.bh / prm.H, h = w.bh - (w.bh / prm.H) * prm.H;
+        const int inst = (prm.mask_bs != 0 ? b : 0) * (prm.mask_hs != 0 ? prm.H : 1) +
+                         (prm.mask_hs != 0 ? h : 0);
+        w.tm = prm.tile_map + (static_cast<long long>(inst) * prm.n_qtiles + w.q_tile) *
+                                  prm.tmap_words;
+        int n = 0;
+        for (int wi = w.kt0 >> 5; wi <= (w.kt_end - 1) >> 5; ++wi) {
+            const uint32_t bits = map_word(w, wi);
+            if (wi == (w.kt0 >> 5)) {
+                w.tm_word = wi;
+                w.tm_bits = bits;
+            }
+            n += __popc(bits);
+        }
+        if (n == w.n_kv) w.tm = nullptr;  // every tile allowed: visit them in a row
+        w.n_kv = n;
+    }
     return w;
 }
+
+// The key tiles an item visits, in order: next() hands out the next one.  With a tile map
+// (tm != nullptr) the allowed tiles are taken one by one from the word in hand, and the map is
+// read again only when that word is used up (kt_end means none is left; callers visit exactly
+// n_kv tiles); otherwise the tiles follow one another from kt0.
+struct TileCursor {
+    const uint32_t* tm;
+    int kt, kt_end, word;  // kt: the tile handed out last
+    uint32_t bits;         // allowed tiles of word `word` not handed out yet
+
+    __device__ __forceinline__ explicit TileCursor(const Item& w)
+        : tm(w.tm), kt(w.kt0 - 1), kt_end(w.kt_end), word(w.tm_word), bits(w.tm_bits) {}
+
+    __device__ __forceinline__ int next() {
+        if (tm == nullptr) return ++kt;
+        while (bits == 0u) {
+            if (++word > ((kt_end - 1) >> 5)) return kt = kt_end;
+            bits = tm[word];  // a word past the first: only the end of the range cuts it
+            if (word == ((kt_end - 1) >> 5) && (kt_end & 31)) bits &= ~(~0u << (kt_end & 31));
+        }
+        kt = (word << 5) + __ffs(bits) - 1;
+        bits &= bits - 1u;
+        return kt;
+    }
+};
 
 // The k-th work item of this CTA, or -1 past the end.  Items are dealt out in rounds of
 // gridDim.x, alternately forwards and backwards (CTA c takes item c of round 0, item G-1-c of
@@ -265,12 +338,13 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int stages, int issue
     }
 }
 
-// MASK: an explicit mask is read (prm.mask); a separate instantiation, so that the unmasked
-// kernels' code is unchanged.
-template <int D, bool CAUSAL, bool SPLIT, bool MASK = false>
+// MASK: 1 = an explicit mask is read (prm.mask), 2 = the same with the mask's tile map
+// (prm.tile_map); separate instantiations, so that the unmasked kernels' code is unchanged.
+template <int D, bool CAUSAL, bool SPLIT, int MASK = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FaParams prm) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM,
+                  const FaParams prm) {
     using C = Cfg<D>;
     constexpr int S_ = C::kStages;
     const int Nq = prm.Nq, Nk = prm.Nk;
@@ -336,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0;; ++k) {
             const int idx = cta_item(k, prm.n_items);
             if (idx < 0) break;
-            const Item w = decode_item<CAUSAL>(idx, prm);
+            const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
             const int slot = k % kFinSlots;
             if (!warp_wait(&bars->fin_full[slot], (k / kFinSlots) & 1, timeout_ns, true)) {
                 record_timeout(12);
@@ -421,14 +495,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tmQ);
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
+                if (MASK) tma_prefetch_desc(&tmM);
                 constexpr uint32_t kTx = C::kTileBytes;
                 int e = 0;  // K-ring entries issued
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
                     if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL>(idx, prm);
-                    // t = -1: the item's Q tile, then its key tiles.
+                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
+                    // t = -1: the item's Q tile, then its key tiles (key tile kt).
+                    TileCursor tiles(w);
+                    int kt = tiles.next();
                     for (int t = w.n_kv > 0 ? -1 : 0; t < w.n_kv; ++t, ++e) {
                         const int s = e % S_;
                         if (e >= S_ &&
@@ -439,11 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         mbar_arrive_expect_tx(&bars->k_full[s], kTx);
                         const CUtensorMap* map = t < 0 ? &tmQ : &tmK;
-                        const int row = t < 0 ? w.q_tile * kBM : (w.kt0 + t) * kBN;
+                        const int row = t < 0 ? w.q_tile * kBM : kt * kBN;
                         const int head = t < 0 ? w.bh : w.kvh;
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, map,
                                         &bars->k_full[s], h * 64, row, head);
+                        if (t >= 0) kt = tiles.next();
                     }
                 }
                 drain_ring(bars->k_full, S_, e, timeout_ns);
@@ -457,8 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
                     if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL>(idx, prm);
-                    for (int t = 0; t < w.n_kv; ++t, ++J) {
+                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
+                    TileCursor tiles(w);
+                    int kt = tiles.next();
+                    for (int t = 0; t < w.n_kv; ++t, ++J, kt = tiles.next()) {
                         const int s = J % S_;
                         if (J >= S_ &&
                             !mbar_wait(&bars->v_empty[s], ((J / S_) - 1) & 1, timeout_ns, true)) {
@@ -466,10 +546,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&bars->v_full[s], kTx);
+                        if (MASK) bars->v_kt[s] = kt;
+                        mbar_arrive_expect_tx(&bars->v_full[s],
+                                              MASK ? kTx + C::kMskBytes : kTx);
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
-                                        &bars->v_full[s], h * 64, (w.kt0 + t) * kBN, w.kvh);
+                                        &bars->v_full[s], h * 64, kt * kBN, w.kvh);
+                        if (MASK) {
+                            // The tile's mask bits for the 128 query rows ride with V: the
+                            // slot is freed only after P V, when the softmax has used them.
+                            const int b = w.bh / prm.H, h = w.bh - b * prm.H;
+                            tma_load_4d(smem + C::kMsk + s * C::kMskBytes, &tmM,
+                                        &bars->v_full[s], 4 * kt, w.q_tile * kBM,
+                                        prm.mask_hs != 0 ? h : 0, prm.mask_bs != 0 ? b : 0);
+                        }
                     }
                 }
                 drain_ring(bars->v_full, S_, J, timeout_ns);
@@ -483,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
                     if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL>(idx, prm);
+                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
                     if (w.n_kv == 0) continue;
                     // The item's Q tile: K ring -> Q buffer qb in TMEM (tcgen05.cp, ordered
                     // before the MMAs below), once the S of item qi - kQ, the buffer's
@@ -555,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
                     if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL>(idx, prm);
+                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
                     if (w.n_kv == 0) continue;
                     // The first P V of an item overwrites O: the epilogue must have read the
                     // previous item's.
@@ -608,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0;; ++k) {
             const int idx = cta_item(k, prm.n_items);
             if (idx < 0) break;
-            J_total += decode_item<CAUSAL>(idx, prm).n_kv;
+            J_total += decode_item<CAUSAL, MASK == 2>(idx, prm).n_kv;
         }
         bool ok = true;
         int J0 = 0;  // first key tile of the item
@@ -616,21 +706,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = cta_item(k, prm.n_items);
             if (idx < 0) break;
             int n, kt0, key_limit;
-            const uint4* mask_row = nullptr;  // this row's mask bits, 16 bytes per key tile
             {
-                const Item w = decode_item<CAUSAL>(idx, prm);
+                const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
                 n = w.n_kv;
                 kt0 = w.kt0;
                 const int q_row = w.q_tile * kBM + r;
                 const int pos = q_row % prm.q_pos;  // position of the row's query
                 key_limit = CAUSAL ? min(w.kv_len - 1, pos + (Nk - prm.q_pos)) : w.kv_len - 1;
-                if (MASK) {
-                    const long long b = w.bh / prm.H, h = w.bh % prm.H;
-                    const long long i = q_row < prm.Nq ? q_row : 0;  // rows past Nq: unused
-                    mask_row = reinterpret_cast<const uint4*>(prm.mask + b * prm.mask_bs +
-                                                              h * prm.mask_hs +
-                                                              i * prm.mask_words);
-                }
             }
             float m_last = -INFINITY;  // reference max this group used last (scaled, log2)
             float l = 0.f;             // this group's sum of 2^(t - m_last) over its tiles
@@ -651,7 +733,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t sr[128];
                 tmem_ld128_sync(tS, sr);
                 warp_arrive_tc(&bars->s_free[g]);  // S(J) is in registers: S(J+2) may go there
-                const int kv0 = (kt0 + t) * kBN;
+                // MASK: the key tile of visit J and the row's 128 bits of it came with V(J)
+                // into V slot J % S_ (the visits of a tile map step over empty tiles; rows
+                // past Nq read zero fill); otherwise visit t is tile kt0 + t.
+                int kt = kt0 + t;
+                uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);
+                if (MASK) {
+                    const int vs = J % S_;
+                    if (!warp_wait(&bars->v_full[vs], (J / S_) & 1, timeout_ns)) {
+                        record_timeout(17);
+                        ok = false;
+                        break;
+                    }
+                    kt = bars->v_kt[vs];
+                    mw = reinterpret_cast<const uint4*>(smem + C::kMsk + vs * C::kMskBytes)[r];
+                }
+                const int kv0 = kt * kBN;
                 if (kv0 + kBN - 1 > key_limit) {
 #pragma unroll
                     for (int e = 0; e < 128; ++e)
@@ -659,9 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (MASK) {
                     // The explicit mask: a key whose bit is 0 takes no part (score -inf).
-                    // Words of all ones or all zeros (the usual case for structured masks)
-                    // cost one test.
-                    const uint4 mw = mask_row[kt0 + t];
+                    // Words of all ones (the usual case for structured masks) cost one test.
                     const uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -849,8 +944,9 @@ int device_sm_count() {
     return n;
 }
 
-template <int D, bool CAUSAL, bool SPLIT, bool MASK = false>
+template <int D, bool CAUSAL, bool SPLIT, int MASK = 0>
 int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const CUtensorMap& tm,
                   const FaParams& prm, cudaStream_t stream) {
     using C = Cfg<D>;
     static std::once_flag once;
@@ -880,29 +976,93 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     const int sms = device_sm_count();
     const long long ctas = (sms > 0 && items > sms) ? sms : items;
     fa_fwd_kernel<D, CAUSAL, SPLIT, MASK>
-        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, p);
+        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, tm, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// The tile map of an explicit mask.  Block `blk` = inst * n_qtiles + qt covers query tile qt of
+// mask instance inst (b = inst / inst_h, h = inst % inst_h); bit kt of its row is set when some
+// query row of the tile allows some key of key tile kt.  For each word of the row (32 key
+// tiles), lane l of warp w ORs the 16-byte group of key tile 32 * word + l down rows w, w + 4,
+// ... of the tile (a warp reads 512 consecutive bytes of a row), the warps' votes meet in
+// shared memory; bits past Nk in the last key tile are not keys and are dropped.
+__global__ void __launch_bounds__(128)
+    mask_tile_map_kernel(const uint32_t* __restrict__ mask, long long mask_bs, long long mask_hs,
+                         int inst_h, int Nq, int Nk, int mask_words, int n_qtiles, int n_kt,
+                         int tmap_words, long long n_blocks, uint32_t* __restrict__ out) {
+    __shared__ uint32_t votes[4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (long long blk = blockIdx.x; blk < n_blocks; blk += gridDim.x) {
+        const int qt = static_cast<int>(blk % n_qtiles);
+        const long long inst = blk / n_qtiles;
+        const uint32_t* base = mask + (inst / inst_h) * mask_bs + (inst % inst_h) * mask_hs;
+        const int r0 = qt * kBM, r1 = min(r0 + kBM, Nq);
+        uint32_t* row_out = out + blk * tmap_words;
+        for (int wi = 0; wi < tmap_words; ++wi) {
+            const int kt = 32 * wi + lane;
+            bool any = false;
+            if (kt < n_kt) {
+                uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 8
+                for (int r = r0 + warp; r < r1; r += 4) {
+                    const uint4 v = reinterpret_cast<const uint4*>(
+                        base + static_cast<long long>(r) * mask_words)[kt];
+                    acc.x |= v.x;
+                    acc.y |= v.y;
+                    acc.z |= v.z;
+                    acc.w |= v.w;
+                }
+                const int valid = Nk - kt * kBN;  // keys of this tile below Nk
+                if (valid < kBN) {
+                    uint32_t w[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int vb = valid - 32 * c;
+                        if (vb <= 0) w[c] = 0u;
+                        else if (vb < 32) w[c] &= ~(~0u << vb);
+                    }
+                    acc = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                any = (acc.x | acc.y | acc.z | acc.w) != 0u;
+            }
+            const unsigned bal = __ballot_sync(0xffffffffu, any);
+            if (lane == 0) votes[warp] = bal;
+            __syncthreads();
+            if (threadIdx.x == 0) row_out[wi] = votes[0] | votes[1] | votes[2] | votes[3];
+            __syncthreads();
+        }
+    }
 }
 
 template <bool SPLIT>
 int launch_dispatch(int64_t d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                    const CUtensorMap& tv, const FaParams& prm, cudaStream_t stream) {
+                    const CUtensorMap& tv, const CUtensorMap& tm, const FaParams& prm,
+                    cudaStream_t stream) {
     if (prm.mask) {  // explicit masks run one pass
         if (SPLIT) return FA_ERR_UNSUPPORTED;
-        if (d == 64)
-            return causal ? launch_kernel<64, true, false, true>(tq, tk, tv, prm, stream)
-                          : launch_kernel<64, false, false, true>(tq, tk, tv, prm, stream);
-        if (d == 128)
-            return causal ? launch_kernel<128, true, false, true>(tq, tk, tv, prm, stream)
-                          : launch_kernel<128, false, false, true>(tq, tk, tv, prm, stream);
+        const bool map = prm.tile_map != nullptr;
+        if (d == 64) {
+            if (map)
+                return causal ? launch_kernel<64, true, false, 2>(tq, tk, tv, tm, prm, stream)
+                              : launch_kernel<64, false, false, 2>(tq, tk, tv, tm, prm, stream);
+            return causal ? launch_kernel<64, true, false, 1>(tq, tk, tv, tm, prm, stream)
+                          : launch_kernel<64, false, false, 1>(tq, tk, tv, tm, prm, stream);
+        }
+        if (d == 128) {
+            if (map)
+                return causal ? launch_kernel<128, true, false, 2>(tq, tk, tv, tm, prm, stream)
+                              : launch_kernel<128, false, false, 2>(tq, tk, tv, tm, prm, stream);
+            return causal ? launch_kernel<128, true, false, 1>(tq, tk, tv, tm, prm, stream)
+                          : launch_kernel<128, false, false, 1>(tq, tk, tv, tm, prm, stream);
+        }
         return FA_ERR_UNSUPPORTED;
     }
     if (d == 64)
-        return causal ? launch_kernel<64, true, SPLIT>(tq, tk, tv, prm, stream)
-                      : launch_kernel<64, false, SPLIT>(tq, tk, tv, prm, stream);
+        return causal ? launch_kernel<64, true, SPLIT>(tq, tk, tv, tm, prm, stream)
+                      : launch_kernel<64, false, SPLIT>(tq, tk, tv, tm, prm, stream);
     if (d == 128)
-        return causal ? launch_kernel<128, true, SPLIT>(tq, tk, tv, prm, stream)
-                      : launch_kernel<128, false, SPLIT>(tq, tk, tv, prm, stream);
+        return causal ? launch_kernel<128, true, SPLIT>(tq, tk, tv, tm, prm, stream)
+                      : launch_kernel<128, false, SPLIT>(tq, tk, tv, tm, prm, stream);
     return FA_ERR_UNSUPPORTED;
 }
 
@@ -933,9 +1093,26 @@ FaParams base_params(const AttnShape& sh, float scale) {
     prm.mask_words = static_cast<int>(4 * ((sh.Nk + kBN - 1) / kBN));
     prm.q_pos = static_cast<int>(sh.q_pos > 0 ? sh.q_pos : sh.Nq);
     prm.n_qtiles = static_cast<int>((sh.Nq + kBM - 1) / kBM);
+    prm.tile_map = sh.tile_map;
+    prm.tmap_words = static_cast<int>(((sh.Nk + kBN - 1) / kBN + 31) / 32);
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.timeout_ns = fa_wait_timeout_ns();
     return prm;
+}
+
+// Fills the tile map of sh.mask into sh.tile_map (stream-ordered before the attention).
+int launch_mask_tile_map(const AttnShape& sh, cudaStream_t stream) {
+    const int n_qtiles = static_cast<int>((sh.Nq + kBM - 1) / kBM);
+    const int n_kt = static_cast<int>((sh.Nk + kBN - 1) / kBN);
+    const long long inst_b = sh.mask_bs != 0 ? sh.B : 1, inst_h = sh.mask_hs != 0 ? sh.H : 1;
+    const long long n_blocks = inst_b * inst_h * n_qtiles;
+    if (n_blocks <= 0 || n_kt <= 0) return FA_OK;
+    const long long grid = n_blocks < 65535LL * 16 ? n_blocks : 65535LL * 16;
+    mask_tile_map_kernel<<<static_cast<unsigned>(grid), 128, 0, stream>>>(
+        sh.mask, sh.mask_bs, sh.mask_hs, static_cast<int>(inst_h), static_cast<int>(sh.Nq),
+        static_cast<int>(sh.Nk), static_cast<int>(4 * n_kt), n_qtiles, n_kt, (n_kt + 31) / 32,
+        n_blocks, sh.tile_map);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
@@ -960,11 +1137,35 @@ int fa_fwd_shape_launch(const void* Q, const void* K, const void* V, void* O, fl
     const int st = make_maps(Q, K, V, sh, &tq, &tk, &tv);
     if (st != FA_OK) return st;
     FaParams prm = base_params(sh, scale);
+    CUtensorMap tm{};
+    if (sh.mask) {
+        const int64_t n_kt = (sh.Nk + kBN - 1) / kBN;
+        const int rc = make_mask_tensor_map(&tm, sh.mask, 4 * n_kt, sh.Nq,
+                                            sh.mask_hs != 0 ? sh.H : 1,
+                                            sh.mask_bs != 0 ? sh.B : 1, sh.mask_hs, sh.mask_bs);
+        if (rc != FA_OK) return rc;
+    }
+    if (sh.mask && sh.tile_map) {
+        const int rc = launch_mask_tile_map(sh, stream);
+        if (rc != FA_OK) return rc;
+    } else {
+        prm.tile_map = nullptr;
+    }
     prm.O = static_cast<__nv_bfloat16*>(O);
     prm.LSE = LSE;
     prm.n_splits = 1;
     prm.tiles_per_split = static_cast<int>((sh.Nk + kBN - 1) / kBN);
-    return launch_dispatch<false>(sh.d, causal, tq, tk, tv, prm, stream);
+    return launch_dispatch<false>(sh.d, causal, tq, tk, tv, tm, prm, stream);
+}
+
+int64_t mask_tile_map_words(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t mask_bs,
+                            int64_t mask_hs) {
+    const int64_t n_qtiles = (Nq + kBM - 1) / kBM, n_kt = (Nk + kBN - 1) / kBN;
+    int64_t a, b, c;
+    if (__builtin_mul_overflow(mask_bs != 0 ? B : 1, mask_hs != 0 ? H : 1, &a) ||
+        __builtin_mul_overflow(a, n_qtiles, &b) || __builtin_mul_overflow(b, (n_kt + 31) / 32, &c))
+        return -1;
+    return c;
 }
 
 int64_t splitkv_choose_splits(int64_t BH, int64_t Nq, int64_t Nk, int64_t requested) {
@@ -1002,7 +1203,8 @@ int fa_fwd_splitkv_launch(const void* Q, const void* K, const void* V, void* O, 
         prm.ws_LSE = ws_LSE;
         prm.n_splits = static_cast<int>(n_splits);
         prm.tiles_per_split = static_cast<int>((n_kv_all + n_splits - 1) / n_splits);
-        const int rc = launch_dispatch<true>(sh.d, causal, tq, tk, tv, prm, stream);
+        const CUtensorMap no_mask{};
+        const int rc = launch_dispatch<true>(sh.d, causal, tq, tk, tv, no_mask, prm, stream);
         if (rc != FA_OK) return rc;
     } else if (n_splits == 1) {
         return fa_fwd_shape_launch(Q, K, V, O, LSE, sh, scale, causal, stream);

@@ -14,6 +14,12 @@ namespace osm {
 // rows of one (b, h), 128-byte swizzle, zero fill outside [0, N) x [0, d).
 int make_bhnd_tensor_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t d);
 
+// Tiled TMA descriptor over an explicit mask: uint32 words [Bm, Hm, Nq, W] with the given
+// strides in words between heads and sequences (used where Hm, Bm > 1); a box of 4 words
+// (one key tile) x 128 query rows, no swizzle, zero fill past Nq.
+int make_mask_tensor_map(CUtensorMap* map, const uint32_t* mask, int64_t W, int64_t Nq,
+                         int64_t Hm, int64_t Bm, int64_t mask_hs, int64_t mask_bs);
+
 // Deadline of every bounded mbarrier wait in the attention kernel.
 unsigned long long fa_wait_timeout_ns();
 
@@ -30,7 +36,16 @@ struct AttnShape {
     // key j allowed.  Not combined with packed query heads.
     const uint32_t* mask = nullptr;
     int64_t mask_bs = 0, mask_hs = 0;
+    // Optional device buffer for the mask's tile map (mask_tile_map_words words): filled by a
+    // pre-pass, then key tiles with no allowed key for a whole query tile are skipped.
+    uint32_t* tile_map = nullptr;
 };
+
+// Words of the tile map of an explicit mask: one row of ceil(ceil(Nk / 128) / 32) words per
+// 128-row query tile and mask instance (B instances when mask_bs != 0, times H when
+// mask_hs != 0).
+int64_t mask_tile_map_words(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t mask_bs,
+                            int64_t mask_hs);
 
 // The same call with the H / H_kv query heads that share a key/value head packed into one row
 // block of (H / H_kv) * Nq rows: the [B, H, Nq, d] memory of Q, O and LSE read as

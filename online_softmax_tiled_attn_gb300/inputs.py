@@ -304,8 +304,10 @@ def pack_mask(mask):
 class MaskWorkload:
     """Attention over Q, K, V [B, H, N, d] (N(0,1), from attn_inputs with this seed) with an
     explicit mask: "prefix_lm" (keys before `prefix` seen by every query, the rest causally;
-    one [1, 1, N, N] mask for all heads) or "random" (each entry allowed with probability
-    `density`, one mask per head, [1, H, N, N])."""
+    one [1, 1, N, N] mask for all heads), "window" (query i sees keys i - window + 1 .. i; one
+    mask for all heads) or "random" (each entry allowed with probability `density`, one mask
+    per head, [1, H, N, N]).  tile_map: whether the call passes fa_fwd_mask a tile map (worth
+    it where whole 128 x 128 tiles are masked)."""
 
     name: str
     B: int
@@ -316,6 +318,8 @@ class MaskWorkload:
     kind: str
     prefix: int = 0
     density: float = 1.0
+    window: int = 0
+    tile_map: bool = True
 
     @property
     def scale(self) -> float:
@@ -326,6 +330,10 @@ class MaskWorkload:
             i = np.arange(self.N)[:, None]
             j = np.arange(self.N)[None, :]
             return ((j < self.prefix) | (j <= i)).astype(np.uint8)[None, None]
+        if self.kind == "window":
+            i = np.arange(self.N)[:, None]
+            j = np.arange(self.N)[None, :]
+            return ((j <= i) & (j > i - self.window)).astype(np.uint8)[None, None]
         return random_mask(1, self.H, self.N, self.N, self.density, self.seed + 1)
 
     @property
@@ -350,7 +358,9 @@ MASK_WORKLOADS = {
         MaskWorkload("mask_prefixlm_b2h16n4096d128", 2, 16, 4096, 128, 1015, "prefix_lm",
                      prefix=1024),
         MaskWorkload("mask_random_b2h16n4096d128", 2, 16, 4096, 128, 1016, "random",
-                     density=0.9),
+                     density=0.9, tile_map=False),
+        MaskWorkload("mask_window_b2h16n8192d128", 2, 16, 8192, 128, 1017, "window",
+                     window=1024),
     ]
 }
 

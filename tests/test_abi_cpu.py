@@ -25,7 +25,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "fa_fwd_gqa_plan",
-              "osm_softmax", "osm_softmax_topk", "fa_bwd", "fa_fwd_mask",
+              "osm_softmax", "osm_softmax_topk", "fa_bwd", "fa_fwd_mask", "fa_fwd_mask_plan",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
@@ -50,7 +50,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 6
+    assert binding.lib().osm_attn_abi_version() == 7
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -213,18 +213,37 @@ def test_fa_bwd_rejects_on_host(over, want):
         (dict(mask=P + 3 * 16384), binding.FA_ERR_INVALID_ARG),    # mask on O
         (dict(d=96), binding.FA_ERR_UNSUPPORTED),
         (dict(Nq=0), binding.FA_OK),
+        (dict(tm=P + 11 * 16384 + 2, tmw=1), binding.FA_ERR_INVALID_ARG),  # tile map misaligned
+        (dict(tm=P + 11 * 16384, tmw=0), binding.FA_ERR_INVALID_ARG),      # tile map too small
+        (dict(tm=P + 3 * 16384, tmw=1), binding.FA_ERR_INVALID_ARG),       # tile map on O
+        (dict(tm=P + 9 * 16384 + 64, tmw=1), binding.FA_ERR_INVALID_ARG),  # tile map on the mask
+        (dict(tm=P, tmw=1), binding.FA_ERR_INVALID_ARG),                   # tile map on Q
     ],
 )
 def test_fa_fwd_mask_rejects_on_host(over, want):
     """B1 H1 N128 d64 at distinct fake addresses (16 KiB per tensor), mask at the tenth."""
     T = 128 * 64 * 2
     a = dict(q=P, k=P + T, v=P + 2 * T, o=P + 3 * T, lse=P + 4 * T, B=1, H=1, Nq=128, Nk=128,
-             d=64, scale=0.125, causal=0, mask=P + 9 * T, mbs=0, mhs=0)
+             d=64, scale=0.125, causal=0, mask=P + 9 * T, mbs=0, mhs=0, tm=0, tmw=0)
     a.update(over)
     rc = binding.fa_fwd_mask_raw(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
                                  a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], a["mask"],
-                                 a["mbs"], a["mhs"], None)
+                                 a["mbs"], a["mhs"], a["tm"], a["tmw"], None)
     assert rc == want
+
+
+def test_fa_fwd_mask_plan_sizes():
+    """One row of ceil(key tiles / 32) words per 128-row query tile and mask instance."""
+    assert binding.mask_plan(1, 1, 128, 128, 0, 0) == 1
+    assert binding.mask_plan(2, 16, 4096, 4096, 0, 0) == 32            # one shared mask
+    assert binding.mask_plan(2, 16, 4096, 4096, 0, 4096 * 128) == 16 * 32   # per head
+    assert binding.mask_plan(2, 16, 4096, 4096, 16 * 4096 * 128, 4096 * 128) == 2 * 16 * 32
+    assert binding.mask_plan(2, 16, 4096, 4096, 16 * 4096 * 128, 0) == 2 * 32  # per sequence
+    assert binding.mask_plan(1, 1, 300, 5000, 0, 0) == 3 * 2           # 40 key tiles: 2 words
+    assert binding.mask_plan(1, 1, 0, 5000, 0, 0) == 0
+    for bad in ((-1, 1, 128, 128, 0, 0), (1, 1, 128, 128, -4, 0), (1, 1, 1 << 31, 128, 0, 0)):
+        with pytest.raises(binding.FaError):
+            binding.mask_plan(*bad)
 
 
 def test_selftest_rejects_out_of_range_timeout_on_host():

@@ -23,9 +23,9 @@ def bits(mask):
     return torch.from_numpy(inputs.pack_mask(mask).view(np.int32)).cuda()
 
 
-def run(q, k, v, mask, causal, scale=None):
+def run(q, k, v, mask, causal, scale=None, skip=True):
     O, L = binding.fa_fwd_mask(q.cuda(), k.cuda(), v.cuda(), bits(mask), scale=scale,
-                               causal=causal)
+                               causal=causal, skip_tiles=skip)
     torch.cuda.synchronize()
     assert binding.device_status() == 0
     return O.float().cpu().numpy(), L.cpu().numpy()
@@ -48,13 +48,14 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("skip", [False, True], ids=["all_tiles", "tile_map"])
 @pytest.mark.parametrize("B,H,Nq,Nk,d,causal,mshape,dens,frows,fkeys", CASES,
                          ids=lambda x: str(x))
-def test_mask_parity(B, H, Nq, Nk, d, causal, mshape, dens, frows, fkeys):
+def test_mask_parity(B, H, Nq, Nk, d, causal, mshape, dens, frows, fkeys, skip):
     q, k, v = qkv(B, H, Nq, Nk, d, seed=8000 + Nq + Nk + d)
     m = inputs.random_mask(mshape[0], mshape[1], Nq, Nk, dens, seed=8100 + Nq,
                            full_rows=frows, full_keys=fkeys)
-    O, L = run(q, k, v, m, causal)
+    O, L = run(q, k, v, m, causal, skip=skip)
     Oref, Lref = oracle.attention_masked(q, k, v, 1.0 / math.sqrt(d), causal, m)
     if frows:
         assert np.isinf(Lref).any()
@@ -70,20 +71,51 @@ def test_all_ones_mask_is_unmasked_attention_bit_for_bit():
     assert np.array_equal(O, O2.float().cpu().numpy()) and np.array_equal(L, L2.cpu().numpy())
 
 
-def test_structured_masks():
-    """A sliding window inside documents and a prefix-LM mask, the shapes such masks take."""
+@pytest.mark.parametrize("skip", [False, True], ids=["all_tiles", "tile_map"])
+def test_structured_masks(skip):
+    """A sliding window inside documents and a prefix-LM mask, the shapes such masks take (with
+    the tile map, most key tiles of the window mask are skipped)."""
     B, H, N, d = 1, 2, 640, 64
     q, k, v = qkv(B, H, N, N, d, seed=8300)
     win = inputs.window_mask(N, N, window=96, doc_len=200)
-    O, L = run(q, k, v, win, False)
+    O, L = run(q, k, v, win, False, skip=skip)
     Oref, Lref = oracle.attention_masked(q, k, v, 1.0 / math.sqrt(d), False, win)
     parity.check_attention_allow_empty(O, L, Oref, Lref, "window")
     i = np.arange(N)[:, None]
     j = np.arange(N)[None, :]
     plm = ((j < 150) | (j <= i)).astype(np.uint8)[None, None]
-    O, L = run(q, k, v, plm, False)
+    O, L = run(q, k, v, plm, False, skip=skip)
     Oref, Lref = oracle.attention_masked(q, k, v, 1.0 / math.sqrt(d), False, plm)
     parity.check_attention_allow_empty(O, L, Oref, Lref, "prefix LM")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_tile_map_skips_whole_tiles(d):
+    """Block-sparse masks where the tile map leaves key tiles, and for one query tile every key
+    tile, out: per-head block-diagonal masks with ragged blocks (3 tiles of keys per head
+    skipped), a query tile with no allowed key at all (O = 0, LSE = -inf for its rows), masks
+    shared over sequences, and causal on top.  Both paths against the oracle, and against each
+    other to the rounding of the sums."""
+    B, H, Nq, Nk = 2, 3, 520, 700
+    q, k, v = qkv(B, H, Nq, Nk, d, seed=8500 + d)
+    i = np.arange(Nq)[:, None]
+    j = np.arange(Nk)[None, :]
+    m = np.zeros((1, H, Nq, Nk), np.uint8)
+    for h in range(H):
+        blk = 150 + 40 * h  # ragged blocks that straddle tile edges
+        m[0, h] = ((i // blk) == (j // blk)) | (j < 10 * h)
+    m[:, :, 256:384] = 0  # query tile 2: nothing allowed
+    for causal in (False, True):
+        Oref, Lref = oracle.attention_masked(q, k, v, 1.0 / math.sqrt(d), causal, m)
+        assert np.isinf(Lref[:, :, 256:384]).all()
+        O0, L0 = run(q, k, v, m, causal, skip=False)
+        O1, L1 = run(q, k, v, m, causal, skip=True)
+        for O, L, what in ((O0, L0, "all tiles"), (O1, L1, "tile map")):
+            parity.check_attention_allow_empty(O, L, Oref, Lref, f"block sparse {what} {causal}")
+            assert (O[:, :, 256:384] == 0).all() and np.isneginf(L[:, :, 256:384]).all()
+        fin = np.isfinite(L0)
+        assert np.array_equal(fin, np.isfinite(L1))
+        assert np.abs(O0 - O1).max() <= 2 ** -7 and np.abs(L0[fin] - L1[fin]).max() <= 1e-5
 
 
 def test_masked_keys_cannot_matter():
