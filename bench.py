@@ -456,6 +456,8 @@ NCU_TRAFFIC_BYTES = {
     "gqa_causal_b2h32kv8n8192d128": 354.289408e6 + 99.04384e6,
     "softmax_topk_65536x4000_k8": 1.048666e9 + 7.303424e6,
     "softmax_topk_512x131072_k32": 268.514816e6 + 3.573504e6,
+    "mask_prefixlm_b2h16n4096d128": 102.0864e6 + 12.406784e6,
+    "mask_window_b2h16n8192d128": 203.465216e6 + 45.116672e6,
 }
 # The backward workloads run three kernels per call; their per-kernel traffic is in the
 # bwd_kv_kernel / bwd_q_kernel summaries, and the call's roofline reports none.
