@@ -50,6 +50,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "osm_internal.h"
 #include "ptx_sm103.cuh"
@@ -105,14 +106,14 @@ struct Bars {
     uint64_t mma_done;
     uint64_t mma_pv_done;
     uint32_t tmem_base;
+    float mref[2][kBM];                // reference max of tile J for tile J+1: [J & 1][row]
+    float fin[kFinSlots][2][2][kBM];   // [item slot][group][m, l][row]
     // MASK: the key tile in V ring slot s, written by the V producer before its arrival on
     // v_full[s] (ordered by that barrier for the softmax, which reads it after the wait).
     int v_kt[kMaxStages];
-    float mref[2][kBM];                // reference max of tile J for tile J+1: [J & 1][row]
-    float fin[kFinSlots][2][2][kBM];   // [item slot][group][m, l][row]
 };
 
-template <int D>
+template <int D, bool M = false>  // M: the kernel reads an explicit mask
 struct Cfg {
     static constexpr int kHalves = D / 64;
     static constexpr int kTileBytes = kHalves * kHalfBytes;  // 128 rows x D bf16
@@ -121,7 +122,7 @@ struct Cfg {
     static constexpr int kV = kK + kStages * kTileBytes;
     static constexpr int kMsk = kV + kStages * kTileBytes;  // MASK: a key tile's mask bits
     static constexpr int kMskBytes = kBM * 16;              // 128 query rows x 16 bytes
-    static constexpr int kBars = kMsk + kStages * kMskBytes;
+    static constexpr int kBars = kMsk + (M ? kStages * kMskBytes : 0);
     static constexpr int kBytes = kBars + static_cast<int>(sizeof(Bars));
     static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
     static constexpr int kP = D == 64 ? 2 : 1;      // P buffers
@@ -187,14 +188,14 @@ struct FaParams {
     const uint32_t* mask;
     long long mask_bs, mask_hs;
     int mask_words;
-    // Optional tile map of the mask (MASK only), or nullptr: bit kt % 32 of word kt / 32 of
+    float scale_log2;
+    unsigned long long timeout_ns;
+    // Optional tile map of the mask (MASK == 2), or nullptr: bit kt % 32 of word kt / 32 of
     // the row at tile_map + (inst * n_qtiles + q_tile) * tmap_words is 0 when no key of key
     // tile kt is allowed for any query of the query tile; such tiles are skipped.  inst is the
     // mask's instance: b and h of the query head where the mask strides are nonzero.
     const uint32_t* tile_map;
     int tmap_words;
-    float scale_log2;
-    unsigned long long timeout_ns;
 };
 
 // One work item: a 128-row query tile of query head bh (over all sequences) against key tiles
@@ -268,9 +269,11 @@ __device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
     }
     w.n_kv = max(0, kt1 - w.kt0);
     w.tm = nullptr;
-    w.kt_end = w.kt0 + w.n_kv;
-    w.tm_word = -1;
-    w.tm_bits = 0u;
+    if (TMAP) {
+        w.kt_end = w.kt0 + w.n_kv;
+        w.tm_word = -1;
+        w.tm_bits = 0u;
+    }
     if (TMAP && prm.tile_map != nullptr && w.n_kv > 0) {
         const int b = w.bh / prm.H, h = w.bh - (w.bh / prm.H) * prm.H;
         const int inst = (prm.mask_bs != 0 ? b : 0) * (prm.mask_hs != 0 ? prm.H : 1) +
@@ -338,14 +341,19 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int stages, int issue
     }
 }
 
+// The mask's tensor map, a kernel parameter only where a mask is read.
+struct NoMaskMap {};
+template <int MASK>
+using MaskMap = typename std::conditional<(MASK != 0), CUtensorMap, NoMaskMap>::type;
+
 // MASK: 1 = an explicit mask is read (prm.mask), 2 = the same with the mask's tile map
 // (prm.tile_map); separate instantiations, so that the unmasked kernels' code is unchanged.
 template <int D, bool CAUSAL, bool SPLIT, int MASK = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ MaskMap<MASK> tmM,
                   const FaParams prm) {
-    using C = Cfg<D>;
+    using C = Cfg<D, (MASK != 0)>;
     constexpr int S_ = C::kStages;
     const int Nq = prm.Nq, Nk = prm.Nk;
     const unsigned long long timeout_ns = prm.timeout_ns;
@@ -495,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tmQ);
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
-                if (MASK) tma_prefetch_desc(&tmM);
+                if constexpr (MASK != 0) tma_prefetch_desc(&tmM);
                 constexpr uint32_t kTx = C::kTileBytes;
                 int e = 0;  // K-ring entries issued
                 bool ok = true;
@@ -516,12 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         mbar_arrive_expect_tx(&bars->k_full[s], kTx);
                         const CUtensorMap* map = t < 0 ? &tmQ : &tmK;
-                        const int row = t < 0 ? w.q_tile * kBM : kt * kBN;
+                        const int row =
+                            t < 0 ? w.q_tile * kBM : (MASK == 2 ? kt : w.kt0 + t) * kBN;
                         const int head = t < 0 ? w.bh : w.kvh;
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, map,
                                         &bars->k_full[s], h * 64, row, head);
-                        if (t >= 0) kt = tiles.next();
+                        if (t >= 0) kt = MASK == 2 ? tiles.next() : kt + 1;
                     }
                 }
                 drain_ring(bars->k_full, S_, e, timeout_ns);
@@ -537,8 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (idx < 0) break;
                     const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
                     TileCursor tiles(w);
-                    int kt = tiles.next();
-                    for (int t = 0; t < w.n_kv; ++t, ++J, kt = tiles.next()) {
+                    int kt = MASK == 2 ? tiles.next() : w.kt0;
+                    for (int t = 0; t < w.n_kv;
+                         ++t, ++J, kt = MASK == 2 ? tiles.next() : kt + 1) {
                         const int s = J % S_;
                         if (J >= S_ &&
                             !mbar_wait(&bars->v_empty[s], ((J / S_) - 1) & 1, timeout_ns, true)) {
@@ -551,8 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               MASK ? kTx + C::kMskBytes : kTx);
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(smem + C::kV + s * C::kTileBytes + h * kHalfBytes, &tmV,
-                                        &bars->v_full[s], h * 64, kt * kBN, w.kvh);
-                        if (MASK) {
+                                        &bars->v_full[s], h * 64,
+                                        (MASK == 2 ? kt : w.kt0 + t) * kBN, w.kvh);
+                        if constexpr (MASK != 0) {
                             // The tile's mask bits for the 128 query rows ride with V: the
                             // slot is freed only after P V, when the softmax has used them.
                             const int b = w.bh / prm.H, h = w.bh - b * prm.H;
@@ -736,25 +747,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // MASK: the key tile of visit J and the row's 128 bits of it came with V(J)
                 // into V slot J % S_ (the visits of a tile map step over empty tiles; rows
                 // past Nq read zero fill); otherwise visit t is tile kt0 + t.
-                int kt = kt0 + t;
-                uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);
-                if (MASK) {
+                int kv0 = (kt0 + t) * kBN;
+                uint4 mw;
+                if constexpr (MASK != 0) {
                     const int vs = J % S_;
                     if (!warp_wait(&bars->v_full[vs], (J / S_) & 1, timeout_ns)) {
                         record_timeout(17);
                         ok = false;
                         break;
                     }
-                    kt = bars->v_kt[vs];
+                    kv0 = bars->v_kt[vs] * kBN;
                     mw = reinterpret_cast<const uint4*>(smem + C::kMsk + vs * C::kMskBytes)[r];
                 }
-                const int kv0 = kt * kBN;
                 if (kv0 + kBN - 1 > key_limit) {
 #pragma unroll
                     for (int e = 0; e < 128; ++e)
                         if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
                 }
-                if (MASK) {
+                if constexpr (MASK != 0) {
                     // The explicit mask: a key whose bit is 0 takes no part (score -inf).
                     // Words of all ones (the usual case for structured masks) cost one test.
                     const uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
@@ -944,11 +954,17 @@ int device_sm_count() {
     return n;
 }
 
+template <int MASK>
+MaskMap<MASK> mask_map(const CUtensorMap& tm) {
+    if constexpr (MASK != 0) return tm;
+    else return NoMaskMap{};
+}
+
 template <int D, bool CAUSAL, bool SPLIT, int MASK = 0>
 int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const CUtensorMap& tm,
                   const FaParams& prm, cudaStream_t stream) {
-    using C = Cfg<D>;
+    using C = Cfg<D, (MASK != 0)>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -976,7 +992,7 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     const int sms = device_sm_count();
     const long long ctas = (sms > 0 && items > sms) ? sms : items;
     fa_fwd_kernel<D, CAUSAL, SPLIT, MASK>
-        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, tm, p);
+        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, mask_map<MASK>(tm), p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
