@@ -9,7 +9,10 @@
 // the best head among the lists.  The outputs are the k columns with the largest x (ties: the
 // smaller column first), their shares y = exp(x - m) / l, and lse = m + ln l.
 //
-// GB300 mapping (HBM-bound: 4 bytes read per element, nothing written per element):
+// GB300 mapping (HBM-bound: 4 bytes read per element, nothing written per element).  Rows with
+// 16-byte access and k >= 2 take the staged kernels further down (rows brought into shared
+// memory by bulk copies); the register kernels described here serve k = 1 and rows that are
+// not 16-byte aligned:
 //   * rows up to 4096 columns: one warp per row; longer rows: the 8 warps of a CTA share a row
 //     and their lists meet in shared memory;
 //   * 16-byte loads when the row allows them;
@@ -964,27 +967,38 @@ int launch(const float* x, long long rows, int cols, int k, float* vals, int* id
            cudaStream_t stream) {
     const bool vec = (cols % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
     const long long sms = sm_count() > 0 ? sm_count() : 148;
-    if (kFiltered<Top> && vec)
-        return cols <= kStagedMaxCols ? launch_staged(x, rows, cols, k, vals, idx, lse, stream)
-                                      : launch_long(x, rows, cols, k, vals, idx, lse, stream);
+    // k >= 2 with 16-byte access: the staged kernels (the register kernels' vector forms for
+    // k >= 2 are not built).
+    if constexpr (kFiltered<Top>) {
+        if (vec)
+            return cols <= kStagedMaxCols
+                       ? launch_staged(x, rows, cols, k, vals, idx, lse, stream)
+                       : launch_long(x, rows, cols, k, vals, idx, lse, stream);
+    }
     if (cols <= 4096) {
         long long grid = (rows + kWarps - 1) / kWarps;
         if (grid > sms * 8) grid = sms * 8;
-        if (vec)
-            topk_warp_rows<true, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-                x, rows, cols, k, vals, idx, lse);
-        else
-            topk_warp_rows<false, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-                x, rows, cols, k, vals, idx, lse);
+        if constexpr (!kFiltered<Top>) {
+            if (vec) {
+                topk_warp_rows<true, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+                    x, rows, cols, k, vals, idx, lse);
+                return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+            }
+        }
+        topk_warp_rows<false, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+            x, rows, cols, k, vals, idx, lse);
     } else {
         long long grid = rows;
         if (grid > sms * 8) grid = sms * 8;
-        if (vec)
-            topk_cta_rows<true, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-                x, rows, cols, k, vals, idx, lse);
-        else
-            topk_cta_rows<false, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-                x, rows, cols, k, vals, idx, lse);
+        if constexpr (!kFiltered<Top>) {
+            if (vec) {
+                topk_cta_rows<true, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+                    x, rows, cols, k, vals, idx, lse);
+                return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+            }
+        }
+        topk_cta_rows<false, Top><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+            x, rows, cols, k, vals, idx, lse);
     }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
