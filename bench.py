@@ -447,13 +447,13 @@ def roofline_hbm(nbytes, ms, peaks, kind, traffic=None):
 # Traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
 # summarised under profiles/, one per workload.  Workloads without a capture report None.
 NCU_TRAFFIC_BYTES = {
-    "mha_b4h16n2048d64": 50.39488e6 + 0.222976e6,
-    "dense_b2h32n8192": 402.803968e6 + 115.572992e6,
-    "causal_b2h32n8192": 680.285696e6 + 120.198656e6,
-    "decode_b8h32q1k32768d128": 4.295259e9 + 3.723264e6,
-    "gqa_decode_b8h32kv8q1k32768d128": 1.073947e9 + 5.79328e6,
+    "mha_b4h16n2048d64": 50.395648e6 + 0.034048e6,
+    "dense_b2h32n8192": 403.199232e6 + 116.581632e6,
+    "causal_b2h32n8192": 701.020672e6 + 119.029504e6,
+    "decode_b8h32q1k32768d128": 4.295266816e9 + 3.664384e6,
+    "gqa_decode_b8h32kv8q1k32768d128": 1.073933824e9 + 5.0816e6,
     "softmax_65536x4000": 1.048683e9 + 0.997987072e9,
-    "gqa_causal_b2h32kv8n8192d128": 354.289408e6 + 99.04384e6,
+    "gqa_causal_b2h32kv8n8192d128": 357.92768e6 + 98.847488e6,
     "softmax_topk_65536x4000_k8": 1.048666e9 + 7.303424e6,
     "softmax_topk_512x131072_k32": 268.514816e6 + 3.573504e6,
     "mask_prefixlm_b2h16n4096d128": 102.0864e6 + 12.406784e6,
