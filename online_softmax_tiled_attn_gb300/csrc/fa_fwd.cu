@@ -36,11 +36,15 @@
 //                   runs them, so two independent issuers keep it fed.  fp32 accumulators.
 //   warps 10, 11    TMA: the K ring (each item's Q tile, then its K tiles; warp 10) and the V
 //                   ring (warp 11); 128-byte swizzle, zero fill past the end of the sequence.
+//                   With an explicit mask the V producer also brings each tile's mask bits
+//                   (16 bytes for each of the 128 query rows) and the tile's index into the V
+//                   slot, where the softmax reads them after the slot's barrier.
 //   warps 12-15     epilogue: the two groups' (m, l) combined with the two-worker merge, O read
 //                   from TMEM once the item's last P V is done (the next item's first P V
 //                   waits for that read), O / l to bf16 and LSE = (m + log2 l) * ln 2.
 // Causal: key tiles above the diagonal are never visited; only diagonal and ragged tiles are
-// masked element by element.
+// masked element by element.  With an explicit mask's tile map, key tiles holding no allowed
+// key for the query tile are not visited either.
 //
 // Every mbarrier wait is bounded (%globaltimer deadline).  A wait that gives up records
 // FA_ERR_TIMEOUT in a device status word; the CTA then drains its own TMA loads and MMAs,
