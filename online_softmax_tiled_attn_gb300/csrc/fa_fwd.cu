@@ -173,7 +173,7 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
 // tiles_per_split key tiles; with n_splits == 1 (SPLIT == false) a work item covers every key
 // and writes the final O (bf16) and LSE, otherwise it writes its range's normalised partial
 // output (fp32) and log-sum-exp to the workspace for the combine kernel.
-struct FaParams {
+struct FaKernelParams {
     __nv_bfloat16* O;  // [BH, Nq, D] bf16 (SPLIT == false)
     float* LSE;        // [BH, Nq] or nullptr (SPLIT == false)
     float* ws_O;       // [n_splits, BH, Nq, D] fp32 (SPLIT == true)
@@ -194,6 +194,11 @@ struct FaParams {
     int mask_words;
     float scale_log2;
     unsigned long long timeout_ns;
+};
+
+// The host's launch state: the kernel's parameters, and the mask's tile map, which reaches the
+// kernel (MASK == 2) with the mask's tensor map instead.
+struct FaParams : FaKernelParams {
     // Optional tile map of the mask (MASK == 2), or nullptr: bit kt % 32 of word kt / 32 of
     // the row at tile_map + (inst * n_qtiles + q_tile) * tmap_words is 0 when no key of key
     // tile kt is allowed for any query of the query tile; such tiles are skipped.  inst is the
@@ -228,7 +233,9 @@ __device__ __forceinline__ uint32_t map_word(const Item& w, int wi) {
 // many as keep their K and V in L2 together), and within a group the longest rows (highest
 // query tiles) first, so that the CTAs' shares even out.
 template <bool CAUSAL, bool TMAP = false>
-__device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
+__device__ __forceinline__ Item decode_item(int idx, const FaKernelParams& prm,
+                                            const uint32_t* tile_map = nullptr,
+                                            int tmap_words = 0) {
     Item w;
     if (CAUSAL) {
         const int per_head = prm.n_qtiles * prm.n_splits;
@@ -278,12 +285,11 @@ __device__ __forceinline__ Item decode_item(int idx, const FaParams& prm) {
         w.tm_word = -1;
         w.tm_bits = 0u;
     }
-    if (TMAP && prm.tile_map != nullptr && w.n_kv > 0) {
+    if (TMAP && tile_map != nullptr && w.n_kv > 0) {
         const int b = w.bh / prm.H, h = w.bh - (w.bh / prm.H) * prm.H;
         const int inst = (prm.mask_bs != 0 ? b : 0) * (prm.mask_hs != 0 ? prm.H : 1) +
                          (prm.mask_hs != 0 ? h : 0);
-        w.tm = prm.tile_map + (static_cast<long long>(inst) * prm.n_qtiles + w.q_tile) *
-                                  prm.tmap_words;
+        w.tm = tile_map + (static_cast<long long>(inst) * prm.n_qtiles + w.q_tile) * tmap_words;
         int n = 0;
         for (int wi = w.kt0 >> 5; wi <= (w.kt_end - 1) >> 5; ++wi) {
             const uint32_t bits = map_word(w, wi);
@@ -345,10 +351,26 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int stages, int issue
     }
 }
 
-// The mask's tensor map, a kernel parameter only where a mask is read.
+// The mask's tensor map and tile map, a kernel parameter only where a mask is read.
+struct MaskArgs {
+    CUtensorMap map;
+    const uint32_t* tile_map;  // MASK == 2: the tile map (FaParams::tile_map)
+    int tmap_words;
+};
 struct NoMaskMap {};
 template <int MASK>
-using MaskMap = typename std::conditional<(MASK != 0), CUtensorMap, NoMaskMap>::type;
+using MaskMap = typename std::conditional<(MASK != 0), MaskArgs, NoMaskMap>::type;
+
+template <int MASK>
+__device__ __forceinline__ const uint32_t* tile_map_of(const MaskMap<MASK>& m) {
+    if constexpr (MASK == 2) return m.tile_map;
+    else return nullptr;
+}
+template <int MASK>
+__device__ __forceinline__ int tmap_words_of(const MaskMap<MASK>& m) {
+    if constexpr (MASK == 2) return m.tmap_words;
+    else return 0;
+}
 
 // MASK: 1 = an explicit mask is read (prm.mask), 2 = the same with the mask's tile map
 // (prm.tile_map); separate instantiations, so that the unmasked kernels' code is unchanged.
@@ -356,7 +378,7 @@ template <int D, bool CAUSAL, bool SPLIT, int MASK = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ MaskMap<MASK> tmM,
-                  const FaParams prm) {
+                  const FaKernelParams prm) {
     using C = Cfg<D, (MASK != 0)>;
     constexpr int S_ = C::kStages;
     const int Nq = prm.Nq, Nk = prm.Nk;
@@ -422,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0;; ++k) {
             const int idx = cta_item(k, prm.n_items);
             if (idx < 0) break;
-            const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
+            const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
             const int slot = k % kFinSlots;
             if (!warp_wait(&bars->fin_full[slot], (k / kFinSlots) & 1, timeout_ns, true)) {
                 record_timeout(12);
@@ -507,14 +529,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tmQ);
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
-                if constexpr (MASK != 0) tma_prefetch_desc(&tmM);
+                if constexpr (MASK != 0) tma_prefetch_desc(&tmM.map);
                 constexpr uint32_t kTx = C::kTileBytes;
                 int e = 0;  // K-ring entries issued
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
                     if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
+                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
                     // t = -1: the item's Q tile, then its key tiles (key tile kt).
                     TileCursor tiles(w);
                     int kt = tiles.next();
@@ -548,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
                     if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
+                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
                     TileCursor tiles(w);
                     int kt = MASK == 2 ? tiles.next() : w.kt0;
                     for (int t = 0; t < w.n_kv;
@@ -571,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // The tile's mask bits for the 128 query rows ride with V: the
                             // slot is freed only after P V, when the softmax has used them.
                             const int b = w.bh / prm.H, h = w.bh - b * prm.H;
-                            tma_load_4d(smem + C::kMsk + s * C::kMskBytes, &tmM,
+                            tma_load_4d(smem + C::kMsk + s * C::kMskBytes, &tmM.map,
                                         &bars->v_full[s], 4 * kt, w.q_tile * kBM,
                                         prm.mask_hs != 0 ? h : 0, prm.mask_bs != 0 ? b : 0);
                         }
@@ -588,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
                     if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
+                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
                     if (w.n_kv == 0) continue;
                     // The item's Q tile: K ring -> Q buffer qb in TMEM (tcgen05.cp, ordered
                     // before the MMAs below), once the S of item qi - kQ, the buffer's
@@ -660,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int idx = cta_item(k, prm.n_items);
                     if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
+                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
                     if (w.n_kv == 0) continue;
                     // The first P V of an item overwrites O: the epilogue must have read the
                     // previous item's.
@@ -713,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0;; ++k) {
             const int idx = cta_item(k, prm.n_items);
             if (idx < 0) break;
-            J_total += decode_item<CAUSAL, MASK == 2>(idx, prm).n_kv;
+            J_total += decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM)).n_kv;
         }
         bool ok = true;
         int J0 = 0;  // first key tile of the item
@@ -722,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (idx < 0) break;
             int n, kt0, key_limit;
             {
-                const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm);
+                const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
                 n = w.n_kv;
                 kt0 = w.kt0;
                 const int q_row = w.q_tile * kBM + r;
@@ -959,8 +981,8 @@ int device_sm_count() {
 }
 
 template <int MASK>
-MaskMap<MASK> mask_map(const CUtensorMap& tm) {
-    if constexpr (MASK != 0) return tm;
+MaskMap<MASK> mask_map(const CUtensorMap& tm, const FaParams& p) {
+    if constexpr (MASK != 0) return MaskArgs{tm, MASK == 2 ? p.tile_map : nullptr, p.tmap_words};
     else return NoMaskMap{};
 }
 
@@ -996,7 +1018,8 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     const int sms = device_sm_count();
     const long long ctas = (sms > 0 && items > sms) ? sms : items;
     fa_fwd_kernel<D, CAUSAL, SPLIT, MASK>
-        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(tq, tk, tv, mask_map<MASK>(tm), p);
+        <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(
+            tq, tk, tv, mask_map<MASK>(tm, p), static_cast<const FaKernelParams&>(p));
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
