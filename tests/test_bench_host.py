@@ -72,3 +72,20 @@ def test_workload_flops_match_the_metric_definition():
     assert w.flops == 4 * 4 * 16 * 2048 ** 2 * 64
     c = inputs.ATTN_WORKLOADS["causal_b2h32n8192"]
     assert c.flops == 4 * 2 * 32 * 8192 ** 2 * 128 / 2
+
+
+def test_mask_workload_flops_count_the_allowed_pairs():
+    """4 d FLOP per allowed (query, key) pair over every head, against the closed forms of the
+    pair counts: prefix-LM row i sees max(prefix, i + 1) keys, a causal window w sees
+    min(i + 1, w).  (The random mask's count is its own; making it here takes a minute.)"""
+    from online_softmax_tiled_attn_gb300 import inputs
+
+    W = inputs.MASK_WORKLOADS
+    p = W["mask_prefixlm_b2h16n4096d128"]
+    pairs = sum(max(p.prefix, i + 1) for i in range(p.N))
+    assert pairs == p.prefix * p.prefix + sum(range(p.prefix + 1, p.N + 1))
+    assert p.flops == 4 * p.d * pairs * p.B * p.H
+    w = W["mask_window_b2h16n8192d128"]
+    pairs = w.window * (w.window + 1) // 2 + (w.N - w.window) * w.window
+    assert w.flops == 4 * w.d * pairs * w.B * w.H
+    assert w.tile_map and p.tile_map and not W["mask_random_b2h16n4096d128"].tile_map
