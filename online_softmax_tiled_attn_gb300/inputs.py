@@ -33,6 +33,7 @@ rows, which belong to the ragged/overflow stress workload).
 """
 from __future__ import annotations
 
+import functools
 import math
 from dataclasses import dataclass
 
@@ -326,6 +327,10 @@ class MaskWorkload:
         return 1.0 / math.sqrt(self.d)
 
     def mask(self):
+        """uint8 [1, 1 or H, N, N], 1 = allowed (made once per workload and kept: read only)."""
+        return _workload_mask(self)
+
+    def _make_mask(self):
         if self.kind == "prefix_lm":
             i = np.arange(self.N)[:, None]
             j = np.arange(self.N)[None, :]
@@ -350,6 +355,13 @@ class MaskWorkload:
         n = self.B * self.H * self.N
         m = self.mask()
         return 4 * n * self.d * 2 + n * 4 + m.shape[1] * self.N * (4 * ((self.N + 127) // 128)) * 4
+
+
+@functools.lru_cache(maxsize=4)
+def _workload_mask(w):
+    m = w._make_mask()
+    m.setflags(write=False)
+    return m
 
 
 MASK_WORKLOADS = {
