@@ -8,6 +8,10 @@
  * TMA descriptors.  Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  * NULL is the legacy default stream) and returns an fa_status code.  Argument errors are
  * found on the host before anything is launched.
+ *
+ * One process drives one GPU: the cached kernel attributes and the address of the device
+ * status word are taken for the device current at the first call that needs them, so every
+ * call must be made with that same device current (run one process per GPU).
  */
 #ifndef OSM_ATTN_H
 #define OSM_ATTN_H
