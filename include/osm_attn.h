@@ -156,13 +156,21 @@ OSM_ATTN_API int fa_fwd_splitkv_plan(int64_t B, int64_t H, int64_t Nq, int64_t N
  * Same arguments and results as fa_fwd_splitkv, minus ws_O / ws_LSE; n_splits = 0 lets the
  * library choose as fa_fwd_splitkv_plan does.  The per-range partial states live in a fixed
  * array of 4 Mi floats (16 MiB) that every GPU loading the library holds until the process
- * exits: a shape needs n_splits * B*H*Nq * (d + 1) floats of it, and one that needs more returns
- * FA_ERR_SCRATCH_LIMIT without launching anything.  The first call made with a device current
- * resolves that device's array address (cudaGetSymbolAddress) and caches it; make that first
- * call before any stream capture.  All calls on a device share the one array: calls that can
- * overlap on the GPU (different streams, or streams not ordered with each other) race on it
- * and must be serialised by the caller.  The array keeps the last call's contents; every entry a
- * call reads is written earlier in the same call, so nothing needs clearing between calls.
+ * exits: a shape needs splits * B*H*Nq * (d + 1) floats of it, where splits is the count
+ * fa_fwd_splitkv_plan returns for the same B, H, Nq, Nk, d and n_splits (the library's choice
+ * when n_splits = 0, and never more than the key tiles, ceil(Nk / 128)); a caller can check a
+ * shape in advance with that call.  A shape that needs more returns FA_ERR_SCRATCH_LIMIT
+ * without launching anything.  The first call made with a device current resolves that
+ * device's array address (cudaGetSymbolAddress) and caches it for the life of the process;
+ * make that first call before any stream capture.  The cached address belongs to the device's
+ * context as it was then: after cudaDeviceReset of that device the process must not call this
+ * entry point again.  All calls on a device share the one array: calls that can overlap on the
+ * GPU (different streams, or streams not ordered with each other) race on it and must be
+ * serialised by the caller.  The array keeps the last call's contents; every entry a call
+ * reads is written earlier in the same call, so nothing needs clearing between calls -- unless
+ * a kernel of the call gave up a bounded wait: then the combine may read entries an earlier
+ * call left behind, and O and LSE of that call are undefined.  osm_attn_device_status reports
+ * that case (FA_ERR_TIMEOUT); a caller that needs to know must read it after the call.
  */
 OSM_ATTN_API int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
                                         float* LSE, int64_t B, int64_t H, int64_t Nq,

@@ -7,14 +7,16 @@ tensor-core products, forms D_i = dO_i . O_i from the bf16 O, and rounds dQ, dK,
 `rounding_model` is the oracle's definition in fp64 with exactly those roundings added; its
 distance from the oracle is the error that arithmetic cannot avoid.  Both errors are measured
 relative to the gradient's scale (the root mean square of the oracle's entries of that tensor),
-and the kernel must stay within 1.5x the model's rms error plus 2e-3 of the scale, and within
-2x the model's max error plus 1e-2 of the scale (the max over millions of entries is an
+and the kernel must stay within 1.2x the model's rms error plus 5e-4 of the scale, and within
+2x the model's max error plus 5e-3 of the scale (the max over millions of entries is an
 extreme-value statistic: where the kernel's fp32 intermediates round a share differently from
 the model's fp64 ones, the two are different samples of the same rounding), under fixed
 ceilings that guard against a model gone wrong itself: max |err| <= 0.3 * rms and
-rms(err) <= 1e-2 * rms.  (The model alone gives rms(err) ~ 2.4e-3 * rms with N(0, 1) inputs and
-~5e-3 * rms with logits of sd 9; its max reaches 0.2 * rms on causal rows whose few shares are
-large.)
+rms(err) <= 7.5e-3 * rms.  (The model alone gives rms(err) ~ 2.4e-3 * rms with N(0, 1) inputs and
+~5e-3 * rms with logits of sd 9; its max reaches 0.23 * rms on causal rows whose few shares are
+large.  Measured on GB300, the kernel's rms error is at most 1.11x the model's and its max
+error at most 1.73x.  An extra error uncorrelated with the rounding passes the rms bound only
+below about 0.25 % of the gradient's rms.)
 """
 import math
 
@@ -28,9 +30,9 @@ from online_softmax_tiled_attn_gb300 import binding, inputs
 pytestmark = pytest.mark.gpu
 
 BWD_MAX_CEIL = 0.3
-BWD_RMS_CEIL = 1e-2
-BWD_RMS_FACTOR, BWD_RMS_SLACK = 1.5, 2e-3
-BWD_MAX_FACTOR, BWD_MAX_SLACK = 2.0, 1e-2
+BWD_RMS_CEIL = 7.5e-3
+BWD_RMS_FACTOR, BWD_RMS_SLACK = 1.2, 5e-4
+BWD_MAX_FACTOR, BWD_MAX_SLACK = 2.0, 5e-3
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -2,7 +2,9 @@
 memory during a call (a plugin or custom-operator hook whose framework forbids allocation
 there, a latency-critical decode loop).  Its partial states live in the library's fixed scratch
 array instead of a caller workspace.  Checked through the C ABI against fa_fwd_splitkv with a
-workspace, on two calls in a row (the second call reuses the scratch the first one left)."""
+workspace, on two calls in a row.  Before each checked call another call with other inputs and
+a larger shape fills most of the array with its own partial states, so a (range, row) entry
+that the checked call failed to write would be read stale and show up as a mismatch."""
 import math
 
 import pytest
@@ -20,6 +22,27 @@ CASES = [
 ]
 
 
+# B1 H16, 128 queries against 8192 keys, d = 128, 15 ranges requested (13 ranges of 5 key
+# tiles): 13 * 2048 * 129 = 3.4 Mi floats, 82 % of the 4 Mi-float array.
+FILL = (1, 16, 128, 8192, 128, 15)
+
+
+def _fill_scratch_with_another_call(seed, stream):
+    B, H, Nq, Nk, d, n_splits = FILL
+    splits, wo, wl = binding.splitkv_plan(B, H, Nq, Nk, d, n_splits)
+    assert splits * B * H * Nq * (d + 1) == wo + wl <= 4 << 20
+    q, _, _ = inputs.attn_inputs(B, H, Nq, d, seed=7100 + seed, qk_std=2.0)
+    _, k, v = inputs.attn_inputs(B, H, Nk, d, seed=7200 + seed, qk_std=2.0)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(qd)
+    rc = binding.fa_fwd_splitkv_noalloc_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(),
+                                            o.data_ptr(), None, B, H, Nq, Nk, d, 0.1, False,
+                                            n_splits, stream)
+    assert rc == binding.FA_OK, binding.status_string(rc)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+
+
 @pytest.mark.parametrize("B,H,Nq,Nk,d,causal,n_splits", CASES, ids=lambda x: str(x))
 def test_noalloc_matches_workspace_entry_point_twice(B, H, Nq, Nk, d, causal, n_splits):
     assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
@@ -32,6 +55,7 @@ def test_noalloc_matches_workspace_entry_point_twice(B, H, Nq, Nk, d, causal, n_
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):
+        _fill_scratch_with_another_call(seed=call, stream=stream)
         o = torch.full_like(qd, float("nan"))
         lse = torch.full((B, H, Nq), float("nan"), device="cuda")
         rc = binding.fa_fwd_splitkv_noalloc_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(),
