@@ -77,6 +77,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kHalfBytes = 128 * 128;         // one 64-column half of a 128-row bf16 tile
 constexpr uint64_t kDrainNs = 1000000000ull;  // drain waits: at least 1 s
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
+// When the reference max moves, it moves to the tile's max plus this headroom (log2 units), so
+// that a row whose max keeps climbing (large logits) moves it rarely: only once the max has
+// climbed by the headroom plus the threshold.  Every share stays <= 2^threshold as before; the
+// shares of the row max start at 2^-headroom, far above the bottom of the fp32 / bf16 range.
+constexpr float kRescaleHeadroom = 24.0f;
 constexpr uint32_t kBarHandOff = 1;  // named barriers 1, 2: reference max of tile J -> J+1
 constexpr uint32_t kBarTeardown = 3; // named barrier 3: TMEM no longer used (warps 0-9, 12-15)
 constexpr uint32_t kTeardownThreads = 448;
@@ -824,8 +829,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 stage = 1;
                 // Move the reference only when this tile's max exceeds it by more than the
-                // threshold (always on the first finite tile: -inf gives +inf > threshold).
-                const float m_new = (mx - m_prev > kRescaleThreshold) ? mx : m_prev;
+                // threshold (always on the first finite tile: -inf gives +inf > threshold),
+                // and then past the tile's max by the headroom.
+                const float m_new =
+                    (mx - m_prev > kRescaleThreshold) ? mx + kRescaleHeadroom : m_prev;
                 if (J + 1 < J_total) {
                     bars->mref[J & 1][r] = m_new;
                     named_bar_arrive(kBarHandOff + (J & 1), 256);
