@@ -134,6 +134,11 @@ struct Cfg {
     static constexpr int kBars = kMsk + (M ? kStages * kMskBytes : 0);
     static constexpr int kBytes = kBars + static_cast<int>(sizeof(Bars));
     static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
+    // Waits that let the waiting thread sleep until the phase completes instead of polling:
+    // polling takes issue slots from the warps sharing the SMSP.  Measured per head dimension
+    // (the MMA issuers' waits at d = 128: +2.5-3 %; the softmax's at d = 64: +2 %).
+    static constexpr bool kSleepMma = D == 128;
+    static constexpr bool kSleepSoftmax = D == 64;
     static constexpr int kP = D == 64 ? 2 : 1;      // P buffers
     static constexpr int kQ = D == 64 ? 2 : 1;      // Q buffers
     static constexpr uint32_t kTmemS = 0;           // S0, S1: 128 columns each
@@ -162,8 +167,9 @@ __device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
 
 // Wait until O += P(k) V has finished.  Callers guarantee that P(k-4) V has finished and that
 // P(k+4) V cannot have, so the parity of completion k >> 2 of barrier k & 3 is unambiguous.
-__device__ __forceinline__ bool pv_wait(Bars* bars, int k, uint64_t timeout_ns) {
-    return warp_wait(&bars->pv_done[k & 3], (k >> 2) & 1, timeout_ns);
+__device__ __forceinline__ bool pv_wait(Bars* bars, int k, uint64_t timeout_ns,
+                                        bool sleep = false) {
+    return warp_wait(&bars->pv_done[k & 3], (k >> 2) & 1, timeout_ns, sleep);
 }
 
 __device__ __forceinline__ void record_timeout(int where) {
@@ -623,9 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int qb = qi % C::kQ;
                     const uint32_t tQ = tmem + C::kTmemQ + qb * (D / 2);
                     int s = e % S_;
-                    if ((qi >= C::kQ &&
-                         !mbar_wait(&bars->q_free[qb], ((qi - C::kQ) / C::kQ) & 1, timeout_ns)) ||
-                        !mbar_wait(&bars->k_full[s], (e / S_) & 1, timeout_ns)) {
+                    if ((qi >= C::kQ && !mbar_wait(&bars->q_free[qb], ((qi - C::kQ) / C::kQ) & 1,
+                                                   timeout_ns, C::kSleepMma)) ||
+                        !mbar_wait(&bars->k_full[s], (e / S_) & 1, timeout_ns, C::kSleepMma)) {
                         record_timeout(3);
                         ok = false;
                         break;
@@ -646,9 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // S(J) overwrites S(J-2): its group must have read it.
                         s = e % S_;
                         const int b = J & 1;
-                        if ((J >= 2 &&
-                             !mbar_wait(&bars->s_free[b], ((J >> 1) - 1) & 1, timeout_ns)) ||
-                            !mbar_wait(&bars->k_full[s], (e / S_) & 1, timeout_ns)) {
+                        if ((J >= 2 && !mbar_wait(&bars->s_free[b], ((J >> 1) - 1) & 1, timeout_ns,
+                                                  C::kSleepMma)) ||
+                            !mbar_wait(&bars->k_full[s], (e / S_) & 1, timeout_ns, C::kSleepMma)) {
                             record_timeout(5);
                             ok = false;
                             break;
@@ -691,15 +697,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (w.n_kv == 0) continue;
                     // The first P V of an item overwrites O: the epilogue must have read the
                     // previous item's.
-                    if (qi >= 1 && !mbar_wait(&bars->o_free, (qi - 1) & 1, timeout_ns)) {
+                    if (qi >= 1 &&
+                        !mbar_wait(&bars->o_free, (qi - 1) & 1, timeout_ns, C::kSleepMma)) {
                         record_timeout(11);
                         ok = false;
                         break;
                     }
                     for (int t = 0; t < w.n_kv; ++t, ++J) {
                         // P is what the tile usually waits for; V has landed long before.
-                        if (!mbar_wait(&bars->p_full[pb], pph, timeout_ns) ||
-                            !mbar_wait(&bars->v_full[vs], vph, timeout_ns)) {
+                        if (!mbar_wait(&bars->p_full[pb], pph, timeout_ns, C::kSleepMma) ||
+                            !mbar_wait(&bars->v_full[vs], vph, timeout_ns, C::kSleepMma)) {
                             record_timeout(6);
                             ok = false;
                             break;
@@ -766,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;  // 0: before tile J's consumer pass, 1: before its producer pass
             for (; ok && J < J0 + n; J += 2, stage = 0) {
                 const int t = J - J0;  // tile within the item
-                if (!warp_wait(&bars->s_full[g], (J >> 1) & 1, timeout_ns)) {
+                if (!warp_wait(&bars->s_full[g], (J >> 1) & 1, timeout_ns, C::kSleepSoftmax)) {
                     record_timeout(8);
                     ok = false;
                     break;
@@ -867,14 +874,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_last = m_new;
                 // P buffer pb was last read by P(J - kP) V.
                 const int pb = J % C::kP;
-                if (J >= C::kP && !pv_wait(bars, J - C::kP, timeout_ns)) {
+                if (J >= C::kP && !pv_wait(bars, J - C::kP, timeout_ns, C::kSleepSoftmax)) {
                     record_timeout(9);
                     ok = false;
                     break;
                 }
                 // The reference moved: O must be rescaled after P(J-1) V and before P(J) V.
                 if (t >= 1 && __any_sync(0xffffffffu, alpha_o != 1.f)) {
-                    if (!pv_wait(bars, J - 1, timeout_ns)) {
+                    if (!pv_wait(bars, J - 1, timeout_ns, C::kSleepSoftmax)) {
                         record_timeout(14);
                         ok = false;
                         break;
