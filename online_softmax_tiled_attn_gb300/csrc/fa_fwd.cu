@@ -106,6 +106,7 @@ struct Bars {
     // each wait exact (see pv_wait).
     uint64_t pv_done[4];
     uint64_t q_free[2];   // the last S of item qi has read Q buffer qi % kQ (tcgen05.commit)
+    uint64_t q_full[2];   // d = 64: item qi's Q tile has landed in shared-memory buffer qi & 1
     uint64_t o_full;      // every P V of a non-empty item finished (tcgen05.commit)
     uint64_t o_free;      // O of a non-empty item read by the epilogue (4 warps)
     // Both softmax groups have written their final (m, l) of item k into fin[k % kFinSlots]
@@ -124,27 +125,39 @@ struct Bars {
 
 template <int D, bool M = false>  // M: the kernel reads an explicit mask
 struct Cfg {
+    // d = 64: the two softmax groups are independent workers.  Each keeps its own running max,
+    // running sum and O accumulator over the key tiles it takes, and the epilogue combines the
+    // two partial states with the two-worker merge; no reference max passes between them.
+    // Two accumulators need 64 more TMEM columns, so the Q tile stays in shared memory and S
+    // is an SS product.  (d = 128 has no room for a second accumulator.)
+    static constexpr bool kIndep = D == 64;
     static constexpr int kHalves = D / 64;
     static constexpr int kTileBytes = kHalves * kHalfBytes;  // 128 rows x D bf16
-    static constexpr int kStages = D == 128 ? 3 : 6;         // K ring and V ring depth
+    static constexpr int kStages = D == 128 ? 3 : 5;         // K ring and V ring depth
     static constexpr int kK = 0;
     static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kMsk = kV + kStages * kTileBytes;  // MASK: a key tile's mask bits
+    static constexpr int kQs = kV + kStages * kTileBytes;     // kIndep: two Q tile buffers
+    static constexpr int kMsk = kQs + (kIndep ? 2 * kTileBytes : 0);  // MASK: mask bits
     static constexpr int kMskBytes = kBM * 16;              // 128 query rows x 16 bytes
     static constexpr int kBars = kMsk + (M ? kStages * kMskBytes : 0);
     static constexpr int kBytes = kBars + static_cast<int>(sizeof(Bars));
     static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
     // Waits that let the waiting thread sleep until the phase completes instead of polling:
-    // polling takes issue slots from the warps sharing the SMSP.  Measured per head dimension
-    // (the MMA issuers' waits at d = 128: +2.5-3 %; the softmax's at d = 64: +2 %).
+    // polling takes issue slots from the warps sharing the SMSP.  And the MMA issuers either
+    // run as whole, converged warps with one elected lane issuing (kWarpIssue), or as lane 0
+    // alone.  Measured per head dimension on GB300: at d = 128 converged issue with sleeping
+    // waits is 2-4 % faster; at d = 64 (SS products for S, bound by shared memory) lane-0
+    // issue with polling waits is 4 % faster.
+    static constexpr bool kWarpIssue = D == 128;
     static constexpr bool kSleepMma = D == 128;
-    static constexpr bool kSleepSoftmax = D == 64;
-    static constexpr int kP = D == 64 ? 2 : 1;      // P buffers
-    static constexpr int kQ = D == 64 ? 2 : 1;      // Q buffers
+    static constexpr bool kSleepSoftmax = true;
+    static constexpr int kP = kIndep ? 2 : 1;       // P buffers (kIndep: one per group)
+    static constexpr int kQ = kIndep ? 0 : 1;       // Q buffers in TMEM
+    static constexpr int kOAcc = kIndep ? 2 : 1;    // O accumulators (kIndep: one per group)
     static constexpr uint32_t kTmemS = 0;           // S0, S1: 128 columns each
     static constexpr uint32_t kTmemP = 256;         // P buffers: 64 columns each
-    static constexpr uint32_t kTmemO = kTmemP + 64 * kP;
-    static constexpr uint32_t kTmemQ = kTmemO + D;  // Q buffers: D/2 columns each
+    static constexpr uint32_t kTmemO = kTmemP + 64 * kP;    // O accumulators: D columns each
+    static constexpr uint32_t kTmemQ = kTmemO + kOAcc * D;  // Q buffers: D/2 columns each
     static_assert(kTmemQ + kQ * (D / 2) <= kTmemCols, "TMEM budget");
     static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
     static_assert(kStages <= kMaxStages, "ring depth");
@@ -163,6 +176,43 @@ __device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
     tc_fence_before();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// The MMA issuers' primitives, for a converged warp (W) or for lane 0 alone: the waits (made
+// warp-uniform in the first case), the products and copies, and the commits.
+template <bool W>
+__device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                            bool sleep) {
+    if constexpr (W) return warp_wait(bar, parity, timeout_ns, sleep);
+    else return mbar_wait(bar, parity, timeout_ns, sleep);
+}
+template <bool W>
+__device__ __forceinline__ void issue_commit(uint64_t* bar) {
+    if constexpr (W) umma_commit_warp(bar);
+    else umma_commit(bar);
+}
+template <bool W>
+__device__ __forceinline__ void issue_ss_x4(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                            uint32_t acc) {
+    if constexpr (W) umma_ss_x4_warp(d, a, b, id, acc);
+    else umma_ss_x4(d, a, b, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_ts_x4(uint32_t d, uint32_t a, uint64_t b, uint32_t step,
+                                            uint32_t id, uint32_t acc) {
+    if constexpr (W) umma_ts_x4_warp(d, a, b, step, id, acc);
+    else umma_ts_x4(d, a, b, step, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_ts_x8(uint32_t d, uint32_t a, uint64_t b, uint32_t step,
+                                            uint32_t id, uint32_t acc) {
+    if constexpr (W) umma_ts_x8_warp(d, a, b, step, id, acc);
+    else umma_ts_x8(d, a, b, step, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_tmem_cp(uint32_t taddr, uint64_t desc) {
+    if constexpr (W) tmem_cp_128x256b_warp(taddr, desc);
+    else tmem_cp_128x256b(taddr, desc);
 }
 
 // Wait until O += P(k) V has finished.  Callers guarantee that P(k-4) V has finished and that
@@ -415,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->s_free[b], 4);
             mbar_init(&bars->p_full[b], 4);
             mbar_init(&bars->q_free[b], 1);
+            mbar_init(&bars->q_full[b], 1);
         }
         for (int b = 0; b < 4; ++b) mbar_init(&bars->pv_done[b], 1);
         for (int b = 0; b < kFinSlots; ++b) {
@@ -467,10 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->fin_free[slot]);
             const float M = fmaxf(m0, m1);
-            float lt = 0.f;
-            if (M != -INFINITY)
-                lt = (m0 == -INFINITY ? 0.f : l0 * ex2_approx(m0 - M)) +
-                     (m1 == -INFINITY ? 0.f : l1 * ex2_approx(m1 - M));
+            // The two groups' states relative to M.  A group with nothing (m = -inf: no tile
+            // of the item, or no allowed key in its tiles) weighs 0.
+            const float w0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - M);
+            const float w1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
+            const float lt = l0 * w0 + l1 * w1;
             const bool have = w.n_kv > 0;
             if (have) {
                 if (!warp_wait(&bars->o_full, qi & 1, timeout_ns, true)) {
@@ -485,39 +537,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
             const size_t row = static_cast<size_t>(w.bh) * Nq + q_row;
             const size_t ws_row = static_cast<size_t>(w.split) * prm.BH * Nq + row;
+            // Columns per step: 32 of the shared accumulator, or 16 of each group's (d = 64),
+            // combined with the merge weights, within the epilogue's register budget.
+            constexpr int CW = C::kIndep ? 16 : 32;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                if (have) {
-                    tmem_ld32_sync(tO + c * 32, o);
-                } else {
+            for (int c = 0; c < D / CW; ++c) {
+                float o[CW];
+                if (!have) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    for (int e = 0; e < CW; ++e) o[e] = 0.f;
+                } else if constexpr (C::kIndep) {
+                    uint32_t a[16], b[16];
+                    tmem_ld16x2_sync(tO + c * 16, tO + D + c * 16, a, b);
+                    // A group that weighs 0 may hold another item's sums: never read into O.
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = (w0 != 0.f ? __uint_as_float(a[e]) * w0 : 0.f) +
+                               (w1 != 0.f ? __uint_as_float(b[e]) * w1 : 0.f);
+                } else {
+                    uint32_t a[32];
+                    tmem_ld32_sync(tO + c * 32, a);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(a[e]);
                 }
                 // After the last read of O the next item's first P V may overwrite it.
-                if (have && c == D / 32 - 1) warp_arrive_tc(&bars->o_free);
+                if (have && c == D / CW - 1) warp_arrive_tc(&bars->o_free);
                 if (!store) continue;
                 if (SPLIT) {
-                    float4* dst = reinterpret_cast<float4*>(prm.ws_O + ws_row * D + c * 32);
+                    float4* dst = reinterpret_cast<float4*>(prm.ws_O + ws_row * D + c * CW);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l,
-                                             __uint_as_float(o[4 * v + 1]) * inv_l,
-                                             __uint_as_float(o[4 * v + 2]) * inv_l,
-                                             __uint_as_float(o[4 * v + 3]) * inv_l);
+                    for (int v = 0; v < CW / 4; ++v)
+                        dst[v] = make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l,
+                                             o[4 * v + 2] * inv_l, o[4 * v + 3] * inv_l);
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(prm.O + row * D + c * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(prm.O + row * D + c * CW);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
+                    for (int v = 0; v < CW / 8; ++v)
                         dst[v] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * v]) * inv_l,
-                                        __uint_as_float(o[8 * v + 1]) * inv_l),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l,
-                                        __uint_as_float(o[8 * v + 3]) * inv_l),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l,
-                                        __uint_as_float(o[8 * v + 5]) * inv_l),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l,
-                                        __uint_as_float(o[8 * v + 7]) * inv_l));
+                            pack_bf16x2(o[8 * v] * inv_l, o[8 * v + 1] * inv_l),
+                            pack_bf16x2(o[8 * v + 2] * inv_l, o[8 * v + 3] * inv_l),
+                            pack_bf16x2(o[8 * v + 4] * inv_l, o[8 * v + 5] * inv_l),
+                            pack_bf16x2(o[8 * v + 6] * inv_l, o[8 * v + 7] * inv_l));
                 }
             }
             if (store) {
@@ -534,6 +594,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_arrive(kBarTeardown, kTeardownThreads);
     } else if (warp >= kMmaWarp) {
         setmaxnreg_dec<40>();
+        // The MMA issuers' waits (see Cfg::kWarpIssue and Cfg::kSleepMma).
+        auto iwait = [&](uint64_t* bar, uint32_t parity) {
+            return issuer_wait<C::kWarpIssue>(bar, parity, timeout_ns, C::kSleepMma);
+        };
+        constexpr bool W = C::kWarpIssue;
         if (warp == kTmaWarp) {
             // ------------------------------------------------------ TMA: Q and K tiles, K ring
             if (lane == 0) {
@@ -542,35 +607,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tmV);
                 if constexpr (MASK != 0) tma_prefetch_desc(&tmM.map);
                 constexpr uint32_t kTx = C::kTileBytes;
-                int e = 0;  // K-ring entries issued
-                bool ok = true;
-                for (int k = 0; ok; ++k) {
-                    const int idx = cta_item(k, prm.n_items);
-                    if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
-                    // t = -1: the item's Q tile, then its key tiles (key tile kt).
-                    TileCursor tiles(w);
-                    int kt = tiles.next();
-                    for (int t = w.n_kv > 0 ? -1 : 0; t < w.n_kv; ++t, ++e) {
-                        const int s = e % S_;
-                        if (e >= S_ &&
-                            !mbar_wait(&bars->k_empty[s], ((e / S_) - 1) & 1, timeout_ns, true)) {
+                if constexpr (C::kIndep) {
+                    // Each non-empty item's Q tile into shared-memory buffer qi & 1, once the
+                    // last S of item qi - 2 has read that buffer; its K tiles into the K ring.
+                    int e = 0, qi = 0;
+                    bool ok = true;
+                    for (int k = 0; ok; ++k) {
+                        const int idx = cta_item(k, prm.n_items);
+                        if (idx < 0) break;
+                        const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
+                        if (w.n_kv == 0) continue;
+                        const int qb = qi & 1;
+                        if (qi >= 2 && !mbar_wait(&bars->q_free[qb], ((qi >> 1) - 1) & 1,
+                                                  timeout_ns, true)) {
                             record_timeout(1);
-                            ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&bars->k_full[s], kTx);
-                        const CUtensorMap* map = t < 0 ? &tmQ : &tmK;
-                        const int row =
-                            t < 0 ? w.q_tile * kBM : (MASK == 2 ? kt : w.kt0 + t) * kBN;
-                        const int head = t < 0 ? w.bh : w.kvh;
-                        for (int h = 0; h < C::kHalves; ++h)
-                            tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, map,
-                                        &bars->k_full[s], h * 64, row, head);
-                        if (t >= 0) kt = MASK == 2 ? tiles.next() : kt + 1;
+                        mbar_arrive_expect_tx(&bars->q_full[qb], kTx);
+                        tma_load_3d(smem + C::kQs + qb * C::kTileBytes, &tmQ, &bars->q_full[qb], 0,
+                                    w.q_tile * kBM, w.bh);
+                        ++qi;
+                        TileCursor tiles(w);
+                        for (int t = 0; t < w.n_kv; ++t, ++e) {
+                            const int kt = tiles.next();
+                            const int s = e % S_;
+                            if (e >= S_ && !mbar_wait(&bars->k_empty[s], ((e / S_) - 1) & 1,
+                                                      timeout_ns, true)) {
+                                record_timeout(1);
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&bars->k_full[s], kTx);
+                            tma_load_3d(smem + C::kK + s * C::kTileBytes, &tmK, &bars->k_full[s],
+                                        0, kt * kBN, w.kvh);
+                        }
                     }
+                    drain_ring(bars->k_full, S_, e, timeout_ns);
+                    drain_ring(bars->q_full, 2, qi, timeout_ns);
+                } else {
+                    int e = 0;  // K-ring entries issued
+                    bool ok = true;
+                    for (int k = 0; ok; ++k) {
+                        const int idx = cta_item(k, prm.n_items);
+                        if (idx < 0) break;
+                        const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
+                        // t = -1: the item's Q tile, then its key tiles (key tile kt).
+                        TileCursor tiles(w);
+                        int kt = tiles.next();
+                        for (int t = w.n_kv > 0 ? -1 : 0; t < w.n_kv; ++t, ++e) {
+                            const int s = e % S_;
+                            if (e >= S_ && !mbar_wait(&bars->k_empty[s], ((e / S_) - 1) & 1,
+                                                      timeout_ns, true)) {
+                                record_timeout(1);
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&bars->k_full[s], kTx);
+                            const CUtensorMap* map = t < 0 ? &tmQ : &tmK;
+                            const int row =
+                                t < 0 ? w.q_tile * kBM : (MASK == 2 ? kt : w.kt0 + t) * kBN;
+                            const int head = t < 0 ? w.bh : w.kvh;
+                            for (int h = 0; h < C::kHalves; ++h)
+                                tma_load_3d(smem + C::kK + s * C::kTileBytes + h * kHalfBytes, map,
+                                            &bars->k_full[s], h * 64, row, head);
+                            if (t >= 0) kt = MASK == 2 ? tiles.next() : kt + 1;
+                        }
+                    }
+                    drain_ring(bars->k_full, S_, e, timeout_ns);
                 }
-                drain_ring(bars->k_full, S_, e, timeout_ns);
             }
         } else if (warp == kTmaVWarp) {
             // ------------------------------------------------------ TMA: V tiles, V ring
@@ -614,69 +718,108 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------ MMA: S = Q K^T
-            if (lane == 0) {
+            if (C::kWarpIssue || lane == 0) {  // a converged warp, or lane 0
                 constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0);
-                int e = 0, J = 0, qi = 0;
-                bool ok = true;
-                for (int k = 0; ok; ++k) {
-                    const int idx = cta_item(k, prm.n_items);
-                    if (idx < 0) break;
-                    const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
-                    if (w.n_kv == 0) continue;
-                    // The item's Q tile: K ring -> Q buffer qb in TMEM (tcgen05.cp, ordered
-                    // before the MMAs below), once the S of item qi - kQ, the buffer's
-                    // previous reader, has finished.
-                    const int qb = qi % C::kQ;
-                    const uint32_t tQ = tmem + C::kTmemQ + qb * (D / 2);
-                    int s = e % S_;
-                    if ((qi >= C::kQ && !mbar_wait(&bars->q_free[qb], ((qi - C::kQ) / C::kQ) & 1,
-                                                   timeout_ns, C::kSleepMma)) ||
-                        !mbar_wait(&bars->k_full[s], (e / S_) & 1, timeout_ns, C::kSleepMma)) {
-                        record_timeout(3);
-                        ok = false;
-                        break;
+                if constexpr (C::kIndep) {
+                    // SS products: A = the item's Q tile in shared-memory buffer qi & 1, B = the
+                    // K tile, both K-major and 128-byte swizzled; four K16 steps (d = 64).
+                    int e = 0, J = 0, qi = 0;
+                    bool ok = true;
+                    for (int k = 0; ok; ++k) {
+                        const int idx = cta_item(k, prm.n_items);
+                        if (idx < 0) break;
+                        const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
+                        if (w.n_kv == 0) continue;
+                        const int qb = qi & 1;
+                        if (!iwait(&bars->q_full[qb], (qi >> 1) & 1)) {
+                            record_timeout(3);
+                            break;
+                        }
+                        const uint64_t qdesc =
+                            smem_desc_sw128(smem_u32(smem + C::kQs + qb * C::kTileBytes), 16, 1024);
+                        for (int t = 0; t < w.n_kv; ++t, ++J, ++e) {
+                            // S(J) overwrites S(J-2): its group must have read it.
+                            const int s = e % S_;
+                            const int b = J & 1;
+                            if ((J >= 2 && !iwait(&bars->s_free[b], ((J >> 1) - 1) & 1)) ||
+                                !iwait(&bars->k_full[s], (e / S_) & 1)) {
+                                record_timeout(5);
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_ss_x4<W>(tmem + C::kTmemS + b * 128, qdesc,
+                                           smem_desc_sw128(sK + s * C::kTileBytes, 16, 1024),
+                                           idS, 0u);
+                            issue_commit<W>(&bars->s_full[b]);
+                            issue_commit<W>(&bars->k_empty[s]);
+                        }
+                        if (ok) issue_commit<W>(&bars->q_free[qb]);
+                        ++qi;
                     }
-                    tc_fence_after();
-                    {
-                        const uint32_t qs = sK + s * C::kTileBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            tmem_cp_128x256b(tQ + kk * 8,
-                                             smem_desc_sw128(qs + (kk >> 2) * kHalfBytes +
-                                                                 (kk & 3) * 32,
-                                                             16, 1024));
-                    }
-                    umma_commit(&bars->k_empty[s]);
-                    ++e;
-                    for (int t = 0; t < w.n_kv; ++t, ++J, ++e) {
-                        // S(J) overwrites S(J-2): its group must have read it.
-                        s = e % S_;
-                        const int b = J & 1;
-                        if ((J >= 2 && !mbar_wait(&bars->s_free[b], ((J >> 1) - 1) & 1, timeout_ns,
-                                                  C::kSleepMma)) ||
-                            !mbar_wait(&bars->k_full[s], (e / S_) & 1, timeout_ns, C::kSleepMma)) {
-                            record_timeout(5);
+                } else {
+                    int e = 0, J = 0, qi = 0;
+                    bool ok = true;
+                    for (int k = 0; ok; ++k) {
+                        const int idx = cta_item(k, prm.n_items);
+                        if (idx < 0) break;
+                        const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
+                        if (w.n_kv == 0) continue;
+                        // The item's Q tile: K ring -> Q buffer qb in TMEM (tcgen05.cp, ordered
+                        // before the MMAs below), once the S of item qi - kQ, the buffer's
+                        // previous reader, has finished.
+                        const int qb = qi % C::kQ;
+                        const uint32_t tQ = tmem + C::kTmemQ + qb * (D / 2);
+                        int s = e % S_;
+                        if ((qi >= C::kQ &&
+                             !iwait(&bars->q_free[qb], ((qi - C::kQ) / C::kQ) & 1)) ||
+                            !iwait(&bars->k_full[s], (e / S_) & 1)) {
+                            record_timeout(3);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        // B_k: the K tile's 16-element slice k (32 bytes apart within each
-                        // 64-column half of the K-major, 128-byte swizzled tile).
-                        const uint32_t kb = sK + s * C::kTileBytes;
+                        {
+                            const uint32_t qs = sK + s * C::kTileBytes;
 #pragma unroll
-                        for (int h = 0; h < C::kHalves; ++h)
-                            umma_ts_x4(tmem + C::kTmemS + b * 128, tQ + h * 32,
-                                       smem_desc_sw128(kb + h * kHalfBytes, 16, 1024), 32 / 16,
-                                       idS, h > 0 ? 1u : 0u);
-                        umma_commit(&bars->s_full[b]);
-                        umma_commit(&bars->k_empty[s]);
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                issue_tmem_cp<W>(tQ + kk * 8,
+                                                 smem_desc_sw128(qs + (kk >> 2) * kHalfBytes +
+                                                                     (kk & 3) * 32,
+                                                                 16, 1024));
+                        }
+                        issue_commit<W>(&bars->k_empty[s]);
+                        ++e;
+                        for (int t = 0; t < w.n_kv; ++t, ++J, ++e) {
+                            // S(J) overwrites S(J-2): its group must have read it.
+                            s = e % S_;
+                            const int b = J & 1;
+                            if ((J >= 2 && !iwait(&bars->s_free[b], ((J >> 1) - 1) & 1)) ||
+                                !iwait(&bars->k_full[s], (e / S_) & 1)) {
+                                record_timeout(5);
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            // B_k: the K tile's 16-element slice k (32 bytes apart within each
+                            // 64-column half of the K-major, 128-byte swizzled tile).
+                            const uint32_t kb = sK + s * C::kTileBytes;
+#pragma unroll
+                            for (int h = 0; h < C::kHalves; ++h)
+                                issue_ts_x4<W>(tmem + C::kTmemS + b * 128, tQ + h * 32,
+                                               smem_desc_sw128(kb + h * kHalfBytes, 16, 1024),
+                                               32 / 16, idS, h > 0 ? 1u : 0u);
+                            issue_commit<W>(&bars->s_full[b]);
+                            issue_commit<W>(&bars->k_empty[s]);
+                        }
+                        if (ok) issue_commit<W>(&bars->q_free[qb]);
+                        ++qi;
                     }
-                    if (ok) umma_commit(&bars->q_free[qb]);
-                    ++qi;
                 }
                 // Drain: no MMA of this thread may still write TMEM when it is freed.
-                umma_commit(&bars->mma_done);
-                mbar_wait(&bars->mma_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
+                issue_commit<W>(&bars->mma_done);
+                issuer_wait<W>(&bars->mma_done, 0,
+                                           timeout_ns > kDrainNs ? timeout_ns : kDrainNs, false);
             }
             __syncwarp();
             named_bar_sync(kBarTeardown, kTeardownThreads);
@@ -684,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_dealloc(tmem, kTmemCols);
         } else if (warp == kMmaPvWarp) {
             // ------------------------------------------------------ MMA: O += P V
-            if (lane == 0) {
+            if (C::kWarpIssue || lane == 0) {  // a converged warp, or lane 0
                 constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 1);
                 int J = 0, qi = 0;
                 int vs = 0, vph = 0;  // V ring slot of tile J and its phase
@@ -698,34 +841,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // The first P V of an item overwrites O: the epilogue must have read the
                     // previous item's.
                     if (qi >= 1 &&
-                        !mbar_wait(&bars->o_free, (qi - 1) & 1, timeout_ns, C::kSleepMma)) {
+                        !iwait(&bars->o_free, (qi - 1) & 1)) {
                         record_timeout(11);
                         ok = false;
                         break;
                     }
                     for (int t = 0; t < w.n_kv; ++t, ++J) {
                         // P is what the tile usually waits for; V has landed long before.
-                        if (!mbar_wait(&bars->p_full[pb], pph, timeout_ns, C::kSleepMma) ||
-                            !mbar_wait(&bars->v_full[vs], vph, timeout_ns, C::kSleepMma)) {
+                        if (!iwait(&bars->p_full[pb], pph) ||
+                            !iwait(&bars->v_full[vs], vph)) {
                             record_timeout(6);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         // B_k: rows 16k..16k+15 of the V tile (MN-major), 2048 bytes apart.
-                        umma_ts_x8(tmem + C::kTmemO, tmem + C::kTmemP + pb * 64,
-                                   smem_desc_sw128(sV + vs * C::kTileBytes, kHalfBytes, 1024),
-                                   2048 / 16, idO, t > 0 ? 1u : 0u);
-                        umma_commit(&bars->pv_done[J & 3]);
-                        umma_commit(&bars->v_empty[vs]);
+                        // With one accumulator per group (d = 64), tile J goes into the
+                        // accumulator of group J & 1, and each group's first tile of the item
+                        // (t = 0 or 1) overwrites it.
+                        const uint32_t acc_o = C::kIndep ? C::kTmemO + (J & 1) * D : C::kTmemO;
+                        const bool first = C::kIndep ? t < 2 : t == 0;
+                        issue_ts_x8<W>(tmem + acc_o, tmem + C::kTmemP + pb * 64,
+                                       smem_desc_sw128(sV + vs * C::kTileBytes, kHalfBytes, 1024),
+                                       2048 / 16, idO, first ? 0u : 1u);
+                        issue_commit<W>(&bars->pv_done[J & 3]);
+                        issue_commit<W>(&bars->v_empty[vs]);
                         if (++vs == S_) { vs = 0; vph ^= 1; }
                         if (++pb == C::kP) { pb = 0; pph ^= 1; }
                     }
-                    if (ok) umma_commit(&bars->o_full);  // every P V of the item, for the epilogue
+                    // every P V of the item, for the epilogue
+                    if (ok) issue_commit<W>(&bars->o_full);
                     ++qi;
                 }
-                umma_commit(&bars->mma_pv_done);
-                mbar_wait(&bars->mma_pv_done, 0, timeout_ns > kDrainNs ? timeout_ns : kDrainNs);
+                issue_commit<W>(&bars->mma_pv_done);
+                issuer_wait<W>(&bars->mma_pv_done, 0,
+                                           timeout_ns > kDrainNs ? timeout_ns : kDrainNs, false);
             }
             __syncwarp();
             tc_fence_before();
@@ -738,7 +888,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x & 127;  // row in the tile == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_addr + C::kTmemS + g * 128;
-        const uint32_t tO = tmem + lane_addr + C::kTmemO;
+        // This group's O accumulator (d = 64: one per group; d = 128: the shared one).
+        const uint32_t tO = tmem + lane_addr + C::kTmemO + (C::kIndep ? g * D : 0);
         const float scale_log2 = prm.scale_log2;
         // Key tiles of this CTA over all its items: the hand-off of the reference max runs
         // through all of them (a tile that starts an item ignores what it receives), so that
@@ -828,9 +979,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < w; ++u) m16[u] = fmaxf(m16[u], m16[u + w]);
                 const float mx = m16[0] * scale_log2;
                 // Reference max after tile J-1 (the other group's), handed over per row; the
-                // first tile of an item starts from -inf.
+                // first tile of an item starts from -inf.  Independent groups (d = 64) keep
+                // their own reference instead.
                 float m_prev = -INFINITY;
-                if (J >= 1) {
+                if constexpr (C::kIndep) {
+                    m_prev = m_last;
+                } else if (J >= 1) {
                     named_bar_sync(kBarHandOff + ((J - 1) & 1), 256);
                     if (t >= 1) m_prev = bars->mref[(J - 1) & 1][r];
                 }
@@ -840,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // and then past the tile's max by the headroom.
                 const float m_new =
                     (mx - m_prev > kRescaleThreshold) ? mx + kRescaleHeadroom : m_prev;
-                if (J + 1 < J_total) {
+                if (!C::kIndep && J + 1 < J_total) {
                     bars->mref[J & 1][r] = m_new;
                     named_bar_arrive(kBarHandOff + (J & 1), 256);
                 }
@@ -879,9 +1033,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                // The reference moved: O must be rescaled after P(J-1) V and before P(J) V.
-                if (t >= 1 && __any_sync(0xffffffffu, alpha_o != 1.f)) {
-                    if (!pv_wait(bars, J - 1, timeout_ns, C::kSleepSoftmax)) {
+                // The reference moved: O must be rescaled after the last P V into it and
+                // before P(J) V: P(J-1) V for the shared accumulator; with one accumulator per
+                // group, P(J-2) V (waited for above), except on the group's first tile of the
+                // item, whose P V overwrites it.
+                if (t >= (C::kIndep ? 2 : 1) && __any_sync(0xffffffffu, alpha_o != 1.f)) {
+                    if (!C::kIndep && !pv_wait(bars, J - 1, timeout_ns, C::kSleepSoftmax)) {
                         record_timeout(14);
                         ok = false;
                         break;
@@ -902,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 warp_arrive_tc(&bars->p_full[pb]);
             }
             // Make up the hand-off passes a stop left out, in the same order.
-            for (; J < J0 + n; J += 2, stage = 0) {
+            for (; !C::kIndep && J < J0 + n; J += 2, stage = 0) {
                 if (stage == 0 && J >= 1) named_bar_sync(kBarHandOff + ((J - 1) & 1), 256);
                 if (stage <= 1 && J + 1 < J_total)
                     named_bar_arrive(kBarHandOff + (J & 1), 256);

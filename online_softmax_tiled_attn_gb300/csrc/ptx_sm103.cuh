@@ -304,6 +304,77 @@ __device__ __forceinline__ void umma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// ------------------------------------------------------------------------------------------
+// The same issue paths for a whole, converged warp: every lane runs the issuing loop (so the
+// operands are warp-uniform values) and the lane that elect.sync picks issues each
+// instruction.  One warp issues M128 N64 K16 products this way at the tensor core's full rate
+// (32 clocks each); a loop run by lane 0 alone reaches one per ~49 clocks.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void umma_ss_x4_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, %4, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_x4_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t b_step16, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t.reg .b64 st;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 q, %5, %5;\n\t"
+        "cvt.u64.u32 st, %3;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, st;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.s64 b, b, st;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(b_step16), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_x8_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t b_step16, uint32_t idesc,
+                                                uint32_t accumulate) {
+    umma_ts_x4_warp(d_tmem, a_tmem, b_desc, b_step16, idesc, accumulate);
+    umma_ts_x4_warp(d_tmem, a_tmem + 32, b_desc + 4ull * b_step16, b_step16, idesc, 1u);
+}
+
+__device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t s_desc) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr), "l"(s_desc)
+        : "memory");
+}
+
+// Arrives once on `bar` when all tcgen05 operations issued so far by the elected lane end.
+// Every MMA of a warp that uses these helpers is issued by the same elected lane (elect.sync
+// picks the lowest active lane, and the loops run fully converged).
+__device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
 // Asynchronous copy of a 128-row x 256-bit matrix from shared memory (described by a matrix
 // descriptor, like an MMA operand) into TMEM lanes 0-127, 8 columns from `taddr`.  Ordered
 // before the tcgen05.mma instructions that the same thread issues after it.
