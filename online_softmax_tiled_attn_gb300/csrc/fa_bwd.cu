@@ -47,6 +47,10 @@ constexpr int kHalf = 128 * 128;  // bytes of one 64-column half of a 128-row bf
 constexpr int kSoftWarps = 16;    // warps 0-15
 constexpr int kTmaWarp = 16;
 constexpr int kMmaWarp = 17;
+// The MMA warp runs its loop as a whole, converged warp and one elected lane issues each
+// product and commit: the operands are then warp-uniform values, and one warp issues short
+// products at the tensor core's pace (a loop run by lane 0 alone issues one per ~49-75 clocks).
+constexpr bool kWarpIssue = true;
 constexpr int kThreads = 18 * 32;
 constexpr uint64_t kDrainNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -89,10 +93,11 @@ __device__ __forceinline__ void grid_place(const BwdParams& prm, int& bh, int& p
 template <int D>
 __device__ __forceinline__ void mma_ss_kmajor(uint32_t d_tmem, uint32_t sA, uint32_t sB,
                                               uint32_t idesc) {
-    umma_ss_x4(d_tmem, smem_desc_sw128(sA, 16, 1024), smem_desc_sw128(sB, 16, 1024), idesc, 0u);
+    issue_ss_x4<kWarpIssue>(d_tmem, smem_desc_sw128(sA, 16, 1024),
+                            smem_desc_sw128(sB, 16, 1024), idesc, 0u);
     if constexpr (D == 128)
-        umma_ss_x4(d_tmem, smem_desc_sw128(sA + kHalf, 16, 1024),
-                   smem_desc_sw128(sB + kHalf, 16, 1024), idesc, 1u);
+        issue_ss_x4<kWarpIssue>(d_tmem, smem_desc_sw128(sA + kHalf, 16, 1024),
+                                smem_desc_sw128(sB + kHalf, 16, 1024), idesc, 1u);
 }
 
 // Rows [64 half, 64 half + 64) of the walked dimension of a TS product whose A operand (bf16
@@ -100,8 +105,9 @@ __device__ __forceinline__ void mma_ss_kmajor(uint32_t d_tmem, uint32_t sA, uint
 // 16 walked rows of K16 step k at columns 16 k .. 16 k + 7); B is the MN-major tile at sB.
 __device__ __forceinline__ void mma_ts_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB,
                                             int half, uint32_t idesc, uint32_t accumulate) {
-    umma_ts_x4_stride16(d_tmem, a_tmem + half * 64,
-                        smem_desc_sw128(sB + half * 4 * 2048, kHalf, 1024), idesc, accumulate);
+    issue_ts_x4_stride16<kWarpIssue>(d_tmem, a_tmem + half * 64,
+                                     smem_desc_sw128(sB + half * 4 * 2048, kHalf, 1024), idesc,
+                                     accumulate);
 }
 
 // Writes N fp32 values (times sc) of one row as bf16.
@@ -243,8 +249,9 @@ __device__ __forceinline__ void mma_ts_kmajor(uint32_t d_tmem, uint32_t a_tmem, 
                                               uint32_t idesc) {
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
-        umma_ts_x4(d_tmem, a_tmem + h * 32, smem_desc_sw128(sB + h * kHalf, 16, 1024), 32 / 16,
-                   idesc, h > 0 ? 1u : 0u);
+        issue_ts_x4<kWarpIssue>(d_tmem, a_tmem + h * 32,
+                                smem_desc_sw128(sB + h * kHalf, 16, 1024), 32 / 16, idesc,
+                                h > 0 ? 1u : 0u);
 }
 
 template <int D, bool CAUSAL>
@@ -331,7 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&bars[kKvBarFull + (issued - 1) % NS], ((issued - 1) / NS) & 1, drain, true);
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+        if (kWarpIssue || lane == 0) {  // a converged warp, or lane 0
+            auto iwait = [&](uint64_t* bar, uint32_t parity) {
+                return issuer_wait<kWarpIssue>(bar, parity, tmo);
+            };
             // ---- tensor-core products -------------------------------------------------------
             // Order per query tile t (buffer b = t % 2): dP^T once S^T is read, S^T of tile
             // t + 1 into the other buffer (once tile t - 1's dV, dK are done with it), then
@@ -342,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idT = idesc_bf16_f32_ab(kTile, D, 0, 1);
             const uint32_t tK = tmem + C::kTmemK, tV = tmem + C::kTmemV;
             const uint32_t sK = smem_u32(smem + C::kK), sV = smem_u32(smem + C::kV);
-            bool ok = mbar_wait(&bars[kKvBarKV], 0, tmo);
+            bool ok = iwait(&bars[kKvBarKV], 0);
             int where = 21;
             if (ok && C::kKvInTmem) {
                 tc_fence_after();
@@ -350,12 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tmem_cp_128x256b(tK + kk * 8, smem_desc_sw128(sKs + off, 16, 1024));
-                    tmem_cp_128x256b(tV + kk * 8, smem_desc_sw128(sVs + off, 16, 1024));
+                    issue_tmem_cp<kWarpIssue>(tK + kk * 8, smem_desc_sw128(sKs + off, 16, 1024));
+                    issue_tmem_cp<kWarpIssue>(tV + kk * 8, smem_desc_sw128(sVs + off, 16, 1024));
                 }
-                umma_commit(&bars[kKvBarKVCopied]);
+                issue_commit<kWarpIssue>(&bars[kKvBarKVCopied]);
             }
-            if (ok) ok = mbar_wait(&bars[kKvBarFull], 0, tmo);
+            if (ok) ok = iwait(&bars[kKvBarFull], 0);
             if (ok) {
                 tc_fence_after();
                 const uint32_t sQ0 = smem_u32(smem + C::kQ);
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ts_kmajor<D>(tmem + C::kTmemBuf, tK, sQ0, idS);
                 else
                     mma_ss_kmajor<D>(tmem + C::kTmemBuf, sK, sQ0, idS);
-                umma_commit(&bars[kKvBarSFull]);
+                issue_commit<kWarpIssue>(&bars[kKvBarSFull]);
             }
             for (int t = 0; ok && t < n_it; ++t) {
                 const int b = t & 1, s = t % NS, s1 = (t + 1) % NS;
@@ -371,18 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sQ = smem_u32(smem + C::kQ + s * C::kTileBytes);
                 const uint32_t sG = smem_u32(smem + C::kG + s * C::kTileBytes);
                 where = 22;
-                if (!(ok = mbar_wait(&bars[kKvBarRead], t & 1, tmo))) break;
+                if (!(ok = iwait(&bars[kKvBarRead], t & 1))) break;
                 tc_fence_after();
                 if constexpr (C::kKvInTmem)
                     mma_ts_kmajor<D>(buf, tV, sG, idS);
                 else
                     mma_ss_kmajor<D>(buf, sV, sG, idS);
-                umma_commit(&bars[kKvBarDpFull]);
+                issue_commit<kWarpIssue>(&bars[kKvBarDpFull]);
                 if (t + 1 < n_it) {
                     where = 24;
-                    if (!(ok = mbar_wait(&bars[kKvBarFull + s1], ((t + 1) / NS) & 1, tmo))) break;
+                    if (!(ok = iwait(&bars[kKvBarFull + s1], ((t + 1) / NS) & 1))) break;
                     where = 25;
-                    if (t >= 1 && !(ok = mbar_wait(&bars[kKvBarSFree + (b ^ 1)], ((t - 1) >> 1) & 1, tmo)))
+                    if (t >= 1 && !(ok = iwait(&bars[kKvBarSFree + (b ^ 1)], ((t - 1) >> 1) & 1)))
                         break;
                     tc_fence_after();
                     const uint32_t nbuf = tmem + C::kTmemBuf + (b ^ 1) * 128;
@@ -391,28 +401,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ts_kmajor<D>(nbuf, tK, sQ1, idS);
                     else
                         mma_ss_kmajor<D>(nbuf, sK, sQ1, idS);
-                    umma_commit(&bars[kKvBarSFull + (b ^ 1)]);
+                    issue_commit<kWarpIssue>(&bars[kKvBarSFull + (b ^ 1)]);
                 }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     where = 26 + h;
-                    if (!(ok = mbar_wait(&bars[kKvBarPds + h], t & 1, tmo))) break;
+                    if (!(ok = iwait(&bars[kKvBarPds + h], t & 1))) break;
                     tc_fence_after();
                     const uint32_t acc = (t > 0 || h > 0) ? 1u : 0u;
                     mma_ts_half(tmem + C::kTmemDV, buf, sG, h, idT, acc);
                     mma_ts_half(tmem + C::kTmemDK, buf + 8, sQ, h, idT, acc);
                 }
                 if (!ok) break;
-                umma_commit(&bars[kKvBarSFree + b]);
-                umma_commit(&bars[kKvBarEmpty + s]);
+                issue_commit<kWarpIssue>(&bars[kKvBarSFree + b]);
+                issue_commit<kWarpIssue>(&bars[kKvBarEmpty + s]);
             }
             if (ok) {
-                umma_commit(&bars[kKvBarAcc]);
+                issue_commit<kWarpIssue>(&bars[kKvBarAcc]);
             } else {
                 record_timeout(prm.status, where);
                 // The products already issued finish before TMEM is freed.
-                umma_commit(&bars[kKvBarDrain]);
-                mbar_wait(&bars[kKvBarDrain], 0, tmo > kDrainNs ? tmo : kDrainNs, true);
+                issue_commit<kWarpIssue>(&bars[kKvBarDrain]);
+                issuer_wait<kWarpIssue>(&bars[kKvBarDrain], 0, tmo > kDrainNs ? tmo : kDrainNs,
+                                        true);
             }
         }
     } else {
@@ -680,7 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+        if (kWarpIssue || lane == 0) {  // a converged warp, or lane 0
+            auto iwait = [&](uint64_t* bar, uint32_t parity) {
+                return issuer_wait<kWarpIssue>(bar, parity, tmo);
+            };
             // ---- tensor-core products -------------------------------------------------------
             // Order per key tile j: S of tile j + 1 into the other buffer (while the
             // element-wise warps work on tile j), dQ of the first half of tile j's keys, of the
@@ -689,59 +703,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_bf16_f32_ab(kTile, kTile, 0, 0);
             constexpr uint32_t idT = idesc_bf16_f32_ab(kTile, D, 0, 1);
             int where = 31;
-            bool ok = mbar_wait(&bars[kQBarQG], 0, tmo) && mbar_wait(&bars[kQBarKFull], 0, tmo) &&
-                      mbar_wait(&bars[kQBarVFull], 0, tmo);
+            bool ok = iwait(&bars[kQBarQG], 0) && iwait(&bars[kQBarKFull], 0) &&
+                      iwait(&bars[kQBarVFull], 0);
             if (ok) {
                 tc_fence_after();
                 mma_ss_kmajor<D>(tmem + C::kTmemS, sQ, smem_u32(smem + C::kK), idS);
-                umma_commit(&bars[kQBarSFull]);
+                issue_commit<kWarpIssue>(&bars[kQBarSFull]);
                 mma_ss_kmajor<D>(tmem + C::kTmemDP, sG, smem_u32(smem + C::kV), idS);
-                umma_commit(&bars[kQBarDpFull]);
-                umma_commit(&bars[kQBarVEmpty]);
+                issue_commit<kWarpIssue>(&bars[kQBarDpFull]);
+                issue_commit<kWarpIssue>(&bars[kQBarVEmpty]);
             }
             for (int j = 0; ok && j < n_j; ++j) {
                 const int s = j & 1, s1 = (j + 1) & 1;
                 const int ks = j % C::kKStages, ks1 = (j + 1) % C::kKStages;
                 if (j + 1 < n_j) {
                     where = 32;
-                    if (!(ok = mbar_wait(&bars[kQBarKFull + ks1], ((j + 1) / C::kKStages) & 1, tmo)))
+                    if (!(ok = iwait(&bars[kQBarKFull + ks1], ((j + 1) / C::kKStages) & 1)))
                         break;
                     where = 33;
-                    if (j >= 1 && !(ok = mbar_wait(&bars[kQBarSFree + s1], ((j - 1) >> 1) & 1, tmo)))
+                    if (j >= 1 && !(ok = iwait(&bars[kQBarSFree + s1], ((j - 1) >> 1) & 1)))
                         break;
                     tc_fence_after();
                     mma_ss_kmajor<D>(tmem + C::kTmemS + s1 * 128, sQ,
                                      smem_u32(smem + C::kK + ks1 * C::kTileBytes), idS);
-                    umma_commit(&bars[kQBarSFull + s1]);
+                    issue_commit<kWarpIssue>(&bars[kQBarSFull + s1]);
                 }
                 const uint32_t sKj = smem_u32(smem + C::kK + ks * C::kTileBytes);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     where = 34 + half;
-                    if (!(ok = mbar_wait(&bars[kQBarP0 + half], j & 1, tmo))) break;
+                    if (!(ok = iwait(&bars[kQBarP0 + half], j & 1))) break;
                     tc_fence_after();
                     mma_ts_half(tmem + C::kTmemDQ, tmem + C::kTmemS + s * 128, sKj, half, idT,
                                 (j > 0 || half > 0) ? 1u : 0u);
                 }
                 if (!ok) break;
-                umma_commit(&bars[kQBarSFree + s]);
-                umma_commit(&bars[kQBarKEmpty + ks]);
+                issue_commit<kWarpIssue>(&bars[kQBarSFree + s]);
+                issue_commit<kWarpIssue>(&bars[kQBarKEmpty + ks]);
                 if (j + 1 < n_j) {
                     where = 36;
-                    if (!(ok = mbar_wait(&bars[kQBarVFull + s1], ((j + 1) >> 1) & 1, tmo))) break;
+                    if (!(ok = iwait(&bars[kQBarVFull + s1], ((j + 1) >> 1) & 1))) break;
                     tc_fence_after();
                     mma_ss_kmajor<D>(tmem + C::kTmemDP, sG,
                                      smem_u32(smem + C::kV + s1 * C::kTileBytes), idS);
-                    umma_commit(&bars[kQBarDpFull]);
-                    umma_commit(&bars[kQBarVEmpty + s1]);
+                    issue_commit<kWarpIssue>(&bars[kQBarDpFull]);
+                    issue_commit<kWarpIssue>(&bars[kQBarVEmpty + s1]);
                 }
             }
             if (ok) {
-                umma_commit(&bars[kQBarAcc]);
+                issue_commit<kWarpIssue>(&bars[kQBarAcc]);
             } else {
                 record_timeout(prm.status, where);
-                umma_commit(&bars[kQBarDrain]);
-                mbar_wait(&bars[kQBarDrain], 0, tmo > kDrainNs ? tmo : kDrainNs, true);
+                issue_commit<kWarpIssue>(&bars[kQBarDrain]);
+                issuer_wait<kWarpIssue>(&bars[kQBarDrain], 0, tmo > kDrainNs ? tmo : kDrainNs,
+                                        true);
             }
         }
     } else {

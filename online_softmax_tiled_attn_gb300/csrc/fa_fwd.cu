@@ -178,43 +178,6 @@ __device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// The MMA issuers' primitives, for a converged warp (W) or for lane 0 alone: the waits (made
-// warp-uniform in the first case), the products and copies, and the commits.
-template <bool W>
-__device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
-                                            bool sleep) {
-    if constexpr (W) return warp_wait(bar, parity, timeout_ns, sleep);
-    else return mbar_wait(bar, parity, timeout_ns, sleep);
-}
-template <bool W>
-__device__ __forceinline__ void issue_commit(uint64_t* bar) {
-    if constexpr (W) umma_commit_warp(bar);
-    else umma_commit(bar);
-}
-template <bool W>
-__device__ __forceinline__ void issue_ss_x4(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
-                                            uint32_t acc) {
-    if constexpr (W) umma_ss_x4_warp(d, a, b, id, acc);
-    else umma_ss_x4(d, a, b, id, acc);
-}
-template <bool W>
-__device__ __forceinline__ void issue_ts_x4(uint32_t d, uint32_t a, uint64_t b, uint32_t step,
-                                            uint32_t id, uint32_t acc) {
-    if constexpr (W) umma_ts_x4_warp(d, a, b, step, id, acc);
-    else umma_ts_x4(d, a, b, step, id, acc);
-}
-template <bool W>
-__device__ __forceinline__ void issue_ts_x8(uint32_t d, uint32_t a, uint64_t b, uint32_t step,
-                                            uint32_t id, uint32_t acc) {
-    if constexpr (W) umma_ts_x8_warp(d, a, b, step, id, acc);
-    else umma_ts_x8(d, a, b, step, id, acc);
-}
-template <bool W>
-__device__ __forceinline__ void issue_tmem_cp(uint32_t taddr, uint64_t desc) {
-    if constexpr (W) tmem_cp_128x256b_warp(taddr, desc);
-    else tmem_cp_128x256b(taddr, desc);
-}
-
 // Wait until O += P(k) V has finished.  Callers guarantee that P(k-4) V has finished and that
 // P(k+4) V cannot have, so the parity of completion k >> 2 of barrier k & 3 is unambiguous.
 __device__ __forceinline__ bool pv_wait(Bars* bars, int k, uint64_t timeout_ns,

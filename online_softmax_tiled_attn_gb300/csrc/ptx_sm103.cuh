@@ -355,6 +355,25 @@ __device__ __forceinline__ void umma_ts_x8_warp(uint32_t d_tmem, uint32_t a_tmem
     umma_ts_x4_warp(d_tmem, a_tmem + 32, b_desc + 4ull * b_step16, b_step16, idesc, 1u);
 }
 
+__device__ __forceinline__ void umma_ts_x4_stride16_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                         uint64_t b_desc, uint32_t idesc,
+                                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, %4, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+        "add.u32 a, %1, 32;\n\tadd.s64 b, b, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+        "add.u32 a, %1, 48;\n\tadd.s64 b, b, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t s_desc) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -374,6 +393,29 @@ __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
             smem_u32(bar))
         : "memory");
 }
+
+// An MMA issuer's primitives, for a converged warp (W = true; the helpers above) or for a loop
+// run by lane 0 alone (W = false): waits (made warp-uniform in the first case), products,
+// copies and commits.
+template <bool W>
+__device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                            bool sleep = false);
+template <bool W>
+__device__ __forceinline__ void issue_commit(uint64_t* bar);
+template <bool W>
+__device__ __forceinline__ void issue_ss_x4(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                            uint32_t acc);
+template <bool W>
+__device__ __forceinline__ void issue_ts_x4(uint32_t d, uint32_t a, uint64_t b, uint32_t step,
+                                            uint32_t id, uint32_t acc);
+template <bool W>
+__device__ __forceinline__ void issue_ts_x8(uint32_t d, uint32_t a, uint64_t b, uint32_t step,
+                                            uint32_t id, uint32_t acc);
+template <bool W>
+__device__ __forceinline__ void issue_ts_x4_stride16(uint32_t d, uint32_t a, uint64_t b,
+                                                     uint32_t id, uint32_t acc);
+template <bool W>
+__device__ __forceinline__ void issue_tmem_cp(uint32_t taddr, uint64_t desc);
 
 // Asynchronous copy of a 128-row x 256-bit matrix from shared memory (described by a matrix
 // descriptor, like an MMA operand) into TMEM lanes 0-127, 8 columns from `taddr`.  Ordered
@@ -624,6 +666,48 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+template <bool W>
+__device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                            bool sleep) {
+    const bool ok = mbar_wait(bar, parity, timeout_ns, sleep);
+    if constexpr (W) return __all_sync(0xffffffffu, ok);
+    else return ok;
+}
+template <bool W>
+__device__ __forceinline__ void issue_commit(uint64_t* bar) {
+    if constexpr (W) umma_commit_warp(bar);
+    else umma_commit(bar);
+}
+template <bool W>
+__device__ __forceinline__ void issue_ss_x4(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                            uint32_t acc) {
+    if constexpr (W) umma_ss_x4_warp(d, a, b, id, acc);
+    else umma_ss_x4(d, a, b, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_ts_x4(uint32_t d, uint32_t a, uint64_t b, uint32_t step,
+                                            uint32_t id, uint32_t acc) {
+    if constexpr (W) umma_ts_x4_warp(d, a, b, step, id, acc);
+    else umma_ts_x4(d, a, b, step, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_ts_x8(uint32_t d, uint32_t a, uint64_t b, uint32_t step,
+                                            uint32_t id, uint32_t acc) {
+    if constexpr (W) umma_ts_x8_warp(d, a, b, step, id, acc);
+    else umma_ts_x8(d, a, b, step, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_ts_x4_stride16(uint32_t d, uint32_t a, uint64_t b,
+                                                     uint32_t id, uint32_t acc) {
+    if constexpr (W) umma_ts_x4_stride16_warp(d, a, b, id, acc);
+    else umma_ts_x4_stride16(d, a, b, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_tmem_cp(uint32_t taddr, uint64_t desc) {
+    if constexpr (W) tmem_cp_128x256b_warp(taddr, desc);
+    else tmem_cp_128x256b(taddr, desc);
 }
 
 }  // namespace osm
