@@ -223,6 +223,54 @@ OSM_ATTN_API int fa_fwd_mask_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk,
                                   int64_t* tile_map_words);
 
 /*
+ * fa_fwd_gqa_mask -- the attention with every option at once: grouped key/value heads and
+ * per-sequence key lengths (as fa_fwd_gqa), an explicit mask with its optional tile map (as
+ * fa_fwd_mask), and one pass or split keys (as fa_fwd_splitkv).
+ *
+ * "How FlashAttention avoids storing the giant score table" (spicyshark.co, Online softmax
+ * lesson): a key that a query may not look at -- masked, past its sequence's length, or after
+ * it when causal -- gets score -inf ("The implementation"), and partial states over disjoint
+ * key ranges combine with the two-worker merge ("From softmax to attention"; "Where this is
+ * used in practice"); "FlashAttention" (paweldubiel.com notes), "Averaging block results is not
+ * enough": grouped-query attention combines with the tiled computation.  Key j is allowed for
+ * query i of head (b, h) when its mask bit is set (the mask layout of fa_fwd_mask), when
+ * j < kv_lens[b] (if kv_lens is given), and, when causal is set, j <= i + (Nk - Nq).  Query head
+ * h reads key/value head h / (H / H_kv).  A row with no allowed key gets O = 0, LSE = -inf.
+ *
+ *   Q, O     bf16 [B, H, Nq, d]; K, V bf16 [B, H_kv, Nk, d]; LSE fp32 [B, H, Nq] or NULL.
+ *   kv_lens  optional DEVICE int32 [B] (clamped to [0, Nk]); NULL: every key is valid.
+ *   mask, mask_b_stride, mask_h_stride, tile_map, tile_map_words   as fa_fwd_mask (strides
+ *            over query heads: the mask of (b, h) starts at mask + b * mask_b_stride +
+ *            h * mask_h_stride); the tile map's size comes from fa_fwd_gqa_mask_plan.
+ *   n_splits 1: one pass, no workspace; > 1: that many key ranges, the partial states in the
+ *            caller's ws_O (fp32 [n_splits, B*H*Nq, d], 16-byte aligned) and ws_LSE (fp32
+ *            [n_splits, B*H*Nq]), as fa_fwd_splitkv.  fa_fwd_gqa_mask_plan chooses a count.
+ * The call is asynchronous on `stream`; the mask, tile map and workspaces are the caller's.
+ * Errors: the union of fa_fwd_gqa's and fa_fwd_mask's.
+ */
+OSM_ATTN_API int fa_fwd_gqa_mask(const void* Q, const void* K, const void* V, void* O,
+                                 float* LSE, int64_t B, int64_t H, int64_t H_kv, int64_t Nq,
+                                 int64_t Nk, int64_t d, float scale, int causal,
+                                 const int32_t* kv_lens, const uint32_t* mask,
+                                 int64_t mask_b_stride, int64_t mask_h_stride, uint32_t* tile_map,
+                                 int64_t tile_map_words, int64_t n_splits, float* ws_O,
+                                 float* ws_LSE, void* stream);
+
+/*
+ * fa_fwd_gqa_mask_plan -- for fa_fwd_gqa_mask: the key ranges to use (n_splits = 0: chosen for
+ * about eight waves of work items, as fa_fwd_splitkv_plan; > 0: that request, capped at the key
+ * tiles), the workspace sizes in floats for that count (0 for one pass), and the tile map's
+ * size in words (as fa_fwd_mask_plan).  Host pointers; FA_ERR_INVALID_ARG for negative or
+ * oversized arguments, H not a multiple of H_kv, or a NULL output; FA_ERR_UNSUPPORTED for
+ * d not in {64, 128}.
+ */
+OSM_ATTN_API int fa_fwd_gqa_mask_plan(int64_t B, int64_t H, int64_t H_kv, int64_t Nq,
+                                      int64_t Nk, int64_t d, int64_t mask_b_stride,
+                                      int64_t mask_h_stride, int64_t n_splits,
+                                      int64_t* splits_out, int64_t* ws_o_floats,
+                                      int64_t* ws_lse_floats, int64_t* tile_map_words);
+
+/*
  * fa_bwd -- the gradients dQ, dK, dV of fa_fwd's attention for an output gradient dO.
  *
  * "FlashAttention" (paweldubiel.com notes), "Mechanism and details", and "How FlashAttention
@@ -313,7 +361,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 7
+#define OSM_ATTN_ABI_VERSION 8
 
 #ifdef __cplusplus
 }

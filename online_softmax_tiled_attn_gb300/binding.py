@@ -69,6 +69,13 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_mask.restype = ctypes.c_int
             L.fa_fwd_mask_plan.argtypes = [i64, i64, i64, i64, i64, i64, i64p]
             L.fa_fwd_mask_plan.restype = ctypes.c_int
+            L.fa_fwd_gqa_mask.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                          ctypes.c_float, ctypes.c_int, vp, vp, i64, i64, vp, i64,
+                                          i64, vp, vp, vp]
+            L.fa_fwd_gqa_mask.restype = ctypes.c_int
+            L.fa_fwd_gqa_mask_plan.argtypes = [i64, i64, i64, i64, i64, i64, i64, i64, i64, i64p,
+                                               i64p, i64p, i64p]
+            L.fa_fwd_gqa_mask_plan.restype = ctypes.c_int
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                  ctypes.c_float, ctypes.c_int, vp]
             L.fa_bwd.restype = ctypes.c_int
@@ -158,6 +165,28 @@ def fa_fwd_mask_raw(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, mask, mask_
     return lib().fa_fwd_mask(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d),
                              float(scale), int(bool(causal)), mask, int(mask_b_stride),
                              int(mask_h_stride), tile_map, int(tile_map_words), stream_ptr)
+
+
+def gqa_mask_plan(B, H, H_kv, Nq, Nk, d, mask_b_stride, mask_h_stride, n_splits=0):
+    """(splits, workspace O floats, workspace LSE floats, tile map words) for fa_fwd_gqa_mask."""
+    s, wo, wl, tm = (ctypes.c_int64(0) for _ in range(4))
+    rc = lib().fa_fwd_gqa_mask_plan(int(B), int(H), int(H_kv), int(Nq), int(Nk), int(d),
+                                    int(mask_b_stride), int(mask_h_stride), int(n_splits),
+                                    ctypes.byref(s), ctypes.byref(wo), ctypes.byref(wl),
+                                    ctypes.byref(tm))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_gqa_mask_plan")
+    return s.value, wo.value, wl.value, tm.value
+
+
+def fa_fwd_gqa_mask_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, H_kv, Nq, Nk, d, scale,
+                        causal, kv_lens_ptr, mask_ptr, mask_b_stride, mask_h_stride, tm_ptr,
+                        tm_words, n_splits, ws_o_ptr, ws_lse_ptr, stream_ptr):
+    return lib().fa_fwd_gqa_mask(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(H_kv),
+                                 int(Nq), int(Nk), int(d), float(scale), int(bool(causal)),
+                                 kv_lens_ptr, mask_ptr, int(mask_b_stride), int(mask_h_stride),
+                                 tm_ptr, int(tm_words), int(n_splits), ws_o_ptr, ws_lse_ptr,
+                                 stream_ptr)
 
 
 def mask_plan(B, H, Nq, Nk, mask_b_stride, mask_h_stride):
@@ -449,4 +478,68 @@ def fa_fwd_mask(q, k, v, mask_bits, scale=None, causal=False, out=None, lse=None
                          tm_ptr, tm_words, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_mask")
+    return O, L
+
+
+def fa_fwd_gqa_mask(q, k, v, mask_bits, kv_lens=None, n_splits=0, scale=None, causal=False,
+                    out=None, lse=None, stream=None, skip_tiles=True, tile_map=None,
+                    workspace=None):
+    """Attention of q [B,H,Nq,d] over k, v [B,H_kv,Nk,d] (CUDA bf16, H_kv divides H) with an
+    explicit mask (mask_bits as for fa_fwd_mask, over the H query heads), optional key lengths
+    kv_lens (CUDA int32 [B]) and n_splits key ranges (0: chosen by the plan call; 1: one pass).
+    skip_tiles / tile_map as for fa_fwd_mask; workspace: (ws_O, ws_LSE) fp32 CUDA tensors of
+    at least the plan's sizes, or made here.  Returns (O, LSE)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 [B, H, N, d] tensor")
+    B, H, Nq, d = q.shape
+    H_kv, Nk = k.shape[1], k.shape[2]
+    if k.shape != (B, H_kv, Nk, d) or v.shape != k.shape:
+        raise ValueError("k, v must be [B, H_kv, Nk, d] with q's B and d")
+    W = 4 * ((Nk + 127) // 128)
+    if (not isinstance(mask_bits, torch.Tensor) or not mask_bits.is_cuda
+            or mask_bits.dtype not in (torch.int32, torch.uint32) or mask_bits.dim() != 4
+            or not mask_bits.is_contiguous() or tuple(mask_bits.shape[2:]) != (Nq, W)
+            or mask_bits.shape[0] not in (1, B) or mask_bits.shape[1] not in (1, H)):
+        raise TypeError("mask_bits must be a contiguous CUDA int32 [B or 1, H or 1, Nq, W]")
+    if kv_lens is not None and (not isinstance(kv_lens, torch.Tensor) or not kv_lens.is_cuda
+                                or kv_lens.dtype != torch.int32 or kv_lens.shape != (B,)):
+        raise TypeError("kv_lens must be a CUDA int32 [B] tensor")
+    hs = Nq * W if mask_bits.shape[1] == H and H > 1 else 0
+    bs = mask_bits.shape[1] * Nq * W if mask_bits.shape[0] == B and B > 1 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    splits, wo, wl, need = gqa_mask_plan(B, H, H_kv, Nq, Nk, d, bs, hs, n_splits)
+    O = torch.empty_like(q) if out is None else out
+    L = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    tm_ptr, tm_words = 0, 0
+    if skip_tiles:
+        if tile_map is None:
+            tile_map = torch.empty(max(need, 1), dtype=torch.int32, device=q.device)
+        if (not isinstance(tile_map, torch.Tensor) or not tile_map.is_cuda
+                or tile_map.dtype not in (torch.int32, torch.uint32)
+                or not tile_map.is_contiguous() or tile_map.numel() < need):
+            raise TypeError(f"tile_map must be a contiguous CUDA int32 tensor of >= {need} words")
+        tm_ptr, tm_words = tile_map.data_ptr(), tile_map.numel()
+    ws_o = ws_l = None
+    if splits > 1:
+        if workspace is None:
+            workspace = (torch.empty(wo, dtype=torch.float32, device=q.device),
+                         torch.empty(wl, dtype=torch.float32, device=q.device))
+        ws_o, ws_l = workspace
+        if ws_o.numel() < wo or ws_l.numel() < wl:
+            raise ValueError("workspace too small for the plan")
+    rc = fa_fwd_gqa_mask_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(),
+                             L.data_ptr(), B, H, H_kv, Nq, Nk, d, scale, causal,
+                             kv_lens.data_ptr() if kv_lens is not None else None,
+                             mask_bits.data_ptr(), bs, hs, tm_ptr, tm_words, max(splits, 1),
+                             ws_o.data_ptr() if ws_o is not None else None,
+                             ws_l.data_ptr() if ws_l is not None else None,
+                             _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_gqa_mask")
     return O, L

@@ -69,7 +69,7 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
         // groups, and the furthest row must not reach an output.
         const int64_t words = 4 * ((Nk + 127) / 128);
         if (!aligned(mask, 16) || mask_bs < 0 || mask_hs < 0 || mask_bs % 4 != 0 ||
-            mask_hs % 4 != 0 || H_kv != H)
+            mask_hs % 4 != 0)
             return FA_ERR_INVALID_ARG;
         int64_t ext, t1, t2, t3;
         if (!mul_ok(B - 1, mask_bs, &t1) || !mul_ok(H - 1, mask_hs, &t2) ||
@@ -226,6 +226,47 @@ int fa_fwd_mask(const void* Q, const void* K, const void* V, void* O, float* LSE
     return attention_call(Q, K, V, O, LSE, B, H, H, Nq, Nk, d, scale, causal, nullptr, 1,
                           nullptr, nullptr, stream, mask, mask_b_stride, mask_h_stride,
                           tile_map, tile_map_words);
+}
+
+int fa_fwd_gqa_mask(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d,
+                    float scale, int causal, const int32_t* kv_lens, const uint32_t* mask,
+                    int64_t mask_b_stride, int64_t mask_h_stride, uint32_t* tile_map,
+                    int64_t tile_map_words, int64_t n_splits, float* ws_O, float* ws_LSE,
+                    void* stream) {
+    if (!mask) return FA_ERR_INVALID_ARG;
+    return attention_call(Q, K, V, O, LSE, B, H, H_kv, Nq, Nk, d, scale, causal, kv_lens,
+                          n_splits, ws_O, ws_LSE, stream, mask, mask_b_stride, mask_h_stride,
+                          tile_map, tile_map_words);
+}
+
+int fa_fwd_gqa_mask_plan(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d,
+                         int64_t mask_b_stride, int64_t mask_h_stride, int64_t n_splits,
+                         int64_t* splits_out, int64_t* ws_o_floats, int64_t* ws_lse_floats,
+                         int64_t* tile_map_words) {
+    if (!splits_out || !ws_o_floats || !ws_lse_floats || !tile_map_words)
+        return FA_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || H_kv < 0 || Nq < 0 || Nk < 0 || d < 0 || n_splits < 0 ||
+        n_splits > 256 || mask_b_stride < 0 || mask_h_stride < 0 || Nq > (1LL << 30) ||
+        Nk > (1LL << 30) || B > (1LL << 30) || H > (1LL << 30))
+        return FA_ERR_INVALID_ARG;
+    if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
+    int64_t bh, rows, elems;
+    if (!mul_ok(B, H, &bh) || !mul_ok(bh, Nq, &rows) || !mul_ok(rows, d, &elems))
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t words = osm::mask_tile_map_words(B, H, Nq, Nk, mask_b_stride, mask_h_stride);
+    if (words < 0) return FA_ERR_INVALID_ARG;
+    // With a mask the query heads run as their own row blocks (no packing by key/value head).
+    const int64_t splits = osm::splitkv_choose_splits(bh, Nq, Nk, n_splits);
+    int64_t o = 0, l = 0;
+    if (splits > 1 && (!mul_ok(elems, splits, &o) || !mul_ok(rows, splits, &l)))
+        return FA_ERR_INVALID_ARG;
+    *splits_out = splits;
+    *ws_o_floats = splits > 1 ? o : 0;
+    *ws_lse_floats = splits > 1 ? l : 0;
+    *tile_map_words = words;
+    return FA_OK;
 }
 
 int fa_fwd_mask_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t mask_b_stride,

@@ -1215,22 +1215,21 @@ template <bool SPLIT>
 int launch_dispatch(int64_t d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                     const CUtensorMap& tv, const CUtensorMap& tm, const FaParams& prm,
                     cudaStream_t stream) {
-    if (prm.mask) {  // explicit masks run one pass
-        if (SPLIT) return FA_ERR_UNSUPPORTED;
+    if (prm.mask) {  // explicit masks: one pass or split keys, with or without a tile map
         const bool map = prm.tile_map != nullptr;
         if (d == 64) {
             if (map)
-                return causal ? launch_kernel<64, true, false, 2>(tq, tk, tv, tm, prm, stream)
-                              : launch_kernel<64, false, false, 2>(tq, tk, tv, tm, prm, stream);
-            return causal ? launch_kernel<64, true, false, 1>(tq, tk, tv, tm, prm, stream)
-                          : launch_kernel<64, false, false, 1>(tq, tk, tv, tm, prm, stream);
+                return causal ? launch_kernel<64, true, SPLIT, 2>(tq, tk, tv, tm, prm, stream)
+                              : launch_kernel<64, false, SPLIT, 2>(tq, tk, tv, tm, prm, stream);
+            return causal ? launch_kernel<64, true, SPLIT, 1>(tq, tk, tv, tm, prm, stream)
+                          : launch_kernel<64, false, SPLIT, 1>(tq, tk, tv, tm, prm, stream);
         }
         if (d == 128) {
             if (map)
-                return causal ? launch_kernel<128, true, false, 2>(tq, tk, tv, tm, prm, stream)
-                              : launch_kernel<128, false, false, 2>(tq, tk, tv, tm, prm, stream);
-            return causal ? launch_kernel<128, true, false, 1>(tq, tk, tv, tm, prm, stream)
-                          : launch_kernel<128, false, false, 1>(tq, tk, tv, tm, prm, stream);
+                return causal ? launch_kernel<128, true, SPLIT, 2>(tq, tk, tv, tm, prm, stream)
+                              : launch_kernel<128, false, SPLIT, 2>(tq, tk, tv, tm, prm, stream);
+            return causal ? launch_kernel<128, true, SPLIT, 1>(tq, tk, tv, tm, prm, stream)
+                          : launch_kernel<128, false, SPLIT, 1>(tq, tk, tv, tm, prm, stream);
         }
         return FA_ERR_UNSUPPORTED;
     }
@@ -1292,6 +1291,26 @@ int launch_mask_tile_map(const AttnShape& sh, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// An explicit mask's tensor map, and its tile map filled by the pre-pass on `stream` when the
+// caller gave a buffer for it (otherwise prm.tile_map is cleared: no tile is skipped).
+int setup_mask(const AttnShape& sh, FaParams* prm, CUtensorMap* tm, cudaStream_t stream) {
+    if (!sh.mask) {
+        prm->tile_map = nullptr;
+        return FA_OK;
+    }
+    const int64_t n_kt = (sh.Nk + kBN - 1) / kBN;
+    int rc = make_mask_tensor_map(tm, sh.mask, 4 * n_kt, sh.Nq, sh.mask_hs != 0 ? sh.H : 1,
+                                  sh.mask_bs != 0 ? sh.B : 1, sh.mask_hs, sh.mask_bs);
+    if (rc != FA_OK) return rc;
+    if (sh.tile_map) {
+        rc = launch_mask_tile_map(sh, stream);
+        if (rc != FA_OK) return rc;
+    } else {
+        prm->tile_map = nullptr;
+    }
+    return FA_OK;
+}
+
 }  // namespace
 
 AttnShape pack_query_heads(const AttnShape& sh) {
@@ -1315,19 +1334,8 @@ int fa_fwd_shape_launch(const void* Q, const void* K, const void* V, void* O, fl
     if (st != FA_OK) return st;
     FaParams prm = base_params(sh, scale);
     CUtensorMap tm{};
-    if (sh.mask) {
-        const int64_t n_kt = (sh.Nk + kBN - 1) / kBN;
-        const int rc = make_mask_tensor_map(&tm, sh.mask, 4 * n_kt, sh.Nq,
-                                            sh.mask_hs != 0 ? sh.H : 1,
-                                            sh.mask_bs != 0 ? sh.B : 1, sh.mask_hs, sh.mask_bs);
-        if (rc != FA_OK) return rc;
-    }
-    if (sh.mask && sh.tile_map) {
-        const int rc = launch_mask_tile_map(sh, stream);
-        if (rc != FA_OK) return rc;
-    } else {
-        prm.tile_map = nullptr;
-    }
+    const int mrc = setup_mask(sh, &prm, &tm, stream);
+    if (mrc != FA_OK) return mrc;
     prm.O = static_cast<__nv_bfloat16*>(O);
     prm.LSE = LSE;
     prm.n_splits = 1;
@@ -1380,8 +1388,10 @@ int fa_fwd_splitkv_launch(const void* Q, const void* K, const void* V, void* O, 
         prm.ws_LSE = ws_LSE;
         prm.n_splits = static_cast<int>(n_splits);
         prm.tiles_per_split = static_cast<int>((n_kv_all + n_splits - 1) / n_splits);
-        const CUtensorMap no_mask{};
-        const int rc = launch_dispatch<true>(sh.d, causal, tq, tk, tv, no_mask, prm, stream);
+        CUtensorMap tm{};
+        const int mrc = setup_mask(sh, &prm, &tm, stream);
+        if (mrc != FA_OK) return mrc;
+        const int rc = launch_dispatch<true>(sh.d, causal, tq, tk, tv, tm, prm, stream);
         if (rc != FA_OK) return rc;
     } else if (n_splits == 1) {
         return fa_fwd_shape_launch(Q, K, V, O, LSE, sh, scale, causal, stream);

@@ -26,6 +26,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "fa_fwd_gqa_plan",
               "osm_softmax", "osm_softmax_topk", "fa_bwd", "fa_fwd_mask", "fa_fwd_mask_plan",
+              "fa_fwd_gqa_mask", "fa_fwd_gqa_mask_plan",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
@@ -50,7 +51,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 7
+    assert binding.lib().osm_attn_abi_version() == 8
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -244,6 +245,51 @@ def test_fa_fwd_mask_plan_sizes():
     for bad in ((-1, 1, 128, 128, 0, 0), (1, 1, 128, 128, -4, 0), (1, 1, 1 << 31, 128, 0, 0)):
         with pytest.raises(binding.FaError):
             binding.mask_plan(*bad)
+
+
+@pytest.mark.parametrize(
+    "over, want",
+    [
+        (dict(mask=0), binding.FA_ERR_INVALID_ARG),                  # no mask
+        (dict(Hkv=3), binding.FA_ERR_INVALID_ARG),                   # H_kv does not divide H
+        (dict(mhs=6), binding.FA_ERR_INVALID_ARG),                   # not whole 16-byte groups
+        (dict(lens=P + 3 * 65536 + 64), binding.FA_ERR_INVALID_ARG),  # key lengths inside O
+        (dict(splits=2), binding.FA_ERR_INVALID_ARG),                # two ranges, no workspace
+        (dict(splits=2, wso=P + 12 * 65536, wsl=P + 12 * 65536 + 8), binding.FA_ERR_INVALID_ARG),
+        (dict(splits=0), binding.FA_ERR_INVALID_ARG),                # 0 is for the plan call
+        (dict(tm=P + 3 * 65536, tmw=1), binding.FA_ERR_INVALID_ARG),  # tile map on O
+        (dict(d=96), binding.FA_ERR_UNSUPPORTED),
+        (dict(Nq=0), binding.FA_OK),
+    ],
+)
+def test_fa_fwd_gqa_mask_rejects_on_host(over, want):
+    """B1 H4 H_kv 2 Nq=Nk=128 d64 at distinct fake addresses (64 KiB slots), mask at the tenth."""
+    T = 65536
+    a = dict(q=P, k=P + T, v=P + 2 * T, o=P + 3 * T, lse=P + 4 * T, B=1, H=4, Hkv=2, Nq=128,
+             Nk=128, d=64, scale=0.125, causal=0, lens=0, mask=P + 9 * T, mbs=0, mhs=0, tm=0,
+             tmw=0, splits=1, wso=0, wsl=0)
+    a.update(over)
+    rc = binding.fa_fwd_gqa_mask_raw(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                                     a["Hkv"], a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"],
+                                     a["lens"], a["mask"], a["mbs"], a["mhs"], a["tm"], a["tmw"],
+                                     a["splits"], a["wso"], a["wsl"], None)
+    assert rc == want
+
+
+def test_fa_fwd_gqa_mask_plan():
+    """The tile map as fa_fwd_mask_plan; split counts over the unpacked query heads; the
+    workspaces sized for the chosen count."""
+    s, wo, wl, tm = binding.gqa_mask_plan(2, 16, 4, 4096, 4096, 128, 0, 4096 * 128, 3)
+    assert s == 3 and wo == 3 * 2 * 16 * 4096 * 128 and wl == 3 * 2 * 16 * 4096
+    assert tm == binding.mask_plan(2, 16, 4096, 4096, 0, 4096 * 128)
+    s, wo, wl, tm = binding.gqa_mask_plan(1, 8, 8, 300, 5000, 64, 0, 0, 1)
+    assert (s, wo, wl, tm) == (1, 0, 0, binding.mask_plan(1, 8, 300, 5000, 0, 0))
+    s, _, _, _ = binding.gqa_mask_plan(1, 1, 1, 128, 300, 64, 0, 0, 64)
+    assert s == 3  # capped at the key tiles
+    for bad in ((1, 4, 3, 128, 128, 64, 0, 0, 0), (1, 4, 2, 128, 128, 64, -4, 0, 0),
+                (1, 4, 2, 128, 128, 64, 0, 0, 300)):
+        with pytest.raises(binding.FaError):
+            binding.gqa_mask_plan(*bad)
 
 
 def test_selftest_rejects_out_of_range_timeout_on_host():
