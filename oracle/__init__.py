@@ -21,7 +21,8 @@ Functions (each a thin ctypes wrapper around ``oracle.c``; the arithmetic lives 
   or past kv_lens[b] are masked like any other key: score -inf).
 * :func:`attention_bwd` -- the gradients dQ, dK, dV of the attention for an output gradient dO,
   the derivative of the definition (the backward pass that recomputes the scores: "FlashAttention"
-  (paweldubiel.com notes), "Mechanism and details").
+  (paweldubiel.com notes), "Mechanism and details"), with grouped key/value heads (the key and
+  value gradients of a shared head sum over its query heads) and optional key lengths.
 * :func:`online_state` -- the pages' block-by-block streaming state (m, l, acc) of one score row
   with an optional trace.  Same lesson, sections "The idea", "From softmax to attention" and
   "A worked example by hand" (Tables 1 and 2); "kbwen.com FlashAttention" page, sections "Two
@@ -93,6 +94,11 @@ class Oracle:
                                          ctypes.c_double, ctypes.c_int, _dp, _dp, _dp,
                                          ctypes.c_int]
         lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_attn_bwd2.argtypes = [_u16p, _u16p, _u16p, _u16p, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.c_double, ctypes.c_int, _i32p,
+                                         _dp, _dp, _dp, ctypes.c_int]
+        lib.oracle_attn_bwd2.restype = ctypes.c_int
         lib.oracle_online_state.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                             _dp]
@@ -235,21 +241,32 @@ class Oracle:
             raise ValueError("oracle_attn4 rejected its arguments")
         return O, L
 
-    def attention_bwd(self, Q, K, V, dO, scale: float, causal: bool, nthreads: int = 0):
-        """Q, K, V, dO: bf16 [B, H, N, d] (bits or CPU torch bf16).  Returns fp64 (dQ, dK, dV)."""
+    def attention_bwd(self, Q, K, V, dO, scale: float, causal: bool, nthreads: int = 0,
+                      kv_lens=None):
+        """Q, dO: bf16 [B, H, N, d]; K, V: bf16 [B, H_kv, N, d] with H_kv dividing H (bits or CPU
+        torch bf16).  kv_lens: optional int32 [B], keys j >= kv_lens[b] excluded.  Returns fp64
+        (dQ [B, H, N, d], dK, dV [B, H_kv, N, d]); a shared key/value head's gradients sum over
+        its query heads."""
         Q, K, V, dO = (_as_bf16_bits(t) for t in (Q, K, V, dO))
-        if not (Q.shape == K.shape == V.shape == dO.shape) or Q.ndim != 4:
-            raise ValueError("Q, K, V, dO must share one [B, H, N, d] shape")
+        if Q.ndim != 4 or Q.shape != dO.shape or K.shape != V.shape or K.ndim != 4 \
+                or K.shape[0] != Q.shape[0] or K.shape[2:] != Q.shape[2:]:
+            raise ValueError("Q, dO [B, H, N, d] and K, V [B, H_kv, N, d] disagree")
         B, H, N, d = Q.shape
+        H_kv = K.shape[1]
+        lens = None
+        if kv_lens is not None:
+            lens = np.ascontiguousarray(np.asarray(kv_lens), dtype=np.int32)
+            if lens.shape != (B,):
+                raise ValueError("kv_lens must have one entry per sequence")
         dQ = np.empty((B, H, N, d), dtype=np.float64)
-        dK = np.empty_like(dQ)
-        dV = np.empty_like(dQ)
-        rc = self._lib.oracle_attn_bwd(_ptr(Q, _u16p), _ptr(K, _u16p), _ptr(V, _u16p),
-                                       _ptr(dO, _u16p), B, H, N, d, float(scale),
-                                       int(bool(causal)), _ptr(dQ, _dp), _ptr(dK, _dp),
-                                       _ptr(dV, _dp), nthreads)
+        dK = np.empty((B, H_kv, N, d), dtype=np.float64)
+        dV = np.empty_like(dK)
+        rc = self._lib.oracle_attn_bwd2(_ptr(Q, _u16p), _ptr(K, _u16p), _ptr(V, _u16p),
+                                        _ptr(dO, _u16p), B, H, H_kv, N, d, float(scale),
+                                        int(bool(causal)), _ptr(lens, _i32p), _ptr(dQ, _dp),
+                                        _ptr(dK, _dp), _ptr(dV, _dp), nthreads)
         if rc != 0:
-            raise ValueError("oracle_attn_bwd rejected its arguments")
+            raise ValueError("oracle_attn_bwd2 rejected its arguments")
         return dQ, dK, dV
 
     # -- streaming state ---------------------------------------------------------------------
@@ -353,8 +370,8 @@ def attention_gqa(Q, K, V, scale, causal, kv_lens=None, rows=None, nthreads: int
     return load().attention_gqa(Q, K, V, scale, causal, kv_lens, rows, nthreads)
 
 
-def attention_bwd(Q, K, V, dO, scale, causal, nthreads: int = 0):
-    return load().attention_bwd(Q, K, V, dO, scale, causal, nthreads)
+def attention_bwd(Q, K, V, dO, scale, causal, nthreads: int = 0, kv_lens=None):
+    return load().attention_bwd(Q, K, V, dO, scale, causal, nthreads, kv_lens)
 
 
 def online_state(s, v, block, trace=False):

@@ -449,77 +449,99 @@ int oracle_attn3(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_
 
 typedef struct {
     const uint16_t *Q, *K, *V, *dO;
-    int64_t N, d;
+    int64_t H, H_kv, N, d;
     double scale;
     int causal;
+    const int32_t* kv_lens; /* [B] valid keys per sequence, or NULL (all N) */
     double *dQ, *dK, *dV;
-    int64_t h0, h1; /* heads [h0, h1) of the flat (b*H + h) index */
+    int64_t g0, g1; /* key/value heads [g0, g1) of the flat (b*H_kv + hk) index */
     int err;
 } bwd_job;
 
 static void* bwd_worker(void* arg) {
     bwd_job* jb = (bwd_job*)arg;
-    const int64_t N = jb->N, d = jb->d;
+    const int64_t N = jb->N, d = jb->d, group = jb->H / jb->H_kv;
     double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     double* q = (double*)malloc(sizeof(double) * (size_t)d);
     double* o = (double*)malloc(sizeof(double) * (size_t)d);
     double* g = (double*)malloc(sizeof(double) * (size_t)d);
     if (!s || !q || !o || !g) { jb->err = 1; free(s); free(q); free(o); free(g); return NULL; }
-    for (int64_t bh = jb->h0; bh < jb->h1; ++bh) {
-        const uint16_t* Qh = jb->Q + bh * N * d;
-        const uint16_t* Kh = jb->K + bh * N * d;
-        const uint16_t* Vh = jb->V + bh * N * d;
-        const uint16_t* Gh = jb->dO + bh * N * d;
-        double* dQh = jb->dQ + bh * N * d;
-        double* dKh = jb->dK + bh * N * d;
-        double* dVh = jb->dV + bh * N * d;
-        for (int64_t t = 0; t < N * d; ++t) { dQh[t] = 0.0; dKh[t] = 0.0; dVh[t] = 0.0; }
-        for (int64_t i = 0; i < N; ++i) {
-            const int64_t nk = jb->causal ? i + 1 : N;
-            for (int64_t k = 0; k < d; ++k) {
-                q[k] = bf16_to_double(Qh[i * d + k]);
-                g[k] = bf16_to_double(Gh[i * d + k]);
-            }
-            /* the shares P_ij of row i (three passes, as the forward definition) */
-            double m = -INFINITY;
-            for (int64_t j = 0; j < nk; ++j) {
-                double acc = 0.0;
-                for (int64_t k = 0; k < d; ++k) acc += q[k] * bf16_to_double(Kh[j * d + k]);
-                s[j] = jb->scale * acc;
-                if (s[j] > m) m = s[j];
-            }
-            double l = 0.0;
-            for (int64_t j = 0; j < nk; ++j) l += exp(s[j] - m);
-            for (int64_t j = 0; j < nk; ++j) s[j] = exp(s[j] - m) / l; /* s now holds P_ij */
-            /* O_i and D_i = dO_i . O_i */
-            for (int64_t k = 0; k < d; ++k) o[k] = 0.0;
-            for (int64_t j = 0; j < nk; ++j)
-                for (int64_t k = 0; k < d; ++k) o[k] += s[j] * bf16_to_double(Vh[j * d + k]);
-            double D = 0.0;
-            for (int64_t k = 0; k < d; ++k) D += g[k] * o[k];
-#if ORACLE_MUTANT == 16
-            D = 0.0; /* mutant: drops the D_i term */
+    for (int64_t bhk = jb->g0; bhk < jb->g1; ++bhk) {
+        const int64_t b = bhk / jb->H_kv, hk = bhk % jb->H_kv;
+        const uint16_t* Kh = jb->K + bhk * N * d;
+        const uint16_t* Vh = jb->V + bhk * N * d;
+        double* dKh = jb->dK + bhk * N * d;
+        double* dVh = jb->dV + bhk * N * d;
+        for (int64_t t = 0; t < N * d; ++t) { dKh[t] = 0.0; dVh[t] = 0.0; }
+        /* keys j < len of this sequence take part */
+        int64_t len = N;
+#if ORACLE_MUTANT != 22
+        if (jb->kv_lens) {
+            len = jb->kv_lens[b];
+            if (len < 0) len = 0;
+            if (len > N) len = N;
+        }
 #endif
-            for (int64_t j = 0; j < nk; ++j) {
-                const double p = s[j];
-                double dp = 0.0;
+        /* the query heads that share this key/value head: their key and value gradients add */
+        for (int64_t hq = hk * group; hq < (hk + 1) * group; ++hq) {
+            const int64_t bh = b * jb->H + hq;
+            const uint16_t* Qh = jb->Q + bh * N * d;
+            const uint16_t* Gh = jb->dO + bh * N * d;
+            double* dQh = jb->dQ + bh * N * d;
+            for (int64_t t = 0; t < N * d; ++t) dQh[t] = 0.0;
+#if ORACLE_MUTANT == 21
+            /* mutant: the shared head keeps only the last query head's part */
+            for (int64_t t = 0; t < N * d; ++t) { dKh[t] = 0.0; dVh[t] = 0.0; }
+#endif
+            for (int64_t i = 0; i < N; ++i) {
+                int64_t nk = jb->causal ? i + 1 : N;
+                if (nk > len) nk = len;
+                if (nk == 0) continue; /* no allowed key: O_i = 0 and the row adds nothing */
                 for (int64_t k = 0; k < d; ++k) {
-                    dp += g[k] * bf16_to_double(Vh[j * d + k]);
-                    dVh[j * d + k] += p * g[k];
+                    q[k] = bf16_to_double(Qh[i * d + k]);
+                    g[k] = bf16_to_double(Gh[i * d + k]);
                 }
+                /* the shares P_ij of row i (three passes, as the forward definition) */
+                double m = -INFINITY;
+                for (int64_t j = 0; j < nk; ++j) {
+                    double acc = 0.0;
+                    for (int64_t k = 0; k < d; ++k) acc += q[k] * bf16_to_double(Kh[j * d + k]);
+                    s[j] = jb->scale * acc;
+                    if (s[j] > m) m = s[j];
+                }
+                double l = 0.0;
+                for (int64_t j = 0; j < nk; ++j) l += exp(s[j] - m);
+                for (int64_t j = 0; j < nk; ++j) s[j] = exp(s[j] - m) / l; /* s holds P_ij */
+                /* O_i and D_i = dO_i . O_i */
+                for (int64_t k = 0; k < d; ++k) o[k] = 0.0;
+                for (int64_t j = 0; j < nk; ++j)
+                    for (int64_t k = 0; k < d; ++k) o[k] += s[j] * bf16_to_double(Vh[j * d + k]);
+                double D = 0.0;
+                for (int64_t k = 0; k < d; ++k) D += g[k] * o[k];
+#if ORACLE_MUTANT == 16
+                D = 0.0; /* mutant: drops the D_i term */
+#endif
+                for (int64_t j = 0; j < nk; ++j) {
+                    const double p = s[j];
+                    double dp = 0.0;
+                    for (int64_t k = 0; k < d; ++k) {
+                        dp += g[k] * bf16_to_double(Vh[j * d + k]);
+                        dVh[j * d + k] += p * g[k];
+                    }
 #if ORACLE_MUTANT == 17
-                const double ds = p * (D - dp); /* mutant: sign of dS flipped */
+                    const double ds = p * (D - dp); /* mutant: sign of dS flipped */
 #else
-                const double ds = p * (dp - D);
+                    const double ds = p * (dp - D);
 #endif
 #if ORACLE_MUTANT == 18
-                const double sc = 1.0; /* mutant: forgets the scale in dQ and dK */
+                    const double sc = 1.0; /* mutant: forgets the scale in dQ and dK */
 #else
-                const double sc = jb->scale;
+                    const double sc = jb->scale;
 #endif
-                for (int64_t k = 0; k < d; ++k) {
-                    dQh[i * d + k] += sc * ds * bf16_to_double(Kh[j * d + k]);
-                    dKh[j * d + k] += sc * ds * q[k];
+                    for (int64_t k = 0; k < d; ++k) {
+                        dQh[i * d + k] += sc * ds * bf16_to_double(Kh[j * d + k]);
+                        dKh[j * d + k] += sc * ds * q[k];
+                    }
                 }
             }
         }
@@ -529,28 +551,37 @@ static void* bwd_worker(void* arg) {
 }
 
 /*
- * Gradients of O = softmax(scale Q K^T [causal]) V with respect to Q, K and V for the output
- * gradient dO.  Q, K, V, dO: bf16 bit patterns [B, H, N, d]; dQ, dK, dV: fp64 [B, H, N, d].
- * Returns 0, or -1 on bad arguments.
+ * Gradients of O = softmax(scale Q K^T [mask]) V with respect to Q, K and V for the output
+ * gradient dO, the derivative of the definition (the backward pass of "FlashAttention"
+ * (paweldubiel.com notes), "Mechanism and details"): per row, P = the softmax shares,
+ * D_i = dO_i . O_i, dP_ij = dO_i . v_j, dS_ij = P_ij (dP_ij - D_i), dQ_i = scale sum_j dS_ij k_j,
+ * dK_j = scale sum_i dS_ij q_i, dV_j = sum_i P_ij dO_i.  Q, dO: bf16 bit patterns [B, H, N, d];
+ * K, V: [B, H_kv, N, d] with H_kv dividing H (query head h reads key/value head h / (H / H_kv),
+ * and the key and value gradients of a shared head sum over its query heads); kv_lens: NULL or
+ * int32 [B], keys j >= kv_lens[b] excluded (clamped to [0, N]); causal: key j allowed for query
+ * i only when j <= i.  A row with no allowed key contributes nothing (dQ_i = 0).  dQ fp64
+ * [B, H, N, d]; dK, dV fp64 [B, H_kv, N, d].  Returns 0, or -1 on bad arguments.
  */
-int oracle_attn_bwd(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const uint16_t* dO,
-                    int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
-                    double* dQ, double* dK, double* dV, int nthreads) {
-    if (B < 0 || H < 0 || N < 0 || d < 1) return -1;
-    const int64_t heads = B * H;
-    if (heads == 0 || N == 0) return 0;
+int oracle_attn_bwd2(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                     const uint16_t* dO, int64_t B, int64_t H, int64_t H_kv, int64_t N, int64_t d,
+                     double scale, int causal, const int32_t* kv_lens, double* dQ, double* dK,
+                     double* dV, int nthreads) {
+    if (B < 0 || H < 0 || H_kv < 1 || N < 0 || d < 1 || (H > 0 && H % H_kv != 0)) return -1;
+    const int64_t kv_heads = B * H_kv;
+    if (B * H == 0 || N == 0) return 0;
     if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return -1;
     int nt = resolve_threads(nthreads);
-    if (nt > heads) nt = (int)heads;
+    if (nt > kv_heads) nt = (int)kv_heads;
     pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
     bwd_job* jobs = (bwd_job*)calloc((size_t)nt, sizeof(bwd_job));
     if (!th || !jobs) { free(th); free(jobs); return -1; }
     for (int t = 0; t < nt; ++t) {
         bwd_job* jb = &jobs[t];
-        jb->Q = Q; jb->K = K; jb->V = V; jb->dO = dO; jb->N = N; jb->d = d; jb->scale = scale;
-        jb->causal = causal; jb->dQ = dQ; jb->dK = dK; jb->dV = dV;
-        jb->h0 = heads * t / nt;
-        jb->h1 = heads * (t + 1) / nt;
+        jb->Q = Q; jb->K = K; jb->V = V; jb->dO = dO; jb->H = H; jb->H_kv = H_kv; jb->N = N;
+        jb->d = d; jb->scale = scale; jb->causal = causal; jb->kv_lens = kv_lens;
+        jb->dQ = dQ; jb->dK = dK; jb->dV = dV;
+        jb->g0 = kv_heads * t / nt;
+        jb->g1 = kv_heads * (t + 1) / nt;
     }
     for (int t = 1; t < nt; ++t) pthread_create(&th[t], NULL, bwd_worker, &jobs[t]);
     bwd_worker(&jobs[0]);
@@ -559,6 +590,14 @@ int oracle_attn_bwd(const uint16_t* Q, const uint16_t* K, const uint16_t* V, con
     for (int t = 0; t < nt; ++t) err |= jobs[t].err;
     free(th); free(jobs);
     return err ? -1 : 0;
+}
+
+/* Every query head with its own key/value head, every key valid. */
+int oracle_attn_bwd(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const uint16_t* dO,
+                    int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                    double* dQ, double* dK, double* dV, int nthreads) {
+    return oracle_attn_bwd2(Q, K, V, dO, B, H, H, N, d, scale, causal, NULL, dQ, dK, dV,
+                            nthreads);
 }
 
 /* Every query head with its own key/value head, every key valid. */

@@ -483,6 +483,95 @@ def pin_attention_bwd_uniform_scores(orc):
     assert np.abs(dV[0, 0] - want).max() < 1e-14
 
 
+def _forward_fp64_gqa(q, k, v, scale, causal, lens):
+    """O of the definition in plain numpy fp64 with grouped key/value heads and key lengths:
+    q [B, H, N, d], k, v [B, H_kv, N, d]; key j allowed for query i of sequence b when
+    j < lens[b] (and j <= i when causal); a row with no allowed key gives 0."""
+    B, H, N, _ = q.shape
+    group = H // k.shape[1]
+    kr = np.repeat(k, group, axis=1)
+    vr = np.repeat(v, group, axis=1)
+    s = scale * np.einsum("bhid,bhjd->bhij", q, kr)
+    allowed = np.ones((B, 1, N, N), bool)
+    allowed &= (np.arange(N)[None, None, None, :] < np.asarray(lens)[:, None, None, None])
+    if causal:
+        allowed &= np.tril(np.ones((N, N), bool))[None, None]
+    s = np.where(allowed, s, -np.inf)
+    mx = s.max(axis=-1, keepdims=True)
+    p = np.where(allowed, np.exp(s - np.where(np.isfinite(mx), mx, 0.0)), 0.0)
+    den = p.sum(axis=-1, keepdims=True)
+    p = np.divide(p, den, out=np.zeros_like(p), where=den > 0)
+    return np.einsum("bhij,bhjd->bhid", p, vr)
+
+
+def pin_attention_bwd_grouped_heads_finite_differences(orc):
+    """Grouped key/value heads and key lengths: the gradients against central differences of
+    L = sum(dO * O) through an independent forward (a sequence with fewer keys than N)."""
+    B, H, Hkv, N, d, lens = 2, 4, 2, 5, 3, [5, 3]
+    for causal in (False, True):
+        q, _, _ = inputs.attn_inputs(B, H, N, d, seed=511 + causal)
+        _, k, v = inputs.attn_inputs(B, Hkv, N, d, seed=521 + causal)
+        g, _, _ = inputs.attn_inputs(B, H, N, d, seed=531 + causal)
+        dQ, dK, dV = orc.attention_bwd(q, k, v, g, 0.6, causal,
+                                       kv_lens=np.array(lens, np.int32))
+        qf, kf, vf, gf = (_bf16_float(t).astype(np.float64) for t in (q, k, v, g))
+
+        def loss(qq, kk, vv):
+            return float((gf * _forward_fp64_gqa(qq, kk, vv, 0.6, causal, lens)).sum())
+
+        eps = 1e-5
+        for which, grad in ((0, dQ), (1, dK), (2, dV)):
+            args = [qf, kf, vf]
+            num = np.zeros_like(args[which])
+            for idx in np.ndindex(args[which].shape):
+                plus = [a.copy() for a in args]
+                minus = [a.copy() for a in args]
+                plus[which][idx] += eps
+                minus[which][idx] -= eps
+                num[idx] = (loss(*plus) - loss(*minus)) / (2 * eps)
+            assert np.abs(grad - num).max() < 1e-7 * max(1.0, np.abs(num).max()), (which, causal)
+
+
+def pin_attention_bwd_grouped_heads_repeat_law(orc):
+    """Grouped heads are the same attention with each key/value head repeated for its query
+    heads; a shared head's gradients are the sums of the repeated copies' gradients (the chain
+    rule for a shared parameter), and dQ is unchanged."""
+    B, H, N, d = 2, 6, 9, 5
+    for Hkv in (1, 2, 3):
+        q, _, _ = inputs.attn_inputs(B, H, N, d, seed=541 + Hkv)
+        _, k, v = inputs.attn_inputs(B, Hkv, N, d, seed=551 + Hkv)
+        g, _, _ = inputs.attn_inputs(B, H, N, d, seed=561 + Hkv)
+        for causal in (False, True):
+            dQ, dK, dV = orc.attention_bwd(q, k, v, g, 0.45, causal)
+            kr = k.repeat_interleave(H // Hkv, dim=1)
+            vr = v.repeat_interleave(H // Hkv, dim=1)
+            dQr, dKr, dVr = orc.attention_bwd(q, kr, vr, g, 0.45, causal)
+            assert np.abs(dQ - dQr).max() < 1e-13
+            sumK = dKr.reshape(B, Hkv, H // Hkv, N, d).sum(axis=2)
+            sumV = dVr.reshape(B, Hkv, H // Hkv, N, d).sum(axis=2)
+            assert np.abs(dK - sumK).max() < 1e-12 and np.abs(dV - sumV).max() < 1e-12
+
+
+def pin_attention_bwd_key_lengths(orc):
+    """Keys at or past a sequence's length take no part: their gradients are exactly 0, and
+    values planted there change no gradient; a sequence of length 0 has all gradients 0."""
+    B, H, Hkv, N, d = 3, 4, 2, 11, 6
+    lens = np.array([11, 4, 0], np.int32)
+    q, _, _ = inputs.attn_inputs(B, H, N, d, seed=571)
+    _, k, v = inputs.attn_inputs(B, Hkv, N, d, seed=572)
+    g, _, _ = inputs.attn_inputs(B, H, N, d, seed=573)
+    for causal in (False, True):
+        dQ, dK, dV = orc.attention_bwd(q, k, v, g, 0.5, causal, kv_lens=lens)
+        for b in range(B):
+            assert np.all(dK[b, :, lens[b]:] == 0) and np.all(dV[b, :, lens[b]:] == 0)
+        assert np.all(dQ[2] == 0) and np.all(dK[2] == 0) and np.all(dV[2] == 0)
+        k2, v2 = k.clone(), v.clone()
+        k2[1, :, 4:] = 50.0
+        v2[1, :, 4:] = -30.0
+        dQ2, dK2, dV2 = orc.attention_bwd(q, k2, v2, g, 0.5, causal, kv_lens=lens)
+        assert np.array_equal(dQ, dQ2) and np.array_equal(dK, dK2) and np.array_equal(dV, dV2)
+
+
 # ----------------------------------------------------------------------------------------------
 # closed forms
 # ----------------------------------------------------------------------------------------------

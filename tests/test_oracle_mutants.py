@@ -28,6 +28,8 @@ MUTANTS = {
     18: "backward forgets the scale in dQ and dK",
     19: "explicit mask ignored",
     20: "explicit mask read transposed",
+    21: "backward keeps only the last query head's part of a shared head's gradients",
+    22: "backward ignores the key lengths",
 }
 
 
