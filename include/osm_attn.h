@@ -297,6 +297,33 @@ OSM_ATTN_API int fa_bwd(const void* Q, const void* K, const void* V, const void*
                         int causal, void* stream);
 
 /*
+ * fa_bwd_gqa -- fa_bwd for the forward of fa_fwd_gqa: grouped key/value heads and per-sequence
+ * key lengths (square attention, Nq = Nk = N).
+ *
+ * The same passages as fa_bwd; grouped-query attention ("FlashAttention" (paweldubiel.com
+ * notes), "Averaging block results is not enough") shares one key/value head among the H / H_kv
+ * query heads of a group, so its key and value gradients are the sums over those query heads;
+ * a key at or past its sequence's length takes no part ("How FlashAttention avoids storing the
+ * giant score table" (spicyshark.co), "The implementation"): its gradients are exactly 0, and a
+ * query with no allowed key (a sequence of length 0) has dQ = 0.
+ *
+ *   Q, O, dO  bf16 [B, H, N, d]; K, V bf16 [B, H_kv, N, d], H_kv dividing H (query head h reads
+ *            key/value head h / (H / H_kv)); all contiguous, 16-byte aligned, read only; O and
+ *            LSE as fa_fwd_gqa wrote them for the same inputs, key lengths, scale and causal.
+ *   LSE      fp32 [B, H, N], read only.
+ *   dQ       bf16 [B, H, N, d]; dK, dV bf16 [B, H_kv, N, d]; 16-byte aligned, written.
+ *   ws_D     fp32 workspace of B*H*N floats, as fa_bwd.
+ *   kv_lens  optional DEVICE int32 [B], 4-byte aligned, read only (clamped to [0, N]); NULL:
+ *            every key is valid.
+ * Errors as fa_bwd, plus FA_ERR_INVALID_ARG when H_kv does not divide H or kv_lens is
+ * misaligned or overlaps an output.
+ */
+OSM_ATTN_API int fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                            float* ws_D, int64_t B, int64_t H, int64_t H_kv, int64_t N, int64_t d,
+                            float scale, int causal, const int32_t* kv_lens, void* stream);
+
+/*
  * osm_softmax_topk -- the k largest entries of every row with their softmax shares, in one
  * read of the row.
  *
@@ -361,7 +388,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 8
+#define OSM_ATTN_ABI_VERSION 9
 
 #ifdef __cplusplus
 }

@@ -79,6 +79,9 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                  ctypes.c_float, ctypes.c_int, vp]
             L.fa_bwd.restype = ctypes.c_int
+            L.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
+                                     i64, ctypes.c_float, ctypes.c_int, vp, vp]
+            L.fa_bwd_gqa.restype = ctypes.c_int
             L.osm_softmax_topk.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
             L.osm_softmax_topk.restype = ctypes.c_int
             L.fa_status_string.argtypes = [ctypes.c_int]
@@ -430,6 +433,50 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, workspace=None, stream
                     B, H, N, d, scale, causal, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_gqa_raw(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, ws_ptr,
+                   B, H, H_kv, N, d, scale, causal, kv_lens_ptr, stream_ptr):
+    return lib().fa_bwd_gqa(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr,
+                            ws_ptr, int(B), int(H), int(H_kv), int(N), int(d), float(scale),
+                            int(bool(causal)), kv_lens_ptr, stream_ptr)
+
+
+def fa_bwd_gqa(q, k, v, o, do, lse, kv_lens=None, scale=None, causal=False, workspace=None,
+               stream=None):
+    """(dQ, dK, dV) of fa_fwd_gqa's attention for the output gradient do: q, o, do CUDA bf16
+    [B,H,N,d], k, v [B,H_kv,N,d], lse fp32 [B,H,N], optional kv_lens CUDA int32 [B].  dK, dV
+    are [B,H_kv,N,d] (a shared key/value head's gradients sum over its query heads)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 [B, H, N, d] tensor")
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if o.shape != q.shape or do.shape != q.shape or k.shape != (B, H_kv, N, d) \
+            or v.shape != k.shape:
+        raise ValueError("q, o, do must be [B, H, N, d] and k, v [B, H_kv, N, d]")
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
+        raise TypeError("lse must be a contiguous fp32 [B, H, N] tensor")
+    if kv_lens is not None and (not isinstance(kv_lens, torch.Tensor) or not kv_lens.is_cuda
+                                or kv_lens.dtype != torch.int32 or kv_lens.shape != (B,)):
+        raise TypeError("kv_lens must be a CUDA int32 [B] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
+    ws_d = (torch.empty(B * H * N, dtype=torch.float32, device=q.device) if workspace is None
+            else workspace)
+    rc = fa_bwd_gqa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                        ws_d.data_ptr(), B, H, H_kv, N, d, scale, causal,
+                        kv_lens.data_ptr() if kv_lens is not None else None,
+                        _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_gqa")
     return dq, dk, dv
 
 

@@ -281,35 +281,49 @@ int fa_fwd_mask_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t mask_
     return FA_OK;
 }
 
-int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-           const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t B, int64_t H,
-           int64_t N, int64_t d, float scale, int causal, void* stream) {
-    if (B < 0 || H < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
-    int64_t bh, rows, elems;
+int fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+               const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t B, int64_t H,
+               int64_t H_kv, int64_t N, int64_t d, float scale, int causal,
+               const int32_t* kv_lens, void* stream) {
+    if (B < 0 || H < 0 || H_kv < 0 || N < 0 || d < 0) return FA_ERR_INVALID_ARG;
+    if (H > 0 && (H_kv < 1 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
+    int64_t bh, rows, elems, bh_kv, kv_elems;
     if (!mul_ok(B, H, &bh) || !mul_ok(bh, N, &rows) || !mul_ok(rows, d, &elems) ||
-        elems > INT64_MAX / 4)
+        elems > INT64_MAX / 4 || !mul_ok(B, H_kv, &bh_kv) || !mul_ok(bh_kv, N, &kv_elems) ||
+        !mul_ok(kv_elems, d, &kv_elems))
         return FA_ERR_INVALID_ARG;
     if (rows == 0) return FA_OK;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-    const void* ins[6] = {Q, K, V, O, dO, LSE};
+    // inputs Q, K, V, O, dO, LSE (+ kv_lens); outputs dQ, dK, dV and the workspace D
+    const void* ins[7] = {Q, K, V, O, dO, LSE, kv_lens};
     const void* outs[4] = {dQ, dK, dV, ws_D};
-    const uint64_t t_bytes = static_cast<uint64_t>(elems) * 2;  // one bf16 tensor
-    const uint64_t r_bytes = static_cast<uint64_t>(rows) * 4;   // one fp32 value per row
-    const uint64_t in_bytes[6] = {t_bytes, t_bytes, t_bytes, t_bytes, t_bytes, r_bytes};
-    const uint64_t out_bytes[4] = {t_bytes, t_bytes, t_bytes, r_bytes};
+    const uint64_t q_bytes = static_cast<uint64_t>(elems) * 2;     // a bf16 [B, H, N, d] tensor
+    const uint64_t kv_bytes = static_cast<uint64_t>(kv_elems) * 2;  // a bf16 [B, H_kv, N, d]
+    const uint64_t r_bytes = static_cast<uint64_t>(rows) * 4;      // one fp32 value per row
+    const uint64_t in_bytes[7] = {q_bytes, kv_bytes, kv_bytes, q_bytes, q_bytes, r_bytes,
+                                  kv_lens ? static_cast<uint64_t>(B) * 4 : 0};
+    const uint64_t out_bytes[4] = {q_bytes, kv_bytes, kv_bytes, r_bytes};
     for (int i = 0; i < 6; ++i)
         if (!ins[i] || !aligned(ins[i], i < 5 ? 16 : 4)) return FA_ERR_INVALID_ARG;
+    if (kv_lens && !aligned(kv_lens, 4)) return FA_ERR_INVALID_ARG;
     for (int i = 0; i < 4; ++i)
         if (!outs[i] || !aligned(outs[i], i < 3 ? 16 : 4)) return FA_ERR_INVALID_ARG;
     for (int i = 0; i < 4; ++i) {
-        for (int j = 0; j < 6; ++j)
+        for (int j = 0; j < 7; ++j)
             if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return FA_ERR_INVALID_ARG;
         for (int j = i + 1; j < 4; ++j)
             if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return FA_ERR_INVALID_ARG;
     }
-    return osm::fa_bwd_launch(Q, K, V, O, dO, LSE, dQ, dK, dV, ws_D, bh, N, d, scale,
-                              causal != 0, static_cast<cudaStream_t>(stream));
+    return osm::fa_bwd_launch(Q, K, V, O, dO, LSE, dQ, dK, dV, ws_D, B, H, H_kv, N, d, kv_lens,
+                              scale, causal != 0, static_cast<cudaStream_t>(stream));
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+           const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t B, int64_t H,
+           int64_t N, int64_t d, float scale, int causal, void* stream) {
+    return fa_bwd_gqa(Q, K, V, O, dO, LSE, dQ, dK, dV, ws_D, B, H, H, N, d, scale, causal,
+                      nullptr, stream);
 }
 
 int osm_softmax_topk(const float* x, int64_t rows, int64_t cols, int64_t k, float* values,

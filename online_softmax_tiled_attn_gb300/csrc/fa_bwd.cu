@@ -60,17 +60,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int dyn_smem(int bytes) { return bytes + 1024 > 116 * 1024 ? bytes + 1024 : 116 * 1024; }
 
 struct BwdParams {
-    const float* LSE;   // [BH, N]
-    const float* Dv;    // [BH, N], written by bwd_prep_kernel
-    __nv_bfloat16* dQ;  // [BH, N, D]
-    __nv_bfloat16* dK;
+    const float* LSE;   // [B H, N]
+    const float* Dv;    // [B H, N], written by bwd_prep_kernel
+    __nv_bfloat16* dQ;  // [B H, N, D]
+    __nv_bfloat16* dK;  // [B H_kv, N, D]
     __nv_bfloat16* dV;
-    int N, n_tiles, BH;
-    int head_group;  // heads per L2-sized group of the grid
+    int N, n_tiles;
+    int H, H_kv;        // query heads and key/value heads per sequence (H_kv divides H)
+    int BH, BH_kv;      // B H and B H_kv
+    int head_group_q;   // query heads per L2-sized group of the dQ grid
+    int head_group_kv;  // key/value heads per L2-sized group of the dK, dV grid
+    const int32_t* kv_lens;  // [B] valid keys per sequence, or nullptr (all N)
     float scale, scale_log2;
     unsigned long long timeout_ns;
     int* status;  // the library's device status word
 };
+
+// Keys of sequence b that take part: kv_lens[b] clamped to [0, N], or N.
+__device__ __forceinline__ int seq_keys(const BwdParams& prm, int b) {
+    return prm.kv_lens ? min(max(prm.kv_lens[b], 0), prm.N) : prm.N;
+}
 
 __device__ __forceinline__ void record_timeout(int* status, int where) {
     atomicCAS(status, 0, FA_ERR_TIMEOUT | (where << 8));
@@ -80,11 +89,12 @@ __device__ __forceinline__ void record_timeout(int* status, int where) {
 // tile index is outer and the head inner, so that the CTAs in flight read different heads'
 // tiles and, with a causal mask, the tiles with the most work start first.  Returns the head
 // and the tile position (0 = first to start) of this CTA.
-__device__ __forceinline__ void grid_place(const BwdParams& prm, int& bh, int& pos) {
-    const int per_group = prm.head_group * prm.n_tiles;
+__device__ __forceinline__ void grid_place(int n_heads, int head_group, int n_tiles, int& bh,
+                                           int& pos) {
+    const int per_group = head_group * n_tiles;
     const int g = blockIdx.x / per_group, idx = blockIdx.x % per_group;
-    const int heads = min(prm.head_group, prm.BH - g * prm.head_group);
-    bh = g * prm.head_group + idx % heads;
+    const int heads = min(head_group, n_heads - g * head_group);
+    bh = g * head_group + idx % heads;
     pos = idx / heads;
 }
 
@@ -267,12 +277,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKvNumBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Key tile 0 sees the most query tiles under a causal mask: it starts first.
-    int bh, jt;
-    grid_place(prm, bh, jt);
+    // Key tile 0 sees the most query tiles under a causal mask: it starts first.  bhk: the
+    // key/value head; its query heads are bh_q0 .. bh_q0 + group - 1, whose query tiles are
+    // walked one head after another (the key and value gradients of a shared head sum over
+    // its query heads).  Keys at or past the sequence's length take no part.
+    int bhk, jt;
+    grid_place(prm.BH_kv, prm.head_group_kv, prm.n_tiles, bhk, jt);
     const int N = prm.N;
+    const int group = prm.H / prm.H_kv;
+    const int b_seq = bhk / prm.H_kv;
+    const int bh_q0 = b_seq * prm.H + (bhk - b_seq * prm.H_kv) * group;
+    const int len = seq_keys(prm, b_seq);
     const int i0 = CAUSAL ? jt : 0;
-    const int n_it = prm.n_tiles - i0;
+    const int n_it1 = prm.n_tiles - i0;  // query tiles walked per query head
+    // A key tile with no key below the length walks nothing; its gradients are 0.
+    const int n_it = jt * kTile < len ? group * n_it1 : 0;
     const unsigned long long tmo = prm.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -303,12 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kTmaWarp) {
-        if (lane == 0) {
+        if (lane == 0 && n_it > 0) {
             // ---- loads ----------------------------------------------------------------------
             mbar_arrive_expect_tx(&bars[kKvBarKV], 2 * C::kTileBytes);
             for (int h = 0; h < D / 64; ++h) {
-                tma_load_3d(smem + C::kKLoad + h * kHalf, &tmK, &bars[kKvBarKV], h * 64, jt * kTile, bh);
-                tma_load_3d(smem + C::kVLoad + h * kHalf, &tmV, &bars[kKvBarKV], h * 64, jt * kTile, bh);
+                tma_load_3d(smem + C::kKLoad + h * kHalf, &tmK, &bars[kKvBarKV], h * 64,
+                            jt * kTile, bhk);
+                tma_load_3d(smem + C::kVLoad + h * kHalf, &tmV, &bars[kKvBarKV], h * 64,
+                            jt * kTile, bhk);
             }
             int issued = 0;
             for (int t = 0; t < n_it; ++t) {
@@ -324,10 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint8_t* q = smem + C::kQ + s * C::kTileBytes;
                 uint8_t* g = smem + C::kG + s * C::kTileBytes;
+                const int hq = bh_q0 + t / n_it1, row = (i0 + t % n_it1) * kTile;
                 mbar_arrive_expect_tx(&bars[kKvBarFull + s], 2 * C::kTileBytes);
                 for (int h = 0; h < D / 64; ++h) {
-                    tma_load_3d(q + h * kHalf, &tmQ, &bars[kKvBarFull + s], h * 64, (i0 + t) * kTile, bh);
-                    tma_load_3d(g + h * kHalf, &tmG, &bars[kKvBarFull + s], h * 64, (i0 + t) * kTile, bh);
+                    tma_load_3d(q + h * kHalf, &tmQ, &bars[kKvBarFull + s], h * 64, row, hq);
+                    tma_load_3d(g + h * kHalf, &tmG, &bars[kKvBarFull + s], h * 64, row, hq);
                 }
                 ++issued;
             }
@@ -335,10 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t drain = tmo > kDrainNs ? tmo : kDrainNs;
             mbar_wait(&bars[kKvBarKV], 0, drain, true);
             if (issued > 0)
-                mbar_wait(&bars[kKvBarFull + (issued - 1) % NS], ((issued - 1) / NS) & 1, drain, true);
+                mbar_wait(&bars[kKvBarFull + (issued - 1) % NS], ((issued - 1) / NS) & 1, drain,
+                          true);
         }
     } else if (warp == kMmaWarp) {
-        if (kWarpIssue || lane == 0) {  // a converged warp, or lane 0
+        if ((kWarpIssue || lane == 0) && n_it > 0) {  // a converged warp, or lane 0
             auto iwait = [&](uint64_t* bar, uint32_t parity) {
                 return issuer_wait<kWarpIssue>(bar, parity, tmo);
             };
@@ -440,28 +463,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool stager = st < 256;
         const int col = st & 127;
         const int slot = (col >> 1) * 4 + (col & 1) + (st >= 128 ? 2 : 0);
-        auto stage_value = [&](int it) -> float {
-            const int q = it * kTile + col;
+        // Walked tile t: query tile i0 + t % n_it1 of query head bh_q0 + t / n_it1.
+        auto stage_value = [&](int t) -> float {
+            const int q = (i0 + t % n_it1) * kTile + col;
             if (q >= N) return st < 128 ? -INFINITY : 0.f;
-            const size_t row = static_cast<size_t>(bh) * N + q;
+            const size_t row = static_cast<size_t>(bh_q0 + t / n_it1) * N + q;
             return st < 128 ? -prm.LSE[row] * kLog2e : -prm.Dv[row];
         };
-        // Rows past N (a ragged last key tile) and, on the diagonal tile of a causal mask, the
-        // queries before the key are masked: first allowed column of this row.
-        const bool ragged_keys = (jt + 1) * kTile > N;
-        const int lo_row = key < N ? 0 : kTile;
-        if (stager) ld_s[slot] = stage_value(i0);
+        // Key rows at or past the sequence's length (or past N: a ragged last key tile) and, on
+        // the diagonal tile of a causal mask, the queries before the key are masked: first
+        // allowed column of this row.
+        const bool ragged_keys = (jt + 1) * kTile > len;
+        const int lo_row = key < len ? 0 : kTile;
+        if (stager && n_it > 0) ld_s[slot] = stage_value(0);
         named_bar_sync(1, kSoftWarps * 32);
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
-            const int it = i0 + t, b = t & 1;
+            const int it = i0 + t % n_it1, b = t & 1;
             const uint32_t t_buf = t_row + C::kTmemBuf + b * 128;
-            const float next = stager && t + 1 < n_it ? stage_value(it + 1) : 0.f;
+            const float next = stager && t + 1 < n_it ? stage_value(t + 1) : 0.f;
             bool good = mbar_wait(&bars[kKvBarSFull + b], (t >> 1) & 1, tmo);
             if (good) {
                 tc_fence_after();
                 const bool diag = CAUSAL && it == jt;
-                const int lo = diag ? (key < N ? r : kTile) : lo_row;
+                const int lo = diag ? (key < len ? r : kTile) : lo_row;
                 float p[2][16];
                 // shares of both query halves (this warp's 16 columns of each); the S^T
                 // columns are then handed over to dP^T
@@ -499,18 +524,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             // ---- dV (warps 0-7) and scale * dK (warps 8-15), half of the columns per warp ----
-            if (!mbar_wait(&bars[kKvBarAcc], 0, tmo)) {
+            const bool is_v = sub < 2;
+            const int c0 = (sub & 1) * (D / 2);
+            const uint32_t src = t_row + (is_v ? C::kTmemDV : C::kTmemDK) + c0;
+            __nv_bfloat16* out = (is_v ? prm.dV : prm.dK) +
+                                 (static_cast<size_t>(bhk) * N + (key < N ? key : 0)) * D + c0;
+            const float sc = is_v ? 1.f : prm.scale;
+            if (n_it == 0) {
+                // no key of the tile below the length: its gradients are 0
+                uint32_t v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    if (key < N) store_row<32>(out + c * 32, v, 1.f);
+            } else if (!mbar_wait(&bars[kKvBarAcc], 0, tmo)) {
                 if (lane == 0) record_timeout(prm.status, 29);
             } else {
                 tc_fence_after();
                 // The TMEM loads are warp-wide (.sync.aligned): every lane issues them, and
                 // only the stores are limited to the keys that exist.
-                const bool is_v = sub < 2;
-                const int c0 = (sub & 1) * (D / 2);
-                const uint32_t src = t_row + (is_v ? C::kTmemDV : C::kTmemDK) + c0;
-                __nv_bfloat16* out = (is_v ? prm.dV : prm.dK) +
-                                     (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * D + c0;
-                const float sc = is_v ? 1.f : prm.scale;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     uint32_t v[32];
@@ -612,12 +645,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kQNumBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // The last query tile sees the most key tiles under a causal mask: it starts first.
+    // The last query tile sees the most key tiles under a causal mask: it starts first.  bh:
+    // the query head; bhk: the key/value head it reads.  Only key tiles holding a key below the
+    // sequence's length are walked; with none, dQ is 0.
     int bh, pos;
-    grid_place(prm, bh, pos);
+    grid_place(prm.BH, prm.head_group_q, prm.n_tiles, bh, pos);
     const int qt = prm.n_tiles - 1 - pos;
     const int N = prm.N;
-    const int n_j = CAUSAL ? qt + 1 : prm.n_tiles;
+    const int b_seq = bh / prm.H;
+    const int bhk = b_seq * prm.H_kv + (bh - b_seq * prm.H) / (prm.H / prm.H_kv);
+    const int len = seq_keys(prm, b_seq);
+    const int n_j = min(CAUSAL ? qt + 1 : prm.n_tiles, (len + kTile - 1) / kTile);
     const unsigned long long tmo = prm.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -649,12 +687,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kTmaWarp) {
-        if (lane == 0) {
+        if (lane == 0 && n_j > 0) {
             // ---- loads ----------------------------------------------------------------------
             mbar_arrive_expect_tx(&bars[kQBarQG], 2 * C::kTileBytes);
             for (int h = 0; h < D / 64; ++h) {
-                tma_load_3d(smem + C::kQ + h * kHalf, &tmQ, &bars[kQBarQG], h * 64, qt * kTile, bh);
-                tma_load_3d(smem + C::kG + h * kHalf, &tmG, &bars[kQBarQG], h * 64, qt * kTile, bh);
+                tma_load_3d(smem + C::kQ + h * kHalf, &tmQ, &bars[kQBarQG], h * 64, qt * kTile,
+                            bh);
+                tma_load_3d(smem + C::kG + h * kHalf, &tmG, &bars[kQBarQG], h * 64, qt * kTile,
+                            bh);
             }
             int k_issued = 0, v_issued = 0;
             for (int j = 0; j < n_j; ++j) {
@@ -666,7 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* k = smem + C::kK + ks * C::kTileBytes;
                 mbar_arrive_expect_tx(&bars[kQBarKFull + ks], C::kTileBytes);
                 for (int h = 0; h < D / 64; ++h)
-                    tma_load_3d(k + h * kHalf, &tmK, &bars[kQBarKFull + ks], h * 64, j * kTile, bh);
+                    tma_load_3d(k + h * kHalf, &tmK, &bars[kQBarKFull + ks], h * 64, j * kTile,
+                                bhk);
                 ++k_issued;
                 const int vs = j & 1;
                 if (j >= 2 && !mbar_wait(&bars[kQBarVEmpty + vs], ((j >> 1) - 1) & 1, tmo, true)) {
@@ -676,7 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* v = smem + C::kV + vs * C::kTileBytes;
                 mbar_arrive_expect_tx(&bars[kQBarVFull + vs], C::kTileBytes);
                 for (int h = 0; h < D / 64; ++h)
-                    tma_load_3d(v + h * kHalf, &tmV, &bars[kQBarVFull + vs], h * 64, j * kTile, bh);
+                    tma_load_3d(v + h * kHalf, &tmV, &bars[kQBarVFull + vs], h * 64, j * kTile,
+                                bhk);
                 ++v_issued;
             }
             const uint64_t drain = tmo > kDrainNs ? tmo : kDrainNs;
@@ -691,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        if (kWarpIssue || lane == 0) {  // a converged warp, or lane 0
+        if ((kWarpIssue || lane == 0) && n_j > 0) {  // a converged warp, or lane 0
             auto iwait = [&](uint64_t* bar, uint32_t parity) {
                 return issuer_wait<kWarpIssue>(bar, parity, tmo);
             };
@@ -780,13 +822,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // Masks: keys after the query on the diagonal tile of a causal mask, and keys past
-            // N (the ragged last key tile): last allowed key column of this row.
+            // Masks: keys after the query on the diagonal tile of a causal mask, and keys at or
+            // past the sequence's length (or past N: the ragged last key tile): last allowed
+            // key column of this row.
             const bool diag = CAUSAL && j == qt;
-            const bool ragged_keys = (j + 1) * kTile > N;
+            const bool ragged_keys = (j + 1) * kTile > len;
             int hi = kTile - 1;
             if (diag) hi = r;
-            if (ragged_keys && N - 1 - j * kTile < hi) hi = N - 1 - j * kTile;
+            if (ragged_keys && len - 1 - j * kTile < hi) hi = len - 1 - j * kTile;
             const uint32_t t_s = t_row + C::kTmemS + s * 128, t_dp = t_row + C::kTmemDP;
 #pragma unroll 1
             for (int k = 0; k < 2; ++k) {
@@ -802,7 +845,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             // ---- scale * dQ of this query tile (a quarter of the columns per warp) ------------
-            if (!mbar_wait(&bars[kQBarAcc], 0, tmo)) {
+            constexpr int kZCols = D / 4;
+            if (n_j == 0) {
+                // no key below the length: dQ is 0
+                uint32_t v[kZCols];
+#pragma unroll
+                for (int e = 0; e < kZCols; ++e) v[e] = 0u;
+                if (q < N) store_row<kZCols>(prm.dQ + row * D + sub * kZCols, v, 1.f);
+            } else if (!mbar_wait(&bars[kQBarAcc], 0, tmo)) {
                 if (lane == 0) record_timeout(prm.status, 38);
             } else {
                 tc_fence_after();
@@ -839,7 +889,7 @@ int bwd_sm_count() {
 
 template <int D, bool CAUSAL>
 int launch_tiles(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                 const CUtensorMap& tg, const BwdParams& prm, long long BH, cudaStream_t stream) {
+                 const CUtensorMap& tg, const BwdParams& prm, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
@@ -852,12 +902,14 @@ int launch_tiles(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
                                         QCfg<D>::kDynSmem);
     });
     if (attr != cudaSuccess) return FA_ERR_CUDA;
-    const long long ctas = BH * prm.n_tiles;
-    if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    bwd_kv_kernel<D, CAUSAL><<<static_cast<unsigned>(ctas), kThreads, KvCfg<D>::kDynSmem, stream>>>(
-        tq, tk, tv, tg, prm);
+    const long long kv_ctas = static_cast<long long>(prm.BH_kv) * prm.n_tiles;
+    const long long q_ctas = static_cast<long long>(prm.BH) * prm.n_tiles;
+    if (q_ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    bwd_kv_kernel<D, CAUSAL>
+        <<<static_cast<unsigned>(kv_ctas), kThreads, KvCfg<D>::kDynSmem, stream>>>(tq, tk, tv, tg,
+                                                                                  prm);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-    bwd_q_kernel<D, CAUSAL><<<static_cast<unsigned>(ctas), kThreads, QCfg<D>::kDynSmem, stream>>>(
+    bwd_q_kernel<D, CAUSAL><<<static_cast<unsigned>(q_ctas), kThreads, QCfg<D>::kDynSmem, stream>>>(
         tq, tk, tv, tg, prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -865,9 +917,12 @@ int launch_tiles(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 }  // namespace
 
 int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                  const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t BH,
-                  int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream) {
-    if (N > (1LL << 30) || BH > (1LL << 30)) return FA_ERR_UNSUPPORTED;
+                  const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t B,
+                  int64_t H, int64_t H_kv, int64_t N, int64_t d, const int32_t* kv_lens,
+                  float scale, bool causal, cudaStream_t stream) {
+    const int64_t BH = B * H, BH_kv = B * H_kv;
+    if (N > (1LL << 30) || BH > (1LL << 30) || H_kv < 1 || H % H_kv != 0)
+        return FA_ERR_UNSUPPORTED;
     const long long rows = BH * N;
     const long long sms = bwd_sm_count() > 0 ? bwd_sm_count() : 148;
     long long grid = (rows + 7) / 8;
@@ -884,8 +939,8 @@ int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, co
 
     CUtensorMap tq, tk, tv, tg;
     int st = make_bhnd_tensor_map(&tq, Q, BH, N, d);
-    if (st == FA_OK) st = make_bhnd_tensor_map(&tk, K, BH, N, d);
-    if (st == FA_OK) st = make_bhnd_tensor_map(&tv, V, BH, N, d);
+    if (st == FA_OK) st = make_bhnd_tensor_map(&tk, K, BH_kv, N, d);
+    if (st == FA_OK) st = make_bhnd_tensor_map(&tv, V, BH_kv, N, d);
     if (st == FA_OK) st = make_bhnd_tensor_map(&tg, dO, BH, N, d);
     if (st != FA_OK) return st;
     BwdParams prm{};
@@ -896,25 +951,35 @@ int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, co
     prm.dV = static_cast<__nv_bfloat16*>(dV);
     prm.N = static_cast<int>(N);
     prm.n_tiles = static_cast<int>((N + kTile - 1) / kTile);
+    prm.H = static_cast<int>(H);
+    prm.H_kv = static_cast<int>(H_kv);
     prm.BH = static_cast<int>(BH);
-    // Heads per group of the grid.  If the walked tiles of all heads (two bf16 [N, d] tensors
-    // each) fit in 64 MB, half of L2, one group.  Otherwise, with a causal mask, groups that
-    // fit (inside a group the longest tiles start first, which keeps the tail short); without
-    // one, a head at a time (measured fastest: the CTAs in flight share two or three heads).
-    const long long head_bytes = 4LL * N * d, budget = 64LL << 20;
-    long long group = BH;
-    if (head_bytes * BH > budget) group = causal ? budget / head_bytes : 1;
-    prm.head_group = static_cast<int>(group < 1 ? 1 : (group > BH ? BH : group));
+    prm.BH_kv = static_cast<int>(BH_kv);
+    prm.kv_lens = kv_lens;
+    // Heads per group of each grid.  If the tiles that the heads' CTAs walk (two bf16 [N, d]
+    // tensors per head: Q and dO of a key/value head's query heads for dK, dV; K and V, shared
+    // by the query heads of a group, for dQ) fit in 64 MB, half of L2, one group.  Otherwise,
+    // with a causal mask, groups that fit (inside a group the longest tiles start first, which
+    // keeps the tail short); without one, a head (a key/value head's query heads for dQ) at a
+    // time (measured fastest: the CTAs in flight share two or three heads).
+    const long long share = H / H_kv, budget = 64LL << 20;
+    auto head_group = [&](long long heads, long long head_bytes, long long one_at_a_time) {
+        long long g = heads;
+        if (head_bytes * heads > budget) g = causal ? budget / head_bytes : one_at_a_time;
+        return static_cast<int>(g < 1 ? 1 : (g > heads ? heads : g));
+    };
+    prm.head_group_kv = head_group(BH_kv, 4LL * N * d * share, 1);
+    prm.head_group_q = head_group(BH, (4LL * N * d + share - 1) / share, share);
     prm.scale = scale;
     prm.scale_log2 = scale * kLog2e;
     prm.timeout_ns = fa_wait_timeout_ns();
     prm.status = device_status_word();
     if (!prm.status) return FA_ERR_CUDA;
     if (d == 64)
-        return causal ? launch_tiles<64, true>(tq, tk, tv, tg, prm, BH, stream)
-                      : launch_tiles<64, false>(tq, tk, tv, tg, prm, BH, stream);
-    return causal ? launch_tiles<128, true>(tq, tk, tv, tg, prm, BH, stream)
-                  : launch_tiles<128, false>(tq, tk, tv, tg, prm, BH, stream);
+        return causal ? launch_tiles<64, true>(tq, tk, tv, tg, prm, stream)
+                      : launch_tiles<64, false>(tq, tk, tv, tg, prm, stream);
+    return causal ? launch_tiles<128, true>(tq, tk, tv, tg, prm, stream)
+                  : launch_tiles<128, false>(tq, tk, tv, tg, prm, stream);
 }
 
 }  // namespace osm

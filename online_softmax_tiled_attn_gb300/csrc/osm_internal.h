@@ -66,9 +66,12 @@ int fa_fwd_splitkv_launch(const void* Q, const void* K, const void* V, void* O, 
 int fa_read_device_status(cudaStream_t stream, int* status);
 // Device address of the status word the kernels' bounded waits report to (null on failure).
 int* device_status_word();
+// Q, O, dO, dQ [B, H, N, d]; K, V, dK, dV [B, H_kv, N, d]; LSE, ws_D [B, H, N]; kv_lens null or
+// a device int32 [B] of valid keys per sequence.
 int fa_bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                  const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t BH,
-                  int64_t N, int64_t d, float scale, bool causal, cudaStream_t stream);
+                  const float* LSE, void* dQ, void* dK, void* dV, float* ws_D, int64_t B,
+                  int64_t H, int64_t H_kv, int64_t N, int64_t d, const int32_t* kv_lens,
+                  float scale, bool causal, cudaStream_t stream);
 int selftest_wait_launch(long long timeout_us, cudaStream_t stream);
 
 int osm_softmax_launch(const float* x, float* y, int64_t rows, int64_t cols, float* lse,

@@ -26,7 +26,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "fa_fwd_gqa_plan",
               "osm_softmax", "osm_softmax_topk", "fa_bwd", "fa_fwd_mask", "fa_fwd_mask_plan",
-              "fa_fwd_gqa_mask", "fa_fwd_gqa_mask_plan",
+              "fa_fwd_gqa_mask", "fa_fwd_gqa_mask_plan", "fa_bwd_gqa",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
@@ -51,7 +51,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 8
+    assert binding.lib().osm_attn_abi_version() == 9
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -290,6 +290,31 @@ def test_fa_fwd_gqa_mask_plan():
                 (1, 4, 2, 128, 128, 64, 0, 0, 300)):
         with pytest.raises(binding.FaError):
             binding.gqa_mask_plan(*bad)
+
+
+@pytest.mark.parametrize(
+    "over, want",
+    [
+        (dict(Hkv=3), binding.FA_ERR_INVALID_ARG),                  # H_kv does not divide H
+        (dict(Hkv=0), binding.FA_ERR_INVALID_ARG),
+        (dict(lens=P + 20 * 65536 + 2), binding.FA_ERR_INVALID_ARG),  # misaligned lengths
+        (dict(dk=P + 20 * 65536 - 32), binding.FA_ERR_INVALID_ARG),  # dK reaches the lengths
+        (dict(dv=P + 64), binding.FA_ERR_INVALID_ARG),               # dV inside Q
+        (dict(N=0), binding.FA_OK),
+        (dict(d=96), binding.FA_ERR_UNSUPPORTED),
+    ],
+)
+def test_fa_bwd_gqa_rejects_on_host(over, want):
+    """B1 H4 H_kv 2 N128 d64 at distinct fake addresses (64 KiB slots), lengths at the 21st."""
+    T = 65536
+    a = dict(q=P, k=P + T, v=P + 2 * T, o=P + 3 * T, do=P + 4 * T, lse=P + 5 * T, dq=P + 6 * T,
+             dk=P + 7 * T, dv=P + 8 * T, ws=P + 9 * T, B=1, H=4, Hkv=2, N=128, d=64, scale=0.125,
+             causal=0, lens=P + 20 * T)
+    a.update(over)
+    rc = binding.fa_bwd_gqa_raw(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"],
+                                a["dk"], a["dv"], a["ws"], a["B"], a["H"], a["Hkv"], a["N"],
+                                a["d"], a["scale"], a["causal"], a["lens"], None)
+    assert rc == want
 
 
 def test_selftest_rejects_out_of_range_timeout_on_host():

@@ -80,7 +80,9 @@ def check_grads(got, ref, model, what):
         assert np.isfinite(g).all(), f"{what}: non-finite {name}"
         scale = math.sqrt(float(np.mean(r * r))) if r.size else 0.0
         if scale == 0.0:
-            assert np.abs(g).max(initial=0.0) == 0.0, f"{what}: {name} should be exactly 0"
+            # Every dS is 0 in exact arithmetic (one key per row: dP_i0 = D_i); the kernel's
+            # fp32 dP - D leaves a residual of its rounding, bounded as in the single-key test.
+            assert np.abs(g).max(initial=0.0) <= 1e-4, f"{what}: {name} should be 0"
             continue
         mx, rms = _rel(np.abs(g - r), scale)
         mmx, mrms = _rel(np.abs(m - r), scale)
@@ -155,3 +157,75 @@ def test_bwd_workloads_full_size_sampled(name):
     model = rounding_model(sl(q), sl(k), sl(v), sl(do), w.scale, w.causal)
     got = [np.stack([g[b, h] for b, h in heads])[None] for g in got]
     print(check_grads(got, ref, model, name))
+
+
+def rounding_model_gqa(q, k, v, do, scale, causal, lens):
+    """rounding_model with grouped key/value heads and key lengths: each key/value head's
+    products over its query heads summed in fp64 (fp32 accumulators in the kernel) before the
+    one rounding of dK, dV to bf16; keys at or past a length masked; rows with no key give 0."""
+    bf = lambda t: t.to(torch.bfloat16).double()  # noqa: E731
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    g = H // Hkv
+    q, k, v, do = (t.double() for t in (q, k, v, do))
+    kr, vr = k.repeat_interleave(g, dim=1), v.repeat_interleave(g, dim=1)
+    allowed = torch.ones(B, 1, N, N, dtype=torch.bool)
+    if lens is not None:
+        allowed &= (torch.arange(N)[None, :] < torch.tensor(lens)[:, None])[:, None, None, :]
+    if causal:
+        allowed &= torch.ones(N, N, dtype=torch.bool).tril()[None, None]
+    S = (scale * (q @ kr.transpose(-1, -2))).masked_fill(~allowed, float("-inf"))
+    P = torch.nan_to_num(torch.softmax(S, dim=-1), nan=0.0)
+    O = bf(P @ vr)
+    D = (do * O).sum(-1, keepdim=True)
+    dS = bf(P * (do @ vr.transpose(-1, -2) - D))
+    dV = bf((bf(P).transpose(-1, -2) @ do).reshape(B, Hkv, g, N, d).sum(2))
+    dK = bf(scale * (dS.transpose(-1, -2) @ q).reshape(B, Hkv, g, N, d).sum(2))
+    dQ = bf(scale * (dS @ kr))
+    return [t.numpy() for t in (dQ, dK, dV)]
+
+
+# (B, H, H_kv, N, d, causal, key lengths)
+GQA_CASES = [
+    (2, 4, 2, 256, 64, False, [256, 100]),
+    (2, 4, 1, 300, 128, True, [300, 129]),     # one key/value head for four query heads
+    (1, 8, 2, 384, 128, False, None),
+    (3, 2, 2, 200, 64, True, [0, 200, 57]),   # a sequence with no key; H_kv = H
+    (1, 6, 3, 129, 128, False, [1]),          # a single key
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal,lens", GQA_CASES, ids=lambda x: str(x))
+def test_bwd_gqa_parity(B, H, Hkv, N, d, causal, lens):
+    """fa_bwd_gqa after fa_fwd_gqa (grouped heads, key lengths) against the oracle's gradients,
+    within the rounding model's error."""
+    seed = 9400 + N + d + H
+    q, _, _ = inputs.attn_inputs(B, H, N, d, seed=seed)
+    _, k, v = inputs.attn_inputs(B, Hkv, N, d, seed=seed + 1)
+    do, _, _ = inputs.attn_inputs(B, H, N, d, seed=seed + 2)
+    scale = 1.0 / math.sqrt(d)
+    qc, kc, vc, gc = (t.cuda() for t in (q, k, v, do))
+    kl = torch.tensor(lens, dtype=torch.int32, device="cuda") if lens is not None else None
+    O, L = binding.fa_fwd_gqa(qc, kc, vc, kv_lens=kl, scale=scale, causal=causal)
+    dq, dk, dv = binding.fa_bwd_gqa(qc, kc, vc, O, gc, L, kv_lens=kl, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    got = [t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)]
+    lens_np = np.array(lens, np.int32) if lens is not None else None
+    ref = oracle.attention_bwd(q, k, v, do, scale, causal, kv_lens=lens_np)
+    model = rounding_model_gqa(q, k, v, do, scale, causal, lens)
+    print(check_grads(got, ref, model, f"gqa {(B, H, Hkv, N, d, causal, lens)}"))
+    if lens is not None:
+        for b, n in enumerate(lens):  # keys past the length: exactly zero
+            assert np.all(got[1][b, :, n:] == 0) and np.all(got[2][b, :, n:] == 0)
+
+
+def test_bwd_gqa_matches_mha_entry_point():
+    """With H_kv = H and no key lengths fa_bwd_gqa is fa_bwd, bit for bit."""
+    q, k, v, do = inputs.bwd_inputs(1, 2, 300, 128, seed=9500)
+    qc, kc, vc, gc = (t.cuda() for t in (q, k, v, do))
+    O, L = binding.fa_fwd(qc, kc, vc, causal=True)
+    a = binding.fa_bwd(qc, kc, vc, O, gc, L, causal=True)
+    b = binding.fa_bwd_gqa(qc, kc, vc, O, gc, L, causal=True)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
