@@ -332,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             jt * kTile, bhk);
             }
             int issued = 0;
-            for (int t = 0; t < n_it; ++t) {
+            int hq = bh_q0, it = i0;  // query head and query tile of walked tile t
+            for (int t = 0; t < n_it; ++t, it = it + 1 < prm.n_tiles ? it + 1 : (++hq, i0)) {
                 const int s = t % NS, u = t / NS;  // stage, its use count
                 bool waited = true;
                 if (u >= 1)
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint8_t* q = smem + C::kQ + s * C::kTileBytes;
                 uint8_t* g = smem + C::kG + s * C::kTileBytes;
-                const int hq = bh_q0 + t / n_it1, row = (i0 + t % n_it1) * kTile;
+                const int row = it * kTile;
                 mbar_arrive_expect_tx(&bars[kKvBarFull + s], 2 * C::kTileBytes);
                 for (int h = 0; h < D / 64; ++h) {
                     tma_load_3d(q + h * kHalf, &tmQ, &bars[kKvBarFull + s], h * 64, row, hq);
@@ -463,11 +464,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool stager = st < 256;
         const int col = st & 127;
         const int slot = (col >> 1) * 4 + (col & 1) + (st >= 128 ? 2 : 0);
-        // Walked tile t: query tile i0 + t % n_it1 of query head bh_q0 + t / n_it1.
-        auto stage_value = [&](int t) -> float {
-            const int q = (i0 + t % n_it1) * kTile + col;
+        // Walked tiles run over query tiles i0 .. n_tiles - 1 of query head bh_q0, then of the
+        // next query head of the group, and so on.
+        auto stage_value = [&](int hq, int it) -> float {
+            const int q = it * kTile + col;
             if (q >= N) return st < 128 ? -INFINITY : 0.f;
-            const size_t row = static_cast<size_t>(bh_q0 + t / n_it1) * N + q;
+            const size_t row = static_cast<size_t>(hq) * N + q;
             return st < 128 ? -prm.LSE[row] * kLog2e : -prm.Dv[row];
         };
         // Key rows at or past the sequence's length (or past N: a ragged last key tile) and, on
@@ -475,13 +477,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // allowed column of this row.
         const bool ragged_keys = (jt + 1) * kTile > len;
         const int lo_row = key < len ? 0 : kTile;
-        if (stager && n_it > 0) ld_s[slot] = stage_value(0);
+        if (stager && n_it > 0) ld_s[slot] = stage_value(bh_q0, i0);
         named_bar_sync(1, kSoftWarps * 32);
         bool ok = true;
-        for (int t = 0; t < n_it; ++t) {
-            const int it = i0 + t % n_it1, b = t & 1;
+        int hq = bh_q0, it = i0;  // query head and query tile of walked tile t
+        for (int t = 0; t < n_it; ++t, it = it + 1 < prm.n_tiles ? it + 1 : (++hq, i0)) {
+            const int b = t & 1;
+            const bool wrap = it + 1 == prm.n_tiles;
             const uint32_t t_buf = t_row + C::kTmemBuf + b * 128;
-            const float next = stager && t + 1 < n_it ? stage_value(t + 1) : 0.f;
+            const float next = stager && t + 1 < n_it
+                                   ? stage_value(wrap ? hq + 1 : hq, wrap ? i0 : it + 1)
+                                   : 0.f;
             bool good = mbar_wait(&bars[kKvBarSFull + b], (t >> 1) & 1, tmo);
             if (good) {
                 tc_fence_after();
