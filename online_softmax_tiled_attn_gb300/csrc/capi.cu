@@ -331,7 +331,7 @@ int osm_softmax_topk(const float* x, int64_t rows, int64_t cols, int64_t k, floa
     if (rows < 0 || cols < 0 || k < 1) return FA_ERR_INVALID_ARG;
     if (rows == 0) return FA_OK;
     if (k > cols) return FA_ERR_INVALID_ARG;
-    if (k > 32) return FA_ERR_UNSUPPORTED;
+    if (k > 1024) return FA_ERR_UNSUPPORTED;
     int64_t elems, outs;
     if (!mul_ok(rows, cols, &elems) || !mul_ok(rows, k, &outs) || elems > INT64_MAX / 4)
         return FA_ERR_INVALID_ARG;

@@ -1003,14 +1003,202 @@ int launch(const float* x, long long rows, int cols, int k, float* vals, int* id
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// --------------------------------------------------------------------------------------------
+// k > 32: radix selection, one CTA per row
+// --------------------------------------------------------------------------------------------
+// For k beyond the warp-wide list, the k-th largest value of a row is found exactly by radix
+// selection on an order-preserving 32-bit key of the fp32 values, eight bits at a time: each
+// pass histograms the next digit of the entries that share the digits found so far, and the
+// digit where the count from the top reaches k is the next digit of the k-th largest key T.
+// The first pass also carries the online (m, l) of the row ("The idea"), merged over the CTA by
+// the two-worker merge.  A last pass keeps every entry above T and, of the entries equal to T,
+// the ones with the smallest columns (a scan over chunks of the row in column order), and the
+// k kept entries are sorted (bitonic, in shared memory).  Five passes over the row: the rows in
+// flight (one per CTA) stay in L2 for the later ones.
+constexpr int kSelThreads = 256;
+constexpr int kSelMaxK = 1024;
+
+// Larger value -> larger key, equal values (-0 and +0 included) -> equal keys; NaN is outside
+// the contract.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    uint32_t b = __float_as_uint(v);
+    if (b == 0x80000000u) b = 0u;  // -0 ranks as +0: the tie rule decides between them
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The digit of the k-th largest among the counts hist[0..255] (from the top), and how many of
+// the entries to count from it are still to be taken: on entry `need` entries are wanted, on
+// return need - (count of the larger digits).  Thread 0 only.
+__device__ __forceinline__ int pick_digit(const unsigned* hist, unsigned& need) {
+    unsigned acc = 0;
+    for (int dgt = 255; dgt >= 0; --dgt) {
+        if (acc + hist[dgt] >= need) {
+            need -= acc;
+            return dgt;
+        }
+        acc += hist[dgt];
+    }
+    return 0;  // not reached: the counts of a pass sum to at least `need`
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+    topk_select_rows(const float* __restrict__ x, long long rows, int cols, int k,
+                     float* __restrict__ vals, int32_t* __restrict__ idx, float* __restrict__ lse) {
+    __shared__ unsigned hist[256];
+    __shared__ float sel_v[kSelMaxK];
+    __shared__ int sel_i[kSelMaxK];
+    __shared__ unsigned sh_prefix, sh_need, sh_count, sh_ties;
+    __shared__ unsigned warp_ties[kSelThreads / 32];
+    __shared__ float red_m[kSelThreads / 32], red_l[kSelThreads / 32];
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    int kp = 1;
+    while (kp < k) kp <<= 1;
+    for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * cols;
+        // ---- pass 1: (m, l) and the top digit ----
+        hist[t] = 0u;
+        __syncthreads();
+        Stat st{-INFINITY, 0.f};
+        for (int c = t; c < cols; c += kSelThreads) {
+            const float v[1] = {xr[c]};
+            update<1>(st, v);
+            atomicAdd(&hist[order_key(v[0]) >> 24], 1u);
+        }
+        st = warp_merge(st);
+        if (lane == 0) { red_m[wid] = st.m; red_l[wid] = st.l; }
+        __syncthreads();
+        if (t == 0) {
+            Stat a{red_m[0], red_l[0]};
+            for (int w = 1; w < kSelThreads / 32; ++w) a = merge(a, Stat{red_m[w], red_l[w]});
+            red_m[0] = a.m;
+            red_l[0] = a.l;
+            unsigned need = static_cast<unsigned>(k);
+            sh_prefix = static_cast<unsigned>(pick_digit(hist, need));
+            sh_need = need;
+        }
+        __syncthreads();
+        const float m = red_m[0], l = red_l[0];
+        // ---- passes 2-4: the next digits among the entries that share the prefix ----
+        for (int shift = 16; shift >= 0; shift -= 8) {
+            const unsigned prefix = sh_prefix;
+            hist[t] = 0u;
+            __syncthreads();
+            for (int c = t; c < cols; c += kSelThreads) {
+                const uint32_t key = order_key(xr[c]);
+                if ((key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 0xffu], 1u);
+            }
+            __syncthreads();
+            if (t == 0) {
+                unsigned need = sh_need;
+                sh_prefix = (prefix << 8) | static_cast<unsigned>(pick_digit(hist, need));
+                sh_need = need;
+            }
+            __syncthreads();
+        }
+        // T = sh_prefix; the entries above it all belong to the k, and the first sh_need (by
+        // column) of the entries equal to it.
+        const uint32_t T = sh_prefix;
+        const unsigned ties_wanted = sh_need;
+        if (t == 0) { sh_count = 0u; sh_ties = 0u; }
+        __syncthreads();
+        // ---- pass 5: collect, in chunks of kSelThreads columns so that ties go by column ----
+        for (int c0 = 0; c0 < cols; c0 += kSelThreads) {
+            const int c = c0 + t;
+            const float v = c < cols ? xr[c] : 0.f;
+            const uint32_t key = c < cols ? order_key(v) : 0u;
+            if (c < cols && key > T) {
+                const unsigned slot = atomicAdd(&sh_count, 1u);
+                sel_v[slot] = v;
+                sel_i[slot] = c;
+            }
+            const bool tie = c < cols && key == T;
+            const unsigned b = __ballot_sync(0xffffffffu, tie);
+            if (lane == 0) warp_ties[wid] = __popc(b);
+            __syncthreads();
+            unsigned before_me = sh_ties;  // ties in the chunks before this one
+            for (int w = 0; w < wid; ++w) before_me += warp_ties[w];
+            before_me += __popc(b & ((1u << lane) - 1u));
+            if (tie && before_me < ties_wanted) {
+                const unsigned slot = atomicAdd(&sh_count, 1u);
+                sel_v[slot] = v;
+                sel_i[slot] = c;
+            }
+            __syncthreads();
+            if (t == 0) {
+                unsigned all = 0;
+                for (int w = 0; w < kSelThreads / 32; ++w) all += warp_ties[w];
+                sh_ties += all;
+            }
+            __syncthreads();
+        }
+        // ---- sort the k entries: larger value first, then the smaller column ----
+        for (int i = k + t; i < kp; i += kSelThreads) {
+            sel_v[i] = -INFINITY;
+            sel_i[i] = INT_MAX;
+        }
+        __syncthreads();
+        for (int size = 2; size <= kp; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = t; i < kp; i += kSelThreads) {
+                    const int j = i ^ stride;
+                    if (j > i) {
+                        // ascending in "rank" (best first) for blocks with (i & size) == 0
+                        const bool up = (i & size) == 0;
+                        const bool ij = before(sel_v[j], sel_i[j], sel_v[i], sel_i[i]);
+                        if (ij == up) {
+                            const float tv = sel_v[i];
+                            sel_v[i] = sel_v[j];
+                            sel_v[j] = tv;
+                            const int ti = sel_i[i];
+                            sel_i[i] = sel_i[j];
+                            sel_i[j] = ti;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        // ---- outputs: the shares exp(x - m) / l, the columns, lse = m + ln l ----
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        for (int i = t; i < k; i += kSelThreads) {
+            const float v = sel_v[i];
+            vals[row * k + i] = (m == -INFINITY) ? 0.f : ex2a((v - m) * kLog2e) * inv_l;
+            idx[row * k + i] = sel_i[i];
+        }
+        if (t == 0 && lse != nullptr) lse[row] = (m == -INFINITY) ? -INFINITY : m + logf(l);
+        __syncthreads();
+    }
+}
+
+int launch_select(const float* x, int64_t rows, int cols, int k, float* vals, int32_t* idx,
+                  float* lse, cudaStream_t stream) {
+    static int blocks_per_sm = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, topk_select_rows,
+                                                          kSelThreads, 0) != cudaSuccess)
+            blocks_per_sm = 1;
+    });
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FA_ERR_CUDA;
+    long long grid = static_cast<long long>(sms) * (blocks_per_sm > 0 ? blocks_per_sm : 1);
+    if (grid > rows) grid = rows;
+    topk_select_rows<<<static_cast<unsigned>(grid), kSelThreads, 0, stream>>>(x, rows, cols, k,
+                                                                              vals, idx, lse);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 int osm_softmax_topk_launch(const float* x, int64_t rows, int64_t cols, int64_t k, float* vals,
                             int32_t* idx, float* lse, cudaStream_t stream) {
     if (cols > INT_MAX / 2 || rows > (1LL << 40)) return FA_ERR_UNSUPPORTED;
-    if (k < 1 || k > 32) return FA_ERR_UNSUPPORTED;
+    if (k < 1 || k > kSelMaxK) return FA_ERR_UNSUPPORTED;
     const int c = static_cast<int>(cols), kk = static_cast<int>(k);
     if (k == 1) return launch<LaneBest>(x, rows, c, kk, vals, idx, lse, stream);
+    if (k > 32) return launch_select(x, rows, c, kk, vals, idx, lse, stream);
     return launch<WarpTop>(x, rows, c, kk, vals, idx, lse, stream);
 }
 

@@ -21,7 +21,8 @@ softmax_65536x4000    fp32 rows [65536, 4000], x = 9*N(0,1) and per row one entr
 decode_b8h32q1k32768  B8 H32, one query against 32768 cached keys, d128, N(0,1), non-causal
                       (the split-key path); seed 1007
 softmax_topk_*        the softmax workload's rows with top-k selection: [65536, 4000] k = 8 (seed
-                      1005, the same rows) and a vocabulary-sized [512, 131072] k = 32 (1011)
+                      1005, the same rows), vocabulary-sized [512, 131072] k = 32 (1011) and
+                      k = 100 (1018)
 gqa_*                 grouped key/value heads (H_kv < H) and per-sequence key lengths, N(0,1):
                       a causal prefill, a ragged-length batch and a grouped decode; seeds
                       1008-1010 (see GQA_WORKLOADS)
@@ -439,6 +440,8 @@ TOPK_WORKLOADS = {
     for w in [
         TopkWorkload("softmax_topk_65536x4000_k8", 65536, 4000, 8, 1005),
         TopkWorkload("softmax_topk_512x131072_k32", 512, 131072, 32, 1011),
+        # vocabulary-scale sampling with a wider candidate set (radix selection, k > 32)
+        TopkWorkload("softmax_topk_512x131072_k100", 512, 131072, 100, 1018),
     ]
 }
 

@@ -158,7 +158,7 @@ def test_fa_fwd_gqa_rejects_on_host(args, want):
         ((P, -1, 10, 1, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),
         ((P, 10, 10, 0, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),   # k = 0
         ((P, 10, 10, 11, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),  # k > cols
-        ((P, 10, 100, 33, P + 40960, P + 81920, 0), binding.FA_ERR_UNSUPPORTED),  # k > 32
+        ((P, 10, 2000, 1025, P + 81920, P + 81920 + 65536, 0), binding.FA_ERR_UNSUPPORTED),  # k > 1024
         ((0, 0, 10, 4, 0, 0, 0), binding.FA_OK),                               # no rows
         ((0, 10, 10, 4, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),   # x null
         ((P + 2, 10, 10, 4, P + 4096, P + 8192, 0), binding.FA_ERR_INVALID_ARG),  # misaligned

@@ -82,3 +82,32 @@ def test_topk_full_size_workloads():
         assert np.abs(v.cpu().numpy()[rows] - vr).max() <= parity.SOFTMAX_Y_ATOL, w.name
         lg = l.cpu().numpy()[rows].astype(np.float64)
         assert (np.abs(lg - lr) / np.maximum(1.0, np.abs(lr))).max() <= parity.SOFTMAX_LSE_RTOL
+
+
+# k > 32: radix selection, a CTA per row (short and long rows, k up to the largest supported)
+LARGE_K = [(64, 4000, 33), (16, 32000, 100), (5, 131072, 64), (40, 300, 257), (3, 5000, 1024),
+           (200, 64, 64), (2, 1024, 1024)]
+
+
+@pytest.mark.parametrize("rows,cols,k", LARGE_K, ids=lambda x: str(x))
+def test_topk_large_k_parity(rows, cols, k):
+    x = inputs.softmax_inputs(rows, cols, seed=9300 + rows + cols + k)
+    check(x, k, f"{(rows, cols, k)}")
+
+
+@pytest.mark.parametrize("cols", [300, 5000])
+def test_topk_large_k_ties_and_masked_rows(cols):
+    """The tie rule (the smaller column first) at the k-th place decides which of many equal
+    values are kept; rows of -inf, a constant row, the overflow row."""
+    g = torch.Generator().manual_seed(71 + cols)
+    x = torch.randint(-4, 5, (12, cols), generator=g).to(torch.float32)
+    x[2] = -float("inf")
+    x[2, cols // 2] = 7.0
+    x[3] = -float("inf")
+    x[4, :] = 1000.0
+    x[4, :3] = torch.tensor([1000.0, 1001.0, 1002.0])
+    x[5] = 3.0
+    x[6, ::2] = -0.0                          # -0 and +0 are equal values
+    x[6, 1::2] = 0.0
+    for k in (33, 100, 299):
+        check(x, k, f"ties cols={cols} k={k}")
