@@ -448,20 +448,27 @@ def roofline_hbm(nbytes, ms, peaks, kind, traffic=None):
 # Traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
 # summarised under profiles/, one per workload.  Workloads without a capture report None.
 NCU_TRAFFIC_BYTES = {
-    "mha_b4h16n2048d64": 50.395648e6 + 0.034048e6,
-    "dense_b2h32n8192": 403.199232e6 + 116.581632e6,
-    "causal_b2h32n8192": 701.020672e6 + 119.029504e6,
-    "decode_b8h32q1k32768d128": 4.295266816e9 + 3.664384e6,
-    "gqa_decode_b8h32kv8q1k32768d128": 1.073933824e9 + 5.0816e6,
-    "softmax_65536x4000": 1.048683e9 + 0.997987072e9,
-    "gqa_causal_b2h32kv8n8192d128": 357.92768e6 + 98.847488e6,
-    "softmax_topk_65536x4000_k8": 1.048666e9 + 7.303424e6,
-    "softmax_topk_512x131072_k32": 268.514816e6 + 3.573504e6,
-    "mask_prefixlm_b2h16n4096d128": 102.0864e6 + 12.406784e6,
-    "mask_window_b2h16n8192d128": 203.465216e6 + 45.116672e6,
+    "mha_b4h16n2048d64": 50398208 + 161792,
+    "dense_b2h32n8192": 402963456 + 117450240,
+    "causal_b2h32n8192": 696293888 + 120343296,
+    "causal_b1h8n32768": 857974272 + 50495488,
+    "ragged_b1h16n4000": 49220864 + 304640,
+    "decode_b8h32q1k32768d128": 4295316736 + 3289600,
+    "gqa_causal_b2h32kv8n8192d128": 374551296 + 102765568,
+    "gqa_ragged_b4h32kv8n4096d128": 172563968 + 92564736,
+    "gqa_decode_b8h32kv8q1k32768d128": 1073931520 + 4781312,
+    "mask_prefixlm_b2h16n4096d128": 102075648 + 13495808,
+    "mask_random_b2h16n4096d128": 156299008 + 19236864,
+    "mask_window_b2h16n8192d128": 203645440 + 46541056,
+    "softmax_65536x4000": 1048660992 + 998156288,
+    "softmax_topk_65536x4000_k8": 1048700672 + 6889216,
+    "softmax_topk_512x131072_k32": 268504320 + 2991616,
+    "softmax_topk_512x131072_k100": 517183744 + 3210496,
+    "bwd_b4h16n2048d64": 170632192 + 11614208,
+    "bwd_b2h16n8192d128": 676055552 + 155576832,
+    "bwd_causal_b2h16n8192d128": 904284160 + 151535616,
 }
-# The backward workloads run three kernels per call; their per-kernel traffic is in the
-# bwd_kv_kernel / bwd_q_kernel summaries, and the call's roofline reports none.
+# The backward workloads: the sum over the call's three kernels (bwd_prep, bwd_kv, bwd_q).
 
 
 # ---------------------------------------------------------------------------------------------

@@ -41,7 +41,9 @@
 //                   slot, where the softmax reads them after the slot's barrier.
 //   warps 12-15     epilogue: the two groups' (m, l) combined with the two-worker merge, O read
 //                   from TMEM once the item's last P V is done (the next item's first P V
-//                   waits for that read), O / l to bf16 and LSE = (m + log2 l) * ln 2.
+//                   waits for that read), O / l to bf16 into a 16 KB staging buffer in shared
+//                   memory, 64 columns at a time, each half written out by one TMA store; and
+//                   LSE = (m + log2 l) * ln 2.
 // Causal: key tiles above the diagonal are never visited; only diagonal and ragged tiles are
 // masked element by element.  With an explicit mask's tile map, key tiles holding no allowed
 // key for the query tile are not visited either.
@@ -85,6 +87,7 @@ constexpr float kRescaleHeadroom = 24.0f;
 constexpr uint32_t kBarHandOff = 1;  // named barriers 1, 2: reference max of tile J -> J+1
 constexpr uint32_t kBarTeardown = 3; // named barrier 3: TMEM no longer used (warps 0-9, 12-15)
 constexpr uint32_t kTeardownThreads = 448;
+constexpr uint32_t kBarEpi = 4;      // named barrier 4: the epilogue's four warps
 constexpr int kMaxStages = 8;
 constexpr int kFinSlots = 4;         // final (m, l) of the last items, see fin_full
 
@@ -133,14 +136,26 @@ struct Cfg {
     static constexpr bool kIndep = D == 64;
     static constexpr int kHalves = D / 64;
     static constexpr int kTileBytes = kHalves * kHalfBytes;  // 128 rows x D bf16
-    static constexpr int kStages = D == 128 ? 3 : 5;         // K ring and V ring depth
+    // K ring and V ring depth (d = 64 with a mask: 4, for the mask bits' slots)
+    static constexpr int kStages = D == 128 ? 3 : (M ? 4 : 5);
     static constexpr int kK = 0;
     static constexpr int kV = kK + kStages * kTileBytes;
     static constexpr int kQs = kV + kStages * kTileBytes;     // kIndep: two Q tile buffers
     static constexpr int kMsk = kQs + (kIndep ? 2 * kTileBytes : 0);  // MASK: mask bits
     static constexpr int kMskBytes = kBM * 16;              // 128 query rows x 16 bytes
     static constexpr int kBars = kMsk + (M ? kStages * kMskBytes : 0);
-    static constexpr int kBytes = kBars + static_cast<int>(sizeof(Bars));
+    // The epilogue's staging buffer: 64 columns of the O tile (128 rows x 128 bytes, the
+    // 128-byte swizzle of the tensor map) on their way to a TMA store.
+    static constexpr int kOst = (kBars + static_cast<int>(sizeof(Bars)) + 1023) & ~1023;
+    static constexpr int kOstBytes = kHalfBytes;
+    static constexpr int kBytes = kOst + kOstBytes;
+    // Registers per thread after the role split: the softmax groups hold a row of 128 scores
+    // (at d = 64 they need more than 200); the epilogue writes O into the staging buffer as it
+    // reads it.  Measured at d = 128: 200 for the softmax and 72 for an epilogue that held
+    // half a row while the first half's store drained was 1-3 % slower on the dense case.
+    static constexpr int kSoftRegs = 208;
+    static constexpr int kEpiRegs = 56;
+    static_assert(2 * 128 * kSoftRegs + 128 * 40 + 128 * kEpiRegs <= 65536, "register split");
     static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
     // Waits that let the waiting thread sleep until the phase completes instead of polling:
     // polling takes issue slots from the warps sharing the SMSP.  And the MMA issuers either
@@ -402,7 +417,7 @@ template <int D, bool CAUSAL, bool SPLIT, int MASK = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ MaskMap<MASK> tmM,
-                  const FaKernelParams prm) {
+                  const __grid_constant__ CUtensorMap tmO, const FaKernelParams prm) {
     using C = Cfg<D, (MASK != 0)>;
     constexpr int S_ = C::kStages;
     const int Nq = prm.Nq, Nk = prm.Nk;
@@ -451,11 +466,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
 
     // Registers: a softmax thread holds a whole row of 128 scores, the other warps little:
-    // 2 x 128 x 208 + 128 x 40 + 128 x 56 is the 512 x 128 launched.  Each role branch sets its
+    // 2 x 128 x kSoftRegs + 128 x 40 + 128 x kEpiRegs is the 512 x 128 launched.  Each role branch sets its
     // own limit and never rejoins the others; the TMEM is freed by warp 8 after a named
     // barrier that the softmax groups, warp 9 and the epilogue arrive at when done with it.
     if (warp >= kEpiWarp0) {
-        setmaxnreg_dec<56>();
+        setmaxnreg_dec<C::kEpiRegs>();
         // ------------------------------------------------------------------ epilogue
         // Per item: the two groups' (m, l) merged with the two-worker merge, O / l read from
         // TMEM once every P V of the item is done, then O (bf16, or the fp32 partial for the
@@ -471,11 +486,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (idx < 0) break;
             const Item w = decode_item<CAUSAL, MASK == 2>(idx, prm, tile_map_of<MASK>(tmM), tmap_words_of<MASK>(tmM));
             const int slot = k % kFinSlots;
-            if (!warp_wait(&bars->fin_full[slot], (k / kFinSlots) & 1, timeout_ns, true)) {
-                record_timeout(12);
+            const bool have = w.n_kv > 0;
+            // The groups' (m, l) of the item, and O once its last P V is done.  The four warps
+            // agree on the outcome of their waits before they go on, so that a wait given up
+            // in one of them never leaves the others at the staging barrier.
+            bool good = warp_wait(&bars->fin_full[slot], (k / kFinSlots) & 1, timeout_ns, true);
+            if (!good) record_timeout(12);
+            if (good && have) {
+                good = warp_wait(&bars->o_full, qi & 1, timeout_ns, true);
+                if (!good) record_timeout(13);
+            }
+            if (!named_bar_and(kBarEpi, 128, good)) {
                 ok = false;
                 break;
             }
+            if (have) tc_fence_after();
             const float m0 = bars->fin[slot][0][0][r], l0 = bars->fin[slot][0][1][r];
             const float m1 = bars->fin[slot][1][0][r], l1 = bars->fin[slot][1][1][r];
             __syncwarp();
@@ -486,61 +511,129 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float w0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - M);
             const float w1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
             const float lt = l0 * w0 + l1 * w1;
-            const bool have = w.n_kv > 0;
-            if (have) {
-                if (!warp_wait(&bars->o_full, qi & 1, timeout_ns, true)) {
-                    record_timeout(13);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
             const int q_row = w.q_tile * kBM + r;
             const bool store = q_row < Nq;
             const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
             const size_t row = static_cast<size_t>(w.bh) * Nq + q_row;
             const size_t ws_row = static_cast<size_t>(w.split) * prm.BH * Nq + row;
-            // Columns per step: 32 of the shared accumulator, or 16 of each group's (d = 64),
-            // combined with the merge weights, within the epilogue's register budget.
-            constexpr int CW = C::kIndep ? 16 : 32;
+            if constexpr (SPLIT) {
+                // fp32 partials, stored as they are read: 32 columns of the shared accumulator
+                // per step, or 16 of each group's (d = 64), within the register budget; the
+                // next item's first P V waits for the last step.
+                constexpr int CW = C::kIndep ? 16 : 32;
 #pragma unroll 1
-            for (int c = 0; c < D / CW; ++c) {
-                float o[CW];
-                if (!have) {
+                for (int c = 0; c < D / CW; ++c) {
+                    float o[CW];
+                    if (!have) {
 #pragma unroll
-                    for (int e = 0; e < CW; ++e) o[e] = 0.f;
-                } else if constexpr (C::kIndep) {
-                    uint32_t a[16], b[16];
-                    tmem_ld16x2_sync(tO + c * 16, tO + D + c * 16, a, b);
-                    // A group that weighs 0 may hold another item's sums: never read into O.
+                        for (int e = 0; e < CW; ++e) o[e] = 0.f;
+                    } else if constexpr (C::kIndep) {
+                        uint32_t a[16], b[16];
+                        tmem_ld16x2_sync(tO + c * 16, tO + D + c * 16, a, b);
+                        // A group that weighs 0 may hold another item's sums: never read.
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        o[e] = (w0 != 0.f ? __uint_as_float(a[e]) * w0 : 0.f) +
-                               (w1 != 0.f ? __uint_as_float(b[e]) * w1 : 0.f);
-                } else {
-                    uint32_t a[32];
-                    tmem_ld32_sync(tO + c * 32, a);
+                        for (int e = 0; e < 16; ++e)
+                            o[e] = (w0 != 0.f ? __uint_as_float(a[e]) * w0 : 0.f) +
+                                   (w1 != 0.f ? __uint_as_float(b[e]) * w1 : 0.f);
+                    } else {
+                        uint32_t a[32];
+                        tmem_ld32_sync(tO + c * 32, a);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(a[e]);
-                }
-                // After the last read of O the next item's first P V may overwrite it.
-                if (have && c == D / CW - 1) warp_arrive_tc(&bars->o_free);
-                if (!store) continue;
-                if (SPLIT) {
+                        for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(a[e]);
+                    }
+                    if (have && c == D / CW - 1) warp_arrive_tc(&bars->o_free);
+                    if (!store) continue;
                     float4* dst = reinterpret_cast<float4*>(prm.ws_O + ws_row * D + c * CW);
 #pragma unroll
                     for (int v = 0; v < CW / 4; ++v)
                         dst[v] = make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l,
                                              o[4 * v + 2] * inv_l, o[4 * v + 3] * inv_l);
-                } else {
-                    uint4* dst = reinterpret_cast<uint4*>(prm.O + row * D + c * CW);
+                }
+            } else {
+                // O / l in bf16 through the staging buffer (128 rows x 64 columns, the
+                // 128-byte swizzle of the tensor map), one TMA store of the 128 x 64 box per
+                // half (rows past Nq are not written): one bulk store instead of a 16-byte
+                // store per row and column group, which crowded the softmax's shared-memory
+                // and TMEM traffic.  Each half goes into the buffer as it is read, once the
+                // buffer's previous store has read it; after the last read the next item's
+                // first P V may overwrite O.
+                uint8_t* ost = smem + C::kOst;
+                uint8_t* rowp = ost + r * 128;
+                auto chunk = [&](int j) -> uint4* {  // 16-byte chunk j (columns 8j..8j+7)
+                    return reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
+                };
+                if (threadIdx.x == kEpiWarp0 * 32) bulk_wait_group_read<0>();
+                named_bar_sync(kBarEpi, 128);
+                if constexpr (C::kIndep) {
+                    // The two groups' accumulators, 8 columns of each per step.
 #pragma unroll
-                    for (int v = 0; v < CW / 8; ++v)
-                        dst[v] = make_uint4(
-                            pack_bf16x2(o[8 * v] * inv_l, o[8 * v + 1] * inv_l),
-                            pack_bf16x2(o[8 * v + 2] * inv_l, o[8 * v + 3] * inv_l),
-                            pack_bf16x2(o[8 * v + 4] * inv_l, o[8 * v + 5] * inv_l),
-                            pack_bf16x2(o[8 * v + 6] * inv_l, o[8 * v + 7] * inv_l));
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t q4[4] = {0u, 0u, 0u, 0u};  // bf16 +0 pairs
+                        if (have) {
+                            uint32_t a[8], b[8];
+                            tmem_ld8x2_sync(tO + j * 8, tO + D + j * 8, a, b);
+                            // A group that weighs 0 may hold another item's sums: never read.
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 =
+                                    (w0 != 0.f ? __uint_as_float(a[2 * e]) * w0 : 0.f) +
+                                    (w1 != 0.f ? __uint_as_float(b[2 * e]) * w1 : 0.f);
+                                const float x1 =
+                                    (w0 != 0.f ? __uint_as_float(a[2 * e + 1]) * w0 : 0.f) +
+                                    (w1 != 0.f ? __uint_as_float(b[2 * e + 1]) * w1 : 0.f);
+                                q4[e] = pack_bf16x2(x0 * inv_l, x1 * inv_l);
+                            }
+                        }
+                        *chunk(j) = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+                    }
+                    if (have) warp_arrive_tc(&bars->o_free);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t q8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        if (have) {
+                            uint32_t a[16];
+                            tmem_ld16_sync(tO + c * 16, a);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                q8[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * inv_l,
+                                                    __uint_as_float(a[2 * e + 1]) * inv_l);
+                        }
+                        *chunk(2 * c) = make_uint4(q8[0], q8[1], q8[2], q8[3]);
+                        *chunk(2 * c + 1) = make_uint4(q8[4], q8[5], q8[6], q8[7]);
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(kBarEpi, 128);
+                if (threadIdx.x == kEpiWarp0 * 32) {
+                    tma_store_3d(&tmO, ost, 0, w.q_tile * kBM, w.bh);
+                    bulk_commit_group();
+                }
+                if constexpr (C::kHalves == 2) {
+                    // half 1 into the buffer once half 0's store has read it
+                    if (threadIdx.x == kEpiWarp0 * 32) bulk_wait_group_read<0>();
+                    named_bar_sync(kBarEpi, 128);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t q8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        if (have) {
+                            uint32_t a[16];
+                            tmem_ld16_sync(tO + 64 + c * 16, a);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                q8[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * inv_l,
+                                                    __uint_as_float(a[2 * e + 1]) * inv_l);
+                        }
+                        *chunk(2 * c) = make_uint4(q8[0], q8[1], q8[2], q8[3]);
+                        *chunk(2 * c + 1) = make_uint4(q8[4], q8[5], q8[6], q8[7]);
+                    }
+                    if (have) warp_arrive_tc(&bars->o_free);
+                    fence_proxy_async_smem();
+                    named_bar_sync(kBarEpi, 128);
+                    if (threadIdx.x == kEpiWarp0 * 32) {
+                        tma_store_3d(&tmO, ost, 64, w.q_tile * kBM, w.bh);
+                        bulk_commit_group();
+                    }
                 }
             }
             if (store) {
@@ -553,6 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             qi += have ? 1 : 0;
         }
         (void)ok;
+        // The TMA stores of O have read the staging buffer and written O before the CTA ends.
+        if (!SPLIT && threadIdx.x == kEpiWarp0 * 32) bulk_wait_group<0>();
         tc_fence_before();
         named_bar_arrive(kBarTeardown, kTeardownThreads);
     } else if (warp >= kMmaWarp) {
@@ -845,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_arrive(kBarTeardown, kTeardownThreads);
         }
     } else {
-        setmaxnreg_inc<208>();
+        setmaxnreg_inc<C::kSoftRegs>();
         // -------------------------------------------------------------------- softmax
         const int g = warp >> 2;          // this group takes the key tiles J with J & 1 == g
         const int r = threadIdx.x & 127;  // row in the tile == TMEM lane
@@ -1149,11 +1244,18 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
             g = ((64LL << 20) / kv_bytes) * share;
         p.head_group = static_cast<int>(g < 1 ? 1 : (g > prm.BH ? prm.BH : g));
     }
+    // The output's tensor map (bf16 [BH, Nq, D], as Q's); the split-key kernels write fp32
+    // partials with plain stores and take Q's map in its place.
+    CUtensorMap to = tq;
+    if (!SPLIT) {
+        const int st = make_bhnd_tensor_map(&to, prm.O, prm.BH, prm.Nq, D);
+        if (st != FA_OK) return st;
+    }
     const int sms = device_sm_count();
     const long long ctas = (sms > 0 && items > sms) ? sms : items;
     fa_fwd_kernel<D, CAUSAL, SPLIT, MASK>
         <<<static_cast<unsigned>(ctas), kThreads, C::kDynSmem, stream>>>(
-            tq, tk, tv, mask_map<MASK>(tm, p), static_cast<const FaKernelParams&>(p));
+            tq, tk, tv, mask_map<MASK>(tm, p), to, static_cast<const FaKernelParams&>(p));
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

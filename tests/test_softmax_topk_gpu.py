@@ -84,9 +84,12 @@ def test_topk_full_size_workloads():
         assert (np.abs(lg - lr) / np.maximum(1.0, np.abs(lr))).max() <= parity.SOFTMAX_LSE_RTOL
 
 
-# k > 32: radix selection, a CTA per row (short and long rows, k up to the largest supported)
+# k > 32: a CTA per row, a floor and a candidate buffer (short and long rows, k up to the largest
+# supported; each thread keeps its 1, 2 or 4 largest values as k crosses 256 and 512; 16-byte
+# and 4-byte loads; several chunks per row)
 LARGE_K = [(64, 4000, 33), (16, 32000, 100), (5, 131072, 64), (40, 300, 257), (3, 5000, 1024),
-           (200, 64, 64), (2, 1024, 1024)]
+           (200, 64, 64), (2, 1024, 1024), (3, 131072, 1024), (4, 65536, 512), (4, 65536, 513),
+           (4, 100003, 300), (6, 70001, 40)]
 
 
 @pytest.mark.parametrize("rows,cols,k", LARGE_K, ids=lambda x: str(x))
@@ -95,10 +98,12 @@ def test_topk_large_k_parity(rows, cols, k):
     check(x, k, f"{(rows, cols, k)}")
 
 
-@pytest.mark.parametrize("cols", [300, 5000])
+@pytest.mark.parametrize("cols", [300, 5000, 20000])
 def test_topk_large_k_ties_and_masked_rows(cols):
     """The tie rule (the smaller column first) at the k-th place decides which of many equal
-    values are kept; rows of -inf, a constant row, the overflow row."""
+    values are kept; rows of -inf, a constant row, the overflow row.  At 20000 columns the rows
+    with more entries at the floor than the candidate buffer holds (constant, nearly constant,
+    fewer than k finite values) take the exact radix route."""
     g = torch.Generator().manual_seed(71 + cols)
     x = torch.randint(-4, 5, (12, cols), generator=g).to(torch.float32)
     x[2] = -float("inf")
