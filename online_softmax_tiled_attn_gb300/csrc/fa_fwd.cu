@@ -12,30 +12,38 @@
 //
 // GB300 mapping.  A persistent CTA per SM works through a list of work items, each a 128-row
 // query tile of one (b, h) against a range of its key tiles (128 keys each); the pipelines run
-// on from one item into the next.  Both products run on the tensor cores with A in TMEM:
-//   S = Q K^T   A = Q (tcgen05.cp from shared memory), B = K tile (shared memory, K-major)
-//   O += P V    A = P (TMEM),                          B = V tile (shared memory, MN-major)
-// TMEM (512 columns): S0 [0,128), S1 [128,256), then kP P buffers of 64 columns, O (d columns)
-// and kQ Q buffers of d/2 columns (kP = kQ = 2 for d=64, 1 for d=128); bf16 operands hold two
-// values per 32-bit column.  S of key tile J goes to S(J & 1), P of tile J to P(J % kP).
+// on from one item into the next.  Both products run on the tensor cores:
+//   S = Q K^T   d = 128: A = Q in TMEM (tcgen05.cp from shared memory); d = 64: A = Q in
+//               shared memory; B = K tile (shared memory, K-major)
+//   O += P V    A = P (TMEM), B = V tile (shared memory, MN-major)
+// TMEM (512 columns): S0 [0,128), S1 [128,256), then kP P buffers of 64 columns, kOAcc O
+// accumulators of d columns and kQ Q buffers of d/2 columns: d = 128 one of each (512
+// columns), d = 64 two P buffers and two O accumulators (one per softmax group) and no Q.
+// bf16 operands hold two values per 32-bit column.  S of key tile J goes to S(J & 1), P of
+// tile J to P(J % kP).
 //   warps 0-3, 4-7  two softmax warpgroups that take the key tiles in turn (group g the tiles
 //                   J with J & 1 == g), one query row per thread (its TMEM lane), whole rows:
-//                   tcgen05.ld of the 128 scores, mask, row max, the row's reference max
-//                   handed on from the previous tile through shared memory (a producer /
-//                   consumer named barrier, the only link between the groups), lazy reference
-//                   max, ex2 of the scaled and shifted scores (scale*log2(e) folded into one
-//                   FFMA), the group's own running sum, P rounded to bf16 into a P buffer.
-//                   While one group computes the exponentials of tile J the other already
-//                   works on tile J+1.  When the reference moves (rare: only beyond 2^8) the
-//                   group scales the O accumulator in TMEM by alpha before its P V.  At the
-//                   end of an item each group leaves its (m, l) for the epilogue.
-//   warps 8, 9      tcgen05.mma, one thread each: warp 8 copies each item's Q into TMEM and
+//                   tcgen05.ld of the 128 scores, mask, row max, lazy reference max, ex2 of
+//                   the scaled and shifted scores (scale*log2(e) folded into one FFMA), the
+//                   group's own running sum, P rounded to bf16 into a P buffer.  While one
+//                   group computes the exponentials of tile J the other already works on tile
+//                   J+1.  d = 128: the groups share one O accumulator; the row's reference max
+//                   is handed on from the previous tile through shared memory (a producer /
+//                   consumer named barrier, the only link between the groups), and when it
+//                   moves (rare: only beyond 2^8) the group scales O in TMEM by alpha before
+//                   its P V.  d = 64: each group keeps its own reference max and O
+//                   accumulator, and the epilogue merges the two.  At the end of an item each
+//                   group leaves its (m, l) for the epilogue.
+//   warps 8, 9      tcgen05.mma: warp 8 (d = 128: after copying each item's Q into TMEM)
 //                   issues S(J+2) as soon as S(J) has been read (two tiles ahead of the
 //                   softmax), warp 9 issues O += P(J) V(J) as soon as P(J) is stored.  One
 //                   thread cannot issue M128 N128 K16 MMAs much faster than the tensor core
-//                   runs them, so two independent issuers keep it fed.  fp32 accumulators.
-//   warps 10, 11    TMA: the K ring (each item's Q tile, then its K tiles; warp 10) and the V
-//                   ring (warp 11); 128-byte swizzle, zero fill past the end of the sequence.
+//                   runs them, so two independent issuers keep it fed; at d = 128 each runs
+//                   as a converged warp with one elected lane issuing.  fp32 accumulators.
+//   warps 10, 11    TMA: the K ring (warp 10: d = 128 each item's Q tile, then its K tiles;
+//                   d = 64 the K tiles, and Q into two shared-memory buffers of its own) and
+//                   the V ring (warp 11); 128-byte swizzle, zero fill past the end of the
+//                   sequence.
 //                   With an explicit mask the V producer also brings each tile's mask bits
 //                   (16 bytes for each of the 128 query rows) and the tile's index into the V
 //                   slot, where the softmax reads them after the slot's barrier.
