@@ -71,6 +71,45 @@ OSM_ATTN_API int fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
                         void* stream);
 
 /*
+ * fa_fwd_host -- fa_fwd with its inputs and outputs in host memory, the host <-> device
+ * copies overlapped with the attention.
+ *
+ * Same computation as fa_fwd (the lesson's "From softmax to attention"; each (b, h) is its own
+ * problem, "The implementation").  The B*H heads are cut into n_chunks groups of consecutive
+ * heads, and each group is pipelined:
+ *   1. its Q, K, V are copied from host to the device staging buffers, on an internal stream;
+ *   2. fa_fwd runs on those heads once they have landed, on `stream`;
+ *   3. its O and LSE are copied back once the group is done, on a second internal stream.
+ * So the next group's inputs and the previous group's outputs move while a group computes.
+ *
+ *   Q_host, K_host, V_host  bf16 [B, H, N, d] in host memory, read.  Page-locked memory
+ *            (cudaHostAlloc, cudaHostRegister) lets the copies overlap; pageable memory is
+ *            correct but serialises them.
+ *   O_host   bf16 [B, H, N, d] in host memory, written.
+ *   LSE_host fp32 [B, H, N] in host memory, written; NULL exactly when LSE_dev is NULL.
+ *   Q_dev, K_dev, V_dev, O_dev  device buffers of the same shape (16-byte aligned, none
+ *            overlapping another), LSE_dev fp32 [B, H, N] device (4-byte aligned) or NULL:
+ *            staging owned by the caller, overwritten (O_dev and LSE_dev end holding O, LSE).
+ *   B, H, N, d, scale, causal  as fa_fwd.
+ *   n_chunks 0: chosen here (one group per 12 MB of Q, K, V, 1 to 16 groups); 1 .. 64
+ *            groups otherwise (more groups than heads means one head per group; above 64 is
+ *            FA_ERR_INVALID_ARG).
+ *   stream   cudaStream_t or NULL.  The work is ordered after everything issued to `stream`
+ *            before the call, and everything issued to `stream` after the call waits for all
+ *            of it, the copies back to the host included: synchronise `stream` before reading
+ *            O_host or reusing any buffer.  Calls from several host threads are serialised
+ *            while they enqueue.
+ * Returns as soon as the work is enqueued.  B*H*N == 0 is a no-op.  Errors: as fa_fwd, plus
+ * FA_ERR_INVALID_ARG for a NULL host pointer, LSE_host without LSE_dev or the reverse, or
+ * overlapping device buffers; FA_ERR_CUDA when a copy, an internal stream or an event fails.
+ */
+OSM_ATTN_API int fa_fwd_host(const void* Q_host, const void* K_host, const void* V_host,
+                             void* O_host, float* LSE_host, void* Q_dev, void* K_dev,
+                             void* V_dev, void* O_dev, float* LSE_dev, int64_t B, int64_t H,
+                             int64_t N, int64_t d, float scale, int causal, int64_t n_chunks,
+                             void* stream);
+
+/*
  * fa_fwd_splitkv -- attention of Nq queries against Nk keys with the keys cut into n_splits
  * contiguous ranges that are processed in parallel (Flash-Decoding), then combined.
  *
@@ -392,7 +431,7 @@ OSM_ATTN_API int osm_attn_selftest_wait(int64_t timeout_us, void* stream);
 /* ABI version of this header (incremented on any incompatible change). */
 OSM_ATTN_API int osm_attn_abi_version(void);
 
-#define OSM_ATTN_ABI_VERSION 9
+#define OSM_ATTN_ABI_VERSION 10
 
 #ifdef __cplusplus
 }

@@ -45,6 +45,9 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_int, vp]
             L.fa_fwd.restype = ctypes.c_int
+            L.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                      i64, ctypes.c_float, ctypes.c_int, i64, vp]
+            L.fa_fwd_host.restype = ctypes.c_int
             L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                          ctypes.c_float, ctypes.c_int, i64, vp, vp, vp]
             L.fa_fwd_splitkv.restype = ctypes.c_int
@@ -114,6 +117,13 @@ def _stream_handle(stream):
 def fa_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, stream_ptr):
     return lib().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
                         float(scale), int(bool(causal)), stream_ptr)
+
+
+def fa_fwd_host_raw(qh, kh, vh, oh, lseh, qd, kd, vd, od, lsed, B, H, N, d, scale, causal,
+                    n_chunks, stream_ptr):
+    return lib().fa_fwd_host(qh, kh, vh, oh, lseh, qd, kd, vd, od, lsed, int(B), int(H),
+                             int(N), int(d), float(scale), int(bool(causal)), int(n_chunks),
+                             stream_ptr)
 
 
 def fa_fwd_splitkv_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, causal,
@@ -265,6 +275,60 @@ def fa_fwd(q, k, v, scale=None, causal=False, out=None, lse=None, return_lse=Tru
                     _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+    return out, lse
+
+
+def fa_fwd_host(q, k, v, scale=None, causal=False, out=None, lse=None, return_lse=True,
+                staging=None, n_chunks=0, stream=None):
+    """O, LSE = attention(q, k, v) for host (CPU) bf16 tensors [B, H, N, d]: the library copies
+    groups of heads to the device, runs the attention and copies O and LSE back, the copies
+    overlapped with the attention.  q, k, v and `out`/`lse` (host, made page-locked here when
+    not given) should be page-locked for the overlap.  `staging` may be the device tensors
+    (q_dev, k_dev, v_dev, o_dev, lse_dev or None); otherwise they are allocated here on the
+    current CUDA device.  Enqueued on `stream` (the current stream by default); the results are
+    ready once it is synchronised, which this function does before it returns."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise TypeError(f"{name} must be a host (CPU) tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 [B, H, N, d] tensor")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    for name, t, dt, n in (("out", out, torch.bfloat16, q.numel()),
+                           ("lse", lse, torch.float32, B * H * N)):
+        if t is not None and (t.is_cuda or t.dtype != dt or t.numel() != n
+                              or not t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous host tensor of {n} {dt} elements")
+    if staging is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        qd = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        staging = (qd, torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd),
+                   torch.empty((B, H, N), dtype=torch.float32, device=dev)
+                   if lse is not None else None)
+    qd, kd, vd, od, ld = staging
+    for t in (qd, kd, vd, od):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.numel() != q.numel():
+            raise TypeError("staging must hold four CUDA bf16 tensors shaped like q")
+    if (ld is None) != (lse is None):
+        raise TypeError("staging's LSE tensor must be given exactly when lse is")
+    s = _stream_handle(stream)
+    rc = fa_fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, qd.data_ptr(),
+                         kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+                         ld.data_ptr() if ld is not None else None, B, H, N, d, scale, causal,
+                         n_chunks, s)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_host")
+    (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return out, lse
 
 

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "osm_internal.h"
 
@@ -130,6 +131,45 @@ int attention_call(const void* Q, const void* K, const void* V, void* O, float* 
 
 }  // namespace
 
+namespace {
+
+// fa_fwd_host's copy streams and events, one set per device, made on first use and kept for
+// the life of the process; calls enqueue under one lock, so that the events of one call are
+// not re-recorded by another before its waits are enqueued.
+constexpr int kHostPipeMaxChunks = 64;
+constexpr int kHostPipeMaxDevices = 64;
+struct HostPipe {
+    bool ready = false;
+    // One stream each way.  (A host-to-device stream per input, Q, K and V, made the copies of
+    // B2 H32 N8192 d128 slower, not faster: 723 against 914 TFLOP/s end to end.)
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in[kHostPipeMaxChunks] = {}, out[kHostPipeMaxChunks] = {};
+};
+std::mutex g_host_pipe_mu;
+HostPipe g_host_pipes[kHostPipeMaxDevices];
+
+// The current device's pipe (made if needed), or nullptr.  Caller holds g_host_pipe_mu.
+HostPipe* host_pipe() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kHostPipeMaxDevices)
+        return nullptr;
+    HostPipe& p = g_host_pipes[dev];
+    if (p.ready) return &p;
+    bool ok = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.done, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; ok && c < kHostPipeMaxChunks; ++c)
+        ok = cudaEventCreateWithFlags(&p.in[c], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p.out[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return nullptr;  // what was made stays for the next attempt to reuse
+    p.ready = true;
+    return &p;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fa_fwd_gqa_plan(int64_t B, int64_t H, int64_t H_kv, int64_t Nq, int64_t Nk, int64_t d,
@@ -181,6 +221,95 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
         return FA_ERR_INVALID_ARG;
     return osm::fa_fwd_launch(Q, K, V, O, LSE, bh, N, d, scale, causal != 0,
                               static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_host(const void* Q_host, const void* K_host, const void* V_host, void* O_host,
+                float* LSE_host, void* Q_dev, void* K_dev, void* V_dev, void* O_dev,
+                float* LSE_dev, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                int causal, int64_t n_chunks, void* stream) {
+    if (B < 0 || H < 0 || N < 0 || d < 0 || n_chunks < 0 || n_chunks > kHostPipeMaxChunks)
+        return FA_ERR_INVALID_ARG;
+    int64_t bh, rows, elems;
+    if (!mul_ok(B, H, &bh) || !mul_ok(bh, N, &rows) || !mul_ok(rows, d, &elems) ||
+        elems > INT64_MAX / 2)
+        return FA_ERR_INVALID_ARG;
+    if (rows == 0) return FA_OK;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!Q_host || !K_host || !V_host || !O_host) return FA_ERR_INVALID_ARG;
+    if ((LSE_host == nullptr) != (LSE_dev == nullptr)) return FA_ERR_INVALID_ARG;
+    if (!Q_dev || !K_dev || !V_dev || !O_dev) return FA_ERR_INVALID_ARG;
+    if (!aligned(Q_dev, 16) || !aligned(K_dev, 16) || !aligned(V_dev, 16) ||
+        !aligned(O_dev, 16) || (LSE_dev && !aligned(LSE_dev, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    const uint64_t bytes = static_cast<uint64_t>(elems) * 2;     // each of Q, K, V, O
+    const uint64_t lse_bytes = static_cast<uint64_t>(rows) * 4;  // LSE
+    const void* dev[4] = {Q_dev, K_dev, V_dev, O_dev};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(dev[i], bytes, dev[j], bytes)) return FA_ERR_INVALID_ARG;
+        if (LSE_dev && overlaps(LSE_dev, lse_bytes, dev[i], bytes)) return FA_ERR_INVALID_ARG;
+    }
+    // Groups of whole heads, never more than the heads.  By default one group per 12 MB of
+    // inputs, 1 to 16 groups: measured on GB300, B2 H32 N8192 d128 (403 MB) ran best at 8-16
+    // groups and B4 H16 N2048 d64 (50 MB) at 4; smaller groups pay launch and copy latency.
+    int64_t n = n_chunks;
+    if (n == 0) {
+        const uint64_t in_bytes = 3 * bytes;
+        n = static_cast<int64_t>(in_bytes / (12ull << 20));
+        n = n < 1 ? 1 : (n > 16 ? 16 : n);
+    }
+    if (n > bh) n = bh;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_host_pipe_mu);
+    HostPipe* P = host_pipe();
+    if (!P) return FA_ERR_CUDA;
+    const uint64_t head_bytes = static_cast<uint64_t>(N) * static_cast<uint64_t>(d) * 2;
+    const uint64_t head_lse = static_cast<uint64_t>(N) * 4;
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    if (!ok(cudaEventRecord(P->start, st)) || !ok(cudaStreamWaitEvent(P->h2d, P->start, 0)) ||
+        !ok(cudaStreamWaitEvent(P->d2h, P->start, 0)))
+        return FA_ERR_CUDA;
+    int rc = FA_OK;
+    for (int64_t c = 0; c < n && rc == FA_OK; ++c) {
+        const int64_t h0 = bh * c / n, h1 = bh * (c + 1) / n;  // heads [h0, h1)
+        const uint64_t off = static_cast<uint64_t>(h0) * head_bytes;
+        const uint64_t len = static_cast<uint64_t>(h1 - h0) * head_bytes;
+        auto at = [&](const void* base, uint64_t o) {
+            return static_cast<const char*>(base) + o;
+        };
+        auto atw = [&](void* base, uint64_t o) { return static_cast<char*>(base) + o; };
+        if (!ok(cudaMemcpyAsync(atw(Q_dev, off), at(Q_host, off), len, cudaMemcpyHostToDevice,
+                                P->h2d)) ||
+            !ok(cudaMemcpyAsync(atw(K_dev, off), at(K_host, off), len, cudaMemcpyHostToDevice,
+                                P->h2d)) ||
+            !ok(cudaMemcpyAsync(atw(V_dev, off), at(V_host, off), len, cudaMemcpyHostToDevice,
+                                P->h2d)) ||
+            !ok(cudaEventRecord(P->in[c], P->h2d)) || !ok(cudaStreamWaitEvent(st, P->in[c], 0))) {
+            rc = FA_ERR_CUDA;
+            break;
+        }
+        float* lse_c = LSE_dev ? LSE_dev + h0 * N : nullptr;
+        rc = osm::fa_fwd_launch(at(Q_dev, off), at(K_dev, off), at(V_dev, off), atw(O_dev, off),
+                                lse_c, h1 - h0, N, d, scale, causal != 0, st);
+        if (rc != FA_OK) break;
+        if (!ok(cudaEventRecord(P->out[c], st)) || !ok(cudaStreamWaitEvent(P->d2h, P->out[c], 0)) ||
+            !ok(cudaMemcpyAsync(atw(O_host, off), at(O_dev, off), len, cudaMemcpyDeviceToHost,
+                                P->d2h)) ||
+            (LSE_host && !ok(cudaMemcpyAsync(LSE_host + h0 * N, lse_c,
+                                             static_cast<uint64_t>(h1 - h0) * head_lse,
+                                             cudaMemcpyDeviceToHost, P->d2h)))) {
+            rc = FA_ERR_CUDA;
+            break;
+        }
+    }
+    // Whatever was enqueued, `stream` waits for both copy streams before its later work.
+    const bool joined = ok(cudaEventRecord(P->done, P->d2h)) &&
+                        ok(cudaStreamWaitEvent(st, P->done, 0)) &&
+                        ok(cudaEventRecord(P->done, P->h2d)) &&
+                        ok(cudaStreamWaitEvent(st, P->done, 0));
+    if (rc == FA_OK && !joined) rc = FA_ERR_CUDA;
+    return rc;
 }
 
 int fa_fwd_splitkv_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,

@@ -26,7 +26,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_gqa", "fa_fwd_gqa_plan",
               "osm_softmax", "osm_softmax_topk", "fa_bwd", "fa_fwd_mask", "fa_fwd_mask_plan",
-              "fa_fwd_gqa_mask", "fa_fwd_gqa_mask_plan", "fa_bwd_gqa",
+              "fa_fwd_gqa_mask", "fa_fwd_gqa_mask_plan", "fa_bwd_gqa", "fa_fwd_host",
               "fa_status_string", "osm_attn_device_status", "osm_attn_selftest_wait",
               "osm_attn_abi_version"):
         assert n in names
@@ -51,7 +51,7 @@ def test_status_strings_and_version():
     for s in range(1, 5):
         assert binding.status_string(s).startswith("FA_ERR_")
     assert binding.status_string(99) == "unknown fa_status"
-    assert binding.lib().osm_attn_abi_version() == 9
+    assert binding.lib().osm_attn_abi_version() == 10
 
 
 # A fake device address: every case below must be rejected on the host, before any launch,
@@ -314,6 +314,38 @@ def test_fa_bwd_gqa_rejects_on_host(over, want):
     rc = binding.fa_bwd_gqa_raw(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"],
                                 a["dk"], a["dv"], a["ws"], a["B"], a["H"], a["Hkv"], a["N"],
                                 a["d"], a["scale"], a["causal"], a["lens"], None)
+    assert rc == want
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(qh=0), binding.FA_ERR_INVALID_ARG),                  # NULL host input
+    (dict(oh=0), binding.FA_ERR_INVALID_ARG),                  # NULL host output
+    (dict(lh=0), binding.FA_ERR_INVALID_ARG),                  # LSE on the device only
+    (dict(ld=0), binding.FA_ERR_INVALID_ARG),                  # LSE on the host only
+    (dict(kd=P + 8 * 65536 + 32), binding.FA_ERR_INVALID_ARG),  # K staging overlaps O staging
+    (dict(ld=P + 5 * 65536 + 64), binding.FA_ERR_INVALID_ARG),  # LSE staging inside V staging
+    (dict(vd=P + 6 * 65536 + 8), binding.FA_ERR_INVALID_ARG),  # misaligned staging
+    (dict(d=96), binding.FA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), binding.FA_ERR_INVALID_ARG),
+    (dict(chunks=-1), binding.FA_ERR_INVALID_ARG),
+    (dict(chunks=65), binding.FA_ERR_INVALID_ARG),
+    (dict(N=0), binding.FA_OK),                                 # empty: nothing enqueued
+])
+def test_fa_fwd_host_rejects_on_host(over, want):
+    """B1 H2 N128 d64 (32 KiB per tensor) at distinct fake addresses (64 KiB slots)."""
+    T = 65536
+    a = dict(qh=P, kh=P + T, vh=P + 2 * T, oh=P + 3 * T, lh=P + 4 * T, qd=P + 5 * T,
+             kd=P + 6 * T, vd=P + 7 * T, od=P + 8 * T, ld=P + 9 * T, B=1, H=2, N=128, d=64,
+             scale=0.125, chunks=0)
+    a.update(over)
+    # the LSE staging test above places LSE inside V's staging slot
+    if over.get("ld") == P + 5 * T + 64:
+        a["vd"] = P + 5 * T
+        a["qd"] = P + 11 * T
+    rc = binding.fa_fwd_host_raw(a["qh"] or None, a["kh"], a["vh"], a["oh"] or None,
+                                 a["lh"] or None, a["qd"], a["kd"], a["vd"], a["od"],
+                                 a["ld"] or None, a["B"], a["H"], a["N"], a["d"], a["scale"],
+                                 0, a["chunks"], None)
     assert rc == want
 
 
