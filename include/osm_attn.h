@@ -378,8 +378,9 @@ OSM_ATTN_API int fa_bwd_gqa(const void* Q, const void* K, const void* V, const v
  *   k        1 .. min(cols, 1024) (k > 1024: FA_ERR_UNSUPPORTED; k > cols: FA_ERR_INVALID_ARG).
  *            k <= 32 reads each row once (a warp-wide list of the best k); larger k reads
  *            it twice: a floor under the k-th largest value, then every entry at or above the
- *            floor into a buffer that is sorted (rows where more than 8192 entries reach the
- *            floor fall back to radix selection, five more passes).
+ *            floor into a buffer that is sorted (rows where more than 4096 entries at
+ *            k <= 256, 8192 above, reach the floor fall back to radix selection, five more
+ *            passes).
  *   values   fp32 [rows, k], indices int32 [rows, k], lse fp32 [rows] or NULL; written; none
  *            may overlap x or each other.
  * rows == 0 is a no-op.  All pointers are device pointers; asynchronous on `stream`.

@@ -1006,13 +1006,13 @@ int launch(const float* x, long long rows, int cols, int k, float* vals, int* id
 // --------------------------------------------------------------------------------------------
 // k > 32: a floor, candidates in shared memory, one CTA per row
 // --------------------------------------------------------------------------------------------
-// For k beyond the warp-wide list, a CTA of kSelThreads threads takes a row in chunks of
+// For k beyond the warp-wide list, a CTA of T threads (256 or 512) takes a row in chunks of
 // `chunk` columns, and runs two passes over each chunk before it takes the next one:
 //   * pass 1 carries each thread's online (m, l) of "The idea" and the Q largest values the
-//     thread has seen (Q = 1, 2 or 4, so that kSelThreads * Q >= 2k).  Any thread whose Q-th
+//     thread has seen (Q = 1, 2 or 4, the fewest with T * Q >= 2k).  Any thread whose Q-th
 //     largest is at least F has Q entries of the row at or above F; so the ceil(k / Q)-th
 //     largest of the threads' Q-th largest values is a floor F under the k-th largest value of
-//     the row (a bitonic sort of the kSelThreads values in shared memory picks it).  F only
+//     the row (a bitonic network over the CTA's T values picks it).  F only
 //     rises from chunk to chunk;
 //   * pass 2 appends every entry at or above F to a candidate buffer in shared memory (a warp
 //     reserves its slots with one atomic).  An entry of an earlier chunk at or above the
@@ -1021,15 +1021,18 @@ int launch(const float* x, long long rows, int cols, int k, float* vals, int* id
 //     included.  Entries below F are dropped from the buffer when it is half full.
 // At the end of the row the (m, l) pairs meet by the two-worker merge, the buffer is sorted
 // (larger value first, then the smaller column) and its first k entries are the row's top k.
-// Rows where more than kSelCap entries reach the floor (many ties at it, or fewer than k
+// Rows where more than 16 T entries reach the floor (many ties at it, or fewer than k
 // finite values) take the exact route instead: radix selection of the k-th largest on an
 // order-preserving 32-bit key, eight bits per pass over the row, then a pass in column order
 // that keeps the entries above it and the first of the entries equal to it.
-constexpr int kSelThreads = 512;
-constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelMaxK = 1024;
-constexpr int kSelCap = 8192;  // candidate entries (value, column) in shared memory
-constexpr int kSelSmem = kSelCap * 8;
+// A CTA of T threads keeps 16 T candidate entries (value, column) in shared memory.
+template <int T>
+struct SelCfg {
+    static constexpr int kWarps = T / 32;
+    static constexpr int kCap = 16 * T;
+    static constexpr int kSmem = kCap * 8;
+};
 
 // Larger value -> larger key, equal values (-0 and +0 included) -> equal keys; NaN is outside
 // the contract.
@@ -1054,13 +1057,14 @@ __device__ __forceinline__ int pick_digit(const unsigned* hist, unsigned& need) 
     return 0;  // not reached: the counts of a pass sum to at least `need`
 }
 
-// Bitonic sort of n (a power of two, up to kSelCap) pairs in shared memory, best first
+// Bitonic sort of n (a power of two, up to SelCfg<T>::kCap) pairs in shared memory, best first
 // (larger value, then the smaller column).  Every thread of the CTA calls it.
+template <int T>
 __device__ __forceinline__ void sort_pairs(float* sv, int* si, int n) {
     const int t = threadIdx.x;
     for (int size = 2; size <= n; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = t; i < n; i += kSelThreads) {
+            for (int i = t; i < n; i += T) {
                 const int j = i ^ stride;
                 if (j > i) {
                     const bool up = (i & size) == 0;  // this block ascends in rank
@@ -1080,7 +1084,8 @@ __device__ __forceinline__ void sort_pairs(float* sv, int* si, int n) {
 }
 
 // Exclusive prefix sum over the CTA of one count per thread; *total gets the sum.  Uses
-// scratch[kSelWarps]; every thread calls it.
+// scratch[SelCfg<T>::kWarps]; every thread calls it.
+template <int T>
 __device__ __forceinline__ unsigned cta_exclusive_scan(unsigned v, unsigned* scratch,
                                                        unsigned* total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -1094,7 +1099,7 @@ __device__ __forceinline__ unsigned cta_exclusive_scan(unsigned v, unsigned* scr
     __syncthreads();
     unsigned base = 0, all = 0;
 #pragma unroll
-    for (int w = 0; w < kSelWarps; ++w) {
+    for (int w = 0; w < SelCfg<T>::kWarps; ++w) {
         const unsigned c = scratch[w];
         base += w < wid ? c : 0u;
         all += c;
@@ -1105,25 +1110,26 @@ __device__ __forceinline__ unsigned cta_exclusive_scan(unsigned v, unsigned* scr
 }
 
 // Keeps the first n buffer entries at or above f (in some order); returns their count.
+template <int T>
 __device__ __forceinline__ unsigned drop_below(float* sv, int* si, unsigned n, float f,
                                                unsigned* scratch) {
-    constexpr int kPer = kSelCap / kSelThreads;
+    constexpr int kPer = SelCfg<T>::kCap / T;
     const int t = threadIdx.x;
     float v[kPer];
     int c[kPer];
     unsigned keep = 0;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-        const unsigned i = static_cast<unsigned>(e * kSelThreads + t);
+        const unsigned i = static_cast<unsigned>(e * T + t);
         v[e] = i < n ? sv[i] : -INFINITY;
         c[e] = i < n ? si[i] : 0;
         keep += (i < n && v[e] >= f) ? 1u : 0u;
     }
     unsigned total;
-    unsigned pos = cta_exclusive_scan(keep, scratch, &total);  // all reads done (barrier)
+    unsigned pos = cta_exclusive_scan<T>(keep, scratch, &total);  // all reads done (barrier)
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-        const unsigned i = static_cast<unsigned>(e * kSelThreads + t);
+        const unsigned i = static_cast<unsigned>(e * T + t);
         if (i < n && v[e] >= f) {
             sv[pos] = v[e];
             si[pos] = c[e];
@@ -1134,14 +1140,15 @@ __device__ __forceinline__ unsigned drop_below(float* sv, int* si, unsigned n, f
     return total;
 }
 
+template <int T>
 struct SelShared {
-    float xv[2][kSelThreads];  // exchange buffers of cta_sort_desc
-    int xc[2][kSelThreads];
+    float xv[2][T];  // exchange buffers of cta_sort_desc
+    int xc[2][T];
     float floor;
     unsigned hist[256];
-    unsigned scratch[kSelWarps];
-    unsigned warp_ties[kSelWarps];
-    float red_m[kSelWarps], red_l[kSelWarps];
+    unsigned scratch[SelCfg<T>::kWarps];
+    unsigned warp_ties[SelCfg<T>::kWarps];
+    float red_m[SelCfg<T>::kWarps], red_l[SelCfg<T>::kWarps];
     unsigned count, prefix, need, ties;
     int overflow;
 };
@@ -1149,10 +1156,11 @@ struct SelShared {
 // Bitonic sort of one (value, column) pair per thread over the CTA, best first: thread i ends
 // with the (i+1)-th best pair.  Partners less than a warp apart trade by shuffles; the others
 // through two alternating shared buffers, one barrier per such step.
-__device__ __forceinline__ void cta_sort_desc(float& v, int& c, SelShared& sh) {
+template <int T>
+__device__ __forceinline__ void cta_sort_desc(float& v, int& c, SelShared<T>& sh) {
     const int i = threadIdx.x;
     int buf = 0;
-    for (int size = 2; size <= kSelThreads; size <<= 1) {
+    for (int size = 2; size <= T; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             float ov;
             int oc;
@@ -1178,18 +1186,19 @@ __device__ __forceinline__ void cta_sort_desc(float& v, int& c, SelShared& sh) {
 }
 
 // The exact route: the k entries of the row (in some order) into sv/si, by radix selection.
+template <int T>
 __device__ void select_exact(const float* __restrict__ xr, int cols, int k, float* sv, int* si,
-                             SelShared& sh) {
+                             SelShared<T>& sh) {
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     if (t == 0) {
         sh.prefix = 0u;
         sh.need = static_cast<unsigned>(k);
     }
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = t; i < 256; i += kSelThreads) sh.hist[i] = 0u;
+        for (int i = t; i < 256; i += T) sh.hist[i] = 0u;
         __syncthreads();
         const unsigned prefix = sh.prefix;
-        for (int c = t; c < cols; c += kSelThreads) {
+        for (int c = t; c < cols; c += T) {
             const uint32_t key = order_key(xr[c]);
             if (shift == 24 || (key >> (shift + 8)) == prefix)
                 atomicAdd(&sh.hist[(key >> shift) & 0xffu], 1u);
@@ -1202,25 +1211,25 @@ __device__ void select_exact(const float* __restrict__ xr, int cols, int k, floa
         }
         __syncthreads();
     }
-    // sh.prefix is the k-th largest key T: every entry above it is kept, and the first sh.need
+    // sh.prefix is the k-th largest key: every entry above it is kept, and the first sh.need
     // (by column) of the entries equal to it.
-    const uint32_t T = sh.prefix;
+    const uint32_t kth = sh.prefix;
     const unsigned ties_wanted = sh.need;
     if (t == 0) {
         sh.count = 0u;
         sh.ties = 0u;
     }
     __syncthreads();
-    for (int c0 = 0; c0 < cols; c0 += kSelThreads) {
+    for (int c0 = 0; c0 < cols; c0 += T) {
         const int c = c0 + t;
         const float v = c < cols ? xr[c] : 0.f;
         const uint32_t key = c < cols ? order_key(v) : 0u;
-        if (c < cols && key > T) {
+        if (c < cols && key > kth) {
             const unsigned slot = atomicAdd(&sh.count, 1u);
             sv[slot] = v;
             si[slot] = c;
         }
-        const bool tie = c < cols && key == T;
+        const bool tie = c < cols && key == kth;
         const unsigned b = __ballot_sync(0xffffffffu, tie);
         if (lane == 0) sh.warp_ties[wid] = __popc(b);
         __syncthreads();
@@ -1235,7 +1244,7 @@ __device__ void select_exact(const float* __restrict__ xr, int cols, int k, floa
         __syncthreads();
         if (t == 0) {
             unsigned all = 0;
-            for (int w = 0; w < kSelWarps; ++w) all += sh.warp_ties[w];
+            for (int w = 0; w < SelCfg<T>::kWarps; ++w) all += sh.warp_ties[w];
             sh.ties += all;
         }
         __syncthreads();
@@ -1243,10 +1252,10 @@ __device__ void select_exact(const float* __restrict__ xr, int cols, int k, floa
 }
 
 // Appends, for every lane whose p[e] holds, (x[e], col[e]) to the buffer; a warp reserves its
-// slots with one atomic.  Entries past kSelCap are not stored and mark the row overflowed.
-template <int N>
+// slots with one atomic.  Entries past SelCfg<T>::kCap are not stored and mark the row overflowed.
+template <int T, int N>
 __device__ __forceinline__ void append(const float (&x)[N], const int (&col)[N],
-                                       const bool (&p)[N], float* sv, int* si, SelShared& sh) {
+                                       const bool (&p)[N], float* sv, int* si, SelShared<T>& sh) {
     const int lane = threadIdx.x & 31;
     unsigned mine = 0;
 #pragma unroll
@@ -1264,7 +1273,7 @@ __device__ __forceinline__ void append(const float (&x)[N], const int (&col)[N],
 #pragma unroll
     for (int e = 0; e < N; ++e) {
         if (p[e]) {
-            if (base < kSelCap) {
+            if (base < SelCfg<T>::kCap) {
                 sv[base] = x[e];
                 si[base] = col[e];
             } else {
@@ -1284,15 +1293,15 @@ __device__ __forceinline__ void keep_largest(float (&b)[Q], float v) {
     }
 }
 
-template <int Q, bool VEC>
-__global__ void __launch_bounds__(kSelThreads, 2)
+template <int T, int Q, bool VEC>
+__global__ void __launch_bounds__(T, 1024 / T)
     topk_select_rows(const float* __restrict__ x, long long rows, int cols, int k, int chunk,
                      float* __restrict__ vals, int32_t* __restrict__ idx,
                      float* __restrict__ lse) {
     extern __shared__ __align__(16) unsigned char sel_smem[];
     float* sv = reinterpret_cast<float*>(sel_smem);
-    int* si = reinterpret_cast<int*>(sel_smem + kSelCap * 4);
-    __shared__ SelShared sh;
+    int* si = reinterpret_cast<int*>(sel_smem + SelCfg<T>::kCap * 4);
+    __shared__ SelShared<T> sh;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int r_bar = (k + Q - 1) / Q;  // the floor is the r_bar-th largest thread bar
     for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -1314,11 +1323,11 @@ __global__ void __launch_bounds__(kSelThreads, 2)
                 const float4* r4 = reinterpret_cast<const float4*>(xr);
                 const int u1 = c1 >> 2;
                 constexpr int kAhead = 4;
-                for (int u0 = (c0 >> 2) + t; u0 < u1; u0 += kAhead * kSelThreads) {
+                for (int u0 = (c0 >> 2) + t; u0 < u1; u0 += kAhead * T) {
                     float4 q[kAhead];
 #pragma unroll
                     for (int a = 0; a < kAhead; ++a) {
-                        const int u = u0 + a * kSelThreads;
+                        const int u = u0 + a * T;
                         q[a] = u < u1 ? __ldg(r4 + u)
                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                     }
@@ -1331,11 +1340,11 @@ __global__ void __launch_bounds__(kSelThreads, 2)
                     }
                 }
             } else {
-                for (int j0 = c0 + t; j0 < c1; j0 += 4 * kSelThreads) {
+                for (int j0 = c0 + t; j0 < c1; j0 += 4 * T) {
                     float v[4];
 #pragma unroll
                     for (int a = 0; a < 4; ++a) {
-                        const int j = j0 + a * kSelThreads;
+                        const int j = j0 + a * T;
                         v[a] = j < c1 ? __ldg(xr + j) : -INFINITY;
                     }
                     update(st, v);
@@ -1347,16 +1356,16 @@ __global__ void __launch_bounds__(kSelThreads, 2)
             {
                 float bv = best[Q - 1];
                 int bc = t;
-                cta_sort_desc(bv, bc, sh);
+                cta_sort_desc<T>(bv, bc, sh);
                 if (t == r_bar - 1) sh.floor = bv;
                 __syncthreads();
                 F = fmaxf(F, sh.floor);
             }
             // ---- drop what fell below the floor once the buffer is half full ----
             const unsigned n_now = sh.count;
-            if (n_now > kSelCap / 2 && n_now <= kSelCap) {
+            if (n_now > SelCfg<T>::kCap / 2 && n_now <= SelCfg<T>::kCap) {
                 __syncthreads();  // every thread has read sh.count
-                const unsigned kept = drop_below(sv, si, n_now, F, sh.scratch);
+                const unsigned kept = drop_below<T>(sv, si, n_now, F, sh.scratch);
                 if (t == 0) sh.count = kept;
             }
             __syncthreads();
@@ -1366,47 +1375,47 @@ __global__ void __launch_bounds__(kSelThreads, 2)
                 const float4* r4 = reinterpret_cast<const float4*>(xr);
                 const int u1 = c1 >> 2;
                 constexpr int kAhead = 4;
-                for (int ub = c0 >> 2; ub < u1; ub += kAhead * kSelThreads) {
+                for (int ub = c0 >> 2; ub < u1; ub += kAhead * T) {
                     float4 q[kAhead];
 #pragma unroll
                     for (int a = 0; a < kAhead; ++a) {
-                        const int u = ub + a * kSelThreads + t;
+                        const int u = ub + a * T + t;
                         q[a] = u < u1 ? __ldg(r4 + u)
                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                     }
                     bool any = false;
 #pragma unroll
                     for (int a = 0; a < kAhead; ++a)
-                        any |= ub + a * kSelThreads + t < u1 &&
+                        any |= ub + a * T + t < u1 &&
                                (q[a].x >= F || q[a].y >= F || q[a].z >= F || q[a].w >= F);
                     if (__any_sync(0xffffffffu, any)) {
 #pragma unroll
                         for (int a = 0; a < kAhead; ++a) {
-                            const int u = ub + a * kSelThreads + t;
+                            const int u = ub + a * T + t;
                             const float v[4] = {q[a].x, q[a].y, q[a].z, q[a].w};
                             const bool in = u < u1;
                             const bool p[4] = {in && v[0] >= F, in && v[1] >= F, in && v[2] >= F,
                                                in && v[3] >= F};
                             const int col[4] = {4 * u, 4 * u + 1, 4 * u + 2, 4 * u + 3};
-                            append(v, col, p, sv, si, sh);
+                            append<T>(v, col, p, sv, si, sh);
                         }
                     }
                 }
             } else {
-                for (int jb = c0; jb < c1; jb += 4 * kSelThreads) {
+                for (int jb = c0; jb < c1; jb += 4 * T) {
                     float v[4];
                     bool p[4];
                     int col[4];
                     bool any = false;
 #pragma unroll
                     for (int a = 0; a < 4; ++a) {
-                        const int j = jb + a * kSelThreads + t;
+                        const int j = jb + a * T + t;
                         v[a] = j < c1 ? __ldg(xr + j) : -INFINITY;
                         p[a] = j < c1 && v[a] >= F;
                         col[a] = j;
                         any |= p[a];
                     }
-                    if (__any_sync(0xffffffffu, any)) append(v, col, p, sv, si, sh);
+                    if (__any_sync(0xffffffffu, any)) append<T>(v, col, p, sv, si, sh);
                 }
             }
             __syncthreads();
@@ -1419,7 +1428,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         }
         __syncthreads();
         Stat a{sh.red_m[0], sh.red_l[0]};
-        for (int w = 1; w < kSelWarps; ++w) a = merge(a, Stat{sh.red_m[w], sh.red_l[w]});
+        for (int w = 1; w < SelCfg<T>::kWarps; ++w) a = merge(a, Stat{sh.red_m[w], sh.red_l[w]});
         const float m = a.m, l = a.l;
         // ---- the top k: from the buffer, else by the exact route ----
         int n;
@@ -1430,14 +1439,14 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         } else {
             const unsigned total = sh.count;
             __syncthreads();  // every thread has read the count
-            n = static_cast<int>(drop_below(sv, si, total, F, sh.scratch));
+            n = static_cast<int>(drop_below<T>(sv, si, total, F, sh.scratch));
         }
         // ---- outputs: the shares exp(x - m) / l, the columns, lse = m + ln l ----
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        if (n <= kSelThreads) {
+        if (n <= T) {
             float v = t < n ? sv[t] : -INFINITY;
             int c = t < n ? si[t] : INT_MAX;
-            cta_sort_desc(v, c, sh);
+            cta_sort_desc<T>(v, c, sh);
             if (t < k) {
                 vals[row * k + t] = (m == -INFINITY) ? 0.f : ex2a((v - m) * kLog2e) * inv_l;
                 idx[row * k + t] = c;
@@ -1445,13 +1454,13 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         } else {
             int np = 1;
             while (np < n) np <<= 1;
-            for (int i = n + t; i < np; i += kSelThreads) {
+            for (int i = n + t; i < np; i += T) {
                 sv[i] = -INFINITY;
                 si[i] = INT_MAX;
             }
             __syncthreads();
-            sort_pairs(sv, si, np);
-            for (int i = t; i < k; i += kSelThreads) {
+            sort_pairs<T>(sv, si, np);
+            for (int i = t; i < k; i += T) {
                 const float v = sv[i];
                 vals[row * k + i] = (m == -INFINITY) ? 0.f : ex2a((v - m) * kLog2e) * inv_l;
                 idx[row * k + i] = si[i];
@@ -1462,25 +1471,25 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     }
 }
 
-template <int Q, bool VEC>
+template <int T, int Q, bool VEC>
 int launch_select_q(const float* x, int64_t rows, int cols, int k, int chunk, float* vals,
                     int32_t* idx, float* lse, cudaStream_t stream) {
     static int blocks_per_sm = 0;
     static cudaError_t attr = cudaSuccess;
     static std::once_flag once;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(topk_select_rows<Q, VEC>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
+        attr = cudaFuncSetAttribute(topk_select_rows<T, Q, VEC>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SelCfg<T>::kSmem);
         if (attr == cudaSuccess &&
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, topk_select_rows<Q, VEC>,
-                                                          kSelThreads, kSelSmem) != cudaSuccess)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, topk_select_rows<T, Q, VEC>,
+                                                          T, SelCfg<T>::kSmem) != cudaSuccess)
             blocks_per_sm = 1;
     });
     if (attr != cudaSuccess) return FA_ERR_CUDA;
     const long long sms = sm_count() > 0 ? sm_count() : 148;
     long long grid = sms * (blocks_per_sm > 0 ? blocks_per_sm : 1);
     if (grid > rows) grid = rows;
-    topk_select_rows<Q, VEC><<<static_cast<unsigned>(grid), kSelThreads, kSelSmem, stream>>>(
+    topk_select_rows<T, Q, VEC><<<static_cast<unsigned>(grid), T, SelCfg<T>::kSmem, stream>>>(
         x, rows, cols, k, chunk, vals, idx, lse);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -1491,18 +1500,32 @@ int launch_select_q(const float* x, int64_t rows, int cols, int k, int chunk, fl
 // and 0.142 ms, so the L2 hits of short chunks do not pay for their count.
 constexpr int kSelChunk = 131072;
 
+// The CTA width by k: 256 threads (four CTAs per SM, whose latency-bound steps overlap) up to
+// k = 256, 512 threads (two per SM, a floor from more threads' values and a buffer of 8192)
+// beyond.  Measured on 512 rows of 131072 columns: k = 100 took 0.142 ms with 512 threads and
+// 0.120 with 256; k = 1024 took 0.268 with 512 threads and 0.362 with 256 (Q = 8, 4096
+// entries); k = 33 took 0.113 with 256 threads and 0.149 with 128 (eight CTAs per SM).
+constexpr int kSelSmallK = 256;
+
+template <int T, int Q>
+int launch_select_vec(bool vec, const float* x, int64_t rows, int cols, int k, float* vals,
+                      int32_t* idx, float* lse, cudaStream_t stream) {
+    return vec ? launch_select_q<T, Q, true>(x, rows, cols, k, kSelChunk, vals, idx, lse, stream)
+               : launch_select_q<T, Q, false>(x, rows, cols, k, kSelChunk, vals, idx, lse,
+                                              stream);
+}
+
 int launch_select(const float* x, int64_t rows, int cols, int k, float* vals, int32_t* idx,
                   float* lse, cudaStream_t stream) {
     const bool vec = (cols % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
-    const int q = 2 * k <= kSelThreads ? 1 : (2 * k <= 2 * kSelThreads ? 2 : 4);
-    if (q == 1)
-        return vec ? launch_select_q<1, true>(x, rows, cols, k, kSelChunk, vals, idx, lse, stream)
-                   : launch_select_q<1, false>(x, rows, cols, k, kSelChunk, vals, idx, lse, stream);
-    if (q == 2)
-        return vec ? launch_select_q<2, true>(x, rows, cols, k, kSelChunk, vals, idx, lse, stream)
-                   : launch_select_q<2, false>(x, rows, cols, k, kSelChunk, vals, idx, lse, stream);
-    return vec ? launch_select_q<4, true>(x, rows, cols, k, kSelChunk, vals, idx, lse, stream)
-               : launch_select_q<4, false>(x, rows, cols, k, kSelChunk, vals, idx, lse, stream);
+    // Q per thread: the fewest with T * Q >= 2k.
+    if (k <= kSelSmallK) {
+        if (2 * k <= 256) return launch_select_vec<256, 1>(vec, x, rows, cols, k, vals, idx, lse, stream);
+        return launch_select_vec<256, 2>(vec, x, rows, cols, k, vals, idx, lse, stream);
+    }
+    if (2 * k <= 512) return launch_select_vec<512, 1>(vec, x, rows, cols, k, vals, idx, lse, stream);
+    if (2 * k <= 1024) return launch_select_vec<512, 2>(vec, x, rows, cols, k, vals, idx, lse, stream);
+    return launch_select_vec<512, 4>(vec, x, rows, cols, k, vals, idx, lse, stream);
 }
 
 }  // namespace
