@@ -41,6 +41,15 @@ NOMINAL_BF16_TFLOPS = 2250.0
 L2_FLUSH_BYTES = 256 << 20
 
 
+def peaks_raw():
+    """MEASURED_PEAKS.json as written, or {} when it is absent."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -445,6 +454,17 @@ def roofline_tensor(flops, ms, peaks, kind, traffic=None):
             "frac_of_nominal_2250": round(achieved / NOMINAL_BF16_TFLOPS, 4)}
 
 
+def exp_rate(w, ms, peaks_raw, sms=152):
+    """The softmax's exponentials per second (one per allowed (query, key) pair: B*H*N^2,
+    halved when causal) against the MUFU's ex2 rate, 32 per clock per SM at the measured
+    maximum SM clock."""
+    n = w.B * w.H * w.N * w.N / (2 if w.causal else 1)
+    rate = n / (ms * 1e-3)
+    mufu = 32 * sms * float(peaks_raw.get("sm_max_mhz", 2070.0)) * 1e6
+    return {"gexp_per_s": round(rate / 1e9, 1), "frac_of_mufu": round(rate / mufu, 4),
+            "mufu_gexp_per_s": round(mufu / 1e9, 1)}
+
+
 def roofline_hbm(nbytes, ms, peaks, kind, traffic=None):
     achieved = nbytes / (ms * 1e-3) / 1e9
     peak = peaks["hbm_gbs"]
@@ -655,6 +675,7 @@ def main(argv=None):
         "frac_of_nominal_bf16_2250": round(value / world / NOMINAL_BF16_TFLOPS, 4),
         "roofline": roofline_tensor(w.flops, ms, peaks, peaks_kind,
                                     NCU_TRAFFIC_BYTES.get(w.name)),
+        "exp_rate": exp_rate(w, ms, peaks_raw()),
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "clocks": clk,
@@ -671,7 +692,8 @@ def main(argv=None):
             other[name] = {"TFLOP/s": round(world * ow.flops / (oms * 1e-3) / 1e12, 2),
                            "ms_per_step": round(oms, 4),
                            "roofline": roofline_tensor(ow.flops, oms, peaks, peaks_kind,
-                                                       NCU_TRAFFIC_BYTES.get(name))}
+                                                       NCU_TRAFFIC_BYTES.get(name)),
+                           "exp_rate": exp_rate(ow, oms, peaks_raw())}
             torch.cuda.empty_cache()
         for name, dw in inputs.DECODE_WORKLOADS.items():
             t, splits = time_splitkv(dw, 20, 3, device, flush)

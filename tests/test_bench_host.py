@@ -89,3 +89,33 @@ def test_mask_workload_flops_count_the_allowed_pairs():
     pairs = w.window * (w.window + 1) // 2 + (w.N - w.window) * w.window
     assert w.flops == 4 * w.d * pairs * w.B * w.H
     assert w.tile_map and p.tile_map and not W["mask_random_b2h16n4096d128"].tile_map
+
+
+def test_ragged_stress_workload_logit_range():
+    """The overflow/ragged stress workload draws Q, K with sd 3, so at scale 1/sqrt(128) its
+    scaled logits have sd 3 * 3 * sqrt(128) / sqrt(128) = 9; over its 16 x 4000 x 4000 scores
+    the largest magnitude observed is about 60 (recorded with the inputs' recipe)."""
+    import torch
+
+    from online_softmax_tiled_attn_gb300 import inputs
+
+    w = inputs.ATTN_WORKLOADS["ragged_b1h16n4000"]
+    q, k, _ = inputs.workload_inputs(w)
+    mx, var = 0.0, 0.0
+    for h in range(w.H):
+        s = (q[0, h].float() @ k[0, h].float().T) * w.scale
+        mx = max(mx, s.abs().max().item())
+        var += s.pow(2).mean().item() / w.H
+    assert abs(var ** 0.5 - 9.0) < 0.1
+    assert 55.0 < mx < 65.0
+
+
+def test_exp_rate_counts_the_allowed_pairs():
+    from online_softmax_tiled_attn_gb300 import inputs
+
+    d = bench.exp_rate(inputs.ATTN_WORKLOADS["dense_b2h32n8192"], 1.0,
+                       {"sm_max_mhz": 2000.0})
+    assert d["gexp_per_s"] == round(2 * 32 * 8192 ** 2 / 1e-3 / 1e9, 1)
+    assert abs(d["frac_of_mufu"] - 2 * 32 * 8192 ** 2 / 1e-3 / (32 * 152 * 2000e6)) < 1e-4
+    c = bench.exp_rate(inputs.ATTN_WORKLOADS["causal_b2h32n8192"], 1.0, {"sm_max_mhz": 2000.0})
+    assert c["gexp_per_s"] == round(2 * 32 * 8192 ** 2 / 2 / 1e-3 / 1e9, 1)
