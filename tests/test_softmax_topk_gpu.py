@@ -89,7 +89,9 @@ def test_topk_full_size_workloads():
 # and 4-byte loads; several chunks per row)
 LARGE_K = [(64, 4000, 33), (16, 32000, 100), (5, 131072, 64), (40, 300, 257), (3, 5000, 1024),
            (200, 64, 64), (2, 1024, 1024), (3, 131072, 1024), (4, 65536, 512), (4, 65536, 513),
-           (4, 100003, 300), (6, 70001, 40)]
+           (4, 100003, 300), (6, 70001, 40),
+           # many rows per CTA, a row of 8196 columns, k = 129 and 256 (two values per thread)
+           (2000, 8196, 40), (7, 16384, 256), (3, 12288, 129), (600, 8192, 33)]
 
 
 @pytest.mark.parametrize("rows,cols,k", LARGE_K, ids=lambda x: str(x))
