@@ -1065,15 +1065,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kv0 = bars->v_kt[vs] * kBN;
                     mw = reinterpret_cast<const uint4*>(smem + C::kMsk + vs * C::kMskBytes)[r];
                 }
-                if (kv0 + kBN - 1 > key_limit) {
-#pragma unroll
-                    for (int e = 0; e < 128; ++e)
-                        if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
-                }
                 if constexpr (MASK != 0) {
-                    // The explicit mask: a key whose bit is 0 takes no part (score -inf).
-                    // Words of all ones (the usual case for structured masks) cost one test.
-                    const uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
+                    // The explicit mask: a key whose bit is 0 takes no part (score -inf).  The
+                    // key limit (causal, key lengths, the end of the keys) is folded into the
+                    // words first, so that one masking pass serves both (a second unrolled pass
+                    // over the row cost these kernels instruction-fetch stalls).  Words of all
+                    // ones (the usual case for structured masks) cost one test.
+                    uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
+                    const int lim = key_limit - kv0;  // the limit allows keys e <= lim
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int lc = lim - 32 * c;
+                        words[c] &= lc >= 31 ? 0xffffffffu
+                                             : (lc < 0 ? 0u : (0xffffffffu >> (31 - lc)));
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         if (words[c] == 0xffffffffu) continue;
@@ -1081,6 +1086,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e)
                             if (!((words[c] >> e) & 1u)) sr[c * 32 + e] = __float_as_uint(-INFINITY);
                     }
+                } else if (kv0 + kBN - 1 > key_limit) {
+#pragma unroll
+                    for (int e = 0; e < 128; ++e)
+                        if (kv0 + e > key_limit) sr[e] = __float_as_uint(-INFINITY);
                 }
                 // Row max with two-input max.f32: on this GPU the three-input form issues far
                 // more slowly and holds back the exponentials that follow.
