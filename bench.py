@@ -485,9 +485,9 @@ NCU_TRAFFIC_BYTES = {
     "gqa_causal_b2h32kv8n8192d128": 363324416 + 102152448,
     "gqa_ragged_b4h32kv8n4096d128": 172562944 + 91484928,
     "gqa_decode_b8h32kv8q1k32768d128": 1073982208 + 5190400,
-    "mask_prefixlm_b2h16n4096d128": 102074880 + 13284608,
-    "mask_random_b2h16n4096d128": 154071296 + 18568960,
-    "mask_window_b2h16n8192d128": 203484416 + 46027264,
+    "mask_prefixlm_b2h16n4096d128": 102078208 + 13319936,
+    "mask_random_b2h16n4096d128": 154048000 + 18532352,
+    "mask_window_b2h16n8192d128": 203418112 + 46082816,
     "softmax_65536x4000": 1048660992 + 998156288,
     "softmax_topk_65536x4000_k8": 1048700672 + 6889216,
     "softmax_topk_512x131072_k32": 268504320 + 2991616,
