@@ -571,9 +571,19 @@ __device__ __forceinline__ void sweep_segment(const float4* __restrict__ s4, int
         md = fmaxf(md, max4(s4[u + 96]));
     }
     for (; u < n4; u += 32) ma = fmaxf(ma, max4(s4[u]));
-    const float sorted = warp_sorted_desc(fmaxf(fmaxf(ma, mb), fmaxf(mc, md)));
-    S.floor = fmaxf(S.floor, __shfl_sync(0xffffffffu, sorted, k - 1));
-    const float m_new = fmaxf(m, __shfl_sync(0xffffffffu, sorted, 0));
+    // Two values per lane, the maxima of disjoint groups (distinct entries): the k-th largest
+    // of the 64 is a floor (k distinct entries reach it), and a tighter one than the k-th
+    // largest of the 32 lane maxima.  With A and B the two sets sorted across the warp, it is
+    // the largest of A[k-1], B[k-1] and min(A[i], B[k-2-i]) for i < k - 1.
+    const float sa = warp_sorted_desc(fmaxf(ma, mb));
+    const float sb = warp_sorted_desc(fmaxf(mc, md));
+    const float sb_pair = __shfl_sync(0xffffffffu, sb, (k - 2 - lane) & 31);
+    float kth = lane < k - 1 ? fminf(sa, sb_pair) : -INFINITY;
+    if (lane == k - 1) kth = fmaxf(sa, sb);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, off));
+    S.floor = fmaxf(S.floor, kth);
+    const float m_new = fmaxf(m, fmaxf(__shfl_sync(0xffffffffu, sa, 0), __shfl_sync(0xffffffffu, sb, 0)));
     if (m != -INFINITY && m_new != m) {  // the same in every lane
         const float f = ex2a((m - m_new) * kLog2e);
 #pragma unroll
