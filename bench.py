@@ -489,8 +489,8 @@ NCU_TRAFFIC_BYTES = {
     "mask_random_b2h16n4096d128": 154048000 + 18532352,
     "mask_window_b2h16n8192d128": 203418112 + 46082816,
     "softmax_65536x4000": 1048660992 + 998156288,
-    "softmax_topk_65536x4000_k8": 1048700672 + 6889216,
-    "softmax_topk_512x131072_k32": 268504320 + 2991616,
+    "softmax_topk_65536x4000_k8": 1048771072 + 6897152,
+    "softmax_topk_512x131072_k32": 268552704 + 3390464,
     "softmax_topk_512x131072_k100": 536930560 + 3014656,
     "bwd_b4h16n2048d64": 170481920 + 12257024,
     "bwd_b2h16n8192d128": 675801856 + 156787968,
