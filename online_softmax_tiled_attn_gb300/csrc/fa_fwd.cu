@@ -170,7 +170,8 @@ struct Cfg {
     // run as whole, converged warps with one elected lane issuing (kWarpIssue), or as lane 0
     // alone.  Measured per head dimension on GB300: at d = 128 converged issue with sleeping
     // waits is 2-4 % faster; at d = 64 (SS products for S, bound by shared memory) lane-0
-    // issue with polling waits is 4 % faster.
+    // issue with polling waits is 4 % faster (sleeping issuer waits there: -1 to -2 %).  The
+    // softmax's sleeping waits: causal d = 128 +1.4 %.
     static constexpr bool kWarpIssue = D == 128;
     static constexpr bool kSleepMma = D == 128;
     static constexpr bool kSleepSoftmax = true;
