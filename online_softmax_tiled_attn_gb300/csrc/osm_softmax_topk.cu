@@ -1016,22 +1016,27 @@ int launch(const float* x, long long rows, int cols, int k, float* vals, int* id
 // --------------------------------------------------------------------------------------------
 // k > 32: a floor, candidates in shared memory, one CTA per row
 // --------------------------------------------------------------------------------------------
-// For k beyond the warp-wide list, a CTA of T threads (256 or 512) takes a row in chunks of
-// `chunk` columns, and runs two passes over each chunk before it takes the next one:
-//   * pass 1 carries each thread's online (m, l) of "The idea" and the Q largest values the
-//     thread has seen (Q = 1, 2 or 4, the fewest with T * Q >= 2k).  Any thread whose Q-th
-//     largest is at least F has Q entries of the row at or above F; so the ceil(k / Q)-th
-//     largest of the threads' Q-th largest values is a floor F under the k-th largest value of
-//     the row (a bitonic network over the CTA's T values picks it).  F only
-//     rises from chunk to chunk;
-//   * pass 2 appends every entry at or above F to a candidate buffer in shared memory (a warp
-//     reserves its slots with one atomic).  An entry of an earlier chunk at or above the
-//     present F was at or above the F of its own chunk, so the buffer holds every entry of the
-//     row seen so far at or above F: the whole top k of those entries, ties at the k-th value
-//     included.  Entries below F are dropped from the buffer when it is half full.
-// At the end of the row the (m, l) pairs meet by the two-worker merge, the buffer is sorted
+// For k beyond the warp-wide list, a CTA of T threads (256 or 512) takes a row:
+//   * each thread carries its online (m, l) of "The idea" and the Q largest values it has seen
+//     (Q = 1, 2 or 4, the fewest with T * Q >= 2k).  Any thread whose Q-th largest is at least
+//     F has Q entries of the row at or above F; so the ceil(k / Q)-th largest of the threads'
+//     Q-th largest values is a floor F under the k-th largest value of the row (a bitonic
+//     network over the CTA's T values picks it), and so is the smallest over the warps of a
+//     warp's c-th largest lane value when the warps' c add up to ceil(k / Q);
+//   * the row's first 32 T columns are read twice: once for (m, l) and the Q largest, which
+//     give the first F, and once more (from L2) to append every entry at or above F to a
+//     candidate buffer in shared memory (a warp reserves its slots with one atomic);
+//   * the rest of the row is read once: every value is offered against the thread's F, then
+//     enters (m, l) and the Q largest, and each warp renews its F from the published warp
+//     floors as it goes.  F only rises, so an entry at or above a later floor was at or above
+//     the floor it was offered against: the buffer holds every entry seen so far at or above
+//     any floor in use, the whole top k with the ties at the k-th value.  Entries below the
+//     floor are dropped when the buffer is half full.
+// At the end of the row the (m, l) pairs meet by the two-worker merge, the final F (from all of
+// the row's values, at or above every floor used before) drops the rest, the buffer is sorted
 // (larger value first, then the smaller column) and its first k entries are the row's top k.
-// Rows where more than 16 T entries reach the floor (many ties at it, or fewer than k
+// A row that overflowed the buffer is read once more against the final F.
+// Rows where more than 16 T entries reach the final floor (many ties at it, or fewer than k
 // finite values) take the exact route instead: radix selection of the k-th largest on an
 // order-preserving 32-bit key, eight bits per pass over the row, then a pass in column order
 // that keeps the entries above it and the first of the entries equal to it.
@@ -1159,6 +1164,7 @@ struct SelShared {
     unsigned scratch[SelCfg<T>::kWarps];
     unsigned warp_ties[SelCfg<T>::kWarps];
     float red_m[SelCfg<T>::kWarps], red_l[SelCfg<T>::kWarps];
+    float wfloor[SelCfg<T>::kWarps];  // each warp's last published floor
     unsigned count, prefix, need, ties;
     int overflow;
 };
@@ -1303,130 +1309,233 @@ __device__ __forceinline__ void keep_largest(float (&b)[Q], float v) {
     }
 }
 
+// A step of the sweep over a row: each thread takes kN values (four float4 in the vector form,
+// four floats otherwise).  The first kHead steps of a row (32 T columns) take two passes (the
+// second from L2), which set the first floor; a warp renews its floor every kRefresh later
+// steps (16384 columns), and every kCheck steps (128 T columns) the CTA meets to drop buffer
+// entries below the floor once the buffer is half full.  Measured on 512 rows of 131072
+// columns: renewing every 8192 columns made k = 100 and k = 33 1.5 and 2.6 % slower (the warp
+// sort's cost), every 32768 made k = 1024 (512 threads) 21 % slower (the buffer overflowed).
+template <int T, bool VEC>
+struct SelStep {
+    static constexpr int kN = VEC ? 16 : 4;
+    static constexpr int kCols = kN * T;
+    static constexpr int kHead = 32 * T / kCols;
+    static constexpr int kRefresh = 16384 / kCols;
+    static constexpr int kCheck = 128 * T / kCols;
+};
+
+// Thread t's values of the step that starts at column `base` (a multiple of 4 in the vector
+// form); columns at or past c1 read as -inf.
+template <int T, bool VEC>
+__device__ __forceinline__ void load_step(const float* __restrict__ xr, int base, int c1,
+                                          float (&v)[SelStep<T, VEC>::kN]) {
+    const int t = threadIdx.x;
+    if constexpr (VEC) {
+        const float4* r4 = reinterpret_cast<const float4*>(xr);
+        const int u1 = c1 >> 2;
+#pragma unroll
+        for (int a = 0; a < SelStep<T, VEC>::kN / 4; ++a) {
+            const int u = (base >> 2) + a * T + t;
+            const float4 q = u < u1 ? __ldg(r4 + u)
+                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            v[4 * a] = q.x;
+            v[4 * a + 1] = q.y;
+            v[4 * a + 2] = q.z;
+            v[4 * a + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int j = base + a * T + t;
+            v[a] = j < c1 ? __ldg(xr + j) : -INFINITY;
+        }
+    }
+}
+
+// The column of value e of thread t's share of the step at `base`.
+template <int T, bool VEC>
+__device__ __forceinline__ int step_col(int base, int e) {
+    if constexpr (VEC) return 4 * ((base >> 2) + (e >> 2) * T + static_cast<int>(threadIdx.x)) + (e & 3);
+    return base + e * T + static_cast<int>(threadIdx.x);
+}
+
+// The largest of a step's values (a tree of pairwise maxima).
+template <int N>
+__device__ __forceinline__ float step_max(const float (&v)[N]) {
+    float w[N / 2];
+#pragma unroll
+    for (int e = 0; e < N / 2; ++e) w[e] = fmaxf(v[2 * e], v[2 * e + 1]);
+#pragma unroll
+    for (int n = N / 2; n > 1; n >>= 1) {
+#pragma unroll
+        for (int e = 0; e < n / 2; ++e) w[e] = fmaxf(w[2 * e], w[2 * e + 1]);
+    }
+    return w[0];
+}
+
+// A step's values (largest mx) enter (m, l) and the thread's Q largest.  exp(x - m) in packed
+// pairs, x - m first, then the scale; l is rescaled by exp(m_old - m_new) only when the running
+// max grows (from -inf: the old l, 0, stays 0).
+template <int Q, int N>
+__device__ __forceinline__ void take_step(Stat& s, float (&best)[Q], const float (&v)[N],
+                                          float mx) {
+    const float m = fmaxf(s.m, mx);
+    if (m != -INFINITY) {  // else nothing finite yet: adds nothing
+        float l = s.l;
+        if (m != s.m) l *= ex2a((s.m - m) * kLog2e);
+        const float2 nm = make_float2(-m, -m), c2 = make_float2(kLog2e, kLog2e);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < N; e += 2) {
+            const float2 d = fmul2(fadd2(make_float2(v[e], v[e + 1]), nm), c2);
+            acc = fadd2(acc, make_float2(ex2a(d.x), ex2a(d.y)));
+        }
+        s = Stat{m, l + (acc.x + acc.y)};
+    }
+    if constexpr (Q == 1) {
+        best[0] = fmaxf(best[0], mx);
+    } else if (mx > best[Q - 1]) {
+#pragma unroll
+        for (int e = 0; e < N; ++e) keep_largest(best, v[e]);
+    }
+}
+
+// The values of a step (columns below c1) at or above f enter the buffer, four at a time (one
+// vote, then one atomic per warp).
+template <int T, bool VEC>
+__device__ __forceinline__ void offer_step(const float (&v)[SelStep<T, VEC>::kN], int base,
+                                           int c1, float f, float* sv, int* si,
+                                           SelShared<T>& sh) {
+#pragma unroll
+    for (int g = 0; g < SelStep<T, VEC>::kN; g += 4) {
+        bool p[4];
+        int col[4];
+        const float x[4] = {v[g], v[g + 1], v[g + 2], v[g + 3]};
+        bool any = false;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            col[e] = step_col<T, VEC>(base, g + e);
+            p[e] = col[e] < c1 && x[e] >= f;
+            any |= p[e];
+        }
+        if (__any_sync(0xffffffffu, any)) append<T>(x, col, p, sv, si, sh);
+    }
+}
+
+// The ceil(k / Q)-th largest of the threads' Q-th largest values: a floor under the k-th
+// largest value of the row (every thread gets it; the CTA meets).
+template <int T>
+__device__ __forceinline__ float cta_floor(float bar, int r_bar, SelShared<T>& sh) {
+    int bc = static_cast<int>(threadIdx.x);
+    cta_sort_desc<T>(bar, bc, sh);
+    if (static_cast<int>(threadIdx.x) == r_bar - 1) sh.floor = bar;
+    __syncthreads();
+    return sh.floor;
+}
+
 template <int T, int Q, bool VEC>
 __global__ void __launch_bounds__(T, 1024 / T)
-    topk_select_rows(const float* __restrict__ x, long long rows, int cols, int k, int chunk,
+    topk_select_rows(const float* __restrict__ x, long long rows, int cols, int k,
                      float* __restrict__ vals, int32_t* __restrict__ idx,
                      float* __restrict__ lse) {
+    using S = SelStep<T, VEC>;
+    constexpr int N = S::kN;
+    constexpr int W = SelCfg<T>::kWarps;
     extern __shared__ __align__(16) unsigned char sel_smem[];
     float* sv = reinterpret_cast<float*>(sel_smem);
     int* si = reinterpret_cast<int*>(sel_smem + SelCfg<T>::kCap * 4);
     __shared__ SelShared<T> sh;
+    volatile float* wfloor = sh.wfloor;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-    const int r_bar = (k + Q - 1) / Q;  // the floor is the r_bar-th largest thread bar
+    const int r_bar = (k + Q - 1) / Q;     // the floor is the r_bar-th largest thread bar
+    const int c_w = (r_bar + W - 1) / W;   // a warp's floor: the c_w-th largest of its lane bars
     for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
         const float* xr = x + row * cols;
         if (t == 0) {
             sh.count = 0u;
             sh.overflow = 0;
         }
+        if (lane == 0) wfloor[wid] = -INFINITY;
         Stat st{-INFINITY, 0.f};
         float best[Q];
 #pragma unroll
         for (int i = 0; i < Q; ++i) best[i] = -INFINITY;
-        float F = -INFINITY;
         __syncthreads();
-        for (int c0 = 0; c0 < cols; c0 += chunk) {
-            const int c1 = min(cols, c0 + chunk);
-            // ---- pass 1: (m, l) and the Q largest of each thread ----
-            if constexpr (VEC) {
-                const float4* r4 = reinterpret_cast<const float4*>(xr);
-                const int u1 = c1 >> 2;
-                constexpr int kAhead = 4;
-                for (int u0 = (c0 >> 2) + t; u0 < u1; u0 += kAhead * T) {
-                    float4 q[kAhead];
+        // ---- the head: (m, l) and the Q largest of each thread, the floor F, then the head's
+        // entries at or above F (its second read hits L2) ----
+        const int h = min(cols, S::kHead * S::kCols);
+        for (int base = 0; base < h; base += S::kCols) {
+            float v[N];
+            load_step<T, VEC>(xr, base, h, v);
+            take_step(st, best, v, step_max(v));
+        }
+        // the first step after the head is on its way during the floor and the head's offers
+        float vn[N];
+        if (h < cols) load_step<T, VEC>(xr, h, cols, vn);
+        float F = cta_floor<T>(best[Q - 1], r_bar, sh);
+        for (int base = 0; base < h; base += S::kCols) {
+            float v[N];
+            load_step<T, VEC>(xr, base, h, v);
+            offer_step<T, VEC>(v, base, h, F, sv, si, sh);
+        }
+        // ---- the rest of the row in one pass, the next step's loads in flight while a step is
+        // worked: each step is offered against the floor (only when its largest value reaches
+        // it), then enters (m, l) and the bars.  A warp's floor (its c_w-th largest lane bar:
+        // c_w Q of its entries reach it) is published in shared memory; the smallest published
+        // value is a floor for the row, since the W warps together have W c_w Q >= k entries
+        // at or above it.  Bars only rise, so a stale value is a floor too, and no barrier is
+        // needed. ----
+        int step = 0;
+        for (int base = h; base < cols; base += S::kCols) {
+            float v[N];
 #pragma unroll
-                    for (int a = 0; a < kAhead; ++a) {
-                        const int u = u0 + a * T;
-                        q[a] = u < u1 ? __ldg(r4 + u)
-                                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                    }
+            for (int e = 0; e < N; ++e) v[e] = vn[e];
+            if (base < cols - S::kCols) load_step<T, VEC>(xr, base + S::kCols, cols, vn);
+            const float mx = step_max(v);
+            if (__any_sync(0xffffffffu, mx >= F)) offer_step<T, VEC>(v, base, cols, F, sv, si, sh);
+            take_step(st, best, v, mx);
+            ++step;
+            if (step % S::kRefresh == 0) {
+                const float wf = warp_kth_largest(best[Q - 1], c_w);
+                if (lane == 0) wfloor[wid] = wf;
+                __syncwarp();
+                float f = lane < W ? wfloor[lane] : INFINITY;
 #pragma unroll
-                    for (int a = 0; a < kAhead; ++a) {
-                        const float v[4] = {q[a].x, q[a].y, q[a].z, q[a].w};
-                        update(st, v);  // -inf past the chunk adds nothing
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) keep_largest(best, v[e]);
-                    }
-                }
-            } else {
-                for (int j0 = c0 + t; j0 < c1; j0 += 4 * T) {
-                    float v[4];
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) {
-                        const int j = j0 + a * T;
-                        v[a] = j < c1 ? __ldg(xr + j) : -INFINITY;
-                    }
-                    update(st, v);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) keep_largest(best, v[e]);
-                }
+                for (int off = 16; off > 0; off >>= 1)
+                    f = fminf(f, __shfl_xor_sync(0xffffffffu, f, off));
+                F = fmaxf(F, f);
             }
-            // ---- the floor: the r_bar-th largest of the threads' Q-th largest values ----
-            {
-                float bv = best[Q - 1];
-                int bc = t;
-                cta_sort_desc<T>(bv, bc, sh);
-                if (t == r_bar - 1) sh.floor = bv;
+            // the trip count is the same in every thread, so every thread meets here
+            if (step % S::kCheck == 0 &&
+                __syncthreads_or(*reinterpret_cast<volatile unsigned*>(&sh.count) >
+                                 SelCfg<T>::kCap / 2)) {
+                const unsigned n_now = sh.count;
+                if (n_now <= SelCfg<T>::kCap) {
+                    // every thread's F is at most the final floor below
+                    const unsigned kept = drop_below<T>(sv, si, n_now, F, sh.scratch);
+                    if (t == 0) sh.count = kept;
+                }
                 __syncthreads();
-                F = fmaxf(F, sh.floor);
             }
-            // ---- drop what fell below the floor once the buffer is half full ----
-            const unsigned n_now = sh.count;
-            if (n_now > SelCfg<T>::kCap / 2 && n_now <= SelCfg<T>::kCap) {
-                __syncthreads();  // every thread has read sh.count
-                const unsigned kept = drop_below<T>(sv, si, n_now, F, sh.scratch);
-                if (t == 0) sh.count = kept;
+        }
+        __syncthreads();  // every entry is in
+        // ---- the final floor, from every value's bars: at or above every floor used above,
+        // so the buffer holds every entry of the row at or above it ----
+        F = cta_floor<T>(best[Q - 1], r_bar, sh);
+        if (sh.overflow) {
+            // more than the buffer reached the running floors: once more over the row against
+            // the final floor
+            __syncthreads();  // every thread has read the flag
+            if (t == 0) {
+                sh.count = 0u;
+                sh.overflow = 0;
             }
             __syncthreads();
-            // ---- pass 2: the entries at or above the floor (four loads per thread in flight
-            // before one vote; the trip counts are the same in every thread) ----
-            if constexpr (VEC) {
-                const float4* r4 = reinterpret_cast<const float4*>(xr);
-                const int u1 = c1 >> 2;
-                constexpr int kAhead = 4;
-                for (int ub = c0 >> 2; ub < u1; ub += kAhead * T) {
-                    float4 q[kAhead];
-#pragma unroll
-                    for (int a = 0; a < kAhead; ++a) {
-                        const int u = ub + a * T + t;
-                        q[a] = u < u1 ? __ldg(r4 + u)
-                                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                    }
-                    bool any = false;
-#pragma unroll
-                    for (int a = 0; a < kAhead; ++a)
-                        any |= ub + a * T + t < u1 &&
-                               (q[a].x >= F || q[a].y >= F || q[a].z >= F || q[a].w >= F);
-                    if (__any_sync(0xffffffffu, any)) {
-#pragma unroll
-                        for (int a = 0; a < kAhead; ++a) {
-                            const int u = ub + a * T + t;
-                            const float v[4] = {q[a].x, q[a].y, q[a].z, q[a].w};
-                            const bool in = u < u1;
-                            const bool p[4] = {in && v[0] >= F, in && v[1] >= F, in && v[2] >= F,
-                                               in && v[3] >= F};
-                            const int col[4] = {4 * u, 4 * u + 1, 4 * u + 2, 4 * u + 3};
-                            append<T>(v, col, p, sv, si, sh);
-                        }
-                    }
-                }
-            } else {
-                for (int jb = c0; jb < c1; jb += 4 * T) {
-                    float v[4];
-                    bool p[4];
-                    int col[4];
-                    bool any = false;
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) {
-                        const int j = jb + a * T + t;
-                        v[a] = j < c1 ? __ldg(xr + j) : -INFINITY;
-                        p[a] = j < c1 && v[a] >= F;
-                        col[a] = j;
-                        any |= p[a];
-                    }
-                    if (__any_sync(0xffffffffu, any)) append<T>(v, col, p, sv, si, sh);
-                }
+            for (int base = 0; base < cols; base += S::kCols) {
+                float v[N];
+                load_step<T, VEC>(xr, base, cols, v);
+                offer_step<T, VEC>(v, base, cols, F, sv, si, sh);
             }
             __syncthreads();
         }
@@ -1482,7 +1591,7 @@ __global__ void __launch_bounds__(T, 1024 / T)
 }
 
 template <int T, int Q, bool VEC>
-int launch_select_q(const float* x, int64_t rows, int cols, int k, int chunk, float* vals,
+int launch_select_q(const float* x, int64_t rows, int cols, int k, float* vals,
                     int32_t* idx, float* lse, cudaStream_t stream) {
     static int blocks_per_sm = 0;
     static cudaError_t attr = cudaSuccess;
@@ -1500,29 +1609,23 @@ int launch_select_q(const float* x, int64_t rows, int cols, int k, int chunk, fl
     long long grid = sms * (blocks_per_sm > 0 ? blocks_per_sm : 1);
     if (grid > rows) grid = rows;
     topk_select_rows<T, Q, VEC><<<static_cast<unsigned>(grid), T, SelCfg<T>::kSmem, stream>>>(
-        x, rows, cols, k, chunk, vals, idx, lse);
+        x, rows, cols, k, vals, idx, lse);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-// Chunks of 131072 columns (512 KB).  Each chunk costs a floor sort, a barrier after each pass
-// and a pass 2 that the CTA runs without HBM loads of its own; measured on 512 rows of 131072
-// columns, k = 100: chunks of 16384, 32768, 65536 and 131072 columns took 0.252, 0.187, 0.156
-// and 0.142 ms, so the L2 hits of short chunks do not pay for their count.
-constexpr int kSelChunk = 131072;
-
 // The CTA width by k: 256 threads (four CTAs per SM, whose latency-bound steps overlap) up to
 // k = 256, 512 threads (two per SM, a floor from more threads' values and a buffer of 8192)
-// beyond.  Measured on 512 rows of 131072 columns: k = 100 took 0.142 ms with 512 threads and
-// 0.120 with 256; k = 1024 took 0.268 with 512 threads and 0.362 with 256 (Q = 8, 4096
-// entries); k = 33 took 0.113 with 256 threads and 0.149 with 128 (eight CTAs per SM).
+// beyond.  Measured on 512 rows of 131072 columns with the earlier form that read every row
+// twice: k = 100 took 0.142 ms with 512 threads and 0.120 with 256; k = 1024 took 0.268 with
+// 512 threads and 0.362 with 256 (Q = 8, 4096 entries); k = 33 took 0.113 with 256 threads and
+// 0.149 with 128 (eight CTAs per SM).
 constexpr int kSelSmallK = 256;
 
 template <int T, int Q>
 int launch_select_vec(bool vec, const float* x, int64_t rows, int cols, int k, float* vals,
                       int32_t* idx, float* lse, cudaStream_t stream) {
-    return vec ? launch_select_q<T, Q, true>(x, rows, cols, k, kSelChunk, vals, idx, lse, stream)
-               : launch_select_q<T, Q, false>(x, rows, cols, k, kSelChunk, vals, idx, lse,
-                                              stream);
+    return vec ? launch_select_q<T, Q, true>(x, rows, cols, k, vals, idx, lse, stream)
+               : launch_select_q<T, Q, false>(x, rows, cols, k, vals, idx, lse, stream);
 }
 
 int launch_select(const float* x, int64_t rows, int cols, int k, float* vals, int32_t* idx,

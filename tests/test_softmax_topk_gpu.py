@@ -118,3 +118,17 @@ def test_topk_large_k_ties_and_masked_rows(cols):
     x[6, 1::2] = 0.0
     for k in (33, 100, 299):
         check(x, k, f"ties cols={cols} k={k}")
+
+
+@pytest.mark.parametrize("cols", [65536, 65537])
+def test_topk_large_k_sorted_and_trending_rows(cols):
+    """Rows in ascending order beat every running floor, so the candidate buffer overflows
+    during the one-read sweep and the row is read once more against the final floor; rows in
+    descending order meet their floor at once; rows that rise slowly under noise push the
+    buffer past half full, so that entries below the floors are dropped during the sweep."""
+    x = inputs.softmax_inputs(12, cols, seed=9401 + cols)
+    x[:4] = x[:4].sort(dim=1).values
+    x[4:8] = x[4:8].sort(dim=1, descending=True).values
+    x[8:] += torch.linspace(0.0, 60.0, cols)
+    for k in (40, 100, 600):
+        check(x, k, f"sorted cols={cols} k={k}")
