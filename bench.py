@@ -491,7 +491,7 @@ NCU_TRAFFIC_BYTES = {
     "softmax_65536x4000": 1048660992 + 998156288,
     "softmax_topk_65536x4000_k8": 1048771072 + 6897152,
     "softmax_topk_512x131072_k32": 268552704 + 3390464,
-    "softmax_topk_512x131072_k100": 268617472 + 3869440,
+    "softmax_topk_512x131072_k100": 268739840 + 3975680,
     "bwd_b4h16n2048d64": 170481920 + 12257024,
     "bwd_b2h16n8192d128": 675801856 + 156787968,
     "bwd_causal_b2h16n8192d128": 903689728 + 151711744,

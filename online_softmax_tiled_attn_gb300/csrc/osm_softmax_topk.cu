@@ -1023,7 +1023,7 @@ int launch(const float* x, long long rows, int cols, int k, float* vals, int* id
 //     Q-th largest values is a floor F under the k-th largest value of the row (a bitonic
 //     network over the CTA's T values picks it), and so is the smallest over the warps of a
 //     warp's c-th largest lane value when the warps' c add up to ceil(k / Q);
-//   * the row's first 32 T columns are read twice: once for (m, l) and the Q largest, which
+//   * the row's first 64 T columns are read twice: once for (m, l) and the Q largest, which
 //     give the first F, and once more (from L2) to append every entry at or above F to a
 //     candidate buffer in shared memory (a warp reserves its slots with one atomic);
 //   * the rest of the row is read once: every value is offered against the thread's F, then
@@ -1267,39 +1267,6 @@ __device__ void select_exact(const float* __restrict__ xr, int cols, int k, floa
     }
 }
 
-// Appends, for every lane whose p[e] holds, (x[e], col[e]) to the buffer; a warp reserves its
-// slots with one atomic.  Entries past SelCfg<T>::kCap are not stored and mark the row overflowed.
-template <int T, int N>
-__device__ __forceinline__ void append(const float (&x)[N], const int (&col)[N],
-                                       const bool (&p)[N], float* sv, int* si, SelShared<T>& sh) {
-    const int lane = threadIdx.x & 31;
-    unsigned mine = 0;
-#pragma unroll
-    for (int e = 0; e < N; ++e) mine += p[e] ? 1u : 0u;
-    unsigned inc = mine;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const unsigned o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
-    }
-    const unsigned warp_total = __shfl_sync(0xffffffffu, inc, 31);
-    unsigned base = 0;
-    if (lane == 0) base = atomicAdd(&sh.count, warp_total);
-    base = __shfl_sync(0xffffffffu, base, 0) + inc - mine;
-#pragma unroll
-    for (int e = 0; e < N; ++e) {
-        if (p[e]) {
-            if (base < SelCfg<T>::kCap) {
-                sv[base] = x[e];
-                si[base] = col[e];
-            } else {
-                sh.overflow = 1;
-            }
-            ++base;
-        }
-    }
-}
-
 template <int Q>
 __device__ __forceinline__ void keep_largest(float (&b)[Q], float v) {
     if (v > b[Q - 1]) {
@@ -1310,7 +1277,7 @@ __device__ __forceinline__ void keep_largest(float (&b)[Q], float v) {
 }
 
 // A step of the sweep over a row: each thread takes kN values (four float4 in the vector form,
-// four floats otherwise).  The first kHead steps of a row (32 T columns) take two passes (the
+// four floats otherwise).  The first kHead steps of a row (64 T columns) take two passes (the
 // second from L2), which set the first floor; a warp renews its floor every kRefresh later
 // steps (16384 columns), and every kCheck steps (128 T columns) the CTA meets to drop buffer
 // entries below the floor once the buffer is half full.  Measured on 512 rows of 131072
@@ -1320,7 +1287,7 @@ template <int T, bool VEC>
 struct SelStep {
     static constexpr int kN = VEC ? 16 : 4;
     static constexpr int kCols = kN * T;
-    static constexpr int kHead = 32 * T / kCols;
+    static constexpr int kHead = 64 * T / kCols;
     static constexpr int kRefresh = 16384 / kCols;
     static constexpr int kCheck = 128 * T / kCols;
 };
@@ -1401,25 +1368,43 @@ __device__ __forceinline__ void take_step(Stat& s, float (&best)[Q], const float
     }
 }
 
-// The values of a step (columns below c1) at or above f enter the buffer, four at a time (one
-// vote, then one atomic per warp).
+// The values of a step (columns below c1) at or above f enter the buffer, four at a time: a
+// vote on the four's largest value, then a ballot per value and one atomic per warp for the
+// slots.  Entries past SelCfg<T>::kCap are not stored and mark the row overflowed.
 template <int T, bool VEC>
 __device__ __forceinline__ void offer_step(const float (&v)[SelStep<T, VEC>::kN], int base,
                                            int c1, float f, float* sv, int* si,
                                            SelShared<T>& sh) {
+    const unsigned lt = (1u << (threadIdx.x & 31)) - 1u;
 #pragma unroll
     for (int g = 0; g < SelStep<T, VEC>::kN; g += 4) {
+        const float gm = fmaxf(fmaxf(v[g], v[g + 1]), fmaxf(v[g + 2], v[g + 3]));
+        if (!__any_sync(0xffffffffu, gm >= f)) continue;
         bool p[4];
-        int col[4];
-        const float x[4] = {v[g], v[g + 1], v[g + 2], v[g + 3]};
-        bool any = false;
+        unsigned bal[4];
+        unsigned total = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            col[e] = step_col<T, VEC>(base, g + e);
-            p[e] = col[e] < c1 && x[e] >= f;
-            any |= p[e];
+            p[e] = step_col<T, VEC>(base, g + e) < c1 && v[g + e] >= f;
+            bal[e] = __ballot_sync(0xffffffffu, p[e]);
+            total += __popc(bal[e]);
         }
-        if (__any_sync(0xffffffffu, any)) append<T>(x, col, p, sv, si, sh);
+        unsigned slot = 0;
+        if ((threadIdx.x & 31) == 0) slot = atomicAdd(&sh.count, total);
+        slot = __shfl_sync(0xffffffffu, slot, 0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (p[e]) {
+                const unsigned pos = slot + __popc(bal[e] & lt);
+                if (pos < SelCfg<T>::kCap) {
+                    sv[pos] = v[g + e];
+                    si[pos] = step_col<T, VEC>(base, g + e);
+                } else {
+                    sh.overflow = 1;
+                }
+            }
+            slot += __popc(bal[e]);
+        }
     }
 }
 
