@@ -376,11 +376,14 @@ OSM_ATTN_API int fa_bwd_gqa(const void* Q, const void* K, const void* V, const v
  *   x        fp32 [rows, cols] contiguous, 4-byte aligned, read only; no NaN (NaN rows give
  *            unspecified results).  A row of -inf gives values 0 and lse -inf.
  *   k        1 .. min(cols, 1024) (k > 1024: FA_ERR_UNSUPPORTED; k > cols: FA_ERR_INVALID_ARG).
- *            k <= 32 reads each row once (a warp-wide list of the best k); larger k reads
- *            it twice: a floor under the k-th largest value, then every entry at or above the
- *            floor into a buffer that is sorted (rows where more than 4096 entries at
- *            k <= 256, 8192 above, reach the floor fall back to radix selection, five more
- *            passes).
+ *            k <= 32 reads each row once (a warp-wide list of the best k).  Larger k also
+ *            reads each row once (its first 64 T columns twice, T = 256 threads up to
+ *            k = 256, 512 above): a floor under the k-th largest value rises as the row
+ *            streams by, and every entry at or above it goes into a buffer that is sorted at
+ *            the end.  A row whose entries overflow the buffer (16 T of them; rows in
+ *            ascending order, for one) is read once more against the final floor; rows where
+ *            more than 16 T entries reach the final floor fall back to radix selection, five
+ *            more passes.
  *   values   fp32 [rows, k], indices int32 [rows, k], lse fp32 [rows] or NULL; written; none
  *            may overlap x or each other.
  * rows == 0 is a no-op.  All pointers are device pointers; asynchronous on `stream`.
